@@ -1,0 +1,221 @@
+"""CPU oracle for the paged KV-cache hot path.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+benchmark's CPU-baseline leg are the only callers.  The product path (the
+CUDA library and its binding) never imports this package, and this package
+imports nothing from the product.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision, nested
+loops); this module compiles it with gcc on first use and wraps it with
+ctypes.  Arrays are numpy; half-width formats travel as their raw integer
+codes (bf16/fp16 as uint16, fp8 e4m3 as uint8).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# dtype codes of the oracle's own enumeration
+BF16, FP16, FP32, E4M3 = 0, 1, 2, 3
+_NP_CODE_TYPE = {BF16: np.uint16, FP16: np.uint16, FP32: np.float32, E4M3: np.uint8}
+DTYPE_NAMES = {"bf16": BF16, "fp16": FP16, "fp32": FP32, "e4m3": E4M3}
+
+ERRORS = {-1: "invalid argument", -2: "duplicate target slot", -3: "out of memory"}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, no fast-math,
+    no FMA contraction) and return the library path."""
+    with _lock:
+        fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+        if force or not fresh:
+            tmp = _LIB_PATH + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                   "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I32, I64, F32, D = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+    C_INT = ctypes.c_int
+    lib.or_encode_array.argtypes = [C_INT, P, I64, P]
+    lib.or_encode_array.restype = C_INT
+    lib.or_decode_array.argtypes = [C_INT, P, I64, P]
+    lib.or_decode_array.restype = C_INT
+    lib.or_format_info.argtypes = [C_INT, P, P]
+    lib.or_format_info.restype = C_INT
+    lib.or_reshape_and_cache.argtypes = [P, P, C_INT, I64, I32, I32, I64, I64, P, P, C_INT,
+                                         I64, I32, I64, P, P, I64, P, P]
+    lib.or_reshape_and_cache.restype = I64
+    lib.or_concat_mla_k.argtypes = [P, C_INT, P, P, C_INT, I64, I32, I32, I32, I64, I64, I64,
+                                    I64, I64]
+    lib.or_concat_mla_k.restype = C_INT
+    lib.or_dense_attention_row.argtypes = [P, P, P, P, P, I64, P, I64, I64, I32, D]
+    lib.or_dense_attention_row.restype = C_INT
+    lib.or_paged_decode_row.argtypes = [P, P, P, P, C_INT, P, P, C_INT, P, P, I32, I32, I32,
+                                        I32, I32, I32, I32, I64, F32]
+    lib.or_paged_decode_row.restype = C_INT
+    lib.or_paged_decode.argtypes = [P, P, P, C_INT, P, P, C_INT, P, P, I32, I32, I32, I32, I32,
+                                    I32, I64, F32]
+    lib.or_paged_decode.restype = C_INT
+    _lib = lib
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc):
+    if rc < 0:
+        raise OracleError(ERRORS.get(int(rc), f"error {rc}"))
+    return rc
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------- formats --
+def encode(dtype: int, y) -> np.ndarray:
+    """float32 values -> codes of `dtype` (nearest, ties to even; e4m3
+    saturates to +-448; NaN -> quiet NaN)."""
+    y = _c(y, np.float32)
+    out = np.empty(y.shape, dtype=_NP_CODE_TYPE[dtype])
+    _check(_load().or_encode_array(dtype, _ptr(y), y.size, _ptr(out)))
+    return out
+
+
+def decode(dtype: int, codes) -> np.ndarray:
+    """codes of `dtype` -> float64 values."""
+    codes = _c(codes, _NP_CODE_TYPE[dtype])
+    out = np.empty(codes.shape, dtype=np.float64)
+    _check(_load().or_decode_array(dtype, _ptr(codes), codes.size, _ptr(out)))
+    return out
+
+
+def format_info(dtype: int):
+    """(number of non-negative finite values, largest finite value)."""
+    n = ctypes.c_int64()
+    m = ctypes.c_double()
+    _check(_load().or_format_info(dtype, ctypes.byref(n), ctypes.byref(m)))
+    return n.value, m.value
+
+
+# ------------------------------------------------------------ cache write --
+def reshape_and_cache(key, value, src_dtype, key_cache, value_cache, cache_dtype,
+                      slot_mapping, swa_slot_mapping=None, k_scale=None, v_scale=None,
+                      key_stride=None, value_stride=None, block_stride=None,
+                      num_heads=None, head_size=None):
+    """Scatter key/value [N, H, d] into the caches [num_blocks, bs, H, d]
+    IN PLACE (the cache arrays are modified).  Returns the number of tokens
+    written.  key/value may be 2-D [N, row] views with explicit strides when
+    num_heads/head_size are given."""
+    if num_heads is None:
+        _, num_heads, head_size = key.shape
+    num_tokens = key.shape[0]
+    if key_stride is None:
+        key_stride = key.strides[0] // key.itemsize
+    if value is not None and value_stride is None:
+        value_stride = value.strides[0] // value.itemsize
+    if value_stride is None:
+        value_stride = 0
+    num_blocks, block_size = key_cache.shape[0], key_cache.shape[1]
+    if block_stride is None:
+        block_stride = key_cache.strides[0] // key_cache.itemsize
+    slot_mapping = _c(slot_mapping, np.int64)
+    swa = None if swa_slot_mapping is None else _c(swa_slot_mapping, np.int64)
+    ks = None if k_scale is None else np.array([k_scale], dtype=np.float32)
+    vs = None if v_scale is None else np.array([v_scale], dtype=np.float32)
+    rc = _load().or_reshape_and_cache(
+        _ptr(key), _ptr(value), src_dtype, num_tokens, num_heads, head_size, key_stride,
+        value_stride, _ptr(key_cache), _ptr(value_cache), cache_dtype, num_blocks, block_size,
+        block_stride, _ptr(slot_mapping), _ptr(swa), 0 if swa is None else swa.size,
+        _ptr(ks), _ptr(vs))
+    return _check(rc)
+
+
+# ------------------------------------------------------------- MLA concat --
+def concat_mla_k(k, k_dtype, k_nope, k_rope, src_dtype):
+    """k[n, h, :nope] = k_nope[n, h, :]; k[n, h, nope:] = k_rope[n, 0, :]
+    (k modified in place; all arrays 3-D with a contiguous last axis)."""
+    n, h, nope = k_nope.shape
+    rope = k_rope.shape[2]
+    es = lambda a, i: a.strides[i] // a.itemsize
+    _check(_load().or_concat_mla_k(
+        _ptr(k), k_dtype, _ptr(k_nope), _ptr(k_rope), src_dtype, n, h, nope, rope,
+        es(k, 0), es(k, 1), es(k_nope, 0), es(k_nope, 1), es(k_rope, 0)))
+    return k
+
+
+# -------------------------------------------------------- decode attention --
+def dense_attention_row(q, K, V, scale):
+    """Dense softmax attention of one query over contiguous rows.
+    Returns (out[d] float64, lse, sum of the softmax weights)."""
+    q = _c(q, np.float64)
+    K = _c(K, np.float64)
+    V = _c(V, np.float64)
+    L, d = K.shape
+    out = np.empty(d, dtype=np.float64)
+    lse = ctypes.c_double()
+    ps = ctypes.c_double()
+    _check(_load().or_dense_attention_row(_ptr(out), ctypes.byref(lse), ctypes.byref(ps),
+                                          _ptr(q), _ptr(K), d, _ptr(V), d, L, d, float(scale)))
+    return out, lse.value, ps.value
+
+
+def paged_decode_row(q, k_cache, v_cache, block_tables, context_lens, b, h, scale,
+                     q_dtype=BF16, cache_dtype=BF16):
+    """One (sequence, query head) row of paged GQA decode attention.
+    q [B, H_Q, d] codes; caches [num_blocks, bs, H_KV, d] codes.
+    Returns (out[d] float64, lse, sum of softmax weights)."""
+    B, HQ, d = q.shape
+    nb, bs, HKV, d2 = k_cache.shape
+    assert d == d2
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    out = np.empty(d, dtype=np.float64)
+    lse = ctypes.c_double()
+    ps = ctypes.c_double()
+    _check(_load().or_paged_decode_row(
+        _ptr(out), ctypes.byref(lse), ctypes.byref(ps), _ptr(_c(q, q.dtype)), q_dtype,
+        _ptr(_c(k_cache, k_cache.dtype)), _ptr(_c(v_cache, v_cache.dtype)), cache_dtype,
+        _ptr(bt), _ptr(cl), b, h, HQ, HKV, d, bs, bt.shape[1], nb, float(scale)))
+    return out, lse.value, ps.value
+
+
+def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
+                 q_dtype=BF16, cache_dtype=BF16):
+    """Every row: returns (out [B, H_Q, d] float32, lse [B, H_Q] float64)."""
+    B, HQ, d = q.shape
+    nb, bs, HKV, _ = k_cache.shape
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    out = np.empty((B, HQ, d), dtype=np.float32)
+    lse = np.empty((B, HQ), dtype=np.float64)
+    _check(_load().or_paged_decode(
+        _ptr(out), _ptr(lse), _ptr(_c(q, q.dtype)), q_dtype, _ptr(_c(k_cache, k_cache.dtype)),
+        _ptr(_c(v_cache, v_cache.dtype)), cache_dtype, _ptr(bt), _ptr(cl), B, HQ, HKV, d, bs,
+        bt.shape[1], nb, float(scale)))
+    return out, lse

@@ -1,0 +1,473 @@
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+Step (the timed unit): one decode step of one layer on the long-context
+workload -- B=8 sequences with contexts of 32K..128K tokens, H_Q=32, H_KV=8,
+d=128, bf16, block size 16, shuffled physical blocks:
+    pa_reshape_and_cache   (write each sequence's newest K/V token)
+    pa_paged_decode_attention  (split kernel + log-sum-exp merge kernel)
+Inputs are resident in HBM before the timed region; the KV cache (~2.9 GB)
+is far larger than L2 (129 MB), so no flush is needed between steps.
+
+Printed as one JSON line:
+  value     decode KV GB/s: algorithmic bytes of the step / step time
+  roofline  the decode attention pair (split + merge) against measured HBM
+  e2e       the same metric through the C ABI with pinned HOST buffers, the
+            per-step inputs copied in and the output copied back each step
+  extras    cache-write tokens/s (32K-token prefill write, fp8/bf16/SWA) and
+            the MLA K assembly (16K tokens), each over its own loop with an
+            L2 flush between iterations
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+
+--impl reference times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("hbm_gbs"):
+            return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        # samples under load: the top 80% (the sampler brackets the timed region)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------- helpers ----
+def up(a, dtype, dev):
+    import torch
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+    return t.view(dtype) if dtype is not None else t
+
+
+def traffic_record(kernel_file):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current source of the kernel (else None)."""
+    rec = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(rec):
+        return None
+    with open(rec) as f:
+        d = json.load(f)
+    with open(kernel_file, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    if d.get("source_sha256_16") != h:
+        return None
+    return d.get("dram_bytes_per_decode_call")
+
+
+# ------------------------------------------------------------ our arm ----
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_cache_309_gb300 import pa
+    from paged_kv_cache_309_gb300 import workloads as wl
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.library()  # fails loudly if the CUDA library is missing
+
+    # ---------------- workload (rank r uses seed 4 + 1000 r: weak scaling)
+    w = wl.long_context_decode(seed=4 + 1000 * rank, block_size=args.block_size)
+    B, HQ, HKV, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
+    kc, vc = up(w.k_cache, torch.bfloat16, dev), up(w.v_cache, torch.bfloat16, dev)
+    q = up(w.q, torch.bfloat16, dev)
+    nk, nv = up(w.new_k, torch.bfloat16, dev), up(w.new_v, torch.bfloat16, dev)
+    sl = torch.from_numpy(w.slot_mapping).to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    out = torch.empty_like(q)
+    mcl = w.max_context_len
+    wsp = pa.decode_workspace(B, HQ, HKV, d, mcl, dev)
+    splits, tps = pa.pa_paged_decode_plan(B, HKV, mcl)
+    stream = torch.cuda.current_stream()
+
+    attn_bytes = wl.kv_bytes_read(w)                         # algorithmic, decode attention
+    write_bytes = B * HKV * d * 2 * 2 * 2 + B * 8             # new K/V read + written, slots
+    step_bytes = attn_bytes + write_bytes
+
+    def step():
+        pa.pa_reshape_and_cache(nk, nv, kc, vc, sl)
+        pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---------------- timed region: exactly K steps
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws_n > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(K):
+            pa.pa_reshape_and_cache(nk, nv, kc, vc, sl)
+            ev[i][0].record(stream)
+            pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp)
+            ev[i][1].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if ws_n > 1:
+        dist.barrier()
+    ms_total = start.elapsed_time(stop)
+    attn_ms = [a.elapsed_time(b) for a, b in ev]
+    if ws_n > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    assert pa.read_device_error(wsp) == 0, "device error word set"
+    ms_step = ms_total / K
+    value = step_bytes * ws_n / (ms_step * 1e-3) / 1e9
+    attn_ms_avg = statistics.mean(attn_ms)
+    peak, peak_kind = hbm_peak()
+    achieved = attn_bytes / (attn_ms_avg * 1e-3) / 1e9
+    traffic = traffic_record(os.path.join(ROOT, "paged_kv_cache_309_gb300", "csrc", "decode.cu"))
+
+    # ---------------- end to end through the C ABI with pinned host buffers
+    hq = torch.from_numpy(w.q.view(np.int16)).pin_memory()
+    hk = torch.from_numpy(w.new_k.view(np.int16)).pin_memory()
+    hv = torch.from_numpy(w.new_v.view(np.int16)).pin_memory()
+    hsl = torch.from_numpy(w.slot_mapping).pin_memory()
+    hbt = torch.from_numpy(w.block_tables).pin_memory()
+    hcl = torch.from_numpy(w.context_lens).pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+    dq, dk, dv = (torch.empty(t.shape, dtype=torch.int16, device=dev) for t in (hq, hk, hv))
+    dsl, dbt, dcl = (torch.empty_like(t, device=dev) for t in (hsl, hbt, hcl))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hsl, hbt, hcl))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        for dst, src in ((dq, hq), (dk, hk), (dv, hv), (dsl, hsl), (dbt, hbt), (dcl, hcl)):
+            dst.copy_(src, non_blocking=True)
+        pa.pa_reshape_and_cache(dk.view(torch.bfloat16), dv.view(torch.bfloat16), kc, vc, dsl)
+        pa.pa_paged_decode_attention(out, dq.view(torch.bfloat16), kc, vc, dbt, dcl, w.scale,
+                                     mcl, wsp)
+        hout.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = max(1, K // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    assert np.array_equal(hout.numpy(), out.view(torch.int16).cpu().numpy())
+
+    result = {
+        "metric": "paged decode-attn KV GB/s (% of HBM peak); cache-write tokens/s",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws_n,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled block pool)",
+        "config": {"workload": w.name, "num_seqs": B, "num_q_heads": HQ, "num_kv_heads": HKV,
+                   "head_size": d, "block_size": w.block_size,
+                   "context_tokens": int(w.context_lens.sum()),
+                   "max_context_len": mcl, "splits": splits, "tokens_per_split": tps,
+                   "step": "reshape_and_cache(new tokens) + paged_decode_attention",
+                   "l2": "inputs larger than L2 (KV cache %.2f GB)" % (
+                       2 * w.k_cache.nbytes / 1e9),
+                   "parallelism": f"replicas x{ws_n} (independent sequences per GPU)"},
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "sequences_per_s": round(B * ws_n / (ms_step * 1e-3), 1),
+        "roofline": {"kernel": "paged_decode_split_kernel + paged_decode_merge_kernel",
+                     "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "bytes_per_launch": attn_bytes, "avg_launch_us": round(attn_ms_avg * 1e3, 2)},
+        "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+    }
+
+    if rank == 0 and not args.no_extras:
+        result["extras"] = run_extras(args, dev, peak)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws_n > 1:
+        dist.destroy_process_group()
+
+
+def timed_loop(fn, iters, warm, dev, flush_bytes=2 * L2_BYTES):
+    """Median and mean device time of fn over `iters` calls, L2 flushed
+    (a 258 MB write) before each call and outside the timed events."""
+    import torch
+    scratch = torch.empty(flush_bytes // 4, dtype=torch.float32, device=dev)
+    for _ in range(warm):
+        fn()
+    times = []
+    s = torch.cuda.current_stream()
+    for _ in range(iters):
+        scratch.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in times]
+    return statistics.median(ms), statistics.mean(ms)
+
+
+def run_extras(args, dev, peak):
+    import torch
+
+    from paged_kv_cache_309_gb300 import pa
+    from paged_kv_cache_309_gb300 import workloads as wl
+    ex = {}
+    iters = args.extra_iters
+    for variant in ("e4m3", "bf16", "e4m3_swa"):
+        w = wl.prefill_write(variant=variant)
+        H, d = w.key.shape[1:]
+        cdt = torch.float8_e4m3fn if w.cache_dtype == "e4m3" else torch.bfloat16
+        kc = torch.zeros((w.num_blocks, w.block_size, H, d), dtype=cdt, device=dev)
+        vc = torch.zeros_like(kc)
+        key, val = up(w.key, torch.bfloat16, dev), up(w.value, torch.bfloat16, dev)
+        sl = torch.from_numpy(w.slot_mapping).to(dev)
+        swa = None if w.swa_slot_mapping is None else torch.from_numpy(w.swa_slot_mapping).to(dev)
+        ks = None if w.k_scale is None else torch.tensor([w.k_scale], dtype=torch.float32,
+                                                         device=dev)
+        vs = None if ks is None else ks.clone()
+        fn = lambda: pa.pa_reshape_and_cache(key, val, kc, vc, sl, swa, ks, vs)
+        med, mean = timed_loop(fn, iters, 3, dev)
+        nbytes = wl.write_bytes(w)
+        toks = w.key.shape[0]
+        ex[w.name] = {"tokens_per_s": round(toks / (med * 1e-3), 1),
+                      "written_tokens": wl.write_tokens_effective(w),
+                      "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 2),
+                      "frac_of_hbm_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4),
+                      "median_us": round(med * 1e3, 2), "algorithmic_bytes": nbytes}
+    m = wl.mla_assembly()
+    N = m.k_nope.shape[0]
+    kn, kr = up(m.k_nope, torch.bfloat16, dev), up(m.k_rope, torch.bfloat16, dev)
+    k = torch.empty((N, 128, 192), dtype=torch.bfloat16, device=dev)
+    med, _ = timed_loop(lambda: pa.pa_concat_mla_k(k, kn, kr), iters, 3, dev)
+    nbytes = N * (128 * 128 * 2 + 64 * 2 + 128 * 192 * 2)
+    ex[m.name] = {"tokens_per_s": round(N / (med * 1e-3), 1),
+                  "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 2),
+                  "frac_of_hbm_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4),
+                  "median_us": round(med * 1e3, 2), "algorithmic_bytes": nbytes}
+    lat = torch.empty((N, 1, 576), dtype=torch.bfloat16, device=dev)
+    ckv, kpe = up(m.c_kv.reshape(N, 1, 512), torch.bfloat16, dev), up(m.k_pe.reshape(N, 1, 64),
+                                                                      torch.bfloat16, dev)
+    cache = torch.zeros((m.num_blocks, m.block_size, 1, 576), dtype=torch.bfloat16, device=dev)
+    sl = torch.from_numpy(m.slot_mapping).to(dev)
+
+    def latent():
+        pa.pa_concat_mla_k(lat, ckv, kpe)
+        pa.pa_reshape_and_cache(lat, None, cache, None, sl)
+    med, _ = timed_loop(latent, iters, 3, dev)
+    nbytes = N * (576 * 2 * 2 + 576 * 2 * 2 + 8)  # concat read+write, then write read+write
+    ex["mla_latent_cache_write_16k"] = {"tokens_per_s": round(N / (med * 1e-3), 1),
+                                        "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 2),
+                                        "median_us": round(med * 1e3, 2),
+                                        "algorithmic_bytes": nbytes}
+    return ex
+
+
+# ------------------------------------------------------ oracle timings ----
+def _oracle_decode_sample(w, rows, max_tokens=None):
+    """Run the oracle on (b, h) rows (optionally on the first max_tokens of
+    each context); return (seconds, algorithmic KV bytes of the sample)."""
+    import oracle
+    lens = w.context_lens.copy()
+    if max_tokens is not None:
+        lens = np.minimum(lens, max_tokens).astype(np.int32)
+    t0 = time.perf_counter()
+    for b, h in rows:
+        oracle.paged_decode_row(w.q, w.k_cache, w.v_cache, w.block_tables, lens, b, h, w.scale)
+    dt = time.perf_counter() - t0
+    G = w.num_q_heads // w.num_kv_heads
+    kv_groups = {(b, h // G) for b, h in rows}
+    nbytes = sum(int(lens[b]) * w.head_size * 2 * 2 for b, _ in kv_groups)
+    return dt, nbytes
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """The oracle (single-threaded C, double precision) on sequence 0's
+    query heads, as many KV-head groups as fit in about budget_s."""
+    G = w.num_q_heads // w.num_kv_heads
+    rows, spent, nbytes = [], 0.0, 0
+    for g in range(w.num_kv_heads):
+        grp = [(0, g * G + i) for i in range(G)]
+        dt, nb = _oracle_decode_sample(w, grp)
+        spent += dt
+        nbytes += nb
+        rows += grp
+        if spent > budget_s:
+            break
+    return {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"sequence 0 (context {int(w.context_lens[0])}), {len(rows)} query heads "
+                      f"({len(rows) // G} KV heads), {spent:.1f} s"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle timed on the same workload, each
+    step a bounded sample (one query-head group of one sequence, its context
+    truncated so the whole run takes about two minutes)."""
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from paged_kv_cache_309_gb300 import workloads as wl
+    import oracle
+    oracle.build()
+    w = wl.long_context_decode(block_size=args.block_size)
+    G = w.num_q_heads // w.num_kv_heads
+    # calibrate the oracle's speed on one group, then size the per-step sample
+    dt, nb = _oracle_decode_sample(w, [(0, i) for i in range(G)], max_tokens=4096)
+    per_token = dt / 4096
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(64, min(int(w.context_lens.min()), budget / per_token)))
+    steps_t = []
+    for i in range(args.warmup + args.steps):
+        b = i % w.num_seqs
+        g = (i // w.num_seqs) % w.num_kv_heads
+        dt, nb = _oracle_decode_sample(w, [(b, g * G + j) for j in range(G)], max_tokens=tokens)
+        if i >= args.warmup:
+            steps_t.append((dt, nb))
+    tot_t = sum(t for t, _ in steps_t)
+    tot_b = sum(b for _, b in steps_t)
+    val = tot_b / tot_t / 1e9
+    line = {"impl": "reference",
+            "metric": "paged decode-attn KV GB/s (% of HBM peak); cache-write tokens/s",
+            "value": round(val, 4), "unit": "GB/s", "n_gpus": ws_n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / len(steps_t), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16, shuffled block pool)",
+            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
+                       "block_size": w.block_size},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"per step: one KV-head group ({G} query heads) of one "
+                                       f"sequence over its first {tokens} tokens"},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--extra-iters", type=int, default=50)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

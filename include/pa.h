@@ -1,0 +1,191 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged KV-cache library.
+ *
+ * Three operations of the decode/prefill hot path of a paged-KV serving
+ * engine:
+ *   pa_reshape_and_cache       scatter per-token K/V into a paged cache
+ *   pa_concat_mla_k            assemble MLA K from k_nope and a shared k_rope
+ *   pa_paged_decode_attention  GQA decode attention over the paged cache
+ *
+ * Common rules
+ *   - Every pointer argument except the `*_host` ones is a DEVICE pointer on
+ *     the current CUDA device.  The caller owns every buffer; the library
+ *     never allocates, frees or synchronises, and keeps no state besides a
+ *     per-device cache of the SM count and of one driver entry point.
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream) and
+ *     runs asynchronously.  No call reads device memory on the host or
+ *     branches on device data, so every call can be captured in a CUDA graph
+ *     (the PagedAttention-principle post, section on host->device metadata
+ *     transfer, explains why host-side branching on device state is
+ *     incompatible with graph capture).
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns an error code and launches nothing.  Index values
+ *     that live in device memory (slots, SWA entries, block ids, context
+ *     lengths) are checked on the device: an out-of-range value is skipped,
+ *     never dereferenced.
+ *   - "Elements" in strides are elements of the array's own dtype.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (the runtime's typedef of this pointer). */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = 1,     /* null pointer, bad size, inconsistent arguments */
+  PA_ERR_UNSUPPORTED = 2, /* valid but not implemented (dtype pair, head size) */
+  PA_ERR_ALIGN = 3,       /* pointer or stride breaks the vector-access rules */
+  PA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+  PA_ERR_CUDA = 5         /* a CUDA runtime call or a launch failed */
+} pa_status;
+
+typedef enum {
+  PA_BF16 = 0,
+  PA_FP16 = 1,
+  PA_FP32 = 2,
+  PA_FP8_E4M3 = 3 /* OCP FP8 E4M3 (max 448, no inf, 0x7F/0xFF NaN) */
+} pa_dtype;
+
+/* Bits of the device-side error word (first 4 bytes of a decode workspace). */
+#define PA_DEVERR_WAIT_TIMEOUT 0x1u   /* a pipeline wait gave up (should never happen) */
+#define PA_DEVERR_CONTEXT_CLIPPED 0x2u /* some context_lens[b] exceeded the planned range */
+
+/* ------------------------------------------------------------------------
+ * pa_reshape_and_cache
+ *
+ * Defined by sglang kernels/ops/kvcache/cache_ops.py, reshape_and_cache_flash
+ * and launch_reshape_and_cache_flash ("slot mapping", "optional scale" and
+ * "target layout" blocks), and the nano-vLLM walkthrough, section 2.6
+ * Attention (store_kvcache_kernel).  For every token t:
+ *     s = slot_mapping[t]
+ *     if s < 0: skip                                  (-1 marks padding)
+ *     if swa_slot_mapping: if s >= swa_len: skip; s = swa_slot_mapping[s];
+ *                          if s < 0: skip
+ *     if s >= num_blocks * block_size: skip
+ *     for h, i:  y = x[t, h, i]  (as float);  if scales: y = y / scale (IEEE)
+ *         cache[s / block_size, s % block_size, h, i] = cast(y)
+ * for K and V.  The cast rounds to nearest-even; to E4M3 it saturates to
+ * +-448.  Two tokens that resolve to the same slot: unspecified winner.
+ *
+ * key, value:   [num_tokens, num_heads, head_size], key_stride/value_stride
+ *               elements between tokens; heads and elements contiguous.
+ *               value may be NULL (K-only cache, e.g. an MLA latent cache);
+ *               then value_cache must be NULL too.
+ * key_cache, value_cache: [num_blocks, block_size, num_heads, head_size],
+ *               block_stride elements between blocks, the rest contiguous.
+ * src_dtype:    PA_BF16, PA_FP16 or PA_FP32.
+ * cache_dtype:  PA_BF16, PA_FP16, PA_FP32 or PA_FP8_E4M3.
+ * slot_mapping: [num_tokens] int64.
+ * swa_slot_mapping: NULL or [swa_len] int64 second-stage table.
+ * k_scale, v_scale: both NULL or both device pointers to one float (> 0).
+ * Alignment: key/value/caches 16-byte aligned; num_heads*head_size,
+ *   key_stride, value_stride and block_stride multiples of 8 elements.
+ * Errors: PA_ERR_INVALID (null/negative/inconsistent), PA_ERR_UNSUPPORTED
+ *   (dtype pair), PA_ERR_ALIGN, PA_ERR_CUDA (launch failed).
+ * ---------------------------------------------------------------------- */
+pa_status pa_reshape_and_cache(const void *key, const void *value, pa_dtype src_dtype,
+                               int64_t num_tokens, int32_t num_heads, int32_t head_size,
+                               int64_t key_stride, int64_t value_stride, void *key_cache,
+                               void *value_cache, pa_dtype cache_dtype, int64_t num_blocks,
+                               int32_t block_size, int64_t block_stride,
+                               const int64_t *slot_mapping, const int64_t *swa_slot_mapping,
+                               int64_t swa_len, const float *k_scale, const float *v_scale,
+                               pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_concat_mla_k
+ *
+ * Defined by sglang cache_ops.py, concat_and_cast_mha_k_kernel and
+ * concat_and_cast_mha_k_triton:
+ *     k[n, h, 0:nope_dim]                  = k_nope[n, h, :]
+ *     k[n, h, nope_dim:nope_dim+rope_dim]  = k_rope[n, 0, :]   (all heads)
+ * with an implicit round-to-nearest-even cast to k_dtype (E4M3 saturates).
+ * Shapes: k [num_tokens, num_heads, nope_dim + rope_dim],
+ *         k_nope [num_tokens, num_heads, nope_dim], k_rope [num_tokens, 1, rope_dim];
+ *         the wrapper's shape checks become num_heads >= 1, equal token
+ *         counts (a single num_tokens) and k's last size = nope + rope.
+ * Strides in elements of each tensor; the last dimension is contiguous.
+ * src_dtype: PA_BF16, PA_FP16 or PA_FP32; k_dtype: any pa_dtype.
+ * Alignment: pointers 16-byte aligned; nope_dim, rope_dim and every stride
+ *   multiples of 8 elements.
+ * ---------------------------------------------------------------------- */
+pa_status pa_concat_mla_k(void *k, pa_dtype k_dtype, const void *k_nope, const void *k_rope,
+                          pa_dtype src_dtype, int64_t num_tokens, int32_t num_heads,
+                          int32_t nope_dim, int32_t rope_dim, int64_t k_stride0,
+                          int64_t k_stride1, int64_t nope_stride0, int64_t nope_stride1,
+                          int64_t rope_stride0, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Paged GQA decode attention.
+ *
+ * The cache is read back along the block table (nano-vLLM walkthrough,
+ * section 2.6: the decode attention kernel reads the physical blocks via
+ * block_tables; PagedAttention-principle post, "paged attention原理": blocks
+ * are physically scattered and the table keeps their logical order).  For
+ * sequence b and query head h, with G = num_q_heads / num_kv_heads and
+ * L = context_lens[b]:
+ *     kv head g = h / G; logical token j lives at physical row
+ *         block_tables[b][j / block_size] * block_size + j % block_size
+ *     out[b, h] = softmax_j(scale * q[b, h] . K_j) @ V_j,   j < L
+ * L counts the token just written (write, then attend).  L = 0 gives a
+ * zero row.  A block id outside [0, num_blocks) drops its tokens from the
+ * softmax.
+ *
+ * q, out: [num_seqs, num_q_heads, head_size] bf16, contiguous.
+ * k_cache, v_cache: [num_blocks, block_size, num_kv_heads, head_size],
+ *   contiguous, cache_dtype PA_BF16 (other dtypes: PA_ERR_UNSUPPORTED).
+ * block_tables: [num_seqs, max_blocks_per_seq] int32; context_lens [num_seqs] int32.
+ * head_size: 128.  block_size: a power of two in [8, 256].
+ * G: 1, 2, 4, 8 or 16.
+ * max_context_len: host-side upper bound on every context_lens[b]; it sets
+ *   the split plan.  Larger lengths are clipped to the plan (and to
+ *   max_blocks_per_seq * block_size) and flag PA_DEVERR_CONTEXT_CLIPPED.
+ * workspace: device buffer of at least pa_paged_decode_workspace_size(...)
+ *   bytes, 256-byte aligned, ZEROED ONCE by the caller before first use.
+ *   Its first 4 bytes are a sticky device-side error word (PA_DEVERR_*);
+ *   the caller reads it whenever it likes and clears it to reset.
+ *   Calls that share a workspace must be ordered on one stream.
+ * Alignment: q, out, caches 16-byte aligned.
+ *
+ * The context is split into equal token ranges (a plan computed from
+ * num_seqs, num_kv_heads, max_context_len and the SM count); each
+ * (range, kv head, sequence) is one CTA that streams its K/V blocks through
+ * shared memory and keeps an fp32 online softmax, and a second kernel merges
+ * the ranges by log-sum-exp.  One range: no merge kernel.
+ * ---------------------------------------------------------------------- */
+size_t pa_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_size,
+                                      int32_t max_context_len);
+
+pa_status pa_paged_decode_attention(void *out, const void *q, const void *k_cache,
+                                    const void *v_cache, pa_dtype cache_dtype,
+                                    const int32_t *block_tables, const int32_t *context_lens,
+                                    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_size, int32_t block_size,
+                                    int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                                    int32_t max_context_len, void *workspace,
+                                    size_t workspace_bytes, pa_stream_t stream);
+
+/* The split plan the two calls above use: *num_splits token ranges of
+ * *tokens_per_split tokens each.  num_sms <= 0 means "the current
+ * device's SM count".  Host only; launches nothing. */
+pa_status pa_paged_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
+                               int32_t num_sms, int32_t *num_splits_host,
+                               int32_t *tokens_per_split_host);
+
+/* Human-readable name of a status code (static string). */
+const char *pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -172,6 +172,13 @@ static void store_elem(int dtype, void *base, int64_t i, float y) {
   ((uint16_t *)base)[i] = (uint16_t)fmt_encode(fmt_of(dtype), (double)y);
 }
 
+/* copy element i of `src` to element j of `dst`, both of `dtype`, bit for bit
+ * (a cast to the same format changes nothing; NaN payloads included) */
+static void copy_elem(int dtype, void *dst, int64_t j, const void *src, int64_t i) {
+  int sz = dtype_size(dtype);
+  memcpy((uint8_t *)dst + j * sz, (const uint8_t *)src + i * sz, (size_t)sz);
+}
+
 static int formats_ready(void) {
   return fmt_ready(&F_BF16) && fmt_ready(&F_FP16) && fmt_ready(&F_E4M3);
 }
@@ -255,6 +262,7 @@ int64_t or_reshape_and_cache(const void *key, const void *value, int src_dtype,
   }
   free(seen);
 
+  const int raw = (src_dtype == cache_dtype) && k_scale == NULL;
   int64_t written = 0;
   for (int64_t t = 0; t < num_tokens; ++t) {
     int64_t s = resolve_slot(slot_mapping, swa_slot_mapping, swa_len, num_slots, t);
@@ -267,11 +275,16 @@ int64_t or_reshape_and_cache(const void *key, const void *value, int src_dtype,
         int64_t kin = t * key_stride + (int64_t)h * head_size + i;
         /* target: [block_idx, block_offset, h, i] */
         int64_t dst = block_idx * block_stride + block_offset * row + (int64_t)h * head_size + i;
+        int64_t vin = t * value_stride + (int64_t)h * head_size + i;
+        if (raw) { /* same format, no scale: a plain copy */
+          copy_elem(src_dtype, key_cache, dst, key, kin);
+          if (value) copy_elem(src_dtype, value_cache, dst, value, vin);
+          continue;
+        }
         float kx = (float)load_elem(src_dtype, key, kin);
         if (k_scale) kx = kx / *k_scale; /* IEEE single-precision division */
         store_elem(cache_dtype, key_cache, dst, kx);
         if (value) {
-          int64_t vin = t * value_stride + (int64_t)h * head_size + i;
           float vx = (float)load_elem(src_dtype, value, vin);
           if (v_scale) vx = vx / *v_scale;
           store_elem(cache_dtype, value_cache, dst, vx);
@@ -299,15 +312,20 @@ int or_concat_mla_k(void *k, int k_dtype, const void *k_nope, const void *k_rope
   if (num_tokens < 0 || num_heads <= 0 || nope_dim <= 0 || rope_dim <= 0) return OR_EINVAL;
   if (dtype_size(k_dtype) == 0 || dtype_size(src_dtype) == 0 || src_dtype == OR_E4M3)
     return OR_EINVAL;
+  const int raw = (k_dtype == src_dtype);
   for (int64_t n = 0; n < num_tokens; ++n) {
     for (int32_t h = 0; h < num_heads; ++h) {
       for (int32_t i = 0; i < nope_dim; ++i) {
-        double x = load_elem(src_dtype, k_nope, n * nope_stride0 + (int64_t)h * nope_stride1 + i);
-        store_elem(k_dtype, k, n * k_stride0 + (int64_t)h * k_stride1 + i, (float)x);
+        int64_t from = n * nope_stride0 + (int64_t)h * nope_stride1 + i;
+        int64_t to = n * k_stride0 + (int64_t)h * k_stride1 + i;
+        if (raw) copy_elem(k_dtype, k, to, k_nope, from);
+        else store_elem(k_dtype, k, to, (float)load_elem(src_dtype, k_nope, from));
       }
       for (int32_t i = 0; i < rope_dim; ++i) {
-        double x = load_elem(src_dtype, k_rope, n * rope_stride0 + i);
-        store_elem(k_dtype, k, n * k_stride0 + (int64_t)h * k_stride1 + nope_dim + i, (float)x);
+        int64_t from = n * rope_stride0 + i;
+        int64_t to = n * k_stride0 + (int64_t)h * k_stride1 + nope_dim + i;
+        if (raw) copy_elem(k_dtype, k, to, k_rope, from);
+        else store_elem(k_dtype, k, to, (float)load_elem(src_dtype, k_rope, from));
       }
     }
   }

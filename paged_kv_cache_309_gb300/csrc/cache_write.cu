@@ -1,0 +1,143 @@
+// cache_write.cu -- reshape_and_cache: scatter per-token K/V rows into the
+// paged cache through slot_mapping (optional SWA remap, optional scale, cast).
+//
+// Follows sglang cache_ops.py, reshape_and_cache_flash ("slot mapping",
+// "optional scale", "target layout" blocks) and the nano-vLLM walkthrough,
+// section 2.6 (store_kvcache_kernel).  Both pages run one program per
+// (token, head block) over a [HEAD_BLOCK, BLOCK_D] tile.  Here one warp owns
+// a (token, chunk group): a token's H*d elements are contiguous in the
+// source row AND in the destination slot row ([bs, H, d] inside a block),
+// so the whole row moves as 16-byte chunks of 8 elements, 32 lanes side by
+// side (fully coalesced), up to 4 chunks of K and 4 of V in flight per lane.
+// The slot is resolved by every lane from the same address (a broadcast), so
+// a skipped token exits the whole warp at once: no divergence.
+#include <type_traits>
+
+#include "pa_internal.cuh"
+
+namespace pa_detail {
+namespace {
+
+constexpr int kWarps = 8;            // warps per CTA
+constexpr int kChunksPerLane = 4;    // chunks of 8 elements per lane per tensor
+constexpr int kChunksPerWarp = 32 * kChunksPerLane;
+
+template <typename S, typename D, bool kRaw>
+__global__ void __launch_bounds__(kWarps * 32) reshape_and_cache_kernel(ReshapeArgs a) {
+  using namespace pa;
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t t = wid / a.groups;
+  const int grp = static_cast<int>(wid - t * a.groups);
+  if (t >= a.num_tokens) return;
+
+  // slot resolution (same value in every lane)
+  int64_t s = __ldg(a.slot_mapping + t);
+  if (s < 0) return;
+  if (a.swa != nullptr) {
+    if (s >= a.swa_len) return;
+    s = __ldg(a.swa + s);
+    if (s < 0) return;
+  }
+  if (s >= a.num_slots) return;
+  const int64_t blk = s / a.block_size;
+  const int64_t off = s - blk * a.block_size;
+  const int64_t row_elems = static_cast<int64_t>(a.row_chunks) * 8;
+  const int64_t dst0 = blk * a.block_stride + off * row_elems;
+
+  const S* ksrc = static_cast<const S*>(a.key) + t * a.key_stride;
+  const S* vsrc = static_cast<const S*>(a.value) + t * a.value_stride;
+  D* kdst = static_cast<D*>(a.key_cache) + dst0;
+  D* vdst = static_cast<D*>(a.value_cache) + dst0;
+  const bool has_v = a.value != nullptr;
+  const int c_begin = grp * kChunksPerWarp + lane;
+
+  Vec8<S> kv[kChunksPerLane], vv[kChunksPerLane];
+#pragma unroll
+  for (int i = 0; i < kChunksPerLane; ++i) {
+    const int c = c_begin + 32 * i;
+    if (c < a.row_chunks) {
+      kv[i] = load8(ksrc + 8 * c);
+      if (has_v) vv[i] = load8(vsrc + 8 * c);
+    }
+  }
+  if constexpr (kRaw) {
+#pragma unroll
+    for (int i = 0; i < kChunksPerLane; ++i) {
+      const int c = c_begin + 32 * i;
+      if (c < a.row_chunks) {
+        store8(kdst + 8 * c, kv[i]);
+        if (has_v) store8(vdst + 8 * c, vv[i]);
+      }
+    }
+  } else {
+    const bool scaled = a.k_scale != nullptr;
+    const float ks = scaled ? __ldg(a.k_scale) : 1.0f;
+    const float vs = scaled ? __ldg(a.v_scale) : 1.0f;
+#pragma unroll
+    for (int i = 0; i < kChunksPerLane; ++i) {
+      const int c = c_begin + 32 * i;
+      if (c < a.row_chunks) {
+        float f[8];
+        to_f32(kv[i], f);
+        if (scaled) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = __fdiv_rn(f[e], ks);  // IEEE division
+        }
+        store8(kdst + 8 * c, from_f32<D>(f));
+        if (has_v) {
+          to_f32(vv[i], f);
+          if (scaled) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __fdiv_rn(f[e], vs);
+          }
+          store8(vdst + 8 * c, from_f32<D>(f));
+        }
+      }
+    }
+  }
+}
+
+template <typename S, typename D>
+pa_status launch_typed(ReshapeArgs a, cudaStream_t stream) {
+  a.groups = (a.row_chunks + kChunksPerWarp - 1) / kChunksPerWarp;
+  const int64_t warps = a.num_tokens * a.groups;
+  const int64_t blocks = (warps + kWarps - 1) / kWarps;
+  if (blocks == 0) return PA_OK;
+  if (blocks > 0x7FFFFFFFll) return PA_ERR_UNSUPPORTED;
+  const bool raw = std::is_same<S, D>::value && a.k_scale == nullptr;
+  if (raw) {
+    if constexpr (std::is_same<S, D>::value)
+      reshape_and_cache_kernel<S, D, true>
+          <<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(a);
+  } else {
+    reshape_and_cache_kernel<S, D, false>
+        <<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(a);
+  }
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+template <typename S>
+pa_status launch_src(const ReshapeArgs& a, pa_dtype dst, cudaStream_t stream) {
+  switch (dst) {
+    case PA_BF16: return launch_typed<S, pa::bf16>(a, stream);
+    case PA_FP16: return launch_typed<S, pa::f16>(a, stream);
+    case PA_FP32: return launch_typed<S, float>(a, stream);
+    case PA_FP8_E4M3: return launch_typed<S, pa::e4m3>(a, stream);
+  }
+  return PA_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+pa_status launch_reshape_and_cache(const ReshapeArgs& a, pa_dtype src, pa_dtype dst,
+                                   cudaStream_t stream) {
+  switch (src) {
+    case PA_BF16: return launch_src<pa::bf16>(a, dst, stream);
+    case PA_FP16: return launch_src<pa::f16>(a, dst, stream);
+    case PA_FP32: return launch_src<float>(a, dst, stream);
+    default: return PA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace pa_detail

@@ -1,0 +1,303 @@
+// pa_internal.cuh -- shared device helpers of the sm_103a paged-KV library.
+//
+// Element vectors (8 elements per 16-byte-class access), round-to-nearest
+// casts through CUDA's conversion intrinsics, and the mbarrier / TMA
+// primitives of the decode pipeline (inline PTX).  Every wait on an mbarrier
+// is bounded by %globaltimer so that a lost transfer turns into an error
+// word on the host side instead of a hung GPU.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------- dtypes --
+using bf16 = __nv_bfloat16;
+using f16 = __half;
+struct e4m3 {  // storage-only tag type for fp8 E4M3
+  uint8_t bits;
+};
+
+template <typename T>
+struct Vec8;  // eight elements, raw
+template <>
+struct Vec8<bf16> { uint4 u; };
+template <>
+struct Vec8<f16> { uint4 u; };
+template <>
+struct Vec8<float> { uint4 u[2]; };
+template <>
+struct Vec8<e4m3> { uint2 u; };
+
+// read-only, streamed loads (the source rows are read exactly once)
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ Vec8<T> load8(const T* p);
+template <>
+__device__ __forceinline__ Vec8<bf16> load8(const bf16* p) { return {ld_stream16(p)}; }
+template <>
+__device__ __forceinline__ Vec8<f16> load8(const f16* p) { return {ld_stream16(p)}; }
+template <>
+__device__ __forceinline__ Vec8<float> load8(const float* p) {
+  Vec8<float> v;
+  v.u[0] = ld_stream16(p);
+  v.u[1] = ld_stream16(p + 4);
+  return v;
+}
+
+template <typename T>
+__device__ __forceinline__ void store8(T* p, const Vec8<T>& v);
+template <>
+__device__ __forceinline__ void store8(bf16* p, const Vec8<bf16>& v) {
+  *reinterpret_cast<uint4*>(p) = v.u;
+}
+template <>
+__device__ __forceinline__ void store8(f16* p, const Vec8<f16>& v) {
+  *reinterpret_cast<uint4*>(p) = v.u;
+}
+template <>
+__device__ __forceinline__ void store8(float* p, const Vec8<float>& v) {
+  reinterpret_cast<uint4*>(p)[0] = v.u[0];
+  reinterpret_cast<uint4*>(p)[1] = v.u[1];
+}
+template <>
+__device__ __forceinline__ void store8(e4m3* p, const Vec8<e4m3>& v) {
+  *reinterpret_cast<uint2*>(p) = v.u;
+}
+
+// widen eight elements to fp32 (exact for every source type)
+__device__ __forceinline__ void to_f32(const Vec8<bf16>& v, float f[8]) {
+  const uint32_t w[4] = {v.u.x, v.u.y, v.u.z, v.u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void to_f32(const Vec8<f16>& v, float f[8]) {
+  const uint32_t w[4] = {v.u.x, v.u.y, v.u.z, v.u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+    float2 t = __half22float2(h);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void to_f32(const Vec8<float>& v, float f[8]) {
+  const uint32_t w[8] = {v.u[0].x, v.u[0].y, v.u[0].z, v.u[0].w,
+                         v.u[1].x, v.u[1].y, v.u[1].z, v.u[1].w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[i]);
+}
+
+// narrow eight fp32 values, round to nearest even (E4M3: saturating)
+template <typename T>
+__device__ __forceinline__ Vec8<T> from_f32(const float f[8]);
+template <>
+__device__ __forceinline__ Vec8<bf16> from_f32(const float f[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i]));
+    uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * i + 1]));
+    w[i] = lo | (hi << 16);
+  }
+  return {make_uint4(w[0], w[1], w[2], w[3])};
+}
+template <>
+__device__ __forceinline__ Vec8<f16> from_f32(const float f[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t lo = __half_as_ushort(__float2half_rn(f[2 * i]));
+    uint32_t hi = __half_as_ushort(__float2half_rn(f[2 * i + 1]));
+    w[i] = lo | (hi << 16);
+  }
+  return {make_uint4(w[0], w[1], w[2], w[3])};
+}
+template <>
+__device__ __forceinline__ Vec8<float> from_f32(const float f[8]) {
+  Vec8<float> v;
+  v.u[0] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  v.u[1] = make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                      __float_as_uint(f[7]));
+  return v;
+}
+template <>
+__device__ __forceinline__ Vec8<e4m3> from_f32(const float f[8]) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t b = __nv_cvt_float_to_fp8(f[i], __NV_SATFINITE, __NV_E4M3);
+    w[i >> 2] |= (b & 0xFFu) << (8 * (i & 3));
+  }
+  return {make_uint2(w[0], w[1])};
+}
+
+// ------------------------------------------------------- mbarrier / TMA --
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+// make barrier initialisation visible to the async (TMA) proxy
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with `parity` to complete.  Gives up (returns false)
+// after `timeout_ns` of wall time, or early once *abort_flag is set by
+// another warp of the CTA.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+  }
+}
+
+// 3-D tiled TMA load global -> shared, completion counted on `bar`.
+// L2 hint: the K/V stream is read once, evict it first.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0,
+                                            int32_t c1, int32_t c2, uint64_t* bar,
+                                            uint64_t l2_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+      "l"(l2_policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+}  // namespace pa
+
+// ------------------------------------------------- internal host launchers --
+namespace pa_detail {
+
+int num_sms_current_device();  // cached per device; 0 if no device
+
+struct ReshapeArgs {
+  const void* key;
+  const void* value;
+  void* key_cache;
+  void* value_cache;
+  const int64_t* slot_mapping;
+  const int64_t* swa;
+  const float* k_scale;
+  const float* v_scale;
+  int64_t swa_len;
+  int64_t num_tokens;
+  int64_t key_stride;
+  int64_t value_stride;
+  int64_t block_stride;
+  int64_t num_slots;
+  int32_t row_chunks;  // (num_heads * head_size) / 8
+  int32_t block_size;
+  int32_t groups;      // chunk groups (warps) per token
+};
+pa_status launch_reshape_and_cache(const ReshapeArgs& a, pa_dtype src, pa_dtype dst,
+                                   cudaStream_t stream);
+
+struct ConcatArgs {
+  void* k;
+  const void* k_nope;
+  const void* k_rope;
+  int64_t num_tokens;
+  int64_t k_stride0, k_stride1, nope_stride0, nope_stride1, rope_stride0;
+  int32_t num_heads;
+  int32_t nope_chunks;  // nope_dim / 8
+  int32_t rope_chunks;  // rope_dim / 8
+};
+pa_status launch_concat_mla_k(const ConcatArgs& a, pa_dtype src, pa_dtype dst,
+                              cudaStream_t stream);
+
+struct DecodePlan {
+  int32_t num_splits;
+  int32_t tokens_per_split;
+};
+DecodePlan make_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
+                            int32_t num_sms);
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                              const DecodePlan& plan);
+
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* workspace;
+  int32_t num_seqs, num_q_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq;
+  int64_t num_blocks;
+  float scale;
+  DecodePlan plan;
+};
+pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace pa_detail

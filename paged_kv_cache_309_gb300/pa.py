@@ -1,0 +1,207 @@
+"""Thin ctypes binding of libpa.so, same names as the C ABI (include/pa.h).
+
+Argument marshalling only: each function turns torch tensors into device
+pointers, sizes and strides, passes the current (or given) CUDA stream and
+raises ``PAError`` on a non-OK status.  All computation happens in the CUDA
+library; there is no fallback: if ``libpa.so`` is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpa.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "pa.h")
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_ALIGN, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(6)
+PA_BF16, PA_FP16, PA_FP32, PA_FP8_E4M3 = range(4)
+PA_DEVERR_WAIT_TIMEOUT = 0x1
+PA_DEVERR_CONTEXT_CLIPPED = 0x2
+
+_TORCH_DTYPE = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16, torch.float32: PA_FP32,
+                torch.float8_e4m3fn: PA_FP8_E4M3}
+
+_lib = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _load().pa_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{where}: {msg}")
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
+                           "(paged_kv_cache_309_gb300.build.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, F32, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    E = ctypes.c_int  # enums
+    lib.pa_status_string.argtypes = [E]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_reshape_and_cache.argtypes = [P, P, E, I64, I32, I32, I64, I64, P, P, E, I64, I32, I64,
+                                         P, P, I64, P, P, P]
+    lib.pa_reshape_and_cache.restype = E
+    lib.pa_concat_mla_k.argtypes = [P, E, P, P, E, I64, I32, I32, I32, I64, I64, I64, I64, I64, P]
+    lib.pa_concat_mla_k.restype = E
+    lib.pa_paged_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32]
+    lib.pa_paged_decode_workspace_size.restype = SZ
+    lib.pa_paged_decode_attention.argtypes = [P, P, P, P, E, P, P, I32, I32, I32, I32, I32, I32,
+                                              I64, F32, I32, P, SZ, P]
+    lib.pa_paged_decode_attention.restype = E
+    lib.pa_paged_decode_plan.argtypes = [I32, I32, I32, I32, ctypes.POINTER(I32),
+                                         ctypes.POINTER(I32)]
+    lib.pa_paged_decode_plan.restype = E
+    _lib = lib
+    return lib
+
+
+def library():
+    """The loaded ctypes library (raises if it was not built)."""
+    return _load()
+
+
+def declared_functions():
+    """Names of the functions include/pa.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status, where):
+    if status != PA_OK:
+        raise PAError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(t):
+    try:
+        return _TORCH_DTYPE[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}") from None
+
+
+def pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
+                         swa_slot_mapping=None, k_scale=None, v_scale=None, stream=None):
+    """key/value [N, H, d] (token stride free), caches [num_blocks, bs, H, d]
+    (block stride free), slot_mapping [N] int64, optional swa table int64,
+    optional k_scale/v_scale one-element float32 device tensors."""
+    lib = _load()
+    N, H, d = key.shape
+    if key.stride(2) != 1 or key.stride(1) != d:
+        raise ValueError("key: heads and elements must be contiguous")
+    if value is not None and (value.shape != key.shape or value.stride(2) != 1
+                              or value.stride(1) != d):
+        raise ValueError("value must match key and be contiguous per token")
+    nb, bs, Hc, dc = key_cache.shape
+    if (Hc, dc) != (H, d) or key_cache.stride(3) != 1 or key_cache.stride(2) != d \
+            or key_cache.stride(1) != H * d:
+        raise ValueError("key_cache must be [num_blocks, bs, H, d], contiguous inside a block")
+    if value_cache is not None and (value_cache.shape != key_cache.shape
+                                    or value_cache.stride() != key_cache.stride()
+                                    or value_cache.dtype != key_cache.dtype):
+        raise ValueError("value_cache must match key_cache")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != N:
+        raise ValueError("slot_mapping must be int64 [N]")
+    swa_len = 0
+    if swa_slot_mapping is not None:
+        if swa_slot_mapping.dtype != torch.int64:
+            raise ValueError("swa_slot_mapping must be int64")
+        swa_len = swa_slot_mapping.numel()
+    st = lib.pa_reshape_and_cache(
+        _ptr(key), _ptr(value), _dtype(key), N, H, d, key.stride(0),
+        0 if value is None else value.stride(0), _ptr(key_cache), _ptr(value_cache),
+        _dtype(key_cache), nb, bs, key_cache.stride(0), _ptr(slot_mapping),
+        _ptr(swa_slot_mapping), swa_len, _ptr(k_scale), _ptr(v_scale), _stream(stream))
+    _check(st, "pa_reshape_and_cache")
+
+
+def pa_concat_mla_k(k, k_nope, k_rope, stream=None):
+    """k [N, H, nope+rope] <- k_nope [N, H, nope] | k_rope [N, 1, rope]."""
+    lib = _load()
+    N, H, nope = k_nope.shape
+    rope = k_rope.shape[2]
+    for t in (k, k_nope, k_rope):
+        if t.stride(2) != 1:
+            raise ValueError("last dimension must be contiguous")
+    if k.shape != (N, H, nope + rope) or k_rope.shape[:2] != (N, 1):
+        raise ValueError("shape mismatch")
+    if k_rope.dtype != k_nope.dtype:
+        raise ValueError("k_nope and k_rope must share a dtype")
+    st = lib.pa_concat_mla_k(_ptr(k), _dtype(k), _ptr(k_nope), _ptr(k_rope), _dtype(k_nope), N, H,
+                             nope, rope, k.stride(0), k.stride(1), k_nope.stride(0),
+                             k_nope.stride(1), k_rope.stride(0), _stream(stream))
+    _check(st, "pa_concat_mla_k")
+
+
+def pa_paged_decode_plan(num_seqs, num_kv_heads, max_context_len, num_sms=0):
+    """(num_splits, tokens_per_split) of the decode split plan."""
+    lib = _load()
+    a, b = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.pa_paged_decode_plan(num_seqs, num_kv_heads, max_context_len, num_sms,
+                                    ctypes.byref(a), ctypes.byref(b)), "pa_paged_decode_plan")
+    return a.value, b.value
+
+
+def pa_paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                   max_context_len):
+    return int(_load().pa_paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads,
+                                                      head_size, max_context_len))
+
+
+def decode_workspace(num_seqs, num_q_heads, num_kv_heads, head_size, max_context_len,
+                     device=None):
+    """A zeroed device workspace of the required size (allocated by torch)."""
+    n = pa_paged_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                       max_context_len)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def read_device_error(workspace) -> int:
+    """The sticky device-side error word (first 4 bytes of the workspace)."""
+    return int(workspace[:4].view(torch.int32).item())
+
+
+def pa_paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                              max_context_len, workspace, stream=None):
+    """out/q [B, H_Q, d] bf16; caches [num_blocks, bs, H_KV, d] bf16 contiguous;
+    block_tables [B, max_blocks_per_seq] int32; context_lens [B] int32."""
+    lib = _load()
+    B, HQ, d = q.shape
+    nb, bs, HKV, dc = k_cache.shape
+    for t, name in ((q, "q"), (out, "out"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                    (block_tables, "block_tables"), (context_lens, "context_lens")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or dc != d:
+        raise ValueError("shape mismatch")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise ValueError("block_tables must be [B, max_blocks_per_seq], context_lens [B]")
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("q and out must be bf16")
+    st = lib.pa_paged_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype(k_cache), _ptr(block_tables),
+        _ptr(context_lens), B, HQ, HKV, d, bs, block_tables.shape[1], nb, float(scale),
+        int(max_context_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(st, "pa_paged_decode_attention")

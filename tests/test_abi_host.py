@@ -1,0 +1,148 @@
+"""The C-ABI library on a host without a GPU: it loads, exports every
+function include/pa.h declares, plans splits correctly and rejects bad
+arguments before launching anything (every call below returns during the
+host-side checks; none reaches a kernel launch)."""
+import ctypes
+import math
+
+import pytest
+
+from paged_kv_cache_309_gb300 import build as pabuild
+from paged_kv_cache_309_gb300 import pa
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pabuild.build()
+    return pa.library()
+
+
+def test_exports_every_declared_function(lib):
+    names = pa.declared_functions()
+    assert {"pa_reshape_and_cache", "pa_concat_mla_k", "pa_paged_decode_attention",
+            "pa_paged_decode_workspace_size", "pa_paged_decode_plan",
+            "pa_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.pa_status_string(code).decode()
+        assert s.startswith("PA_")
+    assert b"unknown" in lib.pa_status_string(99)
+
+
+@pytest.mark.parametrize("B,HKV,ctx,sms", [(8, 8, 131072, 152), (64, 8, 4096, 152),
+                                           (4, 8, 64, 152), (1, 1, 1, 152), (1, 8, 1000, 152),
+                                           (256, 8, 32768, 152), (8, 8, 131072, 148),
+                                           (3, 2, 777, 10)])
+def test_plan_covers_context(B, HKV, ctx, sms):
+    splits, tps = pa.pa_paged_decode_plan(B, HKV, ctx, sms)
+    assert splits >= 1 and tps >= 64 and tps % 64 == 0
+    assert splits * tps >= ctx                      # every token has a split
+    assert (splits - 1) * tps < ctx                 # no split starts past the context
+    if splits > 1:
+        # enough CTAs to fill the machine many times over
+        assert B * HKV * splits >= min(32 * sms, B * HKV * math.ceil(ctx / 64)) * 0.5
+
+
+def test_plan_long_context_example():
+    # B=8, H_KV=8, up to 128K tokens on 152 SMs: ~4864 CTAs planned
+    splits, tps = pa.pa_paged_decode_plan(8, 8, 131072, 152)
+    assert (splits, tps) == (76, 1728)
+
+
+def test_plan_zero_context():
+    assert pa.pa_paged_decode_plan(4, 8, 0, 152) == (1, 64)
+
+
+def test_workspace_size_formula(lib):
+    # one split (short context): only the 256-byte header
+    assert lib.pa_paged_decode_workspace_size(4, 16, 8, 128, 64) == 256
+    # several splits: header + lse partials (256-aligned) + fp32 output partials
+    splits, _ = pa.pa_paged_decode_plan(8, 8, 131072, 0)
+    rows = 8 * 32 * splits
+    want = 256 + (rows * 4 + 255) // 256 * 256 + rows * 128 * 4
+    if splits > 1:
+        assert lib.pa_paged_decode_workspace_size(8, 32, 8, 128, 131072) == want
+
+
+P = ctypes.c_void_p
+FAKE = P(0x100000)          # 16-byte aligned, never dereferenced
+FAKE_MIS = P(0x100008)      # misaligned
+
+
+def _rc(lib, **kw):
+    a = dict(key=FAKE, value=FAKE, src=pa.PA_BF16, n=4, h=8, d=128, ks=1024, vs=1024,
+             kc=FAKE, vc=FAKE, cd=pa.PA_BF16, nb=4, bs=16, bstride=16 * 1024, slot=FAKE,
+             swa=None, swa_len=0, ksc=None, vsc=None)
+    a.update(kw)
+    return lib.pa_reshape_and_cache(a["key"], a["value"], a["src"], a["n"], a["h"], a["d"],
+                                    a["ks"], a["vs"], a["kc"], a["vc"], a["cd"], a["nb"],
+                                    a["bs"], a["bstride"], a["slot"], a["swa"], a["swa_len"],
+                                    a["ksc"], a["vsc"], None)
+
+
+def test_reshape_and_cache_rejects(lib):
+    assert _rc(lib, key=None) == pa.PA_ERR_INVALID
+    assert _rc(lib, slot=None) == pa.PA_ERR_INVALID
+    assert _rc(lib, value=None) == pa.PA_ERR_INVALID          # value_cache given
+    assert _rc(lib, ksc=FAKE) == pa.PA_ERR_INVALID            # only one scale
+    assert _rc(lib, n=-1) == pa.PA_ERR_INVALID
+    assert _rc(lib, h=0) == pa.PA_ERR_INVALID
+    assert _rc(lib, src=pa.PA_FP8_E4M3) == pa.PA_ERR_UNSUPPORTED
+    assert _rc(lib, cd=7) == pa.PA_ERR_UNSUPPORTED
+    assert _rc(lib, h=1, d=12) == pa.PA_ERR_ALIGN             # row not a multiple of 8
+    assert _rc(lib, ks=1028) == pa.PA_ERR_ALIGN
+    assert _rc(lib, bstride=16 * 1024 + 4) == pa.PA_ERR_ALIGN
+    assert _rc(lib, key=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert _rc(lib, ks=512) == pa.PA_ERR_INVALID              # token rows overlap
+    assert _rc(lib, bstride=1024) == pa.PA_ERR_INVALID        # blocks overlap
+    assert _rc(lib, n=0) == pa.PA_OK                          # nothing to do, no launch
+
+
+def _dec(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, kc=FAKE, vc=FAKE, cd=pa.PA_BF16, bt=FAKE, cl=FAKE, B=4, HQ=32,
+             HKV=8, d=128, bs=16, mbps=8, nb=64, scale=0.088, maxctx=128, ws=None, wsb=0)
+    a.update(kw)
+    return lib.pa_paged_decode_attention(a["out"], a["q"], a["kc"], a["vc"], a["cd"], a["bt"],
+                                         a["cl"], a["B"], a["HQ"], a["HKV"], a["d"], a["bs"],
+                                         a["mbps"], a["nb"], a["scale"], a["maxctx"], a["ws"],
+                                         a["wsb"], None)
+
+
+def test_decode_rejects(lib):
+    assert _dec(lib, q=None, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_INVALID
+    assert _dec(lib, HQ=12, HKV=8, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_INVALID
+    assert _dec(lib, scale=float("nan"), ws=FAKE, wsb=1 << 20) == pa.PA_ERR_INVALID
+    assert _dec(lib, cd=pa.PA_FP8_E4M3, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED
+    assert _dec(lib, d=64, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED
+    assert _dec(lib, HQ=24, HKV=8, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED  # G=3
+    assert _dec(lib, bs=12, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED
+    assert _dec(lib, bs=4, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED
+    assert _dec(lib, nb=1 << 28, bs=16, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED
+    assert _dec(lib, out=FAKE_MIS, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_ALIGN
+    assert _dec(lib) == pa.PA_ERR_WORKSPACE
+    assert _dec(lib, ws=FAKE, wsb=16) == pa.PA_ERR_WORKSPACE
+    assert _dec(lib, ws=P(0x100010), wsb=1 << 20) == pa.PA_ERR_ALIGN
+    assert _dec(lib, nb=0, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_INVALID
+    assert _dec(lib, maxctx=-1, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_INVALID
+
+
+def test_concat_rejects(lib):
+    def c(**kw):
+        a = dict(k=FAKE, kd=pa.PA_BF16, kn=FAKE, kr=FAKE, sd=pa.PA_BF16, n=4, h=128, nope=128,
+                 rope=64, k0=128 * 192, k1=192, n0=128 * 128, n1=128, r0=64)
+        a.update(kw)
+        return lib.pa_concat_mla_k(a["k"], a["kd"], a["kn"], a["kr"], a["sd"], a["n"], a["h"],
+                                   a["nope"], a["rope"], a["k0"], a["k1"], a["n0"], a["n1"],
+                                   a["r0"], None)
+    assert c(k=None) == pa.PA_ERR_INVALID
+    assert c(h=0) == pa.PA_ERR_INVALID
+    assert c(sd=pa.PA_FP8_E4M3) == pa.PA_ERR_UNSUPPORTED
+    assert c(nope=100) == pa.PA_ERR_ALIGN
+    assert c(k1=190) == pa.PA_ERR_ALIGN
+    assert c(k1=184) == pa.PA_ERR_INVALID          # heads overlap in k
+    assert c(kr=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert c(n=0) == pa.PA_OK

@@ -153,7 +153,8 @@ def run_ours(args):
     pa.library()  # fails loudly if the CUDA library is missing
 
     # ---------------- workload (rank r uses seed 4 + 1000 r: weak scaling)
-    w = wl.long_context_decode(seed=4 + 1000 * rank, block_size=args.block_size)
+    w = wl.long_context_decode(seed=4 + 1000 * rank, block_size=args.block_size,
+                               num_seqs=args.num_seqs)
     B, HQ, HKV, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
     kc, vc = up(w.k_cache, torch.bfloat16, dev), up(w.v_cache, torch.bfloat16, dev)
     q = up(w.q, torch.bfloat16, dev)
@@ -457,6 +458,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--num-seqs", type=int, default=8,
+                    help="sequences of the long-context workload (8; fewer for profiling)")
     ap.add_argument("--extra-iters", type=int, default=50)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

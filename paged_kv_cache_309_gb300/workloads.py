@@ -296,7 +296,8 @@ def mla_assembly(seed=3, num_tokens=16384, **kw):
     return make_mla("mla_k_assembly_16k", seed, num_tokens, **kw)
 
 
-def long_context_decode(seed=4, block_size=16, **kw):
-    """B=8, context in [32768, 131072], H_Q=32, H_KV=8, d=128, bs 16 or 64."""
-    return make_decode(f"long_context_decode_b8_ctx32k-128k_bs{block_size}", seed, 8, 32768,
-                       131072, 32, 8, 128, block_size, **kw)
+def long_context_decode(seed=4, block_size=16, num_seqs=8, **kw):
+    """B=8, context in [32768, 131072], H_Q=32, H_KV=8, d=128, bs 16 or 64
+    (num_seqs < 8 keeps the first sequences' draws: a smaller profiling case)."""
+    return make_decode(f"long_context_decode_b{num_seqs}_ctx32k-128k_bs{block_size}", seed,
+                       num_seqs, 32768, 131072, 32, 8, 128, block_size, **kw)

@@ -10,8 +10,9 @@
  * Common rules
  *   - Every pointer argument except the `*_host` ones is a DEVICE pointer on
  *     the current CUDA device.  The caller owns every buffer; the library
- *     never allocates, frees or synchronises, and keeps no state besides a
- *     per-device cache of the SM count and of one driver entry point.
+ *     never allocates, frees or synchronises, and keeps no state besides
+ *     per-device caches of the SM count, of one driver entry point and of
+ *     the address of the static decode scratch (see the _static call).
  *   - Work is enqueued on `stream` (NULL = the legacy default stream) and
  *     runs asynchronously.  No call reads device memory on the host or
  *     branches on device data, so every call can be captured in a CUDA graph
@@ -174,7 +175,44 @@ pa_status pa_paged_decode_attention(void *out, const void *q, const void *k_cach
                                     int32_t max_context_len, void *workspace,
                                     size_t workspace_bytes, pa_stream_t stream);
 
-/* The split plan the two calls above use: *num_splits token ranges of
+/* ------------------------------------------------------------------------
+ * pa_paged_decode_attention_static -- the same decode attention for callers
+ * that cannot allocate device memory.
+ *
+ * No counterpart in the paper: this is a deployment variant of the call
+ * above.  Some callers never get to call cudaMalloc: a plugin inside a host
+ * runtime that owns every device buffer and hands the plugin only its input
+ * and output tensors, or a latency-critical loop that must not risk the
+ * device-wide synchronisation an allocation can cause.  Such a caller
+ * cannot provide the split-K workspace, so this entry point uses a scratch
+ * area compiled into the library instead (a 16 MiB __device__ array that
+ * every GPU loading the library holds until the process exits).  It
+ * allocates nothing and calls no allocating routine.
+ *
+ * Arguments are those of pa_paged_decode_attention without the workspace;
+ * the caller still passes every input and the output.  error_word: NULL or
+ * a device pointer to one 4-byte word that receives the PA_DEVERR_* bits of
+ * this call (OR-ed in; the caller clears it); with NULL they are dropped.
+ * Limits: a problem whose split-K partials need more than 16 MiB (see
+ * pa_paged_decode_workspace_size) returns PA_ERR_WORKSPACE and launches
+ * nothing.  The first call on a device looks up the scratch's device
+ * address (once per device, with that device current); make that first
+ * call before any stream capture.  All calls share the one scratch area,
+ * and each call overwrites what the last one left there: calls that may
+ * overlap on the GPU (different streams, no ordering between them) race and
+ * give wrong results -- order them on one stream.
+ * ---------------------------------------------------------------------- */
+pa_status pa_paged_decode_attention_static(void *out, const void *q, const void *k_cache,
+                                           const void *v_cache, pa_dtype cache_dtype,
+                                           const int32_t *block_tables,
+                                           const int32_t *context_lens, int32_t num_seqs,
+                                           int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_size, int32_t block_size,
+                                           int32_t max_blocks_per_seq, int64_t num_blocks,
+                                           float scale, int32_t max_context_len,
+                                           unsigned *error_word, pa_stream_t stream);
+
+/* The split plan the decode calls above use: *num_splits token ranges of
  * *tokens_per_split tokens each.  num_sms <= 0 means "the current
  * device's SM count".  Host only; launches nothing. */
 pa_status pa_paged_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,

@@ -535,6 +535,41 @@ pa_status launch_split(const CUtensorMap& mk, const CUtensorMap& mv, const Decod
 
 }  // namespace
 
+// Scratch of the allocation-free decode entry point.  Every GPU that loads
+// this library holds these 16 MiB for the life of the process.  Host code
+// must not use the name as an address: static_decode_scratch_address() asks
+// the runtime for the device address.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) uint8_t g_static_decode_scratch[kStaticScratchBytes];
+
+size_t static_decode_scratch_bytes() { return kStaticScratchBytes; }
+
+pa_status static_decode_scratch_address(void** ptr) {
+  static std::atomic<void*> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
+  const bool cacheable = dev >= 0 && dev < 64;
+  if (cacheable) {
+    void* p = cache[dev].load();
+    if (p != nullptr) {
+      *ptr = p;
+      return PA_OK;
+    }
+  }
+  // set-up, once per device, with that device current
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_decode_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
+  if (cacheable) cache[dev].store(p);
+  *ptr = p;
+  return PA_OK;
+}
+
 DecodePlan make_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
                             int32_t num_sms) {
   if (num_sms <= 0) num_sms = 148;
@@ -577,7 +612,7 @@ pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  p.err = reinterpret_cast<unsigned*>(ws);
+  p.err = a.error_word != nullptr ? a.error_word : reinterpret_cast<unsigned*>(ws);
   const size_t nrows = static_cast<size_t>(a.num_seqs) * a.num_q_heads * a.plan.num_splits;
   p.ws_lse = reinterpret_cast<float*>(ws + kWorkspaceHeader);
   p.ws_o = reinterpret_cast<float*>(ws + kWorkspaceHeader + (nrows * sizeof(float) + 255) / 256 * 256);

@@ -36,6 +36,51 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 bool is_src_dtype(pa_dtype d) { return d == PA_BF16 || d == PA_FP16 || d == PA_FP32; }
 bool is_any_dtype(pa_dtype d) { return is_src_dtype(d) || d == PA_FP8_E4M3; }
 
+// Host-side checks shared by both decode entry points; fills *a (all but the
+// workspace) on success.
+pa_status check_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       pa_dtype cache_dtype, const int32_t* block_tables,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_size, int32_t block_size,
+                       int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
+                       int32_t max_context_len, pa_detail::DecodeArgs* a) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
+      block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
+      max_context_len > (1 << 30))
+    return PA_ERR_INVALID;
+  if (out == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      block_tables == nullptr || context_lens == nullptr)
+    return PA_ERR_INVALID;
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID;
+  if (cache_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (head_size != 128) return PA_ERR_UNSUPPORTED;
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PA_ERR_UNSUPPORTED;
+  if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0)
+    return PA_ERR_UNSUPPORTED;
+  if (num_blocks * block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return PA_ERR_ALIGN;
+  a->out = out;
+  a->q = q;
+  a->k_cache = k_cache;
+  a->v_cache = v_cache;
+  a->block_tables = block_tables;
+  a->context_lens = context_lens;
+  a->num_seqs = num_seqs;
+  a->num_q_heads = num_q_heads;
+  a->num_kv_heads = num_kv_heads;
+  a->head_size = head_size;
+  a->block_size = block_size;
+  a->max_blocks_per_seq = max_blocks_per_seq;
+  a->num_blocks = num_blocks;
+  a->scale = scale;
+  a->plan = pa_detail::make_decode_plan(num_seqs, num_kv_heads, max_context_len,
+                                        pa_detail::num_sms_current_device());
+  return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -167,46 +212,46 @@ pa_status pa_paged_decode_attention(void* out, const void* q, const void* k_cach
                                     int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
                                     int32_t max_context_len, void* workspace,
                                     size_t workspace_bytes, pa_stream_t stream) {
-  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
-      block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
-      max_context_len > (1 << 30))
-    return PA_ERR_INVALID;
-  if (out == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr ||
-      block_tables == nullptr || context_lens == nullptr)
-    return PA_ERR_INVALID;
-  if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
-  if (!std::isfinite(scale)) return PA_ERR_INVALID;
-  if (cache_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-  if (head_size != 128) return PA_ERR_UNSUPPORTED;
-  const int32_t G = num_q_heads / num_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PA_ERR_UNSUPPORTED;
-  if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0)
-    return PA_ERR_UNSUPPORTED;
-  if (num_blocks * block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
-  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
-    return PA_ERR_ALIGN;
-  const pa_detail::DecodePlan plan = pa_detail::make_decode_plan(
-      num_seqs, num_kv_heads, max_context_len, pa_detail::num_sms_current_device());
-  const size_t need = pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, head_size, plan);
+  pa_detail::DecodeArgs a{};
+  const pa_status st = check_decode(out, q, k_cache, v_cache, cache_dtype, block_tables,
+                                    context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                    block_size, max_blocks_per_seq, num_blocks, scale,
+                                    max_context_len, &a);
+  if (st != PA_OK) return st;
+  const size_t need =
+      pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, head_size, a.plan);
   if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
-  pa_detail::DecodeArgs a{};
-  a.out = out;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
   a.workspace = workspace;
-  a.num_seqs = num_seqs;
-  a.num_q_heads = num_q_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.head_size = head_size;
-  a.block_size = block_size;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_blocks = num_blocks;
-  a.scale = scale;
-  a.plan = plan;
+  a.error_word = nullptr;
+  return pa_detail::launch_paged_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_paged_decode_attention_static(void* out, const void* q, const void* k_cache,
+                                           const void* v_cache, pa_dtype cache_dtype,
+                                           const int32_t* block_tables,
+                                           const int32_t* context_lens, int32_t num_seqs,
+                                           int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_size, int32_t block_size,
+                                           int32_t max_blocks_per_seq, int64_t num_blocks,
+                                           float scale, int32_t max_context_len,
+                                           unsigned* error_word, pa_stream_t stream) {
+  pa_detail::DecodeArgs a{};
+  const pa_status st = check_decode(out, q, k_cache, v_cache, cache_dtype, block_tables,
+                                    context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                    block_size, max_blocks_per_seq, num_blocks, scale,
+                                    max_context_len, &a);
+  if (st != PA_OK) return st;
+  if (error_word != nullptr && !aligned(error_word, 4)) return PA_ERR_ALIGN;
+  const size_t need =
+      pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, head_size, a.plan);
+  if (need > pa_detail::static_decode_scratch_bytes()) return PA_ERR_WORKSPACE;
+  if (num_seqs == 0) return PA_OK;
+  void* scratch = nullptr;
+  const pa_status sst = pa_detail::static_decode_scratch_address(&scratch);
+  if (sst != PA_OK) return sst;
+  a.workspace = scratch;
+  a.error_word = error_word;
   return pa_detail::launch_paged_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

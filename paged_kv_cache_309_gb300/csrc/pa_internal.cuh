@@ -293,11 +293,18 @@ struct DecodeArgs {
   const int32_t* block_tables;
   const int32_t* context_lens;
   void* workspace;
+  unsigned* error_word;  // nullptr: the workspace's own error word
   int32_t num_seqs, num_q_heads, num_kv_heads, head_size, block_size, max_blocks_per_seq;
   int64_t num_blocks;
   float scale;
   DecodePlan plan;
 };
 pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Library-owned decode scratch (a file-scope __device__ array in decode.cu)
+// for callers that cannot allocate: its size, and its device address on the
+// current device (looked up once per device).
+size_t static_decode_scratch_bytes();
+pa_status static_decode_scratch_address(void** ptr);
 
 }  // namespace pa_detail

@@ -58,6 +58,9 @@ def _load():
     lib.pa_paged_decode_attention.argtypes = [P, P, P, P, E, P, P, I32, I32, I32, I32, I32, I32,
                                               I64, F32, I32, P, SZ, P]
     lib.pa_paged_decode_attention.restype = E
+    lib.pa_paged_decode_attention_static.argtypes = [P, P, P, P, E, P, P, I32, I32, I32, I32,
+                                                     I32, I32, I64, F32, I32, P, P]
+    lib.pa_paged_decode_attention_static.restype = E
     lib.pa_paged_decode_plan.argtypes = [I32, I32, I32, I32, ctypes.POINTER(I32),
                                          ctypes.POINTER(I32)]
     lib.pa_paged_decode_plan.restype = E
@@ -205,3 +208,28 @@ def pa_paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_le
         int(max_context_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check(st, "pa_paged_decode_attention")
+
+
+def pa_paged_decode_attention_static(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                     max_context_len, error_word=None, stream=None):
+    """Decode attention without a caller workspace: the split-K partials go
+    to the library's own 16 MiB device scratch (for callers that cannot
+    allocate device memory).  error_word: None or a one-element int32 device
+    tensor that receives the device-side error bits.  Calls sharing the
+    scratch must be ordered on one stream."""
+    lib = _load()
+    B, HQ, d = q.shape
+    nb, bs, HKV, dc = k_cache.shape
+    for t, name in ((q, "q"), (out, "out"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                    (block_tables, "block_tables"), (context_lens, "context_lens")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or dc != d:
+        raise ValueError("shape mismatch")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    st = lib.pa_paged_decode_attention_static(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype(k_cache), _ptr(block_tables),
+        _ptr(context_lens), B, HQ, HKV, d, bs, block_tables.shape[1], nb, float(scale),
+        int(max_context_len), _ptr(error_word), _stream(stream))
+    _check(st, "pa_paged_decode_attention_static")

@@ -15,21 +15,21 @@
 //    All G = H_Q / H_KV query heads of the KV head share the CTA, so each
 //    K/V byte is read from HBM once and used G times.
 //  * one producer warp streams the range in tiles of 64 tokens: per tile it
-//    looks up the tile's physical blocks in the block table and issues one
-//    3-D TMA copy per (block, K|V) -- a [rows, 128] box of one KV head --
-//    into a 3-stage shared-memory ring, signalling an mbarrier with the
-//    byte count; a per-tile 64-bit mask marks the rows that exist (inside
-//    the context and in a valid block).  The L2 policy is evict-first: the
-//    K/V stream is read once.
-//  * four consumer warps compute on CUDA cores in fp32.  A warp splits into
-//    groups of LPT lanes, one token per group; a lane holds 128/LPT
-//    elements of q (for all G heads, pre-multiplied by scale*log2(e)) and of
-//    the output accumulator.  Scores are reduced across the group with
-//    shuffles; the softmax is online in base 2 with a lazy rescale (the
-//    running max moves only when a score exceeds it by more than 2^8, so the
-//    accumulator is almost never rescaled); packed fp32x2 FMAs halve the
-//    issue count of both products.
-//  * epilogue: the groups' (max, sum, accumulator) are merged in shared
+//    looks up the tile's physical blocks in the block table and issues 3-D
+//    TMA copies -- per (block, K|V, 64-element half row) one [rows, 64] box
+//    of one KV head -- into a 3-stage shared-memory ring with the 128-byte
+//    swizzle, signalling an mbarrier with the byte count; a per-tile 64-bit
+//    mask marks the rows that exist (inside the context and in a valid
+//    block).  The L2 policy is evict-first: the K/V stream is read once.
+//  * four consumer warps each take a 16-token slice of every tile and run
+//    the two grouped products on the tensor cores (mma.sync m16n8k16, bf16
+//    in, fp32 accumulate): S^T = K.Q^T (tokens x heads), an fp32 online
+//    softmax in base 2 with warp-shuffle max reductions and a lazy rescale
+//    (the running max moves only when a score beats it by more than 2^8),
+//    then O^T += V^T.P^T (head elements x heads).  CUDA-core FMAs were the
+//    first design; at G = 4 they needed ~66 instructions per token and KV
+//    head and could not keep HBM busy, the tensor cores need a few.
+//  * epilogue: the warps' (max, sum, accumulator) are merged in shared
 //    memory; one split writes bf16 directly, several splits write an fp32
 //    partial and its log2-sum-exp to the workspace and a second kernel
 //    merges them.
@@ -56,14 +56,6 @@ constexpr int kTileBytes = kTile * kRowBytes;
 constexpr float kRescaleLog2 = 8.0f;    // lazy-rescale threshold (base-2 units)
 constexpr int kMergeWarps = 4;
 constexpr size_t kWorkspaceHeader = 256;  // error word + padding
-
-struct __align__(128) DecodeSmem {
-  uint8_t kv[kStages][2][kTileBytes];  // [stage][K, V][64 rows x 256 B]
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t mask[kStages];
-  int abort_flag;
-};
 
 struct DecodeParams {
   __nv_bfloat16* out;
@@ -93,42 +85,66 @@ __device__ __forceinline__ int effective_len(const DecodeParams& p, int b, bool*
   return *clipped ? static_cast<int>(cap) : L;
 }
 
-// lane's VEC-element slice `ld` of a bf16 row in shared memory -> fp32 pairs
-template <int VEC>
-__device__ __forceinline__ void lds_row_pairs(const uint8_t* row, int elem0, float2* out) {
-  if constexpr (VEC == 8) {
-    const uint4 u = *reinterpret_cast<const uint4*>(row + elem0 * 2);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      out[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-  } else {
-    static_assert(VEC == 4, "VEC must be 4 or 8");
-    const uint2 u = *reinterpret_cast<const uint2*>(row + elem0 * 2);
-    out[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u));
-    out[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-  }
+// ===================================================== tensor-core consumer
+// The same split kernel with the grouped products on the tensor cores
+// (mma.sync m16n8k16, bf16 in, fp32 accumulate).  Per consumer warp and
+// tile: a 16-token slice.  S^T = K_slice . Q^T puts tokens on M (16) and
+// query heads on N (8 per n-tile, zero-padded past G); O^T += V^T . P^T puts
+// head elements on M (8 tiles of 16) and heads on N.  The K/V tiles arrive
+// through TMA with the 128-byte swizzle, one box per 64-element half of a
+// row, so that ldmatrix reads eight consecutive tokens from eight different
+// bank groups.  P enters the second product as a pair of bf16 terms (the
+// rounded value and its rounding error), so the weights keep ~16 bits.
+constexpr int kHalfBytes = kTile * 128;  // one 64-row x 64-element region
+struct TcSmemLayout {
+  // per stage: K_lo, K_hi, V_lo, V_hi regions (64 rows x 128 B, swizzled)
+  static constexpr int kStageBytes = 4 * kHalfBytes;
+  static constexpr int kKvBytes = kStages * kStageBytes;
+  static constexpr int kBarOffset = kKvBytes;  // full[], empty[], mask[], abort
+  static constexpr int kBytes = kBarOffset + 3 * kStages * 8 + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KB
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <int G, int LPT>
+template <int NT>  // n-tiles of 8 query heads: G <= 8 -> 1, G = 16 -> 2
 __global__ void __launch_bounds__(kThreads, 2)
-    paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
-                              const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+    paged_decode_split_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                 const __grid_constant__ CUtensorMap tm_v, const DecodeParams p,
+                                 int G) {
   using namespace pa;
-  constexpr int EPL = kD / LPT;            // elements per lane
-  constexpr int VEC = EPL < 8 ? EPL : 8;   // elements per shared-memory load
-  constexpr int NLD = EPL / VEC;           // loads per row per lane
-  constexpr int NP = EPL / 2;              // fp32 pairs per lane
-  constexpr int PPL = VEC / 2;             // pairs per load
-  constexpr int GPW = 32 / LPT;            // token groups per warp
-  constexpr int NG = kConsumerWarps * GPW; // token groups per CTA
-  constexpr int TPW = kTile / kConsumerWarps;
-  constexpr int STEPS = TPW / GPW;
-  static_assert(NG * G * (kD + 3) * 4 + 2 * G * 4 <= static_cast<int>(sizeof(DecodeSmem::kv)),
-                "epilogue scratch must fit in the stage buffers");
-
+  constexpr int NWARP_GROUPS = kConsumerWarps;  // one partial state per consumer warp
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  // 1 KB-aligned base (the 128-byte swizzle pattern repeats every 1 KB)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcSmemLayout::kBarOffset);
+  uint64_t* empty = full + kStages;
+  uint64_t* tile_mask = empty + kStages;
+  int* abort_ptr = reinterpret_cast<int*>(tile_mask + kStages);
 
   const int split = blockIdx.x;
   const int g = blockIdx.y;
@@ -144,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tok_begin = split * p.tokens_per_split;
   const int tok_end = min(tok_begin + p.tokens_per_split, L);
   if (tok_begin >= tok_end) {
-    if (p.num_splits == 1) {  // empty context: a zero row per head
+    if (p.num_splits == 1) {
       for (int i = threadIdx.x; i < G * (kD / 8); i += kThreads) {
         const int h = i / (kD / 8), c = i % (kD / 8);
         reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_q_heads + hq0 + h) *
@@ -158,24 +174,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], kConsumerWarps);
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
     }
-    sm.abort_flag = 0;
+    *abort_ptr = 0;
     mbar_init_fence();
   }
   __syncthreads();
-  volatile int* abort_flag = &sm.abort_flag;
+  volatile int* abort_flag = abort_ptr;
 
-  float m[G], l[G];
-  float2 acc[G][NP];
+  const int gq = lane >> 2;  // mma groupID
+  const int tq = lane & 3;   // thread in group
+  float o[8][NT][4];
+  float m[NT][2], l[NT][2];
   int issued = 0;
-  const int grp = lane / LPT;
-  const int j = lane % LPT;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    const int rpb = bs < kTile ? bs : kTile;  // rows per TMA box
+    const int rpb = bs < kTile ? bs : kTile;
     const int nbox = kTile / rpb;
     const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) {
@@ -187,9 +203,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % kStages;
       if (t >= kStages) {
-        // every lane waits; the outcome is made warp-uniform before any
-        // full-mask collective below
-        const bool w_ok = mbar_wait_bounded(&sm.empty[stage], ((t / kStages) - 1) & 1, abort_flag);
+        const bool w_ok = mbar_wait_bounded(&empty[stage], ((t / kStages) - 1) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
           ok = false;
           break;
@@ -214,17 +228,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits >> 32));
       const uint32_t vb = __ballot_sync(0xffffffffu, valid);
       if (lane == 0) {
-        sm.mask[stage] = (static_cast<uint64_t>(hi) << 32) | lo;
-        mbar_arrive_expect_tx(&sm.full[stage],
-                              static_cast<uint32_t>(__popc(vb) * rpb * kRowBytes * 2));
+        tile_mask[stage] = (static_cast<uint64_t>(hi) << 32) | lo;
+        mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(__popc(vb) * rpb * kRowBytes * 2));
       }
       __syncwarp();
       if (valid) {
-        const int32_t row = bid * bs + row0;  // physical row index (< 2^31, checked on host)
-        tma_load_3d(sm.kv[stage][0] + lane * rpb * kRowBytes, &tm_k, 0, g, row, &sm.full[stage],
-                    pol);
-        tma_load_3d(sm.kv[stage][1] + lane * rpb * kRowBytes, &tm_v, 0, g, row, &sm.full[stage],
-                    pol);
+        const int32_t row = bid * bs + row0;
+        uint8_t* st = smem + stage * TcSmemLayout::kStageBytes + lane * rpb * 128;
+        tma_load_3d(st + 0 * kHalfBytes, &tm_k, 0, g, row, &full[stage], pol);
+        tma_load_3d(st + 1 * kHalfBytes, &tm_k, 64, g, row, &full[stage], pol);
+        tma_load_3d(st + 2 * kHalfBytes, &tm_v, 0, g, row, &full[stage], pol);
+        tma_load_3d(st + 3 * kHalfBytes, &tm_v, 64, g, row, &full[stage], pol);
       }
       issued = t + 1;
     }
@@ -234,103 +248,148 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ------------------------------------------------------------ consumers
-    float2 q2[G][NP];
+    // Q^T as the B operand: b0 = q[head gq][16kk + 2tq .. +1], b1 = [.. + 8]
+    uint32_t qb[NT][8][2];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint8_t* qrow = reinterpret_cast<const uint8_t*>(
-          p.q + (static_cast<int64_t>(b) * p.num_q_heads + hq0 + h) * kD);
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + gq;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          p.q + (static_cast<int64_t>(b) * p.num_q_heads + hq0 + (h < G ? h : 0)) * kD);
 #pragma unroll
-      for (int ld = 0; ld < NLD; ++ld) {
-        float2 t2[PPL];
-        // q is tiny and read once per CTA: plain global loads
-        if constexpr (VEC == 8) {
-          const uint4 u = __ldg(reinterpret_cast<const uint4*>(qrow + (j + LPT * ld) * VEC * 2));
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            t2[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-        } else {
-          const uint2 u = __ldg(reinterpret_cast<const uint2*>(qrow + (j + LPT * ld) * VEC * 2));
-          t2[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u));
-          t2[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
-        }
-#pragma unroll
-        for (int i = 0; i < PPL; ++i)
-          q2[h][ld * PPL + i] = make_float2(t2[i].x * p.scale_log2, t2[i].y * p.scale_log2);
+      for (int kk = 0; kk < 8; ++kk) {
+        qb[nt][kk][0] = h < G ? __ldg(qrow + 8 * kk + tq) : 0u;
+        qb[nt][kk][1] = h < G ? __ldg(qrow + 8 * kk + tq + 4) : 0u;
       }
-      m[h] = -INFINITY;
-      l[h] = 0.f;
 #pragma unroll
-      for (int i = 0; i < NP; ++i) acc[h][i] = make_float2(0.f, 0.f);
+      for (int j = 0; j < 2; ++j) {
+        m[nt][j] = -INFINITY;
+        l[nt][j] = 0.f;
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[mt][nt][c] = 0.f;
     }
+    const int r0 = warp * 16;  // this warp's 16-token slice of each tile
+    // per-lane ldmatrix row offsets (swizzle: 16-byte unit u sits at u ^ (row & 7))
+    const int sw = lane & 7;
+    const uint32_t k_row = static_cast<uint32_t>((r0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * 128);
+    const uint32_t v_row = static_cast<uint32_t>((r0 + (lane & 7) + 8 * (lane >> 4)) * 128);
+    const int k_hi = lane >> 4;        // K: second 8 columns of the k-step
+    const int v_hi = (lane >> 3) & 1;  // V: second 8 head elements of the m-tile
+    const uint32_t smem_base = smem_u32(smem);
 
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % kStages;
-      const bool w_ok = mbar_wait_bounded(&sm.full[stage], (t / kStages) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, w_ok)) {  // warp-uniform before the shuffles below
+      const bool w_ok = mbar_wait_bounded(&full[stage], (t / kStages) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w_ok)) {
         ok = false;
         break;
       }
-      const uint64_t mask = sm.mask[stage];
-      const uint8_t* kb = sm.kv[stage][0];
-      const uint8_t* vbuf = sm.kv[stage][1];
-#pragma unroll 2
-      for (int step = 0; step < STEPS; ++step) {
-        const int r = warp * TPW + step * GPW + grp;
-        const bool valid = (mask >> r) & 1ull;
-        float2 kf[NP];
-#pragma unroll
-        for (int ld = 0; ld < NLD; ++ld)
-          lds_row_pairs<VEC>(kb + r * kRowBytes, (j + LPT * ld) * VEC, kf + ld * PPL);
-        float s[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int i = 0; i < NP; i += 2) {
-            a0 = __ffma2_rn(q2[h][i], kf[i], a0);
-            if (i + 1 < NP) a1 = __ffma2_rn(q2[h][i + 1], kf[i + 1], a1);
+      const uint32_t mask16 = static_cast<uint32_t>(tile_mask[stage] >> r0) & 0xFFFFu;
+      const uint32_t st_base = smem_base + stage * TcSmemLayout::kStageBytes;
+      if (mask16 != 0u) {
+        if (mask16 != 0xFFFFu) {
+          // rows without a token: zero their V rows (0 x NaN would poison P.V)
+          uint8_t* vrow0 = smem + stage * TcSmemLayout::kStageBytes + 2 * kHalfBytes;
+          for (int idx = lane; idx < 16 * 16; idx += 32) {
+            const int rr = idx >> 4, unit = idx & 15;
+            if (!((mask16 >> rr) & 1u))
+              *reinterpret_cast<uint4*>(vrow0 + (unit >> 3) * kHalfBytes + (r0 + rr) * 128 +
+                                        (unit & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
-          s[h] = (a0.x + a0.y) + (a1.x + a1.y);
+          __syncwarp();
         }
+        // ---- S^T = K . Q^T (two accumulator chains)
+        float s0[NT][4], s1[NT][4];
 #pragma unroll
-        for (int off = LPT / 2; off >= 1; off >>= 1) {
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int h = 0; h < G; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
+          for (int c = 0; c < 4; ++c) s0[nt][c] = s1[nt][c] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t a[4];
+          const uint32_t u = static_cast<uint32_t>(((2 * kk) & 7) + k_hi);
+          ldsm_x4(st_base + (kk >> 2) * kHalfBytes + k_row + ((u ^ sw) << 4), a);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (kk & 1) mma_bf16_16816(s1[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+            else mma_bf16_16816(s0[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+          }
         }
-        float pr[G];
+        const bool v0 = (mask16 >> gq) & 1u;        // token r0 + gq
+        const bool v1 = (mask16 >> (gq + 8)) & 1u;  // token r0 + gq + 8
+        uint32_t pb[NT][2], pl[NT][2];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float sv = valid ? s[h] : -INFINITY;
-          if (sv > m[h] + kRescaleLog2) {  // new running max (always taken first)
-            const float corr = exp2f(m[h] - sv);
-            l[h] *= corr;
+        for (int nt = 0; nt < NT; ++nt) {
+          float s[4];
 #pragma unroll
-            for (int i = 0; i < NP; ++i) {
-              acc[h][i].x *= corr;
-              acc[h][i].y *= corr;
+          for (int c = 0; c < 4; ++c) s[c] = (s0[nt][c] + s1[nt][c]) * p.scale_log2;
+          if (!v0) s[0] = s[1] = -INFINITY;
+          if (!v1) s[2] = s[3] = -INFINITY;
+          float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+#pragma unroll
+          for (int off = 4; off <= 16; off <<= 1) {
+            mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+            mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (mx[j] > m[nt][j] + kRescaleLog2) {  // new running max (always on the first)
+              const float corr = exp2f(m[nt][j] - mx[j]);
+              l[nt][j] *= corr;
+#pragma unroll
+              for (int mt = 0; mt < 8; ++mt) {
+                o[mt][nt][j] *= corr;
+                o[mt][nt][j + 2] *= corr;
+              }
+              m[nt][j] = mx[j];
             }
-            m[h] = sv;
           }
-          pr[h] = valid ? exp2f(sv - m[h]) : 0.f;
-          l[h] += pr[h];
+          const float p0 = v0 ? exp2f(s[0] - m[nt][0]) : 0.f;
+          const float p1 = v0 ? exp2f(s[1] - m[nt][1]) : 0.f;
+          const float p2 = v1 ? exp2f(s[2] - m[nt][0]) : 0.f;
+          const float p3 = v1 ? exp2f(s[3] - m[nt][1]) : 0.f;
+          l[nt][0] += p0 + p2;
+          l[nt][1] += p1 + p3;
+          // P as hi + lo bf16 pairs (hi = bf16(p), lo = bf16(p - hi)): the two
+          // products together carry ~16 significant bits of each weight
+          const uint32_t h01 = pack_bf16x2(p0, p1);  // token gq,     heads 2tq, 2tq+1
+          const uint32_t h23 = pack_bf16x2(p2, p3);  // token gq + 8, heads 2tq, 2tq+1
+          const uint32_t l01 = pack_bf16x2(p0 - __uint_as_float(h01 << 16),
+                                           p1 - __uint_as_float(h01 & 0xFFFF0000u));
+          const uint32_t l23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16),
+                                           p3 - __uint_as_float(h23 & 0xFFFF0000u));
+          // transpose into the B operand: b0 = P[2tq, 2tq+1][gq], b1 = P[2tq+8, 2tq+9][gq]
+          const int srcA = 8 * tq + (gq >> 1);
+          const int srcB = srcA + 4;
+          const uint32_t sel = (gq & 1) ? 0x7632u : 0x5410u;
+          pb[nt][0] = __byte_perm(__shfl_sync(0xffffffffu, h01, srcA),
+                                  __shfl_sync(0xffffffffu, h01, srcB), sel);
+          pb[nt][1] = __byte_perm(__shfl_sync(0xffffffffu, h23, srcA),
+                                  __shfl_sync(0xffffffffu, h23, srcB), sel);
+          pl[nt][0] = __byte_perm(__shfl_sync(0xffffffffu, l01, srcA),
+                                  __shfl_sync(0xffffffffu, l01, srcB), sel);
+          pl[nt][1] = __byte_perm(__shfl_sync(0xffffffffu, l23, srcA),
+                                  __shfl_sync(0xffffffffu, l23, srcB), sel);
         }
-        if (valid) {
-          float2 vf[NP];
+        // ---- O^T += V^T . P^T
 #pragma unroll
-          for (int ld = 0; ld < NLD; ++ld)
-            lds_row_pairs<VEC>(vbuf + r * kRowBytes, (j + LPT * ld) * VEC, vf + ld * PPL);
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t a[4];
+          const uint32_t u = static_cast<uint32_t>(((2 * mt) & 7) + v_hi);
+          ldsm_x4_trans(st_base + (2 + (mt >> 2)) * kHalfBytes + v_row + ((u ^ sw) << 4), a);
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float2 pp = make_float2(pr[h], pr[h]);
-#pragma unroll
-            for (int i = 0; i < NP; ++i) acc[h][i] = __ffma2_rn(pp, vf[i], acc[h][i]);
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_bf16_16816(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+            mma_bf16_16816(o[mt][nt], a, pl[nt][0], pl[nt][1]);
           }
         }
+        if (mask16 != 0xFFFFu) fence_proxy_async_smem();  // generic writes before the next TMA
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[stage]);
+      if (lane == 0) mbar_arrive(&empty[stage]);
     }
     if (!ok) {
       *abort_flag = 1;
@@ -339,39 +398,41 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   __syncthreads();
-  if (sm.abort_flag) {
-    // wait (bounded) for copies already in flight before the CTA retires
+  if (*abort_flag) {
     if (warp == kConsumerWarps && lane == 0) {
       for (int t = max(0, issued - kStages); t < issued; ++t)
-        mbar_wait_bounded(&sm.full[t % kStages], (t / kStages) & 1, nullptr);
+        mbar_wait_bounded(&full[t % kStages], (t / kStages) & 1, nullptr);
     }
     return;
   }
 
   // ------------------------------------------------------------ epilogue
-  float* red = reinterpret_cast<float*>(&sm.kv[0][0][0]);  // [NG][G][kD]
-  float* red_m = red + NG * G * kD;                         // [NG][G]
-  float* red_l = red_m + NG * G;                            // [NG][G]
-  float* red_w = red_l + NG * G;                            // [NG][G]
-  float* fin = red_w + NG * G;                              // [G][2]
+  // red[warp][h][d], red_m/red_l[warp][h], red_w[warp][h], fin[h][2]
+  float* red = reinterpret_cast<float*>(smem);
+  const int GH = NT * 8;
+  float* red_m = red + NWARP_GROUPS * GH * kD;
+  float* red_l = red_m + NWARP_GROUPS * GH;
+  float* red_w = red_l + NWARP_GROUPS * GH;
+  float* fin = red_w + NWARP_GROUPS * GH;
   if (warp < kConsumerWarps) {
-    const int gid = warp * GPW + grp;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float* dst = red + (gid * G + h) * kD;
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-      for (int ld = 0; ld < NLD; ++ld) {
-        const int e0 = (j + LPT * ld) * VEC;
-#pragma unroll
-        for (int i = 0; i < PPL; i += 2) {
-          const float2 a = acc[h][ld * PPL + i];
-          const float2 c = acc[h][ld * PPL + i + 1];
-          *reinterpret_cast<float4*>(dst + e0 + 2 * i) = make_float4(a.x, a.y, c.x, c.y);
+      for (int j = 0; j < 2; ++j) {
+        float lv = l[nt][j];
+        lv += __shfl_xor_sync(0xffffffffu, lv, 4);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+        lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+        const int h = nt * 8 + 2 * tq + j;
+        if (gq == 0) {
+          red_m[warp * GH + h] = m[nt][j];
+          red_l[warp * GH + h] = lv;
         }
-      }
-      if (j == 0) {
-        red_m[gid * G + h] = m[h];
-        red_l[gid * G + h] = l[h];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          red[(warp * GH + h) * kD + 16 * mt + gq] = o[mt][nt][j];
+          red[(warp * GH + h) * kD + 16 * mt + gq + 8] = o[mt][nt][j + 2];
+        }
       }
     }
   }
@@ -379,13 +440,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x < G) {
     const int h = threadIdx.x;
     float M = -INFINITY;
-#pragma unroll 4
-    for (int gg = 0; gg < NG; ++gg) M = fmaxf(M, red_m[gg * G + h]);
+#pragma unroll
+    for (int w = 0; w < NWARP_GROUPS; ++w) M = fmaxf(M, red_m[w * GH + h]);
     float Ls = 0.f;
-    for (int gg = 0; gg < NG; ++gg) {
-      const float w = (M == -INFINITY) ? 0.f : exp2f(red_m[gg * G + h] - M);
-      red_w[gg * G + h] = w;
-      Ls += red_l[gg * G + h] * w;
+#pragma unroll
+    for (int w = 0; w < NWARP_GROUPS; ++w) {
+      const float wt = (M == -INFINITY) ? 0.f : exp2f(red_m[w * GH + h] - M);
+      red_w[w * GH + h] = wt;
+      Ls += red_l[w * GH + h] * wt;
     }
     fin[2 * h] = M;
     fin[2 * h + 1] = Ls;
@@ -394,31 +456,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int i = threadIdx.x; i < G * (kD / 4); i += kThreads) {
     const int h = i / (kD / 4);
     const int e0 = (i % (kD / 4)) * 4;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int gg = 0; gg < NG; ++gg) {
-      const float w = red_w[gg * G + h];
-      const float4 v = *reinterpret_cast<const float4*>(red + (gg * G + h) * kD + e0);
-      o.x += w * v.x;
-      o.y += w * v.y;
-      o.z += w * v.z;
-      o.w += w * v.w;
+    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NWARP_GROUPS; ++w) {
+      const float wt = red_w[w * GH + h];
+      const float4 v = *reinterpret_cast<const float4*>(red + (w * GH + h) * kD + e0);
+      acc4.x += wt * v.x;
+      acc4.y += wt * v.y;
+      acc4.z += wt * v.z;
+      acc4.w += wt * v.w;
     }
     const float Ls = fin[2 * h + 1];
     const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-    o.x *= inv;
-    o.y *= inv;
-    o.z *= inv;
-    o.w *= inv;
+    acc4.x *= inv;
+    acc4.y *= inv;
+    acc4.z *= inv;
+    acc4.w *= inv;
     const int64_t row = static_cast<int64_t>(b) * p.num_q_heads + hq0 + h;
     if (p.num_splits == 1) {
-      const uint32_t w0 = __bfloat16_as_ushort(__float2bfloat16_rn(o.x)) |
-                          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o.y))) << 16);
-      const uint32_t w1 = __bfloat16_as_ushort(__float2bfloat16_rn(o.z)) |
-                          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o.w))) << 16);
-      *reinterpret_cast<uint2*>(p.out + row * kD + e0) = make_uint2(w0, w1);
+      *reinterpret_cast<uint2*>(p.out + row * kD + e0) =
+          make_uint2(pack_bf16x2(acc4.x, acc4.y), pack_bf16x2(acc4.z, acc4.w));
     } else {
       const int64_t slot = row * p.num_splits + split;
-      *reinterpret_cast<float4*>(p.ws_o + slot * kD + e0) = o;
+      *reinterpret_cast<float4*>(p.ws_o + slot * kD + e0) = acc4;
       if (e0 == 0) p.ws_lse[slot] = Ls > 0.f ? fin[2 * h] + log2f(Ls) : -INFINITY;
     }
   }
@@ -503,33 +563,35 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
 }
 
-bool make_kv_map(CUtensorMap* map, const void* base, int64_t rows, int32_t num_kv_heads,
-                 int32_t box_rows) {
+// [rows, H_KV, 128] bf16 viewed 3-D; box = 64 elements (one 128-byte half
+// row) x 1 head x box_rows rows, landing 128-byte swizzled in shared memory.
+bool make_kv_map_swizzled(CUtensorMap* map, const void* base, int64_t rows, int32_t num_kv_heads,
+                          int32_t box_rows) {
   auto enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(num_kv_heads),
                               static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBytes),
                                  static_cast<cuuint64_t>(kRowBytes) * num_kv_heads};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), 1u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t es[3] = {1u, 1u, 1u};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int G, int LPT>
-pa_status launch_split(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p,
-                       dim3 grid, cudaStream_t stream) {
+template <int NT>
+pa_status launch_split_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p,
+                          dim3 grid, int G, cudaStream_t stream) {
   static std::atomic<bool> attr_set{false};
-  auto kern = paged_decode_split_kernel<G, LPT>;
+  auto kern = paged_decode_split_tc_kernel<NT>;
   if (!attr_set.load()) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(DecodeSmem))) != cudaSuccess)
+                             TcSmemLayout::kAlloc) != cudaSuccess)
       return PA_ERR_CUDA;
     attr_set.store(true);
   }
-  kern<<<grid, kThreads, sizeof(DecodeSmem), stream>>>(mk, mv, p);
+  kern<<<grid, kThreads, TcSmemLayout::kAlloc, stream>>>(mk, mv, p, G);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -602,8 +664,8 @@ pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int64_t rows = a.num_blocks * a.block_size;
   const int32_t box_rows = a.block_size < kTile ? a.block_size : kTile;
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, a.k_cache, rows, a.num_kv_heads, box_rows) ||
-      !make_kv_map(&mv, a.v_cache, rows, a.num_kv_heads, box_rows))
+  if (!make_kv_map_swizzled(&mk, a.k_cache, rows, a.num_kv_heads, box_rows) ||
+      !make_kv_map_swizzled(&mv, a.v_cache, rows, a.num_kv_heads, box_rows))
     return PA_ERR_CUDA;
 
   DecodeParams p;
@@ -631,11 +693,8 @@ pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
                   static_cast<unsigned>(a.num_seqs));
   pa_status st;
   switch (G) {
-    case 1: st = launch_split<1, 8>(mk, mv, p, grid, stream); break;
-    case 2: st = launch_split<2, 8>(mk, mv, p, grid, stream); break;
-    case 4: st = launch_split<4, 8>(mk, mv, p, grid, stream); break;
-    case 8: st = launch_split<8, 16>(mk, mv, p, grid, stream); break;
-    case 16: st = launch_split<16, 32>(mk, mv, p, grid, stream); break;
+    case 1: case 2: case 4: case 8: st = launch_split_tc<1>(mk, mv, p, grid, G, stream); break;
+    case 16: st = launch_split_tc<2>(mk, mv, p, grid, G, stream); break;
     default: return PA_ERR_UNSUPPORTED;
   }
   if (st != PA_OK || a.plan.num_splits == 1) return st;

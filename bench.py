@@ -4,7 +4,7 @@ Step (the timed unit): one decode step of one layer on the long-context
 workload -- B=8 sequences with contexts of 32K..128K tokens, H_Q=32, H_KV=8,
 d=128, bf16, block size 16, shuffled physical blocks:
     pa_reshape_and_cache   (write each sequence's newest K/V token)
-    pa_paged_decode_attention  (split kernel + log-sum-exp merge kernel)
+    pa_paged_decode_attention  (split kernel with the log-sum-exp merge)
 Inputs are resident in HBM before the timed region; the KV cache (~2.9 GB)
 is far larger than L2 (129 MB), so no flush is needed between steps.
 
@@ -15,7 +15,7 @@ Printed as one JSON line:
             per-step inputs copied in and the output copied back each step
   extras    cache-write tokens/s (32K-token prefill write, fp8/bf16/SWA) and
             the MLA K assembly (16K tokens), each over its own loop with an
-            L2 flush between iterations
+            L2 flush (a 258 MB read) between iterations
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
 --impl reference times the CPU oracle itself as the reference arm.
@@ -293,16 +293,19 @@ def run_ours(args):
 
 
 def timed_loop(fn, iters, warm, dev, flush_bytes=2 * L2_BYTES):
-    """Median and mean device time of fn over `iters` calls, L2 flushed
-    (a 258 MB write) before each call and outside the timed events."""
+    """Median and mean device time of fn over `iters` calls.  Before each
+    call, outside the timed events, L2 is flushed by READING a 258 MB buffer
+    written once up front (a read leaves no dirty lines whose write-back
+    would land inside the timed kernel)."""
     import torch
-    scratch = torch.empty(flush_bytes // 4, dtype=torch.float32, device=dev)
+    scratch = torch.ones(flush_bytes // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
     for _ in range(warm):
         fn()
     times = []
     s = torch.cuda.current_stream()
     for _ in range(iters):
-        scratch.fill_(1.0)
+        torch.amax(scratch, dim=0, out=sink)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(s)
         fn()

@@ -152,15 +152,17 @@ pa_status pa_concat_mla_k(void *k, pa_dtype k_dtype, const void *k_nope, const v
  * workspace: device buffer of at least pa_paged_decode_workspace_size(...)
  *   bytes, 256-byte aligned, ZEROED ONCE by the caller before first use.
  *   Its first 4 bytes are a sticky device-side error word (PA_DEVERR_*);
- *   the caller reads it whenever it likes and clears it to reset.
- *   Calls that share a workspace must be ordered on one stream.
+ *   the caller reads it whenever it likes and clears it to reset.  It also
+ *   holds per-(sequence, kv head) split counters that every call leaves at
+ *   zero.  Calls that share a workspace must be ordered on one stream.
  * Alignment: q, out, caches 16-byte aligned.
  *
  * The context is split into equal token ranges (a plan computed from
  * num_seqs, num_kv_heads, max_context_len and the SM count); each
  * (range, kv head, sequence) is one CTA that streams its K/V blocks through
- * shared memory and keeps an fp32 online softmax, and a second kernel merges
- * the ranges by log-sum-exp.  One range: no merge kernel.
+ * shared memory, computes the grouped products on the tensor cores and keeps
+ * an fp32 online softmax; the last CTA of each (sequence, kv head) merges
+ * the ranges by log-sum-exp.  One launch per call.
  * ---------------------------------------------------------------------- */
 size_t pa_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                       int32_t num_kv_heads, int32_t head_size,

@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_and_cache_kernel(ReshapeA
     }
   } else {
     const bool scaled = a.k_scale != nullptr;
-    const float ks = scaled ? __ldg(a.k_scale) : 1.0f;
-    const float vs = scaled ? __ldg(a.v_scale) : 1.0f;
+    const Divisor ks = make_divisor(scaled ? __ldg(a.k_scale) : 1.0f);
+    const Divisor vs = make_divisor(scaled ? __ldg(a.v_scale) : 1.0f);
 #pragma unroll
     for (int i = 0; i < kChunksPerLane; ++i) {
       const int c = c_begin + 32 * i;
@@ -82,14 +82,14 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_and_cache_kernel(ReshapeA
         to_f32(kv[i], f);
         if (scaled) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = __fdiv_rn(f[e], ks);  // IEEE division
+          for (int e = 0; e < 8; ++e) f[e] = div_rn(f[e], ks);  // IEEE quotient
         }
         store8(kdst + 8 * c, from_f32<D>(f));
         if (has_v) {
           to_f32(vv[i], f);
           if (scaled) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __fdiv_rn(f[e], vs);
+            for (int e = 0; e < 8; ++e) f[e] = div_rn(f[e], vs);
           }
           store8(vdst + 8 * c, from_f32<D>(f));
         }

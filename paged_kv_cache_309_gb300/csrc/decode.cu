@@ -31,8 +31,10 @@
 //    head and could not keep HBM busy, the tensor cores need a few.
 //  * epilogue: the warps' (max, sum, accumulator) are merged in shared
 //    memory; one split writes bf16 directly, several splits write an fp32
-//    partial and its log2-sum-exp to the workspace and a second kernel
-//    merges them.
+//    partial and its log2-sum-exp to the workspace and count themselves in
+//    a per-(sequence, kv head) counter; the CTA that completes the count
+//    merges the splits (weights 2^(lse_s - max)) and zeroes the counter, so
+//    no second kernel is launched.
 //
 // Every mbarrier wait is bounded (2 s); a timeout sets an error bit in the
 // workspace's error word, drains the copies already issued, and exits.
@@ -52,9 +54,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kStages = 3;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRowBytes = kD * 2;       // one bf16 row of one KV head
-constexpr int kTileBytes = kTile * kRowBytes;
 constexpr float kRescaleLog2 = 8.0f;    // lazy-rescale threshold (base-2 units)
-constexpr int kMergeWarps = 4;
 constexpr size_t kWorkspaceHeader = 256;  // error word + padding
 
 struct DecodeParams {
@@ -64,9 +64,11 @@ struct DecodeParams {
   const int32_t* context_lens;
   float* ws_lse;
   float* ws_o;
+  unsigned* counters;  // [B, H_KV] split arrivals, zero between calls
   unsigned* err;
   int64_t num_blocks;
   int32_t num_q_heads;
+  int32_t num_kv_heads;
   int32_t block_size;
   int32_t log2_bs;
   int32_t max_blocks_per_seq;
@@ -131,13 +133,73 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Merge of one (sequence, query head) by one warp: weights 2^(lse_s - max)
+// over the n splits that hold tokens, out = sum_s w_s o_s / sum_s w_s,
+// rounded to bf16.  Partials are read through L2 (__ldcg): other CTAs wrote
+// them during this launch.
+__device__ __forceinline__ void merge_splits_warp(const DecodeParams& p, int64_t bh, int n,
+                                                  int lane) {
+  const float* lse = p.ws_lse + bh * p.num_splits;
+  const float* o = p.ws_o + bh * p.num_splits * kD;
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, __ldcg(lse + s));
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float W = 0.f;
+  if (M != -INFINITY) {
+    for (int s0 = 0; s0 < n; s0 += 32) {
+      const int my = s0 + lane;
+      const float wl = my < n ? exp2f(__ldcg(lse + my) - M) : 0.f;
+      const int cnt = min(32, n - s0);
+      int k = 0;
+      for (; k + 8 <= cnt; k += 8) {
+        float4 v[8];
+        float w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          v[u] = __ldcg(reinterpret_cast<const float4*>(o + static_cast<int64_t>(s0 + k + u) * kD) +
+                        lane);
+          w[u] = __shfl_sync(0xffffffffu, wl, k + u);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          W += w[u];
+          acc.x += w[u] * v[u].x;
+          acc.y += w[u] * v[u].y;
+          acc.z += w[u] * v[u].z;
+          acc.w += w[u] * v[u].w;
+        }
+      }
+      for (; k < cnt; ++k) {
+        const float4 v =
+            __ldcg(reinterpret_cast<const float4*>(o + static_cast<int64_t>(s0 + k) * kD) + lane);
+        const float w = __shfl_sync(0xffffffffu, wl, k);
+        W += w;
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  *reinterpret_cast<uint2*>(p.out + bh * kD + lane * 4) =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+}
+
+template <int NT>
+__device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem,
+                                            float (&o)[8][NT][4], float (&m)[NT][2],
+                                            float (&l)[NT][2], int b, int split, int hq0, int G,
+                                            int warp, int lane);
+
 template <int NT>  // n-tiles of 8 query heads: G <= 8 -> 1, G = 16 -> 2
 __global__ void __launch_bounds__(kThreads, 2)
     paged_decode_split_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                  const __grid_constant__ CUtensorMap tm_v, const DecodeParams p,
                                  int G) {
   using namespace pa;
-  constexpr int NWARP_GROUPS = kConsumerWarps;  // one partial state per consumer warp
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // 1 KB-aligned base (the 128-byte swizzle pattern repeats every 1 KB)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -160,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tok_begin = split * p.tokens_per_split;
   const int tok_end = min(tok_begin + p.tokens_per_split, L);
   if (tok_begin >= tok_end) {
-    if (p.num_splits == 1) {
+    if (split == 0) {  // only when L == 0: a zero row per head
       for (int i = threadIdx.x; i < G * (kD / 8); i += kThreads) {
         const int h = i / (kD / 8), c = i % (kD / 8);
         reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_q_heads + hq0 + h) *
@@ -399,14 +461,55 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   __syncthreads();
   if (*abort_flag) {
+    // wait (bounded) for copies already in flight, then leave an empty
+    // partial so that the split count below still completes
     if (warp == kConsumerWarps && lane == 0) {
       for (int t = max(0, issued - kStages); t < issued; ++t)
         mbar_wait_bounded(&full[t % kStages], (t / kStages) & 1, nullptr);
     }
-    return;
+    if (p.num_splits > 1 && threadIdx.x < G)
+      p.ws_lse[(static_cast<int64_t>(b) * p.num_q_heads + hq0 + threadIdx.x) * p.num_splits +
+               split] = -INFINITY;
+  } else {
+    epilogue_tc<NT>(p, smem, o, m, l, b, split, hq0, G, warp, lane);
   }
+  if (p.num_splits == 1) return;
 
-  // ------------------------------------------------------------ epilogue
+  // ------------------------------------------------- split count and merge
+  // The CTA that completes the count of its (sequence, kv head) merges the
+  // splits of its G query heads and returns the counter to zero.
+  __syncthreads();  // every partial of this CTA is written
+  int* last_flag = abort_ptr + 1;
+  const int n_valid = (L + p.tokens_per_split - 1) / p.tokens_per_split;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    unsigned* ctr = p.counters + static_cast<int64_t>(b) * p.num_kv_heads + g;
+    const unsigned prev = atomicAdd(ctr, 1u);
+    const bool last = prev + 1u == static_cast<unsigned>(n_valid);
+    if (last) {
+      atomicExch(ctr, 0u);
+      __threadfence();
+    }
+    *last_flag = last ? 1 : 0;
+  }
+  __syncthreads();
+  if (*last_flag) {
+    for (int h = warp; h < G; h += kThreads / 32)
+      merge_splits_warp(p, static_cast<int64_t>(b) * p.num_q_heads + hq0 + h, n_valid, lane);
+  }
+}
+
+// Epilogue of the tensor-core split kernel: merge the consumer warps'
+// (max, sum, accumulator) in shared memory; one split writes bf16 output,
+// several splits write an fp32 partial and its log2-sum-exp.
+template <int NT>
+__device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem,
+                                            float (&o)[8][NT][4], float (&m)[NT][2],
+                                            float (&l)[NT][2], int b, int split, int hq0, int G,
+                                            int warp, int lane) {
+  constexpr int NWARP_GROUPS = kConsumerWarps;
+  const int gq = lane >> 2;
+  const int tq = lane & 3;
   // red[warp][h][d], red_m/red_l[warp][h], red_w[warp][h], fin[h][2]
   float* red = reinterpret_cast<float*>(smem);
   const int GH = NT * 8;
@@ -482,70 +585,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (e0 == 0) p.ws_lse[slot] = Ls > 0.f ? fin[2 * h] + log2f(Ls) : -INFINITY;
     }
   }
-}
-
-// One warp per (sequence, query head): weights 2^(lse_s - max) over the
-// splits that hold tokens, out = sum_s w_s o_s / sum_s w_s, rounded to bf16.
-__global__ void __launch_bounds__(kMergeWarps * 32)
-    paged_decode_merge_kernel(const DecodeParams p, int32_t num_seqs) {
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t bh = static_cast<int64_t>(blockIdx.x) * kMergeWarps + warp;
-  if (bh >= static_cast<int64_t>(num_seqs) * p.num_q_heads) return;
-  const int b = static_cast<int>(bh / p.num_q_heads);
-  bool clipped;
-  const int L = effective_len(p, b, &clipped);
-  const int n = (L + p.tokens_per_split - 1) / p.tokens_per_split;
-  const float* lse = p.ws_lse + bh * p.num_splits;
-  const float* o = p.ws_o + bh * p.num_splits * kD;
-
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, lse[s]);
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float W = 0.f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < n; s0 += 32) {
-      const int my = s0 + lane;
-      const float wl = my < n ? exp2f(lse[my] - M) : 0.f;
-      const int cnt = min(32, n - s0);
-      int k = 0;
-      for (; k + 4 <= cnt; k += 4) {
-        float4 v[4];
-        float w[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          v[u] = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s0 + k + u) * kD + lane * 4);
-          w[u] = __shfl_sync(0xffffffffu, wl, k + u);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          W += w[u];
-          acc.x += w[u] * v[u].x;
-          acc.y += w[u] * v[u].y;
-          acc.z += w[u] * v[u].z;
-          acc.w += w[u] * v[u].w;
-        }
-      }
-      for (; k < cnt; ++k) {
-        const float4 v = *reinterpret_cast<const float4*>(o + static_cast<int64_t>(s0 + k) * kD + lane * 4);
-        const float w = __shfl_sync(0xffffffffu, wl, k);
-        W += w;
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
-      }
-    }
-  }
-  const float inv = W > 0.f ? 1.f / W : 0.f;
-  const uint32_t w0 = __bfloat16_as_ushort(__float2bfloat16_rn(acc.x * inv)) |
-                      (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.y * inv))) << 16);
-  const uint32_t w1 = __bfloat16_as_ushort(__float2bfloat16_rn(acc.z * inv)) |
-                      (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc.w * inv))) << 16);
-  *reinterpret_cast<uint2*>(p.out + bh * kD + lane * 4) = make_uint2(w0, w1);
 }
 
 // ---------------------------------------------------------------- host --
@@ -647,13 +686,21 @@ DecodePlan make_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_
   return {static_cast<int32_t>(splits), static_cast<int32_t>(tiles_per_split * kTile)};
 }
 
-size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
-                              const DecodePlan& plan) {
+namespace {
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+// Workspace: [error word | pad to 256] [split counters: B*H_KV u32, padded]
+//            [lse partials: B*H_Q*splits f32, padded] [output partials:
+//            B*H_Q*splits*d f32].  One split needs the header only.
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_size, const DecodePlan& plan) {
   size_t bytes = kWorkspaceHeader;
   if (plan.num_splits > 1) {
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * plan.num_splits;
-    bytes += (rows * sizeof(float) + 255) / 256 * 256;         // lse partials
-    bytes += rows * static_cast<size_t>(head_size) * sizeof(float);  // output partials
+    bytes += align256(static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(unsigned));
+    bytes += align256(rows * sizeof(float));
+    bytes += rows * static_cast<size_t>(head_size) * sizeof(float);
   }
   return bytes;
 }
@@ -676,10 +723,13 @@ pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.err = a.error_word != nullptr ? a.error_word : reinterpret_cast<unsigned*>(ws);
   const size_t nrows = static_cast<size_t>(a.num_seqs) * a.num_q_heads * a.plan.num_splits;
-  p.ws_lse = reinterpret_cast<float*>(ws + kWorkspaceHeader);
-  p.ws_o = reinterpret_cast<float*>(ws + kWorkspaceHeader + (nrows * sizeof(float) + 255) / 256 * 256);
+  const size_t ctr_bytes = align256(static_cast<size_t>(a.num_seqs) * a.num_kv_heads * 4);
+  p.counters = reinterpret_cast<unsigned*>(ws + kWorkspaceHeader);
+  p.ws_lse = reinterpret_cast<float*>(ws + kWorkspaceHeader + ctr_bytes);
+  p.ws_o = reinterpret_cast<float*>(ws + kWorkspaceHeader + ctr_bytes + align256(nrows * 4));
   p.num_blocks = a.num_blocks;
   p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
   int lg = 0;
   while ((1 << lg) < a.block_size) ++lg;
@@ -697,12 +747,7 @@ pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
     case 16: st = launch_split_tc<2>(mk, mv, p, grid, G, stream); break;
     default: return PA_ERR_UNSUPPORTED;
   }
-  if (st != PA_OK || a.plan.num_splits == 1) return st;
-  const int64_t bh = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
-  const int64_t blocks = (bh + kMergeWarps - 1) / kMergeWarps;
-  paged_decode_merge_kernel<<<static_cast<unsigned>(blocks), kMergeWarps * 32, 0, stream>>>(
-      p, a.num_seqs);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return st;
 }
 
 }  // namespace pa_detail

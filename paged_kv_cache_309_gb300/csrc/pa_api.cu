@@ -201,7 +201,7 @@ size_t pa_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
     return 0;
   const pa_detail::DecodePlan plan = pa_detail::make_decode_plan(
       num_seqs, num_kv_heads, max_context_len, pa_detail::num_sms_current_device());
-  return pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, head_size, plan);
+  return pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size, plan);
 }
 
 pa_status pa_paged_decode_attention(void* out, const void* q, const void* k_cache,
@@ -219,7 +219,7 @@ pa_status pa_paged_decode_attention(void* out, const void* q, const void* k_cach
                                     max_context_len, &a);
   if (st != PA_OK) return st;
   const size_t need =
-      pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, head_size, a.plan);
+      pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size, a.plan);
   if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
   a.workspace = workspace;
@@ -244,7 +244,7 @@ pa_status pa_paged_decode_attention_static(void* out, const void* q, const void*
   if (st != PA_OK) return st;
   if (error_word != nullptr && !aligned(error_word, 4)) return PA_ERR_ALIGN;
   const size_t need =
-      pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, head_size, a.plan);
+      pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size, a.plan);
   if (need > pa_detail::static_decode_scratch_bytes()) return PA_ERR_WORKSPACE;
   if (num_seqs == 0) return PA_OK;
   void* scratch = nullptr;

@@ -143,11 +143,44 @@ template <>
 __device__ __forceinline__ Vec8<e4m3> from_f32(const float f[8]) {
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t b = __nv_cvt_float_to_fp8(f[i], __NV_SATFINITE, __NV_E4M3);
-    w[i >> 2] |= (b & 0xFFu) << (8 * (i & 3));
+  for (int i = 0; i < 4; ++i) {  // pairs: .x lands in the low byte
+    const uint32_t b2 = __nv_cvt_float2_to_fp8x2(make_float2(f[2 * i], f[2 * i + 1]),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    w[i >> 1] |= (b2 & 0xFFFFu) << (16 * (i & 1));
   }
   return {make_uint2(w[0], w[1])};
+}
+
+// ------------------------------------------------------------- division --
+// x / s rounded to nearest (IEEE), for one divisor s shared by many x.
+// r = RN(1/s) is computed once; then two residual corrections
+//     q0 = RN(x r),  q1 = RN(q0 + RN(x - s q0) r),  q2 = RN(q1 + RN(x - s q1) r)
+// where each residual x - s q is exact with an FMA.  q1 is within one ulp of
+// x/s, and Markstein's theorem (division with a fused multiply-add: r within
+// half an ulp of 1/s and q within one ulp of x/s give RN(q + (x - s q) r) =
+// RN(x/s)) makes q2 the correctly rounded quotient, provided nothing under-
+// or overflows.  Outside the ranges that guarantee that (and for zeros,
+// infinities and NaN) the library's IEEE division is used.
+struct Divisor {
+  float s, r;
+  bool fast;
+};
+__device__ __forceinline__ Divisor make_divisor(float s) {
+  Divisor d;
+  d.s = s;
+  d.r = __frcp_rn(s);
+  const float as = fabsf(s);
+  d.fast = as >= 0x1p-30f && as <= 0x1p30f;  // false for NaN
+  return d;
+}
+__device__ __forceinline__ float div_rn(float x, const Divisor& d) {
+  const float ax = fabsf(x);
+  if (d.fast && ax >= 0x1p-60f && ax <= 0x1p60f) {
+    float q = __fmul_rn(x, d.r);
+    q = __fmaf_rn(__fmaf_rn(-d.s, q, x), d.r, q);
+    return __fmaf_rn(__fmaf_rn(-d.s, q, x), d.r, q);
+  }
+  return __fdiv_rn(x, d.s);
 }
 
 // ------------------------------------------------------- mbarrier / TMA --
@@ -282,8 +315,8 @@ struct DecodePlan {
 };
 DecodePlan make_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
                             int32_t num_sms);
-size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
-                              const DecodePlan& plan);
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_size, const DecodePlan& plan);
 
 struct DecodeArgs {
   void* out;

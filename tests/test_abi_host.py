@@ -60,10 +60,12 @@ def test_plan_zero_context():
 def test_workspace_size_formula(lib):
     # one split (short context): only the 256-byte header
     assert lib.pa_paged_decode_workspace_size(4, 16, 8, 128, 64) == 256
-    # several splits: header + lse partials (256-aligned) + fp32 output partials
+    # several splits: header + split counters + lse partials (each 256-aligned)
+    # + fp32 output partials
     splits, _ = pa.pa_paged_decode_plan(8, 8, 131072, 0)
     rows = 8 * 32 * splits
-    want = 256 + (rows * 4 + 255) // 256 * 256 + rows * 128 * 4
+    al = lambda x: (x + 255) // 256 * 256
+    want = 256 + al(8 * 8 * 4) + al(rows * 4) + rows * 128 * 4
     if splits > 1:
         assert lib.pa_paged_decode_workspace_size(8, 32, 8, 128, 131072) == want
 

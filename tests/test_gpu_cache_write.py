@@ -222,3 +222,24 @@ def test_decode_step_write_then_read_back():
         L = int(w.context_lens[b])
         blk = w.block_tables[b, (L - 1) // w.block_size]
         assert (gk[blk, (L - 1) % w.block_size] == w.new_k[b]).all()
+
+
+def test_scaled_division_is_ieee_over_fp32_domain():
+    """fp32 -> fp32 writes isolate the scale division: random fp32 bit
+    patterns (every exponent, subnormals, inf, NaN) divided by scales from
+    2^-40 to 2^40, bit-exact against the oracle's IEEE single division."""
+    need_gpu()
+    rng = np.random.default_rng(77)
+    N, H, d = 256, 2, 512  # 262144 values per scale
+    bits = rng.integers(0, 2**32, size=(N, H, d), dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x.reshape(-1)[:8] = [0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -3e-39, 3.4e38]
+    scales = [0.05, 1.0 / 3.0, 0.7, 3.0, 2.0 ** -4, 1.0, 1e-9, 7.5e8, 2.0 ** -40, 2.0 ** 40,
+              1.17549435e-38, 3.0e-30, 6.0e29]
+    scales += list(np.exp2(rng.uniform(-40, 40, size=11)).astype(np.float32))
+    slots = np.arange(N, dtype=np.int64)
+    for s in scales:
+        gk, gv, ok_, ov_ = run_both(x, x, "fp32", slots, N // 16, 16, "fp32",
+                                    scale=(float(np.float32(s)), float(np.float32(s) * 3)))
+        assert_same(gk, ok_, "fp32")
+        assert_same(gv, ov_, "fp32")

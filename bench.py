@@ -10,7 +10,7 @@ is far larger than L2 (129 MB), so no flush is needed between steps.
 
 Printed as one JSON line:
   value     decode KV GB/s: algorithmic bytes of the step / step time
-  roofline  the decode attention pair (split + merge) against measured HBM
+  roofline  the decode attention kernel (one launch) against measured HBM
   e2e       the same metric through the C ABI with pinned HOST buffers, the
             per-step inputs copied in and the output copied back each step
   extras    cache-write tokens/s (32K-token prefill write, fp8/bf16/SWA) and
@@ -48,6 +48,23 @@ def hbm_peak():
         if d.get("hbm_gbs"):
             return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def rank_seed(rank: int) -> int:
+    """Seed of rank r's copy of the workload (rank 0 uses the spec's seed 4)."""
+    return 4 + 1000 * rank
+
+
+def reduce_over_ranks(value: float, op: str, device=None) -> float:
+    """max or sum of a per-rank number over all ranks (identity without a
+    process group); the only cross-rank traffic of the benchmark."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
 
 
 def dist_env():
@@ -153,7 +170,7 @@ def run_ours(args):
     pa.library()  # fails loudly if the CUDA library is missing
 
     # ---------------- workload (rank r uses seed 4 + 1000 r: weak scaling)
-    w = wl.long_context_decode(seed=4 + 1000 * rank, block_size=args.block_size,
+    w = wl.long_context_decode(seed=rank_seed(rank), block_size=args.block_size,
                                num_seqs=args.num_seqs)
     B, HQ, HKV, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
     kc, vc = up(w.k_cache, torch.bfloat16, dev), up(w.v_cache, torch.bfloat16, dev)
@@ -201,13 +218,12 @@ def run_ours(args):
         dist.barrier()
     ms_total = start.elapsed_time(stop)
     attn_ms = [a.elapsed_time(b) for a, b in ev]
-    if ws_n > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_over_ranks(ms_total, "max", dev)
+    job_bytes = reduce_over_ranks(step_bytes, "sum", dev)   # every rank's own workload
+    job_seqs = reduce_over_ranks(B, "sum", dev)
     assert pa.read_device_error(wsp) == 0, "device error word set"
     ms_step = ms_total / K
-    value = step_bytes * ws_n / (ms_step * 1e-3) / 1e9
+    value = job_bytes / (ms_step * 1e-3) / 1e9
     attn_ms_avg = statistics.mean(attn_ms)
     peak, peak_kind = hbm_peak()
     achieved = attn_bytes / (attn_ms_avg * 1e-3) / 1e9
@@ -269,8 +285,8 @@ def run_ours(args):
                        2 * w.k_cache.nbytes / 1e9),
                    "parallelism": f"replicas x{ws_n} (independent sequences per GPU)"},
         "pct_of_hbm_peak": round(100 * value / peak, 2),
-        "sequences_per_s": round(B * ws_n / (ms_step * 1e-3), 1),
-        "roofline": {"kernel": "paged_decode_split_kernel + paged_decode_merge_kernel",
+        "sequences_per_s": round(job_seqs / (ms_step * 1e-3), 1),
+        "roofline": {"kernel": "paged_decode_split_tc_kernel (split-K with in-kernel merge)",
                      "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,

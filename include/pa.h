@@ -200,7 +200,9 @@ pa_status pa_paged_decode_attention(void *out, const void *q, const void *k_cach
  * nothing.  The first call on a device looks up the scratch's device
  * address (once per device, with that device current); make that first
  * call before any stream capture.  All calls share the one scratch area,
- * and each call overwrites what the last one left there: calls that may
+ * and each call overwrites what the last one left there (the split counters
+ * in it, which must start at zero, are zero when the library loads and every
+ * completed call returns them to zero): calls that may
  * overlap on the GPU (different streams, no ordering between them) race and
  * give wrong results -- order them on one stream.
  * ---------------------------------------------------------------------- */

@@ -76,6 +76,9 @@ def _load():
     lib.or_paged_decode_row.argtypes = [P, P, P, P, C_INT, P, P, C_INT, P, P, I32, I32, I32,
                                         I32, I32, I32, I32, I64, F32]
     lib.or_paged_decode_row.restype = C_INT
+    lib.or_paged_decode_row_scaled.argtypes = [P, P, P, P, C_INT, P, P, C_INT, P, P, I32, I32,
+                                               I32, I32, I32, I32, I32, I64, F32, F32, F32]
+    lib.or_paged_decode_row_scaled.restype = C_INT
     lib.or_paged_decode.argtypes = [P, P, P, C_INT, P, P, C_INT, P, P, I32, I32, I32, I32, I32,
                                     I32, I64, F32]
     lib.or_paged_decode.restype = C_INT
@@ -186,9 +189,10 @@ def dense_attention_row(q, K, V, scale):
 
 
 def paged_decode_row(q, k_cache, v_cache, block_tables, context_lens, b, h, scale,
-                     q_dtype=BF16, cache_dtype=BF16):
+                     q_dtype=BF16, cache_dtype=BF16, k_scale=1.0, v_scale=1.0):
     """One (sequence, query head) row of paged GQA decode attention.
-    q [B, H_Q, d] codes; caches [num_blocks, bs, H_KV, d] codes.
+    q [B, H_Q, d] codes; caches [num_blocks, bs, H_KV, d] codes; a quantised
+    cache's codes stand for code * k_scale (K) and code * v_scale (V).
     Returns (out[d] float64, lse, sum of softmax weights)."""
     B, HQ, d = q.shape
     nb, bs, HKV, d2 = k_cache.shape
@@ -198,10 +202,11 @@ def paged_decode_row(q, k_cache, v_cache, block_tables, context_lens, b, h, scal
     out = np.empty(d, dtype=np.float64)
     lse = ctypes.c_double()
     ps = ctypes.c_double()
-    _check(_load().or_paged_decode_row(
+    _check(_load().or_paged_decode_row_scaled(
         _ptr(out), ctypes.byref(lse), ctypes.byref(ps), _ptr(_c(q, q.dtype)), q_dtype,
         _ptr(_c(k_cache, k_cache.dtype)), _ptr(_c(v_cache, v_cache.dtype)), cache_dtype,
-        _ptr(bt), _ptr(cl), b, h, HQ, HKV, d, bs, bt.shape[1], nb, float(scale)))
+        _ptr(bt), _ptr(cl), b, h, HQ, HKV, d, bs, bt.shape[1], nb, float(scale), float(k_scale),
+        float(v_scale)))
     return out, lse.value, ps.value
 
 

@@ -384,12 +384,37 @@ int or_dense_attention_row(double *out, double *lse, double *psum, const double 
  * id is outside [0, num_blocks) is left out of the softmax (the library never
  * dereferences such ids either).  The context is gathered in logical order
  * and handed to the dense definition above. */
+/* With a quantised cache (sglang cache_ops.py, reshape_and_cache_flash,
+ * "optional scale": the cache holds x / k_scale and x / v_scale), the value a
+ * code stands for is code * scale: K rows are multiplied by k_scale and V rows
+ * by v_scale after decoding (in double).  Unquantised caches use 1. */
+int or_paged_decode_row_scaled(double *out, double *lse, double *psum, const void *q,
+                               int q_dtype, const void *k_cache, const void *v_cache,
+                               int cache_dtype, const int32_t *block_tables,
+                               const int32_t *context_lens, int32_t b, int32_t h,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                               int32_t block_size, int32_t max_blocks_per_seq,
+                               int64_t num_blocks, float scale, float k_scale, float v_scale);
+
 int or_paged_decode_row(double *out, double *lse, double *psum, const void *q, int q_dtype,
                         const void *k_cache, const void *v_cache, int cache_dtype,
                         const int32_t *block_tables, const int32_t *context_lens, int32_t b,
                         int32_t h, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
                         int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks,
                         float scale) {
+  return or_paged_decode_row_scaled(out, lse, psum, q, q_dtype, k_cache, v_cache, cache_dtype,
+                                    block_tables, context_lens, b, h, num_q_heads, num_kv_heads,
+                                    head_size, block_size, max_blocks_per_seq, num_blocks, scale,
+                                    1.0f, 1.0f);
+}
+
+int or_paged_decode_row_scaled(double *out, double *lse, double *psum, const void *q,
+                               int q_dtype, const void *k_cache, const void *v_cache,
+                               int cache_dtype, const int32_t *block_tables,
+                               const int32_t *context_lens, int32_t b, int32_t h,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                               int32_t block_size, int32_t max_blocks_per_seq,
+                               int64_t num_blocks, float scale, float k_scale, float v_scale) {
   if (!formats_ready()) return OR_ENOMEM;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return OR_EINVAL;
   if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return OR_EINVAL;
@@ -415,8 +440,8 @@ int or_paged_decode_row(double *out, double *lse, double *psum, const void *q, i
     int64_t phys_row = blk * block_size + j % block_size;
     int64_t base = (phys_row * num_kv_heads + g) * d;
     for (int32_t i = 0; i < d; ++i) {
-      K[n * d + i] = load_elem(cache_dtype, k_cache, base + i);
-      V[n * d + i] = load_elem(cache_dtype, v_cache, base + i);
+      K[n * d + i] = load_elem(cache_dtype, k_cache, base + i) * (double)k_scale;
+      V[n * d + i] = load_elem(cache_dtype, v_cache, base + i) * (double)v_scale;
     }
     ++n;
   }

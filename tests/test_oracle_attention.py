@@ -241,3 +241,67 @@ def test_full_and_row_entry_points_agree():
                                               b, h, w.scale)
             assert (out[b, h] == r.astype(np.float32)).all()
             assert lse[b, h] == l or (math.isinf(l) and math.isinf(lse[b, h]))
+
+
+# ------------------------------------------------- quantised (fp8) caches --
+def _fp8_case(seed=3, L=(37, 100, 5), HKV=2, HQ=8, d=16, bs=8):
+    rng = np.random.default_rng(seed)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    K = [rng.choice(finite, size=(n, HKV, d)) for n in L]
+    V = [rng.choice(finite, size=(n, HKV, d)) for n in L]
+    nblk = [wl.blocks_needed(n, bs) for n in L]
+    nb = sum(nblk) + 2
+    perm = rng.permutation(nb)
+    kc = np.full((nb, bs, HKV, d), 0x7F, np.uint8)
+    vc = np.full((nb, bs, HKV, d), 0x7F, np.uint8)
+    bt = np.full((len(L), max(nblk)), -1, np.int32)
+    cur = 0
+    for b, n in enumerate(L):
+        for j in range(nblk[b]):
+            blk = perm[cur]
+            cur += 1
+            bt[b, j] = blk
+            kc[blk, :min(bs, n - j * bs)] = K[b][j * bs:(j + 1) * bs]
+            vc[blk, :min(bs, n - j * bs)] = V[b][j * bs:(j + 1) * bs]
+    q = rng.standard_normal((len(L), HQ, d)).astype(np.float32)
+    return q, kc, vc, bt, np.array(L, np.int32)
+
+
+def test_fp8_cache_equals_decoded_fp32_cache():
+    """An e4m3 cache with unit scales gives exactly the result of an fp32
+    cache holding the decoded values (torch's e4m3 decode as the library)."""
+    q, kc, vc, bt, lens = _fp8_case()
+    k32 = torch.from_numpy(kc).view(torch.float8_e4m3fn).float().numpy()
+    v32 = torch.from_numpy(vc).view(torch.float8_e4m3fn).float().numpy()
+    for b in range(len(lens)):
+        for h in (0, 3, 7):
+            a = oracle.paged_decode_row(q, kc, vc, bt, lens, b, h, 0.01, q_dtype=oracle.FP32,
+                                        cache_dtype=oracle.E4M3)
+            r = oracle.paged_decode_row(q, k32, v32, bt, lens, b, h, 0.01, q_dtype=oracle.FP32,
+                                        cache_dtype=oracle.FP32)
+            assert (a[0] == r[0]).all() and a[1] == r[1]
+
+
+def test_fp8_scales_act_on_scores_and_values():
+    """k_scale multiplies every score (same as scaling the softmax scale);
+    v_scale multiplies the output.  Powers of two keep both exact."""
+    q, kc, vc, bt, lens = _fp8_case(seed=4)
+    for b in range(len(lens)):
+        for h in (1, 6):
+            base = oracle.paged_decode_row(q, kc, vc, bt, lens, b, h, 0.04, q_dtype=oracle.FP32,
+                                           cache_dtype=oracle.E4M3)
+            ks = oracle.paged_decode_row(q, kc, vc, bt, lens, b, h, 0.01, q_dtype=oracle.FP32,
+                                         cache_dtype=oracle.E4M3, k_scale=4.0)
+            vs = oracle.paged_decode_row(q, kc, vc, bt, lens, b, h, 0.04, q_dtype=oracle.FP32,
+                                         cache_dtype=oracle.E4M3, v_scale=0.125)
+            assert np.allclose(ks[0], base[0], rtol=1e-14, atol=1e-14) and abs(ks[1] - base[1]) < 1e-12
+            assert (vs[0] == base[0] * 0.125).all()
+
+
+def test_fp8_constant_values_closed_form():
+    """V codes all 0x38 (= 1.0) with v_scale 0.5: the output is 0.5."""
+    q, kc, vc, bt, lens = _fp8_case(seed=5)
+    vc[:] = 0x38
+    out, _, _ = oracle.paged_decode_row(q, kc, vc, bt, lens, 1, 2, 0.05, q_dtype=oracle.FP32,
+                                        cache_dtype=oracle.E4M3, k_scale=0.05, v_scale=0.5)
+    assert np.allclose(out, 0.5, atol=1e-15)

@@ -172,8 +172,15 @@ def run_ours(args):
     # ---------------- workload (rank r uses seed 4 + 1000 r: weak scaling)
     w = wl.long_context_decode(seed=rank_seed(rank), block_size=args.block_size,
                                num_seqs=args.num_seqs)
+    fp8 = args.kv_dtype == "e4m3"
+    ksd = vsd = None
+    if fp8:  # same sequences, an e4m3 cache with k_scale = v_scale = 0.05
+        w = wl.as_fp8_history(w, seed=rank_seed(rank) + 100)
+        ksd = torch.tensor([0.05], dtype=torch.float32, device=dev)
+        vsd = torch.tensor([0.05], dtype=torch.float32, device=dev)
     B, HQ, HKV, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
-    kc, vc = up(w.k_cache, torch.bfloat16, dev), up(w.v_cache, torch.bfloat16, dev)
+    cache_t = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    kc, vc = up(w.k_cache, cache_t, dev), up(w.v_cache, cache_t, dev)
     q = up(w.q, torch.bfloat16, dev)
     nk, nv = up(w.new_k, torch.bfloat16, dev), up(w.new_v, torch.bfloat16, dev)
     sl = torch.from_numpy(w.slot_mapping).to(dev)
@@ -185,13 +192,15 @@ def run_ours(args):
     splits, tps = pa.pa_paged_decode_plan(B, HKV, mcl)
     stream = torch.cuda.current_stream()
 
-    attn_bytes = wl.kv_bytes_read(w)                         # algorithmic, decode attention
-    write_bytes = B * HKV * d * 2 * 2 * 2 + B * 8             # new K/V read + written, slots
+    elt = 1 if fp8 else 2
+    attn_bytes = wl.kv_bytes_read(w, elt=elt)                 # algorithmic, decode attention
+    write_bytes = B * HKV * d * 2 * (2 + elt) + B * 8        # new K/V read + written, slots
     step_bytes = attn_bytes + write_bytes
 
     def step():
-        pa.pa_reshape_and_cache(nk, nv, kc, vc, sl)
-        pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp)
+        pa.pa_reshape_and_cache(nk, nv, kc, vc, sl, None, ksd, vsd)
+        pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp, k_scale=ksd,
+                                         v_scale=vsd)
 
     for _ in range(args.warmup):
         step()
@@ -208,9 +217,10 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         start.record(stream)
         for i in range(K):
-            pa.pa_reshape_and_cache(nk, nv, kc, vc, sl)
+            pa.pa_reshape_and_cache(nk, nv, kc, vc, sl, None, ksd, vsd)
             ev[i][0].record(stream)
-            pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp)
+            pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp, k_scale=ksd,
+                                         v_scale=vsd)
             ev[i][1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
@@ -245,9 +255,10 @@ def run_ours(args):
     def e2e_step():
         for dst, src in ((dq, hq), (dk, hk), (dv, hv), (dsl, hsl), (dbt, hbt), (dcl, hcl)):
             dst.copy_(src, non_blocking=True)
-        pa.pa_reshape_and_cache(dk.view(torch.bfloat16), dv.view(torch.bfloat16), kc, vc, dsl)
+        pa.pa_reshape_and_cache(dk.view(torch.bfloat16), dv.view(torch.bfloat16), kc, vc, dsl,
+                                None, ksd, vsd)
         pa.pa_paged_decode_attention(out, dq.view(torch.bfloat16), kc, vc, dbt, dcl, w.scale,
-                                     mcl, wsp)
+                                     mcl, wsp, k_scale=ksd, v_scale=vsd)
         hout.copy_(out.view(torch.int16), non_blocking=True)
 
     for _ in range(args.warmup):
@@ -274,10 +285,11 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16, shuffled block pool)",
+        "dtype": "e4m3 KV, bf16 q/out" if fp8 else "bf16",
+        "data": ("synthetic (seeded random finite e4m3 KV codes, scale 0.05; N(0,1) bf16 q)"
+                 if fp8 else "synthetic (seeded N(0,1) bf16, shuffled block pool)"),
         "config": {"workload": w.name, "num_seqs": B, "num_q_heads": HQ, "num_kv_heads": HKV,
-                   "head_size": d, "block_size": w.block_size,
+                   "head_size": d, "block_size": w.block_size, "kv_dtype": args.kv_dtype,
                    "context_tokens": int(w.context_lens.sum()),
                    "max_context_len": mcl, "splits": splits, "tokens_per_split": tps,
                    "step": "reshape_and_cache(new tokens) + paged_decode_attention",
@@ -396,13 +408,17 @@ def _oracle_decode_sample(w, rows, max_tokens=None):
     lens = w.context_lens.copy()
     if max_tokens is not None:
         lens = np.minimum(lens, max_tokens).astype(np.int32)
+    fp8 = w.k_cache.dtype == np.uint8
+    kw = (dict(cache_dtype=oracle.E4M3, k_scale=w.meta["k_scale"], v_scale=w.meta["v_scale"])
+          if fp8 else {})
     t0 = time.perf_counter()
     for b, h in rows:
-        oracle.paged_decode_row(w.q, w.k_cache, w.v_cache, w.block_tables, lens, b, h, w.scale)
+        oracle.paged_decode_row(w.q, w.k_cache, w.v_cache, w.block_tables, lens, b, h, w.scale,
+                                **kw)
     dt = time.perf_counter() - t0
     G = w.num_q_heads // w.num_kv_heads
     kv_groups = {(b, h // G) for b, h in rows}
-    nbytes = sum(int(lens[b]) * w.head_size * 2 * 2 for b, _ in kv_groups)
+    nbytes = sum(int(lens[b]) * w.head_size * (1 if fp8 else 2) * 2 for b, _ in kv_groups)
     return dt, nbytes
 
 
@@ -477,6 +493,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--kv-dtype", choices=["bf16", "e4m3"], default="bf16",
+                    help="KV cache format of the decode step (e4m3: fp8 with scales)")
     ap.add_argument("--num-seqs", type=int, default=8,
                     help="sequences of the long-context workload (8; fewer for profiling)")
     ap.add_argument("--extra-iters", type=int, default=50)

@@ -142,7 +142,8 @@ pa_status pa_concat_mla_k(void *k, pa_dtype k_dtype, const void *k_nope, const v
  *
  * q, out: [num_seqs, num_q_heads, head_size] bf16, contiguous.
  * k_cache, v_cache: [num_blocks, block_size, num_kv_heads, head_size],
- *   contiguous, cache_dtype PA_BF16 (other dtypes: PA_ERR_UNSUPPORTED).
+ *   contiguous, cache_dtype PA_BF16, or PA_FP8_E4M3 read with unit scales
+ *   (see pa_paged_decode_attention_fp8); other dtypes: PA_ERR_UNSUPPORTED.
  * block_tables: [num_seqs, max_blocks_per_seq] int32; context_lens [num_seqs] int32.
  * head_size: 128.  block_size: a power of two in [8, 256].
  * G: 1, 2, 4, 8 or 16.
@@ -176,6 +177,32 @@ pa_status pa_paged_decode_attention(void *out, const void *q, const void *k_cach
                                     int32_t max_blocks_per_seq, int64_t num_blocks, float scale,
                                     int32_t max_context_len, void *workspace,
                                     size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_paged_decode_attention_fp8 -- decode attention over an FP8 E4M3 cache.
+ *
+ * The cache holds x / k_scale and x / v_scale rounded to e4m3 (written by
+ * pa_reshape_and_cache with the same scales: sglang cache_ops.py,
+ * reshape_and_cache_flash, "optional scale"), so a code stands for
+ * code * scale.  Computes the same attention as pa_paged_decode_attention
+ * with K_j = code * k_scale and V_j = code * v_scale; the codes are read as
+ * they are (half the bytes of bf16), k_scale folds into the score scale and
+ * v_scale into the output.  k_scale, v_scale: both NULL (unit scales) or
+ * both device pointers to one float.  Other arguments, the workspace and the
+ * error word as for pa_paged_decode_attention (which also accepts
+ * PA_FP8_E4M3 caches, with unit scales).  The grouped products run in f16
+ * on the tensor cores: q is carried with a power-of-two prescale, so q
+ * values must be finite.
+ * ---------------------------------------------------------------------- */
+pa_status pa_paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
+                                        const void *v_cache, const float *k_scale,
+                                        const float *v_scale, const int32_t *block_tables,
+                                        const int32_t *context_lens, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_size, int32_t block_size,
+                                        int32_t max_blocks_per_seq, int64_t num_blocks,
+                                        float scale, int32_t max_context_len, void *workspace,
+                                        size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * pa_paged_decode_attention_static -- the same decode attention for callers

@@ -53,7 +53,7 @@ constexpr int kTile = 64;               // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
 constexpr int kStages = 3;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRowBytes = kD * 2;       // one bf16 row of one KV head
+constexpr int kRowBytes = kD * 2;       // one bf16 row of one KV head (tensor map stride)
 constexpr float kRescaleLog2 = 8.0f;    // lazy-rescale threshold (base-2 units)
 constexpr size_t kWorkspaceHeader = 256;  // error word + padding
 
@@ -75,6 +75,8 @@ struct DecodeParams {
   int32_t num_splits;
   int32_t tokens_per_split;
   float scale_log2;
+  const float* k_scale;  // quantised cache: code * k_scale is the value (else null)
+  const float* v_scale;
 };
 
 // context length used by both kernels: clipped to the plan and the table
@@ -97,13 +99,23 @@ __device__ __forceinline__ int effective_len(const DecodeParams& p, int b, bool*
 // row, so that ldmatrix reads eight consecutive tokens from eight different
 // bank groups.  P enters the second product as a pair of bf16 terms (the
 // rounded value and its rounding error), so the weights keep ~16 bits.
-constexpr int kHalfBytes = kTile * 128;  // one 64-row x 64-element region
-struct TcSmemLayout {
-  // per stage: K_lo, K_hi, V_lo, V_hi regions (64 rows x 128 B, swizzled)
-  static constexpr int kStageBytes = 4 * kHalfBytes;
-  static constexpr int kKvBytes = kStages * kStageBytes;
-  static constexpr int kBarOffset = kKvBytes;  // full[], empty[], mask[], abort
-  static constexpr int kBytes = kBarOffset + 3 * kStages * 8 + 16;
+constexpr int kHalfBytes = kTile * 128;  // one 64-row x 128-byte region (8 KB)
+// Shared memory of one CTA.  bf16 cache: per stage K_lo, K_hi, V_lo, V_hi
+// regions (64 rows x 128 B each: one 64-element half of every row).  fp8
+// cache: a 128-element row is 128 bytes, so per stage K and V regions, more
+// stages for the same bytes in flight, and per consumer warp an f16 staging
+// tile (two [16 rows x 128 B] halves) for the converted V slice.  All regions
+// 128-byte swizzled and 1 KB aligned.
+template <bool kFp8>
+struct TcLayout {
+  static constexpr int kStages = kFp8 ? 5 : 3;
+  static constexpr int kRowBytes = kFp8 ? 128 : 256;  // one row of one kv head
+  static constexpr int kStageBytes = (kFp8 ? 2 : 4) * kHalfBytes;
+  static constexpr int kVOffset = (kFp8 ? 1 : 2) * kHalfBytes;
+  static constexpr int kStagingOffset = kStages * kStageBytes;
+  static constexpr int kStagingWarpBytes = kFp8 ? 2 * 16 * 128 : 0;
+  static constexpr int kBarOffset = kStagingOffset + kConsumerWarps * kStagingWarpBytes;
+  static constexpr int kBytes = kBarOffset + 3 * kStages * 8 + 16;  // full, empty, mask, flags
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KB
 };
 
@@ -124,6 +136,24 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+}
+// two e4m3 codes (low byte first) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+      static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
@@ -192,18 +222,21 @@ template <int NT>
 __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem,
                                             float (&o)[8][NT][4], float (&m)[NT][2],
                                             float (&l)[NT][2], int b, int split, int hq0, int G,
-                                            int warp, int lane);
+                                            int warp, int lane, float out_scale);
 
-template <int NT>  // n-tiles of 8 query heads: G <= 8 -> 1, G = 16 -> 2
+// NT: n-tiles of 8 query heads (G <= 8 -> 1, G = 16 -> 2); kFp8: e4m3 cache.
+template <int NT, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_decode_split_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                  const __grid_constant__ CUtensorMap tm_v, const DecodeParams p,
                                  int G) {
   using namespace pa;
+  using Lay = TcLayout<kFp8>;
+  constexpr int kStages = Lay::kStages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // 1 KB-aligned base (the 128-byte swizzle pattern repeats every 1 KB)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TcSmemLayout::kBarOffset);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOffset);
   uint64_t* empty = full + kStages;
   uint64_t* tile_mask = empty + kStages;
   int* abort_ptr = reinterpret_cast<int*>(tile_mask + kStages);
@@ -291,16 +324,22 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t vb = __ballot_sync(0xffffffffu, valid);
       if (lane == 0) {
         tile_mask[stage] = (static_cast<uint64_t>(hi) << 32) | lo;
-        mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(__popc(vb) * rpb * kRowBytes * 2));
+        mbar_arrive_expect_tx(&full[stage],
+                              static_cast<uint32_t>(__popc(vb) * rpb * Lay::kRowBytes * 2));
       }
       __syncwarp();
       if (valid) {
         const int32_t row = bid * bs + row0;
-        uint8_t* st = smem + stage * TcSmemLayout::kStageBytes + lane * rpb * 128;
-        tma_load_3d(st + 0 * kHalfBytes, &tm_k, 0, g, row, &full[stage], pol);
-        tma_load_3d(st + 1 * kHalfBytes, &tm_k, 64, g, row, &full[stage], pol);
-        tma_load_3d(st + 2 * kHalfBytes, &tm_v, 0, g, row, &full[stage], pol);
-        tma_load_3d(st + 3 * kHalfBytes, &tm_v, 64, g, row, &full[stage], pol);
+        uint8_t* st = smem + stage * Lay::kStageBytes + lane * rpb * 128;
+        if constexpr (kFp8) {  // a whole row is one 128-byte box
+          tma_load_3d(st, &tm_k, 0, g, row, &full[stage], pol);
+          tma_load_3d(st + kHalfBytes, &tm_v, 0, g, row, &full[stage], pol);
+        } else {  // two 64-element halves per row
+          tma_load_3d(st + 0 * kHalfBytes, &tm_k, 0, g, row, &full[stage], pol);
+          tma_load_3d(st + 1 * kHalfBytes, &tm_k, 64, g, row, &full[stage], pol);
+          tma_load_3d(st + 2 * kHalfBytes, &tm_v, 0, g, row, &full[stage], pol);
+          tma_load_3d(st + 3 * kHalfBytes, &tm_v, 64, g, row, &full[stage], pol);
+        }
       }
       issued = t + 1;
     }
@@ -310,18 +349,64 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ------------------------------------------------------------ consumers
-    // Q^T as the B operand: b0 = q[head gq][16kk + 2tq .. +1], b1 = [.. + 8]
+    // Q^T as the B operand.  bf16 cache: b0 = q[head gq][16kk + 2tq .. +1],
+    // b1 = [.. + 8].  fp8 cache: the k index of every 16-wide step is
+    // permuted to match how K arrives (see below): b0 = q[16kk + 4tq .. +1],
+    // b1 = q[16kk + 4tq + 2 .. +3], in f16 after a power-of-two prescale
+    // that puts max|q| in [2^14, 2^15) (undone in the score scale).
     uint32_t qb[NT][8][2];
+    float score_scale = p.scale_log2;
+    if constexpr (kFp8) {
+      float qv[NT][8][4];
+      float qmax = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int h = nt * 8 + gq;
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            p.q + (static_cast<int64_t>(b) * p.num_q_heads + hq0 + (h < G ? h : 0)) * kD);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t w0 = h < G ? __ldg(qrow + 8 * kk + 2 * tq) : 0u;
+          const uint32_t w1 = h < G ? __ldg(qrow + 8 * kk + 2 * tq + 1) : 0u;
+          qv[nt][kk][0] = __uint_as_float(w0 << 16);
+          qv[nt][kk][1] = __uint_as_float(w0 & 0xFFFF0000u);
+          qv[nt][kk][2] = __uint_as_float(w1 << 16);
+          qv[nt][kk][3] = __uint_as_float(w1 & 0xFFFF0000u);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) qmax = fmaxf(qmax, fabsf(qv[nt][kk][c]));
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1)
+        qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+      // 2^e with e = 14 - floor(log2(qmax)); finite non-zero q only
+      int e = 0;
+      if (qmax > 0.f && qmax <= 3.0e38f) e = 14 - (static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFF) - 127);
+      const float up = ldexpf(1.0f, e);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          qb[nt][kk][0] = pack_f16x2(qv[nt][kk][0] * up, qv[nt][kk][1] * up);
+          qb[nt][kk][1] = pack_f16x2(qv[nt][kk][2] * up, qv[nt][kk][3] * up);
+        }
+      const float ks = p.k_scale != nullptr ? __ldg(p.k_scale) : 1.f;
+      score_scale = p.scale_log2 * ks * ldexpf(1.0f, -e);
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int h = nt * 8 + gq;
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            p.q + (static_cast<int64_t>(b) * p.num_q_heads + hq0 + (h < G ? h : 0)) * kD);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          qb[nt][kk][0] = h < G ? __ldg(qrow + 8 * kk + tq) : 0u;
+          qb[nt][kk][1] = h < G ? __ldg(qrow + 8 * kk + tq + 4) : 0u;
+        }
+      }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int h = nt * 8 + gq;
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          p.q + (static_cast<int64_t>(b) * p.num_q_heads + hq0 + (h < G ? h : 0)) * kD);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        qb[nt][kk][0] = h < G ? __ldg(qrow + 8 * kk + tq) : 0u;
-        qb[nt][kk][1] = h < G ? __ldg(qrow + 8 * kk + tq + 4) : 0u;
-      }
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         m[nt][j] = -INFINITY;
@@ -340,6 +425,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int k_hi = lane >> 4;        // K: second 8 columns of the k-step
     const int v_hi = (lane >> 3) & 1;  // V: second 8 head elements of the m-tile
     const uint32_t smem_base = smem_u32(smem);
+    // fp8: this warp's f16 staging tile for V (two [16 x 128 B] halves)
+    uint8_t* stg = smem + Lay::kStagingOffset + warp * Lay::kStagingWarpBytes;
+    const uint32_t stg_base = smem_u32(stg);
+    const uint32_t v_row_stg = static_cast<uint32_t>(((lane & 7) + 8 * (lane >> 4)) * 128);
 
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
@@ -350,11 +439,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       const uint32_t mask16 = static_cast<uint32_t>(tile_mask[stage] >> r0) & 0xFFFFu;
-      const uint32_t st_base = smem_base + stage * TcSmemLayout::kStageBytes;
+      const uint32_t st_base = smem_base + stage * Lay::kStageBytes;
       if (mask16 != 0u) {
-        if (mask16 != 0xFFFFu) {
+        if (!kFp8 && mask16 != 0xFFFFu) {
           // rows without a token: zero their V rows (0 x NaN would poison P.V)
-          uint8_t* vrow0 = smem + stage * TcSmemLayout::kStageBytes + 2 * kHalfBytes;
+          uint8_t* vrow0 = smem + stage * Lay::kStageBytes + Lay::kVOffset;
           for (int idx = lane; idx < 16 * 16; idx += 32) {
             const int rr = idx >> 4, unit = idx & 15;
             if (!((mask16 >> rr) & 1u))
@@ -369,15 +458,41 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int c = 0; c < 4; ++c) s0[nt][c] = s1[nt][c] = 0.f;
+        if constexpr (kFp8) {
+          // One ldmatrix.x4 over 32 bytes of 16 fp8 rows (byte pairs as b16)
+          // gives each lane 4 consecutive codes per row and 16-byte group:
+          // row gq in r[0]/r[2], row gq + 8 in r[1]/r[3].  Within a 16-wide
+          // k-step the codes 4tq..4tq+3 serve as k = 2tq, 2tq+1, 2tq+8,
+          // 2tq+9 -- the same permutation q's fragments use.
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          uint32_t a[4];
-          const uint32_t u = static_cast<uint32_t>(((2 * kk) & 7) + k_hi);
-          ldsm_x4(st_base + (kk >> 2) * kHalfBytes + k_row + ((u ^ sw) << 4), a);
+          for (int ks2 = 0; ks2 < 4; ++ks2) {
+            uint32_t r[4];
+            const uint32_t u = static_cast<uint32_t>(2 * ks2 + k_hi);
+            ldsm_x4(st_base + k_row + ((u ^ sw) << 4), r);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            if (kk & 1) mma_bf16_16816(s1[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
-            else mma_bf16_16816(s0[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+            for (int half = 0; half < 2; ++half) {
+              const int kk = 2 * ks2 + half;
+              const uint32_t a[4] = {e4m3x2_to_f16x2(r[2 * half]), e4m3x2_to_f16x2(r[2 * half + 1]),
+                                     e4m3x2_to_f16x2(r[2 * half] >> 16),
+                                     e4m3x2_to_f16x2(r[2 * half + 1] >> 16)};
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                if (half) mma_f16_16816(s1[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+                else mma_f16_16816(s0[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            uint32_t a[4];
+            const uint32_t u = static_cast<uint32_t>(((2 * kk) & 7) + k_hi);
+            ldsm_x4(st_base + (kk >> 2) * kHalfBytes + k_row + ((u ^ sw) << 4), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              if (kk & 1) mma_bf16_16816(s1[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+              else mma_bf16_16816(s0[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+            }
           }
         }
         const bool v0 = (mask16 >> gq) & 1u;        // token r0 + gq
@@ -387,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int nt = 0; nt < NT; ++nt) {
           float s[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) s[c] = (s0[nt][c] + s1[nt][c]) * p.scale_log2;
+          for (int c = 0; c < 4; ++c) s[c] = (s0[nt][c] + s1[nt][c]) * score_scale;
           if (!v0) s[0] = s[1] = -INFINITY;
           if (!v1) s[2] = s[3] = -INFINITY;
           float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
@@ -415,6 +530,19 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float p3 = v1 ? exp2f(s[3] - m[nt][1]) : 0.f;
           l[nt][0] += p0 + p2;
           l[nt][1] += p1 + p3;
+          const int srcA = 8 * tq + (gq >> 1);
+          const int srcB = srcA + 4;
+          const uint32_t sel = (gq & 1) ? 0x7632u : 0x5410u;
+          if constexpr (kFp8) {
+            // P in f16 (11 significant bits) for the f16 product with V
+            const uint32_t f01 = pack_f16x2(p0, p1);
+            const uint32_t f23 = pack_f16x2(p2, p3);
+            pb[nt][0] = __byte_perm(__shfl_sync(0xffffffffu, f01, srcA),
+                                    __shfl_sync(0xffffffffu, f01, srcB), sel);
+            pb[nt][1] = __byte_perm(__shfl_sync(0xffffffffu, f23, srcA),
+                                    __shfl_sync(0xffffffffu, f23, srcB), sel);
+            continue;
+          }
           // P as hi + lo bf16 pairs (hi = bf16(p), lo = bf16(p - hi)): the two
           // products together carry ~16 significant bits of each weight
           const uint32_t h01 = pack_bf16x2(p0, p1);  // token gq,     heads 2tq, 2tq+1
@@ -424,9 +552,6 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint32_t l23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16),
                                            p3 - __uint_as_float(h23 & 0xFFFF0000u));
           // transpose into the B operand: b0 = P[2tq, 2tq+1][gq], b1 = P[2tq+8, 2tq+9][gq]
-          const int srcA = 8 * tq + (gq >> 1);
-          const int srcB = srcA + 4;
-          const uint32_t sel = (gq & 1) ? 0x7632u : 0x5410u;
           pb[nt][0] = __byte_perm(__shfl_sync(0xffffffffu, h01, srcA),
                                   __shfl_sync(0xffffffffu, h01, srcB), sel);
           pb[nt][1] = __byte_perm(__shfl_sync(0xffffffffu, h23, srcA),
@@ -437,18 +562,50 @@ __global__ void __launch_bounds__(kThreads, 2)
                                   __shfl_sync(0xffffffffu, l23, srcB), sel);
         }
         // ---- O^T += V^T . P^T
+        if constexpr (kFp8) {
+          // convert this warp's 16 fp8 V rows to f16 in the staging tile
+          // (rows without a token become zeros: 0 x NaN would poison P.V)
+          const int rr = lane >> 1, hf = lane & 1;
+          const int row = r0 + rr;
+          const bool rv = (mask16 >> rr) & 1u;
+          const uint8_t* vsrc = smem + stage * Lay::kStageBytes + Lay::kVOffset + row * 128;
+          uint8_t* dst = stg + hf * (16 * 128) + rr * 128;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          uint32_t a[4];
-          const uint32_t u = static_cast<uint32_t>(((2 * mt) & 7) + v_hi);
-          ldsm_x4_trans(st_base + (2 + (mt >> 2)) * kHalfBytes + v_row + ((u ^ sw) << 4), a);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_bf16_16816(o[mt][nt], a, pb[nt][0], pb[nt][1]);
-            mma_bf16_16816(o[mt][nt], a, pl[nt][0], pl[nt][1]);
+          for (int c = 0; c < 4; ++c) {
+            const int u = 4 * hf + c;
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (rv) x = *reinterpret_cast<const uint4*>(vsrc + ((u ^ (row & 7)) << 4));
+            const uint4 y0 = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16),
+                                        e4m3x2_to_f16x2(x.y), e4m3x2_to_f16x2(x.y >> 16));
+            const uint4 y1 = make_uint4(e4m3x2_to_f16x2(x.z), e4m3x2_to_f16x2(x.z >> 16),
+                                        e4m3x2_to_f16x2(x.w), e4m3x2_to_f16x2(x.w >> 16));
+            *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (rr & 7)) << 4)) = y0;
+            *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (rr & 7)) << 4)) = y1;
           }
+          __syncwarp();
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a[4];
+            const uint32_t u = static_cast<uint32_t>(((2 * mt) & 7) + v_hi);
+            ldsm_x4_trans(stg_base + (mt >> 2) * (16 * 128) + v_row_stg + ((u ^ sw) << 4), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+          }
+          __syncwarp();  // staging is rewritten by the next tile
+        } else {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a[4];
+            const uint32_t u = static_cast<uint32_t>(((2 * mt) & 7) + v_hi);
+            ldsm_x4_trans(st_base + (2 + (mt >> 2)) * kHalfBytes + v_row + ((u ^ sw) << 4), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_bf16_16816(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+              mma_bf16_16816(o[mt][nt], a, pl[nt][0], pl[nt][1]);
+            }
+          }
+          if (mask16 != 0xFFFFu) fence_proxy_async_smem();  // generic writes before the next TMA
         }
-        if (mask16 != 0xFFFFu) fence_proxy_async_smem();  // generic writes before the next TMA
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
@@ -471,7 +628,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       p.ws_lse[(static_cast<int64_t>(b) * p.num_q_heads + hq0 + threadIdx.x) * p.num_splits +
                split] = -INFINITY;
   } else {
-    epilogue_tc<NT>(p, smem, o, m, l, b, split, hq0, G, warp, lane);
+    const float out_scale = (kFp8 && p.v_scale != nullptr) ? __ldg(p.v_scale) : 1.f;
+    epilogue_tc<NT>(p, smem, o, m, l, b, split, hq0, G, warp, lane, out_scale);
   }
   if (p.num_splits == 1) return;
 
@@ -506,7 +664,7 @@ template <int NT>
 __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem,
                                             float (&o)[8][NT][4], float (&m)[NT][2],
                                             float (&l)[NT][2], int b, int split, int hq0, int G,
-                                            int warp, int lane) {
+                                            int warp, int lane, float out_scale) {
   constexpr int NWARP_GROUPS = kConsumerWarps;
   const int gq = lane >> 2;
   const int tq = lane & 3;
@@ -570,7 +728,7 @@ __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem
       acc4.w += wt * v.w;
     }
     const float Ls = fin[2 * h + 1];
-    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    const float inv = Ls > 0.f ? out_scale / Ls : 0.f;
     acc4.x *= inv;
     acc4.y *= inv;
     acc4.z *= inv;
@@ -619,18 +777,36 @@ bool make_kv_map_swizzled(CUtensorMap* map, const void* base, int64_t rows, int3
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NT>
+// [rows, H_KV, 128] e4m3 viewed 3-D as bytes; box = a whole 128-byte row x
+// 1 head x box_rows rows, 128-byte swizzled.
+bool make_kv_map_fp8(CUtensorMap* map, const void* base, int64_t rows, int32_t num_kv_heads,
+                     int32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(num_kv_heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD),
+                                 static_cast<cuuint64_t>(kD) * num_kv_heads};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), 1u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NT, bool kFp8>
 pa_status launch_split_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p,
                           dim3 grid, int G, cudaStream_t stream) {
   static std::atomic<bool> attr_set{false};
-  auto kern = paged_decode_split_tc_kernel<NT>;
+  auto kern = paged_decode_split_tc_kernel<NT, kFp8>;
+  constexpr int kSmem = TcLayout<kFp8>::kAlloc;
   if (!attr_set.load()) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TcSmemLayout::kAlloc) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+        cudaSuccess)
       return PA_ERR_CUDA;
     attr_set.store(true);
   }
-  kern<<<grid, kThreads, TcSmemLayout::kAlloc, stream>>>(mk, mv, p, G);
+  kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, p, G);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -710,10 +886,14 @@ pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int32_t G = a.num_q_heads / a.num_kv_heads;
   const int64_t rows = a.num_blocks * a.block_size;
   const int32_t box_rows = a.block_size < kTile ? a.block_size : kTile;
+  const bool fp8 = a.cache_dtype == PA_FP8_E4M3;
   CUtensorMap mk, mv;
-  if (!make_kv_map_swizzled(&mk, a.k_cache, rows, a.num_kv_heads, box_rows) ||
-      !make_kv_map_swizzled(&mv, a.v_cache, rows, a.num_kv_heads, box_rows))
-    return PA_ERR_CUDA;
+  const bool maps_ok =
+      fp8 ? make_kv_map_fp8(&mk, a.k_cache, rows, a.num_kv_heads, box_rows) &&
+                make_kv_map_fp8(&mv, a.v_cache, rows, a.num_kv_heads, box_rows)
+          : make_kv_map_swizzled(&mk, a.k_cache, rows, a.num_kv_heads, box_rows) &&
+                make_kv_map_swizzled(&mv, a.v_cache, rows, a.num_kv_heads, box_rows);
+  if (!maps_ok) return PA_ERR_CUDA;
 
   DecodeParams p;
   p.out = static_cast<__nv_bfloat16*>(a.out);
@@ -738,13 +918,21 @@ pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.num_splits = a.plan.num_splits;
   p.tokens_per_split = a.plan.tokens_per_split;
   p.scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
 
   const dim3 grid(static_cast<unsigned>(a.plan.num_splits), static_cast<unsigned>(a.num_kv_heads),
                   static_cast<unsigned>(a.num_seqs));
   pa_status st;
   switch (G) {
-    case 1: case 2: case 4: case 8: st = launch_split_tc<1>(mk, mv, p, grid, G, stream); break;
-    case 16: st = launch_split_tc<2>(mk, mv, p, grid, G, stream); break;
+    case 1: case 2: case 4: case 8:
+      st = fp8 ? launch_split_tc<1, true>(mk, mv, p, grid, G, stream)
+               : launch_split_tc<1, false>(mk, mv, p, grid, G, stream);
+      break;
+    case 16:
+      st = fp8 ? launch_split_tc<2, true>(mk, mv, p, grid, G, stream)
+               : launch_split_tc<2, false>(mk, mv, p, grid, G, stream);
+      break;
     default: return PA_ERR_UNSUPPORTED;
   }
   return st;

@@ -53,7 +53,7 @@ pa_status check_decode(void* out, const void* q, const void* k_cache, const void
     return PA_ERR_INVALID;
   if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
   if (!std::isfinite(scale)) return PA_ERR_INVALID;
-  if (cache_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (cache_dtype != PA_BF16 && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
   if (head_size != 128) return PA_ERR_UNSUPPORTED;
   const int32_t G = num_q_heads / num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PA_ERR_UNSUPPORTED;
@@ -76,6 +76,9 @@ pa_status check_decode(void* out, const void* q, const void* k_cache, const void
   a->max_blocks_per_seq = max_blocks_per_seq;
   a->num_blocks = num_blocks;
   a->scale = scale;
+  a->cache_dtype = cache_dtype;
+  a->k_scale = nullptr;
+  a->v_scale = nullptr;
   a->plan = pa_detail::make_decode_plan(num_seqs, num_kv_heads, max_context_len,
                                         pa_detail::num_sms_current_device());
   return PA_OK;
@@ -224,6 +227,33 @@ pa_status pa_paged_decode_attention(void* out, const void* q, const void* k_cach
   if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
   a.workspace = workspace;
   a.error_word = nullptr;
+  return pa_detail::launch_paged_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_paged_decode_attention_fp8(void* out, const void* q, const void* k_cache,
+                                        const void* v_cache, const float* k_scale,
+                                        const float* v_scale, const int32_t* block_tables,
+                                        const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_size, int32_t block_size,
+                                        int32_t max_blocks_per_seq, int64_t num_blocks,
+                                        float scale, int32_t max_context_len, void* workspace,
+                                        size_t workspace_bytes, pa_stream_t stream) {
+  if ((k_scale == nullptr) != (v_scale == nullptr)) return PA_ERR_INVALID;
+  pa_detail::DecodeArgs a{};
+  const pa_status st = check_decode(out, q, k_cache, v_cache, PA_FP8_E4M3, block_tables,
+                                    context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                    block_size, max_blocks_per_seq, num_blocks, scale,
+                                    max_context_len, &a);
+  if (st != PA_OK) return st;
+  const size_t need =
+      pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size, a.plan);
+  if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
+  a.workspace = workspace;
+  a.error_word = nullptr;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   return pa_detail::launch_paged_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

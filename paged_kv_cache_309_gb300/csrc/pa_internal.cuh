@@ -331,6 +331,9 @@ struct DecodeArgs {
   int64_t num_blocks;
   float scale;
   DecodePlan plan;
+  pa_dtype cache_dtype;    // PA_BF16 or PA_FP8_E4M3
+  const float* k_scale;    // e4m3 cache: device scalars (null = 1)
+  const float* v_scale;
 };
 pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
 

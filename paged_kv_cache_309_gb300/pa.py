@@ -58,6 +58,9 @@ def _load():
     lib.pa_paged_decode_attention.argtypes = [P, P, P, P, E, P, P, I32, I32, I32, I32, I32, I32,
                                               I64, F32, I32, P, SZ, P]
     lib.pa_paged_decode_attention.restype = E
+    lib.pa_paged_decode_attention_fp8.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I32, I32,
+                                                  I32, I32, I64, F32, I32, P, SZ, P]
+    lib.pa_paged_decode_attention_fp8.restype = E
     lib.pa_paged_decode_attention_static.argtypes = [P, P, P, P, E, P, P, I32, I32, I32, I32,
                                                      I32, I32, I64, F32, I32, P, P]
     lib.pa_paged_decode_attention_static.restype = E
@@ -184,9 +187,12 @@ def read_device_error(workspace) -> int:
 
 
 def pa_paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale,
-                              max_context_len, workspace, stream=None):
-    """out/q [B, H_Q, d] bf16; caches [num_blocks, bs, H_KV, d] bf16 contiguous;
-    block_tables [B, max_blocks_per_seq] int32; context_lens [B] int32."""
+                              max_context_len, workspace, stream=None, k_scale=None,
+                              v_scale=None):
+    """out/q [B, H_Q, d] bf16; caches [num_blocks, bs, H_KV, d] bf16 or
+    float8_e4m3fn, contiguous; block_tables [B, max_blocks_per_seq] int32;
+    context_lens [B] int32.  With k_scale/v_scale (one-element float32 device
+    tensors) the e4m3 cache goes through pa_paged_decode_attention_fp8."""
     lib = _load()
     B, HQ, d = q.shape
     nb, bs, HKV, dc = k_cache.shape
@@ -202,6 +208,16 @@ def pa_paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_le
         raise ValueError("block_tables must be [B, max_blocks_per_seq], context_lens [B]")
     if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
         raise ValueError("q and out must be bf16")
+    if k_scale is not None or v_scale is not None:
+        if k_cache.dtype != torch.float8_e4m3fn:
+            raise ValueError("k_scale/v_scale apply to an e4m3 cache")
+        st = lib.pa_paged_decode_attention_fp8(
+            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+            _ptr(block_tables), _ptr(context_lens), B, HQ, HKV, d, bs, block_tables.shape[1], nb,
+            float(scale), int(max_context_len), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+        _check(st, "pa_paged_decode_attention_fp8")
+        return
     st = lib.pa_paged_decode_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype(k_cache), _ptr(block_tables),
         _ptr(context_lens), B, HQ, HKV, d, bs, block_tables.shape[1], nb, float(scale),

@@ -151,6 +151,39 @@ def make_decode(name, seed, num_seqs, ctx_lo, ctx_hi, num_q_heads, num_kv_heads,
                           meta=dict(seed=seed, ctx_lo=ctx_lo, ctx_hi=ctx_hi, pool_blocks=pool_blocks))
 
 
+def random_e4m3_codes(gen: torch.Generator, shape, exp_lo=4, exp_hi=11) -> np.ndarray:
+    """Random finite e4m3 codes: random sign and mantissa, exponent field
+    uniform in [exp_lo, exp_hi] (values 2^(exp_lo-7) .. 2^(exp_hi-6))."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint8)
+    combos = 2 * 8 * (exp_hi - exp_lo + 1)  # sign x mantissa x exponent
+    for lo in range(0, n, _CHUNK):
+        hi = min(n, lo + _CHUNK)
+        c = torch.randint(0, combos, (hi - lo,), generator=gen, dtype=torch.int16).numpy()
+        c = c.astype(np.uint16)
+        sign, man, ex = c & 1, (c >> 1) & 7, exp_lo + (c >> 4)
+        out[lo:hi] = ((sign << 7) | (ex << 3) | man).astype(np.uint8)
+    return out.reshape(shape)
+
+
+def as_fp8_history(w: DecodeWorkload, seed: int, k_scale=0.05, v_scale=0.05) -> DecodeWorkload:
+    """The same sequences, block tables and new tokens with an e4m3 cache:
+    history rows are random finite codes, every other row the e4m3 NaN code
+    (0x7F).  The new tokens stay bf16; the decode step writes them with the
+    scales."""
+    g = _gen(seed)
+    hist = w.k_cache != BF16_NAN
+    kc = np.full(w.k_cache.shape, E4M3_NAN, np.uint8)
+    vc = np.full(w.v_cache.shape, E4M3_NAN, np.uint8)
+    kc[hist] = random_e4m3_codes(g, (int(hist.sum()),))
+    vc[hist] = random_e4m3_codes(g, (int(hist.sum()),))
+    w2 = DecodeWorkload(name=w.name + "_e4m3", q=w.q, k_cache=kc, v_cache=vc,
+                        block_tables=w.block_tables, context_lens=w.context_lens,
+                        new_k=w.new_k, new_v=w.new_v, slot_mapping=w.slot_mapping,
+                        scale=w.scale, meta=dict(w.meta, k_scale=k_scale, v_scale=v_scale))
+    return w2
+
+
 def kv_bytes_read(w: DecodeWorkload, elt: int = 2) -> int:
     """Algorithmic bytes of one decode-attention pass: every context token's
     K and V row for every KV head, the block-table entries those tokens use,

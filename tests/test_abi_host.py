@@ -118,7 +118,7 @@ def test_decode_rejects(lib):
     assert _dec(lib, q=None, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_INVALID
     assert _dec(lib, HQ=12, HKV=8, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_INVALID
     assert _dec(lib, scale=float("nan"), ws=FAKE, wsb=1 << 20) == pa.PA_ERR_INVALID
-    assert _dec(lib, cd=pa.PA_FP8_E4M3, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED
+    assert _dec(lib, cd=pa.PA_FP16, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED
     assert _dec(lib, d=64, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED
     assert _dec(lib, HQ=24, HKV=8, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED  # G=3
     assert _dec(lib, bs=12, ws=FAKE, wsb=1 << 20) == pa.PA_ERR_UNSUPPORTED

@@ -74,6 +74,10 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_and_cache_kernel(ReshapeA
     const bool scaled = a.k_scale != nullptr;
     const Divisor ks = make_divisor(scaled ? __ldg(a.k_scale) : 1.0f);
     const Divisor vs = make_divisor(scaled ? __ldg(a.v_scale) : 1.0f);
+    constexpr bool kToE4m3 = std::is_same<D, e4m3>::value;
+    // largest |x| whose product with r = 1/s stays below FLT_MAX (finite,
+    // so that infinities take the library path)
+    const float kxmax = fminf(1.7e38f * ks.s, 3.0e38f), vxmax = fminf(1.7e38f * vs.s, 3.0e38f);
 #pragma unroll
     for (int i = 0; i < kChunksPerLane; ++i) {
       const int c = c_begin + 32 * i;
@@ -81,15 +85,23 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_and_cache_kernel(ReshapeA
         float f[8];
         to_f32(kv[i], f);
         if (scaled) {
+          if constexpr (kToE4m3) {
+            div8_for_e4m3(f, ks, kxmax);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = div_rn(f[e], ks);  // IEEE quotient
+            for (int e = 0; e < 8; ++e) f[e] = div_rn(f[e], ks);  // IEEE quotient
+          }
         }
         store8(kdst + 8 * c, from_f32<D>(f));
         if (has_v) {
           to_f32(vv[i], f);
           if (scaled) {
+            if constexpr (kToE4m3) {
+              div8_for_e4m3(f, vs, vxmax);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = div_rn(f[e], vs);
+              for (int e = 0; e < 8; ++e) f[e] = div_rn(f[e], vs);
+            }
           }
           store8(vdst + 8 * c, from_f32<D>(f));
         }

@@ -102,13 +102,14 @@ __device__ __forceinline__ int effective_len(const DecodeParams& p, int b, bool*
 constexpr int kHalfBytes = kTile * 128;  // one 64-row x 128-byte region (8 KB)
 // Shared memory of one CTA.  bf16 cache: per stage K_lo, K_hi, V_lo, V_hi
 // regions (64 rows x 128 B each: one 64-element half of every row).  fp8
-// cache: a 128-element row is 128 bytes, so per stage K and V regions, more
-// stages for the same bytes in flight, and per consumer warp an f16 staging
+// cache: a 128-element row is 128 bytes, so per stage K and V regions, a
+// smaller CTA (three per SM, for more warps), and per consumer warp an f16 staging
 // tile (two [16 rows x 128 B] halves) for the converted V slice.  All regions
 // 128-byte swizzled and 1 KB aligned.
 template <bool kFp8>
 struct TcLayout {
-  static constexpr int kStages = kFp8 ? 5 : 3;
+  static constexpr int kStages = 3;
+  static constexpr int kCtasPerSm = kFp8 ? 3 : 2;  // fp8 needs more warps per SM
   static constexpr int kRowBytes = kFp8 ? 128 : 256;  // one row of one kv head
   static constexpr int kStageBytes = (kFp8 ? 2 : 4) * kHalfBytes;
   static constexpr int kVOffset = (kFp8 ? 1 : 2) * kHalfBytes;
@@ -226,7 +227,7 @@ __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem
 
 // NT: n-tiles of 8 query heads (G <= 8 -> 1, G = 16 -> 2); kFp8: e4m3 cache.
 template <int NT, bool kFp8>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
     paged_decode_split_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                  const __grid_constant__ CUtensorMap tm_v, const DecodeParams p,
                                  int G) {
@@ -565,7 +566,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         if constexpr (kFp8) {
           // convert this warp's 16 fp8 V rows to f16 in the staging tile
           // (rows without a token become zeros: 0 x NaN would poison P.V)
-          const int rr = lane >> 1, hf = lane & 1;
+          // lanes 0-15: rows 0-15 of the low half, 16-31: the high half, so the
+          // eight lanes of each shared-memory phase hit eight distinct units
+          const int rr = lane & 15, hf = lane >> 4;
           const int row = r0 + rr;
           const bool rv = (mask16 >> rr) & 1u;
           const uint8_t* vsrc = smem + stage * Lay::kStageBytes + Lay::kVOffset + row * 128;

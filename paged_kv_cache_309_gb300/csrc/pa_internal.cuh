@@ -170,9 +170,42 @@ __device__ __forceinline__ Divisor make_divisor(float s) {
   d.s = s;
   d.r = __frcp_rn(s);
   const float as = fabsf(s);
-  d.fast = as >= 0x1p-30f && as <= 0x1p30f;  // false for NaN
+  d.fast = s > 0.f && as >= 0x1p-30f && as <= 0x1p30f;  // false for NaN
   return d;
 }
+// Chunk of eight quotients by the library division (kept out of line: the
+// rare path of div8_for_e4m3).
+__device__ __noinline__ void div8_library(float (&f)[8], float s) {
+#pragma unroll 1
+  for (int e = 0; e < 8; ++e) f[e] = __fdiv_rn(f[e], s);
+}
+
+// Eight quotients x / s that only feed a round-to-nearest cast to E4M3.
+// Such a cast depends on the fp32 quotient only where |x / s| lies in
+// [2^-11, 480]: smaller values become +-0, larger ones saturate.  With the
+// divisor in [2^-30, 2^30] (d.fast), every quotient in that band has
+// |x| >= 2^-41, where the two residual corrections of div_rn are exact, so
+// no per-value range test is needed -- only that x * r cannot overflow (the
+// chunk's largest |x| at most xmax; NaN passes through as NaN) -- and the
+// sign of a zero quotient is restored from x.  Other chunks use the library.
+__device__ __forceinline__ void div8_for_e4m3(float (&f)[8], const Divisor& d, float xmax) {
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+  if (d.fast && amax <= xmax) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float x = f[e];
+      float q = __fmul_rn(x, d.r);
+      q = __fmaf_rn(__fmaf_rn(-d.s, q, x), d.r, q);
+      q = __fmaf_rn(__fmaf_rn(-d.s, q, x), d.r, q);
+      f[e] = copysignf(q, x);
+    }
+  } else {
+    div8_library(f, d.s);
+  }
+}
+
 __device__ __forceinline__ float div_rn(float x, const Divisor& d) {
   const float ax = fabsf(x);
   if (d.fast && ax >= 0x1p-60f && ax <= 0x1p60f) {

@@ -23,7 +23,7 @@ constexpr int kChunksPerLane = 4;    // chunks of 8 elements per lane per tensor
 constexpr int kChunksPerWarp = 32 * kChunksPerLane;
 
 template <typename S, typename D, bool kRaw>
-__global__ void __launch_bounds__(kWarps * 32) reshape_and_cache_kernel(ReshapeArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(ReshapeArgs a) {
   using namespace pa;
   const int lane = threadIdx.x & 31;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);

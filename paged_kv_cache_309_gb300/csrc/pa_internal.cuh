@@ -175,9 +175,13 @@ __device__ __forceinline__ Divisor make_divisor(float s) {
 }
 // Chunk of eight quotients by the library division (kept out of line: the
 // rare path of div8_for_e4m3).
-__device__ __noinline__ void div8_library(float (&f)[8], float s) {
-#pragma unroll 1
-  for (int e = 0; e < 8; ++e) f[e] = __fdiv_rn(f[e], s);
+struct F8 {
+  float v[8];
+};
+static __device__ __noinline__ F8 div8_library(F8 x, float s) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) x.v[e] = __fdiv_rn(x.v[e], s);
+  return x;
 }
 
 // Eight quotients x / s that only feed a round-to-nearest cast to E4M3.
@@ -202,7 +206,12 @@ __device__ __forceinline__ void div8_for_e4m3(float (&f)[8], const Divisor& d, f
       f[e] = copysignf(q, x);
     }
   } else {
-    div8_library(f, d.s);
+    F8 t;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) t.v[e] = f[e];
+    t = div8_library(t, d.s);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = t.v[e];
   }
 }
 

@@ -2,9 +2,10 @@
 
 Step (the timed unit): one decode step of one layer on the long-context
 workload -- B=8 sequences with contexts of 32K..128K tokens, H_Q=32, H_KV=8,
-d=128, bf16, block size 16, shuffled physical blocks:
-    pa_reshape_and_cache   (write each sequence's newest K/V token)
-    pa_paged_decode_attention  (split kernel with the log-sum-exp merge)
+d=128, bf16, block size 16, shuffled physical blocks: write each sequence's
+newest K/V token into the paged cache, then decode attention over it --
+one launch of pa_paged_decode_step (--step two-call: pa_reshape_and_cache
+followed by pa_paged_decode_attention).
 Inputs are resident in HBM before the timed region; the KV cache (~2.9 GB)
 is far larger than L2 (129 MB), so no flush is needed between steps.
 
@@ -197,10 +198,16 @@ def run_ours(args):
     write_bytes = B * HKV * d * 2 * (2 + elt) + B * 8        # new K/V read + written, slots
     step_bytes = attn_bytes + write_bytes
 
+    fused = args.step == "fused"
+
     def step():
+        if fused:
+            pa.pa_paged_decode_step(out, q, nk, nv, sl, kc, vc, bt, cl, w.scale, mcl, wsp,
+                                    k_scale=ksd, v_scale=vsd)
+            return
         pa.pa_reshape_and_cache(nk, nv, kc, vc, sl, None, ksd, vsd)
         pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp, k_scale=ksd,
-                                         v_scale=vsd)
+                                     v_scale=vsd)
 
     for _ in range(args.warmup):
         step()
@@ -217,10 +224,15 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         start.record(stream)
         for i in range(K):
-            pa.pa_reshape_and_cache(nk, nv, kc, vc, sl, None, ksd, vsd)
-            ev[i][0].record(stream)
-            pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp, k_scale=ksd,
-                                         v_scale=vsd)
+            if fused:
+                ev[i][0].record(stream)
+                pa.pa_paged_decode_step(out, q, nk, nv, sl, kc, vc, bt, cl, w.scale, mcl, wsp,
+                                        k_scale=ksd, v_scale=vsd)
+            else:
+                pa.pa_reshape_and_cache(nk, nv, kc, vc, sl, None, ksd, vsd)
+                ev[i][0].record(stream)
+                pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp,
+                                             k_scale=ksd, v_scale=vsd)
             ev[i][1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
@@ -236,7 +248,8 @@ def run_ours(args):
     value = job_bytes / (ms_step * 1e-3) / 1e9
     attn_ms_avg = statistics.mean(attn_ms)
     peak, peak_kind = hbm_peak()
-    achieved = attn_bytes / (attn_ms_avg * 1e-3) / 1e9
+    kernel_bytes = step_bytes if fused else attn_bytes  # what the timed launch moves
+    achieved = kernel_bytes / (attn_ms_avg * 1e-3) / 1e9
     traffic = traffic_record(os.path.join(ROOT, "paged_kv_cache_309_gb300", "csrc", "decode.cu"))
 
     # ---------------- end to end through the C ABI with pinned host buffers
@@ -255,10 +268,15 @@ def run_ours(args):
     def e2e_step():
         for dst, src in ((dq, hq), (dk, hk), (dv, hv), (dsl, hsl), (dbt, hbt), (dcl, hcl)):
             dst.copy_(src, non_blocking=True)
-        pa.pa_reshape_and_cache(dk.view(torch.bfloat16), dv.view(torch.bfloat16), kc, vc, dsl,
-                                None, ksd, vsd)
-        pa.pa_paged_decode_attention(out, dq.view(torch.bfloat16), kc, vc, dbt, dcl, w.scale,
-                                     mcl, wsp, k_scale=ksd, v_scale=vsd)
+        if fused:
+            pa.pa_paged_decode_step(out, dq.view(torch.bfloat16), dk.view(torch.bfloat16),
+                                    dv.view(torch.bfloat16), dsl, kc, vc, dbt, dcl, w.scale, mcl,
+                                    wsp, k_scale=ksd, v_scale=vsd)
+        else:
+            pa.pa_reshape_and_cache(dk.view(torch.bfloat16), dv.view(torch.bfloat16), kc, vc,
+                                    dsl, None, ksd, vsd)
+            pa.pa_paged_decode_attention(out, dq.view(torch.bfloat16), kc, vc, dbt, dcl,
+                                         w.scale, mcl, wsp, k_scale=ksd, v_scale=vsd)
         hout.copy_(out.view(torch.int16), non_blocking=True)
 
     for _ in range(args.warmup):
@@ -292,21 +310,23 @@ def run_ours(args):
                    "head_size": d, "block_size": w.block_size, "kv_dtype": args.kv_dtype,
                    "context_tokens": int(w.context_lens.sum()),
                    "max_context_len": mcl, "splits": splits, "tokens_per_split": tps,
-                   "step": "reshape_and_cache(new tokens) + paged_decode_attention",
+                   "step": ("paged_decode_step (new-token write + attention, one launch)" if fused
+                            else "reshape_and_cache(new tokens) + paged_decode_attention"),
                    "l2": "inputs larger than L2 (KV cache %.2f GB)" % (
                        2 * w.k_cache.nbytes / 1e9),
                    "parallelism": f"replicas x{ws_n} (independent sequences per GPU)"},
         "pct_of_hbm_peak": round(100 * value / peak, 2),
         "sequences_per_s": round(job_seqs / (ms_step * 1e-3), 1),
-        "roofline": {"kernel": "paged_decode_split_tc_kernel (split-K with in-kernel merge)",
+        "roofline": {"kernel": "paged_decode_split_tc_kernel" + (" (fused write, in-kernel merge)"
+                                                                 if fused else " (in-kernel merge)"),
                      "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "bytes_per_launch": attn_bytes, "avg_launch_us": round(attn_ms_avg * 1e3, 2)},
+                     "bytes_per_launch": kernel_bytes, "avg_launch_us": round(attn_ms_avg * 1e3, 2)},
         "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
+        "gpu_launches": (1 if fused else 2) * K,
         "clocks": clk.summary(),
     }
 
@@ -493,6 +513,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--step", choices=["fused", "two-call"], default="fused",
+                    help="decode step as one launch (pa_paged_decode_step) or write + attention")
     ap.add_argument("--kv-dtype", choices=["bf16", "e4m3"], default="bf16",
                     help="KV cache format of the decode step (e4m3: fp8 with scales)")
     ap.add_argument("--num-seqs", type=int, default=8,

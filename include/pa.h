@@ -1,11 +1,12 @@
 /*
  * pa.h -- C ABI of the GB300 (sm_103a) paged KV-cache library.
  *
- * Three operations of the decode/prefill hot path of a paged-KV serving
- * engine:
- *   pa_reshape_and_cache       scatter per-token K/V into a paged cache
- *   pa_concat_mla_k            assemble MLA K from k_nope and a shared k_rope
- *   pa_paged_decode_attention  GQA decode attention over the paged cache
+ * Operations of the decode/prefill hot path of a paged-KV serving engine:
+ *   pa_reshape_and_cache           scatter per-token K/V into a paged cache
+ *   pa_concat_mla_k                assemble MLA K from k_nope and a shared k_rope
+ *   pa_paged_decode_attention      GQA decode attention over the paged cache
+ *   pa_paged_decode_attention_fp8  the same over an FP8 E4M3 cache with scales
+ *   pa_paged_decode_step           new-token cache write + decode attention, one launch
  *
  * Common rules
  *   - Every pointer argument except the `*_host` ones is a DEVICE pointer on
@@ -58,6 +59,7 @@ typedef enum {
 /* Bits of the device-side error word (first 4 bytes of a decode workspace). */
 #define PA_DEVERR_WAIT_TIMEOUT 0x1u   /* a pipeline wait gave up (should never happen) */
 #define PA_DEVERR_CONTEXT_CLIPPED 0x2u /* some context_lens[b] exceeded the planned range */
+#define PA_DEVERR_SLOT_MISMATCH 0x4u   /* decode step: a slot was not position L-1's slot */
 
 /* ------------------------------------------------------------------------
  * pa_reshape_and_cache
@@ -203,6 +205,36 @@ pa_status pa_paged_decode_attention_fp8(void *out, const void *q, const void *k_
                                         int32_t max_blocks_per_seq, int64_t num_blocks,
                                         float scale, int32_t max_context_len, void *workspace,
                                         size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_paged_decode_step -- one decode step in one launch: write each
+ * sequence's newest K/V token into the cache, then attend.
+ *
+ * Same result as pa_reshape_and_cache(new_k, new_v, ..., slot_mapping,
+ * k_scale, v_scale) followed by pa_paged_decode_attention(_fp8) (the
+ * PagedAttention-principle post, decode dataflow: compute the new token's
+ * q/k/v, write the KV cache, then compute attention).  The CTA that holds
+ * position context_lens[b] - 1 converts the new row exactly as the cache
+ * write does, stores it at slot_mapping[b] and uses it directly.
+ *
+ * new_k, new_v: [num_seqs, num_kv_heads, head_size] bf16, contiguous,
+ *   16-byte aligned.  slot_mapping: [num_seqs] int64; -1 (or any slot
+ *   outside the pool) skips that sequence's write.  A slot that is not the
+ *   slot of position context_lens[b] - 1 is still written but not attended
+ *   to in this call, and sets PA_DEVERR_SLOT_MISMATCH (no other CTA may be
+ *   reading it: keep slot_mapping consistent with the block table).
+ * cache_dtype PA_BF16 (k_scale, v_scale NULL) or PA_FP8_E4M3 (scales as in
+ *   pa_paged_decode_attention_fp8).  Other arguments as for
+ *   pa_paged_decode_attention.
+ * ---------------------------------------------------------------------- */
+pa_status pa_paged_decode_step(void *out, const void *q, const void *new_k, const void *new_v,
+                               const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                               pa_dtype cache_dtype, const float *k_scale, const float *v_scale,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_size, int32_t block_size, int32_t max_blocks_per_seq,
+                               int64_t num_blocks, float scale, int32_t max_context_len,
+                               void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * pa_paged_decode_attention_static -- the same decode attention for callers

@@ -77,7 +77,15 @@ struct DecodeParams {
   float scale_log2;
   const float* k_scale;  // quantised cache: code * k_scale is the value (else null)
   const float* v_scale;
+  // fused decode step (else null): each sequence's newest K/V row
+  // [B, H_KV, d] bf16, written at slot_mapping[b] before it is attended to
+  const __nv_bfloat16* new_k;
+  const __nv_bfloat16* new_v;
+  const int64_t* slot_mapping;
+  void* k_cache;
+  void* v_cache;
 };
+
 
 // context length used by both kernels: clipped to the plan and the table
 __device__ __forceinline__ int effective_len(const DecodeParams& p, int b, bool* clipped) {
@@ -217,6 +225,52 @@ __device__ __forceinline__ void merge_splits_warp(const DecodeParams& p, int64_t
   const float inv = W > 0.f ? 1.f / W : 0.f;
   *reinterpret_cast<uint2*>(p.out + bh * kD + lane * 4) =
       make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+}
+
+// Decode step, fused write: the warp that owns row L-1 of the last tile
+// converts the sequence's new K (lanes 0-15) and V (lanes 16-31) row exactly
+// as pa_reshape_and_cache does, stores it at slot_mapping[b], and -- when
+// that slot is position L-1's slot -- also puts it into the tile in shared
+// memory (the TMA copy may predate the store).  Returns whether shared
+// memory was written.
+template <bool kFp8>
+__device__ __forceinline__ bool fused_token_write(const DecodeParams& p, int b, int g, int L,
+                                                  int row, uint8_t* stage_smem, int v_offset,
+                                                  int lane) {
+  using namespace pa;
+  const int64_t slots = p.num_blocks * p.block_size;
+  const int64_t s = __ldg(p.slot_mapping + b);
+  const int32_t pos_blk = __ldg(p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq +
+                                ((L - 1) >> p.log2_bs));
+  const int64_t pos_slot = static_cast<int64_t>(pos_blk) * p.block_size + ((L - 1) & (p.block_size - 1));
+  if (s < 0 || s >= slots) return false;  // skipped, as in the separate write
+  const bool here = s == pos_slot;
+  if (!here && lane == 0) atomicOr(p.err, PA_DEVERR_SLOT_MISMATCH);
+  const bool is_v = lane >= 16;
+  const int e0 = 8 * (lane & 15);
+  const int64_t src = (static_cast<int64_t>(b) * p.num_kv_heads + g) * kD + e0;
+  const Vec8<bf16> x = load8((is_v ? p.new_v : p.new_k) + src);
+  const int64_t dst = (s * p.num_kv_heads + g) * kD + e0;
+  uint8_t* region = stage_smem + (is_v ? v_offset : 0);
+  if constexpr (kFp8) {
+    float f[8];
+    to_f32(x, f);
+    const float* sc = is_v ? p.v_scale : p.k_scale;
+    if (sc != nullptr) {
+      const Divisor d = make_divisor(__ldg(sc));
+      div8_for_e4m3(f, d, fminf(1.7e38f * d.s, 3.0e38f));
+    }
+    const Vec8<e4m3> y = from_f32<e4m3>(f);
+    store8(static_cast<e4m3*>(is_v ? p.v_cache : p.k_cache) + dst, y);
+    if (here)
+      *reinterpret_cast<uint2*>(region + row * 128 + (((e0 >> 4) ^ (row & 7)) << 4) + (e0 & 15)) = y.u;
+  } else {
+    store8(static_cast<bf16*>(is_v ? p.v_cache : p.k_cache) + dst, x);
+    if (here)
+      *reinterpret_cast<uint4*>(region + (e0 >> 6) * kHalfBytes + row * 128 +
+                                ((((e0 & 63) >> 3) ^ (row & 7)) << 4)) = x.u;
+  }
+  return here;
 }
 
 template <int NT>
@@ -431,6 +485,10 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
     const uint32_t stg_base = smem_u32(stg);
     const uint32_t v_row_stg = static_cast<uint32_t>(((lane & 7) + 8 * (lane >> 4)) * 128);
 
+    // fused decode step: row of position L-1 in the last tile, and its warp
+    const bool fused = p.new_k != nullptr && tok_end == L;
+    const int new_row = fused ? (L - 1 - tok_begin) % kTile : -1;
+
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % kStages;
@@ -441,6 +499,12 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
       }
       const uint32_t mask16 = static_cast<uint32_t>(tile_mask[stage] >> r0) & 0xFFFFu;
       const uint32_t st_base = smem_base + stage * Lay::kStageBytes;
+      bool smem_written = false;
+      if (fused && t == ntiles - 1 && (new_row >> 4) == warp) {
+        smem_written = fused_token_write<kFp8>(p, b, g, L, new_row,
+                                               smem + stage * Lay::kStageBytes, Lay::kVOffset, lane);
+        __syncwarp();
+      }
       if (mask16 != 0u) {
         if (!kFp8 && mask16 != 0xFFFFu) {
           // rows without a token: zero their V rows (0 x NaN would poison P.V)
@@ -595,6 +659,7 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
             for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[mt][nt], a, pb[nt][0], pb[nt][1]);
           }
           __syncwarp();  // staging is rewritten by the next tile
+          if (smem_written) fence_proxy_async_smem();  // generic writes before the next TMA
         } else {
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
@@ -607,7 +672,8 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
               mma_bf16_16816(o[mt][nt], a, pl[nt][0], pl[nt][1]);
             }
           }
-          if (mask16 != 0xFFFFu) fence_proxy_async_smem();  // generic writes before the next TMA
+          if (mask16 != 0xFFFFu || smem_written)
+            fence_proxy_async_smem();  // generic writes before the next TMA
         }
       }
       __syncwarp();
@@ -923,6 +989,11 @@ pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
+  p.new_k = static_cast<const __nv_bfloat16*>(a.new_k);
+  p.new_v = static_cast<const __nv_bfloat16*>(a.new_v);
+  p.slot_mapping = a.slot_mapping;
+  p.k_cache = const_cast<void*>(a.k_cache);
+  p.v_cache = const_cast<void*>(a.v_cache);
 
   const dim3 grid(static_cast<unsigned>(a.plan.num_splits), static_cast<unsigned>(a.num_kv_heads),
                   static_cast<unsigned>(a.num_seqs));

@@ -257,6 +257,39 @@ pa_status pa_paged_decode_attention_fp8(void* out, const void* q, const void* k_
   return pa_detail::launch_paged_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+pa_status pa_paged_decode_step(void* out, const void* q, const void* new_k, const void* new_v,
+                               const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                               pa_dtype cache_dtype, const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_size, int32_t block_size, int32_t max_blocks_per_seq,
+                               int64_t num_blocks, float scale, int32_t max_context_len,
+                               void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if ((k_scale == nullptr) != (v_scale == nullptr)) return PA_ERR_INVALID;
+  if (k_scale != nullptr && cache_dtype != PA_FP8_E4M3) return PA_ERR_INVALID;
+  pa_detail::DecodeArgs a{};
+  const pa_status st = check_decode(out, q, k_cache, v_cache, cache_dtype, block_tables,
+                                    context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                    block_size, max_blocks_per_seq, num_blocks, scale,
+                                    max_context_len, &a);
+  if (st != PA_OK) return st;
+  if (num_seqs > 0 && (new_k == nullptr || new_v == nullptr || slot_mapping == nullptr))
+    return PA_ERR_INVALID;
+  if (!aligned(new_k, 16) || !aligned(new_v, 16)) return PA_ERR_ALIGN;
+  const size_t need =
+      pa_detail::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_size, a.plan);
+  if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
+  a.workspace = workspace;
+  a.error_word = nullptr;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.new_k = new_k;
+  a.new_v = new_v;
+  a.slot_mapping = slot_mapping;
+  return pa_detail::launch_paged_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 pa_status pa_paged_decode_attention_static(void* out, const void* q, const void* k_cache,
                                            const void* v_cache, pa_dtype cache_dtype,
                                            const int32_t* block_tables,

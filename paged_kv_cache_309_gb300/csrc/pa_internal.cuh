@@ -376,6 +376,9 @@ struct DecodeArgs {
   pa_dtype cache_dtype;    // PA_BF16 or PA_FP8_E4M3
   const float* k_scale;    // e4m3 cache: device scalars (null = 1)
   const float* v_scale;
+  const void* new_k;       // fused decode step: [B, H_KV, d] bf16 (else null)
+  const void* new_v;
+  const int64_t* slot_mapping;
 };
 pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
 

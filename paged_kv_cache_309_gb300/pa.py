@@ -21,6 +21,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_ALIGN, PA_ERR_WORKSPACE, PA_ER
 PA_BF16, PA_FP16, PA_FP32, PA_FP8_E4M3 = range(4)
 PA_DEVERR_WAIT_TIMEOUT = 0x1
 PA_DEVERR_CONTEXT_CLIPPED = 0x2
+PA_DEVERR_SLOT_MISMATCH = 0x4
 
 _TORCH_DTYPE = {torch.bfloat16: PA_BF16, torch.float16: PA_FP16, torch.float32: PA_FP32,
                 torch.float8_e4m3fn: PA_FP8_E4M3}
@@ -61,6 +62,9 @@ def _load():
     lib.pa_paged_decode_attention_fp8.argtypes = [P, P, P, P, P, P, P, P, I32, I32, I32, I32,
                                                   I32, I32, I64, F32, I32, P, SZ, P]
     lib.pa_paged_decode_attention_fp8.restype = E
+    lib.pa_paged_decode_step.argtypes = [P, P, P, P, P, P, P, E, P, P, P, P, I32, I32, I32, I32,
+                                         I32, I32, I64, F32, I32, P, SZ, P]
+    lib.pa_paged_decode_step.restype = E
     lib.pa_paged_decode_attention_static.argtypes = [P, P, P, P, E, P, P, I32, I32, I32, I32,
                                                      I32, I32, I64, F32, I32, P, P]
     lib.pa_paged_decode_attention_static.restype = E
@@ -249,3 +253,31 @@ def pa_paged_decode_attention_static(out, q, k_cache, v_cache, block_tables, con
         _ptr(context_lens), B, HQ, HKV, d, bs, block_tables.shape[1], nb, float(scale),
         int(max_context_len), _ptr(error_word), _stream(stream))
     _check(st, "pa_paged_decode_attention_static")
+
+
+def pa_paged_decode_step(out, q, new_k, new_v, slot_mapping, k_cache, v_cache, block_tables,
+                         context_lens, scale, max_context_len, workspace, k_scale=None,
+                         v_scale=None, stream=None):
+    """One decode step in one launch: new_k/new_v [B, H_KV, d] bf16 are
+    written at slot_mapping [B] int64 (bf16 cache, or e4m3 cache with
+    k_scale/v_scale), then attention over the cache as in
+    pa_paged_decode_attention."""
+    lib = _load()
+    B, HQ, d = q.shape
+    nb, bs, HKV, dc = k_cache.shape
+    for t, name in ((q, "q"), (out, "out"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                    (new_k, "new_k"), (new_v, "new_v"), (block_tables, "block_tables"),
+                    (context_lens, "context_lens"), (slot_mapping, "slot_mapping")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if new_k.shape != (B, HKV, d) or new_v.shape != (B, HKV, d) or new_k.dtype != torch.bfloat16:
+        raise ValueError("new_k/new_v must be bf16 [B, H_KV, d]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != B:
+        raise ValueError("slot_mapping must be int64 [B]")
+    st = lib.pa_paged_decode_step(
+        _ptr(out), _ptr(q), _ptr(new_k), _ptr(new_v), _ptr(slot_mapping), _ptr(k_cache),
+        _ptr(v_cache), _dtype(k_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+        _ptr(context_lens), B, HQ, HKV, d, bs, block_tables.shape[1], nb, float(scale),
+        int(max_context_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(st, "pa_paged_decode_step")

@@ -140,9 +140,10 @@ def up(a, dtype, dev):
     return t.view(dtype) if dtype is not None else t
 
 
-def traffic_record(kernel_file):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current source of the kernel (else None)."""
+def traffic_record(kernel_file, workload, step, kv_dtype):
+    """Per-launch DRAM bytes from the committed ncu record, if it was taken
+    on the current source of the kernel and the same workload and step
+    (else None)."""
     rec = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(rec):
         return None
@@ -150,7 +151,8 @@ def traffic_record(kernel_file):
         d = json.load(f)
     with open(kernel_file, "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()[:16]
-    if d.get("source_sha256_16") != h:
+    if (d.get("source_sha256_16") != h or d.get("workload") != workload or d.get("step") != step
+            or d.get("kv_dtype") != kv_dtype):
         return None
     return d.get("dram_bytes_per_decode_call")
 
@@ -250,7 +252,8 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     kernel_bytes = step_bytes if fused else attn_bytes  # what the timed launch moves
     achieved = kernel_bytes / (attn_ms_avg * 1e-3) / 1e9
-    traffic = traffic_record(os.path.join(ROOT, "paged_kv_cache_309_gb300", "csrc", "decode.cu"))
+    traffic = traffic_record(os.path.join(ROOT, "paged_kv_cache_309_gb300", "csrc", "decode.cu"),
+                             w.name, args.step, args.kv_dtype)
 
     # ---------------- end to end through the C ABI with pinned host buffers
     hq = torch.from_numpy(w.q.view(np.int16)).pin_memory()

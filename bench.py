@@ -68,6 +68,17 @@ def reduce_over_ranks(value: float, op: str, device=None) -> float:
     return float(t.item())
 
 
+def bf16_peak():
+    """Dense bf16 tensor TFLOP/s (measured burst, else the fallback)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("bf16_tflops"):
+            return float(d["bf16_tflops"])
+    return 1900.0
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -405,6 +416,23 @@ def run_extras(args, dev, peak):
                   "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 2),
                   "frac_of_hbm_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4),
                   "median_us": round(med * 1e3, 2), "algorithmic_bytes": nbytes}
+    # causal prefill: 4 fresh prompts of 8192 tokens, H_Q=32, H_KV=8, bs=16
+    pw = wl.make_prefill("prefill_attention_b4_8k", 5, [8192] * 4, [8192] * 4, 32, 8, 128, 16)
+    pq = up(pw.q, torch.bfloat16, dev)
+    pout = torch.empty_like(pq)
+    pkc, pvc = up(pw.k_cache, torch.bfloat16, dev), up(pw.v_cache, torch.bfloat16, dev)
+    pbt = torch.from_numpy(pw.block_tables).to(dev)
+    pcu = torch.from_numpy(pw.cu_seqlens_q).to(dev)
+    pcl = torch.from_numpy(pw.context_lens).to(dev)
+    perr = torch.zeros(1, dtype=torch.int32, device=dev)
+    med, _ = timed_loop(lambda: pa.pa_paged_prefill_attention(pout, pq, pkc, pvc, pbt, pcu, pcl,
+                                                              pw.scale, pw.max_q_len, perr),
+                        max(3, iters // 5), 2, dev)
+    flops = wl.prefill_flops(pw)
+    ex[pw.name] = {"tokens_per_s": round(int(pw.cu_seqlens_q[-1]) / (med * 1e-3), 1),
+                   "TFLOP_per_s": round(flops / (med * 1e-3) / 1e12, 2),
+                   "frac_of_bf16_dense_peak": round(flops / (med * 1e-3) / 1e12 / bf16_peak(), 4),
+                   "median_us": round(med * 1e3, 2), "causal_flops": flops}
     lat = torch.empty((N, 1, 576), dtype=torch.bfloat16, device=dev)
     ckv, kpe = up(m.c_kv.reshape(N, 1, 512), torch.bfloat16, dev), up(m.k_pe.reshape(N, 1, 64),
                                                                       torch.bfloat16, dev)

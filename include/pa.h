@@ -7,6 +7,7 @@
  *   pa_paged_decode_attention      GQA decode attention over the paged cache
  *   pa_paged_decode_attention_fp8  the same over an FP8 E4M3 cache with scales
  *   pa_paged_decode_step           new-token cache write + decode attention, one launch
+ *   pa_paged_prefill_attention     causal varlen prefill attention over the paged cache
  *
  * Common rules
  *   - Every pointer argument except the `*_host` ones is a DEVICE pointer on
@@ -235,6 +236,39 @@ pa_status pa_paged_decode_step(void *out, const void *q, const void *new_k, cons
                                int32_t head_size, int32_t block_size, int32_t max_blocks_per_seq,
                                int64_t num_blocks, float scale, int32_t max_context_len,
                                void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_paged_prefill_attention -- causal varlen prefill attention over the
+ * paged cache (the nano-vLLM walkthrough names varlen flash attention with
+ * cu_seqlens_q for prefill; section 2.6: attention reads the cache along
+ * block_tables).
+ *
+ * Sequence b has n_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens; they
+ * are the last n_b of its L_b = context_lens[b] tokens, whose K/V are already
+ * in the cache (pa_reshape_and_cache first).  New token j of sequence b is
+ * at position p = L_b - n_b + j and
+ *     out[cu_seqlens_q[b] + j, h] = softmax_{t <= p}(scale q.K_t) @ V_t
+ * with K_t, V_t of kv head h / (H_Q / H_KV) read through the block table.
+ * Positions below zero (n_b > L_b) give zero rows; a block id outside the
+ * pool drops its tokens.
+ *
+ * q, out: [total_new_tokens, num_q_heads, 128] bf16, contiguous;
+ * cu_seqlens_q [num_seqs + 1] int32 (device), context_lens [num_seqs] int32;
+ * caches, block table, block_size, G as for pa_paged_decode_attention
+ * (bf16 caches).  max_q_len: host upper bound on every n_b (sets the grid;
+ * tokens past it are not computed).  error_word: device pointer to one
+ * 4-byte word receiving PA_DEVERR_* bits (the caller clears it).
+ * Numerics: fp32 accumulation and softmax; the softmax weights enter the
+ * P.V product rounded to bf16.
+ * ---------------------------------------------------------------------- */
+pa_status pa_paged_prefill_attention(void *out, const void *q, const void *k_cache,
+                                     const void *v_cache, pa_dtype cache_dtype,
+                                     const int32_t *block_tables, const int32_t *cu_seqlens_q,
+                                     const int32_t *context_lens, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                     int32_t block_size, int32_t max_blocks_per_seq,
+                                     int64_t num_blocks, float scale, int32_t max_q_len,
+                                     unsigned *error_word, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * pa_paged_decode_attention_static -- the same decode attention for callers

@@ -224,3 +224,21 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
         _ptr(_c(v_cache, v_cache.dtype)), cache_dtype, _ptr(bt), _ptr(cl), B, HQ, HKV, d, bs,
         bt.shape[1], nb, float(scale)))
     return out, lse
+
+
+def paged_prefill_row(q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens, b, j, h,
+                      scale, q_dtype=BF16, cache_dtype=BF16):
+    """Causal prefill attention of one new token: sequence b's j-th new token
+    (of n = cu_seqlens_q[b+1] - cu_seqlens_q[b]) sits at position
+    p = context_lens[b] - n + j and attends to the cached tokens 0..p, i.e.
+    decode attention over a context of p + 1 tokens.  q is [total, H_Q, d].
+    Returns (out[d] float64, lse, sum of softmax weights)."""
+    n = int(cu_seqlens_q[b + 1]) - int(cu_seqlens_q[b])
+    p = int(context_lens[b]) - n + j
+    row = int(cu_seqlens_q[b]) + j
+    lens = np.zeros(np.asarray(context_lens).shape, np.int32)
+    lens[b] = max(p + 1, 0)
+    qrow = np.zeros((len(lens),) + tuple(q.shape[1:]), dtype=q.dtype)
+    qrow[b] = q[row]
+    return paged_decode_row(qrow, k_cache, v_cache, block_tables, lens, b, h, scale,
+                            q_dtype=q_dtype, cache_dtype=cache_dtype)

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libpa.so")
-SOURCES = ["pa_api.cu", "cache_write.cu", "mla_concat.cu", "decode.cu"]
+SOURCES = ["pa_api.cu", "cache_write.cu", "mla_concat.cu", "decode.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

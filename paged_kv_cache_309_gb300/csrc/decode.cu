@@ -48,6 +48,8 @@
 namespace pa_detail {
 namespace {
 
+using namespace pa;
+
 constexpr int kD = 128;                 // head size handled by this kernel
 constexpr int kTile = 64;               // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
@@ -127,50 +129,6 @@ struct TcLayout {
   static constexpr int kBytes = kBarOffset + 3 * kStages * 8 + 16;  // full, empty, mask, flags
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KB
 };
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
-         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
-}
-// two e4m3 codes (low byte first) -> f16x2, exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // Merge of one (sequence, query head) by one warp: weights 2^(lse_s - max)
 // over the n splits that hold tokens, out = sum_s w_s o_s / sum_s w_s,
@@ -814,7 +772,25 @@ __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem
   }
 }
 
-// ---------------------------------------------------------------- host --
+template <int NT, bool kFp8>
+pa_status launch_split_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p,
+                          dim3 grid, int G, cudaStream_t stream) {
+  static std::atomic<bool> attr_set{false};
+  auto kern = paged_decode_split_tc_kernel<NT, kFp8>;
+  constexpr int kSmem = TcLayout<kFp8>::kAlloc;
+  if (!attr_set.load()) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    attr_set.store(true);
+  }
+  kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, p, G);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+// ------------------------------------------------------- tensor maps --
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::atomic<void*> fn{nullptr};
   void* f = fn.load();
@@ -862,24 +838,6 @@ bool make_kv_map_fp8(CUtensorMap* map, const void* base, int64_t rows, int32_t n
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-template <int NT, bool kFp8>
-pa_status launch_split_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p,
-                          dim3 grid, int G, cudaStream_t stream) {
-  static std::atomic<bool> attr_set{false};
-  auto kern = paged_decode_split_tc_kernel<NT, kFp8>;
-  constexpr int kSmem = TcLayout<kFp8>::kAlloc;
-  if (!attr_set.load()) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-        cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set.store(true);
-  }
-  kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, p, G);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
-}
-
-}  // namespace
 
 // Scratch of the allocation-free decode entry point.  Every GPU that loads
 // this library holds these 16 MiB for the life of the process.  Host code

@@ -290,6 +290,52 @@ pa_status pa_paged_decode_step(void* out, const void* q, const void* new_k, cons
   return pa_detail::launch_paged_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+pa_status pa_paged_prefill_attention(void* out, const void* q, const void* k_cache,
+                                     const void* v_cache, pa_dtype cache_dtype,
+                                     const int32_t* block_tables, const int32_t* cu_seqlens_q,
+                                     const int32_t* context_lens, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_size,
+                                     int32_t block_size, int32_t max_blocks_per_seq,
+                                     int64_t num_blocks, float scale, int32_t max_q_len,
+                                     unsigned* error_word, pa_stream_t stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
+      block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_q_len < 0)
+    return PA_ERR_INVALID;
+  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
+  if (out == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      block_tables == nullptr || cu_seqlens_q == nullptr || context_lens == nullptr ||
+      error_word == nullptr)
+    return PA_ERR_INVALID;
+  if (num_q_heads % num_kv_heads != 0 || !std::isfinite(scale)) return PA_ERR_INVALID;
+  if (cache_dtype != PA_BF16 || head_size != 128) return PA_ERR_UNSUPPORTED;
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PA_ERR_UNSUPPORTED;
+  if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0)
+    return PA_ERR_UNSUPPORTED;
+  if (num_blocks * block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(error_word, 4))
+    return PA_ERR_ALIGN;
+  pa_detail::PrefillArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.context_lens = context_lens;
+  a.error_word = error_word;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.max_q_len = max_q_len;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  return pa_detail::launch_paged_prefill(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 pa_status pa_paged_decode_attention_static(void* out, const void* q, const void* k_cache,
                                            const void* v_cache, pa_dtype cache_dtype,
                                            const int32_t* block_tables,

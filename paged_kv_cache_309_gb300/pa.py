@@ -65,6 +65,9 @@ def _load():
     lib.pa_paged_decode_step.argtypes = [P, P, P, P, P, P, P, E, P, P, P, P, I32, I32, I32, I32,
                                          I32, I32, I64, F32, I32, P, SZ, P]
     lib.pa_paged_decode_step.restype = E
+    lib.pa_paged_prefill_attention.argtypes = [P, P, P, P, E, P, P, P, I32, I32, I32, I32, I32,
+                                               I32, I64, F32, I32, P, P]
+    lib.pa_paged_prefill_attention.restype = E
     lib.pa_paged_decode_attention_static.argtypes = [P, P, P, P, E, P, P, I32, I32, I32, I32,
                                                      I32, I32, I64, F32, I32, P, P]
     lib.pa_paged_decode_attention_static.restype = E
@@ -281,3 +284,28 @@ def pa_paged_decode_step(out, q, new_k, new_v, slot_mapping, k_cache, v_cache, b
         int(max_context_len), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check(st, "pa_paged_decode_step")
+
+
+def pa_paged_prefill_attention(out, q, k_cache, v_cache, block_tables, cu_seqlens_q,
+                               context_lens, scale, max_q_len, error_word, stream=None):
+    """Causal varlen prefill: q/out [total_new, H_Q, d] bf16, caches
+    [num_blocks, bs, H_KV, d] bf16, cu_seqlens_q [B+1] int32, context_lens [B]
+    int32 (tokens including the new ones), error_word one int32 on the device."""
+    lib = _load()
+    T, HQ, d = q.shape
+    nb, bs, HKV, dc = k_cache.shape
+    B = context_lens.numel()
+    for t, name in ((q, "q"), (out, "out"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                    (block_tables, "block_tables"), (cu_seqlens_q, "cu_seqlens_q"),
+                    (context_lens, "context_lens")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out.shape != q.shape or cu_seqlens_q.numel() != B + 1 or dc != d:
+        raise ValueError("shape mismatch")
+    if cu_seqlens_q.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("cu_seqlens_q and context_lens must be int32")
+    st = lib.pa_paged_prefill_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _dtype(k_cache), _ptr(block_tables),
+        _ptr(cu_seqlens_q), _ptr(context_lens), B, HQ, HKV, d, bs, block_tables.shape[1], nb,
+        float(scale), int(max_q_len), _ptr(error_word), _stream(stream))
+    _check(st, "pa_paged_prefill_attention")

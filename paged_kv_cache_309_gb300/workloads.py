@@ -334,3 +334,60 @@ def long_context_decode(seed=4, block_size=16, num_seqs=8, **kw):
     (num_seqs < 8 keeps the first sequences' draws: a smaller profiling case)."""
     return make_decode(f"long_context_decode_b{num_seqs}_ctx32k-128k_bs{block_size}", seed,
                        num_seqs, 32768, 131072, 32, 8, 128, block_size, **kw)
+
+
+# -------------------------------------------------------------- prefill ---
+@dataclass
+class PrefillWorkload:
+    """Causal varlen prefill over the paged cache: sequence b has L_b =
+    context_lens[b] cached tokens (all K/V already written), of which the
+    last n_b are new; q holds the new tokens' queries back to back."""
+    name: str
+    q: np.ndarray             # [total_new, H_Q, d] bf16 codes
+    k_cache: np.ndarray       # [num_blocks, bs, H_KV, d]
+    v_cache: np.ndarray
+    block_tables: np.ndarray  # [B, max_blocks_per_seq] int32
+    context_lens: np.ndarray  # [B] int32
+    cu_seqlens_q: np.ndarray  # [B + 1] int32
+    scale: float
+
+    @property
+    def num_seqs(self): return self.context_lens.shape[0]
+    @property
+    def num_q_heads(self): return self.q.shape[1]
+    @property
+    def num_kv_heads(self): return self.k_cache.shape[2]
+    @property
+    def block_size(self): return self.k_cache.shape[1]
+    @property
+    def max_q_len(self): return int(np.diff(self.cu_seqlens_q).max()) if self.num_seqs else 0
+
+
+def make_prefill(name, seed, context_lens, new_lens, num_q_heads, num_kv_heads, head_size,
+                 block_size, q_std=1.0) -> PrefillWorkload:
+    """Caches hold random history for all context_lens[b] positions (a
+    decode-step layout of one more token whose extra row stays NaN and is
+    never read); q: N(0, q_std^2) bf16 for the new tokens."""
+    ctx = np.asarray(context_lens, np.int32)
+    new = np.asarray(new_lens, np.int32)
+    d = make_decode(name, seed, len(ctx), 0, 0, num_q_heads, num_kv_heads, head_size, block_size,
+                    context_lens=ctx + 1)
+    g = _gen(seed + 7919)
+    cu = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    q = randn_bf16(g, (int(cu[-1]), num_q_heads, head_size), std=q_std)
+    return PrefillWorkload(name=name, q=q, k_cache=d.k_cache, v_cache=d.v_cache,
+                           block_tables=d.block_tables, context_lens=ctx, cu_seqlens_q=cu,
+                           scale=1.0 / math.sqrt(head_size))
+
+
+def prefill_flops(w: PrefillWorkload) -> int:
+    """Useful FLOPs of causal prefill: new token j of sequence b attends to
+    p + 1 keys (p = L - n + j); QK and PV cost 2 d FLOPs per key each."""
+    d = w.q.shape[2]
+    tot = 0
+    for b in range(w.num_seqs):
+        L, n = int(w.context_lens[b]), int(w.cu_seqlens_q[b + 1] - w.cu_seqlens_q[b])
+        keys = sum(max(L - n + j + 1, 0) for j in range(n)) if n < 4096 else \
+            n * (L - n) + n * (n + 1) // 2
+        tot += keys * w.num_q_heads * 4 * d
+    return tot

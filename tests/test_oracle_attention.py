@@ -305,3 +305,60 @@ def test_fp8_constant_values_closed_form():
     out, _, _ = oracle.paged_decode_row(q, kc, vc, bt, lens, 1, 2, 0.05, q_dtype=oracle.FP32,
                                         cache_dtype=oracle.E4M3, k_scale=0.05, v_scale=0.5)
     assert np.allclose(out, 0.5, atol=1e-15)
+
+
+# --------------------------------------------------- causal prefill rows ---
+def _prefill_case(seed=8, ctx=(40, 90, 17), new=(40, 7, 17), HKV=2, HQ=4, d=16, bs=8):
+    rng = np.random.default_rng(seed)
+    K = [rng.standard_normal((L, HKV, d)).astype(np.float32) for L in ctx]
+    V = [rng.standard_normal((L, HKV, d)).astype(np.float32) for L in ctx]
+    kc, vc, bt = f32_paged(K, V, bs, HKV, perm_seed=seed)
+    cu = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    q = rng.standard_normal((int(cu[-1]), HQ, d)).astype(np.float32)
+    return q, kc, vc, bt, cu, np.array(ctx, np.int32), K, V
+
+
+def test_prefill_last_row_is_decode():
+    """The last new token sits at position L-1: its row equals decode
+    attention over the whole context."""
+    q, kc, vc, bt, cu, lens, _, _ = _prefill_case()
+    for b in range(len(lens)):
+        j = int(cu[b + 1] - cu[b]) - 1
+        qd = np.zeros((len(lens), q.shape[1], q.shape[2]), np.float32)
+        qd[b] = q[cu[b] + j]
+        for h in range(q.shape[1]):
+            a = oracle.paged_prefill_row(q, kc, vc, bt, cu, lens, b, j, h, 0.3, q_dtype=oracle.FP32,
+                                         cache_dtype=oracle.FP32)
+            r = run_paged(qd, kc, vc, bt, lens, 0.3, b, h)
+            assert (a[0] == r[0]).all()
+
+
+def test_prefill_first_token_of_fresh_sequence_sees_only_itself():
+    """A fresh prefill (n = L): token 0 attends to key 0 alone -> v_0."""
+    q, kc, vc, bt, cu, lens, K, V = _prefill_case()
+    b = 0  # n == L == 40
+    for h in range(q.shape[1]):
+        out, _, ps = oracle.paged_prefill_row(q, kc, vc, bt, cu, lens, b, 0, h, 0.3,
+                                              q_dtype=oracle.FP32, cache_dtype=oracle.FP32)
+        assert (out == V[b][0, h // 2]).all() and ps == 1.0
+
+
+def test_prefill_is_causal():
+    """Changing K/V after position p leaves row p unchanged; changing a key
+    at or before p changes it."""
+    q, kc, vc, bt, cu, lens, K, V = _prefill_case()
+    b, j = 1, 3                       # n = 7, L = 90 -> p = 86
+    p = int(lens[b]) - 7 + j
+    base = oracle.paged_prefill_row(q, kc, vc, bt, cu, lens, b, j, 1, 0.3, q_dtype=oracle.FP32,
+                                    cache_dtype=oracle.FP32)[0]
+    kc2, vc2 = kc.copy(), vc.copy()
+    for t in range(p + 1, int(lens[b])):
+        kc2[bt[b, t // 8], t % 8] = 5.0
+        vc2[bt[b, t // 8], t % 8] = -7.0
+    after = oracle.paged_prefill_row(q, kc2, vc2, bt, cu, lens, b, j, 1, 0.3,
+                                     q_dtype=oracle.FP32, cache_dtype=oracle.FP32)[0]
+    assert (after == base).all()
+    vc2[bt[b, p // 8], p % 8] = -7.0
+    changed = oracle.paged_prefill_row(q, kc2, vc2, bt, cu, lens, b, j, 1, 0.3,
+                                       q_dtype=oracle.FP32, cache_dtype=oracle.FP32)[0]
+    assert not np.allclose(changed, base)

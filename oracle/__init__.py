@@ -27,7 +27,9 @@ _lib = None
 
 # dtype codes of the oracle's own enumeration
 BF16, FP16, FP32, E4M3 = 0, 1, 2, 3
-_NP_CODE_TYPE = {BF16: np.uint16, FP16: np.uint16, FP32: np.float32, E4M3: np.uint8}
+FP64 = 4  # read-only input format (plain float64 arrays) of the MLA functions
+_NP_CODE_TYPE = {BF16: np.uint16, FP16: np.uint16, FP32: np.float32, E4M3: np.uint8,
+                 FP64: np.float64}
 DTYPE_NAMES = {"bf16": BF16, "fp16": FP16, "fp32": FP32, "e4m3": E4M3}
 
 ERRORS = {-1: "invalid argument", -2: "duplicate target slot", -3: "out of memory"}
@@ -82,6 +84,13 @@ def _load():
     lib.or_paged_decode.argtypes = [P, P, P, C_INT, P, P, C_INT, P, P, I32, I32, I32, I32, I32,
                                     I32, I64, F32]
     lib.or_paged_decode.restype = C_INT
+    lib.or_mla_absorb_q.argtypes = [P, P, P, C_INT, P, C_INT, I32, I32, I32, I32, I32]
+    lib.or_mla_absorb_q.restype = C_INT
+    lib.or_mla_decode_row.argtypes = [P, P, P, P, C_INT, P, C_INT, P, P, I32, I32, I32, I32,
+                                      I32, I32, I32, I64, F32]
+    lib.or_mla_decode_row.restype = C_INT
+    lib.or_mla_project_out.argtypes = [P, P, C_INT, P, C_INT, I32, I32, I32, I32]
+    lib.or_mla_project_out.restype = C_INT
     _lib = lib
     return lib
 
@@ -242,3 +251,50 @@ def paged_prefill_row(q, k_cache, v_cache, block_tables, cu_seqlens_q, context_l
     qrow[b] = q[row]
     return paged_decode_row(qrow, k_cache, v_cache, block_tables, lens, b, h, scale,
                             q_dtype=q_dtype, cache_dtype=cache_dtype)
+
+
+# ------------------------------------------------------------- MLA decode --
+def mla_absorb_q(q_nope, q_pe, w_uk, in_dtype=BF16, w_dtype=BF16):
+    """q_lat [B, H, d_c + d_r] float64: [W_UK_h q_nope[b, h] | q_pe[b, h]],
+    with W_UK [d_c, H * d_h] and W_UK_h its columns h*d_h .. (h+1)*d_h - 1."""
+    B, H, dh = q_nope.shape
+    dr = q_pe.shape[2]
+    dc = w_uk.shape[0]
+    assert w_uk.shape[1] == H * dh and q_pe.shape[:2] == (B, H)
+    out = np.empty((B, H, dc + dr), dtype=np.float64)
+    _check(_load().or_mla_absorb_q(_ptr(out), _ptr(_c(q_nope, q_nope.dtype)),
+                                   _ptr(_c(q_pe, q_pe.dtype)), in_dtype,
+                                   _ptr(_c(w_uk, w_uk.dtype)), w_dtype, B, H, dh, dr, dc))
+    return out
+
+
+def mla_decode_row(q_lat, latent_cache, block_tables, context_lens, b, h, scale, d_c,
+                   q_dtype=BF16, cache_dtype=BF16):
+    """One (sequence, head) row of MLA decode over the paged latent cache.
+    q_lat [B, H, d_c + d_r]; latent_cache [num_blocks, bs, (1,) d_c + d_r].
+    Returns (o_lat[d_c] float64, lse, abs_out[d_c]) where abs_out[i] =
+    sum_j p_j |row_j[i]|."""
+    B, H, dk = q_lat.shape
+    nb, bs = latent_cache.shape[0], latent_cache.shape[1]
+    assert latent_cache.shape[-1] == dk and latent_cache.size == nb * bs * dk
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    out = np.empty(d_c, dtype=np.float64)
+    ab = np.empty(d_c, dtype=np.float64)
+    lse = ctypes.c_double()
+    _check(_load().or_mla_decode_row(
+        _ptr(out), ctypes.byref(lse), _ptr(ab), _ptr(_c(q_lat, q_lat.dtype)), q_dtype,
+        _ptr(_c(latent_cache, latent_cache.dtype)), cache_dtype, _ptr(bt), _ptr(cl), b, h, H,
+        d_c, dk - d_c, bs, bt.shape[1], nb, float(scale)))
+    return out, lse.value, ab
+
+
+def mla_project_out(o_lat, w_uv, in_dtype=BF16, w_dtype=BF16):
+    """out [B, H, d_v] float64 = o_lat[b, h, :] W_UV_h with W_UV [d_c, H * d_v]."""
+    B, H, dc = o_lat.shape
+    assert w_uv.shape[0] == dc and w_uv.shape[1] % H == 0
+    dv = w_uv.shape[1] // H
+    out = np.empty((B, H, dv), dtype=np.float64)
+    _check(_load().or_mla_project_out(_ptr(out), _ptr(_c(o_lat, o_lat.dtype)), in_dtype,
+                                      _ptr(_c(w_uv, w_uv.dtype)), w_dtype, B, H, dc, dv))
+    return out

@@ -21,7 +21,11 @@
  *     context gathered, in logical order, through the block table
  *     (PagedAttention-principle post, section "paged attention原理": blocks
  *     may be scattered, a table keeps their order; walkthrough section 2.6:
- *     decode reads the cache back along block_tables).  Arithmetic in double.
+ *     decode reads the cache back along block_tables).  Arithmetic in double;
+ *   - MLA decode keeps one latent row per token (PagedAttention-principle
+ *     post, MLA section: c_kv = x W_DKV is what is cached; K and V of a head
+ *     are c_kv W_UK and c_kv W_UV; the rope part of K rides beside it) and is
+ *     written here in the absorbed form, head by head, with plain loops.
  *
  * Error returns are negative integers (see the OR_E* codes); nothing here
  * aborts.
@@ -36,6 +40,7 @@
 #define OR_FP16 1
 #define OR_FP32 2
 #define OR_E4M3 3
+#define OR_FP64 4 /* read-only: inputs already in double (MLA functions) */
 
 #define OR_OK 0
 #define OR_EINVAL (-1)      /* bad argument                                  */
@@ -160,6 +165,7 @@ static int dtype_size(int dtype) {
 
 /* element i of an array of `dtype` as a double */
 static double load_elem(int dtype, const void *base, int64_t i) {
+  if (dtype == OR_FP64) return ((const double *)base)[i];
   if (dtype == OR_FP32) return (double)((const float *)base)[i];
   if (dtype == OR_E4M3) return fmt_decode(&F_E4M3, ((const uint8_t *)base)[i]);
   return fmt_decode(fmt_of(dtype), ((const uint16_t *)base)[i]);
@@ -473,5 +479,148 @@ int or_paged_decode(float *out, double *lse, const void *q, int q_dtype, const v
     }
   }
   free(row);
+  return OR_OK;
+}
+
+/* ======================================================================== */
+/* MLA decode over the latent cache                                          */
+/* PagedAttention-principle post, MLA section ("MLA 不直接缓存 k 和 v"): per  */
+/* token only c_kv ([d_c]) is cached; k_raw = c_kv W_UK and v_raw = c_kv     */
+/* W_UV with W_UK, W_UV: [d_c, H * d_h], reshaped to [H, d_h]; the rope part  */
+/* of K is added separately (same post, closing remark of the section).       */
+/* ======================================================================== */
+/* Cache row of a token: [c_kv (d_c) | k_pe (d_r)], one row per slot, the    */
+/* layout [num_blocks, block_size, 1, d_c + d_r].                             */
+/*                                                                            */
+/* Absorbed form (a reading: associativity of the two products, not printed  */
+/* on the pages).  For head h with W_UK_h = W_UK[:, h d_h : (h+1) d_h]:       */
+/*   q_nope_h . (c W_UK_h) = (W_UK_h q_nope_h) . c                            */
+/*   sum_j p_j (c_j W_UV_h) = (sum_j p_j c_j) W_UV_h                          */
+/* so decode is one MQA over the latent rows:                                 */
+/*   q_lat[h] = [W_UK_h q_nope_h | q_pe_h]              (d_c + d_r)           */
+/*   o_lat[h] = sum_j softmax_j(scale q_lat[h] . row_j) row_j[0:d_c]          */
+/*   out[h]   = o_lat[h] W_UV_h                          (d_v)                */
+
+/* q_lat [B, H, d_c + d_r] in double from q_nope [B, H, d_h], q_pe [B, H, d_r]
+ * and W_UK [d_c, H * d_h] (row-major), all of in_dtype / w_dtype. */
+int or_mla_absorb_q(double *q_lat, const void *q_nope, const void *q_pe, int in_dtype,
+                    const void *w_uk, int w_dtype, int32_t num_seqs, int32_t num_heads,
+                    int32_t d_h, int32_t d_r, int32_t d_c) {
+  if (!formats_ready()) return OR_ENOMEM;
+  if (!q_lat || !q_nope || !w_uk || (d_r > 0 && !q_pe)) return OR_EINVAL;
+  if (num_seqs < 0 || num_heads <= 0 || d_h <= 0 || d_r < 0 || d_c <= 0) return OR_EINVAL;
+  const int64_t row = (int64_t)d_c + d_r;
+  const int64_t wcols = (int64_t)num_heads * d_h;
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    for (int32_t h = 0; h < num_heads; ++h) {
+      double *dst = q_lat + ((int64_t)b * num_heads + h) * row;
+      const int64_t qn = ((int64_t)b * num_heads + h) * d_h;
+      for (int32_t c = 0; c < d_c; ++c) {
+        double acc = 0.0;
+        for (int32_t i = 0; i < d_h; ++i)
+          acc += load_elem(w_dtype, w_uk, (int64_t)c * wcols + (int64_t)h * d_h + i) *
+                 load_elem(in_dtype, q_nope, qn + i);
+        dst[c] = acc;
+      }
+      for (int32_t r = 0; r < d_r; ++r)
+        dst[d_c + r] = load_elem(in_dtype, q_pe, ((int64_t)b * num_heads + h) * d_r + r);
+    }
+  }
+  return OR_OK;
+}
+
+/* One output row (sequence b, head h) of MLA decode over the paged latent
+ * cache: scores over all d_c + d_r elements of each row, values = the first
+ * d_c.  q_lat [B, H, d_c + d_r] of q_dtype; latent_cache [num_blocks,
+ * block_size, d_c + d_r] of cache_dtype.  Tokens are gathered in logical
+ * order along the block table; a token whose block id is outside
+ * [0, num_blocks) is left out, as in or_paged_decode_row.
+ * out [d_c]; lse = log sum exp of the scaled scores (nullable); abs_out
+ * [d_c] (nullable) = sum_j p_j |row_j[i]|, the scale of the error a rounding
+ * of the weights p_j can cause in out[i]. */
+int or_mla_decode_row(double *out, double *lse, double *abs_out, const void *q_lat, int q_dtype,
+                      const void *latent_cache, int cache_dtype, const int32_t *block_tables,
+                      const int32_t *context_lens, int32_t b, int32_t h, int32_t num_heads,
+                      int32_t d_c, int32_t d_r, int32_t block_size, int32_t max_blocks_per_seq,
+                      int64_t num_blocks, float scale) {
+  if (!formats_ready()) return OR_ENOMEM;
+  if (!out || !q_lat || !latent_cache || !block_tables || !context_lens) return OR_EINVAL;
+  if (num_heads <= 0 || d_c <= 0 || d_r < 0 || block_size <= 0 || max_blocks_per_seq < 0)
+    return OR_EINVAL;
+  if (b < 0 || h < 0 || h >= num_heads) return OR_EINVAL;
+  const int64_t L = context_lens[b];
+  if (L < 0 || L > (int64_t)max_blocks_per_seq * block_size) return OR_EINVAL;
+  const int32_t dk = d_c + d_r;
+
+  double *qd = (double *)malloc(sizeof(double) * (size_t)dk);
+  double *R = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)dk);
+  double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+  if (!qd || !R || !s) { free(qd); free(R); free(s); return OR_ENOMEM; }
+  for (int32_t i = 0; i < dk; ++i)
+    qd[i] = load_elem(q_dtype, q_lat, ((int64_t)b * num_heads + h) * dk + i);
+
+  /* gather the context's latent rows in logical order */
+  int64_t n = 0;
+  for (int64_t j = 0; j < L; ++j) {
+    int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
+    if (blk < 0 || blk >= num_blocks) continue;
+    int64_t base = (blk * block_size + j % block_size) * dk;
+    for (int32_t i = 0; i < dk; ++i) R[n * dk + i] = load_elem(cache_dtype, latent_cache, base + i);
+    ++n;
+  }
+
+  for (int32_t i = 0; i < d_c; ++i) {
+    out[i] = 0.0;
+    if (abs_out) abs_out[i] = 0.0;
+  }
+  if (n == 0) {
+    if (lse) *lse = -INFINITY;
+    free(qd); free(R); free(s);
+    return OR_OK;
+  }
+  /* scores over the whole row, then the softmax, then the weighted sum of
+   * the first d_c elements */
+  double smax = -INFINITY;
+  for (int64_t j = 0; j < n; ++j) {
+    double dot = 0.0;
+    for (int32_t i = 0; i < dk; ++i) dot += qd[i] * R[j * dk + i];
+    s[j] = (double)scale * dot;
+    if (s[j] > smax) smax = s[j];
+  }
+  double l = 0.0;
+  for (int64_t j = 0; j < n; ++j) l += exp(s[j] - smax);
+  for (int64_t j = 0; j < n; ++j) {
+    double p = exp(s[j] - smax) / l;
+    for (int32_t i = 0; i < d_c; ++i) {
+      out[i] += p * R[j * dk + i];
+      if (abs_out) abs_out[i] += p * fabs(R[j * dk + i]);
+    }
+  }
+  if (lse) *lse = smax + log(l);
+  free(qd); free(R); free(s);
+  return OR_OK;
+}
+
+/* out [B, H, d_v] in double = o_lat[b, h, :] W_UV_h, with o_lat [B, H, d_c]
+ * of in_dtype and W_UV [d_c, H * d_v] (row-major) of w_dtype. */
+int or_mla_project_out(double *out, const void *o_lat, int in_dtype, const void *w_uv,
+                       int w_dtype, int32_t num_seqs, int32_t num_heads, int32_t d_c,
+                       int32_t d_v) {
+  if (!formats_ready()) return OR_ENOMEM;
+  if (!out || !o_lat || !w_uv) return OR_EINVAL;
+  if (num_seqs < 0 || num_heads <= 0 || d_c <= 0 || d_v <= 0) return OR_EINVAL;
+  const int64_t wcols = (int64_t)num_heads * d_v;
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    for (int32_t h = 0; h < num_heads; ++h) {
+      const int64_t src = ((int64_t)b * num_heads + h) * d_c;
+      for (int32_t i = 0; i < d_v; ++i) {
+        double acc = 0.0;
+        for (int32_t c = 0; c < d_c; ++c)
+          acc += load_elem(in_dtype, o_lat, src + c) *
+                 load_elem(w_dtype, w_uv, (int64_t)c * wcols + (int64_t)h * d_v + i);
+        out[((int64_t)b * num_heads + h) * d_v + i] = acc;
+      }
+    }
+  }
   return OR_OK;
 }

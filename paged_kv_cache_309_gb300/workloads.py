@@ -391,3 +391,116 @@ def prefill_flops(w: PrefillWorkload) -> int:
             n * (L - n) + n * (n + 1) // 2
         tot += keys * w.num_q_heads * 4 * d
     return tot
+
+
+# ----------------------------------------------------------- MLA decode ---
+@dataclass
+class MLADecodeWorkload:
+    """One MLA decode step over a paged latent cache.
+
+    latent_cache [num_blocks, bs, 1, d_c + d_r]: per token [c_kv | k_pe].
+    q_lat [B, H, d_c + d_r]: the absorbed query, drawn directly (attention
+    tests); q_nope [B, H, d_h], q_pe [B, H, d_r], w_uk [d_c, H * d_h] and
+    w_uv [d_c, H * d_v] are the inputs of the absorbed chain."""
+    name: str
+    q_lat: np.ndarray
+    latent_cache: np.ndarray
+    block_tables: np.ndarray
+    context_lens: np.ndarray
+    q_nope: np.ndarray
+    q_pe: np.ndarray
+    w_uk: np.ndarray
+    w_uv: np.ndarray
+    latent_dim: int
+    scale: float
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self): return self.q_lat.shape[0]
+    @property
+    def num_heads(self): return self.q_lat.shape[1]
+    @property
+    def row_dim(self): return self.q_lat.shape[2]
+    @property
+    def rope_dim(self): return self.row_dim - self.latent_dim
+    @property
+    def num_blocks(self): return self.latent_cache.shape[0]
+    @property
+    def block_size(self): return self.latent_cache.shape[1]
+    @property
+    def max_blocks_per_seq(self): return self.block_tables.shape[1]
+    @property
+    def max_context_len(self): return int(self.context_lens.max()) if self.context_lens.size else 0
+
+
+def make_mla_decode(name, seed, num_seqs, ctx_lo, ctx_hi, num_heads, block_size=64,
+                    latent_dim=512, rope_dim=64, nope_dim=128, v_head_dim=128, q_std=1.0,
+                    context_lens=None, pool_factor=1.1, with_weights=True) -> MLADecodeWorkload:
+    """Seeded MLA decode step.  Latent rows and queries are N(0, 1) bf16
+    (latent rows as in the latent-cache write workload); W_UK ~ N(0, 1/d_h)
+    and W_UV ~ N(0, 1/d_c), so the absorbed query and the output stay O(1).
+    Blocks come from one random permutation of a pool sized to the
+    context +10%; rows past each context and unused blocks are bf16 NaN.
+    Softmax scale 1/sqrt(d_h + d_r), the unabsorbed head's width."""
+    g = _gen(seed)
+    B, H, bs = num_seqs, num_heads, block_size
+    dk = latent_dim + rope_dim
+    if context_lens is None:
+        context_lens = torch.randint(ctx_lo, ctx_hi + 1, (B,), generator=g).numpy()
+    context_lens = np.asarray(context_lens, dtype=np.int32)
+    nblk = [blocks_needed(L, bs) for L in context_lens]
+    need = int(sum(nblk))
+    pool = max(1, math.ceil(pool_factor * need))
+    mbps = max(1, max(nblk) if nblk else 1)
+    perm = randperm(g, pool)
+    block_tables = np.full((B, mbps), -1, dtype=np.int32)
+    used = np.zeros(pool, dtype=bool)
+    cur = 0
+    for b in range(B):
+        block_tables[b, :nblk[b]] = perm[cur:cur + nblk[b]]
+        used[perm[cur:cur + nblk[b]]] = True
+        cur += nblk[b]
+    q_lat = randn_bf16(g, (B, H, dk), std=q_std)
+    cache = np.full((pool, bs, 1, dk), BF16_NAN, dtype=np.uint16)
+    used_ids = np.nonzero(used)[0]
+    cache[used_ids] = randn_bf16(g, (used_ids.size, bs, 1, dk))
+    for b in range(B):
+        L = int(context_lens[b])
+        if L > 0 and L % bs:
+            cache[int(block_tables[b, nblk[b] - 1]), L % bs:] = BF16_NAN
+    if with_weights:
+        q_nope = randn_bf16(g, (B, H, nope_dim))
+        q_pe = randn_bf16(g, (B, H, rope_dim))
+        w_uk = randn_bf16(g, (latent_dim, H * nope_dim), std=1.0 / math.sqrt(nope_dim))
+        w_uv = randn_bf16(g, (latent_dim, H * v_head_dim), std=1.0 / math.sqrt(latent_dim))
+    else:
+        q_nope = q_pe = w_uk = w_uv = None
+    return MLADecodeWorkload(name=name, q_lat=q_lat, latent_cache=cache,
+                             block_tables=block_tables, context_lens=context_lens,
+                             q_nope=q_nope, q_pe=q_pe, w_uk=w_uk, w_uv=w_uv,
+                             latent_dim=latent_dim,
+                             scale=1.0 / math.sqrt(nope_dim + rope_dim),
+                             meta=dict(seed=seed, ctx_lo=ctx_lo, ctx_hi=ctx_hi, pool_blocks=pool))
+
+
+def mla_decode(seed=5, num_heads=128, **kw):
+    """DeepSeek-V3-shaped MLA decode step: B=64, context in [512, 4096] (the
+    decode batch's length mix), H=128 heads (all heads on one GPU), latent
+    512 + rope 64 per token, bs=64 (the latent-cache write's block size)."""
+    return make_mla_decode(f"mla_decode_b64_ctx512-4096_h{num_heads}", seed, 64, 512, 4096,
+                           num_heads, **kw)
+
+
+def mla_bytes_read(w: MLADecodeWorkload, elt: int = 2) -> int:
+    """Algorithmic bytes of one MLA decode attention: every context token's
+    latent row once, plus q_lat in and o_lat out (bf16)."""
+    tokens = int(w.context_lens.astype(np.int64).sum())
+    B, H, dk = w.q_lat.shape
+    return tokens * dk * elt + B * H * (dk + w.latent_dim) * 2
+
+
+def mla_flops(w: MLADecodeWorkload) -> int:
+    """2 * (d_c + d_r) + 2 * d_c flops per (token, head): the score and the
+    weighted sum."""
+    tokens = int(w.context_lens.astype(np.int64).sum())
+    return tokens * w.num_heads * 2 * (w.row_dim + w.latent_dim)

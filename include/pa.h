@@ -8,6 +8,9 @@
  *   pa_paged_decode_attention_fp8  the same over an FP8 E4M3 cache with scales
  *   pa_paged_decode_step           new-token cache write + decode attention, one launch
  *   pa_paged_prefill_attention     causal varlen prefill attention over the paged cache
+ *   pa_mla_absorb_q                MLA: absorbed query [W_UK_h q_nope | q_pe]
+ *   pa_mla_decode_attention        MLA: decode attention over the paged latent cache
+ *   pa_mla_project_out             MLA: latent output times W_UV_h
  *
  * Common rules
  *   - Every pointer argument except the `*_host` ones is a DEVICE pointer on
@@ -315,6 +318,72 @@ pa_status pa_paged_decode_attention_static(void *out, const void *q, const void 
 pa_status pa_paged_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
                                int32_t num_sms, int32_t *num_splits_host,
                                int32_t *tokens_per_split_host);
+
+/* ========================================================================
+ * MLA decode over the latent cache
+ *
+ * PagedAttention-principle post, MLA section ("MLA 不直接缓存 k 和 v"): a
+ * token's cache entry is its latent c_kv = x W_DKV ([d_c]); head h's K and
+ * V are c_kv W_UK_h and c_kv W_UV_h, with W_UK, W_UV: [d_c, H * d_h] and
+ * head h owning columns h*d_h .. (h+1)*d_h - 1; the rope part of K (k_pe,
+ * [d_r], shared by the heads) is added separately.  The cache row of a
+ * token is [c_kv | k_pe] (d_c + d_r elements), the layout
+ * [num_blocks, block_size, 1, d_c + d_r] that pa_reshape_and_cache writes
+ * with num_heads = 1, head_size = d_c + d_r and no value cache.
+ *
+ * Decode runs in the absorbed form (associativity of the products):
+ *   q_lat[b,h] = [W_UK_h q_nope[b,h] | q_pe[b,h]]            pa_mla_absorb_q
+ *   o_lat[b,h] = sum_j softmax_j(scale q_lat[b,h] . row_j) row_j[0:d_c]
+ *                                                   pa_mla_decode_attention
+ *   out[b,h]   = o_lat[b,h] W_UV_h                          pa_mla_project_out
+ * which equals attention with the explicitly reconstructed K and V.
+ * ====================================================================== */
+
+/* q_latent [num_seqs, num_heads, latent_dim + rope_dim] bf16 (written) from
+ * q_nope [num_seqs, num_heads, nope_dim], q_pe [num_seqs, num_heads,
+ * rope_dim] and w_uk [latent_dim, num_heads * nope_dim], all bf16 and
+ * contiguous.  nope_dim and latent_dim must be multiples of 64, rope_dim of
+ * 8; pointers 16-byte aligned.  fp32 accumulation, one bf16 rounding. */
+pa_status pa_mla_absorb_q(void *q_latent, const void *q_nope, const void *q_pe, const void *w_uk,
+                          int32_t num_seqs, int32_t num_heads, int32_t nope_dim, int32_t rope_dim,
+                          int32_t latent_dim, pa_stream_t stream);
+
+/* Bytes of workspace pa_mla_decode_attention needs for these sizes on the
+ * current device (0 for invalid sizes).  The first 4 bytes are the device
+ * error word (PA_DEVERR_* bits; the caller clears it); the rest must be zero
+ * before the first call and is left zero by every completed call. */
+size_t pa_mla_decode_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                    int32_t max_context_len);
+
+/* out_latent [num_seqs, num_heads, latent_dim] bf16 = the attention of each
+ * q_latent row [num_seqs, num_heads, latent_dim + rope_dim] (bf16) over the
+ * first context_lens[b] tokens of latent_cache [num_blocks, block_size,
+ * latent_dim + rope_dim] (bf16), read through block_tables [num_seqs,
+ * max_blocks_per_seq] (int32, logical block i of sequence b is physical
+ * block block_tables[b][i]); scores over all latent_dim + rope_dim
+ * elements, values = the first latent_dim.  Supported: latent_dim 512,
+ * rope_dim 64, num_heads a multiple of 16, block_size a power of two in
+ * [8, 256].  max_context_len: host upper bound on context_lens (sets the
+ * split plan; longer contexts are clipped and flagged in the error word).
+ * A block id outside [0, num_blocks) drops its tokens; an empty context
+ * gives a zero row.  Numerics: fp32 scores, softmax and accumulation; the
+ * softmax weights enter the weighted sum rounded to bf16.  Pointers
+ * 16-byte aligned (workspace 256). */
+pa_status pa_mla_decode_attention(void *out_latent, const void *q_latent,
+                                  const void *latent_cache, const int32_t *block_tables,
+                                  const int32_t *context_lens, int32_t num_seqs,
+                                  int32_t num_heads, int32_t latent_dim, int32_t rope_dim,
+                                  int32_t block_size, int32_t max_blocks_per_seq,
+                                  int64_t num_blocks, float scale, int32_t max_context_len,
+                                  void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* out [num_seqs, num_heads, v_head_dim] bf16 = out_latent[b, h, :] (bf16,
+ * [num_seqs, num_heads, latent_dim]) times W_UV_h, w_uv [latent_dim,
+ * num_heads * v_head_dim] bf16.  latent_dim and v_head_dim multiples of 64;
+ * pointers 16-byte aligned.  fp32 accumulation, one bf16 rounding. */
+pa_status pa_mla_project_out(void *out, const void *out_latent, const void *w_uv,
+                             int32_t num_seqs, int32_t num_heads, int32_t latent_dim,
+                             int32_t v_head_dim, pa_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char *pa_status_string(pa_status status);

@@ -1,0 +1,608 @@
+// mla_decode.cu -- MLA decode attention over the paged latent cache.
+//
+// What is computed (PagedAttention-principle post, MLA section: a token's
+// cache entry is its latent c_kv, K and V of head h are c_kv W_UK_h and
+// c_kv W_UV_h, the rope part of K is carried beside the latent): with the
+// two up-projections absorbed into the query and the output (done by
+// mla_proj.cu), decode is one multi-query attention over the latent rows.
+// For sequence b and head h:
+//   s_j   = scale * q_lat[b, h, :] . row_j           (576 = 512 latent + 64 rope)
+//   o_lat = sum_j softmax(s)_j * row_j[0:512]
+// over the first context_lens[b] logical tokens, read through the block
+// table (nano-vLLM walkthrough, section 2.6).  All heads read the same rows.
+//
+// How (sm_103a):
+//  * grid = (head tile, split, sequence); a head tile is 64 heads (16 when
+//    the head count is not a multiple of 64).  Head tiles of one (split,
+//    sequence) are adjacent in the launch order, so the second reads the
+//    latent rows from L2.
+//  * the split's tokens stream in tiles (32 tokens for 64 heads, 64 for 16)
+//    through a TMA ring: per (block piece, 64-element chunk) one [rows x
+//    128 B] box, 128-byte swizzled, completion on an mbarrier; a per-tile
+//    mask marks the rows that exist.  There is no producer warp: every tile
+//    ends in a CTA barrier, after which the previous tile's stage is free,
+//    so warp 0 refills it there (q_lat and the first stages at the start).
+//    Eight warps of 256 threads leave each thread up to 255 registers.
+//  * eight warps per tile: (1) S = Q . K^T on the tensor cores
+//    (mma.sync m16n8k16, bf16 in, fp32 accumulate; heads on M, each warp a
+//    16-head x 16-token (or 16 x 8) block over all 576 elements) written to
+//    a double-buffered fp32 score tile in shared memory; (2) one barrier;
+//    (3) each warp takes 16 heads x (512 / warps per head block) output
+//    elements: reads its heads' scores straight into the A-fragment
+//    positions, runs an fp32 online softmax in base 2 with a lazy rescale
+//    (the running max moves only when a score beats it by more than 2^8),
+//    rounds the weights to bf16 and accumulates O += P . V from the same
+//    shared-memory tile (V = the first 512 elements of each row).
+//  * epilogue as in the GQA decode kernel: one split writes bf16 o_lat;
+//    several write fp32 partials + log2-sum-exp and the CTA that completes
+//    the per-(sequence, head tile) count merges them and zeroes the count.
+//
+// Every wait is bounded (2 s).  A timeout sets an error bit in the
+// workspace's error word, drains the copies in flight and leaves.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+
+#include "pa_internal.cuh"
+
+namespace pa_detail {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // decode.cu
+
+namespace {
+
+using namespace pa;
+
+constexpr int kLat = 512;                 // latent elements (the value part)
+constexpr int kRope = 64;                 // rope elements
+constexpr int kRow = kLat + kRope;        // 576 elements per cache row
+constexpr int kRowBytes = kRow * 2;       // 1152 bytes
+constexpr int kChunks = kRow / 64;        // nine 64-element (128-byte) chunks
+constexpr int kWarps = 8;                 // all warps compute; warp 0 also issues the loads
+constexpr int kThreads = kWarps * 32;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr size_t kWorkspaceHeader = 256;
+
+template <int HT>
+struct MlaCfg {
+  static constexpr int kMB = HT / 16;                   // 16-head blocks
+  static constexpr int kTile = HT == 64 ? 32 : 64;      // tokens per stage
+  static constexpr int kStages = HT == 64 ? 3 : 2;
+  static constexpr int kWarpsPerMB = kWarps / kMB;      // 2 or 8
+  static constexpr int kSTok = kTile / kWarpsPerMB;     // tokens per warp in S: 16 or 8
+  static constexpr int kDW = kLat / kWarpsPerMB;        // output elements per warp: 256 or 64
+  static constexpr int kQBytes = kChunks * HT * 128;
+  static constexpr int kChunkBytes = kTile * 128;
+  static constexpr int kStageBytes = kChunks * kChunkBytes;
+  static constexpr int kSStride = kTile + 8;            // floats per score row
+  static constexpr int kSBytes = HT * kSStride * 4;
+  static constexpr int kStageOff = kQBytes;
+  static constexpr int kSOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kBarOff = kSOff + 2 * kSBytes;
+  static constexpr int kBytes = kBarOff + (2 * kStages + 1) * 8 + 16;  // full, mask, q, flags
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
+  static_assert(kSTok == 16 || kSTok == 8, "S split");
+};
+
+struct MlaParams {
+  __nv_bfloat16* out;  // [B, H, 512]
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* ws_lse;       // [B, H, splits]
+  float* ws_o;         // [B, H, splits, 512]
+  unsigned* counters;  // [B, H / HT]
+  unsigned* err;
+  int64_t num_blocks;
+  int32_t num_heads;
+  int32_t block_size;
+  int32_t log2_bs;
+  int32_t max_blocks_per_seq;
+  int32_t num_splits;
+  int32_t tokens_per_split;
+  int32_t kv_evict_first;  // one head tile per sequence: nobody re-reads the rows
+  float scale_log2;
+};
+
+__device__ __forceinline__ int mla_effective_len(const MlaParams& p, int b, bool* clipped) {
+  int L = __ldg(p.context_lens + b);
+  L = L < 0 ? 0 : L;
+  const int64_t cap = min(static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size,
+                          static_cast<int64_t>(p.num_splits) * p.tokens_per_split);
+  *clipped = static_cast<int64_t>(L) > cap;
+  return *clipped ? static_cast<int>(cap) : L;
+}
+
+// swizzled address of 16-byte unit `unit` of row `row` in a [rows x 128 B] region
+__device__ __forceinline__ uint32_t swz(uint32_t region, int row, int unit) {
+  return region + static_cast<uint32_t>(row * 128 + ((unit ^ (row & 7)) << 4));
+}
+
+// Merge of one (sequence, head) row by one warp over n splits: weights
+// 2^(lse_s - max), out = sum_s w_s o_s / sum_s w_s in bf16.  Lane owns
+// elements 4*lane + 128*i, i = 0..3.
+__device__ __forceinline__ void mla_merge_warp(const MlaParams& p, int64_t bh, int n, int lane) {
+  const float* lse = p.ws_lse + bh * p.num_splits;
+  const float* o = p.ws_o + bh * p.num_splits * kLat;
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) M = fmaxf(M, __ldcg(lse + s));
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float4 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float W = 0.f;
+  if (M != -INFINITY) {
+    for (int s0 = 0; s0 < n; s0 += 32) {
+      const int my = s0 + lane;
+      const float wl = my < n ? exp2f(__ldcg(lse + my) - M) : 0.f;
+      const int cnt = min(32, n - s0);
+      for (int k = 0; k < cnt; ++k) {
+        const float w = __shfl_sync(0xffffffffu, wl, k);
+        const float4* src = reinterpret_cast<const float4*>(o + static_cast<int64_t>(s0 + k) * kLat);
+        W += w;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 v = __ldcg(src + lane + 32 * i);
+          acc[i].x += w * v.x;
+          acc[i].y += w * v.y;
+          acc[i].z += w * v.z;
+          acc[i].w += w * v.w;
+        }
+      }
+    }
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<uint2*>(p.out + bh * kLat + 4 * lane + 128 * i) =
+        make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
+                   pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
+}
+
+// Loads of one tile (called by warp 0, all lanes): lane i < nbox looks up
+// block piece i of the tile, the lanes agree on the tile's row mask, lane 0
+// posts it and the byte count, and each lane with a valid piece issues one
+// TMA box per 64-element chunk.
+template <int HT>
+__device__ __forceinline__ void mla_issue_tile(const MlaParams& p, const CUtensorMap* tm_kv,
+                                               uint8_t* smem, uint64_t* full, uint64_t* tile_mask,
+                                               const int32_t* bt, int tok0, int tok_end, int stage,
+                                               uint64_t pol, int lane) {
+  using C = MlaCfg<HT>;
+  const int bs = p.block_size;
+  const int rpb = bs < C::kTile ? bs : C::kTile;
+  const int nbox = C::kTile / rpb;
+  const int nval = min(C::kTile, tok_end - tok0);
+  bool valid = false;
+  int rows = 0, bid = -1, row0 = 0;
+  if (lane < nbox) {
+    const int first = tok0 + lane * rpb;
+    rows = min(rpb, nval - lane * rpb);
+    if (rows > 0) {
+      row0 = first & (bs - 1);
+      bid = __ldg(bt + (first >> p.log2_bs));
+      valid = bid >= 0 && static_cast<int64_t>(bid) < p.num_blocks;
+    }
+  }
+  uint64_t bits = 0;
+  if (valid) bits = (rows >= 64 ? ~0ull : ((1ull << rows) - 1ull)) << (lane * rpb);
+  const uint32_t lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits));
+  const uint32_t hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits >> 32));
+  const uint32_t vb = __ballot_sync(0xffffffffu, valid);
+  if (lane == 0) {
+    tile_mask[stage] = (static_cast<uint64_t>(hi) << 32) | lo;
+    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(__popc(vb) * rpb * kRowBytes));
+  }
+  __syncwarp();
+  if (valid) {
+    const int32_t row = bid * bs + row0;
+    uint8_t* st = smem + C::kStageOff + stage * C::kStageBytes + lane * rpb * 128;
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c)
+      tma_load_2d(st + c * C::kChunkBytes, tm_kv, 64 * c, row, &full[stage], pol);
+  }
+}
+
+template <int HT>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
+  using C = MlaCfg<HT>;
+  constexpr int kTile = C::kTile;
+  constexpr int kStages = C::kStages;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* tile_mask = full + kStages;
+  uint64_t* qbar = tile_mask + kStages;
+  int* flags = reinterpret_cast<int*>(qbar + 1);
+
+  const int ht = blockIdx.x;
+  const int split = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h0 = ht * HT;
+
+  bool clipped;
+  const int L = mla_effective_len(p, b, &clipped);
+  if (clipped && split == 0 && ht == 0 && threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
+  const int tok_begin = split * p.tokens_per_split;
+  const int tok_end = min(tok_begin + p.tokens_per_split, L);
+  if (tok_begin >= tok_end) {
+    if (split == 0) {  // L == 0: zero rows
+      for (int i = threadIdx.x; i < HT * (kLat / 8); i += kThreads) {
+        const int h = i / (kLat / 8), c = i % (kLat / 8);
+        reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + h0 + h) *
+                                             kLat)[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    return;
+  }
+  const int ntiles = (tok_end - tok_begin + kTile - 1) / kTile;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    mbar_init(qbar, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const uint32_t smem_base = smem_u32(smem);
+  const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+  const uint64_t pol = p.kv_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+
+  // ---- warp 0 issues q_lat and the first kStages tiles
+  int issued = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_kv);
+      mbar_arrive_expect_tx(qbar, HT * kRowBytes);
+      const uint64_t qpol = l2_policy_evict_normal();
+#pragma unroll 1
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_2d(smem + c * HT * 128, &tm_q, 64 * c, b * p.num_heads + h0, qbar, qpol);
+    }
+    for (; issued < kStages && issued < ntiles; ++issued)
+      mla_issue_tile<HT>(p, &tm_kv, smem, full, tile_mask, bt, tok_begin + issued * kTile,
+                         tok_end, issued, pol, lane);
+  }
+
+  const int gq = lane >> 2;  // mma groupID
+  const int tq = lane & 3;   // thread in group
+  const int mb = warp % C::kMB;  // this warp's 16-head block
+  const int wi = warp / C::kMB;  // its index among that block's warps
+  float o[C::kDW / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < C::kDW / 8; ++nt)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[nt][c] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+
+  // all warps agree on whether q_lat arrived (they meet at a barrier every
+  // tile, so none may leave alone)
+  bool ok = named_barrier_and(1, kThreads, mbar_wait_bounded(qbar, 0, nullptr));
+  // lane-constant parts of the ldmatrix addresses
+  const int qrow = 16 * mb + (lane & 15);  // Q: A operand rows
+  const int qhalf = lane >> 4;             //    second 8 columns of a k-step
+  const int krow = C::kSTok == 16 ? wi * 16 + (lane & 7) + ((lane >> 4) << 3)
+                                  : wi * 8 + (lane & 7);
+  const int khalf = C::kSTok == 16 ? ((lane >> 3) & 1) : (lane >> 3);
+  const int vrow_l = (lane & 7) + (((lane >> 3) & 1) << 3);  // V: token within the k-step
+  const int vhalf = lane >> 4;                               //    second 8 elements
+  float* s_tile = reinterpret_cast<float*>(smem + C::kSOff);
+
+  int consumed = 0;
+  for (int t = 0; t < ntiles && ok; ++t) {
+    const int stage = t % kStages;
+    const bool w_ok = mbar_wait_bounded(&full[stage], (t / kStages) & 1, nullptr);
+    const uint32_t st_base = smem_base + C::kStageOff + stage * C::kStageBytes;
+    float* S = s_tile + (t & 1) * (HT * C::kSStride);
+    uint64_t mask = 0;
+    if (__all_sync(0xffffffffu, w_ok)) {
+      mask = tile_mask[stage];
+      // ---- S = Q . K^T for 16 heads x kSTok tokens over the 576 elements
+      constexpr int NTS = C::kSTok / 8;
+      float sacc[NTS][4];
+#pragma unroll
+      for (int nt = 0; nt < NTS; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sacc[nt][c] = 0.f;
+#pragma unroll 3
+      for (int kc = 0; kc < kChunks * 4; kc += 2) {
+        const int c = kc >> 2;
+        const int j = kc & 3;  // k-steps j and j + 1 of chunk c
+        const uint32_t qreg = smem_base + c * HT * 128;
+        const uint32_t kreg = st_base + c * C::kChunkBytes;
+        if constexpr (C::kSTok == 16) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t a[4], bb[4];
+            ldsm_x4(swz(qreg, qrow, 2 * (j + h2) + qhalf), a);
+            ldsm_x4(swz(kreg, krow, 2 * (j + h2) + khalf), bb);
+            mma_bf16_16816(sacc[0], a, bb[0], bb[1]);
+            mma_bf16_16816(sacc[NTS - 1], a, bb[2], bb[3]);
+          }
+        } else {
+          uint32_t a0[4], a1[4], bb[4];
+          ldsm_x4(swz(qreg, qrow, 2 * j + qhalf), a0);
+          ldsm_x4(swz(qreg, qrow, 2 * j + 2 + qhalf), a1);
+          ldsm_x4(swz(kreg, krow, 2 * j + khalf), bb);
+          mma_bf16_16816(sacc[0], a0, bb[0], bb[1]);
+          mma_bf16_16816(sacc[0], a1, bb[2], bb[3]);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NTS; ++nt) {
+        const int col = wi * C::kSTok + nt * 8 + 2 * tq;
+        float* r0 = S + (16 * mb + gq) * C::kSStride + col;
+        float* r1 = r0 + 8 * C::kSStride;
+        *reinterpret_cast<float2*>(r0) = make_float2(sacc[nt][0], sacc[nt][1]);
+        *reinterpret_cast<float2*>(r1) = make_float2(sacc[nt][2], sacc[nt][3]);
+      }
+      // rows of this warp's tokens that hold no token: zero their value
+      // part (0 x NaN would poison P . V); their scores are masked below
+      const uint32_t my_mask = static_cast<uint32_t>(mask >> (wi * C::kSTok)) &
+                               ((1u << C::kSTok) - 1u);
+      if (my_mask != (1u << C::kSTok) - 1u) {
+        uint8_t* st = smem + C::kStageOff + stage * C::kStageBytes;
+        for (int idx = lane; idx < C::kSTok * 64; idx += 32) {
+          const int rr = idx >> 6, unit = idx & 63;  // 64 units of 16 B = 512 elements
+          if (!((my_mask >> rr) & 1u))
+            *reinterpret_cast<uint4*>(st + (unit >> 3) * C::kChunkBytes +
+                                      (wi * C::kSTok + rr) * 128 + ((unit & 7) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // generic writes before the stage's next TMA fill
+      }
+    }
+    // every warp's scores (and zeroed rows) are in place, and every warp is
+    // done with tile t - 1: its stage takes tile t - 1 + kStages
+    if (!named_barrier_and(1, kThreads, w_ok)) {
+      ok = false;
+      break;
+    }
+    consumed = t + 1;
+    if (warp == 0 && t >= 1 && issued < ntiles) {
+      mla_issue_tile<HT>(p, &tm_kv, smem, full, tile_mask, bt, tok_begin + issued * kTile,
+                         tok_end, issued % kStages, pol, lane);
+      ++issued;
+    }
+    // ---- softmax over this warp's 16 heads, then O += P . V.  The score
+    // tile is read twice (max, then weights) rather than held in registers.
+    constexpr int KS = kTile / 16;
+    // scaled, masked scores at the A-fragment positions of k-step kk:
+    // rows gq (r = 0) and gq + 8 (r = 1), columns 2tq, 2tq+1, 2tq+8, 2tq+9
+    auto load_scores = [&](int kk, int r, float (&x)[4]) {
+      const float* row = S + (16 * mb + gq + 8 * r) * C::kSStride + 16 * kk + 2 * tq;
+      const float2 x0 = *reinterpret_cast<const float2*>(row);
+      const float2 x1 = *reinterpret_cast<const float2*>(row + 8);
+      const uint32_t bits = static_cast<uint32_t>(mask >> (16 * kk + 2 * tq));
+      x[0] = (bits & 1u) ? x0.x * p.scale_log2 : -INFINITY;
+      x[1] = (bits & 2u) ? x0.y * p.scale_log2 : -INFINITY;
+      x[2] = (bits & 0x100u) ? x1.x * p.scale_log2 : -INFINITY;
+      x[3] = (bits & 0x200u) ? x1.y * p.scale_log2 : -INFINITY;
+    };
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float x[4];
+        load_scores(kk, r, x);
+        mx[r] = fmaxf(mx[r], fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
+      }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      if (mx[r] > m_run[r] + kRescaleLog2) {  // new running max (always on the first)
+        const float corr = exp2f(m_run[r] - mx[r]);
+        l_run[r] *= corr;
+#pragma unroll
+        for (int nt = 0; nt < C::kDW / 8; ++nt) {
+          o[nt][2 * r] *= corr;
+          o[nt][2 * r + 1] *= corr;
+        }
+        m_run[r] = mx[r];
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      float pv[2][4];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        load_scores(kk, r, pv[r]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          // a masked score is -inf and m_run is finite once a token was seen
+          pv[r][c] = pv[r][c] == -INFINITY ? 0.f : exp2f(pv[r][c] - m_run[r]);
+          l_run[r] += pv[r][c];
+        }
+      }
+      const uint32_t a[4] = {pack_bf16x2(pv[0][0], pv[0][1]), pack_bf16x2(pv[1][0], pv[1][1]),
+                             pack_bf16x2(pv[0][2], pv[0][3]), pack_bf16x2(pv[1][2], pv[1][3])};
+      const int vrow = 16 * kk + vrow_l;
+#pragma unroll
+      for (int np = 0; np < C::kDW / 16; ++np) {
+        const int d = wi * C::kDW + 16 * np + 8 * vhalf;  // first element of this lane's unit
+        uint32_t bv[4];
+        ldsm_x4_trans(swz(st_base + (d >> 6) * C::kChunkBytes, vrow, (d & 63) >> 3), bv);
+        mma_bf16_16816(o[2 * np], a, bv[0], bv[1]);
+        mma_bf16_16816(o[2 * np + 1], a, bv[2], bv[3]);
+      }
+    }
+  }
+
+  const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + h0;
+  if (!ok) {
+    // wait (bounded) for the copies still in flight, then leave an empty
+    // partial so that the split count below still completes
+    if (threadIdx.x == 0) {
+      atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+      mbar_wait_bounded(qbar, 0, nullptr);
+      for (int t = consumed; t < issued; ++t)
+        mbar_wait_bounded(&full[t % kStages], (t / kStages) & 1, nullptr);
+    }
+    if (p.num_splits > 1 && threadIdx.x < HT)
+      p.ws_lse[(bh0 + threadIdx.x) * p.num_splits + split] = -INFINITY;
+  } else {
+    // ---- epilogue: rows 16mb + gq (+8), elements wi*kDW + 8nt + 2tq (+1)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+      l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int64_t bh = bh0 + 16 * mb + gq + 8 * r;
+      const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
+      if (p.num_splits == 1) {
+        __nv_bfloat16* dst = p.out + bh * kLat + wi * C::kDW + 2 * tq;
+#pragma unroll
+        for (int nt = 0; nt < C::kDW / 8; ++nt)
+          *reinterpret_cast<uint32_t*>(dst + 8 * nt) =
+              pack_bf16x2(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
+      } else {
+        const int64_t slot = bh * p.num_splits + split;
+        float* dst = p.ws_o + slot * kLat + wi * C::kDW + 2 * tq;
+#pragma unroll
+        for (int nt = 0; nt < C::kDW / 8; ++nt)
+          *reinterpret_cast<float2*>(dst + 8 * nt) =
+              make_float2(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
+        if (wi == 0 && tq == 0)
+          p.ws_lse[slot] = l_run[r] > 0.f ? m_run[r] + log2f(l_run[r]) : -INFINITY;
+      }
+    }
+  }
+  if (p.num_splits == 1) return;
+
+  // ------------------------------------------------- split count and merge
+  // The CTA that completes the count of its (sequence, head tile) merges
+  // the splits of its HT heads and returns the counter to zero.
+  __syncthreads();  // every partial of this CTA is written
+  const int n_valid = (L + p.tokens_per_split - 1) / p.tokens_per_split;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    unsigned* ctr = p.counters + static_cast<int64_t>(b) * (p.num_heads / HT) + ht;
+    const unsigned prev = atomicAdd(ctr, 1u);
+    const bool last = prev + 1u == static_cast<unsigned>(n_valid);
+    if (last) {
+      atomicExch(ctr, 0u);
+      __threadfence();
+    }
+    flags[0] = last ? 1 : 0;
+  }
+  __syncthreads();
+  if (flags[0]) {
+    for (int h = warp; h < HT; h += kThreads / 32) mla_merge_warp(p, bh0 + h, n_valid, lane);
+  }
+}
+
+template <int HT>
+pa_status launch_mla_split(const CUtensorMap& mq, const CUtensorMap& mkv, const MlaParams& p,
+                           dim3 grid, cudaStream_t stream) {
+  static std::atomic<bool> attr_set{false};
+  auto kern = mla_decode_split_kernel<HT>;
+  constexpr int kSmem = MlaCfg<HT>::kAlloc;
+  if (!attr_set.load()) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    attr_set.store(true);
+  }
+  kern<<<grid, kThreads, kSmem, stream>>>(mq, mkv, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// 2-D bf16 map over [rows, 576] with a 1152-byte row stride; box = 64
+// elements (128 bytes) x box_rows, 128-byte swizzled.
+bool make_row576_map(CUtensorMap* map, const void* base, int64_t rows, int32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
+  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t es[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+int mla_head_tile(int32_t num_heads) { return num_heads % 64 == 0 ? 64 : 16; }
+
+DecodePlan make_mla_plan(int32_t num_seqs, int32_t num_heads, int32_t max_context_len,
+                         int32_t num_sms) {
+  if (num_sms <= 0) num_sms = 148;
+  const int ht = mla_head_tile(num_heads);
+  const int tile = ht == 64 ? MlaCfg<64>::kTile : MlaCfg<16>::kTile;
+  if (max_context_len <= 0 || num_seqs <= 0 || num_heads <= 0) return {1, tile};
+  const int64_t tiles_max = (static_cast<int64_t>(max_context_len) + tile - 1) / tile;
+  const int64_t work = static_cast<int64_t>(num_seqs) * (num_heads / ht);
+  const int64_t target = 4ll * num_sms;  // one CTA per SM: about four waves
+  int64_t splits = (target + work - 1) / work;
+  if (splits < 1) splits = 1;
+  if (splits > tiles_max) splits = tiles_max;
+  const int64_t tiles_per_split = (tiles_max + splits - 1) / splits;
+  splits = (tiles_max + tiles_per_split - 1) / tiles_per_split;
+  return {static_cast<int32_t>(splits), static_cast<int32_t>(tiles_per_split * tile)};
+}
+
+// [error word | pad] [counters B * H/HT] [lse B*H*splits] [o B*H*splits*512]
+size_t mla_workspace_bytes(int32_t num_seqs, int32_t num_heads, const DecodePlan& plan) {
+  size_t bytes = kWorkspaceHeader;
+  if (plan.num_splits > 1) {
+    const size_t rows = static_cast<size_t>(num_seqs) * num_heads * plan.num_splits;
+    bytes += align256(static_cast<size_t>(num_seqs) * (num_heads / mla_head_tile(num_heads)) * 4);
+    bytes += align256(rows * sizeof(float));
+    bytes += rows * kLat * sizeof(float);
+  }
+  return bytes;
+}
+
+pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0) return PA_OK;
+  const int ht = mla_head_tile(a.num_heads);
+  const int tile = ht == 64 ? MlaCfg<64>::kTile : MlaCfg<16>::kTile;
+  const int32_t box_rows = a.block_size < tile ? a.block_size : tile;
+  CUtensorMap mq, mkv;
+  if (!make_row576_map(&mq, a.q_latent, static_cast<int64_t>(a.num_seqs) * a.num_heads, ht) ||
+      !make_row576_map(&mkv, a.latent_cache, a.num_blocks * a.block_size, box_rows))
+    return PA_ERR_CUDA;
+  MlaParams p;
+  p.out = static_cast<__nv_bfloat16*>(a.out_latent);
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  p.err = reinterpret_cast<unsigned*>(ws);
+  const size_t nrows = static_cast<size_t>(a.num_seqs) * a.num_heads * a.plan.num_splits;
+  const size_t ctr_bytes = align256(static_cast<size_t>(a.num_seqs) * (a.num_heads / ht) * 4);
+  p.counters = reinterpret_cast<unsigned*>(ws + kWorkspaceHeader);
+  p.ws_lse = reinterpret_cast<float*>(ws + kWorkspaceHeader + ctr_bytes);
+  p.ws_o = reinterpret_cast<float*>(ws + kWorkspaceHeader + ctr_bytes + align256(nrows * 4));
+  p.num_blocks = a.num_blocks;
+  p.num_heads = a.num_heads;
+  p.block_size = a.block_size;
+  int lg = 0;
+  while ((1 << lg) < a.block_size) ++lg;
+  p.log2_bs = lg;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_splits = a.plan.num_splits;
+  p.tokens_per_split = a.plan.tokens_per_split;
+  p.kv_evict_first = a.num_heads == ht ? 1 : 0;
+  p.scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
+  const dim3 grid(static_cast<unsigned>(a.num_heads / ht), static_cast<unsigned>(a.plan.num_splits),
+                  static_cast<unsigned>(a.num_seqs));
+  return ht == 64 ? launch_mla_split<64>(mq, mkv, p, grid, stream)
+                  : launch_mla_split<16>(mq, mkv, p, grid, stream);
+}
+
+}  // namespace pa_detail

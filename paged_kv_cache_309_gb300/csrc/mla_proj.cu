@@ -1,0 +1,161 @@
+// mla_proj.cu -- the two per-head products that put MLA decode in its
+// absorbed form (PagedAttention-principle post, MLA section: K and V of head
+// h are c_kv W_UK_h and c_kv W_UV_h with W_UK, W_UV: [d_c, H * d_h] and
+// head h owning columns h*d_h .. (h+1)*d_h - 1):
+//   absorb:  q_lat[b, h, c]  = sum_i q_nope[b, h, i] * W_UK[c, h*d_h + i]   (c < d_c)
+//            q_lat[b, h, d_c + r] = q_pe[b, h, r]
+//   project: out[b, h, i]    = sum_c o_lat[b, h, c] * W_UV[c, h*d_v + i]
+// Both are Y_h = X_h . W_h per head, bf16 in, fp32 accumulate, bf16 out, on
+// the tensor cores (mma.sync m16n8k16).  A CTA computes a 64 (sequences) x
+// 64 (outputs) tile of one head with four warps of 16 rows each; K advances
+// in 64-wide slices staged in padded shared memory (row stride 144 bytes,
+// so the eight rows of an ldmatrix phase hit eight different bank groups).
+// W_UK_h is read with rows = outputs (ldmatrix), W_UV_h with rows = the
+// reduction index (ldmatrix.trans).  At decode batch sizes the weights are
+// the bytes that matter: each weight element is read once per 64 sequences.
+#include "pa_internal.cuh"
+
+namespace pa_detail {
+namespace {
+
+using namespace pa;
+
+constexpr int kTM = 64, kTN = 64, kTK = 64;
+constexpr int kPad = 72;  // elements per staged row (64 + 8)
+constexpr int kThreads = 128;
+
+struct ProjParams {
+  __nv_bfloat16* y;        // [M, H, ldy], columns 0..N-1 written
+  const __nv_bfloat16* x;  // [M, H, K]
+  const __nv_bfloat16* w;
+  const __nv_bfloat16* extra;  // absorb: q_pe [M, H, extra_dim] copied to y columns N..
+  int32_t M, H, K, N, ldy, extra_dim;
+};
+
+// kTransB = false: W(k, n) = w[n, h*K + k]   (absorb, rows = outputs)
+// kTransB = true:  W(k, n) = w[k, h*N + n]   (project, rows = reduction index)
+template <bool kTransB>
+__global__ void __launch_bounds__(kThreads) mla_head_gemm_kernel(const ProjParams p) {
+  __shared__ __align__(16) __nv_bfloat16 xs[kTM * kPad];
+  __shared__ __align__(16) __nv_bfloat16 ws[kTK * kPad];
+  const int n0 = blockIdx.x * kTN;
+  const int h = blockIdx.y;
+  const int m0 = blockIdx.z * kTM;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int64_t xrow = static_cast<int64_t>(p.H) * p.K;
+
+  float acc[kTN / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < kTN / 8; ++nt)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[nt][c] = 0.f;
+
+  const uint32_t xs_base = smem_u32(xs);
+  const uint32_t ws_base = smem_u32(ws);
+  for (int k0 = 0; k0 < p.K; k0 += kTK) {
+    // stage X[m0.., h, k0..] and the weight slice: 64 rows x 8 units of 16 B each
+    for (int i = threadIdx.x; i < 64 * 8; i += kThreads) {
+      const int r = i >> 3, u = i & 7;
+      uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+      if (m0 + r < p.M)
+        xv = __ldg(reinterpret_cast<const uint4*>(p.x + (m0 + r) * xrow +
+                                                  static_cast<int64_t>(h) * p.K + k0) + u);
+      *reinterpret_cast<uint4*>(xs + r * kPad + 8 * u) = xv;
+      const __nv_bfloat16* wsrc =
+          kTransB ? p.w + static_cast<int64_t>(k0 + r) * p.H * p.N + static_cast<int64_t>(h) * p.N + n0
+                  : p.w + static_cast<int64_t>(n0 + r) * p.H * p.K + static_cast<int64_t>(h) * p.K + k0;
+      *reinterpret_cast<uint4*>(ws + r * kPad + 8 * u) =
+          __ldg(reinterpret_cast<const uint4*>(wsrc) + u);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kTK / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(xs_base + static_cast<uint32_t>(((16 * warp + (lane & 15)) * kPad + 16 * kk +
+                                              8 * (lane >> 4)) * 2), a);
+#pragma unroll
+      for (int np = 0; np < kTN / 16; ++np) {
+        uint32_t bb[4];
+        if constexpr (kTransB) {
+          // rows = k: lanes 0-7 k 0-7, 8-15 k 8-15 (n 0-7), 16-31 the same for n 8-15
+          const int kr = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
+          ldsm_x4_trans(ws_base + static_cast<uint32_t>((kr * kPad + 16 * np + 8 * (lane >> 4)) * 2), bb);
+        } else {
+          // rows = n: lanes 0-7 n 0-7 k 0-7, 8-15 n 0-7 k 8-15, 16-31 the same for n 8-15
+          const int nr = 16 * np + (lane & 7) + 8 * (lane >> 4);
+          ldsm_x4(ws_base + static_cast<uint32_t>((nr * kPad + 16 * kk + 8 * ((lane >> 3) & 1)) * 2), bb);
+        }
+        mma_bf16_16816(acc[2 * np], a, bb[0], bb[1]);
+        mma_bf16_16816(acc[2 * np + 1], a, bb[2], bb[3]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int m = m0 + 16 * warp + gq + 8 * r;
+    if (m >= p.M) continue;
+    __nv_bfloat16* dst = p.y + (static_cast<int64_t>(m) * p.H + h) * p.ldy + n0 + 2 * tq;
+#pragma unroll
+    for (int nt = 0; nt < kTN / 8; ++nt)
+      *reinterpret_cast<uint32_t*>(dst + 8 * nt) = pack_bf16x2(acc[nt][2 * r], acc[nt][2 * r + 1]);
+  }
+  // absorb: the rope part of the query is copied behind the latent part
+  if (p.extra != nullptr && blockIdx.x == 0) {
+    const int units = p.extra_dim / 8;
+    for (int i = threadIdx.x; i < kTM * units; i += kThreads) {
+      const int r = i / units, u = i % units;
+      if (m0 + r >= p.M) continue;
+      const int64_t row = static_cast<int64_t>(m0 + r) * p.H + h;
+      *reinterpret_cast<uint4*>(p.y + row * p.ldy + p.N + 8 * u) =
+          __ldg(reinterpret_cast<const uint4*>(p.extra + row * p.extra_dim) + u);
+    }
+  }
+}
+
+}  // namespace
+
+pa_status launch_mla_absorb_q(void* q_latent, const void* q_nope, const void* q_pe,
+                              const void* w_uk, int32_t num_seqs, int32_t num_heads,
+                              int32_t nope_dim, int32_t rope_dim, int32_t latent_dim,
+                              cudaStream_t stream) {
+  ProjParams p;
+  p.y = static_cast<__nv_bfloat16*>(q_latent);
+  p.x = static_cast<const __nv_bfloat16*>(q_nope);
+  p.w = static_cast<const __nv_bfloat16*>(w_uk);
+  p.extra = static_cast<const __nv_bfloat16*>(q_pe);
+  p.M = num_seqs;
+  p.H = num_heads;
+  p.K = nope_dim;
+  p.N = latent_dim;
+  p.ldy = latent_dim + rope_dim;
+  p.extra_dim = rope_dim;
+  const dim3 grid(static_cast<unsigned>(latent_dim / kTN), static_cast<unsigned>(num_heads),
+                  static_cast<unsigned>((num_seqs + kTM - 1) / kTM));
+  mla_head_gemm_kernel<false><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status launch_mla_project_out(void* out, const void* out_latent, const void* w_uv,
+                                 int32_t num_seqs, int32_t num_heads, int32_t latent_dim,
+                                 int32_t v_head_dim, cudaStream_t stream) {
+  ProjParams p;
+  p.y = static_cast<__nv_bfloat16*>(out);
+  p.x = static_cast<const __nv_bfloat16*>(out_latent);
+  p.w = static_cast<const __nv_bfloat16*>(w_uv);
+  p.extra = nullptr;
+  p.M = num_seqs;
+  p.H = num_heads;
+  p.K = latent_dim;
+  p.N = v_head_dim;
+  p.ldy = v_head_dim;
+  p.extra_dim = 0;
+  const dim3 grid(static_cast<unsigned>(v_head_dim / kTN), static_cast<unsigned>(num_heads),
+                  static_cast<unsigned>((num_seqs + kTM - 1) / kTM));
+  mla_head_gemm_kernel<true><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa_detail

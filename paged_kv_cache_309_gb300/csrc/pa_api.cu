@@ -364,4 +364,88 @@ pa_status pa_paged_decode_attention_static(void* out, const void* q, const void*
   return pa_detail::launch_paged_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+pa_status pa_mla_absorb_q(void* q_latent, const void* q_nope, const void* q_pe, const void* w_uk,
+                          int32_t num_seqs, int32_t num_heads, int32_t nope_dim, int32_t rope_dim,
+                          int32_t latent_dim, pa_stream_t stream) {
+  if (num_seqs < 0 || num_heads <= 0 || nope_dim <= 0 || rope_dim < 0 || latent_dim <= 0)
+    return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  if (q_latent == nullptr || q_nope == nullptr || w_uk == nullptr || (rope_dim > 0 && q_pe == nullptr))
+    return PA_ERR_INVALID;
+  if (nope_dim % 64 != 0 || latent_dim % 64 != 0 || rope_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_heads) * nope_dim >= (1ll << 31) / 2) return PA_ERR_UNSUPPORTED;
+  if (!aligned(q_latent, 16) || !aligned(q_nope, 16) || !aligned(w_uk, 16) ||
+      (q_pe != nullptr && !aligned(q_pe, 16)))
+    return PA_ERR_ALIGN;
+  return pa_detail::launch_mla_absorb_q(q_latent, q_nope, rope_dim > 0 ? q_pe : nullptr, w_uk,
+                                        num_seqs, num_heads, nope_dim, rope_dim, latent_dim,
+                                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t pa_mla_decode_workspace_size(int32_t num_seqs, int32_t num_heads,
+                                    int32_t max_context_len) {
+  if (num_seqs < 0 || num_heads <= 0 || num_heads % 16 != 0 || max_context_len < 0 ||
+      max_context_len > (1 << 30))
+    return 0;
+  const pa_detail::DecodePlan plan = pa_detail::make_mla_plan(
+      num_seqs, num_heads, max_context_len, pa_detail::num_sms_current_device());
+  return pa_detail::mla_workspace_bytes(num_seqs, num_heads, plan);
+}
+
+pa_status pa_mla_decode_attention(void* out_latent, const void* q_latent,
+                                  const void* latent_cache, const int32_t* block_tables,
+                                  const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t num_heads, int32_t latent_dim, int32_t rope_dim,
+                                  int32_t block_size, int32_t max_blocks_per_seq,
+                                  int64_t num_blocks, float scale, int32_t max_context_len,
+                                  void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (num_seqs < 0 || num_heads <= 0 || latent_dim <= 0 || rope_dim < 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
+      max_context_len > (1 << 30))
+    return PA_ERR_INVALID;
+  if (out_latent == nullptr || q_latent == nullptr || latent_cache == nullptr ||
+      block_tables == nullptr || context_lens == nullptr)
+    return PA_ERR_INVALID;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID;
+  if (latent_dim != 512 || rope_dim != 64 || num_heads % 16 != 0) return PA_ERR_UNSUPPORTED;
+  if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0)
+    return PA_ERR_UNSUPPORTED;
+  if (num_blocks * block_size >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_seqs) * num_heads >= (1ll << 31)) return PA_ERR_UNSUPPORTED;
+  if (!aligned(out_latent, 16) || !aligned(q_latent, 16) || !aligned(latent_cache, 16))
+    return PA_ERR_ALIGN;
+  pa_detail::MlaDecodeArgs a{};
+  a.out_latent = out_latent;
+  a.q_latent = q_latent;
+  a.latent_cache = latent_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.plan = pa_detail::make_mla_plan(num_seqs, num_heads, max_context_len,
+                                    pa_detail::num_sms_current_device());
+  const size_t need = pa_detail::mla_workspace_bytes(num_seqs, num_heads, a.plan);
+  if (workspace == nullptr || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_ALIGN;
+  a.workspace = workspace;
+  return pa_detail::launch_mla_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_mla_project_out(void* out, const void* out_latent, const void* w_uv,
+                             int32_t num_seqs, int32_t num_heads, int32_t latent_dim,
+                             int32_t v_head_dim, pa_stream_t stream) {
+  if (num_seqs < 0 || num_heads <= 0 || latent_dim <= 0 || v_head_dim <= 0) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  if (out == nullptr || out_latent == nullptr || w_uv == nullptr) return PA_ERR_INVALID;
+  if (latent_dim % 64 != 0 || v_head_dim % 64 != 0) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_heads) * v_head_dim >= (1ll << 31) / 2) return PA_ERR_UNSUPPORTED;
+  if (!aligned(out, 16) || !aligned(out_latent, 16) || !aligned(w_uv, 16)) return PA_ERR_ALIGN;
+  return pa_detail::launch_mla_project_out(out, out_latent, w_uv, num_seqs, num_heads, latent_dim,
+                                           v_head_dim, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

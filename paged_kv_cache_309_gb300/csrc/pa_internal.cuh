@@ -299,6 +299,37 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// 2-D tiled TMA load global -> shared with an L2 hint, completion on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t c0,
+                                            int32_t c1, uint64_t* bar, uint64_t l2_policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(l2_policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Barrier `id` over `nthreads` threads (a multiple of 32) that also returns
+// whether `pred` held in every participating thread.
+__device__ __forceinline__ bool named_barrier_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -449,6 +480,31 @@ struct PrefillArgs {
   float scale;
 };
 pa_status launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+struct MlaDecodeArgs {
+  void* out_latent;          // [B, H, 512] bf16
+  const void* q_latent;      // [B, H, 576] bf16
+  const void* latent_cache;  // [num_blocks, block_size, 576] bf16
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* workspace;
+  int32_t num_seqs, num_heads, block_size, max_blocks_per_seq;
+  int64_t num_blocks;
+  float scale;
+  DecodePlan plan;
+};
+int mla_head_tile(int32_t num_heads);  // 64 when num_heads % 64 == 0, else 16
+DecodePlan make_mla_plan(int32_t num_seqs, int32_t num_heads, int32_t max_context_len,
+                         int32_t num_sms);
+size_t mla_workspace_bytes(int32_t num_seqs, int32_t num_heads, const DecodePlan& plan);
+pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream);
+pa_status launch_mla_absorb_q(void* q_latent, const void* q_nope, const void* q_pe,
+                              const void* w_uk, int32_t num_seqs, int32_t num_heads,
+                              int32_t nope_dim, int32_t rope_dim, int32_t latent_dim,
+                              cudaStream_t stream);
+pa_status launch_mla_project_out(void* out, const void* out_latent, const void* w_uv,
+                                 int32_t num_seqs, int32_t num_heads, int32_t latent_dim,
+                                 int32_t v_head_dim, cudaStream_t stream);
 
 // Library-owned decode scratch (a file-scope __device__ array in decode.cu)
 // for callers that cannot allocate: its size, and its device address on the

@@ -74,6 +74,15 @@ def _load():
     lib.pa_paged_decode_plan.argtypes = [I32, I32, I32, I32, ctypes.POINTER(I32),
                                          ctypes.POINTER(I32)]
     lib.pa_paged_decode_plan.restype = E
+    lib.pa_mla_absorb_q.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, P]
+    lib.pa_mla_absorb_q.restype = E
+    lib.pa_mla_decode_workspace_size.argtypes = [I32, I32, I32]
+    lib.pa_mla_decode_workspace_size.restype = SZ
+    lib.pa_mla_decode_attention.argtypes = [P, P, P, P, P, I32, I32, I32, I32, I32, I32, I64,
+                                            ctypes.c_float, I32, P, SZ, P]
+    lib.pa_mla_decode_attention.restype = E
+    lib.pa_mla_project_out.argtypes = [P, P, P, I32, I32, I32, I32, P]
+    lib.pa_mla_project_out.restype = E
     _lib = lib
     return lib
 
@@ -309,3 +318,73 @@ def pa_paged_prefill_attention(out, q, k_cache, v_cache, block_tables, cu_seqlen
         _ptr(cu_seqlens_q), _ptr(context_lens), B, HQ, HKV, d, bs, block_tables.shape[1], nb,
         float(scale), int(max_q_len), _ptr(error_word), _stream(stream))
     _check(st, "pa_paged_prefill_attention")
+
+
+# ------------------------------------------------------------- MLA decode --
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def pa_mla_absorb_q(q_latent, q_nope, q_pe, w_uk, stream=None):
+    """q_latent [B, H, d_c + d_r] <- [W_UK_h q_nope[b, h] | q_pe[b, h]];
+    q_nope [B, H, d_h], q_pe [B, H, d_r], w_uk [d_c, H * d_h], all bf16."""
+    B, H, dh = q_nope.shape
+    dr = q_pe.shape[2]
+    dc = w_uk.shape[0]
+    for t in (q_latent, q_nope, q_pe, w_uk):
+        _need(t.is_contiguous() and t.dtype == torch.bfloat16, "bf16 contiguous tensors expected")
+    _need(q_latent.shape == (B, H, dc + dr) and q_pe.shape[:2] == (B, H)
+          and w_uk.shape == (dc, H * dh), "shape mismatch")
+    _check(_load().pa_mla_absorb_q(_ptr(q_latent), _ptr(q_nope), _ptr(q_pe), _ptr(w_uk), B, H,
+                                   dh, dr, dc, _stream(stream)), "pa_mla_absorb_q")
+
+
+def pa_mla_decode_workspace_size(num_seqs, num_heads, max_context_len):
+    return int(_load().pa_mla_decode_workspace_size(num_seqs, num_heads, max_context_len))
+
+
+def mla_decode_workspace(num_seqs, num_heads, max_context_len, device=None):
+    """A zeroed device workspace for pa_mla_decode_attention (allocated by torch)."""
+    n = pa_mla_decode_workspace_size(num_seqs, num_heads, max_context_len)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_mla_decode_attention(out_latent, q_latent, latent_cache, block_tables, context_lens,
+                            scale, max_context_len, workspace, latent_dim=512, stream=None):
+    """out_latent [B, H, d_c] bf16; q_latent [B, H, d_c + d_r] bf16;
+    latent_cache [num_blocks, bs, (1,) d_c + d_r] bf16; block_tables
+    [B, max_blocks_per_seq] int32; context_lens [B] int32."""
+    B, H, dk = q_latent.shape
+    nb, bs = latent_cache.shape[0], latent_cache.shape[1]
+    for t, name in ((out_latent, "out_latent"), (q_latent, "q_latent"),
+                    (latent_cache, "latent_cache"), (block_tables, "block_tables"),
+                    (context_lens, "context_lens")):
+        _need(t.is_contiguous(), f"{name} must be contiguous")
+    _need(latent_cache.shape[-1] == dk and latent_cache.numel() == nb * bs * dk,
+          "latent_cache must be [num_blocks, bs, (1,) d_c + d_r]")
+    _need(out_latent.shape == (B, H, latent_dim), "out_latent must be [B, H, d_c]")
+    _need(q_latent.dtype == torch.bfloat16 and out_latent.dtype == torch.bfloat16
+          and latent_cache.dtype == torch.bfloat16, "bf16 tensors expected")
+    _need(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32,
+          "block_tables and context_lens must be int32")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == B and context_lens.numel() == B,
+          "block_tables must be [B, max_blocks_per_seq], context_lens [B]")
+    st = _load().pa_mla_decode_attention(
+        _ptr(out_latent), _ptr(q_latent), _ptr(latent_cache), _ptr(block_tables),
+        _ptr(context_lens), B, H, latent_dim, dk - latent_dim, bs, block_tables.shape[1], nb,
+        float(scale), int(max_context_len), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "pa_mla_decode_attention")
+
+
+def pa_mla_project_out(out, out_latent, w_uv, stream=None):
+    """out [B, H, d_v] <- out_latent[b, h, :] W_UV_h; out_latent [B, H, d_c],
+    w_uv [d_c, H * d_v], all bf16."""
+    B, H, dc = out_latent.shape
+    dv = out.shape[2]
+    for t in (out, out_latent, w_uv):
+        _need(t.is_contiguous() and t.dtype == torch.bfloat16, "bf16 contiguous tensors expected")
+    _need(out.shape[:2] == (B, H) and w_uv.shape == (dc, H * dv), "shape mismatch")
+    _check(_load().pa_mla_project_out(_ptr(out), _ptr(out_latent), _ptr(w_uv), B, H, dc, dv,
+                                      _stream(stream)), "pa_mla_project_out")

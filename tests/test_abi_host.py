@@ -148,3 +148,57 @@ def test_concat_rejects(lib):
     assert c(k1=184) == pa.PA_ERR_INVALID          # heads overlap in k
     assert c(kr=FAKE_MIS) == pa.PA_ERR_ALIGN
     assert c(n=0) == pa.PA_OK
+
+
+def _mla(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, cache=FAKE, bt=FAKE, cl=FAKE, B=4, H=128, dc=512, dr=64, bs=64,
+             mbps=8, nb=64, scale=0.072, maxctx=512, ws=FAKE, wsb=1 << 28)
+    a.update(kw)
+    return lib.pa_mla_decode_attention(a["out"], a["q"], a["cache"], a["bt"], a["cl"], a["B"],
+                                       a["H"], a["dc"], a["dr"], a["bs"], a["mbps"], a["nb"],
+                                       a["scale"], a["maxctx"], a["ws"], a["wsb"], None)
+
+
+def test_mla_decode_rejects(lib):
+    assert _mla(lib, q=None) == pa.PA_ERR_INVALID
+    assert _mla(lib, B=-1) == pa.PA_ERR_INVALID
+    assert _mla(lib, scale=float("inf")) == pa.PA_ERR_INVALID
+    assert _mla(lib, maxctx=-1) == pa.PA_ERR_INVALID
+    assert _mla(lib, dc=256) == pa.PA_ERR_UNSUPPORTED
+    assert _mla(lib, dr=32) == pa.PA_ERR_UNSUPPORTED
+    assert _mla(lib, H=24) == pa.PA_ERR_UNSUPPORTED            # not a multiple of 16
+    assert _mla(lib, bs=4) == pa.PA_ERR_UNSUPPORTED
+    assert _mla(lib, bs=48) == pa.PA_ERR_UNSUPPORTED
+    assert _mla(lib, out=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert _mla(lib, ws=None) == pa.PA_ERR_WORKSPACE
+    assert _mla(lib, wsb=16) == pa.PA_ERR_WORKSPACE
+    assert _mla(lib, ws=P(0x100010)) == pa.PA_ERR_ALIGN
+
+
+def test_mla_workspace_size(lib):
+    assert lib.pa_mla_decode_workspace_size(4, 24, 512) == 0      # heads not a multiple of 16
+    assert lib.pa_mla_decode_workspace_size(4, 128, -1) == 0
+    assert lib.pa_mla_decode_workspace_size(0, 128, 512) >= 256
+    # one split for a short context on many sequences: the header alone
+    assert lib.pa_mla_decode_workspace_size(4096, 128, 32) == 256
+
+
+def test_mla_projections_reject(lib):
+    ab = lambda **kw: lib.pa_mla_absorb_q(*[dict(dict(y=FAKE, qn=FAKE, qp=FAKE, w=FAKE, B=4,
+                                                      H=128, dh=128, dr=64, dc=512), **kw)[k]
+                                            for k in ("y", "qn", "qp", "w", "B", "H", "dh", "dr",
+                                                      "dc")], None)
+    assert ab(qn=None) == pa.PA_ERR_INVALID
+    assert ab(H=0) == pa.PA_ERR_INVALID
+    assert ab(dh=96) == pa.PA_ERR_UNSUPPORTED
+    assert ab(dr=4) == pa.PA_ERR_UNSUPPORTED
+    assert ab(w=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert ab(B=0) == pa.PA_OK
+    pr = lambda **kw: lib.pa_mla_project_out(*[dict(dict(y=FAKE, x=FAKE, w=FAKE, B=4, H=128,
+                                                         dc=512, dv=128), **kw)[k]
+                                               for k in ("y", "x", "w", "B", "H", "dc", "dv")],
+                                             None)
+    assert pr(w=None) == pa.PA_ERR_INVALID
+    assert pr(dv=100) == pa.PA_ERR_UNSUPPORTED
+    assert pr(x=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert pr(B=0) == pa.PA_OK

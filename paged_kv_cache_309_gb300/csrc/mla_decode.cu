@@ -16,17 +16,19 @@
 //    the head count is not a multiple of 64).  Head tiles of one (split,
 //    sequence) are adjacent in the launch order, so the second reads the
 //    latent rows from L2.
-//  * the split's tokens stream in tiles (32 tokens for 64 heads, 64 for 16)
-//    through a TMA ring: per (block piece, 64-element chunk) one [rows x
+//  * the split's tokens stream in tiles of 32 through a TMA ring (3 stages
+//    for 64 heads; for 16 heads 2 stages and two CTAs per SM): per (block piece, 64-element chunk) one [rows x
 //    128 B] box, 128-byte swizzled, completion on an mbarrier; a per-tile
 //    mask marks the rows that exist.  There is no producer warp: every tile
 //    ends in a CTA barrier, after which the previous tile's stage is free,
 //    so warp 0 refills it there (q_lat and the first stages at the start).
-//    Eight warps of 256 threads leave each thread up to 255 registers.
+//    Eight warps of 256 threads leave each thread up to 255 registers (64
+//    heads, one CTA per SM) or 128 (16 heads, two CTAs per SM).
 //  * eight warps per tile: (1) S = Q . K^T on the tensor cores
 //    (mma.sync m16n8k16, bf16 in, fp32 accumulate; heads on M, each warp a
-//    16-head x 16-token (or 16 x 8) block over all 576 elements) written to
-//    a double-buffered fp32 score tile in shared memory; (2) one barrier;
+//    16-head x 16-token block over all 576 elements, or for 16 heads a
+//    16 x 8 block over half of them) written to a double-buffered fp32
+//    score tile in shared memory; (2) one barrier;
 //    (3) each warp takes 16 heads x (512 / warps per head block) output
 //    elements: reads its heads' scores straight into the A-fragment
 //    positions, runs an fp32 online softmax in base 2 with a lazy rescale
@@ -67,22 +69,27 @@ constexpr size_t kWorkspaceHeader = 256;
 template <int HT>
 struct MlaCfg {
   static constexpr int kMB = HT / 16;                   // 16-head blocks
-  static constexpr int kTile = HT == 64 ? 32 : 64;      // tokens per stage
+  static constexpr int kTile = 32;                      // tokens per stage
   static constexpr int kStages = HT == 64 ? 3 : 2;
+  static constexpr int kCtasPerSm = HT == 64 ? 1 : 2;  // 16 heads: two CTAs hide each other's barriers
   static constexpr int kWarpsPerMB = kWarps / kMB;      // 2 or 8
-  static constexpr int kSTok = kTile / kWarpsPerMB;     // tokens per warp in S: 16 or 8
+  // S: a 16-head block's warps split the tile's tokens into kTokGroups
+  // groups and, for 16 heads, the 576-element reduction into two halves
+  static constexpr int kKSplit = HT == 64 ? 1 : 2;
+  static constexpr int kTokGroups = kWarpsPerMB / kKSplit;  // 2 or 4
+  static constexpr int kSTok = kTile / kTokGroups;      // tokens per warp in S: 16 or 8
   static constexpr int kDW = kLat / kWarpsPerMB;        // output elements per warp: 256 or 64
   static constexpr int kQBytes = kChunks * HT * 128;
   static constexpr int kChunkBytes = kTile * 128;
   static constexpr int kStageBytes = kChunks * kChunkBytes;
   static constexpr int kSStride = kTile + 8;            // floats per score row
-  static constexpr int kSBytes = HT * kSStride * 4;
+  static constexpr int kSBytes = kKSplit * HT * kSStride * 4;  // one partial per k-half
   static constexpr int kStageOff = kQBytes;
   static constexpr int kSOff = kStageOff + kStages * kStageBytes;
   static constexpr int kBarOff = kSOff + 2 * kSBytes;
   static constexpr int kBytes = kBarOff + (2 * kStages + 1) * 8 + 16;  // full, mask, q, flags
   static constexpr int kAlloc = kBytes + 1024;
-  static_assert(kAlloc <= 227 * 1024, "shared memory");
+  static_assert(kAlloc * kCtasPerSm <= 227 * 1024, "shared memory");
   static_assert(kSTok == 16 || kSTok == 8, "S split");
 };
 
@@ -206,7 +213,7 @@ __device__ __forceinline__ void mla_issue_tile(const MlaParams& p, const CUtenso
 }
 
 template <int HT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
     mla_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
   using C = MlaCfg<HT>;
@@ -289,8 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // lane-constant parts of the ldmatrix addresses
   const int qrow = 16 * mb + (lane & 15);  // Q: A operand rows
   const int qhalf = lane >> 4;             //    second 8 columns of a k-step
-  const int krow = C::kSTok == 16 ? wi * 16 + (lane & 7) + ((lane >> 4) << 3)
-                                  : wi * 8 + (lane & 7);
+  const int tg = wi % C::kTokGroups;  // S: token group
+  const int kh = wi / C::kTokGroups;  // S: half of the 576-element reduction
+  const int krow = C::kSTok == 16 ? tg * 16 + (lane & 7) + ((lane >> 4) << 3)
+                                  : tg * 8 + (lane & 7);
   const int khalf = C::kSTok == 16 ? ((lane >> 3) & 1) : (lane >> 3);
   const int vrow_l = (lane & 7) + (((lane >> 3) & 1) << 3);  // V: token within the k-step
   const int vhalf = lane >> 4;                               //    second 8 elements
@@ -301,19 +310,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int stage = t % kStages;
     const bool w_ok = mbar_wait_bounded(&full[stage], (t / kStages) & 1, nullptr);
     const uint32_t st_base = smem_base + C::kStageOff + stage * C::kStageBytes;
-    float* S = s_tile + (t & 1) * (HT * C::kSStride);
+    float* S = s_tile + (t & 1) * (C::kKSplit * HT * C::kSStride);
     uint64_t mask = 0;
     if (__all_sync(0xffffffffu, w_ok)) {
       mask = tile_mask[stage];
       // ---- S = Q . K^T for 16 heads x kSTok tokens over the 576 elements
       constexpr int NTS = C::kSTok / 8;
-      float sacc[NTS][4];
+      float sacc[NTS][4], sacc2[1][4];  // sacc2: a second chain for 8-token blocks
 #pragma unroll
       for (int nt = 0; nt < NTS; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) sacc[nt][c] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sacc2[0][c] = 0.f;
+      constexpr int kSteps = kChunks * 4 / C::kKSplit;  // 16-wide k-steps per warp
 #pragma unroll 3
-      for (int kc = 0; kc < kChunks * 4; kc += 2) {
+      for (int kc = kh * kSteps; kc < (kh + 1) * kSteps; kc += 2) {
         const int c = kc >> 2;
         const int j = kc & 3;  // k-steps j and j + 1 of chunk c
         const uint32_t qreg = smem_base + c * HT * 128;
@@ -333,20 +345,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           ldsm_x4(swz(qreg, qrow, 2 * j + 2 + qhalf), a1);
           ldsm_x4(swz(kreg, krow, 2 * j + khalf), bb);
           mma_bf16_16816(sacc[0], a0, bb[0], bb[1]);
-          mma_bf16_16816(sacc[0], a1, bb[2], bb[3]);
+          mma_bf16_16816(sacc2[0], a1, bb[2], bb[3]);
         }
       }
 #pragma unroll
       for (int nt = 0; nt < NTS; ++nt) {
-        const int col = wi * C::kSTok + nt * 8 + 2 * tq;
-        float* r0 = S + (16 * mb + gq) * C::kSStride + col;
+        const int col = tg * C::kSTok + nt * 8 + 2 * tq;
+        float* r0 = S + (kh * HT + 16 * mb + gq) * C::kSStride + col;
         float* r1 = r0 + 8 * C::kSStride;
+        if constexpr (NTS == 1) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) sacc[nt][c] += sacc2[0][c];
+        }
         *reinterpret_cast<float2*>(r0) = make_float2(sacc[nt][0], sacc[nt][1]);
         *reinterpret_cast<float2*>(r1) = make_float2(sacc[nt][2], sacc[nt][3]);
       }
       // rows of this warp's tokens that hold no token: zero their value
       // part (0 x NaN would poison P . V); their scores are masked below
-      const uint32_t my_mask = static_cast<uint32_t>(mask >> (wi * C::kSTok)) &
+      const uint32_t my_mask = static_cast<uint32_t>(mask >> (tg * C::kSTok)) &
                                ((1u << C::kSTok) - 1u);
       if (my_mask != (1u << C::kSTok) - 1u) {
         uint8_t* st = smem + C::kStageOff + stage * C::kStageBytes;
@@ -354,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int rr = idx >> 6, unit = idx & 63;  // 64 units of 16 B = 512 elements
           if (!((my_mask >> rr) & 1u))
             *reinterpret_cast<uint4*>(st + (unit >> 3) * C::kChunkBytes +
-                                      (wi * C::kSTok + rr) * 128 + ((unit & 7) << 4)) =
+                                      (tg * C::kSTok + rr) * 128 + ((unit & 7) << 4)) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();  // generic writes before the stage's next TMA fill
@@ -379,8 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows gq (r = 0) and gq + 8 (r = 1), columns 2tq, 2tq+1, 2tq+8, 2tq+9
     auto load_scores = [&](int kk, int r, float (&x)[4]) {
       const float* row = S + (16 * mb + gq + 8 * r) * C::kSStride + 16 * kk + 2 * tq;
-      const float2 x0 = *reinterpret_cast<const float2*>(row);
-      const float2 x1 = *reinterpret_cast<const float2*>(row + 8);
+      float2 x0 = *reinterpret_cast<const float2*>(row);
+      float2 x1 = *reinterpret_cast<const float2*>(row + 8);
+      if constexpr (C::kKSplit == 2) {  // the other half of the reduction
+        const float2 y0 = *reinterpret_cast<const float2*>(row + HT * C::kSStride);
+        const float2 y1 = *reinterpret_cast<const float2*>(row + HT * C::kSStride + 8);
+        x0 = make_float2(x0.x + y0.x, x0.y + y0.y);
+        x1 = make_float2(x1.x + y1.x, x1.y + y1.y);
+      }
       const uint32_t bits = static_cast<uint32_t>(mask >> (16 * kk + 2 * tq));
       x[0] = (bits & 1u) ? x0.x * p.scale_log2 : -INFINITY;
       x[1] = (bits & 2u) ? x0.y * p.scale_log2 : -INFINITY;
@@ -547,7 +569,8 @@ DecodePlan make_mla_plan(int32_t num_seqs, int32_t num_heads, int32_t max_contex
   if (max_context_len <= 0 || num_seqs <= 0 || num_heads <= 0) return {1, tile};
   const int64_t tiles_max = (static_cast<int64_t>(max_context_len) + tile - 1) / tile;
   const int64_t work = static_cast<int64_t>(num_seqs) * (num_heads / ht);
-  const int64_t target = 4ll * num_sms;  // one CTA per SM: about four waves
+  const int per_sm = ht == 64 ? MlaCfg<64>::kCtasPerSm : MlaCfg<16>::kCtasPerSm;
+  const int64_t target = 4ll * num_sms * per_sm;  // about four waves of resident CTAs
   int64_t splits = (target + work - 1) / work;
   if (splits < 1) splits = 1;
   if (splits > tiles_max) splits = tiles_max;

@@ -46,7 +46,7 @@
 #include <atomic>
 #include <cmath>
 
-#include "pa_internal.cuh"
+#include "mla_common.cuh"
 
 namespace pa_detail {
 
@@ -55,16 +55,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // decode.cu
 namespace {
 
 using namespace pa;
+using namespace mla;
 
-constexpr int kLat = 512;                 // latent elements (the value part)
-constexpr int kRope = 64;                 // rope elements
-constexpr int kRow = kLat + kRope;        // 576 elements per cache row
-constexpr int kRowBytes = kRow * 2;       // 1152 bytes
-constexpr int kChunks = kRow / 64;        // nine 64-element (128-byte) chunks
 constexpr int kWarps = 8;                 // all warps compute; warp 0 also issues the loads
 constexpr int kThreads = kWarps * 32;
-constexpr float kRescaleLog2 = 8.0f;
-constexpr size_t kWorkspaceHeader = 256;
 
 template <int HT>
 struct MlaCfg {
@@ -93,123 +87,14 @@ struct MlaCfg {
   static_assert(kSTok == 16 || kSTok == 8, "S split");
 };
 
-struct MlaParams {
-  __nv_bfloat16* out;  // [B, H, 512]
-  const int32_t* block_tables;
-  const int32_t* context_lens;
-  float* ws_lse;       // [B, H, splits]
-  float* ws_o;         // [B, H, splits, 512]
-  unsigned* counters;  // [B, H / HT]
-  unsigned* err;
-  int64_t num_blocks;
-  int32_t num_heads;
-  int32_t block_size;
-  int32_t log2_bs;
-  int32_t max_blocks_per_seq;
-  int32_t num_splits;
-  int32_t tokens_per_split;
-  int32_t kv_evict_first;  // one head tile per sequence: nobody re-reads the rows
-  float scale_log2;
-};
-
-__device__ __forceinline__ int mla_effective_len(const MlaParams& p, int b, bool* clipped) {
-  int L = __ldg(p.context_lens + b);
-  L = L < 0 ? 0 : L;
-  const int64_t cap = min(static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size,
-                          static_cast<int64_t>(p.num_splits) * p.tokens_per_split);
-  *clipped = static_cast<int64_t>(L) > cap;
-  return *clipped ? static_cast<int>(cap) : L;
-}
-
-// swizzled address of 16-byte unit `unit` of row `row` in a [rows x 128 B] region
-__device__ __forceinline__ uint32_t swz(uint32_t region, int row, int unit) {
-  return region + static_cast<uint32_t>(row * 128 + ((unit ^ (row & 7)) << 4));
-}
-
-// Merge of one (sequence, head) row by one warp over n splits: weights
-// 2^(lse_s - max), out = sum_s w_s o_s / sum_s w_s in bf16.  Lane owns
-// elements 4*lane + 128*i, i = 0..3.
-__device__ __forceinline__ void mla_merge_warp(const MlaParams& p, int64_t bh, int n, int lane) {
-  const float* lse = p.ws_lse + bh * p.num_splits;
-  const float* o = p.ws_o + bh * p.num_splits * kLat;
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, __ldcg(lse + s));
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float4 acc[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float W = 0.f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < n; s0 += 32) {
-      const int my = s0 + lane;
-      const float wl = my < n ? exp2f(__ldcg(lse + my) - M) : 0.f;
-      const int cnt = min(32, n - s0);
-      for (int k = 0; k < cnt; ++k) {
-        const float w = __shfl_sync(0xffffffffu, wl, k);
-        const float4* src = reinterpret_cast<const float4*>(o + static_cast<int64_t>(s0 + k) * kLat);
-        W += w;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = __ldcg(src + lane + 32 * i);
-          acc[i].x += w * v.x;
-          acc[i].y += w * v.y;
-          acc[i].z += w * v.z;
-          acc[i].w += w * v.w;
-        }
-      }
-    }
-  }
-  const float inv = W > 0.f ? 1.f / W : 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    *reinterpret_cast<uint2*>(p.out + bh * kLat + 4 * lane + 128 * i) =
-        make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
-                   pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
-}
-
-// Loads of one tile (called by warp 0, all lanes): lane i < nbox looks up
-// block piece i of the tile, the lanes agree on the tile's row mask, lane 0
-// posts it and the byte count, and each lane with a valid piece issues one
-// TMA box per 64-element chunk.
 template <int HT>
 __device__ __forceinline__ void mla_issue_tile(const MlaParams& p, const CUtensorMap* tm_kv,
                                                uint8_t* smem, uint64_t* full, uint64_t* tile_mask,
                                                const int32_t* bt, int tok0, int tok_end, int stage,
                                                uint64_t pol, int lane) {
   using C = MlaCfg<HT>;
-  const int bs = p.block_size;
-  const int rpb = bs < C::kTile ? bs : C::kTile;
-  const int nbox = C::kTile / rpb;
-  const int nval = min(C::kTile, tok_end - tok0);
-  bool valid = false;
-  int rows = 0, bid = -1, row0 = 0;
-  if (lane < nbox) {
-    const int first = tok0 + lane * rpb;
-    rows = min(rpb, nval - lane * rpb);
-    if (rows > 0) {
-      row0 = first & (bs - 1);
-      bid = __ldg(bt + (first >> p.log2_bs));
-      valid = bid >= 0 && static_cast<int64_t>(bid) < p.num_blocks;
-    }
-  }
-  uint64_t bits = 0;
-  if (valid) bits = (rows >= 64 ? ~0ull : ((1ull << rows) - 1ull)) << (lane * rpb);
-  const uint32_t lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits));
-  const uint32_t hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits >> 32));
-  const uint32_t vb = __ballot_sync(0xffffffffu, valid);
-  if (lane == 0) {
-    tile_mask[stage] = (static_cast<uint64_t>(hi) << 32) | lo;
-    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(__popc(vb) * rpb * kRowBytes));
-  }
-  __syncwarp();
-  if (valid) {
-    const int32_t row = bid * bs + row0;
-    uint8_t* st = smem + C::kStageOff + stage * C::kStageBytes + lane * rpb * 128;
-#pragma unroll 1
-    for (int c = 0; c < kChunks; ++c)
-      tma_load_2d(st + c * C::kChunkBytes, tm_kv, 64 * c, row, &full[stage], pol);
-  }
+  mla_issue_tile_at(p, tm_kv, smem + C::kStageOff + stage * C::kStageBytes, C::kChunkBytes,
+                    C::kTile, &full[stage], &tile_mask[stage], bt, tok0, tok_end, pol, lane);
 }
 
 template <int HT>
@@ -559,17 +444,21 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 
-int mla_head_tile(int32_t num_heads) { return num_heads % 64 == 0 ? 64 : 16; }
+// 128: the tcgen05 kernel (mla_decode_tc.cu); 64 / 16: the mma.sync kernel
+int mla_head_tile(int32_t num_heads) {
+  return num_heads % 128 == 0 ? 128 : num_heads % 64 == 0 ? 64 : 16;
+}
 
 DecodePlan make_mla_plan(int32_t num_seqs, int32_t num_heads, int32_t max_context_len,
                          int32_t num_sms) {
   if (num_sms <= 0) num_sms = 148;
   const int ht = mla_head_tile(num_heads);
-  const int tile = ht == 64 ? MlaCfg<64>::kTile : MlaCfg<16>::kTile;
+  const int tile = ht == 128 ? mla_tc_tile() : ht == 64 ? MlaCfg<64>::kTile : MlaCfg<16>::kTile;
   if (max_context_len <= 0 || num_seqs <= 0 || num_heads <= 0) return {1, tile};
   const int64_t tiles_max = (static_cast<int64_t>(max_context_len) + tile - 1) / tile;
-  const int64_t work = static_cast<int64_t>(num_seqs) * (num_heads / ht);
-  const int per_sm = ht == 64 ? MlaCfg<64>::kCtasPerSm : MlaCfg<16>::kCtasPerSm;
+  // CTAs per split index (a pair per 128-head tile)
+  const int64_t work = static_cast<int64_t>(num_seqs) * (num_heads / ht) * (ht == 128 ? 2 : 1);
+  const int per_sm = ht == 16 ? MlaCfg<16>::kCtasPerSm : 1;
   const int64_t target = 4ll * num_sms * per_sm;  // about four waves of resident CTAs
   int64_t splits = (target + work - 1) / work;
   if (splits < 1) splits = 1;
@@ -594,7 +483,7 @@ size_t mla_workspace_bytes(int32_t num_seqs, int32_t num_heads, const DecodePlan
 pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0) return PA_OK;
   const int ht = mla_head_tile(a.num_heads);
-  const int tile = ht == 64 ? MlaCfg<64>::kTile : MlaCfg<16>::kTile;
+  const int tile = ht == 128 ? mla_tc_tile() : ht == 64 ? MlaCfg<64>::kTile : MlaCfg<16>::kTile;
   const int32_t box_rows = a.block_size < tile ? a.block_size : tile;
   CUtensorMap mq, mkv;
   if (!make_row576_map(&mq, a.q_latent, static_cast<int64_t>(a.num_seqs) * a.num_heads, ht) ||
@@ -620,8 +509,13 @@ pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.num_splits = a.plan.num_splits;
   p.tokens_per_split = a.plan.tokens_per_split;
-  p.kv_evict_first = a.num_heads == ht ? 1 : 0;
+  p.kv_evict_first = (a.num_heads == ht && ht != 128) ? 1 : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
+  if (ht == 128) {
+    const dim3 grid(static_cast<unsigned>(2 * (a.num_heads / ht)),
+                    static_cast<unsigned>(a.plan.num_splits), static_cast<unsigned>(a.num_seqs));
+    return launch_mla_tc(mq, mkv, p, grid, stream);
+  }
   const dim3 grid(static_cast<unsigned>(a.num_heads / ht), static_cast<unsigned>(a.plan.num_splits),
                   static_cast<unsigned>(a.num_seqs));
   return ht == 64 ? launch_mla_split<64>(mq, mkv, p, grid, stream)

@@ -69,10 +69,11 @@ def all_rows(w):
     return [(b, h) for b in range(w.num_seqs) for h in range(w.num_heads)]
 
 
-@pytest.mark.parametrize("H", [16, 32, 48, 64, 128])
+@pytest.mark.parametrize("H", [16, 32, 48, 64, 128, 256])
 def test_mla_head_counts_every_row(H):
-    """Head tiles of 16 (H = 16, 32, 48) and 64 (H = 64, 128); ragged
-    contexts including 1 and a partial last tile."""
+    """mma.sync head tiles of 16 (H = 16, 32, 48) and 64 (H = 64), tcgen05
+    tiles of 128 (H = 128, 256); ragged contexts including 1 and a partial
+    last tile."""
     w = wl.make_mla_decode(f"h{H}", 200 + H, 3, 1, 1, H, block_size=64,
                            context_lens=[1, 97, 300], with_weights=False)
     got, err = gpu_mla(w)
@@ -81,14 +82,15 @@ def test_mla_head_counts_every_row(H):
         check_attn(got[key], r, ab, key)
 
 
+@pytest.mark.parametrize("H", [64, 128])
 @pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 256])
-def test_mla_block_sizes_ragged(bs):
-    w = wl.make_mla_decode(f"bs{bs}", 210 + bs, 5, 1, 1, 64, block_size=bs,
+def test_mla_block_sizes_ragged(bs, H):
+    w = wl.make_mla_decode(f"bs{bs}", 210 + bs, 5, 1, 1, H, block_size=bs,
                            context_lens=[0, 1, 64, 65, 531], with_weights=False)
     got, err = gpu_mla(w, max_context_len=600)
     assert err == 0
     assert (got[0] == 0).all()
-    rows = [(b, h) for b in range(1, 5) for h in (0, 17, 63)]
+    rows = [(b, h) for b in range(1, 5) for h in (0, 17, H - 1)]
     for key, (r, ab) in oracle_rows(w, rows).items():
         check_attn(got[key], r, ab, key)
 
@@ -105,7 +107,7 @@ def test_mla_decode_workload_sampled():
         check_attn(got[key], r, ab, key)
 
 
-@pytest.mark.parametrize("H", [16, 128])
+@pytest.mark.parametrize("H", [16, 64, 128])
 def test_mla_long_context_many_splits(H):
     w = wl.make_mla_decode(f"long{H}", 230 + H, 2, 1, 1, H, block_size=64,
                            context_lens=[20000, 7777], with_weights=False)

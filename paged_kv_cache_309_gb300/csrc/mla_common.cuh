@@ -23,6 +23,7 @@ constexpr size_t kWorkspaceHeader = 256;
 
 struct MlaParams {
   __nv_bfloat16* out;  // [B, H, 512]
+  const __nv_bfloat16* q_latent;  // [B, H, 576]
   const int32_t* block_tables;
   const int32_t* context_lens;
   float* ws_lse;       // [B, H, splits]
@@ -94,6 +95,61 @@ __device__ __forceinline__ void mla_merge_warp(const MlaParams& p, int64_t bh, i
     *reinterpret_cast<uint2*>(p.out + bh * kLat + 4 * lane + 128 * i) =
         make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
                    pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
+}
+
+// Merge of `nheads` (sequence, head) rows bh0 .. bh0 + nheads - 1 over n
+// splits by the whole CTA: weights w_s = 2^(lse_s - max) per head go to
+// shared memory `wsm` (nheads * n floats) once, then every thread owns
+// independent 4-element columns and sums its n partials with independent
+// loads (a warp per head would walk the splits one L2 round trip at a
+// time).  out = sum_s w_s o_s / sum_s w_s, in bf16.
+__device__ __forceinline__ void mla_merge_cta(const MlaParams& p, int64_t bh0, int nheads, int n,
+                                              float* wsm) {
+  for (int h = threadIdx.x; h < nheads; h += blockDim.x) {
+    const float* lse = p.ws_lse + (bh0 + h) * p.num_splits;
+    float M = -INFINITY;
+    for (int s = 0; s < n; ++s) M = fmaxf(M, __ldcg(lse + s));
+    float W = 0.f;
+    for (int s = 0; s < n; ++s) {
+      const float w = M == -INFINITY ? 0.f : exp2f(__ldcg(lse + s) - M);
+      wsm[h * n + s] = w;
+      W += w;
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    for (int s = 0; s < n; ++s) wsm[h * n + s] *= inv;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nheads * (kLat / 4); idx += blockDim.x) {
+    const int h = idx / (kLat / 4), e4 = idx % (kLat / 4);
+    const float4* src =
+        reinterpret_cast<const float4*>(p.ws_o + (bh0 + h) * p.num_splits * kLat) + e4;
+    const float* w = wsm + h * n;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 4 <= n; s += 4) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = __ldcg(src + (s + u) * (kLat / 4));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float ww = w[s + u];
+        acc.x += ww * x[u].x;
+        acc.y += ww * x[u].y;
+        acc.z += ww * x[u].z;
+        acc.w += ww * x[u].w;
+      }
+    }
+    for (; s < n; ++s) {
+      const float4 x = __ldcg(src + s * (kLat / 4));
+      const float ww = w[s];
+      acc.x += ww * x.x;
+      acc.y += ww * x.y;
+      acc.z += ww * x.z;
+      acc.w += ww * x.w;
+    }
+    *reinterpret_cast<uint2*>(p.out + (bh0 + h) * kLat + 4 * e4) =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
 }
 
 // Loads of one tile of `tile` tokens (called by one warp, all lanes): lane

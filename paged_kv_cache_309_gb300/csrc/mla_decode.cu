@@ -406,7 +406,11 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
   }
   __syncthreads();
   if (flags[0]) {
-    for (int h = warp; h < HT; h += kThreads / 32) mla_merge_warp(p, bh0 + h, n_valid, lane);
+    // the pipeline's shared memory is free now: per-head merge weights
+    if (HT * n_valid * 4 <= C::kStageBytes * kStages)
+      mla_merge_cta(p, bh0, HT, n_valid, reinterpret_cast<float*>(smem + C::kStageOff));
+    else
+      for (int h = warp; h < HT; h += kThreads / 32) mla_merge_warp(p, bh0 + h, n_valid, lane);
   }
 }
 
@@ -491,6 +495,7 @@ pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
     return PA_ERR_CUDA;
   MlaParams p;
   p.out = static_cast<__nv_bfloat16*>(a.out_latent);
+  p.q_latent = static_cast<const __nv_bfloat16*>(a.q_latent);
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);

@@ -12,36 +12,38 @@
 // Layout of the work (sm_103a):
 //  * 128 heads are the M dimension of every product (one TMEM lane per
 //    head).  The fp32 output of 128 heads x 512 elements would fill all 512
-//    TMEM columns, leaving none for the scores, so a PAIR of CTAs serves
-//    each (head tile, split, sequence): CTA v accumulates output elements
-//    256v .. 256v + 255 (256 columns) and both compute the whole score tile
-//    (the second one reads the latent rows from L2).  grid = (2 * H / 128,
-//    splits, B), the pair adjacent in launch order.
-//  * per CTA: q_lat of its 128 heads (9 chunks of 128 rows x 128 bytes,
-//    144 KB, the A operand of S) stays in shared memory; the split's tokens
-//    stream through a TMA ring in tiles of kTile (9 chunks of kTile rows x
-//    128 bytes), 128-byte swizzled, with as many stages as fit beside q_lat.
-//  * S[128 x 32] = Q . K^T: 36 tcgen05.mma (M=128, N=32, K=16, bf16 in,
-//    fp32 out) from K-major shared-memory descriptors into a double-buffered
-//    32-column TMEM tile.  O[128 x 256] += P . V: 2 tcgen05.mma (N=256)
-//    with P (bf16, [128 x 32]) from TMEM and V read in place from the same
-//    shared-memory tile as an MN-major operand (its 256 elements of each
-//    row are contiguous).
+//    TMEM columns, so a CLUSTER of two CTAs serves each (head tile, split,
+//    sequence), and CTA v (its rank in the cluster) owns one half of the
+//    row: latent elements 256v .. 256v + 255 (its half of the output) and
+//    rope elements 32v .. 32v + 31.  grid = (2 * H / 128, splits, B).
+//  * CTA v loads only its slice of every latent row (4 latent chunks and
+//    the rope chunk: 640 of the row's 1152 bytes) through an 8-stage TMA
+//    ring of 32-token tiles, 128-byte swizzled; its slice of q_lat (144
+//    TMEM columns of bf16 pairs) sits in tensor memory, so shared memory
+//    holds only the ring and two exchange buffers.
+//  * partial S[128 x 32] over the CTA's 288 elements: 18 tcgen05.mma
+//    (M=128, N=32, K=16) with A = q_lat from TMEM and B = the K-major tile
+//    in shared memory.  The softmax threads (thread = head row) read their
+//    32 partial scores (tcgen05.ld), send them to the other CTA's exchange
+//    buffer through distributed shared memory (st.async, counted in bytes
+//    on the other CTA's mbarrier), and add the other CTA's partials: both
+//    CTAs add the same two numbers, so both run the identical softmax.
+//  * O[128 x 256] += P . V: 2 tcgen05.mma (N=256) with P (bf16) from TMEM
+//    and V = the CTA's latent chunks read in place as an MN-major operand.
 //  * warp roles: warp 0 issues the TMA loads, warp 1 owns TMEM and issues
-//    the MMAs (one thread), warps 2-5 are the softmax: thread = head row,
-//    tcgen05.ld of its 32 scores, fp32 online softmax in base 2 with a lazy
-//    rescale (the running max moves only when a score beats it by more than
-//    2^8; the rescale reads, scales and writes back the TMEM output row),
-//    weights rounded to bf16 and written to TMEM with tcgen05.st.  S(t+1)
-//    runs on the tensor core while the softmax works on tile t.
+//    the MMAs from one thread (whichever of S(next) and P.V(next) is ready),
+//    warps 2-5 load q_lat into TMEM and then run the softmax: fp32, base 2,
+//    lazy rescale (the running max moves only when a score beats it by more
+//    than 2^8; the rescale reads, scales and writes back the TMEM output
+//    row), weights rounded to bf16 and written to TMEM with tcgen05.st.
 //  * epilogue: the softmax threads read their output row from TMEM; one
 //    split writes bf16, several write fp32 partials + log2-sum-exp, and the
 //    CTA that completes the per-(sequence, head tile) count (2 * splits
 //    arrivals) merges them.
 //
 // Every wait is bounded (2 s); a timeout sets an error bit, the roles leave
-// their loops, the MMAs and copies already issued are drained, and TMEM is
-// freed before the CTA exits.
+// their loops, the MMAs and copies already issued are drained, TMEM is
+// freed, and the two CTAs meet at a cluster barrier before either exits.
 #include <atomic>
 #include <cmath>
 
@@ -55,20 +57,21 @@ using namespace mla;
 
 constexpr int kHT = 128;               // heads per CTA (M)
 constexpr int kTile = 32;              // tokens per tile (N of S, K of P.V)
-// as many stages as fit beside the resident q_lat (144 KB)
-constexpr int kStages = kTile == 16 ? 4 : 2;
-constexpr int kHalf = kLat / 2;        // output elements per CTA (N of P.V)
+constexpr int kHalf = kLat / 2;        // output (and latent) elements per CTA
+constexpr int kRopeHalf = kRope / 2;   // rope elements per CTA
 constexpr int kThreads = 6 * 32;
-constexpr int kQChunkBytes = kHT * 128;              // 16 KB
-constexpr int kChunkBytes = kTile * 128;             // 4 KB
-constexpr int kStageBytes = kChunks * kChunkBytes;   // 36 KB
-constexpr int kQOff = 0;
-constexpr int kStageOff = kChunks * kQChunkBytes;    // 144 KB
-constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+constexpr int kChunkBytes = kTile * 128;             // one 64-element chunk of a tile: 4 KB
+constexpr int kLoadChunks = kHalf / 64 + 1;          // 4 latent chunks + the rope chunk
+constexpr int kStageBytes = kLoadChunks * kChunkBytes;  // 20 KB
+constexpr int kStages = 8;
+constexpr int kRecvBytes = kTile * kHT * 4;          // one tile of the peer's partial scores
+constexpr int kStageOff = 0;
+constexpr int kRecvOff = kStageOff + kStages * kStageBytes;
+constexpr int kBarOff = kRecvOff + 2 * kRecvBytes;
 // barriers: q_full, kv_full[kStages], kv_empty[kStages], s_full[2],
-// s_empty[2], p_full[2], pv_done[2], o_final, drain; then tile masks, the
-// TMEM slot and flags
-constexpr int kNumBars = 11 + 2 * kStages;
+// s_empty[2], p_full[2], pv_done[2], recv_full[2], sent_free[2], o_final,
+// drain; then tile masks, the TMEM slot and flags
+constexpr int kNumBars = 15 + 2 * kStages;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
 constexpr int kMiscOff = kMaskOff + kStages * 8;
 constexpr int kBytes = kMiscOff + 32;
@@ -78,8 +81,9 @@ static_assert(kAlloc <= 227 * 1024, "shared memory");
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;      // [0, 256): this CTA's half of the output
-constexpr uint32_t kSCol = 256;    // two kTile-column score tiles
-constexpr uint32_t kPCol = 320;    // two kTile/2-column weight tiles (bf16 pairs)
+constexpr uint32_t kQCol = 256;    // [256, 400): this CTA's half of q_lat (bf16 pairs)
+constexpr uint32_t kSCol = 400;    // [400, 464): two 32-column partial-score tiles
+constexpr uint32_t kPCol = 464;    // [464, 496): two 16-column weight tiles (bf16 pairs)
 
 // ------------------------------------------------------------ tcgen05 ops --
 // Shared-memory matrix descriptor: start, leading and stride byte offsets
@@ -101,14 +105,6 @@ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major) {
 constexpr uint32_t kIdescS = instr_desc(kHT, kTile, false);
 constexpr uint32_t kIdescPV = instr_desc(kHT, kHalf, true);
 
-__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 __device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -146,22 +142,7 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-// 16 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 __device__ __forceinline__ void tc_ld(uint32_t taddr, float (&v)[32]) { tc_ld32(taddr, v); }
-__device__ __forceinline__ void tc_ld(uint32_t taddr, float (&v)[16]) { tc_ld16(taddr, v); }
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -174,6 +155,18 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tc_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -183,38 +176,136 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16])
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void tc_st(uint32_t taddr, const uint32_t (&r)[16]) { tc_st16(taddr, r); }
-__device__ __forceinline__ void tc_st(uint32_t taddr, const uint32_t (&r)[8]) { tc_st8(taddr, r); }
+
+// ---------------------------------------------------------- cluster ops --
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+// asynchronous 16-byte store into the other CTA's shared memory; its
+// completion is counted (16 bytes) on that CTA's mbarrier `bar`
+__device__ __forceinline__ void st_async_peer(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+// 2^x on the multi-function unit (ex2.approx: relative error ~2^-22, far
+// below the bf16 rounding the weights get next)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// arrival on the other CTA's barrier without release ordering: used where
+// the only prior accesses to order are loads whose values are already in use
+__device__ __forceinline__ void arrive_peer_relaxed(uint32_t bar_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait (2 s, or earlier once *abort_flag is set) for a phase whose
+// arrivals come from the other CTA of the cluster
+__device__ __forceinline__ bool wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                     volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63u) == 0u) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+  }
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+// Loads of one tile (one warp, all lanes): like mla_issue_tile_at, but only
+// this CTA's chunks: latent chunks 4v .. 4v + 3 and the rope chunk, into
+// slots 0..4 of the stage.
+__device__ __forceinline__ void issue_half_tile(const MlaParams& p, const CUtensorMap* tm_kv,
+                                                uint8_t* stage, uint64_t* full,
+                                                uint32_t* mask_slot, const int32_t* bt, int tok0,
+                                                int tok_end, int v, uint64_t pol, int lane) {
+  const int bs = p.block_size;
+  const int rpb = bs < kTile ? bs : kTile;
+  const int nbox = kTile / rpb;
+  const int nval = min(kTile, tok_end - tok0);
+  bool valid = false;
+  int rows = 0, bid = -1, row0 = 0;
+  if (lane < nbox) {
+    const int first = tok0 + lane * rpb;
+    rows = min(rpb, nval - lane * rpb);
+    if (rows > 0) {
+      row0 = first & (bs - 1);
+      bid = __ldg(bt + (first >> p.log2_bs));
+      valid = bid >= 0 && static_cast<int64_t>(bid) < p.num_blocks;
+    }
+  }
+  uint32_t bits = 0;
+  if (valid) bits = (rows >= 32 ? ~0u : ((1u << rows) - 1u)) << (lane * rpb);
+  const uint32_t mask = __reduce_or_sync(0xffffffffu, bits);
+  const uint32_t vb = __ballot_sync(0xffffffffu, valid);
+  if (lane == 0) {
+    *mask_slot = mask;
+    mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vb) * rpb * kLoadChunks * 128));
+  }
+  __syncwarp();
+  if (valid) {
+    const int32_t row = bid * bs + row0;
+    uint8_t* st = stage + lane * rpb * 128;
+#pragma unroll 1
+    for (int c = 0; c < kLoadChunks; ++c) {
+      const int chunk = c < 4 ? 4 * v + c : kChunks - 1;
+      tma_load_2d(st + c * kChunkBytes, tm_kv, 64 * chunk, row, full, pol);
+    }
+  }
+}
 
 // ------------------------------------------------------------------ kernel --
-__global__ void __launch_bounds__(kThreads, 1)
-    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;                 // [kStages] tile landed
-  uint64_t* kv_empty = kv_full + kStages;       // [kStages] P.V of the stage's tile done (commit)
-  uint64_t* s_full = kv_empty + kStages;        // [2] scores in TMEM (commit)
-  uint64_t* s_empty = s_full + 2;               // [2] scores read (128 softmax threads)
-  uint64_t* p_full = s_empty + 2;               // [2] weights in TMEM (128 softmax threads)
-  uint64_t* pv_done = p_full + 2;               // [2] P.V done (commit)
-  uint64_t* o_final = pv_done + 2;              // every product done (commit)
-  uint64_t* drain = o_final + 1;                // error path: issued products done
-  uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);
+  uint64_t* q_full = bars + 0;                   // q_lat half in TMEM (128 threads)
+  uint64_t* kv_full = bars + 1;                  // [kStages] tile landed
+  uint64_t* kv_empty = kv_full + kStages;        // [kStages] P.V of the stage's tile done
+  uint64_t* s_full = kv_empty + kStages;         // [2] partial scores in TMEM (commit)
+  uint64_t* s_empty = s_full + 2;                // [2] partial scores read (128 threads)
+  uint64_t* p_full = s_empty + 2;                // [2] weights in TMEM (128 threads)
+  uint64_t* pv_done = p_full + 2;                // [2] P.V done (commit)
+  uint64_t* recv_full = pv_done + 2;             // [2] the peer's partials landed here (peer's 128)
+  uint64_t* sent_free = recv_full + 2;           // [2] the peer consumed what we sent (peer's 128)
+  uint64_t* o_final = sent_free + 2;             // every product done (commit)
+  uint64_t* drain = o_final + 1;                 // error path: issued products done
+  uint32_t* tile_mask = reinterpret_cast<uint32_t*>(smem + kMaskOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);  // [0] abort, [1] last CTA
 
   const int ht = blockIdx.x >> 1;  // 128-head tile
-  const int v = blockIdx.x & 1;    // output half
+  const int v = static_cast<int>(cluster_rank());  // output half = element slice
   const int split = blockIdx.y;
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
@@ -228,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
   const int tok_begin = split * p.tokens_per_split;
   const int tok_end = min(tok_begin + p.tokens_per_split, L);
-  if (tok_begin >= tok_end) {
+  if (tok_begin >= tok_end) {  // both CTAs of the cluster leave here together
     if (split == 0) {  // L == 0: zero rows (this CTA's half)
       for (int i = threadIdx.x; i < kHT * (kHalf / 8); i += kThreads) {
         const int h = i / (kHalf / 8), c = i % (kHalf / 8);
@@ -241,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (tok_end - tok_begin + kTile - 1) / kTile;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, kHT);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
@@ -251,12 +342,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_empty[s], kHT);
       mbar_init(&p_full[s], kHT);
       mbar_init(&pv_done[s], 1);
+      mbar_init(&recv_full[s], 1);   // armed with the byte count by this CTA
+      mbar_init(&sent_free[s], 4);   // one arrival per softmax warp of the other CTA
     }
     mbar_init(o_final, 1);
     mbar_init(drain, 1);
     flags[0] = 0;
     flags[1] = 0;
     mbar_init_fence();
+    // the first two exchanges: expect one tile of partials in each buffer
+    mbar_arrive_expect_tx(&recv_full[0], kRecvBytes);
+    mbar_arrive_expect_tx(&recv_full[1], kRecvBytes);
   }
   if (warp == 1) {  // this warp owns the CTA's tensor memory
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -266,25 +362,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  // both CTAs' barriers are initialised before either arrives on the other's
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* abort_flag = flags;
   const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+  const uint32_t peer = static_cast<uint32_t>(v ^ 1);
   int issued = 0;
 
   if (warp == 0) {
     // -------------------------------------------------------- TMA producer
-    const uint64_t pol = l2_policy_evict_normal();  // the pair's second CTA re-reads the rows
-    if (lane == 0) {
-      prefetch_tensormap(&tm_q);
-      prefetch_tensormap(&tm_kv);
-      mbar_arrive_expect_tx(q_full, kHT * kRowBytes);
-#pragma unroll 1
-      for (int c = 0; c < kChunks; ++c)
-        tma_load_2d(smem + kQOff + c * kQChunkBytes, &tm_q, 64 * c, b * p.num_heads + h0, q_full,
-                    pol);
-    }
+    const uint64_t pol = l2_policy_evict_first();  // each row is read once (the rope chunk twice)
+    if (lane == 0) prefetch_tensormap(&tm_kv);
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % kStages;
@@ -293,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_wait_bounded(&kv_empty[stage], ((t / kStages) - 1) & 1, abort_flag));
         if (!ok) break;
       }
-      mla_issue_tile_at(p, &tm_kv, smem + kStageOff + stage * kStageBytes, kChunkBytes, kTile,
-                        &kv_full[stage], &tile_mask[stage], bt, tok_begin + t * kTile, tok_end,
-                        pol, lane);
+      issue_half_tile(p, &tm_kv, smem + kStageOff + stage * kStageBytes, &kv_full[stage],
+                      &tile_mask[stage], bt,
+                      tok_begin + t * kTile, tok_end, v, pol, lane);
       issued = t + 1;
     }
     if (!ok && lane == 0) {
@@ -305,30 +395,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t q_base = smem_u32(smem + kQOff);
       const uint32_t st_base = smem_u32(smem + kStageOff);
-      // O[:, this half] += P(u) . V(u): V = elements 256v.. of tile u's rows,
-      // MN-major (leading offset: next 64 elements = next chunk; stride
-      // offset: next 8 tokens = 1 KB); P from TMEM, 16 tokens per product
       auto issue_s = [&](int t) {
-        // S(t) = Q . K(t)^T over 36 k-steps of 16 (K-major, 128-byte swizzle:
-        // a k-step inside a 64-element chunk advances the start by 32 bytes)
+        // partial S(t) = Q_v . K_v(t)^T over this CTA's 288 elements: 16
+        // latent k-steps (chunk slots 0..3) and 2 rope k-steps (slot 4,
+        // elements 32v .. 32v + 31); A = q_lat half in TMEM, B = K-major
+        // 128-byte-swizzled tile (a k-step advances the start by 32 bytes)
         const uint32_t kb = st_base + (t % kStages) * kStageBytes;
-#pragma unroll 4
-        for (int kc = 0; kc < kChunks * 4; ++kc) {
-          const int c = kc >> 2, j = kc & 3;
-          tc_mma_ss(tmem + kSCol + kTile * (t & 1),
-                    smem_desc(q_base + c * kQChunkBytes + 32 * j, 16, 1024),
-                    smem_desc(kb + c * kChunkBytes + 32 * j, 16, 1024), kIdescS,
-                    kc > 0 ? 1u : 0u);
-        }
+        const uint32_t d = tmem + kSCol + kTile * (t & 1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          tc_mma_ts(d, tmem + kQCol + 8 * i,
+                    smem_desc(kb + (i >> 2) * kChunkBytes + 32 * (i & 3), 16, 1024), kIdescS,
+                    i > 0 ? 1u : 0u);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          tc_mma_ts(d, tmem + kQCol + 128 + 8 * i,
+                    smem_desc(kb + 4 * kChunkBytes + 64 * v + 32 * i, 16, 1024), kIdescS, 1u);
         tc_commit(&s_full[t & 1]);
       };
       auto issue_pv = [&](int u) {
-        // O[:, this half] += P(u) . V(u): V = elements 256v.. of tile u's
-        // rows, MN-major (leading offset: next 64 elements = next chunk;
-        // stride offset: next 8 tokens = 1 KB); P from TMEM, 16 tokens each
-        const uint32_t vb = st_base + (u % kStages) * kStageBytes + 4 * v * kChunkBytes;
+        // O[:, this half] += P(u) . V(u): V = slots 0..3 of tile u, MN-major
+        // (leading offset: next 64 elements = next slot; stride offset: next
+        // 8 tokens = 1 KB); P from TMEM, 16 tokens per product
+        const uint32_t vb = st_base + (u % kStages) * kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           tc_mma_ts(tmem + kOCol, tmem + kPCol + (kTile / 2) * (u & 1) + 8 * kk,
@@ -341,19 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // other could go: S(ns) needs its tile and its score buffer (read by
       // the softmax two tiles ago), P.V(npv) needs the softmax's weights.
       bool ok = mbar_wait_bounded(q_full, 0, abort_flag);
+      tc_fence_after();
       int ns = 0, npv = 0;
       uint64_t idle_since = 0;
       uint32_t idle = 0;
       while (ok && npv < ntiles) {
         bool progressed = false;
-        if (ns < ntiles && mbar_try_wait(&kv_full[ns % kStages], (ns / kStages) & 1) &&
-            (ns < 2 || mbar_try_wait(&s_empty[ns & 1], ((ns - 2) >> 1) & 1))) {
+        if (ns < ntiles && mbar_test_wait(&kv_full[ns % kStages], (ns / kStages) & 1) &&
+            (ns < 2 || mbar_test_wait(&s_empty[ns & 1], ((ns - 2) >> 1) & 1))) {
           tc_fence_after();
           issue_s(ns);
           ++ns;
           progressed = true;
         }
-        if (npv < ns && mbar_try_wait(&p_full[npv & 1], (npv >> 1) & 1)) {
+        if (npv < ns && mbar_test_wait(&p_full[npv & 1], (npv >> 1) & 1)) {
           tc_fence_after();
           issue_pv(npv);
           ++npv;
@@ -361,9 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (progressed) {
           idle = 0;
-        } else if ((++idle & 255u) == 0u) {  // bounded: 2 s without progress
+        } else if ((++idle & 4095u) == 0u) {  // bounded: 2 s without progress
           const uint64_t now = globaltimer_ns();
-          if (idle == 256u) idle_since = now;
+          if (idle == 4096u) idle_since = now;
           else if (*abort_flag || now - idle_since > kWaitTimeoutNs) ok = false;
         }
       }
@@ -382,33 +473,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     const int row = 32 * (warp & 3) + lane;  // head within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    // this CTA's half of q_lat -> TMEM as bf16 pairs (the A operand of S):
+    // latent elements 256v .. 256v + 255, then rope elements 32v .. 32v + 31
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_latent + (bh0 + row) * kRow);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {  // 4 x 64 latent elements = 4 x 32 columns
+        uint32_t w[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = __ldg(src + (kHalf * v + 64 * c) / 8 + u);
+          w[4 * u] = x.x;
+          w[4 * u + 1] = x.y;
+          w[4 * u + 2] = x.z;
+          w[4 * u + 3] = x.w;
+        }
+        tc_st32u(tmem + lane_addr + kQCol + 32 * c, w);
+      }
+      uint32_t w[16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 x = __ldg(src + (kLat + kRopeHalf * v) / 8 + u);
+        w[4 * u] = x.x;
+        w[4 * u + 1] = x.y;
+        w[4 * u + 2] = x.z;
+        w[4 * u + 3] = x.w;
+      }
+      tc_st16(tmem + lane_addr + kQCol + 128, w);
+      tc_fence_before();
+      mbar_arrive(q_full);
+    }
+    const uint32_t recv_local = smem_u32(smem + kRecvOff);
+    const uint32_t recv_peer = peer_addr(recv_local, peer);
+    const uint32_t recv_full_peer = peer_addr(smem_u32(recv_full), peer);
+    const uint32_t sent_free_peer = peer_addr(smem_u32(sent_free), peer);
+    // Tile u's partial scores: wait for them (and for the tile, whose row
+    // mask is read later), read them, free the score buffer, and send them
+    // into the other CTA's exchange buffer u & 1 once it has consumed what
+    // we sent two tiles ago (asynchronous stores counted on its
+    // recv_full[u & 1]).  Layout [4-column group][row] of float4, so a
+    // warp's 16-byte stores are contiguous.
+    auto fetch_and_send = [&](int u, float (&sp)[kTile]) -> bool {
+      const int ku = u & 1;
+      bool w = mbar_wait_bounded(&s_full[ku], (u >> 1) & 1, abort_flag) &&
+               mbar_wait_bounded(&kv_full[u % kStages], (u / kStages) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) return false;
+      tc_fence_after();
+      tc_ld(tmem + lane_addr + kSCol + kTile * ku, sp);
+      tc_fence_before();
+      mbar_arrive(&s_empty[ku]);
+      if (u >= 2 && !__all_sync(0xffffffffu, wait_cluster_bounded(&sent_free[ku],
+                                                                  ((u - 2) >> 1) & 1, abort_flag)))
+        return false;
+      const uint32_t slot = static_cast<uint32_t>((ku * (kTile / 4) * kHT + row) * 16);
+#pragma unroll
+      for (int g = 0; g < kTile / 4; ++g)
+        st_async_peer(recv_peer + slot + g * kHT * 16,
+                      make_float4(sp[4 * g], sp[4 * g + 1], sp[4 * g + 2], sp[4 * g + 3]),
+                      recv_full_peer + 8 * ku);
+      return true;
+    };
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
+    float s[kTile], s_next[kTile];
+    // software pipeline: tile t + 1's partials travel to the other CTA
+    // while this thread finishes tile t
+    bool ok = fetch_and_send(0, s);
+    for (int t = 0; t < ntiles && ok; ++t) {
       const int stage = t % kStages;
-      ok = mbar_wait_bounded(&s_full[t & 1], (t >> 1) & 1, abort_flag) &&
-           mbar_wait_bounded(&kv_full[stage], (t / kStages) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
+      const int k = t & 1;
+      if (t + 1 < ntiles && !fetch_and_send(t + 1, s_next)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      float s[kTile];
-      tc_ld(tmem + lane_addr + kSCol + kTile * (t & 1), s);
-      tc_fence_before();
-      mbar_arrive(&s_empty[t & 1]);
-      const uint32_t mask = static_cast<uint32_t>(tile_mask[stage]);
+      // ---- the other CTA's partials of tile t, in our buffer k
+      if (!__all_sync(0xffffffffu, wait_cluster_bounded(&recv_full[k], (t >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const float4* mine =
+          reinterpret_cast<const float4*>(smem + kRecvOff) + k * (kTile / 4) * kHT + row;
+      const uint32_t mask = tile_mask[stage];
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < kTile; ++i) {
-        s[i] = ((mask >> i) & 1u) ? s[i] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[i]);
+      for (int g = 0; g < kTile / 4; ++g) {
+        const float4 o = mine[g * kHT];
+        const float other[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          // own + other is the same sum on both CTAs (addition commutes),
+          // so both run an identical softmax
+          const int i = 4 * g + u;
+          const float full = s[i] + other[u];
+          s[i] = ((mask >> i) & 1u) ? full * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, s[i]);
+        }
       }
+      // buffer k is consumed (the values are in registers and used): re-arm
+      // it for tile t + 2 and tell the other CTA
+      __syncwarp();
+      if (row == 0 && t + 2 < ntiles) mbar_arrive_expect_tx(&recv_full[k], kRecvBytes);
+      if (lane == 0) arrive_peer_relaxed(sent_free_peer + 8 * k);
       // lazy rescale; tcgen05.ld/st are warp-wide, so the warp rescales
       // together when any of its rows needs it (the others scale by 1)
       const bool need = mx > m_run + kRescaleLog2;
       if (__any_sync(0xffffffffu, need)) {
-        const float corr = need ? exp2f(m_run - mx) : 1.f;
+        const float corr = need ? fast_exp2(m_run - mx) : 1.f;
         if (t > 0) {
           // the output row holds P.V up to tile t - 1: wait for it
           if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[(t - 1) & 1],
@@ -435,19 +604,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kTile / 2; ++i) {
         // a masked score is -inf and m_run is finite once a token was seen
-        const float p0 = s[2 * i] == -INFINITY ? 0.f : exp2f(s[2 * i] - m_run);
-        const float p1 = s[2 * i + 1] == -INFINITY ? 0.f : exp2f(s[2 * i + 1] - m_run);
+        const float p0 = s[2 * i] == -INFINITY ? 0.f : fast_exp2(s[2 * i] - m_run);
+        const float p1 = s[2 * i + 1] == -INFINITY ? 0.f : fast_exp2(s[2 * i + 1] - m_run);
         l_run += p0 + p1;
         pr[i] = pack_bf16x2(p0, p1);
       }
-      // tokens that do not exist: zero their value rows in this CTA's half
-      // (0 x NaN would poison P.V); thread = (token row / 4, chunk row % 4)
-      constexpr uint32_t kFull = kTile == 32 ? 0xFFFFFFFFu : ((1u << kTile) - 1u);
-      if (mask != kFull) {
+      // tokens that do not exist: zero their value rows (slots 0..3; 0 x NaN
+      // would poison P.V); thread = (token row / 4, slot row % 4)
+      if (mask != 0xFFFFFFFFu) {
         const int r = row >> 2;
-        if (r < kTile && !((mask >> r) & 1u)) {
+        if (!((mask >> r) & 1u)) {
           uint4* dst = reinterpret_cast<uint4*>(smem + kStageOff + stage * kStageBytes +
-                                                (4 * v + (row & 3)) * kChunkBytes + r * 128);
+                                                (row & 3) * kChunkBytes + r * 128);
 #pragma unroll
           for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -455,15 +623,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // the weight tile of tile t - 2 must have been consumed
       if (t >= 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[t & 1], ((t - 2) >> 1) & 1,
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[k], ((t - 2) >> 1) & 1,
                                                        abort_flag))) {
           ok = false;
           break;
         }
       }
-      tc_st(tmem + lane_addr + kPCol + (kTile / 2) * (t & 1), pr);
+      tc_st(tmem + lane_addr + kPCol + (kTile / 2) * k, pr);
       tc_fence_before();
-      mbar_arrive(&p_full[t & 1]);
+      mbar_arrive(&p_full[k]);
+#pragma unroll
+      for (int i = 0; i < kTile; ++i) s[i] = s_next[i];
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_final, 0, abort_flag));
     if (!ok) {
@@ -505,7 +675,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (*abort_flag) {
     if (warp == 0 && lane == 0) {
-      mbar_wait_bounded(q_full, 0, nullptr);
       for (int t = max(0, issued - kStages); t < issued; ++t)
         mbar_wait_bounded(&kv_full[t % kStages], (t / kStages) & 1, nullptr);
     }
@@ -519,6 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols)
                  : "memory");
   }
+  // neither CTA leaves while the other may still write into its shared memory
+  cluster_sync_all();
   if (p.num_splits == 1) return;
 
   // ---- split count and merge: 2 CTAs per split; the CTA that completes
@@ -537,7 +708,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (flags[1]) {
-    for (int h = warp; h < kHT; h += kThreads / 32) mla_merge_warp(p, bh0 + h, n_valid, lane);
+    // the pipeline's shared memory is free now: per-head merge weights
+    if (kHT * n_valid * 4 <= kStages * kStageBytes)
+      mla_merge_cta(p, bh0, kHT, n_valid, reinterpret_cast<float*>(smem + kStageOff));
+    else
+      for (int h = warp; h < kHT; h += kThreads / 32) mla_merge_warp(p, bh0 + h, n_valid, lane);
   }
 }
 
@@ -554,7 +729,8 @@ pa_status launch_mla_tc(const CUtensorMap& mq, const CUtensorMap& mkv, const Mla
       return PA_ERR_CUDA;
     attr_set.store(true);
   }
-  mla_decode_tc_kernel<<<grid, kThreads, kAlloc, stream>>>(mq, mkv, p);
+  (void)mq;  // the kernel loads q_lat into tensor memory itself
+  mla_decode_tc_kernel<<<grid, kThreads, kAlloc, stream>>>(mkv, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -269,6 +269,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with `parity` (mbarrier.try_wait may
+// suspend the thread for a while when the phase is not complete; a thread
+// that polls several barriers in turn must not be held on one of them).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with `parity` to complete.  Gives up (returns false)
 // after `timeout_ns` of wall time, or early once *abort_flag is set by
 // another warp of the CTA.

@@ -463,8 +463,17 @@ DecodePlan make_mla_plan(int32_t num_seqs, int32_t num_heads, int32_t max_contex
   // CTAs per split index (a pair per 128-head tile)
   const int64_t work = static_cast<int64_t>(num_seqs) * (num_heads / ht) * (ht == 128 ? 2 : 1);
   const int per_sm = ht == 16 ? MlaCfg<16>::kCtasPerSm : 1;
-  const int64_t target = 4ll * num_sms * per_sm;  // about four waves of resident CTAs
-  int64_t splits = (target + work - 1) / work;
+  int64_t splits;
+  if (ht == 128) {
+    // tcgen05 clusters (2 CTAs, one per SM): one wave of clusters.  A
+    // cluster needs two free SMs at once and each split adds fp32 partials
+    // and a merge, so splitting further costs more than it balances
+    // (measured: B=64 context 512..4096 is fastest with one split).
+    splits = (num_sms / 2) / (work / 2);
+  } else {
+    const int64_t target = 4ll * num_sms * per_sm;  // about four waves of resident CTAs
+    splits = (target + work - 1) / work;
+  }
   if (splits < 1) splits = 1;
   if (splits > tiles_max) splits = tiles_max;
   const int64_t tiles_per_split = (tiles_max + splits - 1) / splits;

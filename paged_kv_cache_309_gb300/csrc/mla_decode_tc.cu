@@ -56,18 +56,22 @@ using namespace pa;
 using namespace mla;
 
 constexpr int kHT = 128;               // heads per CTA (M)
-constexpr int kTile = 32;              // tokens per tile (N of S, K of P.V)
+constexpr int kTile = 64;              // tokens per tile (N of S, K of P.V)
 constexpr int kHalf = kLat / 2;        // output (and latent) elements per CTA
 constexpr int kRopeHalf = kRope / 2;   // rope elements per CTA
 constexpr int kThreads = 6 * 32;
-constexpr int kChunkBytes = kTile * 128;             // one 64-element chunk of a tile: 4 KB
+constexpr int kChunkBytes = kTile * 128;             // one 64-element chunk of a tile: 8 KB
 constexpr int kLoadChunks = kHalf / 64 + 1;          // 4 latent chunks + the rope chunk
-constexpr int kStageBytes = kLoadChunks * kChunkBytes;  // 20 KB
-constexpr int kStages = 8;
+constexpr int kStageBytes = kLoadChunks * kChunkBytes;  // 40 KB
+constexpr int kStages = 3;
 constexpr int kRecvBytes = kTile * kHT * 4;          // one tile of the peer's partial scores
+constexpr int kPBytes = kHT * kTile * 2;             // one tile of bf16 weights (128-byte rows)
+constexpr int kQRopeBytes = kHT * kRopeHalf * 2;     // this CTA's rope part of q_lat (64-byte rows)
 constexpr int kStageOff = 0;
 constexpr int kRecvOff = kStageOff + kStages * kStageBytes;
-constexpr int kBarOff = kRecvOff + 2 * kRecvBytes;
+constexpr int kPOff = kRecvOff + 2 * kRecvBytes;
+constexpr int kQRopeOff = kPOff + 2 * kPBytes;
+constexpr int kBarOff = kQRopeOff + kQRopeBytes;
 // barriers: q_full, kv_full[kStages], kv_empty[kStages], s_full[2],
 // s_empty[2], p_full[2], pv_done[2], recv_full[2], sent_free[2], o_final,
 // drain; then tile masks, the TMEM slot and flags
@@ -81,20 +85,21 @@ static_assert(kAlloc <= 227 * 1024, "shared memory");
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 0;      // [0, 256): this CTA's half of the output
-constexpr uint32_t kQCol = 256;    // [256, 400): this CTA's half of q_lat (bf16 pairs)
-constexpr uint32_t kSCol = 400;    // [400, 464): two 32-column partial-score tiles
-constexpr uint32_t kPCol = 464;    // [464, 496): two 16-column weight tiles (bf16 pairs)
+constexpr uint32_t kQCol = 256;    // [256, 384): this CTA's latent part of q_lat (bf16 pairs)
+constexpr uint32_t kSCol = 384;    // [384, 512): two 64-column partial-score tiles
 
 // ------------------------------------------------------------ tcgen05 ops --
 // Shared-memory matrix descriptor: start, leading and stride byte offsets
 // (>> 4), the fixed version bit 46, and the swizzle mode in bits 61-63
-// (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// (2 = 128-byte swizzle, 4 = 64-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle = 2) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
-         (static_cast<uint64_t>(2) << 61);
+         (static_cast<uint64_t>(swizzle) << 61);
 }
+constexpr uint32_t kSwizzle64 = 4;  // 64-byte swizzle (rows of 64 bytes, 512-byte atoms)
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1),
 // bf16 A and B (bits 7-9, 10-12 = 1), B major-ness (bit 16: 1 = MN-major),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -105,6 +110,14 @@ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major) {
 constexpr uint32_t kIdescS = instr_desc(kHT, kTile, false);
 constexpr uint32_t kIdescPV = instr_desc(kHT, kHalf, true);
 
+__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -142,7 +155,6 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void tc_ld(uint32_t taddr, float (&v)[32]) { tc_ld32(taddr, v); }
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -167,16 +179,6 @@ __device__ __forceinline__ void tc_st32u(uint32_t taddr, const uint32_t (&r)[32]
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tc_st(uint32_t taddr, const uint32_t (&r)[16]) { tc_st16(taddr, r); }
 
 // ---------------------------------------------------------- cluster ops --
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -246,7 +248,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 // slots 0..4 of the stage.
 __device__ __forceinline__ void issue_half_tile(const MlaParams& p, const CUtensorMap* tm_kv,
                                                 uint8_t* stage, uint64_t* full,
-                                                uint32_t* mask_slot, const int32_t* bt, int tok0,
+                                                uint64_t* mask_slot, const int32_t* bt, int tok0,
                                                 int tok_end, int v, uint64_t pol, int lane) {
   const int bs = p.block_size;
   const int rpb = bs < kTile ? bs : kTile;
@@ -263,12 +265,13 @@ __device__ __forceinline__ void issue_half_tile(const MlaParams& p, const CUtens
       valid = bid >= 0 && static_cast<int64_t>(bid) < p.num_blocks;
     }
   }
-  uint32_t bits = 0;
-  if (valid) bits = (rows >= 32 ? ~0u : ((1u << rows) - 1u)) << (lane * rpb);
-  const uint32_t mask = __reduce_or_sync(0xffffffffu, bits);
+  uint64_t bits = 0;
+  if (valid) bits = (rows >= 64 ? ~0ull : ((1ull << rows) - 1ull)) << (lane * rpb);
+  const uint32_t lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits));
+  const uint32_t hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits >> 32));
   const uint32_t vb = __ballot_sync(0xffffffffu, valid);
   if (lane == 0) {
-    *mask_slot = mask;
+    *mask_slot = (static_cast<uint64_t>(hi) << 32) | lo;
     mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vb) * rpb * kLoadChunks * 128));
   }
   __syncwarp();
@@ -300,7 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* sent_free = recv_full + 2;           // [2] the peer consumed what we sent (peer's 128)
   uint64_t* o_final = sent_free + 2;             // every product done (commit)
   uint64_t* drain = o_final + 1;                 // error path: issued products done
-  uint32_t* tile_mask = reinterpret_cast<uint32_t*>(smem + kMaskOff);
+  uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);  // [0] abort, [1] last CTA
 
@@ -396,11 +399,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t st_base = smem_u32(smem + kStageOff);
+      const uint32_t p_base = smem_u32(smem + kPOff);
+      const uint32_t qr_base = smem_u32(smem + kQRopeOff);
       auto issue_s = [&](int t) {
         // partial S(t) = Q_v . K_v(t)^T over this CTA's 288 elements: 16
-        // latent k-steps (chunk slots 0..3) and 2 rope k-steps (slot 4,
-        // elements 32v .. 32v + 31); A = q_lat half in TMEM, B = K-major
-        // 128-byte-swizzled tile (a k-step advances the start by 32 bytes)
+        // latent k-steps with A = q_lat latent part in TMEM and B = chunk
+        // slots 0..3, then 2 rope k-steps with A = the rope part in shared
+        // memory (64-byte swizzle) and B = slot 4 at elements 32v..32v+31.
+        // B is K-major 128-byte swizzled (a k-step advances the start by 32
+        // bytes inside a 64-element chunk).
         const uint32_t kb = st_base + (t % kStages) * kStageBytes;
         const uint32_t d = tmem + kSCol + kTile * (t & 1);
 #pragma unroll
@@ -410,18 +417,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     i > 0 ? 1u : 0u);
 #pragma unroll
         for (int i = 0; i < 2; ++i)
-          tc_mma_ts(d, tmem + kQCol + 128 + 8 * i,
+          tc_mma_ss(d, smem_desc(qr_base + 32 * i, 16, 512, kSwizzle64),
                     smem_desc(kb + 4 * kChunkBytes + 64 * v + 32 * i, 16, 1024), kIdescS, 1u);
         tc_commit(&s_full[t & 1]);
       };
       auto issue_pv = [&](int u) {
-        // O[:, this half] += P(u) . V(u): V = slots 0..3 of tile u, MN-major
-        // (leading offset: next 64 elements = next slot; stride offset: next
-        // 8 tokens = 1 KB); P from TMEM, 16 tokens per product
+        // O[:, this half] += P(u) . V(u): P = the bf16 weights in shared
+        // memory (K-major, 128-byte swizzle), V = slots 0..3 of tile u,
+        // MN-major (leading offset: next 64 elements = next slot; stride
+        // offset: next 8 tokens = 1 KB); 16 tokens per product
         const uint32_t vb = st_base + (u % kStages) * kStageBytes;
+        const uint32_t pb = p_base + (u & 1) * kPBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ts(tmem + kOCol, tmem + kPCol + (kTile / 2) * (u & 1) + 8 * kk,
+          tc_mma_ss(tmem + kOCol, smem_desc(pb + 32 * kk, 16, 1024),
                     smem_desc(vb + kk * 2048, kChunkBytes, 1024), kIdescPV,
                     (u > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&pv_done[u & 1]);
@@ -474,7 +483,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int row = 32 * (warp & 3) + lane;  // head within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     // this CTA's half of q_lat -> TMEM as bf16 pairs (the A operand of S):
-    // latent elements 256v .. 256v + 255, then rope elements 32v .. 32v + 31
+    // latent elements 256v .. 256v + 255 (bf16 pairs in TMEM), then rope
+    // elements 32v .. 32v + 31 (shared memory)
     {
       const uint4* src = reinterpret_cast<const uint4*>(p.q_latent + (bh0 + row) * kRow);
 #pragma unroll 1
@@ -490,16 +500,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_st32u(tmem + lane_addr + kQCol + 32 * c, w);
       }
-      uint32_t w[16];
+      // rope part -> shared memory, row `row` of 64 bytes, 64-byte swizzle
+      // (16-byte unit u at u ^ ((row >> 1) & 3))
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint4 x = __ldg(src + (kLat + kRopeHalf * v) / 8 + u);
-        w[4 * u] = x.x;
-        w[4 * u + 1] = x.y;
-        w[4 * u + 2] = x.z;
-        w[4 * u + 3] = x.w;
-      }
-      tc_st16(tmem + lane_addr + kQCol + 128, w);
+      for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<uint4*>(smem + kQRopeOff + row * 64 + ((u ^ ((row >> 1) & 3)) << 4)) =
+            __ldg(src + (kLat + kRopeHalf * v) / 8 + u);
+      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(q_full);
     }
@@ -519,7 +526,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                mbar_wait_bounded(&kv_full[u % kStages], (u / kStages) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, w)) return false;
       tc_fence_after();
-      tc_ld(tmem + lane_addr + kSCol + kTile * ku, sp);
+      tc_ld32(tmem + lane_addr + kSCol + kTile * ku, *reinterpret_cast<float(*)[32]>(&sp[0]));
+      tc_ld32(tmem + lane_addr + kSCol + kTile * ku + 32,
+              *reinterpret_cast<float(*)[32]>(&sp[32]));
       tc_fence_before();
       mbar_arrive(&s_empty[ku]);
       if (u >= 2 && !__all_sync(0xffffffffu, wait_cluster_bounded(&sent_free[ku],
@@ -552,7 +561,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const float4* mine =
           reinterpret_cast<const float4*>(smem + kRecvOff) + k * (kTile / 4) * kHT + row;
-      const uint32_t mask = tile_mask[stage];
+      const uint64_t mask = tile_mask[stage];
       float mx = -INFINITY;
 #pragma unroll
       for (int g = 0; g < kTile / 4; ++g) {
@@ -564,7 +573,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // so both run an identical softmax
           const int i = 4 * g + u;
           const float full = s[i] + other[u];
-          s[i] = ((mask >> i) & 1u) ? full * p.scale_log2 : -INFINITY;
+          s[i] = ((mask >> i) & 1ull) ? full * p.scale_log2 : -INFINITY;
           mx = fmaxf(mx, s[i]);
         }
       }
@@ -610,16 +619,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         pr[i] = pack_bf16x2(p0, p1);
       }
       // tokens that do not exist: zero their value rows (slots 0..3; 0 x NaN
-      // would poison P.V); thread = (token row / 4, slot row % 4)
-      if (mask != 0xFFFFFFFFu) {
-        const int r = row >> 2;
-        if (!((mask >> r) & 1u)) {
-          uint4* dst = reinterpret_cast<uint4*>(smem + kStageOff + stage * kStageBytes +
-                                                (row & 3) * kChunkBytes + r * 128);
+      // would poison P.V); piece j = (token j / 4, slot j % 4), two per thread
+      if (mask != ~0ull) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
+        for (int h = 0; h < 2; ++h) {
+          const int j = row + kHT * h;
+          const int r = j >> 2;
+          if (!((mask >> r) & 1ull)) {
+            uint4* dst = reinterpret_cast<uint4*>(smem + kStageOff + stage * kStageBytes +
+                                                  (j & 3) * kChunkBytes + r * 128);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
-        fence_proxy_async_smem();  // generic writes before the tensor core reads them
       }
       // the weight tile of tile t - 2 must have been consumed
       if (t >= 2) {
@@ -629,8 +641,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      tc_st(tmem + lane_addr + kPCol + (kTile / 2) * k, pr);
-      tc_fence_before();
+      // weights -> shared memory buffer k, row `row` of 128 bytes, 128-byte
+      // swizzle (16-byte unit u at u ^ (row & 7)): the A operand of P.V
+      uint8_t* prow = smem + kPOff + k * kPBytes + row * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
+            make_uint4(pr[4 * u], pr[4 * u + 1], pr[4 * u + 2], pr[4 * u + 3]);
+      fence_proxy_async_smem();  // generic writes before the tensor core reads them
       mbar_arrive(&p_full[k]);
 #pragma unroll
       for (int i = 0; i < kTile; ++i) s[i] = s_next[i];

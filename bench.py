@@ -448,6 +448,46 @@ def run_extras(args, dev, peak):
                                         "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 2),
                                         "median_us": round(med * 1e3, 2),
                                         "algorithmic_bytes": nbytes}
+    # MLA decode over the latent cache (DeepSeek-V3-shaped: B=64, context
+    # 512..4096, bs=64): 128 heads (tcgen05 kernel) and 16 heads (one TP8
+    # shard, mma.sync kernel); for 128 heads also the absorbed chain
+    for H in (128, 16):
+        mw = wl.mla_decode(num_heads=H, with_weights=(H == 128))
+        mq, mc = up(mw.q_lat, torch.bfloat16, dev), up(mw.latent_cache, torch.bfloat16, dev)
+        mbt = torch.from_numpy(mw.block_tables).to(dev)
+        mcl = torch.from_numpy(mw.context_lens).to(dev)
+        mout = torch.empty((mw.num_seqs, H, 512), dtype=torch.bfloat16, device=dev)
+        mws = pa.mla_decode_workspace(mw.num_seqs, H, mw.max_context_len, device=dev)
+        attn = lambda: pa.pa_mla_decode_attention(mout, mq, mc, mbt, mcl, mw.scale,
+                                                  mw.max_context_len, mws)
+        med, _ = timed_loop(attn, iters, 3, dev)
+        nbytes, flops = wl.mla_bytes_read(mw), wl.mla_flops(mw)
+        rec = {"kernel": "tcgen05 2-CTA cluster" if H % 128 == 0 else "mma.sync",
+               "tokens_attended_per_s": round(int(mw.context_lens.sum()) / (med * 1e-3), 1),
+               "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 2),
+               "frac_of_hbm_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4),
+               "TFLOP_per_s": round(flops / (med * 1e-3) / 1e12, 2),
+               "frac_of_bf16_dense_peak": round(flops / (med * 1e-3) / 1e12 / bf16_peak(), 4),
+               "median_us": round(med * 1e3, 2), "algorithmic_bytes": nbytes, "flops": flops}
+        if H == 128:
+            qn, qp = up(mw.q_nope, torch.bfloat16, dev), up(mw.q_pe, torch.bfloat16, dev)
+            wuk, wuv = up(mw.w_uk, torch.bfloat16, dev), up(mw.w_uv, torch.bfloat16, dev)
+            qlat = torch.empty_like(mq)
+            o = torch.empty((mw.num_seqs, H, 128), dtype=torch.bfloat16, device=dev)
+            a_med, _ = timed_loop(lambda: pa.pa_mla_absorb_q(qlat, qn, qp, wuk), iters, 3, dev)
+            p_med, _ = timed_loop(lambda: pa.pa_mla_project_out(o, mout, wuv), iters, 3, dev)
+
+            def chain():
+                pa.pa_mla_absorb_q(qlat, qn, qp, wuk)
+                pa.pa_mla_decode_attention(mout, qlat, mc, mbt, mcl, mw.scale,
+                                           mw.max_context_len, mws)
+                pa.pa_mla_project_out(o, mout, wuv)
+            c_med, _ = timed_loop(chain, iters, 3, dev)
+            rec.update({"absorb_q_us": round(a_med * 1e3, 2),
+                        "project_out_us": round(p_med * 1e3, 2),
+                        "chain_us": round(c_med * 1e3, 2),
+                        "chain_seqs_per_s": round(mw.num_seqs / (c_med * 1e-3), 1)})
+        ex[mw.name] = rec
     return ex
 
 
@@ -537,6 +577,25 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_mla_only(args):
+    """MLA decode attention launches only (for an ncu capture of that kernel)."""
+    import torch
+
+    from paged_kv_cache_309_gb300 import build, pa
+    from paged_kv_cache_309_gb300 import workloads as wl
+    build.build()
+    dev = torch.device("cuda", 0)
+    w = wl.mla_decode(num_heads=args.mla_heads, with_weights=False)
+    q, c = up(w.q_lat, torch.bfloat16, dev), up(w.latent_cache, torch.bfloat16, dev)
+    bt, cl = torch.from_numpy(w.block_tables).to(dev), torch.from_numpy(w.context_lens).to(dev)
+    out = torch.empty((w.num_seqs, w.num_heads, 512), dtype=torch.bfloat16, device=dev)
+    ws = pa.mla_decode_workspace(w.num_seqs, w.num_heads, w.max_context_len, device=dev)
+    for _ in range(args.steps):
+        pa.pa_mla_decode_attention(out, q, c, bt, cl, w.scale, w.max_context_len, ws)
+    torch.cuda.synchronize()
+    print(f"{w.name}: {args.steps} launches, device error word {pa.read_device_error(ws)}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -553,9 +612,15 @@ def main():
     ap.add_argument("--extra-iters", type=int, default=50)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mla-heads", type=int, default=0,
+                    help="profiling aid: only run --steps MLA decode attention launches on the "
+                         "B=64 context 512..4096 latent workload with this many heads (no JSON)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.mla_heads:
+        run_mla_only(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

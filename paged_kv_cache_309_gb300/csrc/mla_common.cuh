@@ -38,6 +38,8 @@ struct MlaParams {
   int32_t num_splits;
   int32_t tokens_per_split;
   int32_t kv_evict_first;  // one head tile per sequence: nobody re-reads the rows
+  int32_t num_seqs;
+  int32_t num_slots;       // tcgen05 kernel: partial slots per head tile (2 per cluster)
   float scale_log2;
 };
 

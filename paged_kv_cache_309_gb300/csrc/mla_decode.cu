@@ -465,11 +465,11 @@ DecodePlan make_mla_plan(int32_t num_seqs, int32_t num_heads, int32_t max_contex
   const int per_sm = ht == 16 ? MlaCfg<16>::kCtasPerSm : 1;
   int64_t splits;
   if (ht == 128) {
-    // tcgen05 clusters (2 CTAs, one per SM): one wave of clusters.  A
-    // cluster needs two free SMs at once and each split adds fp32 partials
-    // and a merge, so splitting further costs more than it balances
-    // (measured: B=64 context 512..4096 is fastest with one split).
-    splits = (num_sms / 2) / (work / 2);
+    // tcgen05 kernel: one wave of 2-CTA clusters per 128-head tile, each
+    // taking an equal share of the tiles (the kernel derives the split
+    // from context_lens); num_splits = clusters per head tile
+    const int64_t per_tile = (num_sms / 2) / (num_heads / 128);
+    return {static_cast<int32_t>(per_tile < 1 ? 1 : per_tile), 0};
   } else {
     const int64_t target = 4ll * num_sms * per_sm;  // about four waves of resident CTAs
     splits = (target + work - 1) / work;
@@ -481,9 +481,18 @@ DecodePlan make_mla_plan(int32_t num_seqs, int32_t num_heads, int32_t max_contex
   return {static_cast<int32_t>(splits), static_cast<int32_t>(tiles_per_split * tile)};
 }
 
-// [error word | pad] [counters B * H/HT] [lse B*H*splits] [o B*H*splits*512]
+// mma.sync kernel: [error word | pad] [counters B * H/HT] [lse B*H*splits]
+// [o B*H*splits*512].  tcgen05 kernel: [error word | pad] [counters B * H/128 * 2]
+// [lse H/128 * 2C * 128] [o H/128 * 2C * 128 * 512] with C = plan.num_splits.
 size_t mla_workspace_bytes(int32_t num_seqs, int32_t num_heads, const DecodePlan& plan) {
   size_t bytes = kWorkspaceHeader;
+  if (mla_head_tile(num_heads) == 128) {
+    const size_t rows = static_cast<size_t>(num_heads) * 2 * plan.num_splits;  // slots x heads
+    bytes += align256(static_cast<size_t>(num_seqs) * (num_heads / 128) * 2 * 4);
+    bytes += align256(rows * sizeof(float));
+    bytes += rows * kLat * sizeof(float);
+    return bytes;
+  }
   if (plan.num_splits > 1) {
     const size_t rows = static_cast<size_t>(num_seqs) * num_heads * plan.num_splits;
     bytes += align256(static_cast<size_t>(num_seqs) * (num_heads / mla_head_tile(num_heads)) * 4);
@@ -503,14 +512,18 @@ pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
       !make_row576_map(&mkv, a.latent_cache, a.num_blocks * a.block_size, box_rows))
     return PA_ERR_CUDA;
   MlaParams p;
+  p.num_seqs = a.num_seqs;
+  p.num_slots = 2 * a.plan.num_splits;
   p.out = static_cast<__nv_bfloat16*>(a.out_latent);
   p.q_latent = static_cast<const __nv_bfloat16*>(a.q_latent);
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.err = reinterpret_cast<unsigned*>(ws);
-  const size_t nrows = static_cast<size_t>(a.num_seqs) * a.num_heads * a.plan.num_splits;
-  const size_t ctr_bytes = align256(static_cast<size_t>(a.num_seqs) * (a.num_heads / ht) * 4);
+  const size_t nrows = ht == 128 ? static_cast<size_t>(a.num_heads) * 2 * a.plan.num_splits
+                                  : static_cast<size_t>(a.num_seqs) * a.num_heads * a.plan.num_splits;
+  const size_t ctr_bytes =
+      align256(static_cast<size_t>(a.num_seqs) * (a.num_heads / ht) * (ht == 128 ? 2 : 1) * 4);
   p.counters = reinterpret_cast<unsigned*>(ws + kWorkspaceHeader);
   p.ws_lse = reinterpret_cast<float*>(ws + kWorkspaceHeader + ctr_bytes);
   p.ws_o = reinterpret_cast<float*>(ws + kWorkspaceHeader + ctr_bytes + align256(nrows * 4));
@@ -526,8 +539,8 @@ pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
   p.kv_evict_first = (a.num_heads == ht && ht != 128) ? 1 : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
   if (ht == 128) {
-    const dim3 grid(static_cast<unsigned>(2 * (a.num_heads / ht)),
-                    static_cast<unsigned>(a.plan.num_splits), static_cast<unsigned>(a.num_seqs));
+    const dim3 grid(static_cast<unsigned>(2 * a.plan.num_splits),
+                    static_cast<unsigned>(a.num_heads / ht), 1u);
     return launch_mla_tc(mq, mkv, p, grid, stream);
   }
   const dim3 grid(static_cast<unsigned>(a.num_heads / ht), static_cast<unsigned>(a.plan.num_splits),

@@ -73,12 +73,14 @@ constexpr int kPOff = kRecvOff + 2 * kRecvBytes;
 constexpr int kQRopeOff = kPOff + 2 * kPBytes;
 constexpr int kBarOff = kQRopeOff + kQRopeBytes;
 // barriers: q_full, kv_full[kStages], kv_empty[kStages], s_full[2],
-// s_empty[2], p_full[2], pv_done[2], recv_full[2], sent_free[2], o_final,
-// drain; then tile masks, the TMEM slot and flags
-constexpr int kNumBars = 15 + 2 * kStages;
+// s_empty[2], p_full[2], pv_done[2], recv_full[2], sent_free[2], o_done,
+// drain, part_done; then tile masks, the TMEM slot and flags, the schedule
+constexpr int kNumBars = 16 + 2 * kStages;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
 constexpr int kMiscOff = kMaskOff + kStages * 8;
-constexpr int kBytes = kMiscOff + 32;
+constexpr int kSchedOff = kMiscOff + 32;             // schedule words and the merge list
+constexpr int kMaxMerges = 32;
+constexpr int kBytes = kSchedOff + (8 + 3 * kMaxMerges) * 4;
 constexpr int kAlloc = kBytes + 1024;
 static_assert(kAlloc <= 227 * 1024, "shared memory");
 
@@ -286,54 +288,204 @@ __device__ __forceinline__ void issue_half_tile(const MlaParams& p, const CUtens
   }
 }
 
+// ------------------------------------------------------------- schedule --
+// The work of one 128-head tile is the sequences' 64-token tiles laid end
+// to end in sequence order (T tiles), cut into C contiguous chunks of
+// ceil(T / C) tiles, one per cluster.  Where a chunk crosses a sequence
+// boundary it splits into pieces.  A piece that covers its whole sequence
+// writes bf16 output; the others write an fp32 partial to a slot: 2c for
+// the first piece of cluster c, 2c + 1 for a later one (only a cluster's
+// first and last pieces can be partial), and the CTA that completes a
+// sequence's count merges it.  Every CTA derives the schedule from
+// context_lens itself.
+__device__ __forceinline__ int seq_len_eff(const MlaParams& p, int b, bool* clipped) {
+  int L = __ldg(p.context_lens + b);
+  L = L < 0 ? 0 : L;
+  const int64_t cap = static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
+  *clipped = static_cast<int64_t>(L) > cap;
+  return *clipped ? static_cast<int>(cap) : L;
+}
+__device__ __forceinline__ int seq_tiles(const MlaParams& p, int b) {
+  bool c;
+  return (seq_len_eff(p, b, &c) + kTile - 1) / kTile;
+}
+struct Piece {
+  int b;       // sequence
+  int tb, te;  // tile range [tb, te) of the sequence
+  int pre;     // tiles of the sequences before b (position of its first tile)
+  int n;       // tiles of the sequence
+  bool first;  // the cluster's first piece
+};
+// Walks this cluster's chunk [g, g1) piece by piece (each role keeps its own).
+struct PieceIter {
+  int b, pre, g, g1;
+  bool started;
+  __device__ __forceinline__ bool next(const MlaParams& p, Piece& pc) {
+    if (g >= g1) return false;
+    int n = seq_tiles(p, b);
+    while (pre + n <= g && b + 1 < p.num_seqs) {  // skips finished and empty sequences
+      pre += n;
+      ++b;
+      n = seq_tiles(p, b);
+    }
+    pc.b = b;
+    pc.pre = pre;
+    pc.n = n;
+    pc.tb = g - pre;
+    pc.te = min(n, g1 - pre);
+    pc.first = !started;
+    started = true;
+    g = pre + pc.te;
+    return true;
+  }
+};
+__device__ __forceinline__ int piece_slot(const Piece& pc, int c) { return 2 * c + (pc.first ? 0 : 1); }
+
+// Merge of output half v of the 128 heads of (sequence b, head tile ht)
+// over its pieces, by the whole CTA: the pieces are clusters c_first ..
+// c_last; slot of the first one 2 c_first (+1 if it is not that cluster's
+// first piece), of the others 2c.  Per-head weights 2^(lse - max) go to
+// `wsm` first; then each thread sums 8 four-element columns at a time with
+// all their loads in flight (L2 round trips, not bandwidth, bound a merge).
+__device__ __forceinline__ void merge_pieces(const MlaParams& p, int b, int ht, int v, int pre,
+                                             int n, int chunk, float* wsm) {
+  const int c_first = pre / chunk, c_last = (pre + n - 1) / chunk;
+  const int np = c_last - c_first + 1;
+  const int s0 = 2 * c_first + (pre != c_first * chunk ? 1 : 0);
+  auto slot = [&](int i) { return i == 0 ? s0 : 2 * (c_first + i); };
+  const int64_t base = static_cast<int64_t>(ht) * p.num_slots;
+  const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + ht * kHT;
+  for (int h = threadIdx.x; h < kHT; h += blockDim.x) {
+    float M = -INFINITY;
+    for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(p.ws_lse + (base + slot(i)) * kHT + h));
+    float W = 0.f;
+    for (int i = 0; i < np; ++i) {
+      const float w = M == -INFINITY ? 0.f : exp2f(__ldcg(p.ws_lse + (base + slot(i)) * kHT + h) - M);
+      wsm[h * np + i] = w;
+      W += w;
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    for (int i = 0; i < np; ++i) wsm[h * np + i] *= inv;
+  }
+  __syncthreads();
+  constexpr int kCols = kHalf / 4;  // four-element columns of one head's half
+  constexpr int kBatch = 8;
+  for (int idx0 = threadIdx.x * kBatch; idx0 < kHT * kCols; idx0 += blockDim.x * kBatch) {
+    float4 acc[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < np; ++i) {
+      float4 x[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int idx = idx0 + u;
+        const int h = idx / kCols, e4 = idx % kCols;
+        x[u] = __ldcg(reinterpret_cast<const float4*>(
+                          p.ws_o + ((base + slot(i)) * kHT + h) * kLat + kHalf * v) + e4);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float w = wsm[((idx0 + u) / kCols) * np + i];
+        acc[u].x += w * x[u].x;
+        acc[u].y += w * x[u].y;
+        acc[u].z += w * x[u].z;
+        acc[u].w += w * x[u].w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int idx = idx0 + u;
+      const int h = idx / kCols, e4 = idx % kCols;
+      *reinterpret_cast<uint2*>(p.out + (bh0 + h) * kLat + kHalf * v + 4 * e4) =
+          make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+    }
+  }
+  __syncthreads();
+}
+
 // ------------------------------------------------------------------ kernel --
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* q_full = bars + 0;                   // q_lat half in TMEM (128 threads)
+  uint64_t* q_full = bars + 0;                   // q_lat of the current piece loaded (128 threads)
   uint64_t* kv_full = bars + 1;                  // [kStages] tile landed
   uint64_t* kv_empty = kv_full + kStages;        // [kStages] P.V of the stage's tile done
   uint64_t* s_full = kv_empty + kStages;         // [2] partial scores in TMEM (commit)
   uint64_t* s_empty = s_full + 2;                // [2] partial scores read (128 threads)
-  uint64_t* p_full = s_empty + 2;                // [2] weights in TMEM (128 threads)
+  uint64_t* p_full = s_empty + 2;                // [2] weights in shared memory (128 threads)
   uint64_t* pv_done = p_full + 2;                // [2] P.V done (commit)
-  uint64_t* recv_full = pv_done + 2;             // [2] the peer's partials landed here (peer's 128)
-  uint64_t* sent_free = recv_full + 2;           // [2] the peer consumed what we sent (peer's 128)
-  uint64_t* o_final = sent_free + 2;             // every product done (commit)
-  uint64_t* drain = o_final + 1;                 // error path: issued products done
+  uint64_t* recv_full = pv_done + 2;             // [2] the other CTA's partials landed here
+  uint64_t* sent_free = recv_full + 2;           // [2] the other CTA consumed what we sent
+  uint64_t* o_done = sent_free + 2;              // every product of the current piece done
+  uint64_t* drain = o_done + 1;                  // error path: issued products done
+  uint64_t* part_done = drain + 1;               // a partial's 128 rows are written
   uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
-  int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);  // [0] abort, [1] last CTA
+  int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);  // [0] abort
+  int* sched = reinterpret_cast<int*>(smem + kSchedOff);      // T, chunk, g0, g1, b0, pre0, merges
+  int* merges = sched + 8;                                    // (b, pre, n) per sequence to merge
 
-  const int ht = blockIdx.x >> 1;  // 128-head tile
   const int v = static_cast<int>(cluster_rank());  // output half = element slice
-  const int split = blockIdx.y;
-  const int b = blockIdx.z;
+  const int c = blockIdx.x >> 1;                   // cluster = chunk of the tile list
+  const int C = gridDim.x >> 1;
+  const int ht = blockIdx.y;                       // 128-head tile
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int h0 = ht * kHT;
-  const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + h0;
+  const int B = p.num_seqs;
 
-  bool clipped;
-  const int L = mla_effective_len(p, b, &clipped);
-  if (clipped && split == 0 && blockIdx.x == 0 && threadIdx.x == 0)
-    atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
-  const int tok_begin = split * p.tokens_per_split;
-  const int tok_end = min(tok_begin + p.tokens_per_split, L);
-  if (tok_begin >= tok_end) {  // both CTAs of the cluster leave here together
-    if (split == 0) {  // L == 0: zero rows (this CTA's half)
-      for (int i = threadIdx.x; i < kHT * (kHalf / 8); i += kThreads) {
-        const int h = i / (kHalf / 8), c = i % (kHalf / 8);
-        reinterpret_cast<uint4*>(p.out + (bh0 + h) * kLat + kHalf * v)[c] =
-            make_uint4(0u, 0u, 0u, 0u);
+  // ---- schedule (warp 0): total tiles, this cluster's chunk, its first sequence
+  if (warp == 0) {
+    int T = 0;
+    bool any_clip = false;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      int n = 0;
+      if (b0 + lane < B) {
+        bool cl;
+        n = (seq_len_eff(p, b0 + lane, &cl) + kTile - 1) / kTile;
+        any_clip |= cl;
+      }
+      T += __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n));
+    }
+    if (__any_sync(0xffffffffu, any_clip) && c == 0 && ht == 0 && v == 0 && lane == 0)
+      atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
+    const int chunk = T > 0 ? (T + C - 1) / C : 1;
+    const int g0 = min(T, c * chunk), g1 = min(T, g0 + chunk);
+    int bfirst = 0, prefirst = 0;
+    if (g0 < g1) {
+      int pre = 0;
+      bool found = false;
+      for (int b0 = 0; b0 < B && !found; b0 += 32) {
+        const int n = b0 + lane < B ? seq_tiles(p, b0 + lane) : 0;
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        const int excl = incl - n;
+        const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && pre + excl <= g0 && g0 < pre + incl);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          bfirst = b0 + l;
+          prefirst = pre + __shfl_sync(0xffffffffu, excl, l);
+          found = true;
+        }
+        pre += __shfl_sync(0xffffffffu, incl, 31);
       }
     }
-    return;
+    if (lane == 0) {
+      sched[0] = T;
+      sched[1] = chunk;
+      sched[2] = g0;
+      sched[3] = g1;
+      sched[4] = bfirst;
+      sched[5] = prefirst;
+      sched[6] = 0;  // sequences this CTA merges
+    }
   }
-  const int ntiles = (tok_end - tok_begin + kTile - 1) / kTile;
-
   if (threadIdx.x == 0) {
     mbar_init(q_full, kHT);
     for (int s = 0; s < kStages; ++s) {
@@ -348,10 +500,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&recv_full[s], 1);   // armed with the byte count by this CTA
       mbar_init(&sent_free[s], 4);   // one arrival per softmax warp of the other CTA
     }
-    mbar_init(o_final, 1);
+    mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(part_done, kHT);
     flags[0] = 0;
-    flags[1] = 0;
     mbar_init_fence();
     // the first two exchanges: expect one tile of partials in each buffer
     mbar_arrive_expect_tx(&recv_full[0], kRecvBytes);
@@ -370,8 +522,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* abort_flag = flags;
-  const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+  const int chunk = sched[1], g0 = sched[2], g1 = sched[3];
+  const int ntotal = g1 - g0;  // tiles of this cluster
+  const PieceIter it0{sched[4], sched[5], g0, g1, false};
   const uint32_t peer = static_cast<uint32_t>(v ^ 1);
+
+  // sequences without tokens: zero output rows (cluster c takes b = c mod C)
+  for (int b = c; b < B; b += C) {
+    if (seq_tiles(p, b) != 0) continue;
+    for (int i = threadIdx.x; i < kHT * (kHalf / 8); i += kThreads) {
+      const int h = i / (kHalf / 8), e = i % (kHalf / 8);
+      reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + h0 + h) * kLat +
+                               kHalf * v)[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   int issued = 0;
 
   if (warp == 0) {
@@ -379,17 +543,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint64_t pol = l2_policy_evict_first();  // each row is read once (the rope chunk twice)
     if (lane == 0) prefetch_tensormap(&tm_kv);
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      const int stage = t % kStages;
-      if (t >= kStages) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait_bounded(&kv_empty[stage], ((t / kStages) - 1) & 1, abort_flag));
-        if (!ok) break;
+    PieceIter it = it0;
+    Piece pc;
+    int gt = 0;
+    while (ok && it.next(p, pc)) {
+      const int32_t* bt = p.block_tables + static_cast<int64_t>(pc.b) * p.max_blocks_per_seq;
+      bool cl;
+      const int L = seq_len_eff(p, pc.b, &cl);
+      for (int tl = pc.tb; tl < pc.te; ++tl, ++gt) {
+        const int stage = gt % kStages;
+        if (gt >= kStages) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&kv_empty[stage],
+                                                         ((gt / kStages) - 1) & 1, abort_flag));
+          if (!ok) break;
+        }
+        issue_half_tile(p, &tm_kv, smem + kStageOff + stage * kStageBytes, &kv_full[stage],
+                        &tile_mask[stage], bt, tl * kTile, L, v, pol, lane);
+        issued = gt + 1;
       }
-      issue_half_tile(p, &tm_kv, smem + kStageOff + stage * kStageBytes, &kv_full[stage],
-                      &tile_mask[stage], bt,
-                      tok_begin + t * kTile, tok_end, v, pol, lane);
-      issued = t + 1;
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
@@ -421,42 +592,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     smem_desc(kb + 4 * kChunkBytes + 64 * v + 32 * i, 16, 1024), kIdescS, 1u);
         tc_commit(&s_full[t & 1]);
       };
-      auto issue_pv = [&](int u) {
+      auto issue_pv = [&](int u, bool fresh) {
         // O[:, this half] += P(u) . V(u): P = the bf16 weights in shared
         // memory (K-major, 128-byte swizzle), V = slots 0..3 of tile u,
         // MN-major (leading offset: next 64 elements = next slot; stride
-        // offset: next 8 tokens = 1 KB); 16 tokens per product
+        // offset: next 8 tokens = 1 KB); 16 tokens per product.  The first
+        // tile of a piece starts the output afresh.
         const uint32_t vb = st_base + (u % kStages) * kStageBytes;
         const uint32_t pb = p_base + (u & 1) * kPBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           tc_mma_ss(tmem + kOCol, smem_desc(pb + 32 * kk, 16, 1024),
                     smem_desc(vb + kk * 2048, kChunkBytes, 1024), kIdescPV,
-                    (u > 0 || kk > 0) ? 1u : 0u);
+                    (!fresh || kk > 0) ? 1u : 0u);
         tc_commit(&pv_done[u & 1]);
         tc_commit(&kv_empty[u % kStages]);
       };
       // Issue whichever product is ready, never blocking on one while the
-      // other could go: S(ns) needs its tile and its score buffer (read by
-      // the softmax two tiles ago), P.V(npv) needs the softmax's weights.
-      bool ok = mbar_wait_bounded(q_full, 0, abort_flag);
-      tc_fence_after();
+      // other could go: S(ns) needs its tile, its score buffer (read by the
+      // softmax two tiles ago) and, on a piece's first tile, that piece's
+      // q_lat; P.V(npv) needs the softmax's weights.  After a piece's last
+      // P.V, o_done tells the softmax its output is complete.
+      PieceIter its = it0, itp = it0;
+      Piece pcs, pcp;
+      int ts = its.next(p, pcs) ? pcs.tb : 0;
+      int tp = itp.next(p, pcp) ? pcp.tb : 0;
+      int ks = 0;  // piece ordinal of the S cursor
       int ns = 0, npv = 0;
+      bool ok = true;
       uint64_t idle_since = 0;
       uint32_t idle = 0;
-      while (ok && npv < ntiles) {
+      while (ok && npv < ntotal) {
         bool progressed = false;
-        if (ns < ntiles && mbar_test_wait(&kv_full[ns % kStages], (ns / kStages) & 1) &&
+        if (ns < ntotal && (ts != pcs.tb || mbar_test_wait(q_full, ks & 1)) &&
+            mbar_test_wait(&kv_full[ns % kStages], (ns / kStages) & 1) &&
             (ns < 2 || mbar_test_wait(&s_empty[ns & 1], ((ns - 2) >> 1) & 1))) {
           tc_fence_after();
           issue_s(ns);
           ++ns;
+          if (++ts == pcs.te) {
+            ++ks;
+            if (its.next(p, pcs)) ts = pcs.tb;
+          }
           progressed = true;
         }
         if (npv < ns && mbar_test_wait(&p_full[npv & 1], (npv >> 1) & 1)) {
           tc_fence_after();
-          issue_pv(npv);
+          issue_pv(npv, tp == pcp.tb);
           ++npv;
+          if (++tp == pcp.te) {
+            tc_commit(o_done);
+            if (itp.next(p, pcp)) tp = pcp.tb;
+          }
           progressed = true;
         }
         if (progressed) {
@@ -467,9 +654,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           else if (*abort_flag || now - idle_since > kWaitTimeoutNs) ok = false;
         }
       }
-      if (ok) {
-        tc_commit(o_final);
-      } else {
+      if (!ok) {
         *abort_flag = 1;
         atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
       }
@@ -482,44 +667,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     const int row = 32 * (warp & 3) + lane;  // head within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    // this CTA's half of q_lat -> TMEM as bf16 pairs (the A operand of S):
-    // latent elements 256v .. 256v + 255 (bf16 pairs in TMEM), then rope
-    // elements 32v .. 32v + 31 (shared memory)
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_latent + (bh0 + row) * kRow);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {  // 4 x 64 latent elements = 4 x 32 columns
-        uint32_t w[32];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 x = __ldg(src + (kHalf * v + 64 * c) / 8 + u);
-          w[4 * u] = x.x;
-          w[4 * u + 1] = x.y;
-          w[4 * u + 2] = x.z;
-          w[4 * u + 3] = x.w;
-        }
-        tc_st32u(tmem + lane_addr + kQCol + 32 * c, w);
-      }
-      // rope part -> shared memory, row `row` of 64 bytes, 64-byte swizzle
-      // (16-byte unit u at u ^ ((row >> 1) & 3))
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        *reinterpret_cast<uint4*>(smem + kQRopeOff + row * 64 + ((u ^ ((row >> 1) & 3)) << 4)) =
-            __ldg(src + (kLat + kRopeHalf * v) / 8 + u);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(q_full);
-    }
     const uint32_t recv_local = smem_u32(smem + kRecvOff);
     const uint32_t recv_peer = peer_addr(recv_local, peer);
     const uint32_t recv_full_peer = peer_addr(smem_u32(recv_full), peer);
     const uint32_t sent_free_peer = peer_addr(smem_u32(sent_free), peer);
-    // Tile u's partial scores: wait for them (and for the tile, whose row
-    // mask is read later), read them, free the score buffer, and send them
-    // into the other CTA's exchange buffer u & 1 once it has consumed what
-    // we sent two tiles ago (asynchronous stores counted on its
-    // recv_full[u & 1]).  Layout [4-column group][row] of float4, so a
-    // warp's 16-byte stores are contiguous.
+    // Tile u's partial scores (u counts this cluster's tiles): wait for them
+    // (and for the tile, whose row mask is read later), read them, free the
+    // score buffer, and send them into the other CTA's exchange buffer
+    // u & 1 once it has consumed what we sent two tiles ago (asynchronous
+    // stores counted on its recv_full[u & 1]).  Layout [4-column group][row]
+    // of float4, so a warp's 16-byte stores are contiguous.
     auto fetch_and_send = [&](int u, float (&sp)[kTile]) -> bool {
       const int ku = u & 1;
       bool w = mbar_wait_bounded(&s_full[ku], (u >> 1) & 1, abort_flag) &&
@@ -542,132 +699,173 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       recv_full_peer + 8 * ku);
       return true;
     };
-    float m_run = -INFINITY, l_run = 0.f;
-    float s[kTile], s_next[kTile];
-    // software pipeline: tile t + 1's partials travel to the other CTA
-    // while this thread finishes tile t
-    bool ok = fetch_and_send(0, s);
-    for (int t = 0; t < ntiles && ok; ++t) {
-      const int stage = t % kStages;
-      const int k = t & 1;
-      if (t + 1 < ntiles && !fetch_and_send(t + 1, s_next)) {
-        ok = false;
-        break;
-      }
-      // ---- the other CTA's partials of tile t, in our buffer k
-      if (!__all_sync(0xffffffffu, wait_cluster_bounded(&recv_full[k], (t >> 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      const float4* mine =
-          reinterpret_cast<const float4*>(smem + kRecvOff) + k * (kTile / 4) * kHT + row;
-      const uint64_t mask = tile_mask[stage];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int g = 0; g < kTile / 4; ++g) {
-        const float4 o = mine[g * kHT];
-        const float other[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          // own + other is the same sum on both CTAs (addition commutes),
-          // so both run an identical softmax
-          const int i = 4 * g + u;
-          const float full = s[i] + other[u];
-          s[i] = ((mask >> i) & 1ull) ? full * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[i]);
-        }
-      }
-      // buffer k is consumed (the values are in registers and used): re-arm
-      // it for tile t + 2 and tell the other CTA
-      __syncwarp();
-      if (row == 0 && t + 2 < ntiles) mbar_arrive_expect_tx(&recv_full[k], kRecvBytes);
-      if (lane == 0) arrive_peer_relaxed(sent_free_peer + 8 * k);
-      // lazy rescale; tcgen05.ld/st are warp-wide, so the warp rescales
-      // together when any of its rows needs it (the others scale by 1)
-      const bool need = mx > m_run + kRescaleLog2;
-      if (__any_sync(0xffffffffu, need)) {
-        const float corr = need ? fast_exp2(m_run - mx) : 1.f;
-        if (t > 0) {
-          // the output row holds P.V up to tile t - 1: wait for it
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[(t - 1) & 1],
-                                                         ((t - 1) >> 1) & 1, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+    bool ok = true;
+    PieceIter it = it0;
+    Piece pc;
+    int gbase = 0;    // this cluster's tiles before the current piece
+    int npiece = 0;   // pieces done
+    int npart = 0;    // partial pieces done
+    while (ok && it.next(p, pc)) {
+      const int64_t bh = static_cast<int64_t>(pc.b) * p.num_heads + h0 + row;
+      // this CTA's slice of the piece's q_lat: latent elements 256v .. 256v +
+      // 255 as bf16 pairs in TMEM, rope elements 32v .. 32v + 31 in shared
+      // memory (64-byte swizzle).  The previous piece's products and output
+      // are done (o_done), so both may be overwritten.
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_latent + bh * kRow);
 #pragma unroll 1
-          for (int c = 0; c < kHalf / 32; ++c) {
-            float o[32];
-            tc_ld32(tmem + lane_addr + kOCol + 32 * c, o);
+        for (int cq = 0; cq < 4; ++cq) {  // 4 x 64 latent elements = 4 x 32 columns
+          uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= corr;
-            tc_st32(tmem + lane_addr + kOCol + 32 * c, o);
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = __ldg(src + (kHalf * v + 64 * cq) / 8 + u);
+            w[4 * u] = x.x;
+            w[4 * u + 1] = x.y;
+            w[4 * u + 2] = x.z;
+            w[4 * u + 3] = x.w;
           }
+          tc_st32u(tmem + lane_addr + kQCol + 32 * cq, w);
         }
-        if (need) {
-          l_run *= corr;
-          m_run = mx;
-        }
-      }
-      uint32_t pr[kTile / 2];
 #pragma unroll
-      for (int i = 0; i < kTile / 2; ++i) {
-        // a masked score is -inf and m_run is finite once a token was seen
-        const float p0 = s[2 * i] == -INFINITY ? 0.f : fast_exp2(s[2 * i] - m_run);
-        const float p1 = s[2 * i + 1] == -INFINITY ? 0.f : fast_exp2(s[2 * i + 1] - m_run);
-        l_run += p0 + p1;
-        pr[i] = pack_bf16x2(p0, p1);
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(smem + kQRopeOff + row * 64 + ((u ^ ((row >> 1) & 3)) << 4)) =
+              __ldg(src + (kLat + kRopeHalf * v) / 8 + u);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(q_full);
       }
-      // tokens that do not exist: zero their value rows (slots 0..3; 0 x NaN
-      // would poison P.V); piece j = (token j / 4, slot j % 4), two per thread
-      if (mask != ~0ull) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int j = row + kHT * h;
-          const int r = j >> 2;
-          if (!((mask >> r) & 1ull)) {
-            uint4* dst = reinterpret_cast<uint4*>(smem + kStageOff + stage * kStageBytes +
-                                                  (j & 3) * kChunkBytes + r * 128);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-      }
-      // the weight tile of tile t - 2 must have been consumed
-      if (t >= 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[k], ((t - 2) >> 1) & 1,
-                                                       abort_flag))) {
+      const int n = pc.te - pc.tb;
+      float m_run = -INFINITY, l_run = 0.f;
+      float s[kTile], s_next[kTile];
+      // software pipeline: tile t + 1's partials travel to the other CTA
+      // while this thread finishes tile t
+      ok = fetch_and_send(gbase, s);
+      for (int t = 0; t < n && ok; ++t) {
+        const int gt = gbase + t;
+        const int stage = gt % kStages;
+        const int k = gt & 1;
+        if (t + 1 < n && !fetch_and_send(gt + 1, s_next)) {
           ok = false;
           break;
         }
-      }
-      // weights -> shared memory buffer k, row `row` of 128 bytes, 128-byte
-      // swizzle (16-byte unit u at u ^ (row & 7)): the A operand of P.V
-      uint8_t* prow = smem + kPOff + k * kPBytes + row * 128;
+        // ---- the other CTA's partials of tile gt, in our buffer k
+        if (!__all_sync(0xffffffffu, wait_cluster_bounded(&recv_full[k], (gt >> 1) & 1,
+                                                          abort_flag))) {
+          ok = false;
+          break;
+        }
+        const float4* mine =
+            reinterpret_cast<const float4*>(smem + kRecvOff) + k * (kTile / 4) * kHT + row;
+        const uint64_t mask = tile_mask[stage];
+        float mx = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
-            make_uint4(pr[4 * u], pr[4 * u + 1], pr[4 * u + 2], pr[4 * u + 3]);
-      fence_proxy_async_smem();  // generic writes before the tensor core reads them
-      mbar_arrive(&p_full[k]);
+        for (int g = 0; g < kTile / 4; ++g) {
+          const float4 o = mine[g * kHT];
+          const float other[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-      for (int i = 0; i < kTile; ++i) s[i] = s_next[i];
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_final, 0, abort_flag));
-    if (!ok) {
-      *abort_flag = 1;
-      if (lane == 0) atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
-    } else {
-      // ---- epilogue: this thread's output row, elements 256v .. 256v + 255
-      tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const int64_t bh = bh0 + row;
+          for (int u = 0; u < 4; ++u) {
+            // own + other is the same sum on both CTAs (addition commutes),
+            // so both run an identical softmax
+            const int i = 4 * g + u;
+            const float full = s[i] + other[u];
+            s[i] = ((mask >> i) & 1ull) ? full * p.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, s[i]);
+          }
+        }
+        // buffer k is consumed (the values are in registers and used): re-arm
+        // it for tile gt + 2 and tell the other CTA
+        __syncwarp();
+        if (row == 0 && gt + 2 < ntotal) mbar_arrive_expect_tx(&recv_full[k], kRecvBytes);
+        if (lane == 0) arrive_peer_relaxed(sent_free_peer + 8 * k);
+        // lazy rescale; tcgen05.ld/st are warp-wide, so the warp rescales
+        // together when any of its rows needs it (the others scale by 1)
+        const bool need = mx > m_run + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float corr = need ? fast_exp2(m_run - mx) : 1.f;
+          if (t > 0) {
+            // the output row holds this piece's P.V up to tile gt - 1: wait for it
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[(gt - 1) & 1],
+                                                           ((gt - 1) >> 1) & 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < kHalf / 32; ++c) {
+            for (int cq = 0; cq < kHalf / 32; ++cq) {
+              float o[32];
+              tc_ld32(tmem + lane_addr + kOCol + 32 * cq, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= corr;
+              tc_st32(tmem + lane_addr + kOCol + 32 * cq, o);
+            }
+          }
+          if (need) {
+            l_run *= corr;
+            m_run = mx;
+          }
+        }
+        uint32_t pr[kTile / 2];
+#pragma unroll
+        for (int i = 0; i < kTile / 2; ++i) {
+          // a masked score is -inf and m_run is finite once a token was seen
+          const float p0 = s[2 * i] == -INFINITY ? 0.f : fast_exp2(s[2 * i] - m_run);
+          const float p1 = s[2 * i + 1] == -INFINITY ? 0.f : fast_exp2(s[2 * i + 1] - m_run);
+          l_run += p0 + p1;
+          pr[i] = pack_bf16x2(p0, p1);
+        }
+        // tokens that do not exist: zero their value rows (slots 0..3; 0 x NaN
+        // would poison P.V); piece j = (token j / 4, slot j % 4), two per thread
+        if (mask != ~0ull) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int j = row + kHT * hh;
+            const int r = j >> 2;
+            if (!((mask >> r) & 1ull)) {
+              uint4* dst = reinterpret_cast<uint4*>(smem + kStageOff + stage * kStageBytes +
+                                                    (j & 3) * kChunkBytes + r * 128);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+        }
+        // the weight tile of tile gt - 2 must have been consumed
+        if (gt >= 2) {
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[k], ((gt - 2) >> 1) & 1,
+                                                         abort_flag))) {
+            ok = false;
+            break;
+          }
+        }
+        // weights -> shared memory buffer k, row `row` of 128 bytes, 128-byte
+        // swizzle (16-byte unit u at u ^ (row & 7)): the A operand of P.V
+        uint8_t* prow = smem + kPOff + k * kPBytes + row * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
+              make_uint4(pr[4 * u], pr[4 * u + 1], pr[4 * u + 2], pr[4 * u + 3]);
+        fence_proxy_async_smem();  // generic writes before the tensor core reads them
+        mbar_arrive(&p_full[k]);
+#pragma unroll
+        for (int i = 0; i < kTile; ++i) s[i] = s_next[i];
+      }
+      if (!ok) break;
+      gbase += n;
+      // ---- epilogue of the piece: this thread's output row, elements
+      // 256v .. 256v + 255; bf16 when the piece is its whole sequence, else an
+      // fp32 partial in the piece's slot (and its log2-sum-exp)
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_done, npiece & 1, abort_flag));
+      if (!ok) break;
+      ++npiece;
+      tc_fence_after();
+      const bool whole = pc.tb == 0 && pc.te == pc.n;
+      const int64_t slot = static_cast<int64_t>(ht) * p.num_slots + piece_slot(pc, c);
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+      for (int cq = 0; cq < kHalf / 32; ++cq) {
         float o[32];
-        tc_ld32(tmem + lane_addr + kOCol + 32 * c, o);
-        if (p.num_splits == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + bh * kLat + kHalf * v + 32 * c);
+        tc_ld32(tmem + lane_addr + kOCol + 32 * cq, o);
+        if (whole) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + bh * kLat + kHalf * v + 32 * cq);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             dst[u] = make_uint4(pack_bf16x2(o[8 * u] * inv, o[8 * u + 1] * inv),
@@ -675,20 +873,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 pack_bf16x2(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
                                 pack_bf16x2(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
         } else {
-          float4* dst = reinterpret_cast<float4*>(
-              p.ws_o + (bh * p.num_splits + split) * kLat + kHalf * v + 32 * c);
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * kHT + row) * kLat + kHalf * v +
+                                                  32 * cq);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             dst[u] = make_float4(o[4 * u] * inv, o[4 * u + 1] * inv, o[4 * u + 2] * inv,
                                  o[4 * u + 3] * inv);
         }
       }
-      if (p.num_splits > 1 && v == 0)
-        p.ws_lse[bh * p.num_splits + split] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+      if (!whole) {
+        // both halves write the (identical) log2-sum-exp, each for its own merge
+        p.ws_lse[slot * kHT + row] = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+        // count this CTA's part once its 128 rows are written; the CTA
+        // completing the pieces of b for its half merges that half after its
+        // own work
+        mbar_arrive(part_done);
+        if (row == 0) {
+          if (!mbar_wait_bounded(part_done, npart & 1, abort_flag)) {
+            *abort_flag = 1;
+            atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+          }
+          __threadfence();
+          const int np = (pc.pre + pc.n - 1) / chunk - pc.pre / chunk + 1;
+          // one count per output half: the CTA completing half v merges half v
+          unsigned* ctr = p.counters + (static_cast<int64_t>(pc.b) * gridDim.y + ht) * 2 + v;
+          const unsigned prev = atomicAdd(ctr, 1u);
+          if (prev + 1u == static_cast<unsigned>(np)) {
+            atomicExch(ctr, 0u);
+            __threadfence();
+            const int m = sched[6];
+            if (m < kMaxMerges) {
+              merges[3 * m] = pc.b;
+              merges[3 * m + 1] = pc.pre;
+              merges[3 * m + 2] = pc.n;
+              sched[6] = m + 1;
+            }
+          }
+        }
+        ++npart;
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      if (lane == 0) atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
     }
   }
 
-  // ---- error path: wait (bounded) for the copies still in flight
+  // ---- end: drain on error, free TMEM, leave the cluster together, merge
   tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
@@ -696,8 +927,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int t = max(0, issued - kStages); t < issued; ++t)
         mbar_wait_bounded(&kv_full[t % kStages], (t / kStages) & 1, nullptr);
     }
-    if (p.num_splits > 1 && threadIdx.x < kHT)
-      p.ws_lse[(bh0 + threadIdx.x) * p.num_splits + split] = -INFINITY;
     __syncthreads();
   }
   if (warp == 1) {
@@ -708,30 +937,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   // neither CTA leaves while the other may still write into its shared memory
   cluster_sync_all();
-  if (p.num_splits == 1) return;
-
-  // ---- split count and merge: 2 CTAs per split; the CTA that completes
-  // the count of its (sequence, head tile) merges all 128 heads
-  const int n_valid = (L + p.tokens_per_split - 1) / p.tokens_per_split;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    unsigned* ctr = p.counters + static_cast<int64_t>(b) * (p.num_heads / kHT) + ht;
-    const unsigned prev = atomicAdd(ctr, 1u);
-    const bool last = prev + 1u == 2u * static_cast<unsigned>(n_valid);
-    if (last) {
-      atomicExch(ctr, 0u);
-      __threadfence();
-    }
-    flags[1] = last ? 1 : 0;
-  }
-  __syncthreads();
-  if (flags[1]) {
-    // the pipeline's shared memory is free now: per-head merge weights
-    if (kHT * n_valid * 4 <= kStages * kStageBytes)
-      mla_merge_cta(p, bh0, kHT, n_valid, reinterpret_cast<float*>(smem + kStageOff));
-    else
-      for (int h = warp; h < kHT; h += kThreads / 32) mla_merge_warp(p, bh0 + h, n_valid, lane);
-  }
+  const int nm = sched[6];
+  for (int i = 0; i < nm; ++i)
+    merge_pieces(p, merges[3 * i], ht, v, merges[3 * i + 1], merges[3 * i + 2], chunk,
+                 reinterpret_cast<float*>(smem + kStageOff));
 }
 
 }  // namespace

@@ -179,8 +179,12 @@ def test_mla_workspace_size(lib):
     assert lib.pa_mla_decode_workspace_size(4, 24, 512) == 0      # heads not a multiple of 16
     assert lib.pa_mla_decode_workspace_size(4, 128, -1) == 0
     assert lib.pa_mla_decode_workspace_size(0, 128, 512) >= 256
-    # one split for a short context on many sequences: the header alone
-    assert lib.pa_mla_decode_workspace_size(4096, 128, 32) == 256
+    # mma.sync kernel: one split for a short context on many sequences: the header alone
+    assert lib.pa_mla_decode_workspace_size(4096, 64, 32) == 256
+    # tcgen05 kernel (heads a multiple of 128): counters + two partial slots per
+    # cluster, independent of the context length
+    a = lib.pa_mla_decode_workspace_size(64, 128, 512)
+    assert a > 256 and a == lib.pa_mla_decode_workspace_size(64, 128, 131072)
 
 
 def test_mla_projections_reject(lib):

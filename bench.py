@@ -358,7 +358,9 @@ def timed_loop(fn, iters, warm, dev, flush_bytes=2 * L2_BYTES):
     """Median and mean device time of fn over `iters` calls.  Before each
     call, outside the timed events, L2 is flushed by READING a 258 MB buffer
     written once up front (a read leaves no dirty lines whose write-back
-    would land inside the timed kernel)."""
+    would land inside the timed kernel), and the GPU is kept busy by a short
+    device sleep while the host enqueues the call, so that host-side launch
+    work does not show up as idle time between the events."""
     import torch
     scratch = torch.ones(flush_bytes // 4, dtype=torch.float32, device=dev)
     sink = torch.empty((), dtype=torch.float32, device=dev)
@@ -368,6 +370,7 @@ def timed_loop(fn, iters, warm, dev, flush_bytes=2 * L2_BYTES):
     s = torch.cuda.current_stream()
     for _ in range(iters):
         torch.amax(scratch, dim=0, out=sink)
+        torch.cuda._sleep(200_000)  # ~100 us at 2 GHz: covers the host's enqueue of fn
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(s)
         fn()

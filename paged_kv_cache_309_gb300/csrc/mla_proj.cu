@@ -7,12 +7,15 @@
 //   project: out[b, h, i]    = sum_c o_lat[b, h, c] * W_UV[c, h*d_v + i]
 // Both are Y_h = X_h . W_h per head, bf16 in, fp32 accumulate, bf16 out, on
 // the tensor cores (mma.sync m16n8k16).  A CTA computes a 64 (sequences) x
-// 64 (outputs) tile of one head with four warps of 16 rows each; K advances
-// in 64-wide slices staged in padded shared memory (row stride 144 bytes,
-// so the eight rows of an ldmatrix phase hit eight different bank groups).
+// 64 (outputs) tile of one head with four warps of 16 rows each; the whole
+// K extent is staged once with cp.async in padded shared memory (16 bytes of
+// padding per row, so the eight rows of an ldmatrix phase hit eight
+// different bank groups).
 // W_UK_h is read with rows = outputs (ldmatrix), W_UV_h with rows = the
 // reduction index (ldmatrix.trans).  At decode batch sizes the weights are
 // the bytes that matter: each weight element is read once per 64 sequences.
+#include <atomic>
+
 #include "pa_internal.cuh"
 
 namespace pa_detail {
@@ -20,8 +23,8 @@ namespace {
 
 using namespace pa;
 
-constexpr int kTM = 64, kTN = 64, kTK = 64;
-constexpr int kPad = 72;  // elements per staged row (64 + 8)
+constexpr int kTM = 64, kTN = 64;
+constexpr int kPad = 72;  // elements per staged W_UV row (64 + 8)
 constexpr int kThreads = 128;
 
 struct ProjParams {
@@ -32,12 +35,26 @@ struct ProjParams {
   int32_t M, H, K, N, ldy, extra_dim;
 };
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p cp.async.cg.shared.global [%0], [%1], 16;\n\t"
+      "@!p st.shared.v4.u32 [%0], {0, 0, 0, 0};\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+}
+
 // kTransB = false: W(k, n) = w[n, h*K + k]   (absorb, rows = outputs)
 // kTransB = true:  W(k, n) = w[k, h*N + n]   (project, rows = reduction index)
+// The whole K extent of the CTA's X rows and weight columns is staged with
+// cp.async before any product: one global round trip per CTA instead of
+// one per 64-wide slice (the kernel is latency-bound at decode batch sizes).
 template <bool kTransB>
 __global__ void __launch_bounds__(kThreads) mla_head_gemm_kernel(const ProjParams p) {
-  __shared__ __align__(16) __nv_bfloat16 xs[kTM * kPad];
-  __shared__ __align__(16) __nv_bfloat16 ws[kTK * kPad];
+  extern __shared__ __align__(16) uint8_t dyn[];
+  const int ks = p.K + 8;  // staged row stride (elements): 16 bytes of padding per row
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(dyn);                 // [kTM][ks]
+  __nv_bfloat16* ws = xs + kTM * ks;  // absorb: [kTN rows = n][ks]; project: [K rows = k][kPad]
   const int n0 = blockIdx.x * kTN;
   const int h = blockIdx.y;
   const int m0 = blockIdx.z * kTM;
@@ -45,53 +62,60 @@ __global__ void __launch_bounds__(kThreads) mla_head_gemm_kernel(const ProjParam
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int64_t xrow = static_cast<int64_t>(p.H) * p.K;
+  const int kunits = p.K / 8;  // 16-byte units per X row / absorb weight row
+
+  for (int i = threadIdx.x; i < kTM * kunits; i += kThreads) {
+    const int r = i / kunits, u = i % kunits;
+    const bool ok = m0 + r < p.M;
+    cp_async16(xs + r * ks + 8 * u,
+               p.x + (ok ? (m0 + r) * xrow : 0) + static_cast<int64_t>(h) * p.K + 8 * u, ok);
+  }
+  if constexpr (kTransB) {
+    for (int i = threadIdx.x; i < p.K * 8; i += kThreads) {
+      const int r = i >> 3, u = i & 7;
+      cp_async16(ws + r * kPad + 8 * u,
+                 p.w + static_cast<int64_t>(r) * p.H * p.N + static_cast<int64_t>(h) * p.N + n0 +
+                     8 * u,
+                 true);
+    }
+  } else {
+    for (int i = threadIdx.x; i < kTN * kunits; i += kThreads) {
+      const int r = i / kunits, u = i % kunits;
+      cp_async16(ws + r * ks + 8 * u,
+                 p.w + static_cast<int64_t>(n0 + r) * p.H * p.K + static_cast<int64_t>(h) * p.K +
+                     8 * u,
+                 true);
+    }
+  }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
 
   float acc[kTN / 8][4];
 #pragma unroll
   for (int nt = 0; nt < kTN / 8; ++nt)
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[nt][c] = 0.f;
-
   const uint32_t xs_base = smem_u32(xs);
   const uint32_t ws_base = smem_u32(ws);
-  for (int k0 = 0; k0 < p.K; k0 += kTK) {
-    // stage X[m0.., h, k0..] and the weight slice: 64 rows x 8 units of 16 B each
-    for (int i = threadIdx.x; i < 64 * 8; i += kThreads) {
-      const int r = i >> 3, u = i & 7;
-      uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-      if (m0 + r < p.M)
-        xv = __ldg(reinterpret_cast<const uint4*>(p.x + (m0 + r) * xrow +
-                                                  static_cast<int64_t>(h) * p.K + k0) + u);
-      *reinterpret_cast<uint4*>(xs + r * kPad + 8 * u) = xv;
-      const __nv_bfloat16* wsrc =
-          kTransB ? p.w + static_cast<int64_t>(k0 + r) * p.H * p.N + static_cast<int64_t>(h) * p.N + n0
-                  : p.w + static_cast<int64_t>(n0 + r) * p.H * p.K + static_cast<int64_t>(h) * p.K + k0;
-      *reinterpret_cast<uint4*>(ws + r * kPad + 8 * u) =
-          __ldg(reinterpret_cast<const uint4*>(wsrc) + u);
-    }
-    __syncthreads();
+  for (int kk = 0; kk < p.K / 16; ++kk) {
+    uint32_t a[4];
+    ldsm_x4(xs_base + static_cast<uint32_t>(((16 * warp + (lane & 15)) * ks + 16 * kk +
+                                            8 * (lane >> 4)) * 2), a);
 #pragma unroll
-    for (int kk = 0; kk < kTK / 16; ++kk) {
-      uint32_t a[4];
-      ldsm_x4(xs_base + static_cast<uint32_t>(((16 * warp + (lane & 15)) * kPad + 16 * kk +
-                                              8 * (lane >> 4)) * 2), a);
-#pragma unroll
-      for (int np = 0; np < kTN / 16; ++np) {
-        uint32_t bb[4];
-        if constexpr (kTransB) {
-          // rows = k: lanes 0-7 k 0-7, 8-15 k 8-15 (n 0-7), 16-31 the same for n 8-15
-          const int kr = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
-          ldsm_x4_trans(ws_base + static_cast<uint32_t>((kr * kPad + 16 * np + 8 * (lane >> 4)) * 2), bb);
-        } else {
-          // rows = n: lanes 0-7 n 0-7 k 0-7, 8-15 n 0-7 k 8-15, 16-31 the same for n 8-15
-          const int nr = 16 * np + (lane & 7) + 8 * (lane >> 4);
-          ldsm_x4(ws_base + static_cast<uint32_t>((nr * kPad + 16 * kk + 8 * ((lane >> 3) & 1)) * 2), bb);
-        }
-        mma_bf16_16816(acc[2 * np], a, bb[0], bb[1]);
-        mma_bf16_16816(acc[2 * np + 1], a, bb[2], bb[3]);
+    for (int np = 0; np < kTN / 16; ++np) {
+      uint32_t bb[4];
+      if constexpr (kTransB) {
+        // rows = k: lanes 0-7 k 0-7, 8-15 k 8-15 (n 0-7), 16-31 the same for n 8-15
+        const int kr = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
+        ldsm_x4_trans(ws_base + static_cast<uint32_t>((kr * kPad + 16 * np + 8 * (lane >> 4)) * 2), bb);
+      } else {
+        // rows = n: lanes 0-7 n 0-7 k 0-7, 8-15 n 0-7 k 8-15, 16-31 the same for n 8-15
+        const int nr = 16 * np + (lane & 7) + 8 * (lane >> 4);
+        ldsm_x4(ws_base + static_cast<uint32_t>((nr * ks + 16 * kk + 8 * ((lane >> 3) & 1)) * 2), bb);
       }
+      mma_bf16_16816(acc[2 * np], a, bb[0], bb[1]);
+      mma_bf16_16816(acc[2 * np + 1], a, bb[2], bb[3]);
     }
-    __syncthreads();
   }
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -115,6 +139,28 @@ __global__ void __launch_bounds__(kThreads) mla_head_gemm_kernel(const ProjParam
   }
 }
 
+template <bool kTransB>
+size_t gemm_smem_bytes(int K) {
+  return static_cast<size_t>(kTM) * (K + 8) * 2 +
+         (kTransB ? static_cast<size_t>(K) * kPad * 2 : static_cast<size_t>(kTN) * (K + 8) * 2);
+}
+
+template <bool kTransB>
+pa_status launch_gemm(const ProjParams& p, dim3 grid, cudaStream_t stream) {
+  constexpr int kMaxSmem = 200 * 1024;
+  const size_t smem = gemm_smem_bytes<kTransB>(p.K);
+  if (smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
+  static std::atomic<bool> attr_set{false};
+  if (!attr_set.load()) {
+    if (cudaFuncSetAttribute(mla_head_gemm_kernel<kTransB>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
+      return PA_ERR_CUDA;
+    attr_set.store(true);
+  }
+  mla_head_gemm_kernel<kTransB><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace
 
 pa_status launch_mla_absorb_q(void* q_latent, const void* q_nope, const void* q_pe,
@@ -134,8 +180,7 @@ pa_status launch_mla_absorb_q(void* q_latent, const void* q_nope, const void* q_
   p.extra_dim = rope_dim;
   const dim3 grid(static_cast<unsigned>(latent_dim / kTN), static_cast<unsigned>(num_heads),
                   static_cast<unsigned>((num_seqs + kTM - 1) / kTM));
-  mla_head_gemm_kernel<false><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return launch_gemm<false>(p, grid, stream);
 }
 
 pa_status launch_mla_project_out(void* out, const void* out_latent, const void* w_uv,
@@ -154,8 +199,7 @@ pa_status launch_mla_project_out(void* out, const void* out_latent, const void* 
   p.extra_dim = 0;
   const dim3 grid(static_cast<unsigned>(v_head_dim / kTN), static_cast<unsigned>(num_heads),
                   static_cast<unsigned>((num_seqs + kTM - 1) / kTM));
-  mla_head_gemm_kernel<true><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  return launch_gemm<true>(p, grid, stream);
 }
 
 }  // namespace pa_detail

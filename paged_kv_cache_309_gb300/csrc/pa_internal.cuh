@@ -495,6 +495,7 @@ struct PrefillArgs {
   float scale;
 };
 pa_status launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream);
+pa_status launch_paged_prefill_tc(const PrefillArgs& a, cudaStream_t stream);  // prefill_tc.cu
 
 struct MlaDecodeArgs {
   void* out_latent;          // [B, H, 512] bf16

@@ -349,6 +349,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 pa_status launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.max_q_len == 0) return PA_OK;
+  return launch_paged_prefill_tc(a, stream);
+}
+
+// the mma.sync kernel above (64-row tiles), kept for comparison
+pa_status launch_paged_prefill_mma(const PrefillArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0 || a.max_q_len == 0) return PA_OK;
   const int32_t G = a.num_q_heads / a.num_kv_heads;
   const int64_t rows = a.num_blocks * a.block_size;
   const int32_t box_rows = a.block_size < kTile ? a.block_size : kTile;

@@ -599,6 +599,28 @@ def run_mla_only(args):
     print(f"{w.name}: {args.steps} launches, device error word {pa.read_device_error(ws)}")
 
 
+def run_prefill_only(args):
+    """Causal prefill launches only (for an ncu capture of that kernel)."""
+    import torch
+
+    from paged_kv_cache_309_gb300 import build, pa
+    from paged_kv_cache_309_gb300 import workloads as wl
+    build.build()
+    dev = torch.device("cuda", 0)
+    pw = wl.make_prefill("prefill_attention_b4_8k", 5, [8192] * 4, [8192] * 4, 32, 8, 128, 16)
+    pq = up(pw.q, torch.bfloat16, dev)
+    pout = torch.empty_like(pq)
+    pkc, pvc = up(pw.k_cache, torch.bfloat16, dev), up(pw.v_cache, torch.bfloat16, dev)
+    pbt, pcu = torch.from_numpy(pw.block_tables).to(dev), torch.from_numpy(pw.cu_seqlens_q).to(dev)
+    pcl = torch.from_numpy(pw.context_lens).to(dev)
+    perr = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(args.steps):
+        pa.pa_paged_prefill_attention(pout, pq, pkc, pvc, pbt, pcu, pcl, pw.scale, pw.max_q_len,
+                                      perr)
+    torch.cuda.synchronize()
+    print(f"{pw.name}: {args.steps} launches, device error word {int(perr.item())}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -615,6 +637,9 @@ def main():
     ap.add_argument("--extra-iters", type=int, default=50)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="profiling aid: only run --steps causal prefill launches on the "
+                         "4 x 8192-token workload (no JSON)")
     ap.add_argument("--mla-heads", type=int, default=0,
                     help="profiling aid: only run --steps MLA decode attention launches on the "
                          "B=64 context 512..4096 latent workload with this many heads (no JSON)")
@@ -623,6 +648,9 @@ def main():
         args.warmup = 3
     if args.mla_heads:
         run_mla_only(args)
+        return
+    if args.prefill_only:
+        run_prefill_only(args)
         return
     if args.impl == "reference":
         run_reference(args)

@@ -589,9 +589,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                mbar_wait_bounded(&kv_full[u % kStages], (u / kStages) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, w)) return false;
       tc_fence_after();
-      tc_ld32(tmem + lane_addr + kSCol + kTile * ku, *reinterpret_cast<float(*)[32]>(&sp[0]));
-      tc_ld32(tmem + lane_addr + kSCol + kTile * ku + 32,
-              *reinterpret_cast<float(*)[32]>(&sp[32]));
+      tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * ku, &sp[0]);
+      tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * ku + 32, &sp[32]);
+      tc_wait_ld();
       tc_fence_before();
       mbar_arrive(&s_empty[ku]);
       if (u >= 2 && !__all_sync(0xffffffffu, wait_cluster_bounded(&sent_free[ku],
@@ -663,7 +663,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float4* mine =
             reinterpret_cast<const float4*>(smem + kRecvOff) + k * (kTile / 4) * kHT + row;
         const uint64_t mask = tile_mask[stage];
-        float mx = -INFINITY;
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
         for (int g = 0; g < kTile / 4; ++g) {
           const float4 o = mine[g * kHT];
@@ -675,9 +675,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int i = 4 * g + u;
             const float full = s[i] + other[u];
             s[i] = ((mask >> i) & 1ull) ? full * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, s[i]);
+            mq[u] = fmaxf(mq[u], s[i]);
           }
         }
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         // buffer k is consumed (the values are in registers and used): re-arm
         // it for tile gt + 2 and tell the other CTA
         __syncwarp();
@@ -711,14 +712,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         uint32_t pr[kTile / 2];
+        float lq[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
 #pragma unroll
         for (int i = 0; i < kTile / 2; ++i) {
           // a masked score is -inf and m_run is finite once a token was seen
           const float p0 = s[2 * i] == -INFINITY ? 0.f : fast_exp2(s[2 * i] - m_run);
           const float p1 = s[2 * i + 1] == -INFINITY ? 0.f : fast_exp2(s[2 * i + 1] - m_run);
-          l_run += p0 + p1;
+          lq[i & 3] += p0 + p1;
           pr[i] = pack_bf16x2(p0, p1);
         }
+        l_run += (lq[0] + lq[1]) + (lq[2] + lq[3]);
         // tokens that do not exist: zero their value rows (slots 0..3; 0 x NaN
         // would poison P.V); piece j = (token j / 4, slot j % 4), two per thread
         if (mask != ~0ull) {

@@ -301,6 +301,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// As mbar_wait_bounded, for waits that are usually long (a whole pipeline
+// step): each try_wait may keep the thread suspended for up to `hint_ns`
+// (it resumes as soon as the phase completes), so a waiting warp re-polls
+// rarely and leaves the issue slots of its SM sub-partition to the warps
+// that compute.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_bounded_long(uint64_t* bar, uint32_t parity,
+                                                       volatile int* abort_flag) {
+  constexpr uint32_t kHintNs = 20000;
+  if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
+    if (abort_flag && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
 // 3-D tiled TMA load global -> shared, completion counted on `bar`.
 // L2 hint: the K/V stream is read once, evict it first.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t c0,

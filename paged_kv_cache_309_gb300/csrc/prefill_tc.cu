@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = t % kStages;
       if (t >= kStages) {
         ok = __all_sync(0xffffffffu,
-                        mbar_wait_bounded(&empty[st], ((t / kStages) - 1) & 1, abort_flag));
+                        mbar_wait_bounded_long(&empty[st], ((t / kStages) - 1) & 1, abort_flag));
         if (!ok) break;
       }
       issue_tile_half(p, tm, smem + kStageOff + st * kStageBytes + (is_k ? 0 : 2 * kChunk),
@@ -286,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = ntiles == 0 || mbar_wait_bounded(q_full, 0, abort_flag);
         tc_fence_after();
         for (int t = 0; ok && t < ntiles; ++t) {
-          ok = mbar_wait_bounded(&k_full[t % kStages], (t / kStages) & 1, abort_flag) &&
-               (t < 2 || mbar_wait_bounded(&s_empty[t & 1], ((t - 2) >> 1) & 1, abort_flag));
+          ok = mbar_wait_bounded_long(&k_full[t % kStages], (t / kStages) & 1, abort_flag) &&
+               (t < 2 || mbar_wait_bounded_long(&s_empty[t & 1], ((t - 2) >> 1) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
           // S(t) = Q . K(t)^T: 8 k-steps of 16 over the 128 head elements,
@@ -305,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         for (int u = 0; ok && u < ntiles; ++u) {
-          ok = mbar_wait_bounded(&p_full[u & 1], (u >> 1) & 1, abort_flag) &&
-               mbar_wait_bounded(&v_full[u % kStages], (u / kStages) & 1, abort_flag);
+          ok = mbar_wait_bounded_long(&p_full[u & 1], (u >> 1) & 1, abort_flag) &&
+               mbar_wait_bounded_long(&v_full[u % kStages], (u / kStages) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           // O += P(u) . V(u): 8 k-steps of 16 keys; P from TMEM, V = chunks
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, mn2);
         const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
         lq[i & 1] = fadd2(lq[i & 1], e);
-        pr[i] = pack_bf16x2(e.x, e.y);
+        pr[i] = pack_bf16x2_rn(e.x, e.y);
       }
       l_part += (lq[0].x + lq[0].y) + (lq[1].x + lq[1].y);
       tc_st32u_nowait(tmem + lane_addr + kPCol + (kTile / 2) * k + 32 * half, &pr[0]);

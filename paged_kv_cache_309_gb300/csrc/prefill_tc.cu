@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc2, mn2);
         const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
         lq[i & 1] = fadd2(lq[i & 1], e);
-        pr[i] = pack_bf16x2_rn(e.x, e.y);
+        pr[i] = pack_bf16x2(e.x, e.y);
       }
       l_part += (lq[0].x + lq[0].y) + (lq[1].x + lq[1].y);
       tc_st32u_nowait(tmem + lane_addr + kPCol + (kTile / 2) * k + 32 * half, &pr[0]);

@@ -164,13 +164,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
-// two floats rounded to nearest-even bf16 and packed (lo in bits 0-15) in
-// one conversion instruction
-__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 // max of three (one instruction on sm_100 and later)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

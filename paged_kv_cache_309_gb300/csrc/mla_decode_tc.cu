@@ -77,7 +77,7 @@ constexpr int kBarOff = kQRopeOff + kQRopeBytes;
 // barriers: q_full, kv_full[kStages], kv_empty[kStages], s_full[2],
 // s_empty[2], p_full[2], pv_done[2], recv_full[2], sent_free[2], o_done,
 // drain, part_done; then tile masks, the TMEM slot and flags, the schedule
-constexpr int kNumBars = 16 + 2 * kStages;
+constexpr int kNumBars = 17 + 2 * kStages;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
 constexpr int kMiscOff = kMaskOff + kStages * 8;
 constexpr int kSchedOff = kMiscOff + 32;             // schedule words and the merge list
@@ -248,65 +248,136 @@ struct PieceIter {
 __device__ __forceinline__ int piece_slot(const Piece& pc, int c) { return 2 * c + (pc.first ? 0 : 1); }
 
 // Merge of output half v of the 128 heads of (sequence b, head tile ht)
-// over its pieces, by the whole CTA: the pieces are clusters c_first ..
-// c_last; slot of the first one 2 c_first (+1 if it is not that cluster's
-// first piece), of the others 2c.  Per-head weights 2^(lse - max) go to
-// `wsm` first; then each thread sums 8 four-element columns at a time with
-// all their loads in flight (L2 round trips, not bandwidth, bound a merge).
+// over its pieces, by the whole CTA once its own work is done: the pieces
+// are clusters c_first .. c_last; slot of the first one 2 c_first (+1 if it
+// is not that cluster's first piece), of the others 2c.  Piece i gets weight
+// 2^(lse_i - M) / sum_j 2^(lse_j - M) per head (M the heads' maximum).  The
+// partials are stored half-major ([slot][half][head][256] floats), so the
+// rows of a group of kMrgHeads heads of one piece are one contiguous bulk
+// copy; up to kMrgPieces pieces of a group land under one barrier, and each
+// thread sums eight 16-byte columns of the group from shared memory.
+constexpr int kMrgHeads = 24;
+constexpr int kMrgPieces = 7;
+constexpr int kMrgStageBytes = kMrgPieces * kMrgHeads * kHalf * 4;  // 168 KB
+static_assert(kMrgStageBytes + (2 * kHT + kMrgPieces * kHT) * 4 <= kBarOff,
+              "merge staging fits below the barriers");
+static_assert(kThreads * 8 >= kMrgHeads * kHalf / 4, "eight columns per thread cover a group");
 __device__ __forceinline__ void merge_pieces(const MlaParams& p, int b, int ht, int v, int pre,
-                                             int n, int chunk, float* wsm) {
+                                             int n, int chunk, uint8_t* stage, float* wsm,
+                                             uint64_t* bar, uint32_t& phase) {
   const int c_first = pre / chunk, c_last = (pre + n - 1) / chunk;
   const int np = c_last - c_first + 1;
   const int s0 = 2 * c_first + (pre != c_first * chunk ? 1 : 0);
   auto slot = [&](int i) { return i == 0 ? s0 : 2 * (c_first + i); };
   const int64_t base = static_cast<int64_t>(ht) * p.num_slots;
   const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + ht * kHT;
-  for (int h = threadIdx.x; h < kHT; h += blockDim.x) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  float* wmax = wsm;             // [kHT] per-head maximum of the pieces' lse
+  float* winv = wsm + kHT;       // [kHT] 1 / sum of the weights
+  float* wb = wsm + 2 * kHT;     // [kMrgPieces][kHT] weights of the current batch
+  for (int h = tid; h < kHT; h += nthr) {
+    if (np <= kMrgPieces) {
+      // every piece's lse in flight at once; the weights of all pieces here
+      float l[kMrgPieces];
+#pragma unroll
+      for (int j = 0; j < kMrgPieces; ++j)
+        l[j] = j < np ? __ldcg(p.ws_lse + (base + slot(j)) * kHT + h) : -INFINITY;
+      float M = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kMrgPieces; ++j) M = fmaxf(M, l[j]);
+      float W = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < kMrgPieces; ++j) W += exp2f(l[j] - M);  // 2^-inf = 0 for padding
+      }
+      const float inv = W > 0.f ? 1.f / W : 0.f;
+      wmax[h] = M;
+      winv[h] = inv;
+#pragma unroll
+      for (int j = 0; j < kMrgPieces; ++j)
+        if (j < np) wb[j * kHT + h] = M == -INFINITY ? 0.f : exp2f(l[j] - M) * inv;
+      continue;
+    }
     float M = -INFINITY;
-    for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(p.ws_lse + (base + slot(i)) * kHT + h));
+    for (int i0 = 0; i0 < np; i0 += 4) {
+      float l[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        l[j] = i0 + j < np ? __ldcg(p.ws_lse + (base + slot(i0 + j)) * kHT + h) : -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) M = fmaxf(M, l[j]);
+    }
     float W = 0.f;
-    for (int i = 0; i < np; ++i) {
-      const float w = M == -INFINITY ? 0.f : exp2f(__ldcg(p.ws_lse + (base + slot(i)) * kHT + h) - M);
-      wsm[h * np + i] = w;
-      W += w;
-    }
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    for (int i = 0; i < np; ++i) wsm[h * np + i] *= inv;
-  }
-  __syncthreads();
-  constexpr int kCols = kHalf / 4;  // four-element columns of one head's half
-  constexpr int kBatch = 8;
-  for (int idx0 = threadIdx.x * kBatch; idx0 < kHT * kCols; idx0 += blockDim.x * kBatch) {
-    float4 acc[kBatch];
+    if (M != -INFINITY) {
+      for (int i0 = 0; i0 < np; i0 += 4) {
+        float l[4];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < np; ++i) {
-      float4 x[kBatch];
+        for (int j = 0; j < 4; ++j)
+          l[j] = i0 + j < np ? __ldcg(p.ws_lse + (base + slot(i0 + j)) * kHT + h) : -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int idx = idx0 + u;
-        const int h = idx / kCols, e4 = idx % kCols;
-        x[u] = __ldcg(reinterpret_cast<const float4*>(
-                          p.ws_o + ((base + slot(i)) * kHT + h) * kLat + kHalf * v) + e4);
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const float w = wsm[((idx0 + u) / kCols) * np + i];
-        acc[u].x += w * x[u].x;
-        acc[u].y += w * x[u].y;
-        acc[u].z += w * x[u].z;
-        acc[u].w += w * x[u].w;
+        for (int j = 0; j < 4; ++j) W += exp2f(l[j] - M);  // 2^-inf = 0 for the padding
       }
     }
+    wmax[h] = M;
+    winv[h] = W > 0.f ? 1.f / W : 0.f;
+  }
+  fence_proxy_async_global();  // the partials were written by ordinary stores
+  __syncthreads();
+  constexpr int kCol4 = kHalf / 4;  // 16-byte columns of one head's half row
+  for (int hg0 = 0; hg0 < kHT; hg0 += kMrgHeads) {
+    const int nh = min(kMrgHeads, kHT - hg0);
+    float4 acc[8];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int idx = idx0 + u;
-      const int h = idx / kCols, e4 = idx % kCols;
-      *reinterpret_cast<uint2*>(p.out + (bh0 + h) * kLat + kHalf * v + 4 * e4) =
-          make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+    for (int u = 0; u < 8; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < np; i0 += kMrgPieces) {
+      const int npb = min(kMrgPieces, np - i0);
+      if (np > kMrgPieces) {
+        for (int idx = tid; idx < npb * nh; idx += nthr) {
+          const int j = idx / nh, hh = idx % nh;
+          const float M = wmax[hg0 + hh];
+          const float l = __ldcg(p.ws_lse + (base + slot(i0 + j)) * kHT + hg0 + hh);
+          wb[j * kHT + hg0 + hh] = M == -INFINITY ? 0.f : exp2f(l - M) * winv[hg0 + hh];
+        }
+      }
+      if (tid == 0) {
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(npb * nh * kHalf * 4));
+        for (int j = 0; j < npb; ++j)
+          bulk_load(stage + j * kMrgHeads * (kHalf * 4),
+                    p.ws_o + ((base + slot(i0 + j)) * 2 + v) * kHT * kHalf +
+                        static_cast<int64_t>(hg0) * kHalf,
+                    static_cast<uint32_t>(nh * kHalf * 4), bar);
+      }
+      if (!mbar_wait_bounded(bar, phase, nullptr) && tid == 0) atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+      phase ^= 1u;
+      __syncthreads();  // the batch weights are written
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int col = tid + nthr * u;
+        if (col < nh * kCol4) {
+          const int hh = col / kCol4, e4 = col % kCol4;
+          for (int j = 0; j < npb; ++j) {
+            const float4 x = reinterpret_cast<const float4*>(
+                stage + (j * kMrgHeads + hh) * (kHalf * 4))[e4];
+            const float w = wb[(np > kMrgPieces ? j : i0 + j) * kHT + hg0 + hh];
+            acc[u].x += w * x.x;
+            acc[u].y += w * x.y;
+            acc[u].z += w * x.z;
+            acc[u].w += w * x.w;
+          }
+        }
+      }
+      __syncthreads();  // the staging buffers and weights are free again
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int col = tid + nthr * u;
+      if (col < nh * kCol4) {
+        const int hh = col / kCol4, e4 = col % kCol4;
+        *reinterpret_cast<uint2*>(p.out + (bh0 + hg0 + hh) * kLat + kHalf * v + 4 * e4) =
+            make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+      }
     }
   }
-  __syncthreads();
 }
 
 // ------------------------------------------------------------------ kernel --
@@ -327,6 +398,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* o_done = sent_free + 2;              // every product of the current piece done
   uint64_t* drain = o_done + 1;                  // error path: issued products done
   uint64_t* part_done = drain + 1;               // a partial's 128 rows are written
+  uint64_t* mrg_full = part_done + 1;            // a merge batch's partial rows landed
   uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);  // [0] abort
@@ -409,6 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(part_done, kHT);
+    mbar_init(mrg_full, 1);
     flags[0] = 0;
     mbar_init_fence();
     // the first two exchanges: expect one tile of partials in each buffer
@@ -619,23 +692,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // are done (o_done), so both may be overwritten.
       {
         const uint4* src = reinterpret_cast<const uint4*>(p.q_latent + bh * kRow);
-#pragma unroll 1
-        for (int cq = 0; cq < 4; ++cq) {  // 4 x 64 latent elements = 4 x 32 columns
-          uint32_t w[32];
+        // two chunks per global round trip (4 x 64 latent elements = 4 x 32
+        // columns); the rope part rides with the first pair
+        uint4 rope[4];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) rope[u] = __ldg(src + (kLat + kRopeHalf * v) / 8 + u);
+#pragma unroll 1
+        for (int cq = 0; cq < 4; cq += 2) {
+          uint32_t w[64];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
             const uint4 x = __ldg(src + (kHalf * v + 64 * cq) / 8 + u);
             w[4 * u] = x.x;
             w[4 * u + 1] = x.y;
             w[4 * u + 2] = x.z;
             w[4 * u + 3] = x.w;
           }
-          tc_st32u(tmem + lane_addr + kQCol + 32 * cq, w);
+          tc_st32u_nowait(tmem + lane_addr + kQCol + 32 * cq, &w[0]);
+          tc_st32u_nowait(tmem + lane_addr + kQCol + 32 * cq + 32, &w[32]);
+          tc_wait_st();
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           *reinterpret_cast<uint4*>(smem + kQRopeOff + row * 64 + ((u ^ ((row >> 1) & 3)) << 4)) =
-              __ldg(src + (kLat + kRopeHalf * v) / 8 + u);
+              rope[u];
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(q_full);
@@ -782,7 +862,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 pack_bf16x2(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
                                 pack_bf16x2(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
         } else {
-          float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * kHT + row) * kLat + kHalf * v +
+          // partials are half-major, [slot][half][head][256]: one half's rows
+          // of consecutive heads are contiguous for the merge's bulk copies
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + ((slot * 2 + v) * kHT + row) * kHalf +
                                                   32 * cq);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
@@ -847,9 +929,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // neither CTA leaves while the other may still write into its shared memory
   cluster_sync_all();
   const int nm = sched[6];
+  uint32_t mrg_phase = 0;
   for (int i = 0; i < nm; ++i)
     merge_pieces(p, merges[3 * i], ht, v, merges[3 * i + 1], merges[3 * i + 2], chunk,
-                 reinterpret_cast<float*>(smem + kStageOff));
+                 smem + kStageOff, reinterpret_cast<float*>(smem + kStageOff + kMrgStageBytes),
+                 mrg_full, mrg_phase);
 }
 
 }  // namespace

@@ -61,7 +61,8 @@ constexpr int kHT = 128;               // heads per CTA (M)
 constexpr int kTile = 64;              // tokens per tile (N of S, K of P.V)
 constexpr int kHalf = kLat / 2;        // output (and latent) elements per CTA
 constexpr int kRopeHalf = kRope / 2;   // rope elements per CTA
-constexpr int kThreads = 6 * 32;
+constexpr int kThreads = 7 * 32;
+constexpr int kPVWarp = 6;  // P.V products (warp 1: score products, TMEM owner)
 constexpr int kChunkBytes = kTile * 128;             // one 64-element chunk of a tile: 8 KB
 constexpr int kLoadChunks = kHalf / 64 + 1;          // 4 latent chunks + the rope chunk
 constexpr int kStageBytes = kLoadChunks * kChunkBytes;  // 40 KB
@@ -77,7 +78,7 @@ constexpr int kBarOff = kQRopeOff + kQRopeBytes;
 // barriers: q_full, kv_full[kStages], kv_empty[kStages], s_full[2],
 // s_empty[2], p_full[2], pv_done[2], recv_full[2], sent_free[2], o_done,
 // drain, part_done; then tile masks, the TMEM slot and flags, the schedule
-constexpr int kNumBars = 17 + 2 * kStages;
+constexpr int kNumBars = 18 + 2 * kStages;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
 constexpr int kMiscOff = kMaskOff + kStages * 8;
 constexpr int kSchedOff = kMiscOff + 32;             // schedule words and the merge list
@@ -396,8 +397,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* recv_full = pv_done + 2;             // [2] the other CTA's partials landed here
   uint64_t* sent_free = recv_full + 2;           // [2] the other CTA consumed what we sent
   uint64_t* o_done = sent_free + 2;              // every product of the current piece done
-  uint64_t* drain = o_done + 1;                  // error path: issued products done
-  uint64_t* part_done = drain + 1;               // a partial's 128 rows are written
+  uint64_t* drain = o_done + 1;                  // [2] each issuer's products done
+  uint64_t* part_done = drain + 2;               // a partial's 128 rows are written
   uint64_t* mrg_full = part_done + 1;            // a merge batch's partial rows landed
   uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
@@ -479,7 +480,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&sent_free[s], 4);   // one arrival per softmax warp of the other CTA
     }
     mbar_init(o_done, 1);
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     mbar_init(part_done, kHT);
     mbar_init(mrg_full, 1);
     flags[0] = 0;
@@ -545,101 +547,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
       atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
     }
-  } else if (warp == 1) {
-    // --------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == kPVWarp) {
+    // -------------------------------------------------------- MMA issuers
+    // One thread of warp 1 issues the score products, one thread of the P.V
+    // warp the output products; each blocks in its own bounded waits and
+    // commits its own products (a commit tracks the issuing thread's).
     if (lane == 0) {
+      const bool is_s = warp == 1;
       const uint32_t st_base = smem_u32(smem + kStageOff);
       const uint32_t p_base = smem_u32(smem + kPOff);
       const uint32_t qr_base = smem_u32(smem + kQRopeOff);
-      auto issue_s = [&](int t) {
-        // partial S(t) = Q_v . K_v(t)^T over this CTA's 288 elements: 16
-        // latent k-steps with A = q_lat latent part in TMEM and B = chunk
-        // slots 0..3, then 2 rope k-steps with A = the rope part in shared
-        // memory (64-byte swizzle) and B = slot 4 at elements 32v..32v+31.
-        // B is K-major 128-byte swizzled (a k-step advances the start by 32
-        // bytes inside a 64-element chunk).
-        const uint32_t kb = st_base + (t % kStages) * kStageBytes;
-        const uint32_t d = tmem + kSCol + kTile * (t & 1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          tc_mma_ts(d, tmem + kQCol + 8 * i,
-                    smem_desc(kb + (i >> 2) * kChunkBytes + 32 * (i & 3), 16, 1024), kIdescS,
-                    i > 0 ? 1u : 0u);
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          tc_mma_ss(d, smem_desc(qr_base + 32 * i, 16, 512, kSwizzle64),
-                    smem_desc(kb + 4 * kChunkBytes + 64 * v + 32 * i, 16, 1024), kIdescS, 1u);
-        tc_commit(&s_full[t & 1]);
-      };
-      auto issue_pv = [&](int u, bool fresh) {
-        // O[:, this half] += P(u) . V(u): P = the bf16 weights in shared
-        // memory (K-major, 128-byte swizzle), V = slots 0..3 of tile u,
-        // MN-major (leading offset: next 64 elements = next slot; stride
-        // offset: next 8 tokens = 1 KB); 16 tokens per product.  The first
-        // tile of a piece starts the output afresh.
-        const uint32_t vb = st_base + (u % kStages) * kStageBytes;
-        const uint32_t pb = p_base + (u & 1) * kPBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          tc_mma_ss(tmem + kOCol, smem_desc(pb + 32 * kk, 16, 1024),
-                    smem_desc(vb + kk * 2048, kChunkBytes, 1024), kIdescPV,
-                    (!fresh || kk > 0) ? 1u : 0u);
-        tc_commit(&pv_done[u & 1]);
-        tc_commit(&kv_empty[u % kStages]);
-      };
-      // Issue whichever product is ready, never blocking on one while the
-      // other could go: S(ns) needs its tile, its score buffer (read by the
-      // softmax two tiles ago) and, on a piece's first tile, that piece's
-      // q_lat; P.V(npv) needs the softmax's weights.  After a piece's last
-      // P.V, o_done tells the softmax its output is complete.
-      PieceIter its = it0, itp = it0;
-      Piece pcs, pcp;
-      int ts = its.next(p, pcs) ? pcs.tb : 0;
-      int tp = itp.next(p, pcp) ? pcp.tb : 0;
-      int ks = 0;  // piece ordinal of the S cursor
-      int ns = 0, npv = 0;
+      PieceIter itr = it0;
+      Piece pcr;
       bool ok = true;
-      uint64_t idle_since = 0;
-      uint32_t idle = 0;
-      while (ok && npv < ntotal) {
-        bool progressed = false;
-        if (ns < ntotal && (ts != pcs.tb || mbar_test_wait(q_full, ks & 1)) &&
-            mbar_test_wait(&kv_full[ns % kStages], (ns / kStages) & 1) &&
-            (ns < 2 || mbar_test_wait(&s_empty[ns & 1], ((ns - 2) >> 1) & 1))) {
-          tc_fence_after();
-          issue_s(ns);
-          ++ns;
-          if (++ts == pcs.te) {
-            ++ks;
-            if (its.next(p, pcs)) ts = pcs.tb;
+      int t = 0;    // this cluster's tile counter
+      int kp = 0;   // piece ordinal
+      while (ok && itr.next(p, pcr)) {
+        for (int tl = pcr.tb; tl < pcr.te && ok; ++tl, ++t) {
+          if (is_s) {
+            // partial S(t) = Q_v . K_v(t)^T over this CTA's 288 elements:
+            // 16 latent k-steps with A = q_lat latent part in TMEM and B =
+            // chunk slots 0..3, then 2 rope k-steps with A = the rope part in
+            // shared memory (64-byte swizzle) and B = slot 4 at elements
+            // 32v..32v+31.  B is K-major 128-byte swizzled (a k-step advances
+            // the start by 32 bytes inside a 64-element chunk).  A piece's
+            // first tile waits for that piece's q_lat.
+            ok = (tl != pcr.tb || mbar_wait_bounded_long(q_full, kp & 1, abort_flag)) &&
+                 mbar_wait_bounded_long(&kv_full[t % kStages], (t / kStages) & 1, abort_flag) &&
+                 (t < 2 || mbar_wait_bounded_long(&s_empty[t & 1], ((t - 2) >> 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t kb = st_base + (t % kStages) * kStageBytes;
+            const uint32_t d = tmem + kSCol + kTile * (t & 1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              tc_mma_ts(d, tmem + kQCol + 8 * i,
+                        smem_desc(kb + (i >> 2) * kChunkBytes + 32 * (i & 3), 16, 1024), kIdescS,
+                        i > 0 ? 1u : 0u);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              tc_mma_ss(d, smem_desc(qr_base + 32 * i, 16, 512, kSwizzle64),
+                        smem_desc(kb + 4 * kChunkBytes + 64 * v + 32 * i, 16, 1024), kIdescS, 1u);
+            tc_commit(&s_full[t & 1]);
+          } else {
+            // O[:, this half] += P(t) . V(t): P = the bf16 weights in shared
+            // memory (K-major, 128-byte swizzle), V = slots 0..3 of tile t,
+            // MN-major (leading offset: next 64 elements = next slot; stride
+            // offset: next 8 tokens = 1 KB); 16 tokens per product.  The first
+            // tile of a piece starts the output afresh; after a piece's last
+            // tile, o_done tells the softmax its output is complete.
+            ok = mbar_wait_bounded_long(&p_full[t & 1], (t >> 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vb = st_base + (t % kStages) * kStageBytes;
+            const uint32_t pb = p_base + (t & 1) * kPBytes;
+            const bool fresh = tl == pcr.tb;
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              tc_mma_ss(tmem + kOCol, smem_desc(pb + 32 * kk, 16, 1024),
+                        smem_desc(vb + kk * 2048, kChunkBytes, 1024), kIdescPV,
+                        (!fresh || kk > 0) ? 1u : 0u);
+            tc_commit(&pv_done[t & 1]);
+            tc_commit(&kv_empty[t % kStages]);
+            if (tl + 1 == pcr.te) tc_commit(o_done);
           }
-          progressed = true;
         }
-        if (npv < ns && mbar_test_wait(&p_full[npv & 1], (npv >> 1) & 1)) {
-          tc_fence_after();
-          issue_pv(npv, tp == pcp.tb);
-          ++npv;
-          if (++tp == pcp.te) {
-            tc_commit(o_done);
-            if (itp.next(p, pcp)) tp = pcp.tb;
-          }
-          progressed = true;
-        }
-        if (progressed) {
-          idle = 0;
-        } else if ((++idle & 4095u) == 0u) {  // bounded: 2 s without progress
-          const uint64_t now = globaltimer_ns();
-          if (idle == 4096u) idle_since = now;
-          else if (*abort_flag || now - idle_since > kWaitTimeoutNs) ok = false;
-        }
+        ++kp;
       }
       if (!ok) {
         *abort_flag = 1;
         atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
       }
       // every product issued completes before tensor memory is freed
-      tc_commit(drain);
-      mbar_wait_bounded(drain, 0, nullptr);
+      uint64_t* dr = is_s ? &drain[0] : &drain[1];
+      tc_commit(dr);
+      mbar_wait_bounded(dr, 0, nullptr);
     }
     __syncwarp();
   } else {

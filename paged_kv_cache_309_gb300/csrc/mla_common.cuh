@@ -200,10 +200,12 @@ __device__ __forceinline__ void mla_issue_tile_at(const MlaParams& p, const CUte
 
 }  // namespace mla
 
-// The tcgen05 kernel (mla_decode_tc.cu): 128-head tiles, each (sequence,
-// split) served by a pair of CTAs that own one half of the 512 output
-// elements each.  grid = (2 * H / 128, splits, B).
-pa_status launch_mla_tc(const CUtensorMap& mq, const CUtensorMap& mkv, const mla::MlaParams& p,
+// The tcgen05 kernel (mla_decode_tc.cu): 128-head tiles, each served by a
+// cluster of two CTAs that own one half of the 512 output elements each,
+// clusters spread over a token-balanced list of the sequences' tiles.
+// grid = (2 * clusters, H / 128).  mrope maps the 32 rope elements of a row
+// one CTA uses (64-byte boxes), mkv the latent chunks (128-byte boxes).
+pa_status launch_mla_tc(const CUtensorMap& mrope, const CUtensorMap& mkv, const mla::MlaParams& p,
                         dim3 grid, cudaStream_t stream);
 int mla_tc_tile();  // tokens per tile of the tcgen05 kernel
 

@@ -444,6 +444,20 @@ bool make_row576_map(CUtensorMap* map, const void* base, int64_t rows, int32_t b
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The rope half of one CTA of the tcgen05 kernel: 32 elements (64 bytes) of
+// each row, 64-byte swizzled.
+bool make_rope32_map(CUtensorMap* map, const void* base, int64_t rows, int32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
+  const cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t es[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
@@ -539,9 +553,12 @@ pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
   p.kv_evict_first = (a.num_heads == ht && ht != 128) ? 1 : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;  // log2(e)
   if (ht == 128) {
+    CUtensorMap mrope;
+    if (!make_rope32_map(&mrope, a.latent_cache, a.num_blocks * a.block_size, box_rows))
+      return PA_ERR_CUDA;
     const dim3 grid(static_cast<unsigned>(2 * a.plan.num_splits),
                     static_cast<unsigned>(a.num_heads / ht), 1u);
-    return launch_mla_tc(mq, mkv, p, grid, stream);
+    return launch_mla_tc(mrope, mkv, p, grid, stream);
   }
   const dim3 grid(static_cast<unsigned>(a.num_heads / ht), static_cast<unsigned>(a.plan.num_splits),
                   static_cast<unsigned>(a.num_seqs));

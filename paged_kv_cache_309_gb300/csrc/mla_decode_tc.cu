@@ -12,34 +12,38 @@
 // Layout of the work (sm_103a):
 //  * 128 heads are the M dimension of every product (one TMEM lane per
 //    head).  The fp32 output of 128 heads x 512 elements would fill all 512
-//    TMEM columns, so a CLUSTER of two CTAs serves each (head tile, split,
-//    sequence), and CTA v (its rank in the cluster) owns one half of the
-//    row: latent elements 256v .. 256v + 255 (its half of the output) and
-//    rope elements 32v .. 32v + 31.  grid = (2 * H / 128, splits, B).
-//  * CTA v loads only its slice of every latent row (4 latent chunks and
-//    the rope chunk: 640 of the row's 1152 bytes) through an 8-stage TMA
-//    ring of 32-token tiles, 128-byte swizzled; its slice of q_lat (144
-//    TMEM columns of bf16 pairs) sits in tensor memory, so shared memory
-//    holds only the ring and two exchange buffers.
-//  * partial S[128 x 32] over the CTA's 288 elements: 18 tcgen05.mma
-//    (M=128, N=32, K=16) with A = q_lat from TMEM and B = the K-major tile
-//    in shared memory.  The softmax threads (thread = head row) read their
-//    32 partial scores (tcgen05.ld), send them to the other CTA's exchange
-//    buffer through distributed shared memory (st.async, counted in bytes
-//    on the other CTA's mbarrier), and add the other CTA's partials: both
-//    CTAs add the same two numbers, so both run the identical softmax.
-//  * O[128 x 256] += P . V: 2 tcgen05.mma (N=256) with P (bf16) from TMEM
+//    TMEM columns, so a CLUSTER of two CTAs serves each 128-head tile, and
+//    CTA v (its rank in the cluster) owns one half of the row: latent
+//    elements 256v .. 256v + 255 (its half of the output) and rope elements
+//    32v .. 32v + 31.
+//  * schedule: the sequences' 64-token tiles, laid end to end, are cut into
+//    one contiguous chunk per cluster (one wave of clusters); a chunk that
+//    crosses sequence boundaries is worked piece by piece, a piece that is
+//    not a whole sequence writes an fp32 partial, and the CTA completing a
+//    sequence's pieces merges them after its own work.
+//  * CTA v loads only its slice of every latent row (4 latent chunks of 128
+//    bytes, 128-byte swizzled, and its 64 rope bytes, 64-byte swizzled: 576
+//    of the row's 1152 bytes) through a 4-stage TMA ring of 36 KB.  Its
+//    slice of q_lat sits in TMEM (latent part, bf16 pairs) and in shared
+//    memory (rope part).
+//  * partial S[128 x 64] over the CTA's 288 elements: 18 tcgen05.mma
+//    (M=128, N=64, K=16).  The softmax threads (thread = head row) read
+//    their 64 partial scores (tcgen05.ld), send them to the other CTA's
+//    exchange buffer through distributed shared memory (st.async, counted
+//    in bytes on the other CTA's mbarrier), and add the other CTA's
+//    partials: both CTAs add the same two numbers, so both run the
+//    identical softmax.  The weights (bf16) are written over the score
+//    buffer in TMEM.
+//  * O[128 x 256] += P . V: 4 tcgen05.mma (N=256, K=16) with P from TMEM
 //    and V = the CTA's latent chunks read in place as an MN-major operand.
-//  * warp roles: warp 0 issues the TMA loads, warp 1 owns TMEM and issues
-//    the MMAs from one thread (whichever of S(next) and P.V(next) is ready),
-//    warps 2-5 load q_lat into TMEM and then run the softmax: fp32, base 2,
-//    lazy rescale (the running max moves only when a score beats it by more
-//    than 2^8; the rescale reads, scales and writes back the TMEM output
-//    row), weights rounded to bf16 and written to TMEM with tcgen05.st.
-//  * epilogue: the softmax threads read their output row from TMEM; one
-//    split writes bf16, several write fp32 partials + log2-sum-exp, and the
-//    CTA that completes the per-(sequence, head tile) count (2 * splits
-//    arrivals) merges them.
+//  * warp roles: warp 0 issues the TMA loads; one thread of warp 1 (the TMEM
+//    owner) issues the score products and one thread of warp 6 the output
+//    products, each blocking in bounded waits; warps 2-5 load q_lat and run
+//    the softmax: fp32, base 2, lazy rescale (the running max moves only
+//    when a score beats it by more than 2^8; the rescale reads, scales and
+//    writes back the TMEM output row).
+//  * epilogue of a piece: the softmax threads read their output row from
+//    TMEM and write bf16 (whole sequence) or an fp32 partial + log2-sum-exp.
 //
 // Every wait is bounded (2 s); a timeout sets an error bit, the roles leave
 // their loops, the MMAs and copies already issued are drained, TMEM is
@@ -64,21 +68,20 @@ constexpr int kRopeHalf = kRope / 2;   // rope elements per CTA
 constexpr int kThreads = 7 * 32;
 constexpr int kPVWarp = 6;  // P.V products (warp 1: score products, TMEM owner)
 constexpr int kChunkBytes = kTile * 128;             // one 64-element chunk of a tile: 8 KB
-constexpr int kLoadChunks = kHalf / 64 + 1;          // 4 latent chunks + the rope chunk
-constexpr int kStageBytes = kLoadChunks * kChunkBytes;  // 40 KB
-constexpr int kStages = 3;
+constexpr int kLatChunks = kHalf / 64;               // 4 latent chunks per CTA
+constexpr int kRopeTileBytes = kTile * kRopeHalf * 2;  // this CTA's 32 rope elements: 4 KB
+constexpr int kStageBytes = kLatChunks * kChunkBytes + kRopeTileBytes;  // 36 KB
+constexpr int kStages = 4;
 constexpr int kRecvBytes = kTile * kHT * 4;          // one tile of the peer's partial scores
-constexpr int kPBytes = kHT * kTile * 2;             // one tile of bf16 weights (128-byte rows)
 constexpr int kQRopeBytes = kHT * kRopeHalf * 2;     // this CTA's rope part of q_lat (64-byte rows)
 constexpr int kStageOff = 0;
 constexpr int kRecvOff = kStageOff + kStages * kStageBytes;
-constexpr int kPOff = kRecvOff + 2 * kRecvBytes;
-constexpr int kQRopeOff = kPOff + 2 * kPBytes;
+constexpr int kQRopeOff = kRecvOff + 2 * kRecvBytes;
 constexpr int kBarOff = kQRopeOff + kQRopeBytes;
 // barriers: q_full, kv_full[kStages], kv_empty[kStages], s_full[2],
-// s_empty[2], p_full[2], pv_done[2], recv_full[2], sent_free[2], o_done,
-// drain, part_done; then tile masks, the TMEM slot and flags, the schedule
-constexpr int kNumBars = 18 + 2 * kStages;
+// p_full[2], pv_done[2], recv_full[2], sent_free[2], o_done, drain[2],
+// part_done, mrg_full; then tile masks, the TMEM slot and flags, the schedule
+constexpr int kNumBars = 16 + 2 * kStages;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
 constexpr int kMiscOff = kMaskOff + kStages * 8;
 constexpr int kSchedOff = kMiscOff + 32;             // schedule words and the merge list
@@ -153,9 +156,11 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 
 // Loads of one tile (one warp, all lanes): like mla_issue_tile_at, but only
-// this CTA's chunks: latent chunks 4v .. 4v + 3 and the rope chunk, into
-// slots 0..4 of the stage.
+// this CTA's slice: latent chunks 4v .. 4v + 3 into slots 0..3 of the stage
+// (128-byte rows) and rope elements 32v .. 32v + 31 behind them (64-byte
+// rows, 64-byte swizzle).
 __device__ __forceinline__ void issue_half_tile(const MlaParams& p, const CUtensorMap* tm_kv,
+                                                const CUtensorMap* tm_rope,
                                                 uint8_t* stage, uint64_t* full,
                                                 uint64_t* mask_slot, const int32_t* bt, int tok0,
                                                 int tok_end, int v, uint64_t pol, int lane) {
@@ -181,17 +186,18 @@ __device__ __forceinline__ void issue_half_tile(const MlaParams& p, const CUtens
   const uint32_t vb = __ballot_sync(0xffffffffu, valid);
   if (lane == 0) {
     *mask_slot = (static_cast<uint64_t>(hi) << 32) | lo;
-    mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vb) * rpb * kLoadChunks * 128));
+    mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vb) * rpb *
+                                                      (kLatChunks * 128 + kRopeHalf * 2)));
   }
   __syncwarp();
   if (valid) {
     const int32_t row = bid * bs + row0;
     uint8_t* st = stage + lane * rpb * 128;
 #pragma unroll 1
-    for (int c = 0; c < kLoadChunks; ++c) {
-      const int chunk = c < 4 ? 4 * v + c : kChunks - 1;
-      tma_load_2d(st + c * kChunkBytes, tm_kv, 64 * chunk, row, full, pol);
-    }
+    for (int c = 0; c < kLatChunks; ++c)
+      tma_load_2d(st + c * kChunkBytes, tm_kv, 64 * (kLatChunks * v + c), row, full, pol);
+    tma_load_2d(stage + kLatChunks * kChunkBytes + lane * rpb * (kRopeHalf * 2), tm_rope,
+                kLat + kRopeHalf * v, row, full, pol);
   }
 }
 
@@ -383,7 +389,8 @@ __device__ __forceinline__ void merge_pieces(const MlaParams& p, int b, int ht, 
 
 // ------------------------------------------------------------------ kernel --
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
+    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv,
+                         const __grid_constant__ CUtensorMap tm_rope, const MlaParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
@@ -391,9 +398,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars + 1;                  // [kStages] tile landed
   uint64_t* kv_empty = kv_full + kStages;        // [kStages] P.V of the stage's tile done
   uint64_t* s_full = kv_empty + kStages;         // [2] partial scores in TMEM (commit)
-  uint64_t* s_empty = s_full + 2;                // [2] partial scores read (128 threads)
-  uint64_t* p_full = s_empty + 2;                // [2] weights in shared memory (128 threads)
-  uint64_t* pv_done = p_full + 2;                // [2] P.V done (commit)
+  uint64_t* p_full = s_full + 2;                 // [2] weights written over them (128 threads)
+  uint64_t* pv_done = p_full + 2;                // [2] P.V done, score buffer free (commit)
   uint64_t* recv_full = pv_done + 2;             // [2] the other CTA's partials landed here
   uint64_t* sent_free = recv_full + 2;           // [2] the other CTA consumed what we sent
   uint64_t* o_done = sent_free + 2;              // every product of the current piece done
@@ -473,7 +479,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], kHT);
       mbar_init(&p_full[s], kHT);
       mbar_init(&pv_done[s], 1);
       mbar_init(&recv_full[s], 1);   // armed with the byte count by this CTA
@@ -522,7 +527,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // -------------------------------------------------------- TMA producer
     const uint64_t pol = l2_policy_evict_first();  // each row is read once (the rope chunk twice)
-    if (lane == 0) prefetch_tensormap(&tm_kv);
+    if (lane == 0) {
+      prefetch_tensormap(&tm_kv);
+      prefetch_tensormap(&tm_rope);
+    }
     bool ok = true;
     PieceIter it = it0;
     Piece pc;
@@ -538,7 +546,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                          ((gt / kStages) - 1) & 1, abort_flag));
           if (!ok) break;
         }
-        issue_half_tile(p, &tm_kv, smem + kStageOff + stage * kStageBytes, &kv_full[stage],
+        issue_half_tile(p, &tm_kv, &tm_rope, smem + kStageOff + stage * kStageBytes, &kv_full[stage],
                         &tile_mask[stage], bt, tl * kTile, L, v, pol, lane);
         issued = gt + 1;
       }
@@ -555,7 +563,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const bool is_s = warp == 1;
       const uint32_t st_base = smem_u32(smem + kStageOff);
-      const uint32_t p_base = smem_u32(smem + kPOff);
       const uint32_t qr_base = smem_u32(smem + kQRopeOff);
       PieceIter itr = it0;
       Piece pcr;
@@ -567,14 +574,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (is_s) {
             // partial S(t) = Q_v . K_v(t)^T over this CTA's 288 elements:
             // 16 latent k-steps with A = q_lat latent part in TMEM and B =
-            // chunk slots 0..3, then 2 rope k-steps with A = the rope part in
-            // shared memory (64-byte swizzle) and B = slot 4 at elements
-            // 32v..32v+31.  B is K-major 128-byte swizzled (a k-step advances
-            // the start by 32 bytes inside a 64-element chunk).  A piece's
-            // first tile waits for that piece's q_lat.
+            // chunk slots 0..3 (K-major, 128-byte swizzle: a k-step advances
+            // the start by 32 bytes inside a 64-element chunk), then 2 rope
+            // k-steps with A = the rope part of q_lat and B = the stage's
+            // rope rows (both K-major 64-byte rows, 64-byte swizzle).  Score
+            // buffer t & 1 is free once P.V(t - 2), which read the weights
+            // written over it, is done.  A piece's first tile waits for that
+            // piece's q_lat.
             ok = (tl != pcr.tb || mbar_wait_bounded_long(q_full, kp & 1, abort_flag)) &&
                  mbar_wait_bounded_long(&kv_full[t % kStages], (t / kStages) & 1, abort_flag) &&
-                 (t < 2 || mbar_wait_bounded_long(&s_empty[t & 1], ((t - 2) >> 1) & 1, abort_flag));
+                 (t < 2 || mbar_wait_bounded_long(&pv_done[t & 1], ((t - 2) >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const uint32_t kb = st_base + (t % kStages) * kStageBytes;
@@ -587,24 +596,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 2; ++i)
               tc_mma_ss(d, smem_desc(qr_base + 32 * i, 16, 512, kSwizzle64),
-                        smem_desc(kb + 4 * kChunkBytes + 64 * v + 32 * i, 16, 1024), kIdescS, 1u);
+                        smem_desc(kb + kLatChunks * kChunkBytes + 32 * i, 16, 512, kSwizzle64),
+                        kIdescS, 1u);
             tc_commit(&s_full[t & 1]);
           } else {
-            // O[:, this half] += P(t) . V(t): P = the bf16 weights in shared
-            // memory (K-major, 128-byte swizzle), V = slots 0..3 of tile t,
-            // MN-major (leading offset: next 64 elements = next slot; stride
-            // offset: next 8 tokens = 1 KB); 16 tokens per product.  The first
-            // tile of a piece starts the output afresh; after a piece's last
-            // tile, o_done tells the softmax its output is complete.
+            // O[:, this half] += P(t) . V(t): P = the bf16 weights in TMEM
+            // (pairs, written over the score buffer; 8 columns per 16
+            // tokens), V = slots 0..3 of tile t, MN-major (leading offset:
+            // next 64 elements = next slot; stride offset: next 8 tokens =
+            // 1 KB).  The first tile of a piece starts the output afresh;
+            // after a piece's last tile, o_done tells the softmax its output
+            // is complete.
             ok = mbar_wait_bounded_long(&p_full[t & 1], (t >> 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             const uint32_t vb = st_base + (t % kStages) * kStageBytes;
-            const uint32_t pb = p_base + (t & 1) * kPBytes;
+            const uint32_t pcol = tmem + kSCol + kTile * (t & 1);
             const bool fresh = tl == pcr.tb;
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              tc_mma_ss(tmem + kOCol, smem_desc(pb + 32 * kk, 16, 1024),
+              tc_mma_ts(tmem + kOCol, pcol + 8 * kk,
                         smem_desc(vb + kk * 2048, kChunkBytes, 1024), kIdescPV,
                         (!fresh || kk > 0) ? 1u : 0u);
             tc_commit(&pv_done[t & 1]);
@@ -633,8 +644,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t recv_full_peer = peer_addr(smem_u32(recv_full), peer);
     const uint32_t sent_free_peer = peer_addr(smem_u32(sent_free), peer);
     // Tile u's partial scores (u counts this cluster's tiles): wait for them
-    // (and for the tile, whose row mask is read later), read them, free the
-    // score buffer, and send them into the other CTA's exchange buffer
+    // (and for the tile, whose row mask is read later), read them, and send
+    // them into the other CTA's exchange buffer
     // u & 1 once it has consumed what we sent two tiles ago (asynchronous
     // stores counted on its recv_full[u & 1]).  Layout [4-column group][row]
     // of float4, so a warp's 16-byte stores are contiguous.
@@ -647,8 +658,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * ku, &sp[0]);
       tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * ku + 32, &sp[32]);
       tc_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_empty[ku]);
       if (u >= 2 && !__all_sync(0xffffffffu, wait_cluster_bounded(&sent_free[ku],
                                                                   ((u - 2) >> 1) & 1, abort_flag)))
         return false;
@@ -705,17 +714,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int n = pc.te - pc.tb;
       float m_run = -INFINITY, l_run = 0.f;
       float s[kTile], s_next[kTile];
-      // software pipeline: tile t + 1's partials travel to the other CTA
-      // while this thread finishes tile t
+      // software pipeline: tile t + 1's partials are read and sent once tile
+      // t's exponentials are done (S(t + 1) needed P.V(t - 1) to finish,
+      // since the weights of tile t - 1 sat in its score buffer), and travel
+      // to the other CTA while this thread writes tile t's weights
       ok = fetch_and_send(gbase, s);
       for (int t = 0; t < n && ok; ++t) {
         const int gt = gbase + t;
         const int stage = gt % kStages;
         const int k = gt & 1;
-        if (t + 1 < n && !fetch_and_send(gt + 1, s_next)) {
-          ok = false;
-          break;
-        }
         // ---- the other CTA's partials of tile gt, in our buffer k
         if (!__all_sync(0xffffffffu, wait_cluster_bounded(&recv_full[k], (gt >> 1) & 1,
                                                           abort_flag))) {
@@ -784,6 +791,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pr[i] = pack_bf16x2(p0, p1);
         }
         l_run += (lq[0] + lq[1]) + (lq[2] + lq[3]);
+        if (t + 1 < n && !fetch_and_send(gt + 1, s_next)) {
+          ok = false;
+          break;
+        }
         // tokens that do not exist: zero their value rows (slots 0..3; 0 x NaN
         // would poison P.V); piece j = (token j / 4, slot j % 4), two per thread
         if (mask != ~0ull) {
@@ -798,23 +809,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
             }
           }
+          fence_proxy_async_smem();  // generic writes before the tensor core reads them
         }
-        // the weight tile of tile gt - 2 must have been consumed
-        if (gt >= 2) {
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[k], ((gt - 2) >> 1) & 1,
-                                                         abort_flag))) {
-            ok = false;
-            break;
-          }
-        }
-        // weights -> shared memory buffer k, row `row` of 128 bytes, 128-byte
-        // swizzle (16-byte unit u at u ^ (row & 7)): the A operand of P.V
-        uint8_t* prow = smem + kPOff + k * kPBytes + row * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
-              make_uint4(pr[4 * u], pr[4 * u + 1], pr[4 * u + 2], pr[4 * u + 3]);
-        fence_proxy_async_smem();  // generic writes before the tensor core reads them
+        // weights, as bf16 pairs, over this tile's score buffer in TMEM (the
+        // scores are in registers): the A operand of P.V(gt)
+        tc_st32u_nowait(tmem + lane_addr + kSCol + kTile * k, pr);
+        tc_wait_st();
+        tc_fence_before();
         mbar_arrive(&p_full[k]);
 #pragma unroll
         for (int i = 0; i < kTile; ++i) s[i] = s_next[i];
@@ -922,7 +923,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 int mla_tc_tile() { return kTile; }
 
-pa_status launch_mla_tc(const CUtensorMap& mq, const CUtensorMap& mkv, const MlaParams& p,
+pa_status launch_mla_tc(const CUtensorMap& mrope, const CUtensorMap& mkv, const MlaParams& p,
                         dim3 grid, cudaStream_t stream) {
   static std::atomic<bool> attr_set{false};
   if (!attr_set.load()) {
@@ -931,8 +932,7 @@ pa_status launch_mla_tc(const CUtensorMap& mq, const CUtensorMap& mkv, const Mla
       return PA_ERR_CUDA;
     attr_set.store(true);
   }
-  (void)mq;  // the kernel loads q_lat into tensor memory itself
-  mla_decode_tc_kernel<<<grid, kThreads, kAlloc, stream>>>(mkv, p);
+  mla_decode_tc_kernel<<<grid, kThreads, kAlloc, stream>>>(mkv, mrope, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

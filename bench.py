@@ -160,8 +160,12 @@ def traffic_record(kernel_file, workload, step, kv_dtype):
         return None
     with open(rec) as f:
         d = json.load(f)
-    with open(kernel_file, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    # the kernel's source and the shared device header it includes
+    hs = hashlib.sha256()
+    for path in (kernel_file, os.path.join(os.path.dirname(kernel_file), "pa_internal.cuh")):
+        with open(path, "rb") as f:
+            hs.update(f.read())
+    h = hs.hexdigest()[:16]
     if (d.get("source_sha256_16") != h or d.get("workload") != workload or d.get("step") != step
             or d.get("kv_dtype") != kv_dtype):
         return None

@@ -495,9 +495,9 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const int kk = 2 * ks2 + half;
-              const uint32_t a[4] = {e4m3x2_to_f16x2(r[2 * half]), e4m3x2_to_f16x2(r[2 * half + 1]),
-                                     e4m3x2_to_f16x2(r[2 * half] >> 16),
-                                     e4m3x2_to_f16x2(r[2 * half + 1] >> 16)};
+              uint32_t a[4];
+              e4m3x4_to_f16x2x2(r[2 * half], a[0], a[2]);
+              e4m3x4_to_f16x2x2(r[2 * half + 1], a[1], a[3]);
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 if (half) mma_f16_16816(s1[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
@@ -600,10 +600,11 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
             const int u = 4 * hf + c;
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
             if (rv) x = *reinterpret_cast<const uint4*>(vsrc + ((u ^ (row & 7)) << 4));
-            const uint4 y0 = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16),
-                                        e4m3x2_to_f16x2(x.y), e4m3x2_to_f16x2(x.y >> 16));
-            const uint4 y1 = make_uint4(e4m3x2_to_f16x2(x.z), e4m3x2_to_f16x2(x.z >> 16),
-                                        e4m3x2_to_f16x2(x.w), e4m3x2_to_f16x2(x.w >> 16));
+            uint4 y0, y1;
+            e4m3x4_to_f16x2x2(x.x, y0.x, y0.y);
+            e4m3x4_to_f16x2x2(x.y, y0.z, y0.w);
+            e4m3x4_to_f16x2x2(x.z, y1.x, y1.y);
+            e4m3x4_to_f16x2x2(x.w, y1.z, y1.w);
             *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (rr & 7)) << 4)) = y0;
             *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (rr & 7)) << 4)) = y1;
           }

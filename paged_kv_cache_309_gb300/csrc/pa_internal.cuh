@@ -411,9 +411,21 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// Two floats rounded to nearest-even f16, lo in bits 0-15 (one instruction).
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
-         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// four e4m3 codes (low byte first) -> two f16x2 (codes 0,1 and 2,3), exact;
+// the register's 16-bit halves feed the conversions directly (no shifts or
+// masks)
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo,
+                                                  uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
 }
 // two e4m3 codes (low byte first) -> f16x2, exact
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {

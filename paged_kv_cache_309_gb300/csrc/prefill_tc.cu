@@ -9,29 +9,30 @@
 // cu_seqlens_q).  Query head h uses KV head h / G.
 //
 // How (sm_103a), FlashAttention style with the products on tcgen05:
-//  * grid = (query tile, kv head, sequence), heaviest tiles first; a CTA owns
-//    128 rows = 128/G new tokens x the G query heads of one kv head: the M
-//    dimension of both products, one TMEM lane per row.
-//  * warp 0 streams the key tiles (128 keys: K and V, each two 64-element
-//    chunks of [128 rows x 128 B], 128-byte swizzled) through a 3-stage TMA
-//    ring, one box per block piece, with a 128-bit row mask per tile.
-//  * warp 1 owns TMEM and issues the products from one thread, whichever is
-//    ready: S = Q.K^T (8 tcgen05.mma, M=128, N=128 keys, K=16; Q and K from
-//    shared memory, K-major) into one of two 128-column score tiles, and
-//    O += P.V (8 tcgen05.mma, N=128 head elements) with P (bf16) from TMEM
-//    and V read in place as an MN-major operand.
-//  * warps 2-9 load the CTA's Q rows into shared memory, then per tile read
-//    scores (tcgen05.ld), apply the causal and validity masks, run an fp32
-//    online softmax in base 2 with a lazy rescale (the running max moves
-//    only when a score beats it by more than 2^8; the rescale reads, scales
-//    and writes back the TMEM output row), and write the weights, rounded to
-//    bf16, to TMEM (tcgen05.st).  Two warps share each TMEM lane quadrant,
-//    one per half of the key columns (and of the output columns), and agree
-//    on the row maximum through shared memory: each thread does 64 of its
-//    row's 128 exponentials, and two warps per SM sub-partition hide each
-//    other's TMEM and exponential latencies.  S of the next tile runs on the
-//    tensor core while they work.
-//  * TMEM: output 128 columns, two score tiles of 128, two weight tiles of 64.
+//  * grid = (query tile pair, kv head, sequence), heaviest first; a CTA owns
+//    TWO query tiles of 128 rows (128/G consecutive new tokens x the G
+//    query heads of one kv head each), which share every key/value tile:
+//    half the L2 reads and TMA boxes per flop of one tile per CTA, and the
+//    two tiles' softmax and products interleave.
+//  * TMEM (512 columns): outputs O0, O1 (128 each) and score tiles S0, S1
+//    (128 each); tile i's weights (bf16 pairs) are written over the upper
+//    half of S_i, so S_i(t+1) waits for P.V_i(t).
+//  * warp 0 loads the keys of tile t (two 64-element chunks of [128 rows x
+//    128 B], 128-byte swizzled, one box per block piece) into a 3-slot ring
+//    and posts its 128-bit row mask in an 8-slot ring; warp 2 loads the
+//    values into a 2-slot ring; one thread of warp 1 (the TMEM owner)
+//    issues S_i(t) = Q_i . K(t)^T (8 tcgen05.mma, N = 128 keys, K-major Q and
+//    K), one thread of warp 3 issues O_i += P_i(t) . V(t) (8 tcgen05.mma,
+//    P from TMEM, V read in place as an MN-major operand); each role blocks
+//    in its own bounded waits.
+//  * warps 4-7 run the softmax of query tile 0, warps 8-11 that of tile 1:
+//    one thread per row (its TMEM lane), all 128 keys.  Pass 1 reads the
+//    row's scores in two 64-column halves for the maximum (the upper half
+//    stays in registers); pass 2 turns the upper half and then the re-read
+//    lower half into weights, 2^(s * scale - m) by one paired FMA per two
+//    keys and ex2.approx, written as bf16 pairs over score columns already
+//    read.  fp32 online softmax in base 2 with a lazy rescale (the running
+//    max moves only when a score beats it by more than 2^8).
 // Every wait is bounded (2 s); a timeout sets an error bit, drains what was
 // issued and frees TMEM before the CTA exits.
 #include <atomic>
@@ -46,38 +47,36 @@ using namespace pa;
 using namespace tc;
 
 constexpr int kD = 128;
-constexpr int kM = 128;                        // rows per CTA (tokens x heads)
+constexpr int kM = 128;                        // rows per query tile (tokens x heads)
+constexpr int kQTiles = 2;                     // query tiles per CTA
 constexpr int kTile = 128;                     // keys per tile
-constexpr int kStages = 3;
-constexpr int kSoftmaxThreads = 8 * 32;         // two warps per TMEM lane quadrant
-constexpr int kThreads = 4 * 32 + kSoftmaxThreads;
-constexpr int kVWarp = 10;   // value loads (warp 0: key loads)
-constexpr int kPVWarp = 11;  // P.V products (warp 1: score products, TMEM owner)
+constexpr int kKSlots = 3;                     // key ring
+constexpr int kVSlots = 2;                     // value ring
+constexpr int kThreads = 12 * 32;              // 4 role warps + 2 x 4 softmax warps
 constexpr int kChunk = 128 * 128;              // 64 elements of 128 rows: 16 KB
-constexpr int kQOff = 0;                       // Q: two chunks
-constexpr int kStageOff = 2 * kChunk;          // per stage: K lo, K hi, V lo, V hi
-constexpr int kStageBytes = 4 * kChunk;        // 64 KB
-constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-// Row masks live in their own ring with their own barriers: the K slot of
-// tile t is reloaded once S(t) is done, possibly before the softmax of tile
-// t has read the mask (and its k_full phase may then have moved on); mask
-// slot t % 8 is next written for tile t + 8, whose K load needs S(t + 5),
-// which needs the softmax of tile t + 3 to have read its scores.
+constexpr int kQOff = 0;                       // Q tile i: two chunks at 2i, 2i+1
+constexpr int kKOff = kQTiles * 2 * kChunk;    // key slots: lo, hi chunks
+constexpr int kVOff = kKOff + kKSlots * 2 * kChunk;  // value slots: lo, hi chunks
+constexpr int kBarOff = kVOff + kVSlots * 2 * kChunk;
+// Row masks live in their own ring with their own barriers: the key slot of
+// tile t is refilled once S_0(t) and S_1(t) are done, possibly before the
+// softmax of tile t has read the mask; mask slot t % 8 is next written for
+// tile t + 8, whose keys need S(t + 5), which needs P.V(t + 4), which needs
+// both softmax groups past tile t + 4.
 constexpr int kMaskSlots = 8;
-// q_full, k_full[3], k_empty[3], v_full[3], v_empty[3], mask_full[8],
-// s_full[2], s_empty[2], p_full[2], pv_done[2], o_final, drain[2]
-constexpr int kNumBars = 12 + 4 * kStages + kMaskSlots;
+// q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], mask_full[8],
+// s_full[2], p_full[2], pv_done[2], o_final[2], drain[2]
+constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + kMaskSlots + 5 * kQTiles;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;  // two 64-bit words per slot
 constexpr int kMiscOff = kMaskOff + kMaskSlots * 16;
-constexpr int kXchgOff = kMiscOff + 32;           // [2][kM] floats: pair exchange
-constexpr int kBytes = kXchgOff + 2 * kM * 4;
+constexpr int kBytes = kMiscOff + 32;
 constexpr int kAlloc = kBytes + 1024;
 static_assert(kAlloc <= 227 * 1024, "shared memory");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 0;      // [0, 128): output
-constexpr uint32_t kSCol = 128;    // [128, 384): two score tiles
-constexpr uint32_t kPCol = 384;    // [384, 512): two weight tiles (bf16 pairs)
+constexpr uint32_t kOCol = 0;      // [0, 256): outputs O0, O1
+constexpr uint32_t kSCol = 256;    // [256, 512): score tiles S0, S1 (weights over their upper halves)
+constexpr uint32_t kPHalf = 64;    // weights of tile i at kSCol + 128 i + 64
 constexpr uint32_t kIdescS = instr_desc(kM, kTile, false);
 constexpr uint32_t kIdescPV = instr_desc(kM, kD, true);
 constexpr float kRescaleLog2 = 8.0f;
@@ -92,7 +91,7 @@ struct PrefillTcParams {
   int64_t num_blocks;
   int32_t num_q_heads;
   int32_t group;
-  int32_t tokens_per_cta;  // kM / group
+  int32_t tokens_per_tile;  // kM / group
   int32_t block_size;
   int32_t log2_bs;
   int32_t max_blocks_per_seq;
@@ -167,62 +166,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-  uint64_t* q_full = bars + 0;                 // Q rows in shared memory (256 threads)
-  uint64_t* k_full = bars + 1;                 // [kStages] keys of the tile landed
-  uint64_t* k_empty = k_full + kStages;        // [kStages] S of the slot's tile done
-  uint64_t* v_full = k_empty + kStages;        // [kStages] values of the tile landed
-  uint64_t* v_empty = v_full + kStages;        // [kStages] P.V of the slot's tile done
-  uint64_t* mask_full = v_empty + kStages;     // [kMaskSlots] row mask posted (1 thread)
-  uint64_t* s_full = mask_full + kMaskSlots;   // [2] scores in TMEM (commit)
-  uint64_t* s_empty = s_full + 2;              // [2] scores read (256 threads)
-  uint64_t* p_full = s_empty + 2;              // [2] weights in TMEM (256 threads)
-  uint64_t* pv_done = p_full + 2;              // [2] P.V done (commit)
-  uint64_t* o_final = pv_done + 2;             // every product done (commit)
-  uint64_t* drain = o_final + 1;               // [2] each issuer's products done
+  uint64_t* q_full = bars + 0;                   // both Q tiles in shared memory (256 threads)
+  uint64_t* k_full = bars + 1;                   // [kKSlots] keys of the tile landed
+  uint64_t* k_empty = k_full + kKSlots;          // [kKSlots] S_0 and S_1 of the slot's tile done
+  uint64_t* v_full = k_empty + kKSlots;          // [kVSlots] values of the tile landed
+  uint64_t* v_empty = v_full + kVSlots;          // [kVSlots] P.V_0 and P.V_1 of the slot's tile done
+  uint64_t* mask_full = v_empty + kVSlots;       // [kMaskSlots] row mask posted (1 thread)
+  uint64_t* s_full = mask_full + kMaskSlots;     // [2] S_i in TMEM (commit)
+  uint64_t* p_full = s_full + kQTiles;           // [2] weights of tile i in TMEM (128 threads)
+  uint64_t* pv_done = p_full + kQTiles;          // [2] P.V_i done: S_i free (commit)
+  uint64_t* o_final = pv_done + kQTiles;         // [2] every product into O_i done (commit)
+  uint64_t* drain = o_final + kQTiles;           // [2] each issuer's products done
   uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);  // [kMaskSlots][2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);
 
-  const int qtile = gridDim.x - 1 - blockIdx.x;  // latest positions first
+  const int qpair = gridDim.x - 1 - blockIdx.x;  // latest positions first
   const int g = blockIdx.y;
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
+  const int tpt = p.tokens_per_tile;
 
   const int q0 = __ldg(p.cu_seqlens_q + b);
   const int n = __ldg(p.cu_seqlens_q + b + 1) - q0;
   int L = __ldg(p.context_lens + b);
   const int Lcap = p.max_blocks_per_seq * p.block_size;
   if (L > Lcap) {
-    if (qtile == 0 && g == 0 && threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
+    if (qpair == 0 && g == 0 && threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
     L = Lcap;
   }
-  const int qt0 = qtile * p.tokens_per_cta;
+  const int qt0 = qpair * kQTiles * tpt;  // the CTA's first new token
   if (qt0 >= n) return;
-  const int ntok = min(p.tokens_per_cta, n - qt0);
+  const int ntok = min(kQTiles * tpt, n - qt0);
   const int pos0 = L - n + qt0;           // position of the CTA's first token
   const int kend = min(L, pos0 + ntok);   // keys 0 .. kend-1 are needed
   const int ntiles = kend > 0 ? (kend + kTile - 1) / kTile : 0;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, kSoftmaxThreads);
-    for (int s = 0; s < kStages; ++s) {
+    mbar_init(q_full, kQTiles * kM);
+    for (int s = 0; s < kKSlots; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVSlots; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < kMaskSlots; ++s) mbar_init(&mask_full[s], 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], kSoftmaxThreads);
-      mbar_init(&p_full[s], kSoftmaxThreads);
-      mbar_init(&pv_done[s], 1);
+    for (int i = 0; i < kQTiles; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kM);
+      mbar_init(&pv_done[i], 1);
+      mbar_init(&o_final[i], 1);
+      mbar_init(&drain[i], 1);
     }
-    mbar_init(o_final, 1);
-    mbar_init(&drain[0], 1);
-    mbar_init(&drain[1], 1);
     flags[0] = 0;
     mbar_init_fence();
   }
@@ -240,30 +239,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = flags;
   int issued = 0;  // (load warps) tiles whose keys / values were requested
 
-  if (warp == 0 || warp == kVWarp) {
+  if (warp == 0 || warp == 2) {
     // -------------------------------------------------------- TMA producers
-    // Warp 0 loads the keys of tile t into K slot t % 3 once S of the slot's
-    // previous tile is done and posts the tile's row mask; the V warp loads
-    // the values into V slot t % 3 once P.V of the slot's previous tile is
-    // done.  Each blocks in its own bounded wait (a suspended warp takes no
-    // issue slots from the softmax warps).
+    // Warp 0 loads the keys of tile t into key slot t % 3 once S_0 and S_1
+    // of the slot's previous tile are done, and posts the tile's row mask;
+    // warp 2 loads the values into value slot t % 2 once P.V_0 and P.V_1 of
+    // the slot's previous tile are done.
     const bool is_k = warp == 0;
     const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
+    const int nslots = is_k ? kKSlots : kVSlots;
     uint64_t* empty = is_k ? k_empty : v_empty;
     uint64_t* full = is_k ? k_full : v_full;
+    uint8_t* ring = smem + (is_k ? kKOff : kVOff);
     const uint64_t pol = l2_policy_evict_first();
     if (lane == 0) prefetch_tensormap(tm);
     const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-      const int st = t % kStages;
-      if (t >= kStages) {
+      const int st = t % nslots;
+      if (t >= nslots) {
         ok = __all_sync(0xffffffffu,
-                        mbar_wait_bounded_long(&empty[st], ((t / kStages) - 1) & 1, abort_flag));
+                        mbar_wait_bounded_long(&empty[st], ((t / nslots) - 1) & 1, abort_flag));
         if (!ok) break;
       }
-      issue_tile_half(p, tm, smem + kStageOff + st * kStageBytes + (is_k ? 0 : 2 * kChunk),
-                      &full[st], is_k ? &tile_mask[2 * (t % kMaskSlots)] : nullptr,
+      issue_tile_half(p, tm, ring + st * 2 * kChunk, &full[st],
+                      is_k ? &tile_mask[2 * (t % kMaskSlots)] : nullptr,
                       is_k ? &mask_full[t % kMaskSlots] : nullptr, bt, g, t * kTile, kend, pol,
                       lane);
       issued = t + 1;
@@ -272,56 +272,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
       atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
     }
-  } else if (warp == 1 || warp == kPVWarp) {
+  } else if (warp == 1 || warp == 3) {
     // -------------------------------------------------------- MMA issuers
-    // One thread of warp 1 issues the score products, one thread of the P.V
-    // warp the output products; each commits its own products to their
-    // barriers (a commit tracks the issuing thread's products).
+    // One thread of warp 1 issues the score products, one thread of warp 3
+    // the output products, tile by tile and query tile 0 before 1; each
+    // blocks in its own bounded waits and commits its own products.
     if (lane == 0) {
       const bool is_s = warp == 1;
       const uint32_t q_base = smem_u32(smem + kQOff);
-      const uint32_t st_base = smem_u32(smem + kStageOff);
+      const uint32_t k_base = smem_u32(smem + kKOff);
+      const uint32_t v_base = smem_u32(smem + kVOff);
       bool ok = true;
       if (is_s) {
-        ok = ntiles == 0 || mbar_wait_bounded(q_full, 0, abort_flag);
+        ok = ntiles == 0 || mbar_wait_bounded_long(q_full, 0, abort_flag);
         tc_fence_after();
         for (int t = 0; ok && t < ntiles; ++t) {
-          ok = mbar_wait_bounded_long(&k_full[t % kStages], (t / kStages) & 1, abort_flag) &&
-               (t < 2 || mbar_wait_bounded_long(&s_empty[t & 1], ((t - 2) >> 1) & 1, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          // S(t) = Q . K(t)^T: 8 k-steps of 16 over the 128 head elements,
-          // both operands K-major 128-byte swizzled (a k-step inside a chunk
-          // advances the start by 32 bytes)
-          const uint32_t kb = st_base + (t % kStages) * kStageBytes;
-          const uint32_t d = tmem + kSCol + kTile * (t & 1);
+          ok = mbar_wait_bounded_long(&k_full[t % kKSlots], (t / kKSlots) & 1, abort_flag);
+          const uint32_t kb = k_base + (t % kKSlots) * 2 * kChunk;
+          for (int i = 0; ok && i < kQTiles; ++i) {
+            // S_i is free once P.V_i(t - 1), which read the weights over it, is done
+            ok = t == 0 || mbar_wait_bounded_long(&pv_done[i], (t - 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            // S_i(t) = Q_i . K(t)^T: 8 k-steps of 16 over the 128 head
+            // elements, both operands K-major 128-byte swizzled (a k-step
+            // inside a chunk advances the start by 32 bytes)
+            const uint32_t qb = q_base + i * 2 * kChunk;
+            const uint32_t d = tmem + kSCol + kTile * i;
 #pragma unroll
-          for (int j = 0; j < kD / 16; ++j)
-            tc_mma_ss(d, smem_desc(q_base + (j >> 2) * kChunk + 32 * (j & 3), 16, 1024),
-                      smem_desc(kb + (j >> 2) * kChunk + 32 * (j & 3), 16, 1024), kIdescS,
-                      j > 0 ? 1u : 0u);
-          tc_commit(&s_full[t & 1]);
-          tc_commit(&k_empty[t % kStages]);
+            for (int j = 0; j < kD / 16; ++j)
+              tc_mma_ss(d, smem_desc(qb + (j >> 2) * kChunk + 32 * (j & 3), 16, 1024),
+                        smem_desc(kb + (j >> 2) * kChunk + 32 * (j & 3), 16, 1024), kIdescS,
+                        j > 0 ? 1u : 0u);
+            tc_commit(&s_full[i]);
+          }
+          if (ok) tc_commit(&k_empty[t % kKSlots]);
         }
       } else {
-        for (int u = 0; ok && u < ntiles; ++u) {
-          ok = mbar_wait_bounded_long(&p_full[u & 1], (u >> 1) & 1, abort_flag) &&
-               mbar_wait_bounded_long(&v_full[u % kStages], (u / kStages) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          // O += P(u) . V(u): 8 k-steps of 16 keys; P from TMEM, V = chunks
-          // 2,3 of the slot, MN-major (leading offset: next 64 elements =
-          // next chunk; stride offset: next 8 keys = 1 KB)
-          const uint32_t vb = st_base + (u % kStages) * kStageBytes + 2 * kChunk;
+        for (int t = 0; ok && t < ntiles; ++t) {
+          ok = mbar_wait_bounded_long(&v_full[t % kVSlots], (t / kVSlots) & 1, abort_flag);
+          const uint32_t vb = v_base + (t % kVSlots) * 2 * kChunk;
+          for (int i = 0; ok && i < kQTiles; ++i) {
+            ok = mbar_wait_bounded_long(&p_full[i], t & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            // O_i += P_i(t) . V(t): 8 k-steps of 16 keys; P_i from TMEM (bf16
+            // pairs, 8 columns per k-step), V MN-major (leading offset: next
+            // 64 elements = next chunk; stride offset: next 8 keys = 1 KB)
+            const uint32_t pa = tmem + kSCol + kTile * i + kPHalf;
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            tc_mma_ts(tmem + kOCol, tmem + kPCol + (kTile / 2) * (u & 1) + 8 * kk,
-                      smem_desc(vb + kk * 2048, kChunk, 1024), kIdescPV,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&pv_done[u & 1]);
-          tc_commit(&v_empty[u % kStages]);
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              tc_mma_ts(tmem + kOCol + kD * i, pa + 8 * kk, smem_desc(vb + kk * 2048, kChunk, 1024),
+                        kIdescPV, (t > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&pv_done[i]);
+            if (t + 1 == ntiles) tc_commit(&o_final[i]);
+          }
+          if (ok) tc_commit(&v_empty[t % kVSlots]);
         }
-        if (ok) tc_commit(o_final);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -334,154 +341,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    // Two warps per TMEM lane quadrant: warp w reads lanes 32*(w & 3) ..
-    // +31 (one row each) and, by h = (w - 2) / 4, key columns 64h .. 64h+63
-    // of every score tile and output columns 64h .. 64h+63.  The pair agrees
-    // on each row's tile maximum through shared memory; every wait that can
-    // fail feeds the pair barrier's AND, so both warps leave together.
+    // warps 4-7: query tile 0, warps 8-11: query tile 1; one thread per row
+    // (its TMEM lane), all 128 keys of every tile.
+    const int qi = (warp - 4) >> 2;
     const int quad = warp & 3;
-    const int half = (warp - 2) >> 2;
     const int row = 32 * quad + lane;  // = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(32 * quad) << 16;
-    const int pair_bar = 1 + quad;
-    float* xchg = reinterpret_cast<float*>(smem + kXchgOff);  // [2 slots][kM rows]
-    const int tok = row / G;
+    const uint32_t s_addr = tmem + lane_addr + kSCol + kTile * qi;
+    const uint32_t o_addr = tmem + lane_addr + kOCol + kD * qi;
+    const int tok = qi * tpt + row / G;  // the row's token among the CTA's
     const bool rvalid = tok < ntok;
     const int pos = pos0 + tok;
     const int64_t qrow =
         (static_cast<int64_t>(q0 + qt0 + (rvalid ? tok : 0)) * p.num_q_heads + g * G + row % G) *
         kD;
-    // this half of the Q row -> shared memory chunk h (128-byte swizzle:
-    // 16-byte unit u of row r at u ^ (r & 7)); padding rows are zeros
+    // the Q row -> shared memory (two chunks of 64 elements, 128-byte
+    // swizzle: 16-byte unit u of row r at u ^ (r & 7)); padding rows are zeros
     {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow) + 8 * half;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow);
+      uint8_t* qdst = smem + kQOff + qi * 2 * kChunk + row * 128;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const uint4 x = rvalid ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(smem + kQOff + half * kChunk + row * 128 +
-                                  ((u ^ (row & 7)) << 4)) = x;
+        *reinterpret_cast<uint4*>(qdst + (u >> 3) * kChunk + (((u & 7) ^ (row & 7)) << 4)) = x;
       }
       fence_proxy_async_smem();
       mbar_arrive(q_full);
     }
-    // The pair's exchange slots: at step t half h writes slot (t + h) & 1 and
-    // reads the other one.  The next write to a slot comes either from the
-    // warp that read it or after the following pair barrier, so one barrier
-    // per step suffices.
-    float m_run = -INFINITY, l_part = 0.f;  // l_part: this half's columns only
     const bool pos_scale = p.scale_log2 > 0.f;
     const float sc = pos_scale ? p.scale_log2 : 1.f;
+    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      const int stage = t % kStages;
-      const int k = t & 1;
-      bool w = ok && mbar_wait_bounded(&s_full[k], (t >> 1) & 1, abort_flag) &&
-               mbar_wait_bounded(&mask_full[t % kMaskSlots], (t / kMaskSlots) & 1, abort_flag);
-      w = __all_sync(0xffffffffu, w);
-      float s[kTile / 2];
-      float mx_part = -INFINITY;
-      if (w) {
-        tc_fence_after();
-        tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * k + 64 * half, &s[0]);
-        tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * k + 64 * half + 32, &s[32]);
-        tc_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&s_empty[k]);
-        const uint64_t mw = tile_mask[2 * (t % kMaskSlots) + half];
-        const int kc0 = t * kTile + 64 * half;  // position of this half's first key
-        // with a positive scale the maximum is taken on the raw scores and
-        // the scale folds into the exponent's argument; otherwise the scores
-        // are scaled first
-        if (!pos_scale) {
+    // scores of keys 64h .. 64h + 63 of tile t (already in s): the scale
+    // when it is not folded into the exponent, then the causal and validity
+    // masks unless every key of the half exists and precedes the row
+    auto prep_half = [&](float (&s)[64], int t, int h, uint64_t mw) {
+      if (!pos_scale) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] *= p.scale_log2;
-        }
-        // no mask needed when every key of the half exists and precedes the row
-        if (!(rvalid && mw == ~0ull && kc0 + 63 <= pos)) {
+        for (int c = 0; c < 64; ++c) s[c] *= p.scale_log2;
+      }
+      const int kc0 = t * kTile + 64 * h;
+      if (!(rvalid && mw == ~0ull && kc0 + 63 <= pos)) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (!(rvalid && ((mw >> c) & 1ull) && kc0 + c <= pos)) s[c] = -INFINITY;
-        }
-        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        for (int c = 0; c < 64; ++c)
+          if (!(rvalid && ((mw >> c) & 1ull) && kc0 + c <= pos)) s[c] = -INFINITY;
+      }
+    };
+    auto max_half = [&](const float (&s)[64]) -> float {
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 64; c += 8) {
-          mq[0] = fmax3(mq[0], s[c], s[c + 1]);
-          mq[1] = fmax3(mq[1], s[c + 2], s[c + 3]);
-          mq[2] = fmax3(mq[2], s[c + 4], s[c + 5]);
-          mq[3] = fmax3(mq[3], s[c + 6], s[c + 7]);
-        }
-        mx_part = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      for (int c = 0; c < 64; c += 8) {
+        mq[0] = fmax3(mq[0], s[c], s[c + 1]);
+        mq[1] = fmax3(mq[1], s[c + 2], s[c + 3]);
+        mq[2] = fmax3(mq[2], s[c + 4], s[c + 5]);
+        mq[3] = fmax3(mq[3], s[c + 6], s[c + 7]);
       }
-      xchg[((t + half) & 1) * kM + row] = mx_part;
-      if (!named_barrier_and(pair_bar, 64, w)) {
-        ok = false;
-        break;
-      }
-      // both halves take the same maximum (fmax is exact and commutative);
-      // scaled to base-2 units (a scale of a masked -inf stays -inf)
-      const float mx_raw = fmaxf(mx_part, xchg[((t + half + 1) & 1) * kM + row]);
-      const float mx = pos_scale ? mx_raw * p.scale_log2 : mx_raw;
-      // lazy rescale; tcgen05.ld/st are warp-wide, so the warp rescales
-      // together when any of its rows needs it (the others scale by 1); the
-      // two warps of a pair hold the same rows and decide alike
-      const bool need = mx > m_run + kRescaleLog2;
-      if (__any_sync(0xffffffffu, need)) {
-        const float corr = need ? fast_exp2(m_run - mx) : 1.f;
-        if (t > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[(t - 1) & 1],
-                                                         ((t - 1) >> 1) & 1, abort_flag));
-          if (ok) {
-            tc_fence_after();
-            float o[64];
-            tc_ld32_nowait(tmem + lane_addr + kOCol + 64 * half, &o[0]);
-            tc_ld32_nowait(tmem + lane_addr + kOCol + 64 * half + 32, &o[32]);
-            tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 64; ++i) o[i] *= corr;
-            tc_st32u_nowait(tmem + lane_addr + kOCol + 64 * half,
-                            reinterpret_cast<const uint32_t*>(&o[0]));
-            tc_st32u_nowait(tmem + lane_addr + kOCol + 64 * half + 32,
-                            reinterpret_cast<const uint32_t*>(&o[32]));
-            tc_wait_st();
-          }
-        }
-        if (need) {
-          l_part *= corr;
-          m_run = mx;
-        }
-      }
-      if (!ok) continue;  // the next pair barrier ends the loop for both warps
-      // keys without a cache row: zero their V rows (0 x NaN would poison
-      // P.V); piece j = (key j / 2, V chunk j % 2), one per thread
-      const uint64_t mlo = tile_mask[2 * (t % kMaskSlots)];
-      const uint64_t mhi = tile_mask[2 * (t % kMaskSlots) + 1];
-      if (mlo != ~0ull || mhi != ~0ull) {
-        // the values of tile t must have landed before rows are zeroed
-        // (their slot's previous tile is then done with them as well)
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&v_full[stage], (t / kStages) & 1,
-                                                       abort_flag));
-        if (!ok) continue;
-        const int j = row + kM * half;
-        const int r = j >> 1;
-        if (!mask_bit(mlo, mhi, r)) {
-          uint4* dst = reinterpret_cast<uint4*>(smem + kStageOff + stage * kStageBytes +
-                                                (2 + (j & 1)) * kChunk + r * 128);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();  // generic writes before the tensor core reads them
-      }
-      // the weight tile of tile t - 2 must have been consumed
-      if (t >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pv_done[k], ((t - 2) >> 1) & 1,
-                                                       abort_flag));
-        if (!ok) continue;
-      }
-      // weights, rounded to bf16, as bf16 pairs in TMEM; the row sum of this
-      // half in four independent chains
-      // weight = 2^(s * scale - m): one paired multiply-add per two keys; a
-      // masked score is -inf and 2^-inf = +0 (m is taken as 0 while the row
-      // has seen no key, so the argument is never -inf + inf)
+      return fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+    };
+    // weights of 64 keys as bf16 pairs into 32 TMEM columns; returns their
+    // sum.  2^(s * scale - m): a masked score is -inf and 2^-inf = +0 (m is
+    // taken as 0 while the row has seen no key, so no -inf + inf)
+    auto weights_half = [&](const float (&s)[64], uint32_t dst) -> float {
       const float2 sc2 = make_float2(sc, sc);
       const float mneg = m_run == -INFINITY ? 0.f : -m_run;
       const float2 mn2 = make_float2(mneg, mneg);
@@ -494,37 +414,114 @@ __global__ void __launch_bounds__(kThreads, 1)
         lq[i & 1] = fadd2(lq[i & 1], e);
         pr[i] = pack_bf16x2(e.x, e.y);
       }
-      l_part += (lq[0].x + lq[0].y) + (lq[1].x + lq[1].y);
-      tc_st32u_nowait(tmem + lane_addr + kPCol + (kTile / 2) * k + 32 * half, &pr[0]);
+      tc_st32u_nowait(dst, pr);
+      return (lq[0].x + lq[0].y) + (lq[1].x + lq[1].y);
+    };
+    for (int t = 0; t < ntiles; ++t) {
+      ok = mbar_wait_bounded(&s_full[qi], t & 1, abort_flag) &&
+           mbar_wait_bounded(&mask_full[t % kMaskSlots], (t / kMaskSlots) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      const uint64_t mlo = tile_mask[2 * (t % kMaskSlots)];
+      const uint64_t mhi = tile_mask[2 * (t % kMaskSlots) + 1];
+      tc_fence_after();
+      // pass 1: the row maximum over both halves; the upper half stays in s
+      float s[64];
+      tc_ld32_nowait(s_addr, &s[0]);
+      tc_ld32_nowait(s_addr + 32, &s[32]);
+      tc_wait_ld();
+      prep_half(s, t, 0, mlo);
+      const float mx_lo = max_half(s);
+      tc_ld32_nowait(s_addr + 64, &s[0]);
+      tc_ld32_nowait(s_addr + 96, &s[32]);
+      tc_wait_ld();
+      prep_half(s, t, 1, mhi);
+      const float mx_raw = fmaxf(mx_lo, max_half(s));
+      const float mx = pos_scale ? mx_raw * p.scale_log2 : mx_raw;
+      // lazy rescale; tcgen05.ld/st are warp-wide, so the warp rescales
+      // together when any of its rows needs it (the others scale by 1).
+      // P.V_i(t - 1) is complete: S_i(t) waited for it.
+      const bool need = mx > m_run + kRescaleLog2;
+      if (__any_sync(0xffffffffu, need)) {
+        const float corr = need ? fast_exp2(m_run - mx) : 1.f;
+        if (t > 0) {
+#pragma unroll 1
+          for (int cq = 0; cq < kD / 64; ++cq) {
+            float o[64];
+            tc_ld32_nowait(o_addr + 64 * cq, &o[0]);
+            tc_ld32_nowait(o_addr + 64 * cq + 32, &o[32]);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 64; ++i) o[i] *= corr;
+            tc_st32u_nowait(o_addr + 64 * cq, reinterpret_cast<const uint32_t*>(&o[0]));
+            tc_st32u_nowait(o_addr + 64 * cq + 32, reinterpret_cast<const uint32_t*>(&o[32]));
+            tc_wait_st();
+          }
+        }
+        if (need) {
+          l_run *= corr;
+          m_run = mx;
+        }
+      }
+      // pass 2: weights of keys 64..127 (in registers) over score columns
+      // 96..127, then of the re-read keys 0..63 over columns 64..95 (both
+      // already read): the A operand of P.V_i, keys 2j, 2j+1 in column 64 + j
+      float lsum = weights_half(s, s_addr + kPHalf + 32);
+      tc_ld32_nowait(s_addr, &s[0]);
+      tc_ld32_nowait(s_addr + 32, &s[32]);
+      tc_wait_ld();
+      prep_half(s, t, 0, mlo);
+      lsum += weights_half(s, s_addr + kPHalf);
+      l_run += lsum;
       tc_wait_st();
+      // keys without a cache row: zero their value rows (0 x NaN would
+      // poison P.V), by query tile 0's threads (P.V_1(t) follows P.V_0(t));
+      // piece j = (key j / 2, value chunk j % 2), two per thread
+      if (qi == 0 && (mlo != ~0ull || mhi != ~0ull)) {
+        // the values of tile t must have landed (their slot's previous tile
+        // is then done with them as well)
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&v_full[t % kVSlots], (t / kVSlots) & 1,
+                                                       abort_flag));
+        if (!ok) break;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int j = row + kM * hh;
+          const int r = j >> 1;
+          if (!mask_bit(mlo, mhi, r)) {
+            uint4* dst = reinterpret_cast<uint4*>(smem + kVOff + (t % kVSlots) * 2 * kChunk +
+                                                  (j & 1) * kChunk + r * 128);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();  // generic writes before the tensor core reads them
+      }
       tc_fence_before();
-      mbar_arrive(&p_full[k]);
+      mbar_arrive(&p_full[qi]);
     }
-    // row sum: this half's part plus the partner's (one more exchange step)
-    if (ok && ntiles > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(o_final, 0, abort_flag));
-    xchg[((ntiles + half) & 1) * kM + row] = l_part;
-    ok = named_barrier_and(pair_bar, 64, ok);
-    const float l_run = l_part + xchg[((ntiles + half + 1) & 1) * kM + row];
+    if (ok && ntiles > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&o_final[qi], 0, abort_flag));
     if (!ok) {
       *abort_flag = 1;
       if (lane == 0) atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
     } else if (ntiles == 0) {
-      // no key at all: a zero row (this half's 64 columns)
-      if (rvalid) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + qrow + 64 * half);
+      if (rvalid) {  // no key at all: a zero row
+        uint4* dst = reinterpret_cast<uint4*>(p.out + qrow);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < kD / 8; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
       }
     } else {
-      // ---- epilogue: this half of the thread's output row
+      // ---- epilogue: this thread's output row
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
-      for (int cq = 0; cq < 2; ++cq) {
+      for (int cq = 0; cq < kD / 32; ++cq) {
         float o[32];
-        tc_ld32(tmem + lane_addr + kOCol + 64 * half + 32 * cq, o);  // warp-wide
+        tc_ld32(o_addr + 32 * cq, o);  // warp-wide: every lane loads
         if (rvalid) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + qrow + 64 * half + 32 * cq);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + qrow + 32 * cq);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             dst[u] = make_uint4(pack_bf16x2(o[8 * u] * inv, o[8 * u + 1] * inv),
@@ -540,10 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
-    if ((warp == 0 || warp == kVWarp) && lane == 0) {
+    if ((warp == 0 || warp == 2) && lane == 0) {
       uint64_t* full = warp == 0 ? k_full : v_full;
-      for (int t = max(0, issued - kStages); t < issued; ++t)
-        mbar_wait_bounded(&full[t % kStages], (t / kStages) & 1, nullptr);
+      const int nslots = warp == 0 ? kKSlots : kVSlots;
+      for (int t = max(0, issued - nslots); t < issued; ++t)
+        mbar_wait_bounded(&full[t % nslots], (t / nslots) & 1, nullptr);
     }
     __syncthreads();
   }
@@ -576,15 +574,16 @@ pa_status launch_paged_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
   p.num_blocks = a.num_blocks;
   p.num_q_heads = a.num_q_heads;
   p.group = G;
-  p.tokens_per_cta = kM / G;
+  p.tokens_per_tile = kM / G;
   p.block_size = a.block_size;
   int lg = 0;
   while ((1 << lg) < a.block_size) ++lg;
   p.log2_bs = lg;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  const int64_t qtiles = (static_cast<int64_t>(a.max_q_len) + p.tokens_per_cta - 1) / p.tokens_per_cta;
-  if (qtiles > 0x7FFFFFFF) return PA_ERR_UNSUPPORTED;
+  const int64_t per_cta = static_cast<int64_t>(kQTiles) * p.tokens_per_tile;
+  const int64_t qpairs = (static_cast<int64_t>(a.max_q_len) + per_cta - 1) / per_cta;
+  if (qpairs > 0x7FFFFFFF) return PA_ERR_UNSUPPORTED;
   static std::atomic<bool> attr_set{false};
   if (!attr_set.load()) {
     if (cudaFuncSetAttribute(paged_prefill_tcgen05_kernel,
@@ -592,7 +591,7 @@ pa_status launch_paged_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
       return PA_ERR_CUDA;
     attr_set.store(true);
   }
-  const dim3 grid(static_cast<unsigned>(qtiles), static_cast<unsigned>(a.num_kv_heads),
+  const dim3 grid(static_cast<unsigned>(qpairs), static_cast<unsigned>(a.num_kv_heads),
                   static_cast<unsigned>(a.num_seqs));
   paged_prefill_tcgen05_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;

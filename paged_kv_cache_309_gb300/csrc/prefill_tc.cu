@@ -65,8 +65,8 @@ constexpr int kBarOff = kVOff + kVSlots * 2 * kChunk;
 // both softmax groups past tile t + 4.
 constexpr int kMaskSlots = 8;
 // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], mask_full[8],
-// s_full[2], p_full[2], pv_done[2], o_final[2], drain[2]
-constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + kMaskSlots + 5 * kQTiles;
+// s_full[2], p_full[2], pv_done[2], o_final[2], drain[2], hand[2][4]
+constexpr int kNumBars = 1 + 2 * kKSlots + 2 * kVSlots + kMaskSlots + 5 * kQTiles + 2 * 4;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;  // two 64-bit words per slot
 constexpr int kMiscOff = kMaskOff + kMaskSlots * 16;
 constexpr int kBytes = kMiscOff + 32;
@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pv_done = p_full + kQTiles;          // [2] P.V_i done: S_i free (commit)
   uint64_t* o_final = pv_done + kQTiles;         // [2] every product into O_i done (commit)
   uint64_t* drain = o_final + kQTiles;           // [2] each issuer's products done
+  uint64_t* hand = drain + kQTiles;              // [2][4] weights pass of tile i done (per quadrant)
   uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);  // [kMaskSlots][2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&o_final[i], 1);
       mbar_init(&drain[i], 1);
     }
+    for (int i = 0; i < 2 * 4; ++i) mbar_init(&hand[i], 1);
     flags[0] = 0;
     mbar_init_fence();
   }
@@ -465,6 +467,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_run = mx;
         }
       }
+      // ping-pong: the two query tiles' weights passes alternate on each SM
+      // sub-partition (tile 1's pass of tile t follows tile 0's, tile 0's
+      // pass of tile t + 1 follows tile 1's of tile t), so each runs with the
+      // sub-partition mostly to itself while the tensor core works for the
+      // other query tile
+      if (qi == 1 || t > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&hand[(qi ^ 1) * 4 + quad],
+                                                       (qi == 1 ? t : t - 1) & 1, abort_flag));
+        if (!ok) break;
+      }
       // pass 2: weights of keys 64..127 (in registers) over score columns
       // 96..127, then of the re-read keys 0..63 over columns 64..95 (both
       // already read): the A operand of P.V_i, keys 2j, 2j+1 in column 64 + j
@@ -475,6 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prep_half(s, t, 0, mlo);
       lsum += weights_half(s, s_addr + kPHalf);
       l_run += lsum;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&hand[qi * 4 + quad]);
       tc_wait_st();
       // keys without a cache row: zero their value rows (0 x NaN would
       // poison P.V), by query tile 0's threads (P.V_1(t) follows P.V_0(t));

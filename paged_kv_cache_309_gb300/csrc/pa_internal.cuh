@@ -141,13 +141,17 @@ __device__ __forceinline__ Vec8<float> from_f32(const float f[8]) {
 }
 template <>
 __device__ __forceinline__ Vec8<e4m3> from_f32(const float f[8]) {
-  uint32_t w[2] = {0u, 0u};
+  // four codes per register: two paired conversions (the first value of a
+  // pair in the low byte) joined as the register's 16-bit halves
+  uint32_t w[2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // pairs: .x lands in the low byte
-    const uint32_t b2 = __nv_cvt_float2_to_fp8x2(make_float2(f[2 * i], f[2 * i + 1]),
-                                                 __NV_SATFINITE, __NV_E4M3);
-    w[i >> 1] |= (b2 & 0xFFFFu) << (16 * (i & 1));
-  }
+  for (int i = 0; i < 2; ++i)
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(w[i])
+        : "f"(f[4 * i]), "f"(f[4 * i + 1]), "f"(f[4 * i + 2]), "f"(f[4 * i + 3]));
   return {make_uint2(w[0], w[1])};
 }
 
@@ -192,18 +196,46 @@ static __device__ __noinline__ F8 div8_library(F8 x, float s) {
 // no per-value range test is needed -- only that x * r cannot overflow (the
 // chunk's largest |x| at most xmax; NaN passes through as NaN) -- and the
 // sign of a zero quotient is restored from x.  Other chunks use the library.
+// The same operations on pairs (one instruction for two lanes of work on
+// sm_100 and later; each lane rounds exactly as the scalar operation does).
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(fabsf(b)), "f"(fabsf(c)));
+  return d;
+}
+
 __device__ __forceinline__ void div8_for_e4m3(float (&f)[8], const Divisor& d, float xmax) {
   float amax = 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+  for (int e = 0; e < 8; e += 2) amax = max3_abs(amax, f[e], f[e + 1]);
   if (d.fast && amax <= xmax) {
+    const float2 r2 = make_float2(d.r, d.r), ns2 = make_float2(-d.s, -d.s);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float x = f[e];
-      float q = __fmul_rn(x, d.r);
-      q = __fmaf_rn(__fmaf_rn(-d.s, q, x), d.r, q);
-      q = __fmaf_rn(__fmaf_rn(-d.s, q, x), d.r, q);
-      f[e] = copysignf(q, x);
+    for (int e = 0; e < 8; e += 2) {
+      const float2 x = make_float2(f[e], f[e + 1]);
+      float2 q = mul2_rn(x, r2);
+      q = fma2_rn(fma2_rn(ns2, q, x), r2, q);
+      q = fma2_rn(fma2_rn(ns2, q, x), r2, q);
+      f[e] = copysignf(q.x, x.x);
+      f[e + 1] = copysignf(q.y, x.y);
     }
   } else {
     F8 t;

@@ -65,8 +65,9 @@ constexpr int kHT = 128;               // heads per CTA (M)
 constexpr int kTile = 64;              // tokens per tile (N of S, K of P.V)
 constexpr int kHalf = kLat / 2;        // output (and latent) elements per CTA
 constexpr int kRopeHalf = kRope / 2;   // rope elements per CTA
-constexpr int kThreads = 7 * 32;
-constexpr int kPVWarp = 6;  // P.V products (warp 1: score products, TMEM owner)
+constexpr int kThreads = 11 * 32;
+constexpr int kPVWarp = 6;   // P.V products (warp 1: score products, TMEM owner)
+constexpr int kXWarp0 = 7;   // warps 7-10: score exchange with the other CTA
 constexpr int kChunkBytes = kTile * 128;             // one 64-element chunk of a tile: 8 KB
 constexpr int kLatChunks = kHalf / 64;               // 4 latent chunks per CTA
 constexpr int kRopeTileBytes = kTile * kRopeHalf * 2;  // this CTA's 32 rope elements: 4 KB
@@ -81,7 +82,7 @@ constexpr int kBarOff = kQRopeOff + kQRopeBytes;
 // barriers: q_full, kv_full[kStages], kv_empty[kStages], s_full[2],
 // p_full[2], pv_done[2], recv_full[2], sent_free[2], o_done, drain[2],
 // part_done, mrg_full; then tile masks, the TMEM slot and flags, the schedule
-constexpr int kNumBars = 16 + 2 * kStages;
+constexpr int kNumBars = 18 + 2 * kStages;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
 constexpr int kMiscOff = kMaskOff + kStages * 8;
 constexpr int kSchedOff = kMiscOff + 32;             // schedule words and the merge list
@@ -406,6 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* drain = o_done + 1;                  // [2] each issuer's products done
   uint64_t* part_done = drain + 2;               // a partial's 128 rows are written
   uint64_t* mrg_full = part_done + 1;            // a merge batch's partial rows landed
+  uint64_t* sum_full = mrg_full + 1;             // [2] full scores back in TMEM (128 threads)
   uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);  // [0] abort
@@ -489,6 +491,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&drain[1], 1);
     mbar_init(part_done, kHT);
     mbar_init(mrg_full, 1);
+    mbar_init(&sum_full[0], kHT);
+    mbar_init(&sum_full[1], kHT);
     flags[0] = 0;
     mbar_init_fence();
     // the first two exchanges: expect one tile of partials in each buffer
@@ -635,40 +639,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(dr, 0, nullptr);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ softmax
+  } else if (warp >= kXWarp0) {
+    // -------------------------------------------------------- score exchange
+    // Warps 7-10 (one per TMEM lane quadrant) trade partial scores with the
+    // other CTA, tile by tile and ahead of the softmax: read this CTA's
+    // partial S(u) (u counts this cluster's tiles), send it into the other
+    // CTA's exchange buffer u & 1 once that CTA has consumed what we sent two
+    // tiles ago (asynchronous stores counted in bytes on its recv_full[u &
+    // 1]), add the other CTA's partial from our buffer u & 1 (own + other is
+    // the same sum on both CTAs: addition commutes, so both run an identical
+    // softmax), and write the full scores back over the partials.  Layout of
+    // an exchange buffer: [4-token group][row] of float4, so a warp's 16-byte
+    // stores are contiguous.
     const int row = 32 * (warp & 3) + lane;  // head within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t recv_local = smem_u32(smem + kRecvOff);
-    const uint32_t recv_peer = peer_addr(recv_local, peer);
+    const uint32_t recv_peer = peer_addr(smem_u32(smem + kRecvOff), peer);
     const uint32_t recv_full_peer = peer_addr(smem_u32(recv_full), peer);
     const uint32_t sent_free_peer = peer_addr(smem_u32(sent_free), peer);
-    // Tile u's partial scores (u counts this cluster's tiles): wait for them
-    // (and for the tile, whose row mask is read later), read them, and send
-    // them into the other CTA's exchange buffer
-    // u & 1 once it has consumed what we sent two tiles ago (asynchronous
-    // stores counted on its recv_full[u & 1]).  Layout [4-column group][row]
-    // of float4, so a warp's 16-byte stores are contiguous.
-    auto fetch_and_send = [&](int u, float (&sp)[kTile]) -> bool {
-      const int ku = u & 1;
-      bool w = mbar_wait_bounded(&s_full[ku], (u >> 1) & 1, abort_flag) &&
-               mbar_wait_bounded(&kv_full[u % kStages], (u / kStages) & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, w)) return false;
+    bool ok = true;
+    for (int u = 0; u < ntotal; ++u) {
+      const int k = u & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded_long(&s_full[k], (u >> 1) & 1, abort_flag));
+      if (!ok) break;
       tc_fence_after();
-      tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * ku, &sp[0]);
-      tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * ku + 32, &sp[32]);
+      float sp[kTile];
+      tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * k, &sp[0]);
+      tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * k + 32, &sp[32]);
       tc_wait_ld();
-      if (u >= 2 && !__all_sync(0xffffffffu, wait_cluster_bounded(&sent_free[ku],
-                                                                  ((u - 2) >> 1) & 1, abort_flag)))
-        return false;
-      const uint32_t slot = static_cast<uint32_t>((ku * (kTile / 4) * kHT + row) * 16);
+      if (u >= 2) {
+        ok = __all_sync(0xffffffffu, wait_cluster_bounded(&sent_free[k], ((u - 2) >> 1) & 1,
+                                                          abort_flag));
+        if (!ok) break;
+      }
+      const uint32_t slot = static_cast<uint32_t>((k * (kTile / 4) * kHT + row) * 16);
 #pragma unroll
       for (int g = 0; g < kTile / 4; ++g)
         st_async_peer(recv_peer + slot + g * kHT * 16,
                       make_float4(sp[4 * g], sp[4 * g + 1], sp[4 * g + 2], sp[4 * g + 3]),
-                      recv_full_peer + 8 * ku);
-      return true;
-    };
+                      recv_full_peer + 8 * k);
+      ok = __all_sync(0xffffffffu, wait_cluster_bounded(&recv_full[k], (u >> 1) & 1, abort_flag));
+      if (!ok) break;
+      const float4* other =
+          reinterpret_cast<const float4*>(smem + kRecvOff) + k * (kTile / 4) * kHT + row;
+#pragma unroll
+      for (int g = 0; g < kTile / 4; ++g) {
+        const float4 o = other[g * kHT];
+        sp[4 * g] += o.x;
+        sp[4 * g + 1] += o.y;
+        sp[4 * g + 2] += o.z;
+        sp[4 * g + 3] += o.w;
+      }
+      // buffer k is consumed (the values are in registers): re-arm it for
+      // tile u + 2 and tell the other CTA
+      __syncwarp();
+      if (row == 0 && u + 2 < ntotal) mbar_arrive_expect_tx(&recv_full[k], kRecvBytes);
+      if (lane == 0) arrive_peer_relaxed(sent_free_peer + 8 * k);
+      tc_st32u_nowait(tmem + lane_addr + kSCol + kTile * k, reinterpret_cast<const uint32_t*>(&sp[0]));
+      tc_st32u_nowait(tmem + lane_addr + kSCol + kTile * k + 32,
+                      reinterpret_cast<const uint32_t*>(&sp[32]));
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sum_full[k]);
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      if (lane == 0) atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int row = 32 * (warp & 3) + lane;  // head within the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     bool ok = true;
     PieceIter it = it0;
     Piece pc;
@@ -713,46 +753,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const int n = pc.te - pc.tb;
       float m_run = -INFINITY, l_run = 0.f;
-      float s[kTile], s_next[kTile];
-      // software pipeline: tile t + 1's partials are read and sent once tile
-      // t's exponentials are done (S(t + 1) needed P.V(t - 1) to finish,
-      // since the weights of tile t - 1 sat in its score buffer), and travel
-      // to the other CTA while this thread writes tile t's weights
-      ok = fetch_and_send(gbase, s);
       for (int t = 0; t < n && ok; ++t) {
         const int gt = gbase + t;
         const int stage = gt % kStages;
         const int k = gt & 1;
-        // ---- the other CTA's partials of tile gt, in our buffer k
-        if (!__all_sync(0xffffffffu, wait_cluster_bounded(&recv_full[k], (gt >> 1) & 1,
-                                                          abort_flag))) {
+        // ---- the full scores of tile gt (summed by the exchange warps), and
+        // the tile itself, whose row mask is read here
+        const bool w = mbar_wait_bounded(&sum_full[k], (gt >> 1) & 1, abort_flag) &&
+                       mbar_wait_bounded(&kv_full[stage], (gt / kStages) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
-        const float4* mine =
-            reinterpret_cast<const float4*>(smem + kRecvOff) + k * (kTile / 4) * kHT + row;
+        tc_fence_after();
+        float s[kTile];
+        tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * k, &s[0]);
+        tc_ld32_nowait(tmem + lane_addr + kSCol + kTile * k + 32, &s[32]);
+        tc_wait_ld();
         const uint64_t mask = tile_mask[stage];
         float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
-        for (int g = 0; g < kTile / 4; ++g) {
-          const float4 o = mine[g * kHT];
-          const float other[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            // own + other is the same sum on both CTAs (addition commutes),
-            // so both run an identical softmax
-            const int i = 4 * g + u;
-            const float full = s[i] + other[u];
-            s[i] = ((mask >> i) & 1ull) ? full * p.scale_log2 : -INFINITY;
-            mq[u] = fmaxf(mq[u], s[i]);
-          }
+        for (int i = 0; i < kTile; ++i) {
+          s[i] = ((mask >> i) & 1ull) ? s[i] * p.scale_log2 : -INFINITY;
+          mq[i & 3] = fmaxf(mq[i & 3], s[i]);
         }
         const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-        // buffer k is consumed (the values are in registers and used): re-arm
-        // it for tile gt + 2 and tell the other CTA
-        __syncwarp();
-        if (row == 0 && gt + 2 < ntotal) mbar_arrive_expect_tx(&recv_full[k], kRecvBytes);
-        if (lane == 0) arrive_peer_relaxed(sent_free_peer + 8 * k);
         // lazy rescale; tcgen05.ld/st are warp-wide, so the warp rescales
         // together when any of its rows needs it (the others scale by 1)
         const bool need = mx > m_run + kRescaleLog2;
@@ -791,10 +816,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pr[i] = pack_bf16x2(p0, p1);
         }
         l_run += (lq[0] + lq[1]) + (lq[2] + lq[3]);
-        if (t + 1 < n && !fetch_and_send(gt + 1, s_next)) {
-          ok = false;
-          break;
-        }
         // tokens that do not exist: zero their value rows (slots 0..3; 0 x NaN
         // would poison P.V); piece j = (token j / 4, slot j % 4), two per thread
         if (mask != ~0ull) {
@@ -817,8 +838,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[k]);
-#pragma unroll
-        for (int i = 0; i < kTile; ++i) s[i] = s_next[i];
       }
       if (!ok) break;
       gbase += n;

@@ -19,8 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libpa.so")
-SOURCES = ["pa_api.cu", "cache_write.cu", "mla_concat.cu", "decode.cu", "prefill.cu",
-           "mla_decode.cu", "mla_decode_tc.cu", "mla_proj.cu", "prefill_tc.cu"]
+SOURCES = ["pa_api.cu", "cache_write.cu", "mla_concat.cu", "decode.cu", "mla_decode.cu",
+           "mla_decode_tc.cu", "mla_proj.cu", "prefill_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

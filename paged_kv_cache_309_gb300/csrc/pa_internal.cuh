@@ -301,21 +301,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of the phase with `parity` (mbarrier.try_wait may
-// suspend the thread for a while when the phase is not complete; a thread
-// that polls several barriers in turn must not be held on one of them).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait for the phase with `parity` to complete.  Gives up (returns false)
 // after `timeout_ns` of wall time, or early once *abort_flag is set by
 // another warp of the CTA.
@@ -459,12 +444,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t&
       : "=r"(lo), "=r"(hi)
       : "r"(four_codes));
 }
-// two e4m3 codes (low byte first) -> f16x2, exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
 // Two floats rounded to nearest-even bf16, lo in bits 0-15: one conversion
 // instruction for the pair (two scalar conversions plus a merge cost several
 // times more issue time in the softmax loops).
@@ -585,8 +564,7 @@ struct PrefillArgs {
   int64_t num_blocks;
   float scale;
 };
-pa_status launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream);
-pa_status launch_paged_prefill_tc(const PrefillArgs& a, cudaStream_t stream);  // prefill_tc.cu
+pa_status launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream);  // prefill_tc.cu
 
 struct MlaDecodeArgs {
   void* out_latent;          // [B, H, 512] bf16

@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-pa_status launch_paged_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
+pa_status launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.max_q_len == 0) return PA_OK;
   const int32_t G = a.num_q_heads / a.num_kv_heads;
   const int64_t rows = a.num_blocks * a.block_size;

@@ -6,14 +6,16 @@
 //            q_lat[b, h, d_c + r] = q_pe[b, h, r]
 //   project: out[b, h, i]    = sum_c o_lat[b, h, c] * W_UV[c, h*d_v + i]
 // Both are Y_h = X_h . W_h per head, bf16 in, fp32 accumulate, bf16 out, on
-// the tensor cores (mma.sync m16n8k16).  A CTA computes a 64 (sequences) x
-// 64 (outputs) tile of one head with four warps of 16 rows each; the whole
-// K extent is staged once with cp.async in padded shared memory (16 bytes of
-// padding per row, so the eight rows of an ldmatrix phase hit eight
-// different bank groups).
+// the tensor cores (mma.sync m16n8k16).  A CTA owns 64 rows (sequences) of
+// one head and a group of 64-column output chunks; it walks its (column
+// chunk, 64-wide K chunk) steps through a 3-stage cp.async ring of 64 x 64
+// operand tiles (16 bytes of padding per row, so the eight rows of an
+// ldmatrix phase hit eight different bank groups), accumulating a 64 x 64
+// chunk in four warps of 16 rows.  At decode batch sizes the weights are the
+// bytes that matter: every weight element is read once per 64 sequences, and
+// two column groups per head make one wave of CTAs.
 // W_UK_h is read with rows = outputs (ldmatrix), W_UV_h with rows = the
-// reduction index (ldmatrix.trans).  At decode batch sizes the weights are
-// the bytes that matter: each weight element is read once per 64 sequences.
+// reduction index (ldmatrix.trans).
 #include <atomic>
 
 #include "pa_internal.cuh"
@@ -23,9 +25,14 @@ namespace {
 
 using namespace pa;
 
-constexpr int kTM = 64, kTN = 64;
-constexpr int kPad = 72;  // elements per staged W_UV row (64 + 8)
+constexpr int kTM = 64, kTN = 64, kTK = 64;   // CTA rows, column chunk, K chunk
+constexpr int kPad = 72;                       // elements per staged row (64 + 8)
+constexpr int kTileBytes = 64 * kPad * 2;      // one staged 64 x 64 tile: 9 KB
+constexpr int kStages = 3;
+constexpr int kStageBytes = 2 * kTileBytes;    // X tile, then W tile
+constexpr int kSmem = kStages * kStageBytes;   // 54 KB
 constexpr int kThreads = 128;
+constexpr int kGroups = 2;                     // column groups per head
 
 struct ProjParams {
   __nv_bfloat16* y;        // [M, H, ldy], columns 0..N-1 written
@@ -33,6 +40,7 @@ struct ProjParams {
   const __nv_bfloat16* w;
   const __nv_bfloat16* extra;  // absorb: q_pe [M, H, extra_dim] copied to y columns N..
   int32_t M, H, K, N, ldy, extra_dim;
+  int32_t chunks_per_group;  // 64-column chunks per CTA
 };
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, bool pred) {
@@ -46,86 +54,106 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src,
 
 // kTransB = false: W(k, n) = w[n, h*K + k]   (absorb, rows = outputs)
 // kTransB = true:  W(k, n) = w[k, h*N + n]   (project, rows = reduction index)
-// The whole K extent of the CTA's X rows and weight columns is staged with
-// cp.async before any product: one global round trip per CTA instead of
-// one per 64-wide slice (the kernel is latency-bound at decode batch sizes).
 template <bool kTransB>
 __global__ void __launch_bounds__(kThreads) mla_head_gemm_kernel(const ProjParams p) {
   extern __shared__ __align__(16) uint8_t dyn[];
-  const int ks = p.K + 8;  // staged row stride (elements): 16 bytes of padding per row
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(dyn);                 // [kTM][ks]
-  __nv_bfloat16* ws = xs + kTM * ks;  // absorb: [kTN rows = n][ks]; project: [K rows = k][kPad]
-  const int n0 = blockIdx.x * kTN;
   const int h = blockIdx.y;
   const int m0 = blockIdx.z * kTM;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int64_t xrow = static_cast<int64_t>(p.H) * p.K;
-  const int kunits = p.K / 8;  // 16-byte units per X row / absorb weight row
+  const int nk = p.K / kTK;
+  const int c_first = blockIdx.x * p.chunks_per_group;
+  const int c_count = min(p.chunks_per_group, p.N / kTN - c_first);
+  const int steps = c_count > 0 ? c_count * nk : 0;
 
-  for (int i = threadIdx.x; i < kTM * kunits; i += kThreads) {
-    const int r = i / kunits, u = i % kunits;
-    const bool ok = m0 + r < p.M;
-    cp_async16(xs + r * ks + 8 * u,
-               p.x + (ok ? (m0 + r) * xrow : 0) + static_cast<int64_t>(h) * p.K + 8 * u, ok);
-  }
-  if constexpr (kTransB) {
-    for (int i = threadIdx.x; i < p.K * 8; i += kThreads) {
+  // step s: column chunk c_first + s / nk, K chunk s % nk; 512 16-byte units
+  // per tile, four per thread
+  auto load_step = [&](int s) {
+    uint8_t* st = dyn + (s % kStages) * kStageBytes;
+    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(st);
+    __nv_bfloat16* ws = reinterpret_cast<__nv_bfloat16*>(st + kTileBytes);
+    const int n0 = (c_first + s / nk) * kTN, k0 = (s % nk) * kTK;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = threadIdx.x + kThreads * j;
       const int r = i >> 3, u = i & 7;
-      cp_async16(ws + r * kPad + 8 * u,
-                 p.w + static_cast<int64_t>(r) * p.H * p.N + static_cast<int64_t>(h) * p.N + n0 +
-                     8 * u,
-                 true);
+      const bool ok = m0 + r < p.M;
+      cp_async16(xs + r * kPad + 8 * u,
+                 p.x + (ok ? (m0 + r) * xrow : 0) + static_cast<int64_t>(h) * p.K + k0 + 8 * u, ok);
+      if constexpr (kTransB)
+        cp_async16(ws + r * kPad + 8 * u,
+                   p.w + static_cast<int64_t>(k0 + r) * p.H * p.N + static_cast<int64_t>(h) * p.N +
+                       n0 + 8 * u,
+                   true);
+      else
+        cp_async16(ws + r * kPad + 8 * u,
+                   p.w + static_cast<int64_t>(n0 + r) * p.H * p.K + static_cast<int64_t>(h) * p.K +
+                       k0 + 8 * u,
+                   true);
     }
-  } else {
-    for (int i = threadIdx.x; i < kTN * kunits; i += kThreads) {
-      const int r = i / kunits, u = i % kunits;
-      cp_async16(ws + r * ks + 8 * u,
-                 p.w + static_cast<int64_t>(n0 + r) * p.H * p.K + static_cast<int64_t>(h) * p.K +
-                     8 * u,
-                 true);
-    }
+  };
+  // one commit group per step (empty ones past the end), so that at step s
+  // exactly one newer group may still be pending
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < steps) load_step(s);
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
 
   float acc[kTN / 8][4];
 #pragma unroll
   for (int nt = 0; nt < kTN / 8; ++nt)
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[nt][c] = 0.f;
-  const uint32_t xs_base = smem_u32(xs);
-  const uint32_t ws_base = smem_u32(ws);
-  for (int kk = 0; kk < p.K / 16; ++kk) {
-    uint32_t a[4];
-    ldsm_x4(xs_base + static_cast<uint32_t>(((16 * warp + (lane & 15)) * ks + 16 * kk +
-                                            8 * (lane >> 4)) * 2), a);
+  for (int s = 0; s < steps; ++s) {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncthreads();  // step s is in shared memory for all; step s - 1's stage is free
+    if (s + kStages - 1 < steps) load_step(s + kStages - 1);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const uint32_t xs_base = smem_u32(dyn + (s % kStages) * kStageBytes);
+    const uint32_t ws_base = xs_base + kTileBytes;
 #pragma unroll
-    for (int np = 0; np < kTN / 16; ++np) {
-      uint32_t bb[4];
-      if constexpr (kTransB) {
-        // rows = k: lanes 0-7 k 0-7, 8-15 k 8-15 (n 0-7), 16-31 the same for n 8-15
-        const int kr = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
-        ldsm_x4_trans(ws_base + static_cast<uint32_t>((kr * kPad + 16 * np + 8 * (lane >> 4)) * 2), bb);
-      } else {
-        // rows = n: lanes 0-7 n 0-7 k 0-7, 8-15 n 0-7 k 8-15, 16-31 the same for n 8-15
-        const int nr = 16 * np + (lane & 7) + 8 * (lane >> 4);
-        ldsm_x4(ws_base + static_cast<uint32_t>((nr * ks + 16 * kk + 8 * ((lane >> 3) & 1)) * 2), bb);
+    for (int kk = 0; kk < kTK / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(xs_base + static_cast<uint32_t>(((16 * warp + (lane & 15)) * kPad + 16 * kk +
+                                              8 * (lane >> 4)) * 2), a);
+#pragma unroll
+      for (int np = 0; np < kTN / 16; ++np) {
+        uint32_t bb[4];
+        if constexpr (kTransB) {
+          // rows = k: lanes 0-7 k 0-7, 8-15 k 8-15 (n 0-7), 16-31 the same for n 8-15
+          const int kr = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
+          ldsm_x4_trans(ws_base + static_cast<uint32_t>((kr * kPad + 16 * np + 8 * (lane >> 4)) * 2), bb);
+        } else {
+          // rows = n: lanes 0-7 n 0-7 k 0-7, 8-15 n 0-7 k 8-15, 16-31 the same for n 8-15
+          const int nr = 16 * np + (lane & 7) + 8 * (lane >> 4);
+          ldsm_x4(ws_base + static_cast<uint32_t>((nr * kPad + 16 * kk + 8 * ((lane >> 3) & 1)) * 2), bb);
+        }
+        mma_bf16_16816(acc[2 * np], a, bb[0], bb[1]);
+        mma_bf16_16816(acc[2 * np + 1], a, bb[2], bb[3]);
       }
-      mma_bf16_16816(acc[2 * np], a, bb[0], bb[1]);
-      mma_bf16_16816(acc[2 * np + 1], a, bb[2], bb[3]);
+    }
+    if (s % nk == nk - 1) {
+      // the column chunk is complete: write it and start the next
+      const int n0 = (c_first + s / nk) * kTN;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int m = m0 + 16 * warp + gq + 8 * r;
+        if (m >= p.M) continue;
+        __nv_bfloat16* dst = p.y + (static_cast<int64_t>(m) * p.H + h) * p.ldy + n0 + 2 * tq;
+#pragma unroll
+        for (int nt = 0; nt < kTN / 8; ++nt)
+          *reinterpret_cast<uint32_t*>(dst + 8 * nt) =
+              pack_bf16x2(acc[nt][2 * r], acc[nt][2 * r + 1]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < kTN / 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[nt][c] = 0.f;
     }
   }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int m = m0 + 16 * warp + gq + 8 * r;
-    if (m >= p.M) continue;
-    __nv_bfloat16* dst = p.y + (static_cast<int64_t>(m) * p.H + h) * p.ldy + n0 + 2 * tq;
-#pragma unroll
-    for (int nt = 0; nt < kTN / 8; ++nt)
-      *reinterpret_cast<uint32_t*>(dst + 8 * nt) = pack_bf16x2(acc[nt][2 * r], acc[nt][2 * r + 1]);
-  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   // absorb: the rope part of the query is copied behind the latent part
   if (p.extra != nullptr && blockIdx.x == 0) {
     const int units = p.extra_dim / 8;
@@ -140,24 +168,20 @@ __global__ void __launch_bounds__(kThreads) mla_head_gemm_kernel(const ProjParam
 }
 
 template <bool kTransB>
-size_t gemm_smem_bytes(int K) {
-  return static_cast<size_t>(kTM) * (K + 8) * 2 +
-         (kTransB ? static_cast<size_t>(K) * kPad * 2 : static_cast<size_t>(kTN) * (K + 8) * 2);
-}
-
-template <bool kTransB>
-pa_status launch_gemm(const ProjParams& p, dim3 grid, cudaStream_t stream) {
-  constexpr int kMaxSmem = 200 * 1024;
-  const size_t smem = gemm_smem_bytes<kTransB>(p.K);
-  if (smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
+pa_status launch_gemm(ProjParams p, cudaStream_t stream) {
+  const int chunks = p.N / kTN;
+  const int groups = chunks < kGroups ? chunks : kGroups;
+  p.chunks_per_group = (chunks + groups - 1) / groups;
+  const dim3 grid(static_cast<unsigned>(groups), static_cast<unsigned>(p.H),
+                  static_cast<unsigned>((p.M + kTM - 1) / kTM));
   static std::atomic<bool> attr_set{false};
   if (!attr_set.load()) {
     if (cudaFuncSetAttribute(mla_head_gemm_kernel<kTransB>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
       return PA_ERR_CUDA;
     attr_set.store(true);
   }
-  mla_head_gemm_kernel<kTransB><<<grid, kThreads, smem, stream>>>(p);
+  mla_head_gemm_kernel<kTransB><<<grid, kThreads, kSmem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -167,6 +191,7 @@ pa_status launch_mla_absorb_q(void* q_latent, const void* q_nope, const void* q_
                               const void* w_uk, int32_t num_seqs, int32_t num_heads,
                               int32_t nope_dim, int32_t rope_dim, int32_t latent_dim,
                               cudaStream_t stream) {
+  if (num_seqs == 0) return PA_OK;
   ProjParams p;
   p.y = static_cast<__nv_bfloat16*>(q_latent);
   p.x = static_cast<const __nv_bfloat16*>(q_nope);
@@ -178,14 +203,13 @@ pa_status launch_mla_absorb_q(void* q_latent, const void* q_nope, const void* q_
   p.N = latent_dim;
   p.ldy = latent_dim + rope_dim;
   p.extra_dim = rope_dim;
-  const dim3 grid(static_cast<unsigned>(latent_dim / kTN), static_cast<unsigned>(num_heads),
-                  static_cast<unsigned>((num_seqs + kTM - 1) / kTM));
-  return launch_gemm<false>(p, grid, stream);
+  return launch_gemm<false>(p, stream);
 }
 
 pa_status launch_mla_project_out(void* out, const void* out_latent, const void* w_uv,
                                  int32_t num_seqs, int32_t num_heads, int32_t latent_dim,
                                  int32_t v_head_dim, cudaStream_t stream) {
+  if (num_seqs == 0) return PA_OK;
   ProjParams p;
   p.y = static_cast<__nv_bfloat16*>(out);
   p.x = static_cast<const __nv_bfloat16*>(out_latent);
@@ -197,9 +221,7 @@ pa_status launch_mla_project_out(void* out, const void* out_latent, const void* 
   p.N = v_head_dim;
   p.ldy = v_head_dim;
   p.extra_dim = 0;
-  const dim3 grid(static_cast<unsigned>(v_head_dim / kTN), static_cast<unsigned>(num_heads),
-                  static_cast<unsigned>((num_seqs + kTM - 1) / kTM));
-  return launch_gemm<true>(p, grid, stream);
+  return launch_gemm<true>(p, stream);
 }
 
 }  // namespace pa_detail

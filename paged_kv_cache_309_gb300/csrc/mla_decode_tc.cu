@@ -27,21 +27,22 @@
 //    slice of q_lat sits in TMEM (latent part, bf16 pairs) and in shared
 //    memory (rope part).
 //  * partial S[128 x 64] over the CTA's 288 elements: 18 tcgen05.mma
-//    (M=128, N=64, K=16).  The softmax threads (thread = head row) read
-//    their 64 partial scores (tcgen05.ld), send them to the other CTA's
+//    (M=128, N=64, K=16).  The exchange threads (thread = head row) read
+//    the 64 partial scores (tcgen05.ld), send them to the other CTA's
 //    exchange buffer through distributed shared memory (st.async, counted
-//    in bytes on the other CTA's mbarrier), and add the other CTA's
-//    partials: both CTAs add the same two numbers, so both run the
-//    identical softmax.  The weights (bf16) are written over the score
-//    buffer in TMEM.
+//    in bytes on the other CTA's mbarrier), add the other CTA's partials
+//    and write the full scores back: both CTAs add the same two numbers, so
+//    both run the identical softmax.  The softmax threads write the weights
+//    (bf16) over the score buffer in TMEM.
 //  * O[128 x 256] += P . V: 4 tcgen05.mma (N=256, K=16) with P from TMEM
 //    and V = the CTA's latent chunks read in place as an MN-major operand.
 //  * warp roles: warp 0 issues the TMA loads; one thread of warp 1 (the TMEM
 //    owner) issues the score products and one thread of warp 6 the output
-//    products, each blocking in bounded waits; warps 2-5 load q_lat and run
-//    the softmax: fp32, base 2, lazy rescale (the running max moves only
-//    when a score beats it by more than 2^8; the rescale reads, scales and
-//    writes back the TMEM output row).
+//    products, each blocking in bounded waits; warps 7-10 trade the partial
+//    scores with the other CTA; warps 2-5 load q_lat and run the softmax:
+//    fp32, base 2, lazy rescale (the running max moves only when a score
+//    beats it by more than 2^8; the rescale reads, scales and writes back
+//    the TMEM output row).
 //  * epilogue of a piece: the softmax threads read their output row from
 //    TMEM and write bf16 (whole sequence) or an fp32 partial + log2-sum-exp.
 //

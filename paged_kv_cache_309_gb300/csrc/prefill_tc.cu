@@ -1,7 +1,7 @@
 // prefill_tc.cu -- causal varlen prefill attention over the paged cache on
 // the 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
-// What is computed (as prefill.cu): sequence b has n_b = cu_seqlens_q[b+1]
+// What is computed: sequence b has n_b = cu_seqlens_q[b+1]
 // - cu_seqlens_q[b] new tokens, the last n_b of its context_lens[b] = L_b
 // cached tokens; new token j sits at position p = L_b - n_b + j and attends
 // causally to tokens 0..p, read along the block table (nano-vLLM

@@ -385,6 +385,15 @@ pa_status pa_mla_project_out(void *out, const void *out_latent, const void *w_uv
                              int32_t num_seqs, int32_t num_heads, int32_t latent_dim,
                              int32_t v_head_dim, pa_stream_t stream);
 
+/* Diagnostic of the failure path every pipeline kernel shares: launches one
+ * CTA whose threads wait, with the same bounded wait the pipelines use, on a
+ * barrier that nothing completes.  After the wait limit (2 s) the kernel
+ * sets PA_DEVERR_WAIT_TIMEOUT in *error_word (a device pointer to one 4-byte
+ * word, 4-byte aligned; the caller clears it) and exits, leaving the context
+ * usable.  Stream-ordered; returns PA_ERR_INVALID for a null word and
+ * PA_ERR_CUDA if the launch fails. */
+pa_status pa_selftest_bounded_wait(unsigned *error_word, pa_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *pa_status_string(pa_status status);
 

@@ -84,9 +84,28 @@ pa_status check_decode(void* out, const void* q, const void* k_cache, const void
   return PA_OK;
 }
 
+// One CTA waits on a barrier nothing arrives on: the bounded wait gives up
+// after its limit and the error bit is set, as in any pipeline kernel.
+__global__ void selftest_bounded_wait_kernel(unsigned* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    pa::mbar_init(&bar, 1);
+    pa::mbar_init_fence();
+  }
+  __syncthreads();
+  const bool ok = pa::mbar_wait_bounded(&bar, 0, nullptr);
+  if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) atomicOr(err, PA_DEVERR_WAIT_TIMEOUT);
+}
+
 }  // namespace
 
 extern "C" {
+
+pa_status pa_selftest_bounded_wait(unsigned* error_word, pa_stream_t stream) {
+  if (error_word == nullptr || !aligned(error_word, 4)) return PA_ERR_INVALID;
+  selftest_bounded_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(error_word);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
 
 const char* pa_status_string(pa_status s) {
   switch (s) {

@@ -83,6 +83,8 @@ def _load():
     lib.pa_mla_decode_attention.restype = E
     lib.pa_mla_project_out.argtypes = [P, P, P, I32, I32, I32, I32, P]
     lib.pa_mla_project_out.restype = E
+    lib.pa_selftest_bounded_wait.argtypes = [P, P]
+    lib.pa_selftest_bounded_wait.restype = E
     _lib = lib
     return lib
 
@@ -318,6 +320,14 @@ def pa_paged_prefill_attention(out, q, k_cache, v_cache, block_tables, cu_seqlen
         _ptr(cu_seqlens_q), _ptr(context_lens), B, HQ, HKV, d, bs, block_tables.shape[1], nb,
         float(scale), int(max_q_len), _ptr(error_word), _stream(stream))
     _check(st, "pa_paged_prefill_attention")
+
+
+def pa_selftest_bounded_wait(error_word, stream=None):
+    """Diagnostic: one CTA's bounded wait on a barrier nothing completes runs
+    out (2 s) and sets PA_DEVERR_WAIT_TIMEOUT (1) in error_word, a one-element
+    int32 device tensor the caller cleared."""
+    st = _load().pa_selftest_bounded_wait(_ptr(error_word), _stream(stream))
+    _check(st, "pa_selftest_bounded_wait")
 
 
 # ------------------------------------------------------------- MLA decode --

@@ -776,15 +776,10 @@ __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem
 template <int NT, bool kFp8>
 pa_status launch_split_tc(const CUtensorMap& mk, const CUtensorMap& mv, const DecodeParams& p,
                           dim3 grid, int G, cudaStream_t stream) {
-  static std::atomic<bool> attr_set{false};
+  static std::atomic<uint64_t> smem_raised{0};
   auto kern = paged_decode_split_tc_kernel<NT, kFp8>;
   constexpr int kSmem = TcLayout<kFp8>::kAlloc;
-  if (!attr_set.load()) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-        cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set.store(true);
-  }
+  if (!ensure_smem_limit(kern, kSmem, smem_raised)) return PA_ERR_CUDA;
   kern<<<grid, kThreads, kSmem, stream>>>(mk, mv, p, G);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

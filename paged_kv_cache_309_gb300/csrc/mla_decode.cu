@@ -417,15 +417,10 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
 template <int HT>
 pa_status launch_mla_split(const CUtensorMap& mq, const CUtensorMap& mkv, const MlaParams& p,
                            dim3 grid, cudaStream_t stream) {
-  static std::atomic<bool> attr_set{false};
+  static std::atomic<uint64_t> smem_raised{0};
   auto kern = mla_decode_split_kernel<HT>;
   constexpr int kSmem = MlaCfg<HT>::kAlloc;
-  if (!attr_set.load()) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
-        cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set.store(true);
-  }
+  if (!ensure_smem_limit(kern, kSmem, smem_raised)) return PA_ERR_CUDA;
   kern<<<grid, kThreads, kSmem, stream>>>(mq, mkv, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

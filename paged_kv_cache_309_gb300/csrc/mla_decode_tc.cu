@@ -945,13 +945,8 @@ int mla_tc_tile() { return kTile; }
 
 pa_status launch_mla_tc(const CUtensorMap& mrope, const CUtensorMap& mkv, const MlaParams& p,
                         dim3 grid, cudaStream_t stream) {
-  static std::atomic<bool> attr_set{false};
-  if (!attr_set.load()) {
-    if (cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kAlloc) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set.store(true);
-  }
+  static std::atomic<uint64_t> smem_raised{0};
+  if (!ensure_smem_limit(mla_decode_tc_kernel, kAlloc, smem_raised)) return PA_ERR_CUDA;
   mla_decode_tc_kernel<<<grid, kThreads, kAlloc, stream>>>(mkv, mrope, p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

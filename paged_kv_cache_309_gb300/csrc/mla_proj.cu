@@ -174,13 +174,8 @@ pa_status launch_gemm(ProjParams p, cudaStream_t stream) {
   p.chunks_per_group = (chunks + groups - 1) / groups;
   const dim3 grid(static_cast<unsigned>(groups), static_cast<unsigned>(p.H),
                   static_cast<unsigned>((p.M + kTM - 1) / kTM));
-  static std::atomic<bool> attr_set{false};
-  if (!attr_set.load()) {
-    if (cudaFuncSetAttribute(mla_head_gemm_kernel<kTransB>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set.store(true);
-  }
+  static std::atomic<uint64_t> smem_raised{0};
+  if (!ensure_smem_limit(mla_head_gemm_kernel<kTransB>, kSmem, smem_raised)) return PA_ERR_CUDA;
   mla_head_gemm_kernel<kTransB><<<grid, kThreads, kSmem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

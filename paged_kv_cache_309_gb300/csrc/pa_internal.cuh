@@ -14,6 +14,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pa.h"
 
 namespace pa {
@@ -474,6 +476,23 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 // ------------------------------------------------- internal host launchers --
 namespace pa_detail {
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device: the attribute is per device, and `raised` (one per
+// call site) holds a bit for each device already done.
+template <typename Kernel>
+inline bool ensure_smem_limit(Kernel kernel, int bytes, std::atomic<uint64_t>& raised) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (raised.load() & bit) != 0ull) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  raised.fetch_or(bit);
+  return true;
+}
+
 
 int num_sms_current_device();  // cached per device; 0 if no device
 

@@ -598,13 +598,8 @@ pa_status launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream) {
   const int64_t per_cta = static_cast<int64_t>(kQTiles) * p.tokens_per_tile;
   const int64_t qpairs = (static_cast<int64_t>(a.max_q_len) + per_cta - 1) / per_cta;
   if (qpairs > 0x7FFFFFFF) return PA_ERR_UNSUPPORTED;
-  static std::atomic<bool> attr_set{false};
-  if (!attr_set.load()) {
-    if (cudaFuncSetAttribute(paged_prefill_tcgen05_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc) != cudaSuccess)
-      return PA_ERR_CUDA;
-    attr_set.store(true);
-  }
+  static std::atomic<uint64_t> smem_raised{0};
+  if (!ensure_smem_limit(paged_prefill_tcgen05_kernel, kAlloc, smem_raised)) return PA_ERR_CUDA;
   const dim3 grid(static_cast<unsigned>(qpairs), static_cast<unsigned>(a.num_kv_heads),
                   static_cast<unsigned>(a.num_seqs));
   paged_prefill_tcgen05_kernel<<<grid, kThreads, kAlloc, stream>>>(mk, mv, p);

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(Resha
   using namespace pa;
   const int lane = threadIdx.x & 31;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  const int64_t t = wid / a.groups;
+  const int64_t t = a.groups == 1 ? wid : wid / a.groups;  // a 64-bit division is long
   const int grp = static_cast<int>(wid - t * a.groups);
   if (t >= a.num_tokens) return;
 
@@ -40,7 +40,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(Resha
     if (s < 0) return;
   }
   if (s >= a.num_slots) return;
-  const int64_t blk = s / a.block_size;
+  const int64_t blk = (a.block_size & (a.block_size - 1)) == 0
+                          ? s >> (__ffs(a.block_size) - 1)
+                          : s / a.block_size;
   const int64_t off = s - blk * a.block_size;
   const int64_t row_elems = static_cast<int64_t>(a.row_chunks) * 8;
   const int64_t dst0 = blk * a.block_stride + off * row_elems;
@@ -83,22 +85,22 @@ __global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(Resha
       const int c = c_begin + 32 * i;
       if (c < a.row_chunks) {
         float f[8];
-        to_f32(kv[i], f);
-        if (scaled) {
-          if constexpr (kToE4m3) {
-            div8_for_e4m3(f, ks, kxmax);
-          } else {
+        if (kToE4m3 && scaled) {
+          div8_for_e4m3(kv[i], f, ks, kxmax);
+        } else {
+          to_f32(kv[i], f);
+          if (scaled) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = div_rn(f[e], ks);  // IEEE quotient
           }
         }
         store8(kdst + 8 * c, from_f32<D>(f));
         if (has_v) {
-          to_f32(vv[i], f);
-          if (scaled) {
-            if constexpr (kToE4m3) {
-              div8_for_e4m3(f, vs, vxmax);
-            } else {
+          if (kToE4m3 && scaled) {
+            div8_for_e4m3(vv[i], f, vs, vxmax);
+          } else {
+            to_f32(vv[i], f);
+            if (scaled) {
 #pragma unroll
               for (int e = 0; e < 8; ++e) f[e] = div_rn(f[e], vs);
             }

@@ -212,11 +212,12 @@ __device__ __forceinline__ bool fused_token_write(const DecodeParams& p, int b, 
   uint8_t* region = stage_smem + (is_v ? v_offset : 0);
   if constexpr (kFp8) {
     float f[8];
-    to_f32(x, f);
     const float* sc = is_v ? p.v_scale : p.k_scale;
     if (sc != nullptr) {
       const Divisor d = make_divisor(__ldg(sc));
-      div8_for_e4m3(f, d, fminf(1.7e38f * d.s, 3.0e38f));
+      div8_for_e4m3(x, f, d, fminf(1.7e38f * d.s, 3.0e38f));
+    } else {
+      to_f32(x, f);
     }
     const Vec8<e4m3> y = from_f32<e4m3>(f);
     store8(static_cast<e4m3*>(is_v ? p.v_cache : p.k_cache) + dst, y);

@@ -106,6 +106,27 @@ __device__ __forceinline__ void to_f32(const Vec8<float>& v, float f[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[i]);
 }
+// the same, negated (-x: the sign bit flipped in the source format, exact)
+__device__ __forceinline__ void to_f32_neg(const Vec8<bf16>& v, float f[8]) {
+  const uint32_t w[4] = {v.u.x, v.u.y, v.u.z, v.u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float((w[i] << 16) ^ 0x80000000u);
+    f[2 * i + 1] = __uint_as_float((w[i] & 0xFFFF0000u) ^ 0x80000000u);
+  }
+}
+__device__ __forceinline__ void to_f32_neg(const Vec8<f16>& v, float f[8]) {
+  Vec8<f16> n;
+  n.u = make_uint4(v.u.x ^ 0x80008000u, v.u.y ^ 0x80008000u, v.u.z ^ 0x80008000u,
+                   v.u.w ^ 0x80008000u);
+  to_f32(n, f);
+}
+__device__ __forceinline__ void to_f32_neg(const Vec8<float>& v, float f[8]) {
+  const uint32_t w[8] = {v.u[0].x, v.u[0].y, v.u[0].z, v.u[0].w,
+                         v.u[1].x, v.u[1].y, v.u[1].z, v.u[1].w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(w[i] ^ 0x80000000u);
+}
 
 // narrow eight fp32 values, round to nearest even (E4M3: saturating)
 template <typename T>
@@ -190,14 +211,6 @@ static __device__ __noinline__ F8 div8_library(F8 x, float s) {
   return x;
 }
 
-// Eight quotients x / s that only feed a round-to-nearest cast to E4M3.
-// Such a cast depends on the fp32 quotient only where |x / s| lies in
-// [2^-11, 480]: smaller values become +-0, larger ones saturate.  With the
-// divisor in [2^-30, 2^30] (d.fast), every quotient in that band has
-// |x| >= 2^-41, where the two residual corrections of div_rn are exact, so
-// no per-value range test is needed -- only that x * r cannot overflow (the
-// chunk's largest |x| at most xmax; NaN passes through as NaN) -- and the
-// sign of a zero quotient is restored from x.  Other chunks use the library.
 // The same operations on pairs (one instruction for two lanes of work on
 // sm_100 and later; each lane rounds exactly as the scalar operation does).
 __device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
@@ -224,25 +237,43 @@ __device__ __forceinline__ float max3_abs(float a, float b, float c) {
   return d;
 }
 
-__device__ __forceinline__ void div8_for_e4m3(float (&f)[8], const Divisor& d, float xmax) {
+// Eight quotients x / s (x: the eight source elements of v) that only feed
+// a round-to-nearest cast to E4M3.  Such a cast depends on the fp32 quotient
+// only where |x / s| lies in [2^-11, 480]: smaller values become +-0, larger
+// ones saturate.  With the divisor in [2^-30, 2^30] (d.fast), every quotient
+// in that band has |x| >= 2^-41, where the two residual corrections of
+// div_rn are exact, so no per-value range test is needed -- only that x * r
+// cannot overflow (the chunk's largest |x| at most xmax; NaN passes through
+// as NaN).  Other chunks use the library.
+// The corrections run on n = -x, which the widening gives at no extra cost:
+//     y0 = RN(n (-r)),  y' = RN(y + RN(s y + n) (-r)).
+// Round-to-nearest is symmetric in sign, so RN(s y + n) = -RN(x - s y) and
+// every step equals the one of div_rn for a nonzero quotient; for a zero one
+// the signed-zero sums give the sign of x (x = -0: RN(-0 + +0) = +0, then
+// RN(+0 (-r) + -0) = -0), with no separate sign fix-up.
+template <typename S>
+__device__ __forceinline__ void div8_for_e4m3(const Vec8<S>& v, float (&f)[8], const Divisor& d,
+                                              float xmax) {
+  float n[8];
+  to_f32_neg(v, n);
   float amax = 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; e += 2) amax = max3_abs(amax, f[e], f[e + 1]);
+  for (int e = 0; e < 8; e += 2) amax = max3_abs(amax, n[e], n[e + 1]);
   if (d.fast && amax <= xmax) {
-    const float2 r2 = make_float2(d.r, d.r), ns2 = make_float2(-d.s, -d.s);
+    const float2 nr2 = make_float2(-d.r, -d.r), s2 = make_float2(d.s, d.s);
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-      const float2 x = make_float2(f[e], f[e + 1]);
-      float2 q = mul2_rn(x, r2);
-      q = fma2_rn(fma2_rn(ns2, q, x), r2, q);
-      q = fma2_rn(fma2_rn(ns2, q, x), r2, q);
-      f[e] = copysignf(q.x, x.x);
-      f[e + 1] = copysignf(q.y, x.y);
+      const float2 ne = make_float2(n[e], n[e + 1]);
+      float2 y = mul2_rn(ne, nr2);
+      y = fma2_rn(fma2_rn(s2, y, ne), nr2, y);
+      y = fma2_rn(fma2_rn(s2, y, ne), nr2, y);
+      f[e] = y.x;
+      f[e + 1] = y.y;
     }
   } else {
     F8 t;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) t.v[e] = f[e];
+    for (int e = 0; e < 8; ++e) t.v[e] = -n[e];
     t = div8_library(t, d.s);
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] = t.v[e];

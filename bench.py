@@ -640,6 +640,41 @@ def run_prefill_only(args):
           f"{tf:.1f} TFLOP/s), device error word {int(perr.item())}")
 
 
+def run_write_only(args):
+    """Cache-write launches only (for an ncu capture of that kernel): --steps
+    launches of the 32K-token prefill write to an e4m3 cache (scale 0.05),
+    then --steps of the same write to a bf16 cache."""
+    import torch
+
+    from paged_kv_cache_309_gb300 import build, pa
+    from paged_kv_cache_309_gb300 import workloads as wl
+    build.build()
+    dev = torch.device("cuda", 0)
+    for variant in ("e4m3", "bf16"):
+        w = wl.prefill_write(variant=variant)
+        H, d = w.key.shape[1:]
+        cdt = torch.float8_e4m3fn if w.cache_dtype == "e4m3" else torch.bfloat16
+        kc = torch.zeros((w.num_blocks, w.block_size, H, d), dtype=cdt, device=dev)
+        vc = torch.zeros_like(kc)
+        key, val = up(w.key, torch.bfloat16, dev), up(w.value, torch.bfloat16, dev)
+        sl = torch.from_numpy(w.slot_mapping).to(dev)
+        ks = None if w.k_scale is None else torch.tensor([w.k_scale], dtype=torch.float32,
+                                                         device=dev)
+        vs = None if ks is None else ks.clone()
+        pa.pa_reshape_and_cache(key, val, kc, vc, sl, None, ks, vs)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps - 1):
+            pa.pa_reshape_and_cache(key, val, kc, vc, sl, None, ks, vs)
+        e1.record()
+        torch.cuda.synchronize()
+        per = e0.elapsed_time(e1) / max(1, args.steps - 1)
+        gbs = wl.write_bytes(w) / (per * 1e-3) / 1e9
+        print(f"{w.name}: {args.steps} launches, {per * 1e3:.1f} us per launch (back to back, "
+              f"{gbs:.0f} GB/s)")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -659,6 +694,9 @@ def main():
     ap.add_argument("--prefill-only", action="store_true",
                     help="profiling aid: only run --steps causal prefill launches on the "
                          "4 x 8192-token workload (no JSON)")
+    ap.add_argument("--write-only", action="store_true",
+                    help="profiling aid: only run --steps cache-write launches of the 32K-token "
+                         "prefill write, e4m3 then bf16 cache (no JSON)")
     ap.add_argument("--mla-heads", type=int, default=0,
                     help="profiling aid: only run --steps MLA decode attention launches on the "
                          "B=64 context 512..4096 latent workload with this many heads (no JSON)")
@@ -670,6 +708,9 @@ def main():
         return
     if args.prefill_only:
         run_prefill_only(args)
+        return
+    if args.write_only:
+        run_write_only(args)
         return
     if args.impl == "reference":
         run_reference(args)

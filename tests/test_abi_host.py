@@ -206,3 +206,93 @@ def test_mla_projections_reject(lib):
     assert pr(dv=100) == pa.PA_ERR_UNSUPPORTED
     assert pr(x=FAKE_MIS) == pa.PA_ERR_ALIGN
     assert pr(B=0) == pa.PA_OK
+
+
+_DEC_KEYS = ("out", "q", "kc", "vc", "cd", "bt", "cl", "B", "HQ", "HKV", "d", "bs", "mbps",
+             "nb", "scale", "maxctx")
+
+
+def _dec_args(**kw):
+    a = dict(out=FAKE, q=FAKE, kc=FAKE, vc=FAKE, cd=pa.PA_BF16, bt=FAKE, cl=FAKE, B=4, HQ=32,
+             HKV=8, d=128, bs=16, mbps=8, nb=64, scale=0.088, maxctx=128)
+    a.update(kw)
+    return a
+
+
+def test_decode_fp8_rejects(lib):
+    def fp8(ksc=FAKE, vsc=FAKE, ws=FAKE, wsb=1 << 20, **kw):
+        a = _dec_args(**kw)
+        return lib.pa_paged_decode_attention_fp8(
+            a["out"], a["q"], a["kc"], a["vc"], ksc, vsc, a["bt"], a["cl"], a["B"], a["HQ"],
+            a["HKV"], a["d"], a["bs"], a["mbps"], a["nb"], a["scale"], a["maxctx"], ws, wsb,
+            None)
+    assert fp8(vsc=None) == pa.PA_ERR_INVALID                 # one scale without the other
+    assert fp8(ksc=None) == pa.PA_ERR_INVALID
+    assert fp8(q=None) == pa.PA_ERR_INVALID                   # the shared decode checks
+    assert fp8(HQ=12) == pa.PA_ERR_INVALID
+    assert fp8(d=64) == pa.PA_ERR_UNSUPPORTED
+    assert fp8(bs=12) == pa.PA_ERR_UNSUPPORTED
+    assert fp8(kc=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert fp8(ws=None) == pa.PA_ERR_WORKSPACE
+    assert fp8(wsb=16) == pa.PA_ERR_WORKSPACE
+    assert fp8(ws=P(0x100010)) == pa.PA_ERR_ALIGN             # workspace below 256 B alignment
+
+
+def test_decode_step_rejects(lib):
+    def step(nk=FAKE, nv=FAKE, sl=FAKE, ksc=None, vsc=None, ws=FAKE, wsb=1 << 20, **kw):
+        a = _dec_args(**kw)
+        return lib.pa_paged_decode_step(
+            a["out"], a["q"], nk, nv, sl, a["kc"], a["vc"], a["cd"], ksc, vsc, a["bt"], a["cl"],
+            a["B"], a["HQ"], a["HKV"], a["d"], a["bs"], a["mbps"], a["nb"], a["scale"],
+            a["maxctx"], ws, wsb, None)
+    assert step(ksc=FAKE) == pa.PA_ERR_INVALID                # one scale
+    assert step(ksc=FAKE, vsc=FAKE) == pa.PA_ERR_INVALID      # scales with a bf16 cache
+    assert step(nk=None) == pa.PA_ERR_INVALID                 # new tokens missing
+    assert step(sl=None) == pa.PA_ERR_INVALID
+    assert step(nv=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert step(cd=pa.PA_FP16) == pa.PA_ERR_UNSUPPORTED
+    assert step(scale=float("inf")) == pa.PA_ERR_INVALID
+    assert step(ws=None) == pa.PA_ERR_WORKSPACE
+    assert step(ws=P(0x100010)) == pa.PA_ERR_ALIGN
+
+
+def test_prefill_rejects(lib):
+    def pf(cu=FAKE, mql=64, err=FAKE, **kw):
+        a = _dec_args(**kw)
+        return lib.pa_paged_prefill_attention(
+            a["out"], a["q"], a["kc"], a["vc"], a["cd"], a["bt"], cu, a["cl"], a["B"], a["HQ"],
+            a["HKV"], a["d"], a["bs"], a["mbps"], a["nb"], a["scale"], mql, err, None)
+    assert pf(B=0) == pa.PA_OK                                # nothing to attend, no launch
+    assert pf(mql=0) == pa.PA_OK
+    assert pf(mql=-1) == pa.PA_ERR_INVALID
+    assert pf(HQ=0) == pa.PA_ERR_INVALID
+    assert pf(nb=0) == pa.PA_ERR_INVALID
+    assert pf(cu=None) == pa.PA_ERR_INVALID
+    assert pf(err=None) == pa.PA_ERR_INVALID                  # the error word is required
+    assert pf(HQ=12) == pa.PA_ERR_INVALID
+    assert pf(scale=float("nan")) == pa.PA_ERR_INVALID
+    assert pf(cd=pa.PA_FP8_E4M3) == pa.PA_ERR_UNSUPPORTED
+    assert pf(d=64) == pa.PA_ERR_UNSUPPORTED
+    assert pf(HQ=24) == pa.PA_ERR_UNSUPPORTED                 # G = 3
+    assert pf(bs=4) == pa.PA_ERR_UNSUPPORTED
+    assert pf(nb=1 << 28) == pa.PA_ERR_UNSUPPORTED            # slots past int32
+    assert pf(out=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert pf(err=P(0x100002)) == pa.PA_ERR_ALIGN
+
+
+def test_static_decode_rejects(lib):
+    def st(err=None, **kw):
+        a = _dec_args(**kw)
+        return lib.pa_paged_decode_attention_static(*[a[k] for k in _DEC_KEYS], err, None)
+    assert st(q=None) == pa.PA_ERR_INVALID
+    assert st(HQ=12) == pa.PA_ERR_INVALID
+    assert st(d=64) == pa.PA_ERR_UNSUPPORTED
+    assert st(vc=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert st(err=P(0x100002)) == pa.PA_ERR_ALIGN             # error word not 4-byte aligned
+    assert st(B=0) == pa.PA_OK                                # no sequences: returns before
+                                                              # touching the device scratch
+
+
+def test_selftest_rejects(lib):
+    assert lib.pa_selftest_bounded_wait(None, None) == pa.PA_ERR_INVALID
+    assert lib.pa_selftest_bounded_wait(P(0x100002), None) == pa.PA_ERR_INVALID

@@ -136,7 +136,8 @@ def test_dtype_pairs(src, cdt):
 
 # ---------------------------------------------------- layouts and skips ----
 @pytest.mark.parametrize("H,d,bs", [(8, 128, 16), (1, 576, 64), (3, 64, 8), (128, 192, 4),
-                                    (2, 8, 1), (1, 8, 16), (16, 1024, 2)])
+                                    (2, 8, 1), (1, 8, 16), (16, 1024, 2),
+                                    (8, 128, 12), (2, 64, 3)])  # block sizes not powers of two
 def test_shapes(H, d, bs):
     rng = np.random.default_rng(H * 1000 + d)
     N = 37

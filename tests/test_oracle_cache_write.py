@@ -139,6 +139,24 @@ def test_swa_second_stage():
         assert (flat[tgt] == 0x7FC0).all()
 
 
+def test_swa_hand_worked_example():
+    """Five tokens, a 5-entry SWA table and a 4-slot SWA pool (2 blocks of 2),
+    resolved by hand: token 0 -> s=2 -> swa[2]=1; token 1 -> -1 (skip);
+    token 2 -> s=4 -> swa[4]=2; token 3 -> s=0 -> swa[0]=-1 (skip);
+    token 4 -> s=3 -> swa[3]=0.  Slot 3 is never written."""
+    H, d = 1, 8
+    key = bf16((5, H, d))
+    slots = np.array([2, -1, 4, 0, 3], dtype=np.int64)
+    swa = np.array([-1, -1, 1, 0, 2], dtype=np.int64)
+    kc = poison_cache(2, 2, H, d)
+    n = oracle.reshape_and_cache(key, None, oracle.BF16, kc, None, oracle.BF16, slots,
+                                 swa_slot_mapping=swa)
+    assert n == 3
+    flat = kc.reshape(4, H, d)
+    assert (flat[0] == key[4]).all() and (flat[1] == key[0]).all() and (flat[2] == key[2]).all()
+    assert (flat[3] == 0x7FC0).all()
+
+
 def test_duplicate_slot_refused():
     key = bf16((3, 1, 8))
     kc = poison_cache(2, 2, 1, 8)
@@ -199,6 +217,23 @@ def test_scaled_bf16_vs_library():
     kf = torch.from_numpy(key.view(np.int16)).view(torch.bfloat16).float().numpy()
     ref = torch.from_numpy(kf / np.float32(0.3)).to(torch.bfloat16).view(torch.int16).numpy()
     assert (kc.reshape(-1, H, d) == ref.view(np.uint16)).all()
+
+
+def test_scaled_same_format_power_of_two_scales_closed_form():
+    """Dividing by 2 or by 1/2 is exact, so a scaled bf16 -> bf16 write only
+    moves the exponent field of a normal value (well inside the range) by one:
+    code - 0x80 for K with k_scale = 2, code + 0x80 for V with v_scale = 0.5."""
+    N, H, d = 48, 2, 16
+    key, val = bf16((N, H, d)), bf16((N, H, d))
+    for a in (key, val):  # keep exponent fields in [2, 253]
+        e = (a >> 7) & 0xFF
+        a[(e < 2) | (e > 253)] = 0x3F80  # 1.0
+    slots = RNG.permutation(N).astype(np.int64)
+    kc, vc = poison_cache(3, 16, H, d), poison_cache(3, 16, H, d)
+    oracle.reshape_and_cache(key, val, oracle.BF16, kc, vc, oracle.BF16, slots, k_scale=2.0,
+                             v_scale=0.5)
+    assert (kc.reshape(-1, H, d)[slots] == key - 0x80).all()
+    assert (vc.reshape(-1, H, d)[slots] == val + 0x80).all()
 
 
 def test_fp16_and_fp32_sources():

@@ -173,6 +173,30 @@ def test_abs_out_bounds_out():
     np.testing.assert_allclose(got, ab, rtol=1e-14)
 
 
+def test_absorb_and_project_one_hot_weights_per_head():
+    """One-hot weights that differ per head: W_UK[h d_h + i, h d_h + i] = 1
+    puts head h's q_nope in latent slots h d_h .. h d_h + d_h - 1 (zeros
+    elsewhere); W_UV[h d_v + i, h d_v + i] = 1 makes out[b, h, i] =
+    o_lat[b, h, h d_v + i]."""
+    B, H, dh, dr, dc = 2, 3, 2, 2, 8
+    rng = np.random.default_rng(5)
+    qn = rng.standard_normal((B, H, dh))
+    qp = rng.standard_normal((B, H, dr))
+    w = np.zeros((dc, H * dh))
+    for h in range(H):
+        for i in range(dh):
+            w[h * dh + i, h * dh + i] = 1.0
+    q_lat = oracle.mla_absorb_q(qn, qp, w, in_dtype=oracle.FP64, w_dtype=oracle.FP64)
+    for h in range(H):
+        expect = np.zeros((B, dc))
+        expect[:, h * dh:(h + 1) * dh] = qn[:, h]
+        assert (q_lat[:, h, :dc] == expect).all() and (q_lat[:, h, dc:] == qp[:, h]).all()
+    o_lat = rng.standard_normal((B, H, dc))
+    out = oracle.mla_project_out(o_lat, w, in_dtype=oracle.FP64, w_dtype=oracle.FP64)
+    for h in range(H):
+        assert (out[:, h] == o_lat[:, h, h * dh:(h + 1) * dh]).all()
+
+
 def test_absorb_and_project_identity_weights():
     """W_UK_h = [I_dh ; 0] puts q_nope in the first d_h latent slots; W_UV_h
     = [I_dv ; 0] reads the first d_v latent slots back."""

@@ -6,7 +6,8 @@ scale in the cache write, the MLA assembly, decode attention or the MLA
 chain, a dropped term, an off-by-one in the causal position.  It then runs
 every pin in tests/test_oracle_*.py against that copy
 (tests/oracle_pin_battery.py, in a child process) and requires at least one
-pin to fail.  The unmodified copy must pass every pin.  The mistakes keep
+pins to fail (two, so that no mistake rests on a single pin).  The
+unmodified copy must pass every pin.  The mistakes keep
 every access in bounds, so a failing pin, not a crash, is what catches them.
 """
 import json
@@ -125,4 +126,5 @@ def test_unmodified_oracle_passes_every_pin(results):
 @pytest.mark.parametrize("mid", [m[0] for m in MUTATIONS])
 def test_planted_mistake_is_caught(results, mid):
     r = results[mid]
-    assert r["failed"], f"no pin fails with the mistake {mid!r} planted in the oracle"
+    # every planted mistake fails at least two independent pins
+    assert len(r["failed"]) >= 2, (mid, r["failed"])

@@ -5,10 +5,10 @@ rule or sign in a number format, a wrong index, stride, head mapping or
 scale in the cache write, the MLA assembly, decode attention or the MLA
 chain, a dropped term, an off-by-one in the causal position.  It then runs
 every pin in tests/test_oracle_*.py against that copy
-(tests/oracle_pin_battery.py, in a child process) and requires at least one
-pins to fail (two, so that no mistake rests on a single pin).  The
-unmodified copy must pass every pin.  The mistakes keep
-every access in bounds, so a failing pin, not a crash, is what catches them.
+(tests/oracle_pin_battery.py, in a child process) and requires at least two
+pins to fail, so that no mistake rests on a single pin.  The unmodified
+copy must pass every pin.  The mistakes keep every access in bounds, so a
+failing pin, not a crash, is what catches them.
 """
 import json
 import os

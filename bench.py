@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -520,6 +521,27 @@ def _oracle_decode_sample(w, rows, max_tokens=None):
     return dt, nbytes
 
 
+def host_cpu():
+    """The host's CPU model (from /proc/cpuinfo; Arm cores report an
+    implementer and part number instead of a name) and its core count."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key:
+                    model = line.split(":", 1)[1].strip()
+                    break
+            if model:
+                if key == "CPU part":
+                    model = f"{platform.machine()} CPU part {model}"
+                break
+    except OSError:
+        pass
+    return {"cpu_model": model or platform.machine(), "nproc": os.cpu_count()}
+
+
 def cpu_baseline(w, budget_s=15.0):
     """The oracle (single-threaded C, double precision) on sequence 0's
     query heads, as many KV-head groups as fit in about budget_s."""
@@ -534,7 +556,7 @@ def cpu_baseline(w, budget_s=15.0):
         if spent > budget_s:
             break
     return {"value": round(nbytes / spent / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
+            "kind": "oracle", **host_cpu(),
             "sample": f"sequence 0 (context {int(w.context_lens[0])}), {len(rows)} query heads "
                       f"({len(rows) // G} KV heads), {spent:.1f} s"}
 
@@ -576,7 +598,7 @@ def run_reference(args):
                        "num_kv_heads": w.num_kv_heads, "head_size": w.head_size,
                        "block_size": w.block_size},
             "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle",
+                             "kind": "oracle", **host_cpu(),
                              "sample": f"per step: one KV-head group ({G} query heads) of one "
                                        f"sequence over its first {tokens} tokens"},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -296,3 +296,17 @@ def test_static_decode_rejects(lib):
 def test_selftest_rejects(lib):
     assert lib.pa_selftest_bounded_wait(None, None) == pa.PA_ERR_INVALID
     assert lib.pa_selftest_bounded_wait(P(0x100002), None) == pa.PA_ERR_INVALID
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: without the built CUDA library every call raises."""
+    monkeypatch.setattr(pa, "_lib", None)
+    monkeypatch.setattr(pa, "LIB_PATH", str(tmp_path / "libpa.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        pa.library()
+    import torch
+    with pytest.raises(RuntimeError, match="missing"):
+        x = torch.zeros(4, 1, 8, dtype=torch.bfloat16)
+        pa.pa_reshape_and_cache(x, x, torch.zeros(1, 4, 1, 8, dtype=torch.bfloat16),
+                                torch.zeros(1, 4, 1, 8, dtype=torch.bfloat16),
+                                torch.arange(4, dtype=torch.int64))

@@ -153,9 +153,9 @@ def up(a, dtype, dev):
 
 
 def traffic_record(kernel_file, workload, step, kv_dtype):
-    """Per-launch DRAM bytes from the committed ncu record, if it was taken
-    on the current source of the kernel and the same workload and step
-    (else None)."""
+    """Per-launch DRAM bytes from the committed ncu records, if one was taken
+    on the current source of the kernel and the same workload, step and KV
+    format (else None)."""
     rec = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(rec):
         return None
@@ -167,19 +167,119 @@ def traffic_record(kernel_file, workload, step, kv_dtype):
         with open(path, "rb") as f:
             hs.update(f.read())
     h = hs.hexdigest()[:16]
-    if (d.get("source_sha256_16") != h or d.get("workload") != workload or d.get("step") != step
-            or d.get("kv_dtype") != kv_dtype):
-        return None
-    return d.get("dram_bytes_per_decode_call")
+    for r in d.get("records", [d]):
+        if (r.get("source_sha256_16") == h and r.get("workload") == workload
+                and r.get("step") == step and r.get("kv_dtype") == kv_dtype):
+            return r.get("dram_bytes_per_decode_call")
+    return None
 
 
 # ------------------------------------------------------------ our arm ----
+class DecodeStep:
+    """One variant of the decode step (block size, KV format, one launch or
+    two) on the long-context workload, resident on the device."""
+
+    def __init__(self, seed, block_size, kv_dtype, step, num_seqs, dev):
+        import torch
+
+        from paged_kv_cache_309_gb300 import pa
+        from paged_kv_cache_309_gb300 import workloads as wl
+        w = wl.long_context_decode(seed=seed, block_size=block_size, num_seqs=num_seqs)
+        self.fp8 = kv_dtype == "e4m3"
+        self.kv_dtype, self.step_kind = kv_dtype, step
+        self.ksd = self.vsd = None
+        if self.fp8:  # same sequences, an e4m3 cache with k_scale = v_scale = 0.05
+            w = wl.as_fp8_history(w, seed=seed + 100)
+            self.ksd = torch.tensor([0.05], dtype=torch.float32, device=dev)
+            self.vsd = torch.tensor([0.05], dtype=torch.float32, device=dev)
+        self.w = w
+        B, HQ, HKV, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
+        cache_t = torch.float8_e4m3fn if self.fp8 else torch.bfloat16
+        self.kc, self.vc = up(w.k_cache, cache_t, dev), up(w.v_cache, cache_t, dev)
+        self.q = up(w.q, torch.bfloat16, dev)
+        self.nk, self.nv = up(w.new_k, torch.bfloat16, dev), up(w.new_v, torch.bfloat16, dev)
+        self.sl = torch.from_numpy(w.slot_mapping).to(dev)
+        self.bt = torch.from_numpy(w.block_tables).to(dev)
+        self.cl = torch.from_numpy(w.context_lens).to(dev)
+        self.out = torch.empty_like(self.q)
+        self.mcl = w.max_context_len
+        self.wsp = pa.decode_workspace(B, HQ, HKV, d, self.mcl, dev)
+        self.splits, self.tps = pa.pa_paged_decode_plan(B, HKV, self.mcl)
+        elt = 1 if self.fp8 else 2
+        self.attn_bytes = wl.kv_bytes_read(w, elt=elt)  # algorithmic, decode attention
+        self.write_bytes = B * HKV * d * 2 * (2 + elt) + B * 8  # new K/V read + written, slots
+        self.step_bytes = self.attn_bytes + self.write_bytes
+        self.fused = step == "fused"
+        self.dev = dev
+
+    def attention(self, q=None, nk=None, nv=None, sl=None, bt=None, cl=None):
+        """The timed launch: the fused step, or the attention of the two-call step."""
+        from paged_kv_cache_309_gb300 import pa
+        q, bt, cl = (self.q if q is None else q, self.bt if bt is None else bt,
+                     self.cl if cl is None else cl)
+        if self.fused:
+            pa.pa_paged_decode_step(self.out, q, self.nk if nk is None else nk,
+                                    self.nv if nv is None else nv, self.sl if sl is None else sl,
+                                    self.kc, self.vc, bt, cl, self.w.scale, self.mcl, self.wsp,
+                                    k_scale=self.ksd, v_scale=self.vsd)
+        else:
+            pa.pa_paged_decode_attention(self.out, q, self.kc, self.vc, bt, cl, self.w.scale,
+                                         self.mcl, self.wsp, k_scale=self.ksd, v_scale=self.vsd)
+
+    def write(self, nk=None, nv=None, sl=None):
+        """The cache write of the two-call step (nothing for the fused step)."""
+        from paged_kv_cache_309_gb300 import pa
+        if not self.fused:
+            pa.pa_reshape_and_cache(self.nk if nk is None else nk, self.nv if nv is None else nv,
+                                    self.kc, self.vc, self.sl if sl is None else sl, None,
+                                    self.ksd, self.vsd)
+
+    def timed(self, K, warmup, clock_device, barrier=None):
+        """W untimed steps, then exactly K steps between a barrier and a
+        synchronize on both sides; CUDA events on the launching stream around
+        the whole region and around each timed attention launch; nvidia-smi
+        samples the clocks meanwhile.  Returns (ms over the K steps, mean ms
+        per attention launch, clock summary)."""
+        import torch
+        stream = torch.cuda.current_stream()
+        for _ in range(warmup):
+            self.write()
+            self.attention()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if barrier:
+            barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(clock_device) as clk:
+            start.record(stream)
+            for i in range(K):
+                self.write()
+                ev[i][0].record(stream)
+                self.attention()
+                ev[i][1].record(stream)
+            stop.record(stream)
+            torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        return (start.elapsed_time(stop), statistics.mean(a.elapsed_time(b) for a, b in ev),
+                clk.summary())
+
+    def kernel_bytes(self):
+        """Algorithmic bytes of the timed launch."""
+        return self.step_bytes if self.fused else self.attn_bytes
+
+    def traffic(self):
+        return traffic_record(os.path.join(ROOT, "paged_kv_cache_309_gb300", "csrc", "decode.cu"),
+                              self.w.name, self.step_kind, self.kv_dtype)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     from paged_kv_cache_309_gb300 import pa
-    from paged_kv_cache_309_gb300 import workloads as wl
 
     ws_n, rank, local = dist_env()
     if ws_n > 1:
@@ -189,96 +289,35 @@ def run_ours(args):
     pa.library()  # fails loudly if the CUDA library is missing
 
     # ---------------- workload (rank r uses seed 4 + 1000 r: weak scaling)
-    w = wl.long_context_decode(seed=rank_seed(rank), block_size=args.block_size,
-                               num_seqs=args.num_seqs)
-    fp8 = args.kv_dtype == "e4m3"
-    ksd = vsd = None
-    if fp8:  # same sequences, an e4m3 cache with k_scale = v_scale = 0.05
-        w = wl.as_fp8_history(w, seed=rank_seed(rank) + 100)
-        ksd = torch.tensor([0.05], dtype=torch.float32, device=dev)
-        vsd = torch.tensor([0.05], dtype=torch.float32, device=dev)
+    st = DecodeStep(rank_seed(rank), args.block_size, args.kv_dtype, args.step, args.num_seqs,
+                    dev)
+    w, fused, fp8 = st.w, st.fused, st.fp8
     B, HQ, HKV, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_size
-    cache_t = torch.float8_e4m3fn if fp8 else torch.bfloat16
-    kc, vc = up(w.k_cache, cache_t, dev), up(w.v_cache, cache_t, dev)
-    q = up(w.q, torch.bfloat16, dev)
-    nk, nv = up(w.new_k, torch.bfloat16, dev), up(w.new_v, torch.bfloat16, dev)
-    sl = torch.from_numpy(w.slot_mapping).to(dev)
-    bt = torch.from_numpy(w.block_tables).to(dev)
-    cl = torch.from_numpy(w.context_lens).to(dev)
-    out = torch.empty_like(q)
-    mcl = w.max_context_len
-    wsp = pa.decode_workspace(B, HQ, HKV, d, mcl, dev)
-    splits, tps = pa.pa_paged_decode_plan(B, HKV, mcl)
     stream = torch.cuda.current_stream()
-
-    elt = 1 if fp8 else 2
-    attn_bytes = wl.kv_bytes_read(w, elt=elt)                 # algorithmic, decode attention
-    write_bytes = B * HKV * d * 2 * (2 + elt) + B * 8        # new K/V read + written, slots
-    step_bytes = attn_bytes + write_bytes
-
-    fused = args.step == "fused"
-
-    def step():
-        if fused:
-            pa.pa_paged_decode_step(out, q, nk, nv, sl, kc, vc, bt, cl, w.scale, mcl, wsp,
-                                    k_scale=ksd, v_scale=vsd)
-            return
-        pa.pa_reshape_and_cache(nk, nv, kc, vc, sl, None, ksd, vsd)
-        pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp, k_scale=ksd,
-                                     v_scale=vsd)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
 
     # ---------------- timed region: exactly K steps
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if ws_n > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        start.record(stream)
-        for i in range(K):
-            if fused:
-                ev[i][0].record(stream)
-                pa.pa_paged_decode_step(out, q, nk, nv, sl, kc, vc, bt, cl, w.scale, mcl, wsp,
-                                        k_scale=ksd, v_scale=vsd)
-            else:
-                pa.pa_reshape_and_cache(nk, nv, kc, vc, sl, None, ksd, vsd)
-                ev[i][0].record(stream)
-                pa.pa_paged_decode_attention(out, q, kc, vc, bt, cl, w.scale, mcl, wsp,
-                                             k_scale=ksd, v_scale=vsd)
-            ev[i][1].record(stream)
-        stop.record(stream)
-        torch.cuda.synchronize()
-    if ws_n > 1:
-        dist.barrier()
-    ms_total = start.elapsed_time(stop)
-    attn_ms = [a.elapsed_time(b) for a, b in ev]
+    barrier = dist.barrier if ws_n > 1 else None
+    ms_total, attn_ms_avg, clocks = st.timed(K, args.warmup, local, barrier)
     ms_total = reduce_over_ranks(ms_total, "max", dev)
-    job_bytes = reduce_over_ranks(step_bytes, "sum", dev)   # every rank's own workload
+    job_bytes = reduce_over_ranks(st.step_bytes, "sum", dev)   # every rank's own workload
     job_seqs = reduce_over_ranks(B, "sum", dev)
-    assert pa.read_device_error(wsp) == 0, "device error word set"
+    assert pa.read_device_error(st.wsp) == 0, "device error word set"
     ms_step = ms_total / K
     value = job_bytes / (ms_step * 1e-3) / 1e9
-    attn_ms_avg = statistics.mean(attn_ms)
     peak, peak_kind = hbm_peak()
-    kernel_bytes = step_bytes if fused else attn_bytes  # what the timed launch moves
+    kernel_bytes = st.kernel_bytes()
     achieved = kernel_bytes / (attn_ms_avg * 1e-3) / 1e9
-    traffic = traffic_record(os.path.join(ROOT, "paged_kv_cache_309_gb300", "csrc", "decode.cu"),
-                             w.name, args.step, args.kv_dtype)
 
-    # ---------------- end to end through the C ABI with pinned host buffers
+    # ---------------- end to end through the C ABI with pinned host buffers:
+    # every step copies its inputs in and its output back, over the same K
     hq = torch.from_numpy(w.q.view(np.int16)).pin_memory()
     hk = torch.from_numpy(w.new_k.view(np.int16)).pin_memory()
     hv = torch.from_numpy(w.new_v.view(np.int16)).pin_memory()
     hsl = torch.from_numpy(w.slot_mapping).pin_memory()
     hbt = torch.from_numpy(w.block_tables).pin_memory()
     hcl = torch.from_numpy(w.context_lens).pin_memory()
-    hout = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+    hout = torch.empty(st.out.shape, dtype=torch.int16).pin_memory()
     dq, dk, dv = (torch.empty(t.shape, dtype=torch.int16, device=dev) for t in (hq, hk, hv))
     dsl, dbt, dcl = (torch.empty_like(t, device=dev) for t in (hsl, hbt, hcl))
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hsl, hbt, hcl))
@@ -287,29 +326,27 @@ def run_ours(args):
     def e2e_step():
         for dst, src in ((dq, hq), (dk, hk), (dv, hv), (dsl, hsl), (dbt, hbt), (dcl, hcl)):
             dst.copy_(src, non_blocking=True)
-        if fused:
-            pa.pa_paged_decode_step(out, dq.view(torch.bfloat16), dk.view(torch.bfloat16),
-                                    dv.view(torch.bfloat16), dsl, kc, vc, dbt, dcl, w.scale, mcl,
-                                    wsp, k_scale=ksd, v_scale=vsd)
-        else:
-            pa.pa_reshape_and_cache(dk.view(torch.bfloat16), dv.view(torch.bfloat16), kc, vc,
-                                    dsl, None, ksd, vsd)
-            pa.pa_paged_decode_attention(out, dq.view(torch.bfloat16), kc, vc, dbt, dcl,
-                                         w.scale, mcl, wsp, k_scale=ksd, v_scale=vsd)
-        hout.copy_(out.view(torch.int16), non_blocking=True)
+        bq, bk, bv = (t.view(torch.bfloat16) for t in (dq, dk, dv))
+        st.write(bk, bv, dsl)
+        st.attention(bq, bk, bv, dsl, dbt, dcl)
+        hout.copy_(st.out.view(torch.int16), non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
     torch.cuda.synchronize()
-    Ke = max(1, K // 4)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
     e0.record(stream)
-    for _ in range(Ke):
+    for _ in range(K):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / Ke
-    assert np.array_equal(hout.numpy(), out.view(torch.int16).cpu().numpy())
+    e2e_wall_ms = (time.perf_counter() - t0) * 1e3 / K
+    e2e_ms = reduce_over_ranks(e0.elapsed_time(e1), "max", dev) / K
+    assert np.array_equal(hout.numpy(), st.out.view(torch.int16).cpu().numpy())
 
     result = {
         "metric": "paged decode-attn KV GB/s (% of HBM peak); cache-write tokens/s",
@@ -328,7 +365,7 @@ def run_ours(args):
         "config": {"workload": w.name, "num_seqs": B, "num_q_heads": HQ, "num_kv_heads": HKV,
                    "head_size": d, "block_size": w.block_size, "kv_dtype": args.kv_dtype,
                    "context_tokens": int(w.context_lens.sum()),
-                   "max_context_len": mcl, "splits": splits, "tokens_per_split": tps,
+                   "max_context_len": st.mcl, "splits": st.splits, "tokens_per_split": st.tps,
                    "step": ("paged_decode_step (new-token write + attention, one launch)" if fused
                             else "reshape_and_cache(new tokens) + paged_decode_attention"),
                    "l2": "inputs larger than L2 (KV cache %.2f GB)" % (
@@ -340,23 +377,65 @@ def run_ours(args):
                                                                  if fused else " (in-kernel merge)"),
                      "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "frac": round(achieved / peak, 4), "traffic": st.traffic(),
                      "bytes_per_launch": kernel_bytes, "avg_launch_us": round(attn_ms_avg * 1e3, 2)},
-        "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": {"value": round(job_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "host_wall_ms_per_step": round(e2e_wall_ms, 5),
+                "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (1 if fused else 2) * K,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
+    del st, dq, dk, dv, dsl, dbt, dcl
 
     if rank == 0 and not args.no_extras:
-        result["extras"] = run_extras(args, dev, peak)
+        torch.cuda.empty_cache()
+        result["extras"] = run_step_extras(args, dev, peak, local)
+        result["extras"].update(run_extras(args, dev, peak))
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if ws_n > 1:
         dist.destroy_process_group()
+
+
+def run_step_extras(args, dev, peak, clock_device):
+    """The other variants of the long-context decode step the benchmark's
+    workload names -- block size 64 (bf16 cache) and an fp8 e4m3 cache with
+    k_scale = v_scale = 0.05 (block size 16) -- each timed exactly like the
+    main line (K steps after W warm-up steps, CUDA events, clocks sampled)."""
+    import torch
+
+    from paged_kv_cache_309_gb300 import pa
+    ex = {}
+    for bs, kv in ((64, "bf16"), (16, "e4m3")):
+        if (bs, kv) == (args.block_size, args.kv_dtype):
+            continue
+        st = DecodeStep(rank_seed(0), bs, kv, "fused", args.num_seqs, dev)
+        ms_total, attn_ms, clocks = st.timed(args.steps, args.warmup, clock_device)
+        assert pa.read_device_error(st.wsp) == 0, "device error word set"
+        ms_step = ms_total / args.steps
+        kb = st.kernel_bytes()
+        ach = kb / (attn_ms * 1e-3) / 1e9
+        name = st.w.name + ("_e4m3" if st.fp8 else "")
+        ex[name] = {"step": "paged_decode_step (new-token write + attention, one launch)",
+                    "block_size": bs, "kv_dtype": kv,
+                    "k_scale": 0.05 if st.fp8 else None, "v_scale": 0.05 if st.fp8 else None,
+                    "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": round(ms_step, 5),
+                    "GB_per_s": round(st.step_bytes / (ms_step * 1e-3) / 1e9, 2),
+                    "sequences_per_s": round(st.w.num_seqs / (ms_step * 1e-3), 1),
+                    "context_tokens_per_s": round(int(st.w.context_lens.sum()) /
+                                                  (ms_step * 1e-3), 1),
+                    "roofline": {"kernel": "paged_decode_split_tc_kernel (fused write)",
+                                 "bound": "hbm", "achieved": round(ach, 2), "peak": peak,
+                                 "unit": "GB/s", "frac": round(ach / peak, 4),
+                                 "traffic": st.traffic(), "bytes_per_launch": kb,
+                                 "avg_launch_us": round(attn_ms * 1e3, 2)},
+                    "clocks": clocks}
+        del st
+        torch.cuda.empty_cache()
+    return ex
 
 
 def timed_loop(fn, iters, warm, dev, flush_bytes=2 * L2_BYTES):

@@ -170,6 +170,12 @@ pa_status pa_concat_mla_k(void *k, pa_dtype k_dtype, const void *k_nope, const v
  * shared memory, computes the grouped products on the tensor cores and keeps
  * an fp32 online softmax; the last CTA of each (sequence, kv head) merges
  * the ranges by log-sum-exp.  One launch per call.
+ *
+ * pa_paged_decode_workspace_size returns the bytes the call above needs
+ * (0 for invalid sizes).  It takes num_kv_heads and no block_size: the
+ * split plan counts CTAs per (sequence, kv head) and cuts token ranges in
+ * multiples of 64 tokens whatever the block size, so the partials depend on
+ * num_seqs, num_q_heads, num_kv_heads, head_size and max_context_len only.
  * ---------------------------------------------------------------------- */
 size_t pa_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                       int32_t num_kv_heads, int32_t head_size,
@@ -290,12 +296,16 @@ pa_status pa_paged_prefill_attention(void *out, const void *q, const void *k_cac
  * Arguments are those of pa_paged_decode_attention without the workspace;
  * the caller still passes every input and the output.  error_word: NULL or
  * a device pointer to one 4-byte word that receives the PA_DEVERR_* bits of
- * this call (OR-ed in; the caller clears it); with NULL they are dropped.
+ * this call (OR-ed in; the caller clears it).  With NULL the bits go to the
+ * first word of the library's own scratch, which no call reads or clears:
+ * they are lost, harmlessly.
  * Limits: a problem whose split-K partials need more than 16 MiB (see
  * pa_paged_decode_workspace_size) returns PA_ERR_WORKSPACE and launches
  * nothing.  The first call on a device looks up the scratch's device
- * address (once per device, with that device current); make that first
- * call before any stream capture.  All calls share the one scratch area,
+ * address (once per device, with that device current) and keeps it for the
+ * life of the process; make that first call before any stream capture.  A
+ * device reset (cudaDeviceReset) after the first call is not supported: the
+ * kept address would be stale.  All calls share the one scratch area,
  * and each call overwrites what the last one left there (the split counters
  * in it, which must start at zero, are zero when the library loads and every
  * completed call returns them to zero): calls that may

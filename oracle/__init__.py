@@ -91,6 +91,9 @@ def _load():
     lib.or_mla_decode_row.restype = C_INT
     lib.or_mla_project_out.argtypes = [P, P, C_INT, P, C_INT, I32, I32, I32, I32]
     lib.or_mla_project_out.restype = C_INT
+    lib.or_mla_decode_explicit.argtypes = [P, P, P, P, C_INT, P, C_INT, P, P, C_INT, P, P, I32,
+                                           I32, I32, I32, I32, I32, I32, I32, I32, I64, F32]
+    lib.or_mla_decode_explicit.restype = C_INT
     _lib = lib
     return lib
 
@@ -298,3 +301,28 @@ def mla_project_out(o_lat, w_uv, in_dtype=BF16, w_dtype=BF16):
     _check(_load().or_mla_project_out(_ptr(out), _ptr(_c(o_lat, o_lat.dtype)), in_dtype,
                                       _ptr(_c(w_uv, w_uv.dtype)), w_dtype, B, H, dc, dv))
     return out
+
+
+def mla_decode_explicit_row(q_nope, q_pe, latent_cache, w_uk, w_uv, block_tables, context_lens,
+                            b, h, scale, d_c, q_dtype=BF16, cache_dtype=BF16, w_dtype=BF16):
+    """One (sequence, head) row of MLA decode in the pages' form: rebuild
+    K_j = [c_kv_j W_UK_h | k_pe_j] and V_j = c_kv_j W_UV_h for every context
+    token, then softmax attention of [q_nope | q_pe].  q_nope [B, H, d_h],
+    q_pe [B, H, d_r], latent_cache [num_blocks, bs, (1,) d_c + d_r], w_uk
+    [d_c, H * d_h], w_uv [d_c, H * d_v].  Returns (out[d_v] float64, lse)."""
+    B, H, dh = q_nope.shape
+    dr = q_pe.shape[2]
+    nb, bs = latent_cache.shape[0], latent_cache.shape[1]
+    assert latent_cache.shape[-1] == d_c + dr and latent_cache.size == nb * bs * (d_c + dr)
+    assert w_uk.shape == (d_c, H * dh) and w_uv.shape[0] == d_c and w_uv.shape[1] % H == 0
+    dv = w_uv.shape[1] // H
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    out = np.empty(dv, dtype=np.float64)
+    lse = ctypes.c_double()
+    _check(_load().or_mla_decode_explicit(
+        _ptr(out), ctypes.byref(lse), _ptr(_c(q_nope, q_nope.dtype)), _ptr(_c(q_pe, q_pe.dtype)),
+        q_dtype, _ptr(_c(latent_cache, latent_cache.dtype)), cache_dtype,
+        _ptr(_c(w_uk, w_uk.dtype)), _ptr(_c(w_uv, w_uv.dtype)), w_dtype, _ptr(bt), _ptr(cl), b,
+        h, H, dh, dr, d_c, dv, bs, bt.shape[1], nb, float(scale)))
+    return out, lse.value

@@ -24,8 +24,11 @@
  *     decode reads the cache back along block_tables).  Arithmetic in double;
  *   - MLA decode keeps one latent row per token (PagedAttention-principle
  *     post, MLA section: c_kv = x W_DKV is what is cached; K and V of a head
- *     are c_kv W_UK and c_kv W_UV; the rope part of K rides beside it) and is
- *     written here in the absorbed form, head by head, with plain loops.
+ *     are c_kv W_UK and c_kv W_UV; the rope part of K rides beside it).  It
+ *     is written here twice, head by head, with plain loops: in the pages'
+ *     own form (or_mla_decode_explicit: K and V rebuilt from the latent,
+ *     then plain attention) and in the absorbed form the three library calls
+ *     take (or_mla_absorb_q, or_mla_decode_row, or_mla_project_out).
  *
  * Error returns are negative integers (see the OR_E* codes); nothing here
  * aborts.
@@ -622,5 +625,108 @@ int or_mla_project_out(double *out, const void *o_lat, int in_dtype, const void 
       }
     }
   }
+  return OR_OK;
+}
+
+/* MLA decode of one (sequence b, head h) row in the pages' own form, with
+ * no absorption (PagedAttention-principle post, MLA section): for every
+ * context token j, gathered in logical order along the block table, rebuild
+ *   K_j = [c_kv_j W_UK_h | k_pe_j]          (d_h + d_r)
+ *   V_j =  c_kv_j W_UV_h                     (d_v)
+ * from its cached row [c_kv_j | k_pe_j], then plain softmax attention of
+ *   q = [q_nope[b, h] | q_pe[b, h]]:  s_j = scale q . K_j,
+ *   out = sum_j softmax_j(s) V_j.
+ * W_UK [d_c, H * d_h] and W_UV [d_c, H * d_v] row-major, head h owning
+ * columns h*d_h .. (h+1)*d_h - 1 (resp. d_v).  q_nope [B, H, d_h], q_pe
+ * [B, H, d_r] of q_dtype; latent_cache [num_blocks, block_size, d_c + d_r]
+ * of cache_dtype; weights of w_dtype.  out [d_v]; lse nullable.  A token
+ * whose block id is outside [0, num_blocks) is left out. */
+int or_mla_decode_explicit(double *out, double *lse, const void *q_nope, const void *q_pe,
+                           int q_dtype, const void *latent_cache, int cache_dtype,
+                           const void *w_uk, const void *w_uv, int w_dtype,
+                           const int32_t *block_tables, const int32_t *context_lens, int32_t b,
+                           int32_t h, int32_t num_heads, int32_t d_h, int32_t d_r, int32_t d_c,
+                           int32_t d_v, int32_t block_size, int32_t max_blocks_per_seq,
+                           int64_t num_blocks, float scale) {
+  if (!formats_ready()) return OR_ENOMEM;
+  if (!out || !q_nope || (d_r > 0 && !q_pe) || !latent_cache || !w_uk || !w_uv ||
+      !block_tables || !context_lens)
+    return OR_EINVAL;
+  if (num_heads <= 0 || d_h <= 0 || d_r < 0 || d_c <= 0 || d_v <= 0 || block_size <= 0 ||
+      max_blocks_per_seq < 0 || b < 0 || h < 0 || h >= num_heads)
+    return OR_EINVAL;
+  const int64_t L = context_lens[b];
+  if (L < 0 || L > (int64_t)max_blocks_per_seq * block_size) return OR_EINVAL;
+  const int32_t row = d_c + d_r;
+  const int32_t dk = d_h + d_r;
+
+  double *q = (double *)malloc(sizeof(double) * (size_t)dk);
+  double *K = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)dk);
+  double *V = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)d_v);
+  double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+  double *c = (double *)malloc(sizeof(double) * (size_t)row);
+  /* head h's weight columns, decoded once: wk[i][k] = W_UK[k, h d_h + i],
+   * wv[i][k] = W_UV[k, h d_v + i] */
+  double *wk = (double *)malloc(sizeof(double) * (size_t)d_h * (size_t)d_c);
+  double *wv = (double *)malloc(sizeof(double) * (size_t)d_v * (size_t)d_c);
+  if (!q || !K || !V || !s || !c || !wk || !wv) {
+    free(q); free(K); free(V); free(s); free(c); free(wk); free(wv);
+    return OR_ENOMEM;
+  }
+  for (int32_t k = 0; k < d_c; ++k) {
+    for (int32_t i = 0; i < d_h; ++i)
+      wk[(int64_t)i * d_c + k] =
+          load_elem(w_dtype, w_uk, (int64_t)k * num_heads * d_h + (int64_t)h * d_h + i);
+    for (int32_t i = 0; i < d_v; ++i)
+      wv[(int64_t)i * d_c + k] =
+          load_elem(w_dtype, w_uv, (int64_t)k * num_heads * d_v + (int64_t)h * d_v + i);
+  }
+  for (int32_t i = 0; i < d_h; ++i)
+    q[i] = load_elem(q_dtype, q_nope, ((int64_t)b * num_heads + h) * d_h + i);
+  for (int32_t r = 0; r < d_r; ++r)
+    q[d_h + r] = load_elem(q_dtype, q_pe, ((int64_t)b * num_heads + h) * d_r + r);
+
+  /* rebuild K and V of head h for every context token */
+  int64_t n = 0;
+  for (int64_t j = 0; j < L; ++j) {
+    int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
+    if (blk < 0 || blk >= num_blocks) continue;
+    int64_t base = (blk * block_size + j % block_size) * row;
+    for (int32_t i = 0; i < row; ++i) c[i] = load_elem(cache_dtype, latent_cache, base + i);
+    for (int32_t i = 0; i < d_h; ++i) { /* K_j[i] = sum_k c_kv_j[k] W_UK[k, h d_h + i] */
+      double acc = 0.0;
+      for (int32_t k = 0; k < d_c; ++k) acc += c[k] * wk[(int64_t)i * d_c + k];
+      K[n * dk + i] = acc;
+    }
+    for (int32_t r = 0; r < d_r; ++r) K[n * dk + d_h + r] = c[d_c + r];
+    for (int32_t i = 0; i < d_v; ++i) { /* V_j[i] = sum_k c_kv_j[k] W_UV[k, h d_v + i] */
+      double acc = 0.0;
+      for (int32_t k = 0; k < d_c; ++k) acc += c[k] * wv[(int64_t)i * d_c + k];
+      V[n * d_v + i] = acc;
+    }
+    ++n;
+  }
+
+  for (int32_t i = 0; i < d_v; ++i) out[i] = 0.0;
+  if (n == 0) {
+    if (lse) *lse = -INFINITY;
+  } else {
+    /* plain softmax attention over the rebuilt K and V */
+    double smax = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+      double dot = 0.0;
+      for (int32_t i = 0; i < dk; ++i) dot += q[i] * K[j * dk + i];
+      s[j] = (double)scale * dot;
+      if (s[j] > smax) smax = s[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) l += exp(s[j] - smax);
+    for (int64_t j = 0; j < n; ++j) {
+      double p = exp(s[j] - smax) / l;
+      for (int32_t i = 0; i < d_v; ++i) out[i] += p * V[j * d_v + i];
+    }
+    if (lse) *lse = smax + log(l);
+  }
+  free(q); free(K); free(V); free(s); free(c); free(wk); free(wv);
   return OR_OK;
 }

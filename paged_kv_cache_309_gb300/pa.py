@@ -107,12 +107,63 @@ def _check(status, where):
         raise PAError(status, where)
 
 
+def _on_device(**tensors):
+    """Refuse, before anything is launched, a tensor the kernels cannot use:
+    every tensor passed (None is skipped) must be a CUDA tensor on the
+    current CUDA device, because the library takes its pointers as device
+    addresses of that device (a host or another GPU's pointer would be
+    dereferenced as one)."""
+    cur = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{name} must be a torch tensor")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (it is on {t.device})")
+        if cur is None:
+            cur = torch.cuda.current_device()
+        if t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{cur}")
+
+
+def _word(t, name):
+    """A device word the kernels OR 4-byte error bits into: int32, at least
+    one element, on the current device."""
+    if t is None:
+        return
+    _on_device(**{name: t})
+    if t.dtype != torch.int32 or t.numel() < 1:
+        raise ValueError(f"{name} must be an int32 tensor with at least one element")
+
+
+def _scales(k_scale, v_scale):
+    """k_scale/v_scale: both None, or both one-element float32 device tensors."""
+    if (k_scale is None) != (v_scale is None):
+        raise ValueError("give both k_scale and v_scale, or neither")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is None:
+            continue
+        _on_device(**{name: t})
+        if t.dtype != torch.float32 or t.numel() < 1:
+            raise ValueError(f"{name} must be a float32 tensor with at least one element")
+
+
+def _workspace(t):
+    """A decode workspace: a uint8 device tensor on the current device."""
+    _on_device(workspace=t)
+    if not t.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+
+
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
+    if stream is not None and s.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream belongs to {s.device}, not the current device")
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -128,6 +179,9 @@ def pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
     """key/value [N, H, d] (token stride free), caches [num_blocks, bs, H, d]
     (block stride free), slot_mapping [N] int64, optional swa table int64,
     optional k_scale/v_scale one-element float32 device tensors."""
+    _on_device(key=key, value=value, key_cache=key_cache, value_cache=value_cache,
+               slot_mapping=slot_mapping, swa_slot_mapping=swa_slot_mapping)
+    _scales(k_scale, v_scale)
     lib = _load()
     N, H, d = key.shape
     if key.stride(2) != 1 or key.stride(1) != d:
@@ -160,6 +214,7 @@ def pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
 
 def pa_concat_mla_k(k, k_nope, k_rope, stream=None):
     """k [N, H, nope+rope] <- k_nope [N, H, nope] | k_rope [N, 1, rope]."""
+    _on_device(k=k, k_nope=k_nope, k_rope=k_rope)
     lib = _load()
     N, H, nope = k_nope.shape
     rope = k_rope.shape[2]
@@ -211,6 +266,10 @@ def pa_paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_le
     float8_e4m3fn, contiguous; block_tables [B, max_blocks_per_seq] int32;
     context_lens [B] int32.  With k_scale/v_scale (one-element float32 device
     tensors) the e4m3 cache goes through pa_paged_decode_attention_fp8."""
+    _on_device(out=out, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+               context_lens=context_lens)
+    _workspace(workspace)
+    _scales(k_scale, v_scale)
     lib = _load()
     B, HQ, d = q.shape
     nb, bs, HKV, dc = k_cache.shape
@@ -251,6 +310,9 @@ def pa_paged_decode_attention_static(out, q, k_cache, v_cache, block_tables, con
     allocate device memory).  error_word: None or a one-element int32 device
     tensor that receives the device-side error bits.  Calls sharing the
     scratch must be ordered on one stream."""
+    _on_device(out=out, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+               context_lens=context_lens)
+    _word(error_word, "error_word")
     lib = _load()
     B, HQ, d = q.shape
     nb, bs, HKV, dc = k_cache.shape
@@ -276,6 +338,11 @@ def pa_paged_decode_step(out, q, new_k, new_v, slot_mapping, k_cache, v_cache, b
     written at slot_mapping [B] int64 (bf16 cache, or e4m3 cache with
     k_scale/v_scale), then attention over the cache as in
     pa_paged_decode_attention."""
+    _on_device(out=out, q=q, new_k=new_k, new_v=new_v, slot_mapping=slot_mapping,
+               k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+               context_lens=context_lens)
+    _workspace(workspace)
+    _scales(k_scale, v_scale)
     lib = _load()
     B, HQ, d = q.shape
     nb, bs, HKV, dc = k_cache.shape
@@ -302,6 +369,11 @@ def pa_paged_prefill_attention(out, q, k_cache, v_cache, block_tables, cu_seqlen
     """Causal varlen prefill: q/out [total_new, H_Q, d] bf16, caches
     [num_blocks, bs, H_KV, d] bf16, cu_seqlens_q [B+1] int32, context_lens [B]
     int32 (tokens including the new ones), error_word one int32 on the device."""
+    if error_word is None:
+        raise ValueError("error_word is required")
+    _on_device(out=out, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+               cu_seqlens_q=cu_seqlens_q, context_lens=context_lens)
+    _word(error_word, "error_word")
     lib = _load()
     T, HQ, d = q.shape
     nb, bs, HKV, dc = k_cache.shape
@@ -326,6 +398,9 @@ def pa_selftest_bounded_wait(error_word, stream=None):
     """Diagnostic: one CTA's bounded wait on a barrier nothing completes runs
     out (2 s) and sets PA_DEVERR_WAIT_TIMEOUT (1) in error_word, a one-element
     int32 device tensor the caller cleared."""
+    if error_word is None:
+        raise ValueError("error_word is required")
+    _word(error_word, "error_word")
     st = _load().pa_selftest_bounded_wait(_ptr(error_word), _stream(stream))
     _check(st, "pa_selftest_bounded_wait")
 
@@ -339,6 +414,7 @@ def _need(cond, msg):
 def pa_mla_absorb_q(q_latent, q_nope, q_pe, w_uk, stream=None):
     """q_latent [B, H, d_c + d_r] <- [W_UK_h q_nope[b, h] | q_pe[b, h]];
     q_nope [B, H, d_h], q_pe [B, H, d_r], w_uk [d_c, H * d_h], all bf16."""
+    _on_device(q_latent=q_latent, q_nope=q_nope, q_pe=q_pe, w_uk=w_uk)
     B, H, dh = q_nope.shape
     dr = q_pe.shape[2]
     dc = w_uk.shape[0]
@@ -365,6 +441,9 @@ def pa_mla_decode_attention(out_latent, q_latent, latent_cache, block_tables, co
     """out_latent [B, H, d_c] bf16; q_latent [B, H, d_c + d_r] bf16;
     latent_cache [num_blocks, bs, (1,) d_c + d_r] bf16; block_tables
     [B, max_blocks_per_seq] int32; context_lens [B] int32."""
+    _on_device(out_latent=out_latent, q_latent=q_latent, latent_cache=latent_cache,
+               block_tables=block_tables, context_lens=context_lens)
+    _workspace(workspace)
     B, H, dk = q_latent.shape
     nb, bs = latent_cache.shape[0], latent_cache.shape[1]
     for t, name in ((out_latent, "out_latent"), (q_latent, "q_latent"),
@@ -391,6 +470,7 @@ def pa_mla_decode_attention(out_latent, q_latent, latent_cache, block_tables, co
 def pa_mla_project_out(out, out_latent, w_uv, stream=None):
     """out [B, H, d_v] <- out_latent[b, h, :] W_UV_h; out_latent [B, H, d_c],
     w_uv [d_c, H * d_v], all bf16."""
+    _on_device(out=out, out_latent=out_latent, w_uv=w_uv)
     B, H, dc = out_latent.shape
     dv = out.shape[2]
     for t in (out, out_latent, w_uv):

@@ -304,9 +304,7 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(pa, "LIB_PATH", str(tmp_path / "libpa.so"))
     with pytest.raises(RuntimeError, match="missing"):
         pa.library()
-    import torch
     with pytest.raises(RuntimeError, match="missing"):
-        x = torch.zeros(4, 1, 8, dtype=torch.bfloat16)
-        pa.pa_reshape_and_cache(x, x, torch.zeros(1, 4, 1, 8, dtype=torch.bfloat16),
-                                torch.zeros(1, 4, 1, 8, dtype=torch.bfloat16),
-                                torch.arange(4, dtype=torch.int64))
+        pa.pa_paged_decode_plan(8, 8, 1000)
+    with pytest.raises(RuntimeError, match="missing"):
+        pa.pa_paged_decode_workspace_size(8, 32, 8, 128, 1000)

@@ -202,9 +202,11 @@ def test_mla_project_out(B):
 
 
 def test_mla_chain_matches_explicit_attention():
-    """absorb -> attention -> project on the GPU against the oracle's chain
-    fed with the GPU's own intermediate codes, and the end result against
-    explicit K/V attention within the stated bar."""
+    """absorb -> attention -> project on the GPU against the pages' own form
+    of MLA decode (the oracle rebuilds each head's K = [c_kv W_UK_h | k_pe]
+    and V = c_kv W_UV_h from the cached latent rows, then runs plain softmax
+    attention) on sampled heads of every sequence, and against the oracle's
+    absorbed chain on every row, both within the stated bar."""
     w = wl.make_mla_decode("chain", 300, 4, 100, 900, 128, with_weights=True)
     need_gpu()
     B, H = w.num_seqs, w.num_heads
@@ -231,3 +233,11 @@ def test_mla_chain_matches_explicit_attention():
     ref = oracle.mla_project_out(ol, w.w_uv, in_dtype=oracle.FP64)
     err_ = np.abs(got - ref)
     assert (err_ <= ATOL + RTOL * np.abs(ref)).all(), err_.max()
+    # the pages' form: K and V rebuilt per head, no absorption
+    for b in range(B):
+        for h in (0, 1, 63, 64, 127):
+            exp_row, _ = oracle.mla_decode_explicit_row(w.q_nope, w.q_pe, w.latent_cache, w.w_uk,
+                                                        w.w_uv, w.block_tables, w.context_lens,
+                                                        b, h, w.scale, 512)
+            e = np.abs(got[b, h] - exp_row)
+            assert (e <= ATOL + RTOL * np.abs(exp_row)).all(), (b, h, e.max())

@@ -213,3 +213,73 @@ def test_absorb_and_project_identity_weights():
     o_lat = rng.standard_normal((B, H, dc))
     out = oracle.mla_project_out(o_lat, eye, in_dtype=oracle.FP64, w_dtype=oracle.FP64)
     assert (out == o_lat[:, :, :dh]).all()
+
+
+# ---- the pages' explicit form (K and V rebuilt from the latent per head) --
+def _explicit(w, b, h):
+    return oracle.mla_decode_explicit_row(w.q_nope, w.q_pe, w.latent_cache, w.w_uk, w.w_uv,
+                                          w.block_tables, w.context_lens, b, h, w.scale,
+                                          w.latent_dim)
+
+
+def _numpy_explicit(w, b, h):
+    """K = [C W_UK_h | k_pe], V = C W_UV_h, softmax attention (numpy)."""
+    dc, H, dh = w.latent_dim, w.num_heads, w.q_nope.shape[2]
+    dv = w.w_uv.shape[1] // H
+    WUK, WUV = bf16_to_f64(w.w_uk), bf16_to_f64(w.w_uv)
+    R = gather_rows(w, b)
+    C, KPE = R[:, :dc], R[:, dc:]
+    k = np.concatenate([C @ WUK[:, h * dh:(h + 1) * dh], KPE], axis=1)
+    v = C @ WUV[:, h * dv:(h + 1) * dv]
+    q = np.concatenate([bf16_to_f64(w.q_nope)[b, h], bf16_to_f64(w.q_pe)[b, h]])
+    s = float(np.float32(w.scale)) * (k @ q)
+    p = np.exp(s - s.max())
+    return (p / p.sum()) @ v, s.max() + math.log(np.exp(s - s.max()).sum())
+
+
+def test_explicit_form_equals_numpy_reconstruction():
+    w = small(seed=21, B=2, H=3, lens=(9, 22))
+    for b in range(w.num_seqs):
+        for h in range(w.num_heads):
+            got, lse = _explicit(w, b, h)
+            ref, rlse = _numpy_explicit(w, b, h)
+            np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-12)
+            assert abs(lse - rlse) <= 1e-11 * max(1.0, abs(rlse))
+
+
+def test_explicit_form_equals_absorbed_chain():
+    w = small(seed=22, B=3, H=4, dh=16, dr=8, dc=32, bs=8, lens=(1, 19, 45))
+    q_lat = oracle.mla_absorb_q(w.q_nope, w.q_pe, w.w_uk)
+    o_lat = np.empty((w.num_seqs, w.num_heads, w.latent_dim))
+    lses = np.empty((w.num_seqs, w.num_heads))
+    for b in range(w.num_seqs):
+        for h in range(w.num_heads):
+            o_lat[b, h], lses[b, h], _ = oracle.mla_decode_row(
+                q_lat, w.latent_cache, w.block_tables, w.context_lens, b, h, w.scale,
+                w.latent_dim, q_dtype=oracle.FP64)
+    chain = oracle.mla_project_out(o_lat, w.w_uv, in_dtype=oracle.FP64)
+    for b in range(w.num_seqs):
+        for h in range(w.num_heads):
+            got, lse = _explicit(w, b, h)
+            np.testing.assert_allclose(got, chain[b, h], rtol=1e-10, atol=1e-12)
+            assert abs(lse - lses[b, h]) <= 1e-10 * max(1.0, abs(lse))
+
+
+def test_explicit_one_token_is_its_projected_latent():
+    # one token: softmax weight 1, so out = c_kv_0 W_UV_h (a plain product)
+    w = small(seed=23, B=2, H=3, lens=(1, 1))
+    dc, H = w.latent_dim, w.num_heads
+    dv = w.w_uv.shape[1] // H
+    WUV = bf16_to_f64(w.w_uv)
+    for b in range(w.num_seqs):
+        c0 = gather_rows(w, b)[0, :dc]
+        for h in range(H):
+            got, _ = _explicit(w, b, h)
+            np.testing.assert_allclose(got, c0 @ WUV[:, h * dv:(h + 1) * dv], rtol=1e-12,
+                                       atol=1e-13)
+
+
+def test_explicit_empty_context_is_zero():
+    w = small(seed=24, B=2, H=2, lens=(0, 5))
+    got, lse = _explicit(w, 0, 1)
+    assert (got == 0).all() and lse == -math.inf

@@ -85,6 +85,16 @@ MUTATIONS = [
      "load_elem(w_dtype, w_uv, (int64_t)c * wcols + i)"),
     ("mla_lse_without_max", "oracle.c", "  if (lse) *lse = smax + log(l);\n  free(qd); free(R);",
      "  if (lse) *lse = log(l);\n  free(qd); free(R);"),
+    # MLA in the pages' explicit form
+    ("explicit_wuv_of_head0", "oracle.c",
+     "load_elem(w_dtype, w_uv, (int64_t)k * num_heads * d_v + (int64_t)h * d_v + i);",
+     "load_elem(w_dtype, w_uv, (int64_t)k * num_heads * d_v + i);"),
+    ("explicit_rope_dropped", "oracle.c",
+     "for (int32_t r = 0; r < d_r; ++r) K[n * dk + d_h + r] = c[d_c + r];",
+     "for (int32_t r = 0; r < d_r; ++r) K[n * dk + d_h + r] = 0.0;"),
+    ("explicit_wuk_head_stride_dropped", "oracle.c",
+     "load_elem(w_dtype, w_uk, (int64_t)k * num_heads * d_h + (int64_t)h * d_h + i);",
+     "load_elem(w_dtype, w_uk, (int64_t)k * num_heads * d_h + (int64_t)h + i);"),
     # causal prefill position
     ("prefill_position_off_by_one", "__init__.py", "p = int(context_lens[b]) - n + j\n",
      "p = int(context_lens[b]) - n + j - 1\n"),

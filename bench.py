@@ -417,7 +417,7 @@ def run_step_extras(args, dev, peak, clock_device):
         ms_step = ms_total / args.steps
         kb = st.kernel_bytes()
         ach = kb / (attn_ms * 1e-3) / 1e9
-        name = st.w.name + ("_e4m3" if st.fp8 else "")
+        name = st.w.name
         ex[name] = {"step": "paged_decode_step (new-token write + attention, one launch)",
                     "block_size": bs, "kv_dtype": kv,
                     "k_scale": 0.05 if st.fp8 else None, "v_scale": 0.05 if st.fp8 else None,
@@ -520,19 +520,18 @@ def run_extras(args, dev, peak):
                    "TFLOP_per_s": round(flops / (med * 1e-3) / 1e12, 2),
                    "frac_of_bf16_dense_peak": round(flops / (med * 1e-3) / 1e12 / bf16_peak(), 4),
                    "median_us": round(med * 1e3, 2), "causal_flops": flops}
-    lat = torch.empty((N, 1, 576), dtype=torch.bfloat16, device=dev)
-    ckv, kpe = up(m.c_kv.reshape(N, 1, 512), torch.bfloat16, dev), up(m.k_pe.reshape(N, 1, 64),
-                                                                      torch.bfloat16, dev)
+    # the latent-cache write: [c_kv | k_pe] per token into [256, 64, 1, 576]
+    # in one pass (pa_concat_and_cache_mla)
+    ckv, kpe = up(m.c_kv, torch.bfloat16, dev), up(m.k_pe, torch.bfloat16, dev)
     cache = torch.zeros((m.num_blocks, m.block_size, 1, 576), dtype=torch.bfloat16, device=dev)
     sl = torch.from_numpy(m.slot_mapping).to(dev)
-
-    def latent():
-        pa.pa_concat_mla_k(lat, ckv, kpe)
-        pa.pa_reshape_and_cache(lat, None, cache, None, sl)
-    med, _ = timed_loop(latent, iters, 3, dev)
-    nbytes = N * (576 * 2 * 2 + 576 * 2 * 2 + 8)  # concat read+write, then write read+write
-    ex["mla_latent_cache_write_16k"] = {"tokens_per_s": round(N / (med * 1e-3), 1),
+    med, _ = timed_loop(lambda: pa.pa_concat_and_cache_mla(ckv, kpe, cache, sl), iters, 3, dev)
+    nbytes = N * (576 * 2 * 2 + 8)  # each row read and written once, plus its slot
+    ex["mla_latent_cache_write_16k"] = {"call": "pa_concat_and_cache_mla (one launch)",
+                                        "tokens_per_s": round(N / (med * 1e-3), 1),
                                         "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 2),
+                                        "frac_of_hbm_peak": round(nbytes / (med * 1e-3) / 1e9 /
+                                                                  peak, 4),
                                         "median_us": round(med * 1e3, 2),
                                         "algorithmic_bytes": nbytes}
     # MLA decode over the latent cache (DeepSeek-V3-shaped: B=64, context
@@ -711,6 +710,38 @@ def run_mla_only(args):
           f"device error word {pa.read_device_error(ws)}")
 
 
+def run_proj_only(args):
+    """MLA projection launches only (for an ncu capture of those kernels):
+    --steps absorb launches, then --steps project launches, at B=64, 128
+    heads; prints back-to-back and L2-flushed times."""
+    import torch
+
+    from paged_kv_cache_309_gb300 import build, pa
+    from paged_kv_cache_309_gb300 import workloads as wl
+    build.build()
+    dev = torch.device("cuda", 0)
+    w = wl.mla_decode(num_heads=128, with_weights=True)
+    qn, qp = up(w.q_nope, torch.bfloat16, dev), up(w.q_pe, torch.bfloat16, dev)
+    wuk, wuv = up(w.w_uk, torch.bfloat16, dev), up(w.w_uv, torch.bfloat16, dev)
+    qlat = torch.empty((w.num_seqs, 128, 576), dtype=torch.bfloat16, device=dev)
+    olat = torch.randn((w.num_seqs, 128, 512), device=dev).to(torch.bfloat16)
+    out = torch.empty((w.num_seqs, 128, 128), dtype=torch.bfloat16, device=dev)
+    for name, fn in (("absorb", lambda: pa.pa_mla_absorb_q(qlat, qn, qp, wuk)),
+                     ("project", lambda: pa.pa_mla_project_out(out, olat, wuv))):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps - 1):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        per = e0.elapsed_time(e1) / max(1, args.steps - 1)
+        med, _ = timed_loop(fn, max(3, args.steps), 2, dev)
+        print(f"{name}: {args.steps} launches, {per * 1e3:.2f} us per launch back to back, "
+              f"{med * 1e3:.2f} us median with L2 flushed")
+
+
 def run_prefill_only(args):
     """Causal prefill launches only (for an ncu capture of that kernel)."""
     import torch
@@ -798,6 +829,9 @@ def main():
     ap.add_argument("--write-only", action="store_true",
                     help="profiling aid: only run --steps cache-write launches of the 32K-token "
                          "prefill write, e4m3 then bf16 cache (no JSON)")
+    ap.add_argument("--mla-proj", action="store_true",
+                    help="profiling aid: only run --steps MLA absorb then project launches "
+                         "(B=64, 128 heads; no JSON)")
     ap.add_argument("--mla-heads", type=int, default=0,
                     help="profiling aid: only run --steps MLA decode attention launches on the "
                          "B=64 context 512..4096 latent workload with this many heads (no JSON)")
@@ -806,6 +840,9 @@ def main():
         args.warmup = 3
     if args.mla_heads:
         run_mla_only(args)
+        return
+    if args.mla_proj:
+        run_proj_only(args)
         return
     if args.prefill_only:
         run_prefill_only(args)

@@ -4,6 +4,7 @@
  * Operations of the decode/prefill hot path of a paged-KV serving engine:
  *   pa_reshape_and_cache           scatter per-token K/V into a paged cache
  *   pa_concat_mla_k                assemble MLA K from k_nope and a shared k_rope
+ *   pa_concat_and_cache_mla        write MLA latent rows [c_kv | k_pe] into a paged cache
  *   pa_paged_decode_attention      GQA decode attention over the paged cache
  *   pa_paged_decode_attention_fp8  the same over an FP8 E4M3 cache with scales
  *   pa_paged_decode_step           new-token cache write + decode attention, one launch
@@ -129,6 +130,40 @@ pa_status pa_concat_mla_k(void *k, pa_dtype k_dtype, const void *k_nope, const v
                           int32_t nope_dim, int32_t rope_dim, int64_t k_stride0,
                           int64_t k_stride1, int64_t nope_stride0, int64_t nope_stride1,
                           int64_t rope_stride0, pa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * pa_concat_and_cache_mla -- the MLA latent-cache write in one pass.
+ *
+ * PagedAttention-principle post, MLA section: what a token caches is its
+ * latent c_kv (d_c elements) with the rope part of its key, k_pe (d_r,
+ * shared by the heads), beside it.  For every token t:
+ *     s = slot_mapping[t];  skip if s < 0 or s >= num_blocks * block_size
+ *     latent_cache[s / block_size, s % block_size, 0:d_c]       = cast(kv_c[t] / scale)
+ *     latent_cache[s / block_size, s % block_size, d_c:d_c+d_r] = cast(k_pe[t] / scale)
+ * (without a scale, a plain cast), i.e. the same bytes as pa_concat_mla_k
+ * with one head (assembling [kv_c | k_pe]) followed by pa_reshape_and_cache
+ * with head_size d_c + d_r and no value cache, but with one read and one
+ * write of each row.  Casts and the scale division as in
+ * pa_reshape_and_cache.
+ *
+ * kv_c [num_tokens, latent_dim], k_pe [num_tokens, rope_dim]: kv_c_stride,
+ *   k_pe_stride elements between tokens, rows contiguous; src_dtype PA_BF16,
+ *   PA_FP16 or PA_FP32.
+ * latent_cache [num_blocks, block_size, latent_dim + rope_dim] of
+ *   cache_dtype (any pa_dtype), block_stride elements between blocks.
+ * slot_mapping [num_tokens] int64.  scale: NULL or a device pointer to one
+ *   float (> 0).
+ * Alignment: pointers 16-byte aligned; latent_dim, rope_dim and the strides
+ *   multiples of 8 elements.
+ * Errors: PA_ERR_INVALID, PA_ERR_UNSUPPORTED (dtype pair), PA_ERR_ALIGN,
+ *   PA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+pa_status pa_concat_and_cache_mla(const void *kv_c, const void *k_pe, pa_dtype src_dtype,
+                                  int64_t num_tokens, int32_t latent_dim, int32_t rope_dim,
+                                  int64_t kv_c_stride, int64_t k_pe_stride, void *latent_cache,
+                                  pa_dtype cache_dtype, int64_t num_blocks, int32_t block_size,
+                                  int64_t block_stride, const int64_t *slot_mapping,
+                                  const float *scale, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Paged GQA decode attention.
@@ -373,8 +408,11 @@ size_t pa_mla_decode_workspace_size(int32_t num_seqs, int32_t num_heads,
  * block block_tables[b][i]); scores over all latent_dim + rope_dim
  * elements, values = the first latent_dim.  Supported: latent_dim 512,
  * rope_dim 64, num_heads a multiple of 16, block_size a power of two in
- * [8, 256].  max_context_len: host upper bound on context_lens (sets the
- * split plan; longer contexts are clipped and flagged in the error word).
+ * [8, 256].  max_context_len: host hint on context_lens (0 or less: a
+ * one-chunk plan); the work is cut into equal token chunks from the actual
+ * context_lens on the device, so no length is clipped to the hint.  A
+ * length beyond max_blocks_per_seq * block_size is clipped to the table and
+ * flagged (PA_DEVERR_CONTEXT_CLIPPED).
  * A block id outside [0, num_blocks) drops its tokens; an empty context
  * gives a zero row.  Numerics: fp32 scores, softmax and accumulation; the
  * softmax weights enter the weighted sum rounded to bf16.  Pointers

@@ -11,6 +11,9 @@
 // side (fully coalesced), up to 4 chunks of K and 4 of V in flight per lane.
 // The slot is resolved by every lane from the same address (a broadcast), so
 // a skipped token exits the whole warp at once: no divergence.
+// The two-source form (kTwoSrc, pa_concat_and_cache_mla) reads the first
+// key_chunks chunks of each row from `key` and the rest from `key2`, which
+// assembles an MLA latent row [c_kv | k_pe] and stores it in the same pass.
 #include <type_traits>
 
 #include "pa_internal.cuh"
@@ -22,24 +25,12 @@ constexpr int kWarps = 8;            // warps per CTA
 constexpr int kChunksPerLane = 4;    // chunks of 8 elements per lane per tensor
 constexpr int kChunksPerWarp = 32 * kChunksPerLane;
 
-template <typename S, typename D, bool kRaw>
-__global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(ReshapeArgs a) {
+// Writes token t's row to slot s (already resolved and in the pool): the
+// lane's chunks c_begin, c_begin + 32, ... of the row's chunk group.
+template <typename S, typename D, bool kRaw, bool kTwoSrc>
+__device__ __forceinline__ void write_row(const ReshapeArgs& a, int64_t t, int64_t s, int grp,
+                                          int lane) {
   using namespace pa;
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  const int64_t t = a.groups == 1 ? wid : wid / a.groups;  // a 64-bit division is long
-  const int grp = static_cast<int>(wid - t * a.groups);
-  if (t >= a.num_tokens) return;
-
-  // slot resolution (same value in every lane)
-  int64_t s = __ldg(a.slot_mapping + t);
-  if (s < 0) return;
-  if (a.swa != nullptr) {
-    if (s >= a.swa_len) return;
-    s = __ldg(a.swa + s);
-    if (s < 0) return;
-  }
-  if (s >= a.num_slots) return;
   const int64_t blk = (a.block_size & (a.block_size - 1)) == 0
                           ? s >> (__ffs(a.block_size) - 1)
                           : s / a.block_size;
@@ -49,6 +40,10 @@ __global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(Resha
 
   const S* ksrc = static_cast<const S*>(a.key) + t * a.key_stride;
   const S* vsrc = static_cast<const S*>(a.value) + t * a.value_stride;
+  // two-source rows: chunk c >= key_chunks comes from key2 (chunk c - key_chunks)
+  const S* k2src = kTwoSrc ? static_cast<const S*>(a.key2) + t * a.key2_stride -
+                                 8 * static_cast<int64_t>(a.key_chunks)
+                           : nullptr;
   D* kdst = static_cast<D*>(a.key_cache) + dst0;
   D* vdst = static_cast<D*>(a.value_cache) + dst0;
   const bool has_v = a.value != nullptr;
@@ -59,7 +54,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(Resha
   for (int i = 0; i < kChunksPerLane; ++i) {
     const int c = c_begin + 32 * i;
     if (c < a.row_chunks) {
-      kv[i] = load8(ksrc + 8 * c);
+      kv[i] = load8((kTwoSrc && c >= a.key_chunks ? k2src : ksrc) + 8 * c);
       if (has_v) vv[i] = load8(vsrc + 8 * c);
     }
   }
@@ -112,21 +107,87 @@ __global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(Resha
   }
 }
 
+// kTPW = 1: one warp per (token, chunk group); every lane resolves the slot
+// from the same address (a broadcast), so a skipped token exits the warp.
+// kTPW = 8 (a second-stage SWA table, rows of one chunk group): lanes 0-7
+// resolve eight tokens' slots and table entries side by side, then the warp
+// writes the rows that survived one after another.  Under a sliding window
+// most tokens fall out of the window; batching their two dependent index
+// loads keeps the grid to one wave instead of paying both loads per token.
+// Warp w takes tokens w, w + NW, w + 2 NW, ... (NW warps in the grid), so a
+// window of consecutive surviving tokens spreads over all warps (about one
+// row each) instead of queueing eight rows on a few warps.
+template <typename S, typename D, bool kRaw, bool kTwoSrc, int kTPW>
+__global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(ReshapeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if constexpr (kTPW == 1) {
+    const int64_t t = a.groups == 1 ? wid : wid / a.groups;  // a 64-bit division is long
+    const int grp = static_cast<int>(wid - t * a.groups);
+    if (t >= a.num_tokens) return;
+    // slot resolution (same value in every lane)
+    int64_t s = __ldg(a.slot_mapping + t);
+    if (s < 0) return;
+    if (a.swa != nullptr) {
+      if (s >= a.swa_len) return;
+      s = __ldg(a.swa + s);
+      if (s < 0) return;
+    }
+    if (s >= a.num_slots) return;
+    write_row<S, D, kRaw, kTwoSrc>(a, t, s, grp, lane);
+  } else {
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+    if (wid >= a.num_tokens) return;
+    int64_t s = -1;
+    const int64_t tl = wid + lane * nw;  // lane j < kTPW resolves token wid + j * NW
+    if (lane < kTPW && tl < a.num_tokens) {
+      s = __ldg(a.slot_mapping + tl);
+      if (s >= 0 && a.swa != nullptr) s = s < a.swa_len ? __ldg(a.swa + s) : -1;
+      if (s >= a.num_slots) s = -1;
+    }
+    uint32_t valid = __ballot_sync(0xffffffffu, s >= 0);
+    while (valid != 0u) {
+      const int j = __ffs(valid) - 1;
+      valid &= valid - 1u;
+      write_row<S, D, kRaw, kTwoSrc>(a, wid + j * nw, __shfl_sync(0xffffffffu, s, j), 0, lane);
+    }
+  }
+}
+
+constexpr int kSwaTokensPerWarp = 8;
+
 template <typename S, typename D>
 pa_status launch_typed(ReshapeArgs a, cudaStream_t stream) {
   a.groups = (a.row_chunks + kChunksPerWarp - 1) / kChunksPerWarp;
-  const int64_t warps = a.num_tokens * a.groups;
+  const bool batched = a.swa != nullptr && a.groups == 1 && a.key2 == nullptr;
+  const int64_t warps = batched ? (a.num_tokens + kSwaTokensPerWarp - 1) / kSwaTokensPerWarp
+                                : a.num_tokens * a.groups;
   const int64_t blocks = (warps + kWarps - 1) / kWarps;
   if (blocks == 0) return PA_OK;
   if (blocks > 0x7FFFFFFFll) return PA_ERR_UNSUPPORTED;
   const bool raw = std::is_same<S, D>::value && a.k_scale == nullptr;
-  if (raw) {
+  const unsigned grid = static_cast<unsigned>(blocks);
+  if (a.key2 != nullptr) {
+    if (raw) {
+      if constexpr (std::is_same<S, D>::value)
+        reshape_and_cache_kernel<S, D, true, true, 1><<<grid, kWarps * 32, 0, stream>>>(a);
+    } else {
+      reshape_and_cache_kernel<S, D, false, true, 1><<<grid, kWarps * 32, 0, stream>>>(a);
+    }
+  } else if (batched) {
+    if (raw) {
+      if constexpr (std::is_same<S, D>::value)
+        reshape_and_cache_kernel<S, D, true, false, kSwaTokensPerWarp>
+            <<<grid, kWarps * 32, 0, stream>>>(a);
+    } else {
+      reshape_and_cache_kernel<S, D, false, false, kSwaTokensPerWarp>
+          <<<grid, kWarps * 32, 0, stream>>>(a);
+    }
+  } else if (raw) {
     if constexpr (std::is_same<S, D>::value)
-      reshape_and_cache_kernel<S, D, true>
-          <<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(a);
+      reshape_and_cache_kernel<S, D, true, false, 1><<<grid, kWarps * 32, 0, stream>>>(a);
   } else {
-    reshape_and_cache_kernel<S, D, false>
-        <<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(a);
+    reshape_and_cache_kernel<S, D, false, false, 1><<<grid, kWarps * 32, 0, stream>>>(a);
   }
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

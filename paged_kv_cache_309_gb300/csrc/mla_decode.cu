@@ -12,10 +12,14 @@
 // table (nano-vLLM walkthrough, section 2.6).  All heads read the same rows.
 //
 // How (sm_103a):
-//  * grid = (head tile, split, sequence); a head tile is 64 heads (16 when
-//    the head count is not a multiple of 64).  Head tiles of one (split,
-//    sequence) are adjacent in the launch order, so the second reads the
-//    latent rows from L2.
+//  * grid = (head tile, chunk); a head tile is 64 heads (16 when the head
+//    count is not a multiple of 64), one wave of resident CTAs per head
+//    tile.  Token-balanced schedule: the sequences' 32-token tiles laid end
+//    to end are cut into one equal chunk per CTA, derived by every CTA from
+//    context_lens; a chunk that crosses sequences runs as pieces (q_lat
+//    reloaded per piece, the pipeline's stage and phase counters running on
+//    across pieces).  Head tiles of one chunk are adjacent in the launch
+//    order, so the second reads the latent rows from L2.
 //  * the split's tokens stream in tiles of 32 through a TMA ring (3 stages
 //    for 64 heads; for 16 heads 2 stages and two CTAs per SM): per (block piece, 64-element chunk) one [rows x
 //    128 B] box, 128-byte swizzled, completion on an mbarrier; a per-tile
@@ -35,9 +39,11 @@
 //    (the running max moves only when a score beats it by more than 2^8),
 //    rounds the weights to bf16 and accumulates O += P . V from the same
 //    shared-memory tile (V = the first 512 elements of each row).
-//  * epilogue as in the GQA decode kernel: one split writes bf16 o_lat;
-//    several write fp32 partials + log2-sum-exp and the CTA that completes
-//    the per-(sequence, head tile) count merges them and zeroes the count.
+//  * epilogue per piece: a piece holding a whole sequence writes bf16 o_lat;
+//    the others write fp32 partials + log2-sum-exp to the chunk's two slots
+//    (its first and its last piece) and count themselves per (sequence,
+//    head tile); the CTA that completes a count merges that sequence after
+//    its own pieces and zeroes the count.
 //
 // Every wait is bounded (2 s).  A timeout sets an error bit in the
 // workspace's error word, drains the copies in flight and leaves.
@@ -81,7 +87,7 @@ struct MlaCfg {
   static constexpr int kStageOff = kQBytes;
   static constexpr int kSOff = kStageOff + kStages * kStageBytes;
   static constexpr int kBarOff = kSOff + 2 * kSBytes;
-  static constexpr int kBytes = kBarOff + (2 * kStages + 1) * 8 + 16;  // full, mask, q, flags
+  static constexpr int kBytes = kBarOff + (2 * kStages + 1) * 8 + 64;  // full, mask, q, schedule
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc * kCtasPerSm <= 227 * 1024, "shared memory");
   static_assert(kSTok == 16 || kSTok == 8, "S split");
@@ -97,6 +103,123 @@ __device__ __forceinline__ void mla_issue_tile(const MlaParams& p, const CUtenso
                     C::kTile, &full[stage], &tile_mask[stage], bt, tok0, tok_end, pol, lane);
 }
 
+// ------------------------------------------------------------- schedule --
+// The work of one head tile is the sequences' kTile-token tiles laid end to
+// end in sequence order (T tiles), cut into NC contiguous chunks of
+// ceil(T / NC) tiles, one per CTA (one wave of CTAs per head tile).  Where
+// a chunk crosses a sequence boundary it splits into pieces.  A piece that
+// covers its whole sequence writes bf16 output; the others write an fp32
+// partial to a slot: 2c for the first piece of chunk c, 2c + 1 for a later
+// one (only a chunk's first and last pieces can be partial), and the CTA
+// that completes a sequence's count merges it once its own work is done.
+// Every CTA derives the schedule from context_lens itself.
+__device__ __forceinline__ int bal_len(const MlaParams& p, int b, bool* clipped) {
+  int L = __ldg(p.context_lens + b);
+  L = L < 0 ? 0 : L;
+  const int64_t cap = static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size;
+  *clipped = static_cast<int64_t>(L) > cap;
+  return *clipped ? static_cast<int>(cap) : L;
+}
+template <int kTile>
+__device__ __forceinline__ int bal_tiles(const MlaParams& p, int b) {
+  bool c;
+  return (bal_len(p, b, &c) + kTile - 1) / kTile;
+}
+struct BalPiece {
+  int b;       // sequence
+  int tb, te;  // tile range [tb, te) of the sequence
+  int pre;     // tiles of the sequences before b
+  int n;       // tiles of the sequence
+  bool first;  // the chunk's first piece
+};
+// Walks a chunk [g, g1) piece by piece.
+template <int kTile>
+struct BalIter {
+  int b, pre, g, g1;
+  bool started;
+  __device__ __forceinline__ bool next(const MlaParams& p, BalPiece& pc) {
+    if (g >= g1) return false;
+    int n = bal_tiles<kTile>(p, b);
+    while (pre + n <= g && b + 1 < p.num_seqs) {  // skips finished and empty sequences
+      pre += n;
+      ++b;
+      n = bal_tiles<kTile>(p, b);
+    }
+    pc.b = b;
+    pc.pre = pre;
+    pc.n = n;
+    pc.tb = g - pre;
+    pc.te = min(n, g1 - pre);
+    pc.first = !started;
+    started = true;
+    g = pre + pc.te;
+    return true;
+  }
+};
+
+// Merge of (sequence b, head tile ht) over its pieces by the whole CTA: the
+// pieces are chunks c_first .. c_last, slot of the first 2 c_first (+1 if it
+// is not that chunk's first piece), of the others 2c.  Per head, piece i
+// gets weight 2^(lse_i - M) / sum_j 2^(lse_j - M); wsm holds HT * np
+// weights.  The partials were written by other CTAs in this launch: read
+// through L2 (__ldcg).
+template <int HT>
+__device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int ht, int pre, int n,
+                                                 int chunk, float* wsm) {
+  const int c_first = pre / chunk, c_last = (pre + n - 1) / chunk;
+  const int np = c_last - c_first + 1;
+  const int s0 = 2 * c_first + (pre != c_first * chunk ? 1 : 0);
+  auto slot = [&](int i) { return i == 0 ? s0 : 2 * (c_first + i); };
+  const int64_t base = static_cast<int64_t>(ht) * p.num_slots;
+  for (int h = threadIdx.x; h < HT; h += blockDim.x) {
+    float M = -INFINITY;
+    for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(p.ws_lse + (base + slot(i)) * HT + h));
+    float W = 0.f;
+    for (int i = 0; i < np; ++i) {
+      const float w = M == -INFINITY ? 0.f : exp2f(__ldcg(p.ws_lse + (base + slot(i)) * HT + h) - M);
+      wsm[h * np + i] = w;
+      W += w;
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    for (int i = 0; i < np; ++i) wsm[h * np + i] *= inv;
+  }
+  __syncthreads();
+  const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + static_cast<int64_t>(ht) * HT;
+  for (int idx = threadIdx.x; idx < HT * (kLat / 4); idx += blockDim.x) {
+    const int h = idx / (kLat / 4), e4 = idx % (kLat / 4);
+    const float* w = wsm + h * np;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int i = 0;
+    for (; i + 4 <= np; i += 4) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        x[u] = __ldcg(reinterpret_cast<const float4*>(
+                          p.ws_o + ((base + slot(i + u)) * HT + h) * kLat) + e4);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float ww = w[i + u];
+        acc.x += ww * x[u].x;
+        acc.y += ww * x[u].y;
+        acc.z += ww * x[u].z;
+        acc.w += ww * x[u].w;
+      }
+    }
+    for (; i < np; ++i) {
+      const float4 x =
+          __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + slot(i)) * HT + h) * kLat) + e4);
+      const float ww = w[i];
+      acc.x += ww * x.x;
+      acc.y += ww * x.y;
+      acc.z += ww * x.z;
+      acc.w += ww * x.w;
+    }
+    *reinterpret_cast<uint2*>(p.out + (bh0 + h) * kLat + 4 * e4) =
+        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
+  __syncthreads();  // wsm is free again
+}
+
 template <int HT>
 __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
     mla_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -109,32 +232,67 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* tile_mask = full + kStages;
   uint64_t* qbar = tile_mask + kStages;
-  int* flags = reinterpret_cast<int*>(qbar + 1);
+  int* sched = reinterpret_cast<int*>(qbar + 1);  // [0..5] schedule, [6] merges, [7..12] their pieces
 
   const int ht = blockIdx.x;
-  const int split = blockIdx.y;
-  const int b = blockIdx.z;
+  const int c = blockIdx.y;    // chunk of the head tile's tile list
+  const int NC = gridDim.y;    // chunks per head tile
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int h0 = ht * HT;
+  const int B = p.num_seqs;
 
-  bool clipped;
-  const int L = mla_effective_len(p, b, &clipped);
-  if (clipped && split == 0 && ht == 0 && threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
-  const int tok_begin = split * p.tokens_per_split;
-  const int tok_end = min(tok_begin + p.tokens_per_split, L);
-  if (tok_begin >= tok_end) {
-    if (split == 0) {  // L == 0: zero rows
-      for (int i = threadIdx.x; i < HT * (kLat / 8); i += kThreads) {
-        const int h = i / (kLat / 8), c = i % (kLat / 8);
-        reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + h0 + h) *
-                                             kLat)[c] = make_uint4(0u, 0u, 0u, 0u);
+  // ---- schedule (warp 0): total tiles, this CTA's chunk, its first sequence
+  if (warp == 0) {
+    int T = 0;
+    bool any_clip = false;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      int n = 0;
+      if (b0 + lane < B) {
+        bool cl;
+        n = (bal_len(p, b0 + lane, &cl) + kTile - 1) / kTile;
+        any_clip |= cl;
+      }
+      T += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n)));
+    }
+    if (__any_sync(0xffffffffu, any_clip) && c == 0 && ht == 0 && lane == 0)
+      atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
+    const int chunk = T > 0 ? (T + NC - 1) / NC : 1;
+    const int g0 = min(T, c * chunk), g1 = min(T, g0 + chunk);
+    int bfirst = 0, prefirst = 0;
+    if (g0 < g1) {
+      int pre = 0;
+      bool found = false;
+      for (int b0 = 0; b0 < B && !found; b0 += 32) {
+        const int n = b0 + lane < B ? bal_tiles<kTile>(p, b0 + lane) : 0;
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        const int excl = incl - n;
+        const uint32_t hit =
+            __ballot_sync(0xffffffffu, n > 0 && pre + excl <= g0 && g0 < pre + incl);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          bfirst = b0 + l;
+          prefirst = pre + __shfl_sync(0xffffffffu, excl, l);
+          found = true;
+        }
+        pre += __shfl_sync(0xffffffffu, incl, 31);
       }
     }
-    return;
+    if (lane == 0) {
+      sched[0] = T;
+      sched[1] = chunk;
+      sched[2] = g0;
+      sched[3] = g1;
+      sched[4] = bfirst;
+      sched[5] = prefirst;
+      sched[6] = 0;  // sequences this CTA merges
+    }
   }
-  const int ntiles = (tok_end - tok_begin + kTile - 1) / kTile;
-
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
@@ -142,42 +300,54 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
     mbar_init_fence();
   }
   __syncthreads();
-  const uint32_t smem_base = smem_u32(smem);
-  const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
-  const uint64_t pol = p.kv_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+  const int chunk = sched[1], g0 = sched[2], g1 = sched[3];
+  const BalIter<kTile> it0{sched[4], sched[5], g0, g1, false};
 
-  // ---- warp 0 issues q_lat and the first kStages tiles
+  // sequences without tokens: zero output rows (chunk c takes b = c mod NC)
+  for (int b = c; b < B; b += NC) {
+    if (bal_tiles<kTile>(p, b) != 0) continue;
+    for (int i = threadIdx.x; i < HT * (kLat / 8); i += kThreads) {
+      const int h = i / (kLat / 8), e = i % (kLat / 8);
+      reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + h0 + h) *
+                                           kLat)[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  if (g0 >= g1) return;
+
+  const uint32_t smem_base = smem_u32(smem);
+  const uint64_t pol = p.kv_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+  const int ntotal = g1 - g0;  // tiles of this chunk
+
+  // ---- the issuing side (warp 0): tile u of the chunk, across pieces
+  BalIter<kTile> iti = it0;
+  BalPiece pci{};
+  int tli = 0, Li = 0;
+  const int32_t* bti = nullptr;
+  auto issue_next = [&](int u) {  // warp 0, all lanes
+    if (tli >= pci.te || bti == nullptr) {
+      iti.next(p, pci);
+      tli = pci.tb;
+      bool cl;
+      Li = bal_len(p, pci.b, &cl);
+      bti = p.block_tables + static_cast<int64_t>(pci.b) * p.max_blocks_per_seq;
+    }
+    mla_issue_tile<HT>(p, &tm_kv, smem, full, tile_mask, bti, tli * kTile, Li, u % kStages, pol,
+                       lane);
+    ++tli;
+  };
   int issued = 0;
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_kv);
-      mbar_arrive_expect_tx(qbar, HT * kRowBytes);
-      const uint64_t qpol = l2_policy_evict_normal();
-#pragma unroll 1
-      for (int c = 0; c < kChunks; ++c)
-        tma_load_2d(smem + c * HT * 128, &tm_q, 64 * c, b * p.num_heads + h0, qbar, qpol);
     }
-    for (; issued < kStages && issued < ntiles; ++issued)
-      mla_issue_tile<HT>(p, &tm_kv, smem, full, tile_mask, bt, tok_begin + issued * kTile,
-                         tok_end, issued, pol, lane);
+    for (; issued < kStages && issued < ntotal; ++issued) issue_next(issued);
   }
 
   const int gq = lane >> 2;  // mma groupID
   const int tq = lane & 3;   // thread in group
   const int mb = warp % C::kMB;  // this warp's 16-head block
   const int wi = warp / C::kMB;  // its index among that block's warps
-  float o[C::kDW / 8][4];
-#pragma unroll
-  for (int nt = 0; nt < C::kDW / 8; ++nt)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) o[nt][c] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-
-  // all warps agree on whether q_lat arrived (they meet at a barrier every
-  // tile, so none may leave alone)
-  bool ok = named_barrier_and(1, kThreads, mbar_wait_bounded(qbar, 0, nullptr));
   // lane-constant parts of the ldmatrix addresses
   const int qrow = 16 * mb + (lane & 15);  // Q: A operand rows
   const int qhalf = lane >> 4;             //    second 8 columns of a k-step
@@ -190,175 +360,192 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
   const int vhalf = lane >> 4;                               //    second 8 elements
   float* s_tile = reinterpret_cast<float*>(smem + C::kSOff);
 
-  int consumed = 0;
-  for (int t = 0; t < ntiles && ok; ++t) {
-    const int stage = t % kStages;
-    const bool w_ok = mbar_wait_bounded(&full[stage], (t / kStages) & 1, nullptr);
-    const uint32_t st_base = smem_base + C::kStageOff + stage * C::kStageBytes;
-    float* S = s_tile + (t & 1) * (C::kKSplit * HT * C::kSStride);
-    uint64_t mask = 0;
-    if (__all_sync(0xffffffffu, w_ok)) {
-      mask = tile_mask[stage];
-      // ---- S = Q . K^T for 16 heads x kSTok tokens over the 576 elements
-      constexpr int NTS = C::kSTok / 8;
-      float sacc[NTS][4], sacc2[1][4];  // sacc2: a second chain for 8-token blocks
+  bool ok = true;
+  int u = 0;       // tiles of this chunk consumed
+  int npiece = 0;  // pieces started (the parity of qbar)
+  BalIter<kTile> itc = it0;
+  BalPiece pc;
+  while (itc.next(p, pc)) {
+    const int b = pc.b;
+    const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + h0;
+    const bool whole = pc.tb == 0 && pc.te == pc.n;
+    const int slot = 2 * c + (pc.first ? 0 : 1);
+    float o[C::kDW / 8][4];
 #pragma unroll
-      for (int nt = 0; nt < NTS; ++nt)
+    for (int nt = 0; nt < C::kDW / 8; ++nt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) sacc[nt][c] = 0.f;
+      for (int cc = 0; cc < 4; ++cc) o[nt][cc] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    if (ok) {
+      // this piece's q_lat rows (every warp is done with the previous ones:
+      // the last tile of a piece ends in a CTA barrier, the epilogue reads
+      // registers only)
+      if (warp == 0 && lane == 0) {
+        mbar_arrive_expect_tx(qbar, HT * kRowBytes);
+        const uint64_t qpol = l2_policy_evict_normal();
+#pragma unroll 1
+        for (int ch = 0; ch < kChunks; ++ch)
+          tma_load_2d(smem + ch * HT * 128, &tm_q, 64 * ch, b * p.num_heads + h0, qbar, qpol);
+      }
+      // all warps agree on whether q_lat arrived (they meet at a barrier
+      // every tile, so none may leave alone)
+      ok = named_barrier_and(1, kThreads, mbar_wait_bounded(qbar, npiece & 1, nullptr));
+    }
+    ++npiece;
+    for (int tl = pc.tb; tl < pc.te && ok; ++tl, ++u) {
+      const int stage = u % kStages;
+      const bool w_ok = mbar_wait_bounded(&full[stage], (u / kStages) & 1, nullptr);
+      const uint32_t st_base = smem_base + C::kStageOff + stage * C::kStageBytes;
+      float* S = s_tile + (u & 1) * (C::kKSplit * HT * C::kSStride);
+      uint64_t mask = 0;
+      if (__all_sync(0xffffffffu, w_ok)) {
+        mask = tile_mask[stage];
+        // ---- S = Q . K^T for 16 heads x kSTok tokens over the 576 elements
+        constexpr int NTS = C::kSTok / 8;
+        float sacc[NTS][4], sacc2[1][4];  // sacc2: a second chain for 8-token blocks
 #pragma unroll
-      for (int c = 0; c < 4; ++c) sacc2[0][c] = 0.f;
-      constexpr int kSteps = kChunks * 4 / C::kKSplit;  // 16-wide k-steps per warp
+        for (int nt = 0; nt < NTS; ++nt)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) sacc[nt][cc] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) sacc2[0][cc] = 0.f;
+        constexpr int kSteps = kChunks * 4 / C::kKSplit;  // 16-wide k-steps per warp
 #pragma unroll 3
-      for (int kc = kh * kSteps; kc < (kh + 1) * kSteps; kc += 2) {
-        const int c = kc >> 2;
-        const int j = kc & 3;  // k-steps j and j + 1 of chunk c
-        const uint32_t qreg = smem_base + c * HT * 128;
-        const uint32_t kreg = st_base + c * C::kChunkBytes;
-        if constexpr (C::kSTok == 16) {
+        for (int kc = kh * kSteps; kc < (kh + 1) * kSteps; kc += 2) {
+          const int ch = kc >> 2;
+          const int j = kc & 3;  // k-steps j and j + 1 of chunk ch
+          const uint32_t qreg = smem_base + ch * HT * 128;
+          const uint32_t kreg = st_base + ch * C::kChunkBytes;
+          if constexpr (C::kSTok == 16) {
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            uint32_t a[4], bb[4];
-            ldsm_x4(swz(qreg, qrow, 2 * (j + h2) + qhalf), a);
-            ldsm_x4(swz(kreg, krow, 2 * (j + h2) + khalf), bb);
-            mma_bf16_16816(sacc[0], a, bb[0], bb[1]);
-            mma_bf16_16816(sacc[NTS - 1], a, bb[2], bb[3]);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t a[4], bb[4];
+              ldsm_x4(swz(qreg, qrow, 2 * (j + h2) + qhalf), a);
+              ldsm_x4(swz(kreg, krow, 2 * (j + h2) + khalf), bb);
+              mma_bf16_16816(sacc[0], a, bb[0], bb[1]);
+              mma_bf16_16816(sacc[NTS - 1], a, bb[2], bb[3]);
+            }
+          } else {
+            uint32_t a0[4], a1[4], bb[4];
+            ldsm_x4(swz(qreg, qrow, 2 * j + qhalf), a0);
+            ldsm_x4(swz(qreg, qrow, 2 * j + 2 + qhalf), a1);
+            ldsm_x4(swz(kreg, krow, 2 * j + khalf), bb);
+            mma_bf16_16816(sacc[0], a0, bb[0], bb[1]);
+            mma_bf16_16816(sacc2[0], a1, bb[2], bb[3]);
           }
-        } else {
-          uint32_t a0[4], a1[4], bb[4];
-          ldsm_x4(swz(qreg, qrow, 2 * j + qhalf), a0);
-          ldsm_x4(swz(qreg, qrow, 2 * j + 2 + qhalf), a1);
-          ldsm_x4(swz(kreg, krow, 2 * j + khalf), bb);
-          mma_bf16_16816(sacc[0], a0, bb[0], bb[1]);
-          mma_bf16_16816(sacc2[0], a1, bb[2], bb[3]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NTS; ++nt) {
+          const int col = tg * C::kSTok + nt * 8 + 2 * tq;
+          float* r0 = S + (kh * HT + 16 * mb + gq) * C::kSStride + col;
+          float* r1 = r0 + 8 * C::kSStride;
+          if constexpr (NTS == 1) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) sacc[nt][cc] += sacc2[0][cc];
+          }
+          *reinterpret_cast<float2*>(r0) = make_float2(sacc[nt][0], sacc[nt][1]);
+          *reinterpret_cast<float2*>(r1) = make_float2(sacc[nt][2], sacc[nt][3]);
+        }
+        // rows of this warp's tokens that hold no token: zero their value
+        // part (0 x NaN would poison P . V); their scores are masked below
+        const uint32_t my_mask = static_cast<uint32_t>(mask >> (tg * C::kSTok)) &
+                                 ((1u << C::kSTok) - 1u);
+        if (my_mask != (1u << C::kSTok) - 1u) {
+          uint8_t* st = smem + C::kStageOff + stage * C::kStageBytes;
+          for (int idx = lane; idx < C::kSTok * 64; idx += 32) {
+            const int rr = idx >> 6, unit = idx & 63;  // 64 units of 16 B = 512 elements
+            if (!((my_mask >> rr) & 1u))
+              *reinterpret_cast<uint4*>(st + (unit >> 3) * C::kChunkBytes +
+                                        (tg * C::kSTok + rr) * 128 + ((unit & 7) << 4)) =
+                  make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();  // generic writes before the stage's next TMA fill
         }
       }
-#pragma unroll
-      for (int nt = 0; nt < NTS; ++nt) {
-        const int col = tg * C::kSTok + nt * 8 + 2 * tq;
-        float* r0 = S + (kh * HT + 16 * mb + gq) * C::kSStride + col;
-        float* r1 = r0 + 8 * C::kSStride;
-        if constexpr (NTS == 1) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) sacc[nt][c] += sacc2[0][c];
+      // every warp's scores (and zeroed rows) are in place, and every warp
+      // is done with tile u - 1: its stage takes tile u - 1 + kStages
+      if (!named_barrier_and(1, kThreads, w_ok)) {
+        ok = false;
+        break;
+      }
+      if (warp == 0 && u >= 1 && issued < ntotal) {
+        issue_next(issued);
+        ++issued;
+      }
+      // ---- softmax over this warp's 16 heads, then O += P . V.  The score
+      // tile is read twice (max, then weights) rather than held in registers.
+      constexpr int KS = kTile / 16;
+      // scaled, masked scores at the A-fragment positions of k-step kk:
+      // rows gq (r = 0) and gq + 8 (r = 1), columns 2tq, 2tq+1, 2tq+8, 2tq+9
+      auto load_scores = [&](int kk, int r, float (&x)[4]) {
+        const float* row = S + (16 * mb + gq + 8 * r) * C::kSStride + 16 * kk + 2 * tq;
+        float2 x0 = *reinterpret_cast<const float2*>(row);
+        float2 x1 = *reinterpret_cast<const float2*>(row + 8);
+        if constexpr (C::kKSplit == 2) {  // the other half of the reduction
+          const float2 y0 = *reinterpret_cast<const float2*>(row + HT * C::kSStride);
+          const float2 y1 = *reinterpret_cast<const float2*>(row + HT * C::kSStride + 8);
+          x0 = make_float2(x0.x + y0.x, x0.y + y0.y);
+          x1 = make_float2(x1.x + y1.x, x1.y + y1.y);
         }
-        *reinterpret_cast<float2*>(r0) = make_float2(sacc[nt][0], sacc[nt][1]);
-        *reinterpret_cast<float2*>(r1) = make_float2(sacc[nt][2], sacc[nt][3]);
-      }
-      // rows of this warp's tokens that hold no token: zero their value
-      // part (0 x NaN would poison P . V); their scores are masked below
-      const uint32_t my_mask = static_cast<uint32_t>(mask >> (tg * C::kSTok)) &
-                               ((1u << C::kSTok) - 1u);
-      if (my_mask != (1u << C::kSTok) - 1u) {
-        uint8_t* st = smem + C::kStageOff + stage * C::kStageBytes;
-        for (int idx = lane; idx < C::kSTok * 64; idx += 32) {
-          const int rr = idx >> 6, unit = idx & 63;  // 64 units of 16 B = 512 elements
-          if (!((my_mask >> rr) & 1u))
-            *reinterpret_cast<uint4*>(st + (unit >> 3) * C::kChunkBytes +
-                                      (tg * C::kSTok + rr) * 128 + ((unit & 7) << 4)) =
-                make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();  // generic writes before the stage's next TMA fill
-      }
-    }
-    // every warp's scores (and zeroed rows) are in place, and every warp is
-    // done with tile t - 1: its stage takes tile t - 1 + kStages
-    if (!named_barrier_and(1, kThreads, w_ok)) {
-      ok = false;
-      break;
-    }
-    consumed = t + 1;
-    if (warp == 0 && t >= 1 && issued < ntiles) {
-      mla_issue_tile<HT>(p, &tm_kv, smem, full, tile_mask, bt, tok_begin + issued * kTile,
-                         tok_end, issued % kStages, pol, lane);
-      ++issued;
-    }
-    // ---- softmax over this warp's 16 heads, then O += P . V.  The score
-    // tile is read twice (max, then weights) rather than held in registers.
-    constexpr int KS = kTile / 16;
-    // scaled, masked scores at the A-fragment positions of k-step kk:
-    // rows gq (r = 0) and gq + 8 (r = 1), columns 2tq, 2tq+1, 2tq+8, 2tq+9
-    auto load_scores = [&](int kk, int r, float (&x)[4]) {
-      const float* row = S + (16 * mb + gq + 8 * r) * C::kSStride + 16 * kk + 2 * tq;
-      float2 x0 = *reinterpret_cast<const float2*>(row);
-      float2 x1 = *reinterpret_cast<const float2*>(row + 8);
-      if constexpr (C::kKSplit == 2) {  // the other half of the reduction
-        const float2 y0 = *reinterpret_cast<const float2*>(row + HT * C::kSStride);
-        const float2 y1 = *reinterpret_cast<const float2*>(row + HT * C::kSStride + 8);
-        x0 = make_float2(x0.x + y0.x, x0.y + y0.y);
-        x1 = make_float2(x1.x + y1.x, x1.y + y1.y);
-      }
-      const uint32_t bits = static_cast<uint32_t>(mask >> (16 * kk + 2 * tq));
-      x[0] = (bits & 1u) ? x0.x * p.scale_log2 : -INFINITY;
-      x[1] = (bits & 2u) ? x0.y * p.scale_log2 : -INFINITY;
-      x[2] = (bits & 0x100u) ? x1.x * p.scale_log2 : -INFINITY;
-      x[3] = (bits & 0x200u) ? x1.y * p.scale_log2 : -INFINITY;
-    };
-    float mx[2] = {-INFINITY, -INFINITY};
+        const uint32_t bits = static_cast<uint32_t>(mask >> (16 * kk + 2 * tq));
+        x[0] = (bits & 1u) ? x0.x * p.scale_log2 : -INFINITY;
+        x[1] = (bits & 2u) ? x0.y * p.scale_log2 : -INFINITY;
+        x[2] = (bits & 0x100u) ? x1.x * p.scale_log2 : -INFINITY;
+        x[3] = (bits & 0x200u) ? x1.y * p.scale_log2 : -INFINITY;
+      };
+      float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk)
+      for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          float x[4];
+          load_scores(kk, r, x);
+          mx[r] = fmaxf(mx[r], fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
+        }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        float x[4];
-        load_scores(kk, r, x);
-        mx[r] = fmaxf(mx[r], fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
-      }
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        if (mx[r] > m_run[r] + kRescaleLog2) {  // new running max (always on the first)
+          const float corr = exp2f(m_run[r] - mx[r]);
+          l_run[r] *= corr;
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      if (mx[r] > m_run[r] + kRescaleLog2) {  // new running max (always on the first)
-        const float corr = exp2f(m_run[r] - mx[r]);
-        l_run[r] *= corr;
-#pragma unroll
-        for (int nt = 0; nt < C::kDW / 8; ++nt) {
-          o[nt][2 * r] *= corr;
-          o[nt][2 * r + 1] *= corr;
-        }
-        m_run[r] = mx[r];
-      }
-    }
-#pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-      float pv[2][4];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        load_scores(kk, r, pv[r]);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          // a masked score is -inf and m_run is finite once a token was seen
-          pv[r][c] = pv[r][c] == -INFINITY ? 0.f : exp2f(pv[r][c] - m_run[r]);
-          l_run[r] += pv[r][c];
+          for (int nt = 0; nt < C::kDW / 8; ++nt) {
+            o[nt][2 * r] *= corr;
+            o[nt][2 * r + 1] *= corr;
+          }
+          m_run[r] = mx[r];
         }
       }
-      const uint32_t a[4] = {pack_bf16x2(pv[0][0], pv[0][1]), pack_bf16x2(pv[1][0], pv[1][1]),
-                             pack_bf16x2(pv[0][2], pv[0][3]), pack_bf16x2(pv[1][2], pv[1][3])};
-      const int vrow = 16 * kk + vrow_l;
 #pragma unroll
-      for (int np = 0; np < C::kDW / 16; ++np) {
-        const int d = wi * C::kDW + 16 * np + 8 * vhalf;  // first element of this lane's unit
-        uint32_t bv[4];
-        ldsm_x4_trans(swz(st_base + (d >> 6) * C::kChunkBytes, vrow, (d & 63) >> 3), bv);
-        mma_bf16_16816(o[2 * np], a, bv[0], bv[1]);
-        mma_bf16_16816(o[2 * np + 1], a, bv[2], bv[3]);
+      for (int kk = 0; kk < KS; ++kk) {
+        float pv[2][4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          load_scores(kk, r, pv[r]);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            // a masked score is -inf and m_run is finite once a token was seen
+            pv[r][cc] = pv[r][cc] == -INFINITY ? 0.f : exp2f(pv[r][cc] - m_run[r]);
+            l_run[r] += pv[r][cc];
+          }
+        }
+        const uint32_t a[4] = {pack_bf16x2(pv[0][0], pv[0][1]), pack_bf16x2(pv[1][0], pv[1][1]),
+                               pack_bf16x2(pv[0][2], pv[0][3]), pack_bf16x2(pv[1][2], pv[1][3])};
+        const int vrow = 16 * kk + vrow_l;
+#pragma unroll
+        for (int np = 0; np < C::kDW / 16; ++np) {
+          const int d = wi * C::kDW + 16 * np + 8 * vhalf;  // first element of this lane's unit
+          uint32_t bv[4];
+          ldsm_x4_trans(swz(st_base + (d >> 6) * C::kChunkBytes, vrow, (d & 63) >> 3), bv);
+          mma_bf16_16816(o[2 * np], a, bv[0], bv[1]);
+          mma_bf16_16816(o[2 * np + 1], a, bv[2], bv[3]);
+        }
       }
     }
-  }
 
-  const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + h0;
-  if (!ok) {
-    // wait (bounded) for the copies still in flight, then leave an empty
-    // partial so that the split count below still completes
-    if (threadIdx.x == 0) {
-      atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
-      mbar_wait_bounded(qbar, 0, nullptr);
-      for (int t = consumed; t < issued; ++t)
-        mbar_wait_bounded(&full[t % kStages], (t / kStages) & 1, nullptr);
-    }
-    if (p.num_splits > 1 && threadIdx.x < HT)
-      p.ws_lse[(bh0 + threadIdx.x) * p.num_splits + split] = -INFINITY;
-  } else {
-    // ---- epilogue: rows 16mb + gq (+8), elements wi*kDW + 8nt + 2tq (+1)
+    // ---- epilogue of the piece: rows 16mb + gq (+8), elements wi*kDW + 8nt + 2tq (+1)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
@@ -366,52 +553,63 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
     }
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const int64_t bh = bh0 + 16 * mb + gq + 8 * r;
-      const float inv = l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
-      if (p.num_splits == 1) {
-        __nv_bfloat16* dst = p.out + bh * kLat + wi * C::kDW + 2 * tq;
+      const int hh = 16 * mb + gq + 8 * r;
+      // after a timeout the piece is empty: weight 0 in the merge, zero row if whole
+      const float inv = ok && l_run[r] > 0.f ? 1.f / l_run[r] : 0.f;
+      if (whole) {
+        __nv_bfloat16* dst = p.out + (bh0 + hh) * kLat + wi * C::kDW + 2 * tq;
 #pragma unroll
         for (int nt = 0; nt < C::kDW / 8; ++nt)
           *reinterpret_cast<uint32_t*>(dst + 8 * nt) =
               pack_bf16x2(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
       } else {
-        const int64_t slot = bh * p.num_splits + split;
-        float* dst = p.ws_o + slot * kLat + wi * C::kDW + 2 * tq;
+        const int64_t srow = (static_cast<int64_t>(ht) * p.num_slots + slot) * HT + hh;
+        float* dst = p.ws_o + srow * kLat + wi * C::kDW + 2 * tq;
 #pragma unroll
         for (int nt = 0; nt < C::kDW / 8; ++nt)
           *reinterpret_cast<float2*>(dst + 8 * nt) =
               make_float2(o[nt][2 * r] * inv, o[nt][2 * r + 1] * inv);
         if (wi == 0 && tq == 0)
-          p.ws_lse[slot] = l_run[r] > 0.f ? m_run[r] + log2f(l_run[r]) : -INFINITY;
+          p.ws_lse[srow] = ok && l_run[r] > 0.f ? m_run[r] + log2f(l_run[r]) : -INFINITY;
+      }
+    }
+    if (!whole) {
+      // count the piece; the CTA that completes the sequence's count merges
+      // it after its own work and returns the counter to zero
+      __syncthreads();  // every partial of this piece is written
+      if (threadIdx.x == 0) {
+        __threadfence();
+        const int c_first = pc.pre / chunk, c_last = (pc.pre + pc.n - 1) / chunk;
+        unsigned* ctr = p.counters + static_cast<int64_t>(b) * (p.num_heads / HT) + ht;
+        const unsigned prev = atomicAdd(ctr, 1u);
+        if (prev + 1u == static_cast<unsigned>(c_last - c_first + 1)) {
+          atomicExch(ctr, 0u);
+          __threadfence();
+          const int k = sched[6]++;
+          sched[7 + 3 * k] = b;
+          sched[8 + 3 * k] = pc.pre;
+          sched[9 + 3 * k] = pc.n;
+        }
       }
     }
   }
-  if (p.num_splits == 1) return;
 
-  // ------------------------------------------------- split count and merge
-  // The CTA that completes the count of its (sequence, head tile) merges
-  // the splits of its HT heads and returns the counter to zero.
-  __syncthreads();  // every partial of this CTA is written
-  const int n_valid = (L + p.tokens_per_split - 1) / p.tokens_per_split;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    unsigned* ctr = p.counters + static_cast<int64_t>(b) * (p.num_heads / HT) + ht;
-    const unsigned prev = atomicAdd(ctr, 1u);
-    const bool last = prev + 1u == static_cast<unsigned>(n_valid);
-    if (last) {
-      atomicExch(ctr, 0u);
-      __threadfence();
+  if (!ok) {
+    // wait (bounded) for the copies still in flight before leaving
+    if (threadIdx.x == 0) {
+      atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+      mbar_wait_bounded(qbar, (npiece - 1) & 1, nullptr);
+      for (int t = u; t < issued; ++t)
+        mbar_wait_bounded(&full[t % kStages], (t / kStages) & 1, nullptr);
     }
-    flags[0] = last ? 1 : 0;
   }
+  // ---- merges this CTA completed (at most its first and last piece); the
+  // pipeline's shared memory is free now and holds the merge weights
   __syncthreads();
-  if (flags[0]) {
-    // the pipeline's shared memory is free now: per-head merge weights
-    if (HT * n_valid * 4 <= C::kStageBytes * kStages)
-      mla_merge_cta(p, bh0, HT, n_valid, reinterpret_cast<float*>(smem + C::kStageOff));
-    else
-      for (int h = warp; h < HT; h += kThreads / 32) mla_merge_warp(p, bh0 + h, n_valid, lane);
-  }
+  const int nmerge = sched[6];
+  for (int k = 0; k < nmerge; ++k)
+    merge_pieces_cta<HT>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k], chunk,
+                         reinterpret_cast<float*>(smem + C::kStageOff));
 }
 
 template <int HT>
@@ -466,48 +664,27 @@ DecodePlan make_mla_plan(int32_t num_seqs, int32_t num_heads, int32_t max_contex
                          int32_t num_sms) {
   if (num_sms <= 0) num_sms = 148;
   const int ht = mla_head_tile(num_heads);
-  const int tile = ht == 128 ? mla_tc_tile() : ht == 64 ? MlaCfg<64>::kTile : MlaCfg<16>::kTile;
-  if (max_context_len <= 0 || num_seqs <= 0 || num_heads <= 0) return {1, tile};
-  const int64_t tiles_max = (static_cast<int64_t>(max_context_len) + tile - 1) / tile;
-  // CTAs per split index (a pair per 128-head tile)
-  const int64_t work = static_cast<int64_t>(num_seqs) * (num_heads / ht) * (ht == 128 ? 2 : 1);
-  const int per_sm = ht == 16 ? MlaCfg<16>::kCtasPerSm : 1;
-  int64_t splits;
-  if (ht == 128) {
-    // tcgen05 kernel: one wave of 2-CTA clusters per 128-head tile, each
-    // taking an equal share of the tiles (the kernel derives the split
-    // from context_lens); num_splits = clusters per head tile
-    const int64_t per_tile = (num_sms / 2) / (num_heads / 128);
-    return {static_cast<int32_t>(per_tile < 1 ? 1 : per_tile), 0};
-  } else {
-    const int64_t target = 4ll * num_sms * per_sm;  // about four waves of resident CTAs
-    splits = (target + work - 1) / work;
-  }
-  if (splits < 1) splits = 1;
-  if (splits > tiles_max) splits = tiles_max;
-  const int64_t tiles_per_split = (tiles_max + splits - 1) / splits;
-  splits = (tiles_max + tiles_per_split - 1) / tiles_per_split;
-  return {static_cast<int32_t>(splits), static_cast<int32_t>(tiles_per_split * tile)};
+  if (max_context_len <= 0 || num_seqs <= 0 || num_heads <= 0) return {1, 0};
+  // One wave per head tile: 2-CTA clusters for the tcgen05 kernel, resident
+  // CTAs for the mma.sync kernel, each taking an equal share of the tile's
+  // token tiles (the kernels derive their chunk from context_lens);
+  // num_splits = chunks (clusters) per head tile
+  const int64_t per_tile = ht == 128 ? (num_sms / 2) / (num_heads / 128)
+                                     : static_cast<int64_t>(ht == 16 ? MlaCfg<16>::kCtasPerSm : 1) *
+                                           num_sms / (num_heads / ht);
+  return {static_cast<int32_t>(per_tile < 1 ? 1 : per_tile), 0};
 }
 
-// mma.sync kernel: [error word | pad] [counters B * H/HT] [lse B*H*splits]
-// [o B*H*splits*512].  tcgen05 kernel: [error word | pad] [counters B * H/128 * 2]
-// [lse H/128 * 2C * 128] [o H/128 * 2C * 128 * 512] with C = plan.num_splits.
+// [error word | pad] [counters B * H/HT (x 2 output halves for HT = 128)]
+// [lse H/HT * 2C * HT] [o H/HT * 2C * HT * 512], C = plan.num_splits chunks
+// (clusters) per head tile, two partial slots each.
 size_t mla_workspace_bytes(int32_t num_seqs, int32_t num_heads, const DecodePlan& plan) {
+  const int ht = mla_head_tile(num_heads);
   size_t bytes = kWorkspaceHeader;
-  if (mla_head_tile(num_heads) == 128) {
-    const size_t rows = static_cast<size_t>(num_heads) * 2 * plan.num_splits;  // slots x heads
-    bytes += align256(static_cast<size_t>(num_seqs) * (num_heads / 128) * 2 * 4);
-    bytes += align256(rows * sizeof(float));
-    bytes += rows * kLat * sizeof(float);
-    return bytes;
-  }
-  if (plan.num_splits > 1) {
-    const size_t rows = static_cast<size_t>(num_seqs) * num_heads * plan.num_splits;
-    bytes += align256(static_cast<size_t>(num_seqs) * (num_heads / mla_head_tile(num_heads)) * 4);
-    bytes += align256(rows * sizeof(float));
-    bytes += rows * kLat * sizeof(float);
-  }
+  const size_t rows = static_cast<size_t>(num_heads) * 2 * plan.num_splits;  // slots x heads
+  bytes += align256(static_cast<size_t>(num_seqs) * (num_heads / ht) * (ht == 128 ? 2 : 1) * 4);
+  bytes += align256(rows * sizeof(float));
+  bytes += rows * kLat * sizeof(float);
   return bytes;
 }
 
@@ -529,8 +706,7 @@ pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
   p.context_lens = a.context_lens;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.err = reinterpret_cast<unsigned*>(ws);
-  const size_t nrows = ht == 128 ? static_cast<size_t>(a.num_heads) * 2 * a.plan.num_splits
-                                  : static_cast<size_t>(a.num_seqs) * a.num_heads * a.plan.num_splits;
+  const size_t nrows = static_cast<size_t>(a.num_heads) * 2 * a.plan.num_splits;
   const size_t ctr_bytes =
       align256(static_cast<size_t>(a.num_seqs) * (a.num_heads / ht) * (ht == 128 ? 2 : 1) * 4);
   p.counters = reinterpret_cast<unsigned*>(ws + kWorkspaceHeader);
@@ -556,7 +732,7 @@ pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
     return launch_mla_tc(mrope, mkv, p, grid, stream);
   }
   const dim3 grid(static_cast<unsigned>(a.num_heads / ht), static_cast<unsigned>(a.plan.num_splits),
-                  static_cast<unsigned>(a.num_seqs));
+                  1u);
   return ht == 64 ? launch_mla_split<64>(mq, mkv, p, grid, stream)
                   : launch_mla_split<16>(mq, mkv, p, grid, stream);
 }

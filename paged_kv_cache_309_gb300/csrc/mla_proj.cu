@@ -6,21 +6,44 @@
 //            q_lat[b, h, d_c + r] = q_pe[b, h, r]
 //   project: out[b, h, i]    = sum_c o_lat[b, h, c] * W_UV[c, h*d_v + i]
 // Both are Y_h = X_h . W_h per head, bf16 in, fp32 accumulate, bf16 out, on
-// the tensor cores (mma.sync m16n8k16).  A CTA owns 64 rows (sequences) of
-// one head and a group of 64-column output chunks; it walks its (column
-// chunk, 64-wide K chunk) steps through a 3-stage cp.async ring of 64 x 64
-// operand tiles (16 bytes of padding per row, so the eight rows of an
-// ldmatrix phase hit eight different bank groups), accumulating a 64 x 64
-// chunk in four warps of 16 rows.  At decode batch sizes the weights are the
-// bytes that matter: every weight element is read once per 64 sequences, and
-// two column groups per head make one wave of CTAs.
+// the tensor cores (mma.sync m16n8k16).  At decode batch sizes the weights
+// are the bytes that matter (16.8 MB per call at 128 heads against ~2 MB of
+// activations), read once per 64 sequences, so the kernels are built to keep
+// the most weight bytes in flight.
+//
+// mla_head_gemm_tma_kernel (K = 128, N a multiple of 128: the absorb
+// product at d_h = 128): a CTA owns 64 rows (sequences) of one head and 128
+// output columns over the whole reduction.  One thread issues every load of
+// the CTA up front -- six 8 KB TMA boxes (64 rows x 128 bytes, 128-byte
+// swizzled), two mbarriers, one per 64-wide half of K -- so all 48 KB are in
+// flight before any math; 512 CTAs at four per SM make one wave at 128
+// heads.  The rope rows of the query are read into registers meanwhile.
+// Four warps of 16 rows multiply each half as it lands (ldmatrix on the
+// swizzled tiles); the bf16 results go through shared memory and leave as
+// full 256-byte rows.  A per-CTA timeline showed the late q_pe copy and
+// narrow 8-byte stores dominating an earlier fp32-staged epilogue.  A version
+// for larger K split the reduction over clusters of CTAs and summed the fp32
+// partials through distributed shared memory; it measured slower than the
+// ring kernel below (16.6 against 12.6 us for the output projection at B =
+// 64, 128 heads), so that shape stays on the ring kernel.
+//
+// mla_head_gemm_kernel (every other shape): a CTA owns 64 rows of one head
+// and a group of 64-column output chunks, walking its (column chunk, 64-wide
+// K chunk) steps through a 3-stage cp.async ring of 64 x 64 operand tiles
+// (16 bytes of padding per row, so the eight rows of an ldmatrix phase hit
+// eight different bank groups).
 // W_UK_h is read with rows = outputs (ldmatrix), W_UV_h with rows = the
 // reduction index (ldmatrix.trans).
+#include <cudaTypedefs.h>
+
 #include <atomic>
 
 #include "pa_internal.cuh"
 
 namespace pa_detail {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // decode.cu
+
 namespace {
 
 using namespace pa;
@@ -167,8 +190,242 @@ __global__ void __launch_bounds__(kThreads) mla_head_gemm_kernel(const ProjParam
   }
 }
 
+// ---------------------------------------------------------- TMA path --
+constexpr int kBM = 64;                   // sequences per CTA
+constexpr int kBN = 128;                  // output columns per CTA
+constexpr int kBK = 128;                  // reduction slice per CTA
+constexpr int kBox = 64 * 64 * 2;         // one TMA box: 64 rows x 128 bytes
+constexpr int kTmaData = 6 * kBox;        // X (2 k halves) + W (2 n halves x 2 k halves)
+constexpr int kTmaSmem = kTmaData + 1024 + 64;  // + alignment slack + barriers
+constexpr int kPeRegs = 4;                // 16-byte units of q_pe held per thread
+
+struct TmaProjParams {
+  __nv_bfloat16* y;            // [M, H, ldy]: columns 0..N-1 written
+  const __nv_bfloat16* extra;  // absorb: q_pe [M, H, extra_dim] copied to y columns N..
+  int32_t M, H, K, N, ldy, extra_dim;
+};
+
+// kTransB = false: W(k, n) = w[n, h*K + k]   (absorb, rows = outputs)
+// kTransB = true:  W(k, n) = w[k, h*N + n]   (project, rows = reduction index)
+// mx: X [M, H, K] as 3-D {K, H, M}, box {64, 1, 64}; mw: w as 2-D, box {64, 64}.
+template <bool kTransB>
+__global__ void __launch_bounds__(kThreads) mla_head_gemm_tma_kernel(
+    const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mw,
+    const TmaProjParams p) {
+  extern __shared__ uint8_t dyn_raw[];
+  // 128-byte swizzled boxes want 1024-byte aligned destinations
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + kTmaData);
+  const int nchunks = p.N / kBN;
+  const int h = blockIdx.y / nchunks, nc = blockIdx.y % nchunks;
+  const int n0 = nc * kBN, k0 = 0, m0 = blockIdx.z * kBM;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+
+  if (tid == 0) {
+    prefetch_tensormap(&mx);
+    prefetch_tensormap(&mw);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // every load of the CTA, issued at once: half kh of the slice is X box
+    // kh and the two W boxes of that half (24 KB on bar[kh])
+    const uint64_t pol_w = l2_policy_evict_first();   // weights: read once
+    const uint64_t pol_x = l2_policy_evict_normal();  // X: shared by the column blocks
+#pragma unroll
+    for (int kh = 0; kh < 2; ++kh) {
+      mbar_arrive_expect_tx(&bar[kh], 3 * kBox);
+      tma_load_3d(base + kh * kBox, &mx, k0 + 64 * kh, h, m0, &bar[kh], pol_x);
+#pragma unroll
+      for (int nh = 0; nh < 2; ++nh) {
+        uint8_t* dst = base + (2 + 2 * nh + kh) * kBox;
+        if constexpr (kTransB)
+          tma_load_2d(dst, &mw, h * p.N + n0 + 64 * nh, k0 + 64 * kh, &bar[kh], pol_w);
+        else
+          tma_load_2d(dst, &mw, h * p.K + k0 + 64 * kh, n0 + 64 * nh, &bar[kh], pol_w);
+      }
+    }
+  }
+
+  // absorb: the rope part of the query rides behind the latent part; its
+  // rows (up to kPeRegs 16-byte units per thread) are read now, while the
+  // tiles are in flight, and stored at the end
+  const bool copy_pe = p.extra != nullptr && nc == 0;
+  const int pe_units = p.extra_dim / 8;
+  const bool pe_in_regs = pe_units * kBM <= kPeRegs * kThreads;
+  uint4 pe[kPeRegs];
+  if (copy_pe && pe_in_regs) {
+#pragma unroll
+    for (int j = 0; j < kPeRegs; ++j) {
+      const int i = tid + kThreads * j;
+      const int r = i / pe_units, u = i - (i / pe_units) * pe_units;
+      pe[j] = (i < kBM * pe_units && m0 + r < p.M)
+                  ? __ldg(reinterpret_cast<const uint4*>(
+                              p.extra + (static_cast<int64_t>(m0 + r) * p.H + h) * p.extra_dim) + u)
+                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  float acc[kBN / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < kBN / 8; ++nt)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[nt][c] = 0.f;
+  bool ok = true;
+#pragma unroll
+  for (int kh = 0; kh < 2; ++kh) {
+    ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(&bar[kh], 0, nullptr));
+    if (!ok) break;
+    const uint32_t xs = smem_u32(base + kh * kBox);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t a[4];
+      const int row = 16 * warp + (lane & 15);
+      const int ua = 2 * kk + (lane >> 4);
+      ldsm_x4(xs + static_cast<uint32_t>(row * 128 + ((ua ^ (row & 7)) << 4)), a);
+#pragma unroll
+      for (int np = 0; np < kBN / 16; ++np) {
+        const uint32_t ws = smem_u32(base + (2 + 2 * (np >> 2) + kh) * kBox);
+        uint32_t bb[4];
+        if constexpr (kTransB) {
+          // rows = k: lanes 0-7 k 0-7, 8-15 k 8-15 (n 0-7), 16-31 the same for n 8-15
+          const int kr = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
+          const int ub = 2 * (np & 3) + (lane >> 4);
+          ldsm_x4_trans(ws + static_cast<uint32_t>(kr * 128 + ((ub ^ (kr & 7)) << 4)), bb);
+        } else {
+          // rows = n: lanes 0-7 n 0-7 k 0-7, 8-15 n 0-7 k 8-15, 16-31 the same for n 8-15
+          const int nr = 16 * (np & 3) + (lane & 7) + 8 * (lane >> 4);
+          const int ub = 2 * kk + ((lane >> 3) & 1);
+          ldsm_x4(ws + static_cast<uint32_t>(nr * 128 + ((ub ^ (nr & 7)) << 4)), bb);
+        }
+        mma_bf16_16816(acc[2 * np], a, bb[0], bb[1]);
+        mma_bf16_16816(acc[2 * np + 1], a, bb[2], bb[3]);
+      }
+    }
+  }
+  if (!ok) {
+    // a load never landed (never expected): wait once more, bounded, for the
+    // copies still in flight into this CTA's shared memory; the CTA's
+    // outputs become NaN
+    if (tid == 0) {
+      mbar_wait_bounded(&bar[0], 0, nullptr);
+      mbar_wait_bounded(&bar[1], 0, nullptr);
+    }
+  }
+  __syncthreads();  // every warp is done with the input tiles
+
+  const float bad = __int_as_float(0x7fc00000);
+  // bf16 rows staged in shared memory (Y[64][128], 16-byte chunk c of row r
+  // at chunk c ^ (r & 7), so a warp's eight rows hit eight bank groups),
+  // then stored as full 256-byte rows
+  uint8_t* Y = base;
+#pragma unroll
+  for (int nt = 0; nt < kBN / 8; ++nt)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int row = 16 * warp + gq + 8 * r;
+      const uint32_t v = ok ? pack_bf16x2(acc[nt][2 * r], acc[nt][2 * r + 1])
+                            : pack_bf16x2(bad, bad);
+      *reinterpret_cast<uint32_t*>(Y + row * 256 + ((nt ^ (row & 7)) << 4) + tq * 4) = v;
+    }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kBM * 16 / kThreads; ++j) {
+    const int idx = tid + kThreads * j;
+    const int row = idx >> 4, c = idx & 15;
+    const int m = m0 + row;
+    if (m < p.M)
+      *reinterpret_cast<uint4*>(p.y + (static_cast<int64_t>(m) * p.H + h) * p.ldy + n0 + 8 * c) =
+          *reinterpret_cast<const uint4*>(Y + row * 256 + ((c ^ (row & 7)) << 4));
+  }
+  if (copy_pe) {
+    if (pe_in_regs) {
+#pragma unroll
+      for (int j = 0; j < kPeRegs; ++j) {
+        const int i = tid + kThreads * j;
+        const int r = i / pe_units, u = i - (i / pe_units) * pe_units;
+        if (i < kBM * pe_units && m0 + r < p.M)
+          *reinterpret_cast<uint4*>(p.y + (static_cast<int64_t>(m0 + r) * p.H + h) * p.ldy + p.N +
+                                    8 * u) = pe[j];
+      }
+    } else {
+      for (int i = tid; i < kBM * pe_units; i += kThreads) {
+        const int r = i / pe_units, u = i % pe_units;
+        if (m0 + r >= p.M) continue;
+        const int64_t row = static_cast<int64_t>(m0 + r) * p.H + h;
+        *reinterpret_cast<uint4*>(p.y + row * p.ldy + p.N + 8 * u) =
+            __ldg(reinterpret_cast<const uint4*>(p.extra + row * p.extra_dim) + u);
+      }
+    }
+  }
+}
+
+// 2-D map over w [rows, cols] bf16, 64 x 64 boxes, 128-byte swizzle.
+bool make_weight_map(CUtensorMap* map, const void* w, int64_t rows, int64_t cols) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64u, 64u};
+  const cuuint32_t es[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over x [M, H, K] bf16 as {K, H, M}, boxes of 64 elements x 1 head x
+// 64 rows (rows past M read as zero), 128-byte swizzle.
+bool make_rows_map(CUtensorMap* map, const void* x, int32_t M, int32_t H, int32_t K) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2,
+                                 static_cast<cuuint64_t>(K) * 2 * static_cast<cuuint64_t>(H)};
+  const cuuint32_t box[3] = {64u, 1u, 64u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The TMA path covers K = 128 (the absorb product at d_h = 128) and N a
+// multiple of 128.
+bool tma_path_fits(const ProjParams& p) { return p.K == kBK && p.N % kBN == 0; }
+
+
+template <bool kTransB>
+pa_status launch_gemm_tma(const ProjParams& q, cudaStream_t stream) {
+  CUtensorMap mx, mw;
+  const bool maps = make_rows_map(&mx, q.x, q.M, q.H, q.K) &&
+                    (kTransB ? make_weight_map(&mw, q.w, q.K, static_cast<int64_t>(q.H) * q.N)
+                             : make_weight_map(&mw, q.w, q.N, static_cast<int64_t>(q.H) * q.K));
+  if (!maps) return PA_ERR_CUDA;
+  TmaProjParams p;
+  p.y = q.y;
+  p.extra = q.extra;
+  p.M = q.M;
+  p.H = q.H;
+  p.K = q.K;
+  p.N = q.N;
+  p.ldy = q.ldy;
+  p.extra_dim = q.extra_dim;
+  static std::atomic<uint64_t> smem_raised{0};
+  auto kern = mla_head_gemm_tma_kernel<kTransB>;
+  if (!ensure_smem_limit(kern, kTmaSmem, smem_raised)) return PA_ERR_CUDA;
+  const dim3 grid(1u, static_cast<unsigned>(q.H * (q.N / kBN)),
+                  static_cast<unsigned>((q.M + kBM - 1) / kBM));
+  kern<<<grid, kThreads, kTmaSmem, stream>>>(mx, mw, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 template <bool kTransB>
 pa_status launch_gemm(ProjParams p, cudaStream_t stream) {
+  if (tma_path_fits(p)) return launch_gemm_tma<kTransB>(p, stream);
   const int chunks = p.N / kTN;
   const int groups = chunks < kGroups ? chunks : kGroups;
   p.chunks_per_group = (chunks + groups - 1) / groups;

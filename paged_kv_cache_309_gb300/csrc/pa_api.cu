@@ -201,6 +201,45 @@ pa_status pa_concat_mla_k(void* k, pa_dtype k_dtype, const void* k_nope, const v
                                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+pa_status pa_concat_and_cache_mla(const void* kv_c, const void* k_pe, pa_dtype src_dtype,
+                                  int64_t num_tokens, int32_t latent_dim, int32_t rope_dim,
+                                  int64_t kv_c_stride, int64_t k_pe_stride, void* latent_cache,
+                                  pa_dtype cache_dtype, int64_t num_blocks, int32_t block_size,
+                                  int64_t block_stride, const int64_t* slot_mapping,
+                                  const float* scale, pa_stream_t stream) {
+  if (num_tokens < 0 || latent_dim <= 0 || rope_dim <= 0 || block_size <= 0 || num_blocks < 0)
+    return PA_ERR_INVALID;
+  if (num_tokens == 0) return PA_OK;  // nothing to write; pointers may be null
+  if (kv_c == nullptr || k_pe == nullptr || latent_cache == nullptr || slot_mapping == nullptr)
+    return PA_ERR_INVALID;
+  if (!is_src_dtype(src_dtype) || !is_any_dtype(cache_dtype)) return PA_ERR_UNSUPPORTED;
+  if (latent_dim % 8 != 0 || rope_dim % 8 != 0) return PA_ERR_ALIGN;
+  const int64_t row = static_cast<int64_t>(latent_dim) + rope_dim;
+  if (row / 8 > 0x7FFFFFFFll) return PA_ERR_UNSUPPORTED;
+  if (kv_c_stride % 8 != 0 || k_pe_stride % 8 != 0 || block_stride % 8 != 0) return PA_ERR_ALIGN;
+  if (num_tokens > 1 && (kv_c_stride < latent_dim || k_pe_stride < rope_dim))
+    return PA_ERR_INVALID;
+  if (num_blocks > 1 && block_stride < row * block_size) return PA_ERR_INVALID;
+  if (!aligned(kv_c, 16) || !aligned(k_pe, 16) || !aligned(latent_cache, 16)) return PA_ERR_ALIGN;
+  pa_detail::ReshapeArgs a{};
+  a.key = kv_c;
+  a.key2 = k_pe;
+  a.key_stride = kv_c_stride;
+  a.key2_stride = k_pe_stride;
+  a.key_chunks = latent_dim / 8;
+  a.key_cache = latent_cache;
+  a.slot_mapping = slot_mapping;
+  a.k_scale = scale;
+  a.v_scale = scale;
+  a.num_tokens = num_tokens;
+  a.block_stride = block_stride;
+  a.num_slots = num_blocks * block_size;
+  a.row_chunks = static_cast<int32_t>(row / 8);
+  a.block_size = block_size;
+  return pa_detail::launch_reshape_and_cache(a, src_dtype, cache_dtype,
+                                             reinterpret_cast<cudaStream_t>(stream));
+}
+
 pa_status pa_paged_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_context_len,
                                int32_t num_sms, int32_t* num_splits_host,
                                int32_t* tokens_per_split_host) {

@@ -553,6 +553,11 @@ struct ReshapeArgs {
   int32_t row_chunks;  // (num_heads * head_size) / 8
   int32_t block_size;
   int32_t groups;      // chunk groups (warps) per token
+  // two-source rows (pa_concat_and_cache_mla): chunks >= key_chunks of a
+  // row come from key2 (null: every chunk from key)
+  const void* key2;
+  int64_t key2_stride;
+  int32_t key_chunks;
 };
 pa_status launch_reshape_and_cache(const ReshapeArgs& a, pa_dtype src, pa_dtype dst,
                                    cudaStream_t stream);

@@ -54,6 +54,9 @@ def _load():
     lib.pa_reshape_and_cache.restype = E
     lib.pa_concat_mla_k.argtypes = [P, E, P, P, E, I64, I32, I32, I32, I64, I64, I64, I64, I64, P]
     lib.pa_concat_mla_k.restype = E
+    lib.pa_concat_and_cache_mla.argtypes = [P, P, E, I64, I32, I32, I64, I64, P, E, I64, I32,
+                                            I64, P, P, P]
+    lib.pa_concat_and_cache_mla.restype = E
     lib.pa_paged_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32]
     lib.pa_paged_decode_workspace_size.restype = SZ
     lib.pa_paged_decode_attention.argtypes = [P, P, P, P, E, P, P, I32, I32, I32, I32, I32, I32,
@@ -229,6 +232,39 @@ def pa_concat_mla_k(k, k_nope, k_rope, stream=None):
                              nope, rope, k.stride(0), k.stride(1), k_nope.stride(0),
                              k_nope.stride(1), k_rope.stride(0), _stream(stream))
     _check(st, "pa_concat_mla_k")
+
+
+def pa_concat_and_cache_mla(kv_c, k_pe, latent_cache, slot_mapping, scale=None, stream=None):
+    """latent_cache [num_blocks, bs, (1,) d_c + d_r] <- [kv_c[t] | k_pe[t]] at
+    slot_mapping[t] (int64 [N]; negative or out-of-pool slots skipped);
+    kv_c [N, d_c] and k_pe [N, d_r] (token stride free, rows contiguous);
+    optional scale: one-element float32 device tensor (x / scale before the
+    cast)."""
+    _on_device(kv_c=kv_c, k_pe=k_pe, latent_cache=latent_cache, slot_mapping=slot_mapping)
+    if scale is not None:
+        _on_device(scale=scale)
+        if scale.dtype != torch.float32 or scale.numel() < 1:
+            raise ValueError("scale must be a float32 tensor with at least one element")
+    lib = _load()
+    kc = kv_c.view(kv_c.shape[0], -1) if kv_c.dim() == 3 else kv_c
+    kp = k_pe.view(k_pe.shape[0], -1) if k_pe.dim() == 3 else k_pe
+    N, dc = kc.shape
+    dr = kp.shape[1]
+    if kp.shape[0] != N or kc.stride(1) != 1 or kp.stride(1) != 1:
+        raise ValueError("kv_c [N, d_c] and k_pe [N, d_r] with contiguous rows expected")
+    if kp.dtype != kc.dtype:
+        raise ValueError("kv_c and k_pe must share a dtype")
+    nb, bs = latent_cache.shape[0], latent_cache.shape[1]
+    if latent_cache.shape[-1] != dc + dr or latent_cache.numel() != nb * bs * (dc + dr) \
+            or not latent_cache.is_contiguous():
+        raise ValueError("latent_cache must be [num_blocks, bs, (1,) d_c + d_r], contiguous")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != N:
+        raise ValueError("slot_mapping must be int64 [N]")
+    st = lib.pa_concat_and_cache_mla(
+        _ptr(kc), _ptr(kp), _dtype(kc), N, dc, dr, kc.stride(0), kp.stride(0),
+        _ptr(latent_cache), _dtype(latent_cache), nb, bs, bs * (dc + dr), _ptr(slot_mapping),
+        _ptr(scale), _stream(stream))
+    _check(st, "pa_concat_and_cache_mla")
 
 
 def pa_paged_decode_plan(num_seqs, num_kv_heads, max_context_len, num_sms=0):

@@ -150,6 +150,27 @@ def test_concat_rejects(lib):
     assert c(n=0) == pa.PA_OK
 
 
+def test_concat_and_cache_mla_rejects(lib):
+    def c(**kw):
+        a = dict(kvc=FAKE, kpe=FAKE, sd=pa.PA_BF16, n=4, dc=512, dr=64, cs=512, ps=64,
+                 cache=FAKE, cd=pa.PA_BF16, nb=4, bs=64, bstride=64 * 576, slot=FAKE, sc=None)
+        a.update(kw)
+        return lib.pa_concat_and_cache_mla(a["kvc"], a["kpe"], a["sd"], a["n"], a["dc"], a["dr"],
+                                           a["cs"], a["ps"], a["cache"], a["cd"], a["nb"],
+                                           a["bs"], a["bstride"], a["slot"], a["sc"], None)
+    assert c(kvc=None) == pa.PA_ERR_INVALID
+    assert c(kpe=None) == pa.PA_ERR_INVALID
+    assert c(slot=None) == pa.PA_ERR_INVALID
+    assert c(dr=0) == pa.PA_ERR_INVALID
+    assert c(sd=pa.PA_FP8_E4M3) == pa.PA_ERR_UNSUPPORTED
+    assert c(dc=500) == pa.PA_ERR_ALIGN
+    assert c(ps=68) == pa.PA_ERR_ALIGN
+    assert c(cs=256) == pa.PA_ERR_INVALID           # token rows of kv_c overlap
+    assert c(bstride=64 * 512) == pa.PA_ERR_INVALID  # blocks overlap
+    assert c(cache=FAKE_MIS) == pa.PA_ERR_ALIGN
+    assert c(n=0) == pa.PA_OK
+
+
 def _mla(lib, **kw):
     a = dict(out=FAKE, q=FAKE, cache=FAKE, bt=FAKE, cl=FAKE, B=4, H=128, dc=512, dr=64, bs=64,
              mbps=8, nb=64, scale=0.072, maxctx=512, ws=FAKE, wsb=1 << 28)
@@ -179,12 +200,17 @@ def test_mla_workspace_size(lib):
     assert lib.pa_mla_decode_workspace_size(4, 24, 512) == 0      # heads not a multiple of 16
     assert lib.pa_mla_decode_workspace_size(4, 128, -1) == 0
     assert lib.pa_mla_decode_workspace_size(0, 128, 512) >= 256
-    # mma.sync kernel: one split for a short context on many sequences: the header alone
-    assert lib.pa_mla_decode_workspace_size(4096, 64, 32) == 256
-    # tcgen05 kernel (heads a multiple of 128): counters + two partial slots per
-    # cluster, independent of the context length
-    a = lib.pa_mla_decode_workspace_size(64, 128, 512)
-    assert a > 256 and a == lib.pa_mla_decode_workspace_size(64, 128, 131072)
+    # both kernels: counters + two partial slots per chunk of the balanced
+    # schedule, independent of the context length
+    for B, H in ((64, 128), (64, 16), (4096, 64), (3, 48)):
+        a = lib.pa_mla_decode_workspace_size(B, H, 512)
+        assert a > 256 and a == lib.pa_mla_decode_workspace_size(B, H, 131072)
+    # the partial slots do not depend on the batch: only the counters grow with B
+    al = lambda x: (x + 255) // 256 * 256
+    for H, per_b in ((16, 4), (64, 4), (128, 8)):
+        d = lib.pa_mla_decode_workspace_size(4096, H, 512) - lib.pa_mla_decode_workspace_size(
+            64, H, 512)
+        assert d == al(4096 * per_b) - al(64 * per_b)
 
 
 def test_mla_projections_reject(lib):

@@ -91,3 +91,71 @@ def test_mla_latent_cache_write_16k():
     s = int(w.slot_mapping[0])
     assert (got[s // 64, s % 64, 0, :512] == w.c_kv[0]).all()
     assert (got[s // 64, s % 64, 0, 512:] == w.k_pe[0]).all()
+
+
+# ------------------------------------------- one-pass latent-cache write --
+def fused_latent_write(ckv, kpe, slots, num_blocks, bs, src, cdt, scale=None, pad=0):
+    """pa_concat_and_cache_mla on the GPU (sources optionally inside wider
+    rows, `pad` extra elements per token) and the oracle's two steps
+    (concat with one head, then the K-only cache write); cache codes of both."""
+    need_gpu()
+    N, dc = ckv.shape
+    dr = kpe.shape[1]
+    big_c = np.zeros((N, dc + pad), dtype=ckv.dtype)
+    big_c[:, :dc] = ckv
+    big_p = np.zeros((N, dr + pad), dtype=kpe.dtype)
+    big_p[:, :dr] = kpe
+    poison = {"bf16": 0x7FC0, "fp16": 0x7E00, "fp32": np.float32("nan"), "e4m3": 0x7F}[cdt]
+    init = np.full((num_blocks, bs, 1, dc + dr), poison, dtype=_NP[cdt])
+    cache = to_dev(init, cdt)
+    sd = None if scale is None else torch.tensor([scale], dtype=torch.float32, device="cuda")
+    pa.pa_concat_and_cache_mla(to_dev(big_c, src)[:, :dc], to_dev(big_p, src)[:, :dr], cache,
+                               torch.from_numpy(np.asarray(slots, np.int64)).cuda(), sd)
+    torch.cuda.synchronize()
+    got = to_host(cache, cdt)
+    lat = np.zeros((N, 1, dc + dr), dtype=_NP[src])
+    oracle.concat_mla_k(lat, _ORC[src], ckv.reshape(N, 1, dc), kpe.reshape(N, 1, dr), _ORC[src])
+    ref = init.copy()
+    oracle.reshape_and_cache(lat, None, _ORC[src], ref, None, _ORC[cdt],
+                             np.asarray(slots, np.int64), k_scale=scale, v_scale=scale)
+    return got, ref
+
+
+def test_concat_and_cache_mla_16k_full():
+    """The latent write of the MLA workload in one pass: bit-exact against
+    the oracle's concat + cache write, every byte of the cache."""
+    w = wl.mla_assembly()
+    got, ref = fused_latent_write(w.c_kv, w.k_pe, w.slot_mapping, w.num_blocks, w.block_size,
+                                  "bf16", "bf16")
+    assert codes_equal(got, ref, "bf16").all()
+    s = int(w.slot_mapping[5])
+    assert (got[s // 64, s % 64, 0, :512] == w.c_kv[5]).all()
+    assert (got[s // 64, s % 64, 0, 512:] == w.k_pe[5]).all()
+
+
+@pytest.mark.parametrize("cdt,scale", [("e4m3", 0.05), ("bf16", 0.3), ("e4m3", None),
+                                       ("fp32", None)])
+def test_concat_and_cache_mla_scaled_casts_and_skips(cdt, scale):
+    w = wl.mla_assembly(num_tokens=300)
+    slots = w.slot_mapping.copy()
+    slots[::7] = -1                                   # padding tokens
+    slots[3] = w.num_blocks * w.block_size + 5        # outside the pool
+    got, ref = fused_latent_write(w.c_kv, w.k_pe, slots, w.num_blocks, w.block_size, "bf16", cdt,
+                                  scale=scale, pad=24)
+    assert codes_equal(got, ref, cdt).all()
+
+
+@pytest.mark.parametrize("N,dc,dr,bs", [(1, 8, 8, 8), (37, 512, 64, 16), (64, 256, 32, 128)])
+def test_concat_and_cache_mla_shapes(N, dc, dr, bs):
+    g = torch.Generator().manual_seed(N + dc)
+    ckv = wl.randn_bf16(g, (N, dc))
+    kpe = wl.randn_bf16(g, (N, dr))
+    nb = (N + bs - 1) // bs + 1
+    slots = wl.randperm(g, nb * bs)[:N].astype(np.int64)
+    got, ref = fused_latent_write(ckv, kpe, slots, nb, bs, "bf16", "bf16")
+    assert codes_equal(got, ref, "bf16").all()
+    rng = np.random.default_rng(N)
+    got, ref = fused_latent_write(rng.standard_normal((N, dc)).astype(np.float32),
+                                  rng.standard_normal((N, dr)).astype(np.float32), slots, nb, bs,
+                                  "fp32", "e4m3", scale=0.25)
+    assert codes_equal(got, ref, "e4m3").all()

@@ -143,12 +143,27 @@ def test_mla_repeat_reuses_workspace_and_is_deterministic():
     assert (ws[256:].view(torch.int32)[:w.num_seqs * 2] == 0).all()
 
 
-def test_mla_clipped_context_is_flagged():
-    w = wl.make_mla_decode("clip", 260, 2, 1, 1, 16, block_size=16, context_lens=[500, 300],
+@pytest.mark.parametrize("H", [16, 128])
+def test_mla_context_hint_and_clipping(H):
+    """A max_context_len hint below the real lengths changes nothing (each
+    CTA takes an equal share of the real tiles); a length beyond the block
+    table is clipped to it and flagged."""
+    # sequence 0 fills its last block: clipping to the table adds no
+    # NaN-poisoned row past its context
+    w = wl.make_mla_decode("clip", 260, 2, 1, 1, H, block_size=16, context_lens=[512, 300],
                            with_weights=False)
     got, err = gpu_mla(w, max_context_len=256)
+    assert err == 0
+    for key, (r, ab) in oracle_rows(w, [(0, 0), (0, H - 1), (1, 3)]).items():
+        check_attn(got[key], r, ab, key)
+    w.context_lens = w.context_lens.copy()
+    w.context_lens[0] = w.max_blocks_per_seq * 16 + 40   # past the table
+    got, err = gpu_mla(w)
     assert err & pa.PA_DEVERR_CONTEXT_CLIPPED
     assert np.isfinite(got).all()
+    w.context_lens[0] = w.max_blocks_per_seq * 16        # what the clipped row attends to
+    for key, (r, ab) in oracle_rows(w, [(0, 0), (0, H - 1)]).items():
+        check_attn(got[key], r, ab, key)
 
 
 def test_mla_large_scores():
@@ -199,6 +214,39 @@ def test_mla_project_out(B):
     W = bf16_codes_to_f64(w.w_uv).reshape(512, 128, 128)       # [c, h, i]
     absum = np.einsum("bhc,chi->bhi", np.abs(ol), np.abs(W))
     check_proj(got, ref, absum)
+
+
+@pytest.mark.parametrize("nope,dc,dv,H,B", [
+    (64, 512, 64, 16, 5),      # absorb K = 64: both on the cp.async ring kernel
+    (256, 256, 128, 32, 64),   # absorb K = 256: both on the ring kernel
+    (128, 1024, 128, 16, 9),   # absorb on the TMA kernel with N = 1024; project K = 1024
+    (128, 512, 128, 16, 130),  # three 64-row tiles, the last one ragged
+])
+def test_mla_projection_shapes(nope, dc, dv, H, B):
+    """Both projections over shapes that select each kernel path (the TMA
+    kernel for absorb at d_h = 128, the ring kernel otherwise), against the
+    oracle."""
+    w = wl.make_mla_decode("pshape", 310 + B, B, 10, 20, H, with_weights=True, nope_dim=nope,
+                           latent_dim=dc, v_head_dim=dv)
+    need_gpu()
+    q_lat = torch.empty((B, H, dc + 64), dtype=torch.bfloat16, device="cuda")
+    pa.pa_mla_absorb_q(q_lat, to_dev(w.q_nope, "bf16"), to_dev(w.q_pe, "bf16"),
+                       to_dev(w.w_uk, "bf16"))
+    o_lat = wl.randn_bf16(torch.Generator().manual_seed(B), (B, H, dc), std=0.05)
+    out = torch.empty((B, H, dv), dtype=torch.bfloat16, device="cuda")
+    pa.pa_mla_project_out(out, to_dev(o_lat, "bf16"), to_dev(w.w_uv, "bf16"))
+    torch.cuda.synchronize()
+    got = bf16_codes_to_f64(to_host(q_lat, "bf16"))
+    ref = oracle.mla_absorb_q(w.q_nope, w.q_pe, w.w_uk)
+    absum = np.einsum("bhi,chi->bhc", np.abs(bf16_codes_to_f64(w.q_nope)),
+                      np.abs(bf16_codes_to_f64(w.w_uk).reshape(dc, H, nope)))
+    check_proj(got[:, :, :dc], ref[:, :, :dc], absum, "absorb")
+    assert (to_host(q_lat, "bf16")[:, :, dc:] == w.q_pe).all()
+    got = bf16_codes_to_f64(to_host(out, "bf16"))
+    ref = oracle.mla_project_out(o_lat, w.w_uv)
+    absum = np.einsum("bhc,chi->bhi", np.abs(bf16_codes_to_f64(o_lat)),
+                      np.abs(bf16_codes_to_f64(w.w_uv).reshape(dc, H, dv)))
+    check_proj(got, ref, absum, "project")
 
 
 def test_mla_chain_matches_explicit_attention():

@@ -53,7 +53,6 @@ using namespace pa;
 constexpr int kD = 128;                 // head size handled by this kernel
 constexpr int kTile = 64;               // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
-constexpr int kStages = 3;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRowBytes = kD * 2;       // one bf16 row of one KV head (tensor map stride)
 constexpr float kRescaleLog2 = 8.0f;    // lazy-rescale threshold (base-2 units)
@@ -113,19 +112,16 @@ constexpr int kHalfBytes = kTile * 128;  // one 64-row x 128-byte region (8 KB)
 // Shared memory of one CTA.  bf16 cache: per stage K_lo, K_hi, V_lo, V_hi
 // regions (64 rows x 128 B each: one 64-element half of every row).  fp8
 // cache: a 128-element row is 128 bytes, so per stage K and V regions, a
-// smaller CTA (three per SM, for more warps), and per consumer warp an f16 staging
-// tile (two [16 rows x 128 B] halves) for the converted V slice.  All regions
-// 128-byte swizzled and 1 KB aligned.
+// smaller CTA (three per SM, for more warps) and four stages (more bytes in
+// flight per SM).  All regions 128-byte swizzled and 1 KB aligned.
 template <bool kFp8>
 struct TcLayout {
-  static constexpr int kStages = 3;
+  static constexpr int kStages = kFp8 ? 4 : 3;
   static constexpr int kCtasPerSm = kFp8 ? 3 : 2;  // fp8 needs more warps per SM
   static constexpr int kRowBytes = kFp8 ? 128 : 256;  // one row of one kv head
   static constexpr int kStageBytes = (kFp8 ? 2 : 4) * kHalfBytes;
   static constexpr int kVOffset = (kFp8 ? 1 : 2) * kHalfBytes;
-  static constexpr int kStagingOffset = kStages * kStageBytes;
-  static constexpr int kStagingWarpBytes = kFp8 ? 2 * 16 * 128 : 0;
-  static constexpr int kBarOffset = kStagingOffset + kConsumerWarps * kStagingWarpBytes;
+  static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kBytes = kBarOffset + 3 * kStages * 8 + 16;  // full, empty, mask, flags
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KB
 };
@@ -232,7 +228,7 @@ __device__ __forceinline__ bool fused_token_write(const DecodeParams& p, int b, 
   return here;
 }
 
-template <int NT>
+template <int NT, bool kPairRows>
 __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem,
                                             float (&o)[8][NT][4], float (&m)[NT][2],
                                             float (&l)[NT][2], int b, int split, int hq0, int G,
@@ -308,9 +304,20 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
       prefetch_tensormap(&tm_v);
     }
     const int32_t* bt = p.block_tables + static_cast<int64_t>(b) * p.max_blocks_per_seq;
+    // lane i < nbox: block id of piece i of tile t (-1 past the range); the
+    // next tile's ids are read one iteration ahead, before the wait for a
+    // free stage, so their global-memory latency is off the issue path
+    auto tile_bid = [&](int t) -> int {
+      const int first = tok_begin + t * kTile + lane * rpb;
+      return (t < ntiles && lane < nbox && first < tok_end) ? __ldg(bt + (first >> p.log2_bs))
+                                                            : -1;
+    };
+    int bid_next = tile_bid(0);
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int stage = t % kStages;
+      const int bid_cur = bid_next;
+      bid_next = tile_bid(t + 1);
       if (t >= kStages) {
         const bool w_ok = mbar_wait_bounded(&empty[stage], ((t / kStages) - 1) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) {
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
         rows = min(rpb, nval - lane * rpb);
         if (rows > 0) {
           row0 = first & (bs - 1);
-          bid = __ldg(bt + (first >> p.log2_bs));
+          bid = bid_cur;
           valid = bid >= 0 && static_cast<int64_t>(bid) < p.num_blocks;
         }
       }
@@ -439,10 +446,10 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
     const int k_hi = lane >> 4;        // K: second 8 columns of the k-step
     const int v_hi = (lane >> 3) & 1;  // V: second 8 head elements of the m-tile
     const uint32_t smem_base = smem_u32(smem);
-    // fp8: this warp's f16 staging tile for V (two [16 x 128 B] halves)
-    uint8_t* stg = smem + Lay::kStagingOffset + warp * Lay::kStagingWarpBytes;
-    const uint32_t stg_base = smem_u32(stg);
-    const uint32_t v_row_stg = static_cast<uint32_t>(((lane & 7) + 8 * (lane >> 4)) * 128);
+    // fp8 V: ldmatrix.trans rows r0 + (lane & 7) (+8 for lanes 8-15, 24-31),
+    // 16-byte unit 2j (lanes 0-15) or 2j + 1 (lanes 16-31)
+    const int v8_row = r0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+    const uint32_t v8_off = static_cast<uint32_t>(v8_row * 128);
 
     // fused decode step: row of position L-1 in the last tile, and its warp
     const bool fused = p.new_k != nullptr && tok_end == L;
@@ -465,11 +472,12 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
         __syncwarp();
       }
       if (mask16 != 0u) {
-        if (!kFp8 && mask16 != 0xFFFFu) {
+        if (mask16 != 0xFFFFu) {
           // rows without a token: zero their V rows (0 x NaN would poison P.V)
           uint8_t* vrow0 = smem + stage * Lay::kStageBytes + Lay::kVOffset;
-          for (int idx = lane; idx < 16 * 16; idx += 32) {
-            const int rr = idx >> 4, unit = idx & 15;
+          constexpr int kUnits = kFp8 ? 8 : 16;  // 16-byte units of a V row in the stage
+          for (int idx = lane; idx < 16 * kUnits; idx += 32) {
+            const int rr = idx / kUnits, unit = idx % kUnits;
             if (!((mask16 >> rr) & 1u))
               *reinterpret_cast<uint4*>(vrow0 + (unit >> 3) * kHalfBytes + (r0 + rr) * 128 +
                                         (unit & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -587,39 +595,32 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
         }
         // ---- O^T += V^T . P^T
         if constexpr (kFp8) {
-          // convert this warp's 16 fp8 V rows to f16 in the staging tile
-          // (rows without a token become zeros: 0 x NaN would poison P.V)
-          // lanes 0-15: rows 0-15 of the low half, 16-31: the high half, so the
-          // eight lanes of each shared-memory phase hit eight distinct units
-          const int rr = lane & 15, hf = lane >> 4;
-          const int row = r0 + rr;
-          const bool rv = (mask16 >> rr) & 1u;
-          const uint8_t* vsrc = smem + stage * Lay::kStageBytes + Lay::kVOffset + row * 128;
-          uint8_t* dst = stg + hf * (16 * 128) + rr * 128;
+          // V^T straight from the e4m3 rows: ldmatrix.trans of byte pairs
+          // gives lane (gq, tq), for tokens 2tq, 2tq+1 (+8 in r[1], r[3]), the
+          // codes of head elements 2gq and 2gq + 1 of a 16-element unit.
+          // The rows of an m-tile are therefore paired: A row gq carries
+          // element 16mt + 2gq and row gq + 8 element 16mt + 2gq + 1 (the
+          // epilogue puts them back in order).  One byte permute per
+          // register groups each element's two tokens; two conversions make
+          // the f16 pairs.
+          const uint32_t vbase = st_base + Lay::kVOffset;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int u = 4 * hf + c;
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (rv) x = *reinterpret_cast<const uint4*>(vsrc + ((u ^ (row & 7)) << 4));
-            uint4 y0, y1;
-            e4m3x4_to_f16x2x2(x.x, y0.x, y0.y);
-            e4m3x4_to_f16x2x2(x.y, y0.z, y0.w);
-            e4m3x4_to_f16x2x2(x.z, y1.x, y1.y);
-            e4m3x4_to_f16x2x2(x.w, y1.z, y1.w);
-            *reinterpret_cast<uint4*>(dst + (((2 * c) ^ (rr & 7)) << 4)) = y0;
-            *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ (rr & 7)) << 4)) = y1;
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[4];
+            const int unit = 2 * j + (lane >> 4);
+            ldsm_x4_trans(vbase + v8_off + static_cast<uint32_t>((unit ^ (v8_row & 7)) << 4), r);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // m-tile 2j + h from r[2h] (tokens 0-7), r[2h+1] (8-15)
+              uint32_t a[4];
+              e4m3x4_to_f16x2x2(__byte_perm(r[2 * h], 0u, 0x3120u), a[0], a[1]);
+              e4m3x4_to_f16x2x2(__byte_perm(r[2 * h + 1], 0u, 0x3120u), a[2], a[3]);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma_f16_16816(o[2 * j + h][nt], a, pb[nt][0], pb[nt][1]);
+            }
           }
-          __syncwarp();
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            uint32_t a[4];
-            const uint32_t u = static_cast<uint32_t>(((2 * mt) & 7) + v_hi);
-            ldsm_x4_trans(stg_base + (mt >> 2) * (16 * 128) + v_row_stg + ((u ^ sw) << 4), a);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_f16_16816(o[mt][nt], a, pb[nt][0], pb[nt][1]);
-          }
-          __syncwarp();  // staging is rewritten by the next tile
-          if (smem_written) fence_proxy_async_smem();  // generic writes before the next TMA
+          if (mask16 != 0xFFFFu || smem_written)
+            fence_proxy_async_smem();  // generic writes before the next TMA
         } else {
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
@@ -658,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
                split] = -INFINITY;
   } else {
     const float out_scale = (kFp8 && p.v_scale != nullptr) ? __ldg(p.v_scale) : 1.f;
-    epilogue_tc<NT>(p, smem, o, m, l, b, split, hq0, G, warp, lane, out_scale);
+    epilogue_tc<NT, kFp8>(p, smem, o, m, l, b, split, hq0, G, warp, lane, out_scale);
   }
   if (p.num_splits == 1) return;
 
@@ -688,8 +689,10 @@ __global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
 
 // Epilogue of the tensor-core split kernel: merge the consumer warps'
 // (max, sum, accumulator) in shared memory; one split writes bf16 output,
-// several splits write an fp32 partial and its log2-sum-exp.
-template <int NT>
+// several splits write an fp32 partial and its log2-sum-exp.  kPairRows:
+// accumulator rows gq / gq + 8 of m-tile mt hold head elements 16mt + 2gq
+// and 16mt + 2gq + 1 (fp8 cache) instead of 16mt + gq and 16mt + gq + 8.
+template <int NT, bool kPairRows>
 __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem,
                                             float (&o)[8][NT][4], float (&m)[NT][2],
                                             float (&l)[NT][2], int b, int split, int hq0, int G,
@@ -720,8 +723,10 @@ __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem
         }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          red[(warp * GH + h) * kD + 16 * mt + gq] = o[mt][nt][j];
-          red[(warp * GH + h) * kD + 16 * mt + gq + 8] = o[mt][nt][j + 2];
+          const int e_lo = kPairRows ? 16 * mt + 2 * gq : 16 * mt + gq;
+          const int e_hi = kPairRows ? e_lo + 1 : e_lo + 8;
+          red[(warp * GH + h) * kD + e_lo] = o[mt][nt][j];
+          red[(warp * GH + h) * kD + e_hi] = o[mt][nt][j + 2];
         }
       }
     }

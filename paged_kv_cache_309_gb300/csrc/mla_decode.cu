@@ -96,11 +96,12 @@ struct MlaCfg {
 template <int HT>
 __device__ __forceinline__ void mla_issue_tile(const MlaParams& p, const CUtensorMap* tm_kv,
                                                uint8_t* smem, uint64_t* full, uint64_t* tile_mask,
-                                               const int32_t* bt, int tok0, int tok_end, int stage,
+                                               int lane_bid, int tok0, int tok_end, int stage,
                                                uint64_t pol, int lane) {
   using C = MlaCfg<HT>;
   mla_issue_tile_at(p, tm_kv, smem + C::kStageOff + stage * C::kStageBytes, C::kChunkBytes,
-                    C::kTile, &full[stage], &tile_mask[stage], bt, tok0, tok_end, pol, lane);
+                    C::kTile, &full[stage], &tile_mask[stage], lane_bid, tok0, tok_end, pol,
+                    lane);
 }
 
 // ------------------------------------------------------------- schedule --
@@ -318,22 +319,32 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
   const uint64_t pol = p.kv_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
   const int ntotal = g1 - g0;  // tiles of this chunk
 
-  // ---- the issuing side (warp 0): tile u of the chunk, across pieces
+  // ---- the issuing side (warp 0): tile u of the chunk, across pieces.  The
+  // next tile in issue order is prepared one issue ahead: its position, and
+  // its block ids read from the table (the read's latency then falls in the
+  // compute of a tile, not on warp 0's way to the next CTA barrier)
   BalIter<kTile> iti = it0;
   BalPiece pci{};
   int tli = 0, Li = 0;
   const int32_t* bti = nullptr;
-  auto issue_next = [&](int u) {  // warp 0, all lanes
+  int pre_tok0 = 0, pre_len = 0, pre_bid = -1;
+  auto prepare_next = [&]() {  // warp 0, all lanes
     if (tli >= pci.te || bti == nullptr) {
-      iti.next(p, pci);
+      if (!iti.next(p, pci)) return;
       tli = pci.tb;
       bool cl;
       Li = bal_len(p, pci.b, &cl);
       bti = p.block_tables + static_cast<int64_t>(pci.b) * p.max_blocks_per_seq;
     }
-    mla_issue_tile<HT>(p, &tm_kv, smem, full, tile_mask, bti, tli * kTile, Li, u % kStages, pol,
-                       lane);
+    pre_tok0 = tli * kTile;
+    pre_len = Li;
+    pre_bid = mla_tile_bid(p, bti, pre_tok0, Li, kTile, lane);
     ++tli;
+  };
+  auto issue_next = [&](int u) {  // warp 0, all lanes: the prepared tile, then prepare the next
+    mla_issue_tile<HT>(p, &tm_kv, smem, full, tile_mask, pre_bid, pre_tok0, pre_len, u % kStages,
+                       pol, lane);
+    if (u + 1 < ntotal) prepare_next();
   };
   int issued = 0;
   if (warp == 0) {
@@ -341,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_kv);
     }
+    prepare_next();
     for (; issued < kStages && issued < ntotal; ++issued) issue_next(issued);
   }
 

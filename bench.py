@@ -773,16 +773,31 @@ def run_prefill_only(args):
 
 
 def run_write_only(args):
-    """Cache-write launches only (for an ncu capture of that kernel): --steps
-    launches of the 32K-token prefill write to an e4m3 cache (scale 0.05),
-    then --steps of the same write to a bf16 cache."""
+    """Cache-write launches only (for an ncu capture of those kernels):
+    --steps launches each of the 32K-token prefill write to an e4m3 cache
+    (scale 0.05), to a bf16 cache, to an e4m3 cache through the SWA table
+    (window 4096), then of the 16K-token MLA latent-cache write."""
     import torch
 
     from paged_kv_cache_309_gb300 import build, pa
     from paged_kv_cache_309_gb300 import workloads as wl
     build.build()
     dev = torch.device("cuda", 0)
-    for variant in ("e4m3", "bf16"):
+
+    def run(name, fn, nbytes):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps - 1):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        per = e0.elapsed_time(e1) / max(1, args.steps - 1)
+        print(f"{name}: {args.steps} launches, {per * 1e3:.1f} us per launch (back to back, "
+              f"{nbytes / (per * 1e-3) / 1e9:.0f} GB/s)")
+
+    for variant in ("e4m3", "bf16", "e4m3_swa"):
         w = wl.prefill_write(variant=variant)
         H, d = w.key.shape[1:]
         cdt = torch.float8_e4m3fn if w.cache_dtype == "e4m3" else torch.bfloat16
@@ -790,21 +805,19 @@ def run_write_only(args):
         vc = torch.zeros_like(kc)
         key, val = up(w.key, torch.bfloat16, dev), up(w.value, torch.bfloat16, dev)
         sl = torch.from_numpy(w.slot_mapping).to(dev)
+        swa = None if w.swa_slot_mapping is None else torch.from_numpy(w.swa_slot_mapping).to(dev)
         ks = None if w.k_scale is None else torch.tensor([w.k_scale], dtype=torch.float32,
                                                          device=dev)
         vs = None if ks is None else ks.clone()
-        pa.pa_reshape_and_cache(key, val, kc, vc, sl, None, ks, vs)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps - 1):
-            pa.pa_reshape_and_cache(key, val, kc, vc, sl, None, ks, vs)
-        e1.record()
-        torch.cuda.synchronize()
-        per = e0.elapsed_time(e1) / max(1, args.steps - 1)
-        gbs = wl.write_bytes(w) / (per * 1e-3) / 1e9
-        print(f"{w.name}: {args.steps} launches, {per * 1e3:.1f} us per launch (back to back, "
-              f"{gbs:.0f} GB/s)")
+        run(w.name, lambda: pa.pa_reshape_and_cache(key, val, kc, vc, sl, swa, ks, vs),
+            wl.write_bytes(w))
+    m = wl.mla_assembly()
+    N = m.c_kv.shape[0]
+    ckv, kpe = up(m.c_kv, torch.bfloat16, dev), up(m.k_pe, torch.bfloat16, dev)
+    cache = torch.zeros((m.num_blocks, m.block_size, 1, 576), dtype=torch.bfloat16, device=dev)
+    msl = torch.from_numpy(m.slot_mapping).to(dev)
+    run("mla_latent_cache_write_16k", lambda: pa.pa_concat_and_cache_mla(ckv, kpe, cache, msl),
+        N * (576 * 2 * 2 + 8))
 
 
 def main():
@@ -828,7 +841,8 @@ def main():
                          "4 x 8192-token workload (no JSON)")
     ap.add_argument("--write-only", action="store_true",
                     help="profiling aid: only run --steps cache-write launches of the 32K-token "
-                         "prefill write, e4m3 then bf16 cache (no JSON)")
+                         "prefill write (e4m3, bf16, e4m3 through the SWA table), then of the "
+                         "16K-token MLA latent-cache write (no JSON)")
     ap.add_argument("--mla-proj", action="store_true",
                     help="profiling aid: only run --steps MLA absorb then project launches "
                          "(B=64, 128 heads; no JSON)")

@@ -111,12 +111,13 @@ __device__ __forceinline__ int effective_len(const DecodeParams& p, int b, bool*
 constexpr int kHalfBytes = kTile * 128;  // one 64-row x 128-byte region (8 KB)
 // Shared memory of one CTA.  bf16 cache: per stage K_lo, K_hi, V_lo, V_hi
 // regions (64 rows x 128 B each: one 64-element half of every row).  fp8
-// cache: a 128-element row is 128 bytes, so per stage K and V regions, a
-// smaller CTA (three per SM, for more warps) and four stages (more bytes in
-// flight per SM).  All regions 128-byte swizzled and 1 KB aligned.
+// cache: a 128-element row is 128 bytes, so per stage K and V regions and a
+// smaller CTA: three per SM, four when G <= 8 (the consumers then fit 96
+// registers), for more warps against latency.  All regions 128-byte
+// swizzled and 1 KB aligned.
 template <bool kFp8>
 struct TcLayout {
-  static constexpr int kStages = kFp8 ? 4 : 3;
+  static constexpr int kStages = 3;
   static constexpr int kCtasPerSm = kFp8 ? 3 : 2;  // fp8 needs more warps per SM
   static constexpr int kRowBytes = kFp8 ? 128 : 256;  // one row of one kv head
   static constexpr int kStageBytes = (kFp8 ? 2 : 4) * kHalfBytes;
@@ -236,7 +237,7 @@ __device__ __forceinline__ void epilogue_tc(const DecodeParams& p, uint8_t* smem
 
 // NT: n-tiles of 8 query heads (G <= 8 -> 1, G = 16 -> 2); kFp8: e4m3 cache.
 template <int NT, bool kFp8>
-__global__ void __launch_bounds__(kThreads, TcLayout<kFp8>::kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, (kFp8 && NT == 1) ? 4 : TcLayout<kFp8>::kCtasPerSm)
     paged_decode_split_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                  const __grid_constant__ CUtensorMap tm_v, const DecodeParams p,
                                  int G) {

@@ -1,0 +1,129 @@
+"""Randomised GPU parity: seeded random shapes for every kernel family,
+checked against the oracle with the same bars as the targeted tests
+(bit-exact cache writes; decode and MLA outputs within the stated 1e-2 bar
+and the tight bf16-output bounds of test_gpu_decode.py and
+test_gpu_mla_decode.py).
+
+Each case draws its configuration from a seeded generator, so a failure
+names a reproducible case: the group size, KV heads, block size, context
+lengths (empty and one-token contexts included), q scale and cache format
+for decode; source/cache dtypes, heads, head size, block size, strides,
+scales, skip fraction and an SWA table for the cache write; head count,
+block size and context lengths for MLA decode.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_309_gb300 import workloads as wl
+from tests.gpu_util import need_gpu
+from tests.test_gpu_cache_write import assert_same, run_both
+from tests.test_gpu_decode import check, gpu_decode_step, oracle_write
+from tests.test_gpu_decode_fp8 import fp8_decode_step, oracle_fp8
+from tests.test_gpu_mla_decode import check_attn, gpu_mla, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _lens(rng, B, hi):
+    """Context lengths (each includes the token the step writes): mostly
+    uniform in [1, hi], with a one-token and, for B > 2, an empty context."""
+    lens = rng.integers(1, hi + 1, size=B)
+    lens[rng.integers(0, B)] = 1
+    if B > 2:
+        lens[rng.integers(0, B)] = 0
+    return [int(x) for x in lens]
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_fuzz_decode_step(case):
+    """One decode step (write the new tokens, then attend) on a random shape,
+    every output row against the oracle; even cases use a bf16 cache, odd
+    cases an e4m3 cache with random scales."""
+    need_gpu()
+    rng = np.random.default_rng(1000 + case)
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    HKV = int(rng.choice([1, 2, 4, 8])) if G < 16 else int(rng.choice([1, 2]))
+    bs = int(rng.choice([8, 16, 32, 64, 128, 256]))
+    B = int(rng.integers(1, 9))
+    lens = _lens(rng, B, int(rng.choice([40, 700, 3000])))
+    q_std = float(rng.choice([0.3, 1.0, 4.0]))
+    w = wl.make_decode(f"fz{case}", 2000 + case, B, 0, 0, G * HKV, HKV, 128, bs, q_std=q_std,
+                       context_lens=lens)
+    what = dict(G=G, HKV=HKV, bs=bs, lens=lens, q_std=q_std)
+    if case % 2 == 0:
+        got, err, _ = gpu_decode_step(w)
+        assert err == 0, what
+        oracle_write(w)
+        ref, _ = oracle.paged_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                                     w.scale)
+        ref = {(b, h): ref[b, h].astype(np.float64) for b in range(B) for h in range(G * HKV)}
+    else:
+        ks, vs = float(rng.choice([0.02, 0.05, 0.25])), float(rng.choice([0.03, 0.05, 0.5]))
+        w = wl.as_fp8_history(w, seed=3000 + case, k_scale=ks, v_scale=vs)
+        got, err, _, _ = fp8_decode_step(w, ks, vs)
+        assert err == 0, what
+        ref = oracle_fp8(w, ks, vs)
+    for (b, h), r in ref.items():
+        if lens[b] == 0:
+            assert (got[b, h] == 0).all(), (what, b)
+        check(got[b, h], np.asarray(r, np.float64), (what, b, h))
+
+
+@pytest.mark.parametrize("case", range(10))
+def test_fuzz_cache_write(case):
+    """A random cache write against the oracle, every byte of both caches."""
+    rng = np.random.default_rng(4000 + case)
+    src = str(rng.choice(["bf16", "bf16", "fp16", "fp32"]))
+    cdt = str(rng.choice(["bf16", "fp16", "fp32", "e4m3", "e4m3"]))
+    H = int(rng.choice([1, 2, 4, 8]))
+    d = int(rng.choice([16, 64, 128, 256])) if cdt == "e4m3" else int(rng.choice([8, 64, 128, 192]))
+    bs = int(rng.choice([8, 16, 32, 64]))
+    N = int(rng.integers(1, 3000))
+    skip = float(rng.choice([0.0, 0.05, 0.5]))
+    swa = int(rng.choice([0, 0, N // 2 + 1]))
+    scaled = bool(rng.integers(0, 2)) or cdt == "e4m3"
+    scale = (float(rng.choice([0.05, 0.3, 2.0])), float(rng.choice([0.07, 1.0]))) if scaled else None
+    w = wl.make_prefill_write(f"fw{case}", 5000 + case, N, H, d, bs, skip_frac=skip,
+                              swa_window=swa or None)
+    key, value = w.key, w.value
+    if src != "bf16":  # the same values in the other source format
+        f32 = (key.astype(np.uint32) << 16).view(np.float32)
+        f32v = (value.astype(np.uint32) << 16).view(np.float32)
+        if src == "fp32":
+            key, value = f32, f32v
+        else:
+            key = f32.astype(np.float16).view(np.uint16)
+            value = f32v.astype(np.float16).view(np.uint16)
+    pad = int(rng.choice([0, 8, 24]))
+    bpad = int(rng.choice([0, 16]))
+    gk, gv, ok_, ov_ = run_both(key, value, src, w.slot_mapping, w.num_blocks, bs, cdt,
+                                swa=w.swa_slot_mapping, scale=scale, key_stride_pad=pad,
+                                block_pad=bpad)
+    assert_same(gk, ok_, cdt)
+    assert_same(gv, ov_, cdt)
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_fuzz_mla_decode(case):
+    """MLA decode over the latent cache on a random shape (the mma.sync
+    kernel for 16/32/48/64 heads, tcgen05 for 128 and 256), a sample of rows
+    of every sequence against the oracle."""
+    rng = np.random.default_rng(6000 + case)
+    H = int(rng.choice([16, 32, 48, 64, 128, 256]))
+    bs = int(rng.choice([8, 16, 32, 64, 128]))
+    B = int(rng.integers(1, 12))
+    lens = _lens(rng, B, int(rng.choice([60, 900, 5000])))
+    w = wl.make_mla_decode(f"fm{case}", 7000 + case, B, 1, 1, H, block_size=bs,
+                           context_lens=lens, q_std=float(rng.choice([0.5, 1.0, 3.0])),
+                           with_weights=False)
+    got, err = gpu_mla(w, max_context_len=int(rng.choice([max(lens), 64])))
+    assert err == 0
+    rows = [(b, int(h)) for b in range(B) for h in rng.choice(H, min(H, 6), replace=False)]
+    for key, (r, ab) in oracle_rows(w, rows).items():
+        if lens[key[0]] == 0:
+            assert (got[key] == 0).all(), key
+        check_attn(got[key], r, ab, (dict(H=H, bs=bs, lens=lens), key))

@@ -527,13 +527,21 @@ def run_extras(args, dev, peak):
     sl = torch.from_numpy(m.slot_mapping).to(dev)
     med, _ = timed_loop(lambda: pa.pa_concat_and_cache_mla(ckv, kpe, cache, sl), iters, 3, dev)
     nbytes = N * (576 * 2 * 2 + 8)  # each row read and written once, plus its slot
+    # context for a launch this short: a plain device-to-device copy of the same
+    # rows (N x 1152 B read and written), timed the same way
+    csrc = torch.empty(N * 576, dtype=torch.bfloat16, device=dev)
+    cdst = torch.empty_like(csrc)
+    cmed, _ = timed_loop(lambda: cdst.copy_(csrc), iters, 3, dev)
+    del csrc, cdst
     ex["mla_latent_cache_write_16k"] = {"call": "pa_concat_and_cache_mla (one launch)",
                                         "tokens_per_s": round(N / (med * 1e-3), 1),
                                         "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 2),
                                         "frac_of_hbm_peak": round(nbytes / (med * 1e-3) / 1e9 /
                                                                   peak, 4),
                                         "median_us": round(med * 1e3, 2),
-                                        "algorithmic_bytes": nbytes}
+                                        "algorithmic_bytes": nbytes,
+                                        "same_bytes_device_copy_us": round(cmed * 1e3, 2),
+                                        "frac_of_same_bytes_copy_rate": round(cmed / med, 4)}
     # MLA decode over the latent cache (DeepSeek-V3-shaped: B=64, context
     # 512..4096, bs=64): 128 heads (tcgen05 kernel) and 16 heads (one TP8
     # shard, mma.sync kernel); for 128 heads also the absorbed chain

@@ -24,6 +24,9 @@ namespace {
 constexpr int kWarps = 8;            // warps per CTA
 constexpr int kChunksPerLane = 4;    // chunks of 8 elements per lane per tensor
 constexpr int kChunksPerWarp = 32 * kChunksPerLane;
+constexpr int kTwoSrcRowsPerWarp = 2;
+constexpr int kTwoSrcSlotsPerLane = 5;  // 160 chunks: two rows of up to 80 chunks (the
+                                        // 576-element MLA latent row is 72)
 
 // Writes token t's row to slot s (already resolved and in the pool): the
 // lane's chunks c_begin, c_begin + 32, ... of the row's chunk group.
@@ -107,6 +110,76 @@ __device__ __forceinline__ void write_row(const ReshapeArgs& a, int64_t t, int64
   }
 }
 
+// Two-source rows (K only, rows of at most 128 chunks), kRows tokens per
+// warp: chunk c of the warp's kRows * row_chunks is chunk c % row_chunks of
+// row c / row_chunks; every load of the rows is issued before the first
+// store, so a warp keeps kRows rows in flight (the MLA latent row is 72
+// chunks, which one warp alone covers with 2.25 chunks per lane).  s[r] < 0:
+// row r is skipped.
+// s[r] for a row index known only at run time, by selects (no local-memory array)
+template <int kRows>
+__device__ __forceinline__ int64_t pick_row(const int64_t (&s)[kRows], int r) {
+  int64_t v = -1;
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) v = r == i ? s[i] : v;
+  return v;
+}
+
+template <typename S, typename D, bool kRaw, int kRows>
+__device__ __forceinline__ void write_rows_two_src(const ReshapeArgs& a, int64_t t0,
+                                                   const int64_t (&s)[kRows], int lane) {
+  using namespace pa;
+  constexpr int kMax = kTwoSrcSlotsPerLane;  // chunks per lane (kRows rows fit 32 * kMax)
+  const int rc = a.row_chunks;
+  Vec8<S> x[kMax];
+#pragma unroll
+  for (int i = 0; i < kMax; ++i) {
+    const int c = lane + 32 * i;
+    const int r = c / rc, cc = c - (c / rc) * rc;
+    if (r < kRows && pick_row(s, r) >= 0) {
+      const int64_t t = t0 + r;
+      const S* src = cc < a.key_chunks
+                         ? static_cast<const S*>(a.key) + t * a.key_stride + 8 * cc
+                         : static_cast<const S*>(a.key2) + t * a.key2_stride +
+                               8 * (cc - a.key_chunks);
+      x[i] = load8(src);
+    }
+  }
+  const bool scaled = a.k_scale != nullptr;
+  const Divisor ks = make_divisor(!kRaw && scaled ? __ldg(a.k_scale) : 1.0f);
+  const float kxmax = fminf(1.7e38f * ks.s, 3.0e38f);
+  constexpr bool kToE4m3 = std::is_same<D, e4m3>::value;
+#pragma unroll
+  for (int i = 0; i < kMax; ++i) {
+    const int c = lane + 32 * i;
+    const int r = c / rc, cc = c - (c / rc) * rc;
+    const int64_t sr = pick_row(s, r);
+    if (r < kRows && sr >= 0) {
+      const int64_t blk = (a.block_size & (a.block_size - 1)) == 0
+                              ? sr >> (__ffs(a.block_size) - 1)
+                              : sr / a.block_size;
+      const int64_t off = sr - blk * a.block_size;
+      D* dst = static_cast<D*>(a.key_cache) + blk * a.block_stride +
+               off * static_cast<int64_t>(rc) * 8 + 8 * cc;
+      if constexpr (kRaw) {
+        store8(dst, x[i]);
+      } else {
+        float f[8];
+        if (kToE4m3 && scaled) {
+          div8_for_e4m3(x[i], f, ks, kxmax);
+        } else {
+          to_f32(x[i], f);
+          if (scaled) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = div_rn(f[e], ks);  // IEEE quotient
+          }
+        }
+        store8(dst, from_f32<D>(f));
+      }
+    }
+  }
+}
+
 // kTPW = 1: one warp per (token, chunk group); every lane resolves the slot
 // from the same address (a broadcast), so a skipped token exits the warp.
 // kTPW = 8 (a second-stage SWA table, rows of one chunk group): lanes 0-7
@@ -121,7 +194,18 @@ template <typename S, typename D, bool kRaw, bool kTwoSrc, int kTPW>
 __global__ void __launch_bounds__(kWarps * 32, 4) reshape_and_cache_kernel(ReshapeArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if constexpr (kTPW == 1) {
+  if constexpr (kTwoSrc && kTPW > 1) {
+    // kTPW two-source rows per warp (rows of one chunk group, no SWA table)
+    const int64_t t0 = wid * kTPW;
+    if (t0 >= a.num_tokens) return;
+    int64_t s[kTPW];
+#pragma unroll
+    for (int r = 0; r < kTPW; ++r) {
+      s[r] = t0 + r < a.num_tokens ? __ldg(a.slot_mapping + t0 + r) : -1;
+      if (s[r] >= a.num_slots) s[r] = -1;
+    }
+    write_rows_two_src<S, D, kRaw, kTPW>(a, t0, s, lane);
+  } else if constexpr (kTPW == 1) {
     const int64_t t = a.groups == 1 ? wid : wid / a.groups;  // a 64-bit division is long
     const int grp = static_cast<int>(wid - t * a.groups);
     if (t >= a.num_tokens) return;
@@ -160,14 +244,29 @@ template <typename S, typename D>
 pa_status launch_typed(ReshapeArgs a, cudaStream_t stream) {
   a.groups = (a.row_chunks + kChunksPerWarp - 1) / kChunksPerWarp;
   const bool batched = a.swa != nullptr && a.groups == 1 && a.key2 == nullptr;
+  // (32-bit sources keep one row per warp: two rows of them do not fit the registers)
+  const bool paired = sizeof(S) == 2 && a.key2 != nullptr && a.swa == nullptr &&
+                      kTwoSrcRowsPerWarp * a.row_chunks <= 32 * kTwoSrcSlotsPerLane;
   const int64_t warps = batched ? (a.num_tokens + kSwaTokensPerWarp - 1) / kSwaTokensPerWarp
-                                : a.num_tokens * a.groups;
+                        : paired ? (a.num_tokens + kTwoSrcRowsPerWarp - 1) / kTwoSrcRowsPerWarp
+                                 : a.num_tokens * a.groups;
   const int64_t blocks = (warps + kWarps - 1) / kWarps;
   if (blocks == 0) return PA_OK;
   if (blocks > 0x7FFFFFFFll) return PA_ERR_UNSUPPORTED;
   const bool raw = std::is_same<S, D>::value && a.k_scale == nullptr;
   const unsigned grid = static_cast<unsigned>(blocks);
-  if (a.key2 != nullptr) {
+  if (paired) {
+    if constexpr (sizeof(S) == 2) {
+      if (raw) {
+        if constexpr (std::is_same<S, D>::value)
+          reshape_and_cache_kernel<S, D, true, true, kTwoSrcRowsPerWarp>
+              <<<grid, kWarps * 32, 0, stream>>>(a);
+      } else {
+        reshape_and_cache_kernel<S, D, false, true, kTwoSrcRowsPerWarp>
+            <<<grid, kWarps * 32, 0, stream>>>(a);
+      }
+    }
+  } else if (a.key2 != nullptr) {
     if (raw) {
       if constexpr (std::is_same<S, D>::value)
         reshape_and_cache_kernel<S, D, true, true, 1><<<grid, kWarps * 32, 0, stream>>>(a);

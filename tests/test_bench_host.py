@@ -68,13 +68,28 @@ def test_traffic_null_without_a_record(root):
                                 "bf16") is None
 
 
-def test_committed_record_names_its_hashed_sources():
+def test_committed_records_name_their_hashed_sources():
     with open(os.path.join(bench.ROOT, "profiles", "decode_traffic.json")) as f:
-        rec = json.load(f)
-    assert rec["hashed_sources"] == ["paged_kv_cache_309_gb300/csrc/decode.cu",
-                                     "paged_kv_cache_309_gb300/csrc/pa_internal.cuh"]
-    assert rec["dram_bytes_per_decode_call"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
-    assert "--clock-control none" in rec["command"]
+        d = json.load(f)
+    assert d["hashed_sources"] == ["paged_kv_cache_309_gb300/csrc/decode.cu",
+                                   "paged_kv_cache_309_gb300/csrc/pa_internal.cuh"]
+    assert d["records"]
+    keys = set()
+    for rec in d["records"]:
+        assert rec["dram_bytes_per_decode_call"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+        assert "--clock-control none" in rec["command"]
+        key = (rec["workload"], rec["step"], rec["kv_dtype"])
+        assert key not in keys  # one record per workload, step and KV format
+        keys.add(key)
+
+
+def test_traffic_picks_the_matching_record(root):
+    recs = [dict(workload=f"w{i}", step="fused", kv_dtype=k, source_sha256_16=_sources_hash(),
+                 dram_bytes_per_decode_call=100 + i) for i, k in enumerate(["bf16", "e4m3"])]
+    (root / "profiles" / "decode_traffic.json").write_text(json.dumps({"records": recs}))
+    assert bench.traffic_record(KERNEL, "w1", "fused", "e4m3") == 101
+    assert bench.traffic_record(KERNEL, "w0", "fused", "bf16") == 100
+    assert bench.traffic_record(KERNEL, "w1", "fused", "bf16") is None
 
 
 def test_peak_from_measured_file_else_fallback(root):

@@ -8,7 +8,8 @@ Each case draws its configuration from a seeded generator, so a failure
 names a reproducible case: the group size, KV heads, block size, context
 lengths (empty and one-token contexts included), q scale and cache format
 for decode; source/cache dtypes, heads, head size, block size, strides,
-scales, skip fraction and an SWA table for the cache write; head count,
+scales, skip fraction and an SWA table for the cache write; row split,
+block size, formats, scale and skips for the one-pass latent write; head count,
 block size and context lengths for MLA decode.
 """
 import math
@@ -19,10 +20,11 @@ import torch
 
 import oracle
 from paged_kv_cache_309_gb300 import workloads as wl
-from tests.gpu_util import need_gpu
+from tests.gpu_util import codes_equal, need_gpu
 from tests.test_gpu_cache_write import assert_same, run_both
 from tests.test_gpu_decode import check, gpu_decode_step, oracle_write
 from tests.test_gpu_decode_fp8 import fp8_decode_step, oracle_fp8
+from tests.test_gpu_mla import fused_latent_write
 from tests.test_gpu_mla_decode import check_attn, gpu_mla, oracle_rows
 
 pytestmark = pytest.mark.gpu
@@ -105,6 +107,30 @@ def test_fuzz_cache_write(case):
                                 block_pad=bpad)
     assert_same(gk, ok_, cdt)
     assert_same(gv, ov_, cdt)
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_fuzz_latent_write(case):
+    """A random one-pass latent write ([c_kv | k_pe] rows, odd token counts,
+    rows of one and of two chunk groups) against the oracle's concat + cache
+    write, every byte of the cache."""
+    rng = np.random.default_rng(8000 + case)
+    dc = 8 * int(rng.integers(1, 160))
+    dr = 8 * int(rng.integers(1, 17))
+    bs = int(rng.choice([1, 8, 16, 64]))
+    N = int(rng.integers(1, 700))
+    src = str(rng.choice(["bf16", "fp16"]))
+    cdt = str(rng.choice(["bf16", "fp16", "e4m3"]))
+    scale = float(rng.choice([0.05, 0.5])) if cdt == "e4m3" or rng.integers(0, 2) else None
+    nb = (N + bs - 1) // bs + int(rng.integers(0, 3))
+    slots = rng.permutation(nb * bs)[:N].astype(np.int64)
+    slots[rng.random(N) < float(rng.choice([0.0, 0.1]))] = -1
+    f = rng.standard_normal((N, dc + dr)).astype(np.float32)
+    bits = (f.view(np.uint32) >> 16).astype(np.uint16) if src == "bf16" \
+        else f.astype(np.float16).view(np.uint16)
+    got, ref = fused_latent_write(bits[:, :dc].copy(), bits[:, dc:].copy(), slots, nb, bs, src,
+                                  cdt, scale=scale, pad=int(rng.choice([0, 8])))
+    assert codes_equal(got, ref, cdt).all(), dict(dc=dc, dr=dr, bs=bs, N=N, src=src, cdt=cdt)
 
 
 @pytest.mark.parametrize("case", range(8))

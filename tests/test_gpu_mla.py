@@ -145,7 +145,8 @@ def test_concat_and_cache_mla_scaled_casts_and_skips(cdt, scale):
     assert codes_equal(got, ref, cdt).all()
 
 
-@pytest.mark.parametrize("N,dc,dr,bs", [(1, 8, 8, 8), (37, 512, 64, 16), (64, 256, 32, 128)])
+@pytest.mark.parametrize("N,dc,dr,bs", [(1, 8, 8, 8), (37, 512, 64, 16), (64, 256, 32, 128),
+                                         (9, 576, 64, 16), (20, 1024, 64, 32)])
 def test_concat_and_cache_mla_shapes(N, dc, dr, bs):
     g = torch.Generator().manual_seed(N + dc)
     ckv = wl.randn_bf16(g, (N, dc))

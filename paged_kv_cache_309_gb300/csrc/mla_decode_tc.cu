@@ -44,7 +44,10 @@
 //    beats it by more than 2^8; the rescale reads, scales and writes back
 //    the TMEM output row).
 //  * epilogue of a piece: the softmax threads read their output row from
-//    TMEM and write bf16 (whole sequence) or an fp32 partial + log2-sum-exp.
+//    TMEM and write bf16 (whole sequence) or an fp32 partial + log2-sum-exp
+//    (column-quad-major, so a warp's stores are 512 contiguous bytes).  The
+//    next piece's q_lat is loaded before that epilogue, as soon as this
+//    piece's last scores were read, so its score products overlap it.
 //
 // Every wait is bounded (2 s); a timeout sets an error bit, the roles leave
 // their loops, the MMAs and copies already issued are drained, TMEM is
@@ -82,8 +85,10 @@ constexpr int kQRopeOff = kRecvOff + 2 * kRecvBytes;
 constexpr int kBarOff = kQRopeOff + kQRopeBytes;
 // barriers: q_full, kv_full[kStages], kv_empty[kStages], s_full[2],
 // p_full[2], pv_done[2], recv_full[2], sent_free[2], o_done, drain[2],
-// part_done, mrg_full; then tile masks, the TMEM slot and flags, the schedule
-constexpr int kNumBars = 18 + 2 * kStages;
+// part_done, sum_full[2], mrg_full[kMrgBufs]; then tile masks, the TMEM
+// slot and flags, the schedule
+constexpr int kMrgBufs = 3;
+constexpr int kNumBars = 17 + kMrgBufs + 2 * kStages;
 constexpr int kMaskOff = kBarOff + kNumBars * 8;
 constexpr int kMiscOff = kMaskOff + kStages * 8;
 constexpr int kSchedOff = kMiscOff + 32;             // schedule words and the merge list
@@ -151,6 +156,9 @@ __device__ __forceinline__ bool wait_cluster_bounded(uint64_t* bar, uint32_t par
       if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
     }
   }
+}
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
@@ -260,20 +268,29 @@ __device__ __forceinline__ int piece_slot(const Piece& pc, int c) { return 2 * c
 // over its pieces, by the whole CTA once its own work is done: the pieces
 // are clusters c_first .. c_last; slot of the first one 2 c_first (+1 if it
 // is not that cluster's first piece), of the others 2c.  Piece i gets weight
-// 2^(lse_i - M) / sum_j 2^(lse_j - M) per head (M the heads' maximum).  The
-// partials are stored half-major ([slot][half][head][256] floats), so the
-// rows of a group of kMrgHeads heads of one piece are one contiguous bulk
-// copy; up to kMrgPieces pieces of a group land under one barrier, and each
-// thread sums eight 16-byte columns of the group from shared memory.
-constexpr int kMrgHeads = 24;
-constexpr int kMrgPieces = 7;
-constexpr int kMrgStageBytes = kMrgPieces * kMrgHeads * kHalf * 4;  // 168 KB
-static_assert(kMrgStageBytes + (2 * kHT + kMrgPieces * kHT) * 4 <= kBarOff,
+// 2^(lse_i - M) / sum_j 2^(lse_j - M) per head (M the heads' maximum).
+// Partials are stored column-quad-major, [slot][half][quad][head] of float4
+// (a warp's epilogue stores are then 512 contiguous bytes), so one group of
+// kMrgQuads quads of all 128 heads of one piece is one contiguous 16 KB bulk
+// copy.  Jobs are (group, batch of up to kMrgPieces pieces); up to kMrgBufs
+// jobs are in flight, each buffer on its own barrier.  A thread sums
+// (quad, head) pairs with the head fastest (conflict-free shared reads),
+// the bf16 results go through a padded tile and leave as 64-byte row
+// segments of the output.
+constexpr int kMrgQuads = 8;                                // 32 columns per group
+constexpr int kMrgGroups = kHalf / 4 / kMrgQuads;           // 8 groups per half row
+constexpr int kMrgGroupBytes = kMrgQuads * kHT * 16;        // one piece's rows of a group
+constexpr int kMrgPieces = 7;                               // pieces per batch
+constexpr int kMrgStageBytes = 9 * kMrgGroupBytes;          // 144 KB of job buffers
+constexpr int kMrgOutPitch = kMrgQuads * 8 + 16;            // bf16 tile row: 64 B + pad
+constexpr int kMrgOutOff = kMrgStageBytes;
+constexpr int kMrgWOff = kMrgOutOff + kHT * kMrgOutPitch;
+constexpr int kMrgPairs = (kMrgQuads * kHT + kThreads - 1) / kThreads;  // pairs per thread
+static_assert(kMrgWOff + (2 * kHT + kMrgPieces * kHT) * 4 <= kBarOff,
               "merge staging fits below the barriers");
-static_assert(kThreads * 8 >= kMrgHeads * kHalf / 4, "eight columns per thread cover a group");
 __device__ __forceinline__ void merge_pieces(const MlaParams& p, int b, int ht, int v, int pre,
-                                             int n, int chunk, uint8_t* stage, float* wsm,
-                                             uint64_t* bar, uint32_t& phase) {
+                                             int n, int chunk, uint8_t* stage, uint64_t* bar,
+                                             uint32_t* phase) {
   const int c_first = pre / chunk, c_last = (pre + n - 1) / chunk;
   const int np = c_last - c_first + 1;
   const int s0 = 2 * c_first + (pre != c_first * chunk ? 1 : 0);
@@ -281,9 +298,11 @@ __device__ __forceinline__ void merge_pieces(const MlaParams& p, int b, int ht, 
   const int64_t base = static_cast<int64_t>(ht) * p.num_slots;
   const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + ht * kHT;
   const int tid = threadIdx.x, nthr = blockDim.x;
+  float* wsm = reinterpret_cast<float*>(stage + kMrgWOff);
   float* wmax = wsm;             // [kHT] per-head maximum of the pieces' lse
   float* winv = wsm + kHT;       // [kHT] 1 / sum of the weights
   float* wb = wsm + 2 * kHT;     // [kMrgPieces][kHT] weights of the current batch
+  uint8_t* otile = stage + kMrgOutOff;
   for (int h = tid; h < kHT; h += nthr) {
     if (np <= kMrgPieces) {
       // every piece's lse in flight at once; the weights of all pieces here
@@ -332,59 +351,83 @@ __device__ __forceinline__ void merge_pieces(const MlaParams& p, int b, int ht, 
   }
   fence_proxy_async_global();  // the partials were written by ordinary stores
   __syncthreads();
-  constexpr int kCol4 = kHalf / 4;  // 16-byte columns of one head's half row
-  for (int hg0 = 0; hg0 < kHT; hg0 += kMrgHeads) {
-    const int nh = min(kMrgHeads, kHT - hg0);
-    float4 acc[8];
+  const int nbp = min(np, kMrgPieces);                      // pieces per batch
+  const int nbatch = (np + nbp - 1) / nbp;
+  const int njobs = kMrgGroups * nbatch;
+  const int nbuf = min(kMrgBufs, kMrgStageBytes / (nbp * kMrgGroupBytes));
+  auto issue = [&](int job) {  // thread 0: one batch of pieces of one group
+    const int g = job / nbatch, i0 = (job % nbatch) * nbp;
+    const int npb = min(nbp, np - i0);
+    uint64_t* bb = &bar[job % nbuf];
+    uint8_t* dst = stage + (job % nbuf) * nbp * kMrgGroupBytes;
+    mbar_arrive_expect_tx(bb, static_cast<uint32_t>(npb * kMrgGroupBytes));
+    for (int j = 0; j < npb; ++j)
+      bulk_load(dst + j * kMrgGroupBytes,
+                p.ws_o + ((base + slot(i0 + j)) * 2 + v) * kHT * kHalf +
+                    static_cast<int64_t>(g) * kMrgQuads * kHT * 4,
+                static_cast<uint32_t>(kMrgGroupBytes), bb);
+  };
+  if (tid == 0)
+    for (int job = 0; job < min(nbuf, njobs); ++job) issue(job);
+  float4 acc[kMrgPairs];
+  for (int job = 0; job < njobs; ++job) {
+    const int g = job / nbatch, bi = job % nbatch, i0 = bi * nbp;
+    const int npb = min(nbp, np - i0);
+    if (bi == 0) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < np; i0 += kMrgPieces) {
-      const int npb = min(kMrgPieces, np - i0);
-      if (np > kMrgPieces) {
-        for (int idx = tid; idx < npb * nh; idx += nthr) {
-          const int j = idx / nh, hh = idx % nh;
-          const float M = wmax[hg0 + hh];
-          const float l = __ldcg(p.ws_lse + (base + slot(i0 + j)) * kHT + hg0 + hh);
-          wb[j * kHT + hg0 + hh] = M == -INFINITY ? 0.f : exp2f(l - M) * winv[hg0 + hh];
-        }
-      }
-      if (tid == 0) {
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(npb * nh * kHalf * 4));
-        for (int j = 0; j < npb; ++j)
-          bulk_load(stage + j * kMrgHeads * (kHalf * 4),
-                    p.ws_o + ((base + slot(i0 + j)) * 2 + v) * kHT * kHalf +
-                        static_cast<int64_t>(hg0) * kHalf,
-                    static_cast<uint32_t>(nh * kHalf * 4), bar);
-      }
-      if (!mbar_wait_bounded(bar, phase, nullptr) && tid == 0) atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
-      phase ^= 1u;
-      __syncthreads();  // the batch weights are written
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int col = tid + nthr * u;
-        if (col < nh * kCol4) {
-          const int hh = col / kCol4, e4 = col % kCol4;
-          for (int j = 0; j < npb; ++j) {
-            const float4 x = reinterpret_cast<const float4*>(
-                stage + (j * kMrgHeads + hh) * (kHalf * 4))[e4];
-            const float w = wb[(np > kMrgPieces ? j : i0 + j) * kHT + hg0 + hh];
-            acc[u].x += w * x.x;
-            acc[u].y += w * x.y;
-            acc[u].z += w * x.z;
-            acc[u].w += w * x.w;
-          }
-        }
-      }
-      __syncthreads();  // the staging buffers and weights are free again
+      for (int u = 0; u < kMrgPairs; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int col = tid + nthr * u;
-      if (col < nh * kCol4) {
-        const int hh = col / kCol4, e4 = col % kCol4;
-        *reinterpret_cast<uint2*>(p.out + (bh0 + hg0 + hh) * kLat + kHalf * v + 4 * e4) =
-            make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+    if (np > kMrgPieces) {  // this batch's weights
+      for (int idx = tid; idx < npb * kHT; idx += nthr) {
+        const int j = idx / kHT, h = idx % kHT;
+        const float M = wmax[h];
+        const float l = __ldcg(p.ws_lse + (base + slot(i0 + j)) * kHT + h);
+        wb[j * kHT + h] = M == -INFINITY ? 0.f : exp2f(l - M) * winv[h];
       }
+      __syncthreads();
+    }
+    const int buf = job % nbuf;
+    if (!mbar_wait_bounded(&bar[buf], phase[buf], nullptr) && tid == 0)
+      atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+    phase[buf] ^= 1u;
+    const float4* src = reinterpret_cast<const float4*>(stage + buf * nbp * kMrgGroupBytes);
+#pragma unroll
+    for (int u = 0; u < kMrgPairs; ++u) {
+      const int idx = tid + nthr * u;  // (quad, head), head fastest
+      if (idx < kMrgQuads * kHT) {
+        const int h = idx % kHT;
+        for (int j = 0; j < npb; ++j) {
+          const float4 x = src[j * (kMrgQuads * kHT) + idx];
+          const float w = wb[(np > kMrgPieces ? j : i0 + j) * kHT + h];
+          acc[u].x += w * x.x;
+          acc[u].y += w * x.y;
+          acc[u].z += w * x.z;
+          acc[u].w += w * x.w;
+        }
+      }
+    }
+    __syncthreads();  // buffer `buf` (and this batch's weights) are free again
+    if (tid == 0 && job + nbuf < njobs) issue(job + nbuf);
+    if (bi + 1 == nbatch) {
+      // group g done: bf16 through the padded tile, out as 64-byte row segments
+#pragma unroll
+      for (int u = 0; u < kMrgPairs; ++u) {
+        const int idx = tid + nthr * u;
+        if (idx < kMrgQuads * kHT) {
+          const int q = idx / kHT, h = idx % kHT;
+          *reinterpret_cast<uint2*>(otile + h * kMrgOutPitch + q * 8) =
+              make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+        }
+      }
+      __syncthreads();
+      for (int idx = tid; idx < kHT * (kMrgQuads / 2); idx += nthr) {
+        const int h = idx / (kMrgQuads / 2), c16 = idx % (kMrgQuads / 2);
+        *reinterpret_cast<uint4*>(p.out + (bh0 + h) * kLat + kHalf * v + 4 * kMrgQuads * g +
+                                  8 * c16) =
+            *reinterpret_cast<const uint4*>(otile + h * kMrgOutPitch + 16 * c16);
+      }
+      // the tile is rewritten only after the next job's barrier, which every
+      // thread reaches after its share of this write-out
     }
   }
 }
@@ -407,8 +450,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* o_done = sent_free + 2;              // every product of the current piece done
   uint64_t* drain = o_done + 1;                  // [2] each issuer's products done
   uint64_t* part_done = drain + 2;               // a partial's 128 rows are written
-  uint64_t* mrg_full = part_done + 1;            // a merge batch's partial rows landed
-  uint64_t* sum_full = mrg_full + 1;             // [2] full scores back in TMEM (128 threads)
+  uint64_t* sum_full = part_done + 1;            // [2] full scores back in TMEM (128 threads)
+  uint64_t* mrg_full = sum_full + 2;             // [kMrgBufs] a merge batch's partial rows landed
   uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);  // [0] abort
@@ -491,7 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
     mbar_init(part_done, kHT);
-    mbar_init(mrg_full, 1);
+    for (int i = 0; i < kMrgBufs; ++i) mbar_init(&mrg_full[i], 1);
     mbar_init(&sum_full[0], kHT);
     mbar_init(&sum_full[1], kHT);
     flags[0] = 0;
@@ -716,34 +759,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int gbase = 0;    // this cluster's tiles before the current piece
     int npiece = 0;   // pieces done
     int npart = 0;    // partial pieces done
-    while (ok && it.next(p, pc)) {
-      const int64_t bh = static_cast<int64_t>(pc.b) * p.num_heads + h0 + row;
-      // this CTA's slice of the piece's q_lat: latent elements 256v .. 256v +
-      // 255 as bf16 pairs in TMEM, rope elements 32v .. 32v + 31 in shared
-      // memory (64-byte swizzle).  The previous piece's products and output
-      // are done (o_done), so both may be overwritten.
+    // this CTA's slice of a piece's q_lat: latent elements 256v .. 256v + 255
+    // as bf16 pairs in TMEM, rope elements 32v .. 32v + 31 in shared memory
+    // (64-byte swizzle).  Called once every score product of the previous
+    // piece is done (its last scores were read), so both may be overwritten:
+    // the next piece's score products start while this piece's last output
+    // products and its epilogue run.
+    auto load_q = [&](const Piece& q) {
+      const int64_t qbh = static_cast<int64_t>(q.b) * p.num_heads + h0 + row;
       {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q_latent + bh * kRow);
-        // two chunks per global round trip (4 x 64 latent elements = 4 x 32
-        // columns); the rope part rides with the first pair
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_latent + qbh * kRow);
+        // the whole slice in one global round trip (4 x 64 latent elements
+        // = 128 columns, and the rope part)
         uint4 rope[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) rope[u] = __ldg(src + (kLat + kRopeHalf * v) / 8 + u);
-#pragma unroll 1
-        for (int cq = 0; cq < 4; cq += 2) {
-          uint32_t w[64];
+        uint32_t w[128];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const uint4 x = __ldg(src + (kHalf * v + 64 * cq) / 8 + u);
-            w[4 * u] = x.x;
-            w[4 * u + 1] = x.y;
-            w[4 * u + 2] = x.z;
-            w[4 * u + 3] = x.w;
-          }
-          tc_st32u_nowait(tmem + lane_addr + kQCol + 32 * cq, &w[0]);
-          tc_st32u_nowait(tmem + lane_addr + kQCol + 32 * cq + 32, &w[32]);
-          tc_wait_st();
+        for (int u = 0; u < 32; ++u) {
+          const uint4 x = __ldg(src + (kHalf * v) / 8 + u);
+          w[4 * u] = x.x;
+          w[4 * u + 1] = x.y;
+          w[4 * u + 2] = x.z;
+          w[4 * u + 3] = x.w;
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tc_st32u_nowait(tmem + lane_addr + kQCol + 32 * j, &w[32 * j]);
+        tc_wait_st();
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           *reinterpret_cast<uint4*>(smem + kQRopeOff + row * 64 + ((u ^ ((row >> 1) & 3)) << 4)) =
@@ -752,6 +794,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(q_full);
       }
+    };
+    // the next piece's slice of q_lat into L2 while this piece runs
+    auto prefetch_q = [&](const Piece& q) {
+      const char* src = reinterpret_cast<const char*>(
+          p.q_latent + (static_cast<int64_t>(q.b) * p.num_heads + h0 + row) * kRow);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) prefetch_l2(src + kHalf * 2 * v + 128 * u);
+      prefetch_l2(src + (kLat + kRopeHalf * v) * 2);
+    };
+    bool have = it.next(p, pc);
+    if (have) load_q(pc);
+    while (ok && have) {
+      const int64_t bh = static_cast<int64_t>(pc.b) * p.num_heads + h0 + row;
+      PieceIter it_next = it;
+      Piece nx;
+      const bool has_next = it_next.next(p, nx);
+      if (has_next) prefetch_q(nx);
       const int n = pc.te - pc.tb;
       float m_run = -INFINITY, l_run = 0.f;
       for (int t = 0; t < n && ok; ++t) {
@@ -842,6 +901,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       gbase += n;
+      // every score product of this piece is done: the next piece's q_lat
+      // goes in now, ahead of this piece's epilogue
+      if (has_next) load_q(nx);
       // ---- epilogue of the piece: this thread's output row, elements
       // 256v .. 256v + 255; bf16 when the piece is its whole sequence, else an
       // fp32 partial in the piece's slot (and its log2-sum-exp)
@@ -865,14 +927,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 pack_bf16x2(o[8 * u + 4] * inv, o[8 * u + 5] * inv),
                                 pack_bf16x2(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
         } else {
-          // partials are half-major, [slot][half][head][256]: one half's rows
-          // of consecutive heads are contiguous for the merge's bulk copies
-          float4* dst = reinterpret_cast<float4*>(p.ws_o + ((slot * 2 + v) * kHT + row) * kHalf +
-                                                  32 * cq);
+          // partials are column-quad-major, [slot][half][quad][head] of
+          // float4: the warp's 32 rows of one quad are 512 contiguous bytes
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + (slot * 2 + v) * kHT * kHalf) + row;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            dst[u] = make_float4(o[4 * u] * inv, o[4 * u + 1] * inv, o[4 * u + 2] * inv,
-                                 o[4 * u + 3] * inv);
+            dst[(8 * cq + u) * kHT] = make_float4(o[4 * u] * inv, o[4 * u + 1] * inv,
+                                                  o[4 * u + 2] * inv, o[4 * u + 3] * inv);
         }
       }
       if (!whole) {
@@ -906,6 +967,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         ++npart;
       }
+      it = it_next;
+      pc = nx;
+      have = has_next;
     }
     if (!ok) {
       *abort_flag = 1;
@@ -932,11 +996,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // neither CTA leaves while the other may still write into its shared memory
   cluster_sync_all();
   const int nm = sched[6];
-  uint32_t mrg_phase = 0;
+  uint32_t mrg_phase[kMrgBufs] = {};
   for (int i = 0; i < nm; ++i)
     merge_pieces(p, merges[3 * i], ht, v, merges[3 * i + 1], merges[3 * i + 2], chunk,
-                 smem + kStageOff, reinterpret_cast<float*>(smem + kStageOff + kMrgStageBytes),
-                 mrg_full, mrg_phase);
+                 smem + kStageOff, mrg_full, mrg_phase);
 }
 
 }  // namespace

@@ -187,7 +187,8 @@ pa_status pa_concat_and_cache_mla(const void *kv_c, const void *k_pe, pa_dtype s
  *   (see pa_paged_decode_attention_fp8); other dtypes: PA_ERR_UNSUPPORTED.
  * block_tables: [num_seqs, max_blocks_per_seq] int32; context_lens [num_seqs] int32.
  * head_size: 128.  block_size: a power of two in [8, 256].
- * G: 1, 2, 4, 8 or 16.
+ * G: 1, 2, 4, 8 or 16.  num_seqs above 65535: PA_ERR_UNSUPPORTED (one grid
+ * dimension per sequence).
  * max_context_len: host-side upper bound on every context_lens[b]; it sets
  *   the split plan.  Larger lengths are clipped to the plan (and to
  *   max_blocks_per_seq * block_size) and flag PA_DEVERR_CONTEXT_CLIPPED.
@@ -201,10 +202,11 @@ pa_status pa_concat_and_cache_mla(const void *kv_c, const void *k_pe, pa_dtype s
  *
  * The context is split into equal token ranges (a plan computed from
  * num_seqs, num_kv_heads, max_context_len and the SM count); each
- * (range, kv head, sequence) is one CTA that streams its K/V blocks through
- * shared memory, computes the grouped products on the tensor cores and keeps
- * an fp32 online softmax; the last CTA of each (sequence, kv head) merges
- * the ranges by log-sum-exp.  One launch per call.
+ * (kv head, range, sequence) is one CTA, kv heads adjacent in launch order
+ * (the CTAs of one range read the same token rows together), that streams
+ * its K/V blocks through shared memory, computes the grouped products on
+ * the tensor cores and keeps an fp32 online softmax; the last CTA of each
+ * (sequence, kv head) merges the ranges by log-sum-exp.  One launch per call.
  *
  * pa_paged_decode_workspace_size returns the bytes the call above needs
  * (0 for invalid sizes).  It takes num_kv_heads and no block_size: the

@@ -252,8 +252,10 @@ __global__ void __launch_bounds__(kThreads, (kFp8 && NT == 1) ? 4 : TcLayout<kFp
   uint64_t* tile_mask = empty + kStages;
   int* abort_ptr = reinterpret_cast<int*>(tile_mask + kStages);
 
-  const int split = blockIdx.x;
-  const int g = blockIdx.y;
+  // kv heads fastest in launch order: the H_KV CTAs of one (sequence, split)
+  // read the same token rows (each row holds every kv head) at the same time
+  const int g = blockIdx.x;
+  const int split = blockIdx.y;
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -887,6 +889,7 @@ DecodePlan make_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t max_
   int64_t splits = (target + work - 1) / work;
   if (splits < 1) splits = 1;
   if (splits > tiles_max) splits = tiles_max;
+  if (splits > 65535) splits = 65535;  // the grid's y extent
   const int64_t tiles_per_split = (tiles_max + splits - 1) / splits;
   splits = (tiles_max + tiles_per_split - 1) / tiles_per_split;
   return {static_cast<int32_t>(splits), static_cast<int32_t>(tiles_per_split * kTile)};
@@ -956,7 +959,8 @@ pa_status launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.k_cache = const_cast<void*>(a.k_cache);
   p.v_cache = const_cast<void*>(a.v_cache);
 
-  const dim3 grid(static_cast<unsigned>(a.plan.num_splits), static_cast<unsigned>(a.num_kv_heads),
+  if (a.plan.num_splits > 65535 || a.num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  const dim3 grid(static_cast<unsigned>(a.num_kv_heads), static_cast<unsigned>(a.plan.num_splits),
                   static_cast<unsigned>(a.num_seqs));
   pa_status st;
   switch (G) {

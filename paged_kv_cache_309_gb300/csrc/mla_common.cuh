@@ -61,8 +61,13 @@ __device__ __forceinline__ int mla_tile_bid(const MlaParams& p, const int32_t* b
 // Loads of one tile of `tile` tokens (called by one warp, all lanes): lane
 // i < nbox holds the id of block piece i of the tile (mla_tile_bid), the
 // lanes agree on the tile's row mask, lane 0 posts it and the byte count on
-// `full`, and each lane with a valid piece issues one TMA box per 64-element
-// chunk into `stage` (chunk c at stage + c * chunk_bytes, rows of 128 bytes).
+// `full`, and each lane with a valid piece loads its rows into `stage`
+// (chunk c at stage + c * chunk_bytes, rows of 128 bytes).  When a block
+// covers the whole tile (one piece), tm_kv is a 3-D map {64 elements, rows,
+// 9 chunks} and one TMA instruction brings all nine chunks in that layout;
+// otherwise tm_kv is 2-D and each piece takes one box per chunk.  (A TMA
+// instruction costs its issuing warp ~180 cycles here, so nine per tile kept
+// the issuing warp of the mma.sync kernel ~1.6 K cycles from its own work.)
 __device__ __forceinline__ void mla_issue_tile_at(const MlaParams& p, const CUtensorMap* tm_kv,
                                                   uint8_t* stage, int chunk_bytes, int tile,
                                                   uint64_t* full, uint64_t* mask_slot,
@@ -96,9 +101,13 @@ __device__ __forceinline__ void mla_issue_tile_at(const MlaParams& p, const CUte
   if (valid) {
     const int32_t row = bid * bs + row0;
     uint8_t* st = stage + lane * rpb * 128;
+    if (nbox == 1) {
+      tma_load_3d(st, tm_kv, 0, row, 0, full, pol);
+    } else {
 #pragma unroll 1
-    for (int c = 0; c < kChunks; ++c)
-      tma_load_2d(st + c * chunk_bytes, tm_kv, 64 * c, row, full, pol);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_2d(st + c * chunk_bytes, tm_kv, 64 * c, row, full, pol);
+    }
   }
 }
 

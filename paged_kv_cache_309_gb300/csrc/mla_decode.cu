@@ -396,9 +396,8 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
       if (warp == 0 && lane == 0) {
         mbar_arrive_expect_tx(qbar, HT * kRowBytes);
         const uint64_t qpol = l2_policy_evict_normal();
-#pragma unroll 1
-        for (int ch = 0; ch < kChunks; ++ch)
-          tma_load_2d(smem + ch * HT * 128, &tm_q, 64 * ch, b * p.num_heads + h0, qbar, qpol);
+        // one box: 9 chunks x HT rows x 128 bytes (chunk c at smem + c * HT * 128)
+        tma_load_3d(smem, &tm_q, 0, b * p.num_heads + h0, 0, qbar, qpol);
       }
       // all warps agree on whether q_lat arrived (they meet at a barrier
       // every tile, so none may leave alone)
@@ -649,6 +648,24 @@ bool make_row576_map(CUtensorMap* map, const void* base, int64_t rows, int32_t b
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over the same [rows, 576] rows as {64 elements, rows, 9
+// chunks} (strides 1152 and 128 bytes): a box {64, box_rows, 9} lands as
+// nine [box_rows x 128 B] chunk regions one after another, 128-byte
+// swizzled, the layout the 2-D boxes build one chunk at a time.
+bool make_row576_chunked_map(CUtensorMap* map, const void* base, int64_t rows,
+                             int32_t box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(kChunks)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBytes), 128u};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(kChunks)};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The rope half of one CTA of the tcgen05 kernel: 32 elements (64 bytes) of
 // each row, 64-byte swizzled.
 bool make_rope32_map(CUtensorMap* map, const void* base, int64_t rows, int32_t box_rows) {
@@ -706,8 +723,15 @@ pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
   const int tile = ht == 128 ? mla_tc_tile() : ht == 64 ? MlaCfg<64>::kTile : MlaCfg<16>::kTile;
   const int32_t box_rows = a.block_size < tile ? a.block_size : tile;
   CUtensorMap mq, mkv;
-  if (!make_row576_map(&mq, a.q_latent, static_cast<int64_t>(a.num_seqs) * a.num_heads, ht) ||
-      !make_row576_map(&mkv, a.latent_cache, a.num_blocks * a.block_size, box_rows))
+  // mma.sync kernel: q_lat rows and, when a block covers a whole tile, the
+  // latent tiles come as one 3-D box each (all nine 64-element chunks)
+  const bool chunked_kv = ht != 128 && box_rows == tile;
+  const int64_t cache_rows = a.num_blocks * a.block_size;
+  if (!(ht == 128 ? make_row576_map(&mq, a.q_latent, static_cast<int64_t>(a.num_seqs) * a.num_heads, ht)
+                  : make_row576_chunked_map(&mq, a.q_latent,
+                                            static_cast<int64_t>(a.num_seqs) * a.num_heads, ht)) ||
+      !(chunked_kv ? make_row576_chunked_map(&mkv, a.latent_cache, cache_rows, box_rows)
+                   : make_row576_map(&mkv, a.latent_cache, cache_rows, box_rows)))
     return PA_ERR_CUDA;
   MlaParams p;
   p.num_seqs = a.num_seqs;

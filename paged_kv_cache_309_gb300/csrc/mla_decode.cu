@@ -21,13 +21,15 @@
 //    across pieces).  Head tiles of one chunk are adjacent in the launch
 //    order, so the second reads the latent rows from L2.
 //  * the split's tokens stream in tiles of 32 through a TMA ring (3 stages
-//    for 64 heads; for 16 heads 2 stages and two CTAs per SM): per (block piece, 64-element chunk) one [rows x
-//    128 B] box, 128-byte swizzled, completion on an mbarrier; a per-tile
-//    mask marks the rows that exist.  There is no producer warp: every tile
-//    ends in a CTA barrier, after which the previous tile's stage is free,
-//    so warp 0 refills it there (q_lat and the first stages at the start).
-//    Eight warps of 256 threads leave each thread up to 255 registers (64
-//    heads, one CTA per SM) or 128 (16 heads, two CTAs per SM).
+//    for 64 heads; for 16 heads 2 stages and two CTAs per SM), 128-byte
+//    swizzled, completion on an mbarrier; a per-tile mask marks the rows
+//    that exist.  When a block covers the tile it is one 3-D box (all nine
+//    64-element chunks), else one [rows x 128 B] box per (block piece,
+//    chunk).  A ninth warp issues the loads: it refills a stage once all
+//    eight compute warps have arrived on the stage's `empty` barrier after
+//    their P . V of the tile there (warp 0 issued them before, between the
+//    CTA barrier and its own softmax, which every warp then waited for).
+//    Compute warp 0 loads each piece's q_lat (one 3-D box).
 //  * eight warps per tile: (1) S = Q . K^T on the tensor cores
 //    (mma.sync m16n8k16, bf16 in, fp32 accumulate; heads on M, each warp a
 //    16-head x 16-token block over all 576 elements, or for 16 heads a
@@ -63,8 +65,9 @@ namespace {
 using namespace pa;
 using namespace mla;
 
-constexpr int kWarps = 8;                 // all warps compute; warp 0 also issues the loads
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 8;                 // compute warps; warp kWarps issues the tile loads
+constexpr int kComputeThreads = kWarps * 32;
+constexpr int kThreads = kComputeThreads + 32;
 
 template <int HT>
 struct MlaCfg {
@@ -72,6 +75,10 @@ struct MlaCfg {
   static constexpr int kTile = 32;                      // tokens per stage
   static constexpr int kStages = HT == 64 ? 3 : 2;
   static constexpr int kCtasPerSm = HT == 64 ? 1 : 2;  // 16 heads: two CTAs hide each other's barriers
+  // registers per thread of the nine-warp block (measured on GB300: 16 heads
+  // at 96 keep two CTAs per SM, by ncu's occupancy section, without the
+  // spills of 80; 64 heads launch at 168 and not at 200)
+  static constexpr int kMaxRegs = HT == 64 ? 168 : 96;
   static constexpr int kWarpsPerMB = kWarps / kMB;      // 2 or 8
   // S: a 16-head block's warps split the tile's tokens into kTokGroups
   // groups and, for 16 heads, the 576-element reduction into two halves
@@ -87,7 +94,7 @@ struct MlaCfg {
   static constexpr int kStageOff = kQBytes;
   static constexpr int kSOff = kStageOff + kStages * kStageBytes;
   static constexpr int kBarOff = kSOff + 2 * kSBytes;
-  static constexpr int kBytes = kBarOff + (2 * kStages + 1) * 8 + 64;  // full, mask, q, schedule
+  static constexpr int kBytes = kBarOff + (3 * kStages + 1) * 8 + 64;  // full, mask, q, empty, schedule
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kAlloc * kCtasPerSm <= 227 * 1024, "shared memory");
   static_assert(kSTok == 16 || kSTok == 8, "S split");
@@ -222,7 +229,7 @@ __device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int 
 }
 
 template <int HT>
-__global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
+__global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
     mla_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
   using C = MlaCfg<HT>;
@@ -233,7 +240,9 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* tile_mask = full + kStages;
   uint64_t* qbar = tile_mask + kStages;
-  int* sched = reinterpret_cast<int*>(qbar + 1);  // [0..5] schedule, [6] merges, [7..12] their pieces
+  uint64_t* empty = qbar + 1;                       // [kStages] every compute warp is done with a stage
+  int* sched = reinterpret_cast<int*>(empty + kStages);  // [0..5] schedule, [6] merges, [7..12] their pieces, [13] abort
+  volatile int* abort_flag = sched + 13;
 
   const int ht = blockIdx.x;
   const int c = blockIdx.y;    // chunk of the head tile's tile list
@@ -292,11 +301,15 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
       sched[4] = bfirst;
       sched[5] = prefirst;
       sched[6] = 0;  // sequences this CTA merges
+      sched[13] = 0;
     }
   }
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
     mbar_init(qbar, 1);
     mbar_init_fence();
   }
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
   // sequences without tokens: zero output rows (chunk c takes b = c mod NC)
   for (int b = c; b < B; b += NC) {
     if (bal_tiles<kTile>(p, b) != 0) continue;
-    for (int i = threadIdx.x; i < HT * (kLat / 8); i += kThreads) {
+    for (int i = threadIdx.x; i < HT * (kLat / 8); i += blockDim.x) {
       const int h = i / (kLat / 8), e = i % (kLat / 8);
       reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + h0 + h) *
                                            kLat)[e] = make_uint4(0u, 0u, 0u, 0u);
@@ -319,16 +332,18 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
   const uint64_t pol = p.kv_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
   const int ntotal = g1 - g0;  // tiles of this chunk
 
-  // ---- the issuing side (warp 0): tile u of the chunk, across pieces.  The
-  // next tile in issue order is prepared one issue ahead: its position, and
-  // its block ids read from the table (the read's latency then falls in the
-  // compute of a tile, not on warp 0's way to the next CTA barrier)
+  // ---- the issuing side (warp kWarps): tile u of the chunk, across pieces,
+  // into stage u % kStages once every compute warp has finished P.V of tile
+  // u - kStages there (the stage's `empty` barrier).  The next tile is
+  // prepared one issue ahead: its position, and its block ids read from the
+  // table.  (Warp 0 used to issue between the CTA barrier and its own softmax,
+  // ~1 K cycles per tile that every warp then waited for at the next barrier.)
   BalIter<kTile> iti = it0;
   BalPiece pci{};
   int tli = 0, Li = 0;
   const int32_t* bti = nullptr;
   int pre_tok0 = 0, pre_len = 0, pre_bid = -1;
-  auto prepare_next = [&]() {  // warp 0, all lanes
+  auto prepare_next = [&]() {  // issuing warp, all lanes
     if (tli >= pci.te || bti == nullptr) {
       if (!iti.next(p, pci)) return;
       tli = pci.tb;
@@ -341,19 +356,32 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
     pre_bid = mla_tile_bid(p, bti, pre_tok0, Li, kTile, lane);
     ++tli;
   };
-  auto issue_next = [&](int u) {  // warp 0, all lanes: the prepared tile, then prepare the next
+  auto issue_next = [&](int u) {  // issuing warp, all lanes: the prepared tile, then the next
     mla_issue_tile<HT>(p, &tm_kv, smem, full, tile_mask, pre_bid, pre_tok0, pre_len, u % kStages,
                        pol, lane);
     if (u + 1 < ntotal) prepare_next();
   };
   int issued = 0;
-  if (warp == 0) {
-    if (lane == 0) {
-      prefetch_tensormap(&tm_q);
-      prefetch_tensormap(&tm_kv);
-    }
+  if (warp == kWarps) {
+    if (lane == 0) prefetch_tensormap(&tm_kv);
     prepare_next();
-    for (; issued < kStages && issued < ntotal; ++issued) issue_next(issued);
+    bool pok = true;
+    for (; issued < ntotal; ++issued) {
+      if (issued >= kStages) {
+        pok = __all_sync(0xffffffffu,
+                         mbar_wait_bounded(&empty[issued % kStages],
+                                           static_cast<uint32_t>(((issued / kStages) - 1) & 1),
+                                           abort_flag));
+        if (!pok) break;
+      }
+      issue_next(issued);
+    }
+    if (!pok && lane == 0) {
+      *abort_flag = 1;
+      atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+    }
+  } else if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_q);
   }
 
   const int gq = lane >> 2;  // mma groupID
@@ -377,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
   int npiece = 0;  // pieces started (the parity of qbar)
   BalIter<kTile> itc = it0;
   BalPiece pc;
-  while (itc.next(p, pc)) {
+  while (warp < kWarps && itc.next(p, pc)) {  // the compute warps
     const int b = pc.b;
     const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + h0;
     const bool whole = pc.tb == 0 && pc.te == pc.n;
@@ -401,12 +429,12 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
       }
       // all warps agree on whether q_lat arrived (they meet at a barrier
       // every tile, so none may leave alone)
-      ok = named_barrier_and(1, kThreads, mbar_wait_bounded(qbar, npiece & 1, nullptr));
+      ok = named_barrier_and(1, kComputeThreads, mbar_wait_bounded(qbar, npiece & 1, abort_flag));
     }
     ++npiece;
     for (int tl = pc.tb; tl < pc.te && ok; ++tl, ++u) {
       const int stage = u % kStages;
-      const bool w_ok = mbar_wait_bounded(&full[stage], (u / kStages) & 1, nullptr);
+      const bool w_ok = mbar_wait_bounded(&full[stage], (u / kStages) & 1, abort_flag);
       const uint32_t st_base = smem_base + C::kStageOff + stage * C::kStageBytes;
       float* S = s_tile + (u & 1) * (C::kKSplit * HT * C::kSStride);
       uint64_t mask = 0;
@@ -476,13 +504,9 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
       }
       // every warp's scores (and zeroed rows) are in place, and every warp
       // is done with tile u - 1: its stage takes tile u - 1 + kStages
-      if (!named_barrier_and(1, kThreads, w_ok)) {
+      if (!named_barrier_and(1, kComputeThreads, w_ok)) {
         ok = false;
         break;
-      }
-      if (warp == 0 && u >= 1 && issued < ntotal) {
-        issue_next(issued);
-        ++issued;
       }
       // ---- softmax over this warp's 16 heads, then O += P . V.  The score
       // tile is read twice (max, then weights) rather than held in registers.
@@ -554,6 +578,10 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
           mma_bf16_16816(o[2 * np + 1], a, bv[2], bv[3]);
         }
       }
+      // this warp is done with the stage (its scores were read into
+      // registers before the barrier's other side could rewrite them)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
     }
 
     // ---- epilogue of the piece: rows 16mb + gq (+8), elements wi*kDW + 8nt + 2tq (+1)
@@ -587,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
     if (!whole) {
       // count the piece; the CTA that completes the sequence's count merges
       // it after its own work and returns the counter to zero
-      __syncthreads();  // every partial of this piece is written
+      named_barrier_and(1, kComputeThreads, true);  // every partial of this piece is written
       if (threadIdx.x == 0) {
         __threadfence();
         const int c_first = pc.pre / chunk, c_last = (pc.pre + pc.n - 1) / chunk;
@@ -605,18 +633,23 @@ __global__ void __launch_bounds__(kThreads, MlaCfg<HT>::kCtasPerSm)
     }
   }
 
-  if (!ok) {
-    // wait (bounded) for the copies still in flight before leaving
-    if (threadIdx.x == 0) {
-      atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
-      mbar_wait_bounded(qbar, (npiece - 1) & 1, nullptr);
-      for (int t = u; t < issued; ++t)
+  if (!ok && threadIdx.x == 0) {
+    // stop the issuing warp, and wait (bounded) for the q_lat copy in flight
+    *abort_flag = 1;
+    atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+    mbar_wait_bounded(qbar, (npiece - 1) & 1, nullptr);
+  }
+  __syncthreads();
+  if (*abort_flag) {
+    // the tiles issued but not consumed (at most the last kStages) land
+    // before the shared memory is reused or released
+    if (warp == kWarps && lane == 0)
+      for (int t = issued > kStages ? issued - kStages : 0; t < issued; ++t)
         mbar_wait_bounded(&full[t % kStages], (t / kStages) & 1, nullptr);
-    }
+    __syncthreads();
   }
   // ---- merges this CTA completed (at most its first and last piece); the
   // pipeline's shared memory is free now and holds the merge weights
-  __syncthreads();
   const int nmerge = sched[6];
   for (int k = 0; k < nmerge; ++k)
     merge_pieces_cta<HT>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k], chunk,

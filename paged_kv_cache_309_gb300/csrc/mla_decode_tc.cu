@@ -213,14 +213,25 @@ __device__ __forceinline__ void issue_half_tile(const MlaParams& p, const CUtens
 
 // ------------------------------------------------------------- schedule --
 // The work of one 128-head tile is the sequences' 64-token tiles laid end
-// to end in sequence order (T tiles), cut into C contiguous chunks of
-// ceil(T / C) tiles, one per cluster.  Where a chunk crosses a sequence
-// boundary it splits into pieces.  A piece that covers its whole sequence
-// writes bf16 output; the others write an fp32 partial to a slot: 2c for
-// the first piece of cluster c, 2c + 1 for a later one (only a cluster's
-// first and last pieces can be partial), and the CTA that completes a
-// sequence's count merges it.  Every CTA derives the schedule from
-// context_lens itself.
+// to end in sequence order (T tiles), cut into C contiguous chunks, one per
+// cluster, of equal COST: tile t of sequence b sits at cost t + kPieceCost
+// * (b + 1) (every sequence start is charged kPieceCost tiles: a cluster
+// pays for each piece it starts a q_lat load, a pipeline drain and an
+// epilogue), the cost line of length T + kPieceCost * B is cut into C equal
+// parts (min(C, total) parts, so that each part spans at least one cost
+// unit and no cluster inside a sequence's span is empty; the clusters past
+// them get no work), and cluster(t) = floor(cost(t) * C / total) in closed
+// form.  Where
+// a chunk crosses a sequence boundary it splits into pieces.  A piece that
+// covers its whole sequence writes bf16 output; the others write an fp32
+// partial to a slot: 2c for a piece whose sequence began in an earlier
+// cluster, 2c + 1 for one whose sequence begins in cluster c (a cluster has
+// at most one of each), and the CTA that completes a sequence's count
+// merges it.  Every CTA derives the schedule from context_lens itself.
+constexpr int kPieceCost = 4;  // tiles
+__device__ __forceinline__ int bal_cluster(int64_t t, int b, int64_t total, int C) {
+  return static_cast<int>((t + static_cast<int64_t>(kPieceCost) * (b + 1)) * C / total);
+}
 __device__ __forceinline__ int seq_len_eff(const MlaParams& p, int b, bool* clipped) {
   int L = __ldg(p.context_lens + b);
   L = L < 0 ? 0 : L;
@@ -262,7 +273,7 @@ struct PieceIter {
     return true;
   }
 };
-__device__ __forceinline__ int piece_slot(const Piece& pc, int c) { return 2 * c + (pc.first ? 0 : 1); }
+__device__ __forceinline__ int piece_slot(const Piece& pc, int c) { return 2 * c + (pc.tb > 0 ? 0 : 1); }
 
 // Merge of output half v of the 128 heads of (sequence b, head tile ht)
 // over its pieces, by the whole CTA once its own work is done: the pieces
@@ -289,11 +300,12 @@ constexpr int kMrgPairs = (kMrgQuads * kHT + kThreads - 1) / kThreads;  // pairs
 static_assert(kMrgWOff + (2 * kHT + kMrgPieces * kHT) * 4 <= kBarOff,
               "merge staging fits below the barriers");
 __device__ __forceinline__ void merge_pieces(const MlaParams& p, int b, int ht, int v, int pre,
-                                             int n, int chunk, uint8_t* stage, uint64_t* bar,
-                                             uint32_t* phase) {
-  const int c_first = pre / chunk, c_last = (pre + n - 1) / chunk;
+                                             int n, int64_t total, int C, uint8_t* stage,
+                                             uint64_t* bar, uint32_t* phase) {
+  const int c_first = bal_cluster(pre, b, total, C);
+  const int c_last = bal_cluster(pre + n - 1, b, total, C);
   const int np = c_last - c_first + 1;
-  const int s0 = 2 * c_first + (pre != c_first * chunk ? 1 : 0);
+  const int s0 = 2 * c_first + 1;  // the sequence begins in c_first, continues in the others
   auto slot = [&](int i) { return i == 0 ? s0 : 2 * (c_first + i); };
   const int64_t base = static_cast<int64_t>(ht) * p.num_slots;
   const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + ht * kHT;
@@ -455,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* tile_mask = reinterpret_cast<uint64_t*>(smem + kMaskOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* flags = reinterpret_cast<int*>(smem + kMiscOff + 8);  // [0] abort
-  int* sched = reinterpret_cast<int*>(smem + kSchedOff);      // T, chunk, g0, g1, b0, pre0, merges
+  int* sched = reinterpret_cast<int*>(smem + kSchedOff);      // T, -, g0, g1, b0, pre0, merges
   int* merges = sched + 8;                                    // (b, pre, n) per sequence to merge
 
   const int v = static_cast<int>(cluster_rank());  // output half = element slice
@@ -482,14 +494,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (__any_sync(0xffffffffu, any_clip) && c == 0 && ht == 0 && v == 0 && lane == 0)
       atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
-    const int chunk = T > 0 ? (T + C - 1) / C : 1;
-    const int g0 = min(T, c * chunk), g1 = min(T, g0 + chunk);
-    int bfirst = 0, prefirst = 0;
-    if (g0 < g1) {
+    // first tile of cluster k: the smallest t with cost(t) * C >= k * total,
+    // found in the first non-empty sequence whose last tile reaches that
+    // cost (T when none does); also that sequence and its first tile
+    const int64_t total = static_cast<int64_t>(T) + static_cast<int64_t>(kPieceCost) * B;
+    const int Ce = total < C ? static_cast<int>(total) : C;  // parts of the cost line
+    auto cut = [&](int k, int& bk, int& prek) -> int {
+      if (k >= Ce) return T;
+      const int64_t x = (static_cast<int64_t>(k) * total + Ce - 1) / Ce;  // cost(t) >= x
       int pre = 0;
-      bool found = false;
-      for (int b0 = 0; b0 < B && !found; b0 += 32) {
-        const int n = b0 + lane < B ? seq_tiles(p, b0 + lane) : 0;
+      for (int b0 = 0; b0 < B; b0 += 32) {
+        const int bb = b0 + lane;
+        const int n = bb < B ? seq_tiles(p, bb) : 0;
         int incl = n;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -497,19 +513,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (lane >= off) incl += y;
         }
         const int excl = incl - n;
-        const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && pre + excl <= g0 && g0 < pre + incl);
+        const int64_t last = static_cast<int64_t>(pre) + incl - 1 +
+                             static_cast<int64_t>(kPieceCost) * (bb + 1);
+        const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && last >= x);
         if (hit) {
           const int l = __ffs(hit) - 1;
-          bfirst = b0 + l;
-          prefirst = pre + __shfl_sync(0xffffffffu, excl, l);
-          found = true;
+          bk = b0 + l;
+          prek = pre + __shfl_sync(0xffffffffu, excl, l);
+          const int64_t t = x - static_cast<int64_t>(kPieceCost) * (bk + 1);
+          return t > prek ? static_cast<int>(t) : prek;
         }
         pre += __shfl_sync(0xffffffffu, incl, 31);
       }
-    }
+      return T;
+    };
+    int bfirst = 0, prefirst = 0, bnext = 0, prenext = 0;
+    const int g0 = cut(c, bfirst, prefirst);
+    const int g1 = cut(c + 1, bnext, prenext);
     if (lane == 0) {
       sched[0] = T;
-      sched[1] = chunk;
+      sched[1] = 0;
       sched[2] = g0;
       sched[3] = g1;
       sched[4] = bfirst;
@@ -556,7 +579,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* abort_flag = flags;
-  const int chunk = sched[1], g0 = sched[2], g1 = sched[3];
+  const int g0 = sched[2], g1 = sched[3];
+  const int64_t total = static_cast<int64_t>(sched[0]) + static_cast<int64_t>(kPieceCost) * B;
+  const int Ce = total < C ? static_cast<int>(total) : C;  // clusters with work
   const int ntotal = g1 - g0;  // tiles of this cluster
   const PieceIter it0{sched[4], sched[5], g0, g1, false};
   const uint32_t peer = static_cast<uint32_t>(v ^ 1);
@@ -949,7 +974,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
           }
           __threadfence();
-          const int np = (pc.pre + pc.n - 1) / chunk - pc.pre / chunk + 1;
+          const int np = bal_cluster(pc.pre + pc.n - 1, pc.b, total, Ce) -
+                         bal_cluster(pc.pre, pc.b, total, Ce) + 1;
           // one count per output half: the CTA completing half v merges half v
           unsigned* ctr = p.counters + (static_cast<int64_t>(pc.b) * gridDim.y + ht) * 2 + v;
           const unsigned prev = atomicAdd(ctr, 1u);
@@ -998,7 +1024,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int nm = sched[6];
   uint32_t mrg_phase[kMrgBufs] = {};
   for (int i = 0; i < nm; ++i)
-    merge_pieces(p, merges[3 * i], ht, v, merges[3 * i + 1], merges[3 * i + 2], chunk,
+    merge_pieces(p, merges[3 * i], ht, v, merges[3 * i + 1], merges[3 * i + 2], total, Ce,
                  smem + kStageOff, mrg_full, mrg_phase);
 }
 

@@ -113,14 +113,23 @@ __device__ __forceinline__ void mla_issue_tile(const MlaParams& p, const CUtenso
 
 // ------------------------------------------------------------- schedule --
 // The work of one head tile is the sequences' kTile-token tiles laid end to
-// end in sequence order (T tiles), cut into NC contiguous chunks of
-// ceil(T / NC) tiles, one per CTA (one wave of CTAs per head tile).  Where
-// a chunk crosses a sequence boundary it splits into pieces.  A piece that
-// covers its whole sequence writes bf16 output; the others write an fp32
-// partial to a slot: 2c for the first piece of chunk c, 2c + 1 for a later
-// one (only a chunk's first and last pieces can be partial), and the CTA
-// that completes a sequence's count merges it once its own work is done.
-// Every CTA derives the schedule from context_lens itself.
+// end in sequence order (T tiles), cut into NC contiguous chunks, one per
+// CTA (one wave of CTAs per head tile), of equal cost: tile t of sequence b
+// sits at cost t + kPieceCost * (b + 1) (a piece's q_lat load and epilogue
+// are charged to its sequence's start), the cost line of length T +
+// kPieceCost * B is cut into min(NC, that) equal parts (each part spans a
+// cost unit, so no chunk inside a sequence's span is empty), and a tile's
+// chunk is floor(cost * parts / total) in closed form.  Where a chunk
+// crosses a sequence boundary it splits into pieces.  A piece that covers
+// its whole sequence writes bf16 output; the others write an fp32 partial
+// to a slot: 2c for a piece whose sequence began in an earlier chunk, 2c + 1
+// for one whose sequence begins in chunk c (at most one of each), and the
+// CTA that completes a sequence's count merges it once its own work is
+// done.  Every CTA derives the schedule from context_lens itself.
+constexpr int kPieceCost = 2;  // tiles
+__device__ __forceinline__ int bal_chunk(int64_t t, int b, int64_t total, int parts) {
+  return static_cast<int>((t + static_cast<int64_t>(kPieceCost) * (b + 1)) * parts / total);
+}
 __device__ __forceinline__ int bal_len(const MlaParams& p, int b, bool* clipped) {
   int L = __ldg(p.context_lens + b);
   L = L < 0 ? 0 : L;
@@ -166,17 +175,18 @@ struct BalIter {
 };
 
 // Merge of (sequence b, head tile ht) over its pieces by the whole CTA: the
-// pieces are chunks c_first .. c_last, slot of the first 2 c_first (+1 if it
-// is not that chunk's first piece), of the others 2c.  Per head, piece i
+// pieces are chunks c_first .. c_last, slot of the first 2 c_first + 1 (the
+// sequence begins there), of the others 2c.  Per head, piece i
 // gets weight 2^(lse_i - M) / sum_j 2^(lse_j - M); wsm holds HT * np
 // weights.  The partials were written by other CTAs in this launch: read
 // through L2 (__ldcg).
 template <int HT>
 __device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int ht, int pre, int n,
-                                                 int chunk, float* wsm) {
-  const int c_first = pre / chunk, c_last = (pre + n - 1) / chunk;
+                                                 int64_t total, int parts, float* wsm) {
+  const int c_first = bal_chunk(pre, b, total, parts);
+  const int c_last = bal_chunk(pre + n - 1, b, total, parts);
   const int np = c_last - c_first + 1;
-  const int s0 = 2 * c_first + (pre != c_first * chunk ? 1 : 0);
+  const int s0 = 2 * c_first + 1;
   auto slot = [&](int i) { return i == 0 ? s0 : 2 * (c_first + i); };
   const int64_t base = static_cast<int64_t>(ht) * p.num_slots;
   for (int h = threadIdx.x; h < HT; h += blockDim.x) {
@@ -267,14 +277,18 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
     }
     if (__any_sync(0xffffffffu, any_clip) && c == 0 && ht == 0 && lane == 0)
       atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
-    const int chunk = T > 0 ? (T + NC - 1) / NC : 1;
-    const int g0 = min(T, c * chunk), g1 = min(T, g0 + chunk);
-    int bfirst = 0, prefirst = 0;
-    if (g0 < g1) {
+    // first tile of chunk k: the smallest t with cost(t) * parts >= k * total,
+    // in the first non-empty sequence whose last tile reaches that cost (T
+    // when none does); also that sequence and its first tile
+    const int64_t total = static_cast<int64_t>(T) + static_cast<int64_t>(kPieceCost) * B;
+    const int parts = total < NC ? static_cast<int>(total) : NC;
+    auto cut = [&](int k, int& bk, int& prek) -> int {
+      if (k >= parts) return T;
+      const int64_t x = (static_cast<int64_t>(k) * total + parts - 1) / parts;  // cost(t) >= x
       int pre = 0;
-      bool found = false;
-      for (int b0 = 0; b0 < B && !found; b0 += 32) {
-        const int n = b0 + lane < B ? bal_tiles<kTile>(p, b0 + lane) : 0;
+      for (int b0 = 0; b0 < B; b0 += 32) {
+        const int bb = b0 + lane;
+        const int n = bb < B ? bal_tiles<kTile>(p, bb) : 0;
         int incl = n;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -282,20 +296,26 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
           if (lane >= off) incl += y;
         }
         const int excl = incl - n;
-        const uint32_t hit =
-            __ballot_sync(0xffffffffu, n > 0 && pre + excl <= g0 && g0 < pre + incl);
+        const int64_t last = static_cast<int64_t>(pre) + incl - 1 +
+                             static_cast<int64_t>(kPieceCost) * (bb + 1);
+        const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && last >= x);
         if (hit) {
           const int l = __ffs(hit) - 1;
-          bfirst = b0 + l;
-          prefirst = pre + __shfl_sync(0xffffffffu, excl, l);
-          found = true;
+          bk = b0 + l;
+          prek = pre + __shfl_sync(0xffffffffu, excl, l);
+          const int64_t t = x - static_cast<int64_t>(kPieceCost) * (bk + 1);
+          return t > prek ? static_cast<int>(t) : prek;
         }
         pre += __shfl_sync(0xffffffffu, incl, 31);
       }
-    }
+      return T;
+    };
+    int bfirst = 0, prefirst = 0, bnext = 0, prenext = 0;
+    const int g0 = cut(c, bfirst, prefirst);
+    const int g1 = cut(c + 1, bnext, prenext);
     if (lane == 0) {
       sched[0] = T;
-      sched[1] = chunk;
+      sched[1] = 0;
       sched[2] = g0;
       sched[3] = g1;
       sched[4] = bfirst;
@@ -314,7 +334,9 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
     mbar_init_fence();
   }
   __syncthreads();
-  const int chunk = sched[1], g0 = sched[2], g1 = sched[3];
+  const int g0 = sched[2], g1 = sched[3];
+  const int64_t total = static_cast<int64_t>(sched[0]) + static_cast<int64_t>(kPieceCost) * B;
+  const int parts = total < NC ? static_cast<int>(total) : NC;  // chunks with work
   const BalIter<kTile> it0{sched[4], sched[5], g0, g1, false};
 
   // sequences without tokens: zero output rows (chunk c takes b = c mod NC)
@@ -409,7 +431,7 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
     const int b = pc.b;
     const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + h0;
     const bool whole = pc.tb == 0 && pc.te == pc.n;
-    const int slot = 2 * c + (pc.first ? 0 : 1);
+    const int slot = 2 * c + (pc.tb > 0 ? 0 : 1);
     float o[C::kDW / 8][4];
 #pragma unroll
     for (int nt = 0; nt < C::kDW / 8; ++nt)
@@ -618,7 +640,8 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
       named_barrier_and(1, kComputeThreads, true);  // every partial of this piece is written
       if (threadIdx.x == 0) {
         __threadfence();
-        const int c_first = pc.pre / chunk, c_last = (pc.pre + pc.n - 1) / chunk;
+        const int c_first = bal_chunk(pc.pre, b, total, parts);
+        const int c_last = bal_chunk(pc.pre + pc.n - 1, b, total, parts);
         unsigned* ctr = p.counters + static_cast<int64_t>(b) * (p.num_heads / HT) + ht;
         const unsigned prev = atomicAdd(ctr, 1u);
         if (prev + 1u == static_cast<unsigned>(c_last - c_first + 1)) {
@@ -652,7 +675,7 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
   // pipeline's shared memory is free now and holds the merge weights
   const int nmerge = sched[6];
   for (int k = 0; k < nmerge; ++k)
-    merge_pieces_cta<HT>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k], chunk,
+    merge_pieces_cta<HT>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k], total, parts,
                          reinterpret_cast<float*>(smem + C::kStageOff));
 }
 

@@ -189,51 +189,73 @@ __device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int 
   const int s0 = 2 * c_first + 1;
   auto slot = [&](int i) { return i == 0 ? s0 : 2 * (c_first + i); };
   const int64_t base = static_cast<int64_t>(ht) * p.num_slots;
+  // every (head, piece) lse in one round of loads, then the weights per head
+  for (int idx = threadIdx.x; idx < HT * np; idx += blockDim.x) {
+    const int h = idx / np, i = idx - (idx / np) * np;
+    wsm[idx] = __ldcg(p.ws_lse + (base + slot(i)) * HT + h);
+  }
+  __syncthreads();
   for (int h = threadIdx.x; h < HT; h += blockDim.x) {
+    float* wh = wsm + h * np;
     float M = -INFINITY;
-    for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(p.ws_lse + (base + slot(i)) * HT + h));
+    for (int i = 0; i < np; ++i) M = fmaxf(M, wh[i]);
     float W = 0.f;
     for (int i = 0; i < np; ++i) {
-      const float w = M == -INFINITY ? 0.f : exp2f(__ldcg(p.ws_lse + (base + slot(i)) * HT + h) - M);
-      wsm[h * np + i] = w;
+      const float w = M == -INFINITY ? 0.f : exp2f(wh[i] - M);
+      wh[i] = w;
       W += w;
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
-    for (int i = 0; i < np; ++i) wsm[h * np + i] *= inv;
+    for (int i = 0; i < np; ++i) wh[i] *= inv;
   }
   __syncthreads();
   const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + static_cast<int64_t>(ht) * HT;
-  for (int idx = threadIdx.x; idx < HT * (kLat / 4); idx += blockDim.x) {
+  // kU 16-byte columns per thread and two pieces per round in flight (the
+  // loads are L2 round trips; one column at a time left the merge latency-bound)
+  constexpr int kCols = HT * (kLat / 4);
+  constexpr int kU = 4;
+  const int nthr = blockDim.x;
+  auto part = [&](int i, int idx) {
     const int h = idx / (kLat / 4), e4 = idx % (kLat / 4);
-    const float* w = wsm + h * np;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int i = 0;
-    for (; i + 4 <= np; i += 4) {
-      float4 x[4];
+    return __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + slot(i)) * HT + h) * kLat) + e4);
+  };
+  for (int i0 = threadIdx.x; i0 < kCols; i0 += kU * nthr) {
+    float4 acc[kU];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        x[u] = __ldcg(reinterpret_cast<const float4*>(
-                          p.ws_o + ((base + slot(i + u)) * HT + h) * kLat) + e4);
+    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < np; i += 2) {
+      const bool two = i + 1 < np;
+      float4 x0[kU], x1[kU];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float ww = w[i + u];
-        acc.x += ww * x[u].x;
-        acc.y += ww * x[u].y;
-        acc.z += ww * x[u].z;
-        acc.w += ww * x[u].w;
+      for (int u = 0; u < kU; ++u) {
+        const int idx = i0 + u * nthr;
+        if (idx < kCols) {
+          x0[u] = part(i, idx);
+          x1[u] = two ? part(i + 1, idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int idx = i0 + u * nthr;
+        if (idx < kCols) {
+          const float* w = wsm + (idx / (kLat / 4)) * np;
+          const float w0 = w[i], w1 = two ? w[i + 1] : 0.f;
+          acc[u].x += w0 * x0[u].x + w1 * x1[u].x;
+          acc[u].y += w0 * x0[u].y + w1 * x1[u].y;
+          acc[u].z += w0 * x0[u].z + w1 * x1[u].z;
+          acc[u].w += w0 * x0[u].w + w1 * x1[u].w;
+        }
       }
     }
-    for (; i < np; ++i) {
-      const float4 x =
-          __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + slot(i)) * HT + h) * kLat) + e4);
-      const float ww = w[i];
-      acc.x += ww * x.x;
-      acc.y += ww * x.y;
-      acc.z += ww * x.z;
-      acc.w += ww * x.w;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int idx = i0 + u * nthr;
+      if (idx < kCols) {
+        const int h = idx / (kLat / 4), e4 = idx % (kLat / 4);
+        *reinterpret_cast<uint2*>(p.out + (bh0 + h) * kLat + 4 * e4) =
+            make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+      }
     }
-    *reinterpret_cast<uint2*>(p.out + (bh0 + h) * kLat + 4 * e4) =
-        make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
   __syncthreads();  // wsm is free again
 }

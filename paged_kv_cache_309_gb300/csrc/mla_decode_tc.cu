@@ -299,6 +299,60 @@ constexpr int kMrgWOff = kMrgOutOff + kHT * kMrgOutPitch;
 constexpr int kMrgPairs = (kMrgQuads * kHT + kThreads - 1) / kThreads;  // pairs per thread
 static_assert(kMrgWOff + (2 * kHT + kMrgPieces * kHT) * 4 <= kBarOff,
               "merge staging fits below the barriers");
+// Merge of NP pieces by plain coalesced loads straight into registers: R
+// column groups per round, so that R * NP 16-byte loads per (quad, head)
+// pair are in flight per thread (the bulk copies above land at ~30-40 GB/s
+// per SM whatever their number; this keeps ~100 KB of loads in flight).
+// src(j) is piece j's partial half ([quad][head] float4), w its weights.
+template <int NP, int R>
+__device__ __forceinline__ void merge_direct(const MlaParams& p, const float4* const (&src)[NP],
+                                             const float* wb, int64_t bh0, int v,
+                                             uint8_t* otile) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  for (int g0 = 0; g0 < kMrgGroups; g0 += R) {
+    float4 x[R][kMrgPairs][NP];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int u = 0; u < kMrgPairs; ++u) {
+        const int idx = tid + nthr * u;
+#pragma unroll
+        for (int j = 0; j < NP; ++j)
+          if (idx < kMrgQuads * kHT) x[r][u][j] = __ldcg(src[j] + (g0 + r) * kMrgQuads * kHT + idx);
+      }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int g = g0 + r;
+#pragma unroll
+      for (int u = 0; u < kMrgPairs; ++u) {
+        const int idx = tid + nthr * u;
+        if (idx < kMrgQuads * kHT) {
+          const int q = idx / kHT, h = idx % kHT;
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < NP; ++j) {
+            const float w = wb[j * kHT + h];
+            a.x += w * x[r][u][j].x;
+            a.y += w * x[r][u][j].y;
+            a.z += w * x[r][u][j].z;
+            a.w += w * x[r][u][j].w;
+          }
+          *reinterpret_cast<uint2*>(otile + h * kMrgOutPitch + q * 8) =
+              make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+        }
+      }
+      __syncthreads();
+      for (int idx = tid; idx < kHT * (kMrgQuads / 2); idx += nthr) {
+        const int h = idx / (kMrgQuads / 2), c16 = idx % (kMrgQuads / 2);
+        *reinterpret_cast<uint4*>(p.out + (bh0 + h) * kLat + kHalf * v + 4 * kMrgQuads * g +
+                                  8 * c16) =
+            *reinterpret_cast<const uint4*>(otile + h * kMrgOutPitch + 16 * c16);
+      }
+      __syncthreads();
+    }
+  }
+}
+
 __device__ __forceinline__ void merge_pieces(const MlaParams& p, int b, int ht, int v, int pre,
                                              int n, int64_t total, int C, uint8_t* stage,
                                              uint64_t* bar, uint32_t* phase) {
@@ -363,6 +417,19 @@ __device__ __forceinline__ void merge_pieces(const MlaParams& p, int b, int ht, 
   }
   fence_proxy_async_global();  // the partials were written by ordinary stores
   __syncthreads();
+  if (np == 2 || np == 3) {
+    const float4* srcs[3];
+    for (int j = 0; j < np; ++j)
+      srcs[j] = reinterpret_cast<const float4*>(p.ws_o + ((base + slot(j)) * 2 + v) * kHT * kHalf);
+    if (np == 2) {
+      const float4* const s2[2] = {srcs[0], srcs[1]};
+      merge_direct<2, 2>(p, s2, wb, bh0, v, otile);
+    } else {
+      const float4* const s3[3] = {srcs[0], srcs[1], srcs[2]};
+      merge_direct<3, 1>(p, s3, wb, bh0, v, otile);
+    }
+    return;
+  }
   const int nbp = min(np, kMrgPieces);                      // pieces per batch
   const int nbatch = (np + nbp - 1) / nbp;
   const int njobs = kMrgGroups * nbatch;

@@ -82,6 +82,23 @@ def test_mla_head_counts_every_row(H):
         check_attn(got[key], r, ab, key)
 
 
+@pytest.mark.parametrize("H", [16, 128])
+def test_mla_two_and_three_piece_merges(H):
+    """Thirty sequences of 600..700 tokens: each spans two or three chunks
+    of the cost-balanced schedule, so every sequence ends in a merge of two
+    or three pieces (the register-load merge of the tcgen05 kernel); rows of
+    every sequence against the oracle."""
+    rng = np.random.default_rng(77 + H)
+    lens = [int(x) for x in rng.integers(600, 701, size=30)]
+    w = wl.make_mla_decode(f"m23_{H}", 330 + H, 30, 1, 1, H, block_size=64, context_lens=lens,
+                           with_weights=False)
+    got, err = gpu_mla(w)
+    assert err == 0
+    rows = [(b, h) for b in range(30) for h in (0, H // 2 + 3, H - 1)]
+    for key, (r, ab) in oracle_rows(w, rows).items():
+        check_attn(got[key], r, ab, key)
+
+
 @pytest.mark.parametrize("H", [64, 128])
 @pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 256])
 def test_mla_block_sizes_ragged(bs, H):

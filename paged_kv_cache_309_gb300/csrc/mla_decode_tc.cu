@@ -548,16 +548,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- schedule (warp 0): total tiles, this cluster's chunk, its first sequence
   if (warp == 0) {
+    // tiles per sequence: up to 32 * kR sequences in registers (their loads
+    // in flight together), which the two cuts below then read
+    constexpr int kR = 4;
+    const bool in_regs = B <= 32 * kR;
+    int nreg[kR];
     int T = 0;
     bool any_clip = false;
-    for (int b0 = 0; b0 < B; b0 += 32) {
-      int n = 0;
-      if (b0 + lane < B) {
-        bool cl;
-        n = (seq_len_eff(p, b0 + lane, &cl) + kTile - 1) / kTile;
-        any_clip |= cl;
+    if (in_regs) {
+#pragma unroll
+      for (int r = 0; r < kR; ++r) {
+        nreg[r] = 0;
+        if (32 * r + lane < B) {
+          bool cl;
+          nreg[r] = (seq_len_eff(p, 32 * r + lane, &cl) + kTile - 1) / kTile;
+          any_clip |= cl;
+        }
       }
-      T += __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n));
+#pragma unroll
+      for (int r = 0; r < kR; ++r)
+        T += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(nreg[r])));
+    } else {
+      for (int b0 = 0; b0 < B; b0 += 32) {
+        int n = 0;
+        if (b0 + lane < B) {
+          bool cl;
+          n = (seq_len_eff(p, b0 + lane, &cl) + kTile - 1) / kTile;
+          any_clip |= cl;
+        }
+        T += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n)));
+      }
     }
     if (__any_sync(0xffffffffu, any_clip) && c == 0 && ht == 0 && v == 0 && lane == 0)
       atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
@@ -572,7 +592,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int pre = 0;
       for (int b0 = 0; b0 < B; b0 += 32) {
         const int bb = b0 + lane;
-        const int n = bb < B ? seq_tiles(p, bb) : 0;
+        int n = 0;
+        if (in_regs) {
+#pragma unroll
+          for (int r = 0; r < kR; ++r) n = 32 * r == b0 ? nreg[r] : n;  // selects, no local array
+        } else {
+          n = bb < B ? seq_tiles(p, bb) : 0;
+        }
         int incl = n;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -607,7 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       sched[6] = 0;  // sequences this CTA merges
     }
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 64) {  // (warp 0 computes the schedule, warp 1 allocates TMEM)
     mbar_init(q_full, kHT);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kv_full[s], 1);

@@ -14,11 +14,11 @@
 // How (sm_103a):
 //  * grid = (head tile, chunk); a head tile is 64 heads (16 when the head
 //    count is not a multiple of 64), one wave of resident CTAs per head
-//    tile.  Token-balanced schedule: the sequences' 32-token tiles laid end
-//    to end are cut into one equal chunk per CTA, derived by every CTA from
-//    context_lens; a chunk that crosses sequences runs as pieces (q_lat
-//    reloaded per piece, the pipeline's stage and phase counters running on
-//    across pieces).  Head tiles of one chunk are adjacent in the launch
+//    tile.  Balanced schedule: the sequences' 32-token tiles laid end to
+//    end are cut into one chunk of equal cost per CTA (each sequence start
+//    charged 2 tiles), derived by every CTA from context_lens; a chunk that
+//    crosses sequences runs as pieces (q_lat reloaded per piece, the
+//    pipeline's stage and phase counters running on across pieces).  Head tiles of one chunk are adjacent in the launch
 //    order, so the second reads the latent rows from L2.
 //  * the split's tokens stream in tiles of 32 through a TMA ring (3 stages
 //    for 64 heads; for 16 heads 2 stages and two CTAs per SM), 128-byte
@@ -43,7 +43,8 @@
 //    shared-memory tile (V = the first 512 elements of each row).
 //  * epilogue per piece: a piece holding a whole sequence writes bf16 o_lat;
 //    the others write fp32 partials + log2-sum-exp to the chunk's two slots
-//    (its first and its last piece) and count themselves per (sequence,
+//    (a piece whose sequence began in an earlier chunk, one whose sequence
+//    begins in this chunk) and count themselves per (sequence,
 //    head tile); the CTA that completes a count merges that sequence after
 //    its own pieces and zeroes the count.
 //

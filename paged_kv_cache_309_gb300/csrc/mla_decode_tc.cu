@@ -17,10 +17,11 @@
 //    elements 256v .. 256v + 255 (its half of the output) and rope elements
 //    32v .. 32v + 31.
 //  * schedule: the sequences' 64-token tiles, laid end to end, are cut into
-//    one contiguous chunk per cluster (one wave of clusters); a chunk that
-//    crosses sequence boundaries is worked piece by piece, a piece that is
-//    not a whole sequence writes an fp32 partial, and the CTA completing a
-//    sequence's pieces merges them after its own work.
+//    one contiguous chunk of equal cost per cluster (one wave of clusters;
+//    each sequence start is charged 4 tiles); a chunk that crosses sequence
+//    boundaries is worked piece by piece, a piece that is not a whole
+//    sequence writes an fp32 partial, and the CTA completing a sequence's
+//    pieces merges them after its own work.
 //  * CTA v loads only its slice of every latent row (4 latent chunks of 128
 //    bytes, 128-byte swizzled, and its 64 rope bytes, 64-byte swizzled: 576
 //    of the row's 1152 bytes) through a 4-stage TMA ring of 36 KB.  Its

@@ -99,6 +99,24 @@ def test_mla_two_and_three_piece_merges(H):
         check_attn(got[key], r, ab, key)
 
 
+@pytest.mark.parametrize("H", [16, 128])
+def test_mla_many_short_sequences(H):
+    """Two hundred sequences of 1..300 tokens (more than the 128 whose tile
+    counts the tcgen05 kernel's schedule keeps in registers, and more
+    sequences than clusters): sampled rows of every tenth sequence and the
+    last one against the oracle."""
+    rng = np.random.default_rng(91 + H)
+    B = 200
+    lens = [int(x) for x in rng.integers(1, 301, size=B)]
+    w = wl.make_mla_decode(f"many_{H}", 350 + H, B, 1, 1, H, block_size=16, context_lens=lens,
+                           with_weights=False)
+    got, err = gpu_mla(w)
+    assert err == 0
+    rows = [(b, h) for b in list(range(0, B, 10)) + [B - 1] for h in (0, H - 1)]
+    for key, (r, ab) in oracle_rows(w, rows).items():
+        check_attn(got[key], r, ab, key)
+
+
 @pytest.mark.parametrize("H", [64, 128])
 @pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 256])
 def test_mla_block_sizes_ragged(bs, H):

@@ -24,7 +24,7 @@
 //    pieces merges them after its own work.
 //  * CTA v loads only its slice of every latent row (4 latent chunks of 128
 //    bytes, 128-byte swizzled, and its 64 rope bytes, 64-byte swizzled: 576
-//    of the row's 1152 bytes) through a 4-stage TMA ring of 36 KB.  Its
+//    of the row's 1152 bytes) through a 3-stage TMA ring of 36 KB.  Its
 //    slice of q_lat sits in TMEM (latent part, bf16 pairs) and in shared
 //    memory (rope part).
 //  * partial S[128 x 64] over the CTA's 288 elements: 18 tcgen05.mma
@@ -77,7 +77,7 @@ constexpr int kChunkBytes = kTile * 128;             // one 64-element chunk of 
 constexpr int kLatChunks = kHalf / 64;               // 4 latent chunks per CTA
 constexpr int kRopeTileBytes = kTile * kRopeHalf * 2;  // this CTA's 32 rope elements: 4 KB
 constexpr int kStageBytes = kLatChunks * kChunkBytes + kRopeTileBytes;  // 36 KB
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kRecvBytes = kTile * kHT * 4;          // one tile of the peer's partial scores
 constexpr int kQRopeBytes = kHT * kRopeHalf * 2;     // this CTA's rope part of q_lat (64-byte rows)
 constexpr int kStageOff = 0;

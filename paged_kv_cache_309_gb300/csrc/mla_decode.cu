@@ -56,6 +56,7 @@
 #include <cmath>
 
 #include "mla_common.cuh"
+#include "tc_ops.cuh"
 
 namespace pa_detail {
 
@@ -261,6 +262,75 @@ __device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int 
   __syncthreads();  // wsm is free again
 }
 
+// Warp 0 of a CTA (all lanes): the schedule of chunk c of NC, written to
+// sched[0] = T (the head tile's tiles), sched[2..3] = the chunk's tile range
+// [g0, g1), sched[4..5] = the sequence of its first tile and the tiles before
+// that sequence, sched[6] = 0 (merges recorded), sched[13] = 0 (abort flag).
+template <int kTile>
+__device__ __forceinline__ void bal_schedule(const MlaParams& p, int c, int NC, bool report_clip,
+                                             int* sched, int lane) {
+  const int B = p.num_seqs;
+  int T = 0;
+  bool any_clip = false;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    int n = 0;
+    if (b0 + lane < B) {
+      bool cl;
+      n = (bal_len(p, b0 + lane, &cl) + kTile - 1) / kTile;
+      any_clip |= cl;
+    }
+    T += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n)));
+  }
+  if (__any_sync(0xffffffffu, any_clip) && report_clip && lane == 0)
+    atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
+  // first tile of chunk k: the smallest t with cost(t) * parts >= k * total,
+  // in the first non-empty sequence whose last tile reaches that cost (T
+  // when none does); also that sequence and its first tile
+  const int64_t total = static_cast<int64_t>(T) + static_cast<int64_t>(kPieceCost) * B;
+  const int parts = total < NC ? static_cast<int>(total) : NC;
+  auto cut = [&](int k, int& bk, int& prek) -> int {
+    if (k >= parts) return T;
+    const int64_t x = (static_cast<int64_t>(k) * total + parts - 1) / parts;  // cost(t) >= x
+    int pre = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int bb = b0 + lane;
+      const int n = bb < B ? bal_tiles<kTile>(p, bb) : 0;
+      int incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const int excl = incl - n;
+      const int64_t last = static_cast<int64_t>(pre) + incl - 1 +
+                           static_cast<int64_t>(kPieceCost) * (bb + 1);
+      const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && last >= x);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        bk = b0 + l;
+        prek = pre + __shfl_sync(0xffffffffu, excl, l);
+        const int64_t t = x - static_cast<int64_t>(kPieceCost) * (bk + 1);
+        return t > prek ? static_cast<int>(t) : prek;
+      }
+      pre += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return T;
+  };
+  int bfirst = 0, prefirst = 0, bnext = 0, prenext = 0;
+  const int g0 = cut(c, bfirst, prefirst);
+  const int g1 = cut(c + 1, bnext, prenext);
+  if (lane == 0) {
+    sched[0] = T;
+    sched[1] = 0;
+    sched[2] = g0;
+    sched[3] = g1;
+    sched[4] = bfirst;
+    sched[5] = prefirst;
+    sched[6] = 0;  // sequences this CTA merges
+    sched[13] = 0;
+  }
+}
+
 template <int HT>
 __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
     mla_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -286,67 +356,7 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
   const int B = p.num_seqs;
 
   // ---- schedule (warp 0): total tiles, this CTA's chunk, its first sequence
-  if (warp == 0) {
-    int T = 0;
-    bool any_clip = false;
-    for (int b0 = 0; b0 < B; b0 += 32) {
-      int n = 0;
-      if (b0 + lane < B) {
-        bool cl;
-        n = (bal_len(p, b0 + lane, &cl) + kTile - 1) / kTile;
-        any_clip |= cl;
-      }
-      T += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n)));
-    }
-    if (__any_sync(0xffffffffu, any_clip) && c == 0 && ht == 0 && lane == 0)
-      atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
-    // first tile of chunk k: the smallest t with cost(t) * parts >= k * total,
-    // in the first non-empty sequence whose last tile reaches that cost (T
-    // when none does); also that sequence and its first tile
-    const int64_t total = static_cast<int64_t>(T) + static_cast<int64_t>(kPieceCost) * B;
-    const int parts = total < NC ? static_cast<int>(total) : NC;
-    auto cut = [&](int k, int& bk, int& prek) -> int {
-      if (k >= parts) return T;
-      const int64_t x = (static_cast<int64_t>(k) * total + parts - 1) / parts;  // cost(t) >= x
-      int pre = 0;
-      for (int b0 = 0; b0 < B; b0 += 32) {
-        const int bb = b0 + lane;
-        const int n = bb < B ? bal_tiles<kTile>(p, bb) : 0;
-        int incl = n;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += y;
-        }
-        const int excl = incl - n;
-        const int64_t last = static_cast<int64_t>(pre) + incl - 1 +
-                             static_cast<int64_t>(kPieceCost) * (bb + 1);
-        const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && last >= x);
-        if (hit) {
-          const int l = __ffs(hit) - 1;
-          bk = b0 + l;
-          prek = pre + __shfl_sync(0xffffffffu, excl, l);
-          const int64_t t = x - static_cast<int64_t>(kPieceCost) * (bk + 1);
-          return t > prek ? static_cast<int>(t) : prek;
-        }
-        pre += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      return T;
-    };
-    int bfirst = 0, prefirst = 0, bnext = 0, prenext = 0;
-    const int g0 = cut(c, bfirst, prefirst);
-    const int g1 = cut(c + 1, bnext, prenext);
-    if (lane == 0) {
-      sched[0] = T;
-      sched[1] = 0;
-      sched[2] = g0;
-      sched[3] = g1;
-      sched[4] = bfirst;
-      sched[5] = prefirst;
-      sched[6] = 0;  // sequences this CTA merges
-      sched[13] = 0;
-    }
-  }
+  if (warp == 0) bal_schedule<kTile>(p, c, NC, c == 0 && ht == 0, sched, lane);
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
@@ -702,6 +712,682 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
                          reinterpret_cast<float*>(smem + C::kStageOff));
 }
 
+// ------------------------------------------------------------------------
+// Tokens-on-M tcgen05 kernel for 16-head tiles.  With 16 heads, heads on M
+// cannot feed the 5th-generation tensor cores (M is 64 or 128), so both
+// products put the 64 tokens of a tile (or 128 latent elements) on M and the
+// 16 heads on N:
+//   S^T(t)  = K(t) . Q^T      M = 64 tokens, N = 16, K = 576: 36 tcgen05.mma,
+//                             A = the tile's rows (K-major, 128-byte swizzle),
+//                             B = the piece's q_lat rows; into TMEM, where row r
+//                             sits in lane 32 (r / 16) + r % 16
+//   O^T    += V(t)^T . P^T    M = 128 latent elements (four blocks), N = 16,
+//                             K = 64 tokens: 16 tcgen05.mma, A = the same tile
+//                             read MN-major (its 64 elements of a chunk are
+//                             contiguous), B = the bf16 weights written by
+//                             the softmax warps (K-major, [16 heads][64 tokens])
+// A narrow tcgen05.mma costs ~58-60 issue cycles on this part however small
+// it is (measured for M = 64 and 128, N = 16 to 64), so a tile is ~3.1 K
+// cycles of products, about what one SM's share of HBM needs to bring the
+// tile's 72 KB.  The schedule, the partial slots and the merge are those of
+// the mma.sync kernel above, in 64-token tiles and one CTA per SM.
+namespace tok {
+constexpr int HT = 16;
+constexpr int kTile = 64;                           // tokens per tile
+constexpr int kChunkBytes = kTile * 128;            // one 64-element chunk of the tile's rows
+constexpr int kSChunks = 3;                         // chunks per score unit
+constexpr int kSUnitBytes = kSChunks * kChunkBytes; // 24 KB
+constexpr int kSUnits = 5;                          // score-unit ring
+constexpr int kVUnitBytes = 2 * kChunkBytes;        // 16 KB: the 128 latent elements of one output block
+constexpr int kVUnits = 4;                          // value-unit ring
+constexpr int kMasks = 4;                           // row-mask ring (tiles)
+constexpr int kQBytes = kChunks * HT * 128;         // 18 KB: q_lat rows, nine [16 x 128 B] chunks
+constexpr int kPBytes = HT * 128;                   // 2 KB: weights, [16 heads x 64 tokens] bf16
+constexpr int kQOff = 0;                            // two q_lat buffers (pieces alternate)
+constexpr int kPOff = kQOff + 2 * kQBytes;          // two weight buffers (tiles alternate)
+constexpr int kSUOff = kPOff + 2 * kPBytes;
+constexpr int kVUOff = kSUOff + kSUnits * kSUnitBytes;
+constexpr int kScrOff = kVUOff + kVUnits * kVUnitBytes;
+constexpr int kScrBytes = (2 * 4 * HT + 4 * HT) * 4;  // per-quadrant maxima (x 2 tiles), row sums
+constexpr int kBarOff = kScrOff + kScrBytes;
+// su_full, su_empty, vu_full, vu_empty, mask_full, tile_mask, then q_full,
+// q_empty, s_full, s_free, p_full, pv_done, drain (2 each), o_full, o_free
+constexpr int kNumBars = 2 * kSUnits + 2 * kVUnits + 2 * kMasks + 7 * 2 + 2;
+constexpr int kBytes = kBarOff + kNumBars * 8 + 16 + 16 * 4;  // barriers, TMEM slot, schedule
+constexpr int kAlloc = kBytes + 1024;
+static_assert(kQOff % 1024 == 0 && kPOff % 1024 == 0 && kSUOff % 1024 == 0 &&
+                  kVUOff % 1024 == 0 && kQBytes % 1024 == 0 && kSUnitBytes % 1024 == 0 &&
+                  kVUnitBytes % 1024 == 0,
+              "128-byte swizzled operands start on 1 KB boundaries");
+static_assert(kAlloc <= 227 * 1024, "shared memory");
+static_assert(kSChunks * 3 == kChunks, "three score units per tile");
+// warps: 0 score-unit loads, 1 score products (+ TMEM), 2 output products,
+// 3 value-unit loads, 4-11 softmax
+constexpr int kWarps = 12;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSW0 = 4;     // first softmax warp; warp w reads TMEM lane quadrant w % 4
+constexpr int kSWarps = 8;  // softmax warps: two per lane quadrant, eight heads each
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kSCol = 0;   // two 16-column score buffers
+constexpr uint32_t kOCol = 32;  // O^T: four 16-column blocks (latent elements 128 j ..)
+constexpr uint32_t kIdescS = tc::instr_desc(64, HT, false);
+constexpr uint32_t kIdescPV = tc::instr_desc(128, HT, false, true);
+
+// Loads chunks [c0, c0 + nc) of the rows of one tile (tokens tok0 .. of a
+// sequence of tok_end tokens) into dst, chunk c at dst + (c - c0) *
+// kChunkBytes as [64 rows x 128 B], 128-byte swizzled; called by one warp,
+// all lanes.  Lane i < nbox holds the block id of block piece i of the tile
+// (mla_tile_bid).  A block that covers the tile is one 3-D box of nc chunks
+// (tm3, whose box depth is nc), smaller blocks take one 2-D box (tm2) per
+// piece and chunk.  Rows of invalid or missing pieces are not loaded.  When
+// mask is not null, lane 0 stores there the tile's row mask.
+__device__ __forceinline__ void issue_chunks(const MlaParams& p, const CUtensorMap* tm3,
+                                             const CUtensorMap* tm2, uint8_t* dst, int c0, int nc,
+                                             uint64_t* full, int lane_bid, int tok0, int tok_end,
+                                             uint64_t pol, int lane, uint64_t* mask) {
+  const int bs = p.block_size;
+  const int rpb = bs < kTile ? bs : kTile;
+  const int nbox = kTile / rpb;
+  const int nval = min(kTile, tok_end - tok0);
+  bool valid = false;
+  int rows = 0, row0 = 0;
+  if (lane < nbox) {
+    rows = min(rpb, nval - lane * rpb);
+    if (rows > 0) {
+      row0 = (tok0 + lane * rpb) & (bs - 1);
+      valid = lane_bid >= 0 && static_cast<int64_t>(lane_bid) < p.num_blocks;
+    }
+  }
+  if (mask != nullptr) {
+    uint64_t bits = 0;
+    if (valid) bits = (rows >= 64 ? ~0ull : ((1ull << rows) - 1ull)) << (lane * rpb);
+    const uint32_t lo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits));
+    const uint32_t hi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(bits >> 32));
+    if (lane == 0) *mask = (static_cast<uint64_t>(hi) << 32) | lo;
+  }
+  const uint32_t vb = __ballot_sync(0xffffffffu, valid);
+  if (lane == 0) mbar_arrive_expect_tx(full, static_cast<uint32_t>(__popc(vb) * rpb * nc * 128));
+  __syncwarp();
+  if (valid) {
+    const int32_t row = lane_bid * bs + row0;
+    uint8_t* st = dst + lane * rpb * 128;
+    if (nbox == 1) {
+      tma_load_3d(st, tm3, 0, row, c0, full, pol);
+    } else {
+#pragma unroll 1
+      for (int c = 0; c < nc; ++c)
+        tma_load_2d(st + c * kChunkBytes, tm2, 64 * (c0 + c), row, full, pol);
+    }
+  }
+}
+
+// The tile positions of a chunk in order, with the block id of the current
+// tile read one tile ahead (the issuing warps' walk; all lanes).
+struct TileWalk {
+  BalIter<kTile> it;
+  BalPiece pc;
+  int tl, L, bid;
+  const int32_t* bt;
+  bool have, first;  // a current tile; it starts a piece
+  __device__ __forceinline__ bool advance(const MlaParams& p) {
+    first = false;
+    if (bt == nullptr || tl >= pc.te) {
+      if (!it.next(p, pc)) return false;
+      tl = pc.tb;
+      bool cl;
+      L = bal_len(p, pc.b, &cl);
+      bt = p.block_tables + static_cast<int64_t>(pc.b) * p.max_blocks_per_seq;
+      first = true;
+    }
+    return true;
+  }
+  __device__ __forceinline__ void start(const MlaParams& p, const BalIter<kTile>& it0, int lane) {
+    it = it0;
+    bt = nullptr;
+    tl = 0;
+    have = advance(p);
+    bid = have ? mla_tile_bid(p, bt, tl * kTile, L, kTile, lane) : -1;
+  }
+};
+}  // namespace tok
+
+__global__ void __launch_bounds__(tok::kThreads, 1)
+    mla_decode_tok_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_s3,
+                          const __grid_constant__ CUtensorMap tm_v2,
+                          const __grid_constant__ CUtensorMap tm_kv, const MlaParams p) {
+  using namespace tok;
+  using namespace tc;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* su_full = bars;                      // [kSUnits] a score unit landed
+  uint64_t* su_empty = su_full + kSUnits;        // [kSUnits] its score products are done
+  uint64_t* vu_full = su_empty + kSUnits;        // [kVUnits] a value unit landed
+  uint64_t* vu_empty = vu_full + kVUnits;        // [kVUnits] its output products are done
+  uint64_t* mask_full = vu_empty + kVUnits;      // [kMasks] a tile's row mask is written
+  uint64_t* tile_mask = mask_full + kMasks;      // [kMasks] rows of the tile that exist
+  uint64_t* q_full = tile_mask + kMasks;         // [2] a piece's q_lat landed
+  uint64_t* q_empty = q_full + 2;                // [2] that piece's score products are done
+  uint64_t* s_full = q_empty + 2;                // [2] scores of a tile in TMEM
+  uint64_t* s_free = s_full + 2;                 // [2] the softmax warps have read them
+  uint64_t* p_full = s_free + 2;                 // [2] weights of a tile written
+  uint64_t* pv_done = p_full + 2;                // [2] its output products are done
+  uint64_t* drain = pv_done + 2;                 // [2] every product of an issuing thread is done
+  uint64_t* o_full = drain + 2;                  // a piece's output is complete in TMEM
+  uint64_t* o_free = o_full + 1;                 // the epilogue has read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  int* sched = reinterpret_cast<int*>(smem + kBarOff + kNumBars * 8 + 16);
+  volatile int* abort_flag = sched + 13;
+  float* wmax = reinterpret_cast<float*>(smem + kScrOff);  // [2 tiles][4 quadrants][16 heads]
+  float* lsum = wmax + 2 * 4 * HT;                          // [4 quadrants][16 heads]
+
+  const int ht = blockIdx.x;
+  const int c = blockIdx.y;
+  const int NC = gridDim.y;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h0 = ht * HT;
+  const int B = p.num_seqs;
+
+  if (warp == 0) bal_schedule<kTile>(p, c, NC, c == 0 && ht == 0, sched, lane);
+  if (threadIdx.x == 64) {  // not warp 1, which allocates the tensor memory meanwhile
+    for (int s = 0; s < kSUnits; ++s) {
+      mbar_init(&su_full[s], 1);
+      mbar_init(&su_empty[s], 1);
+    }
+    for (int s = 0; s < kVUnits; ++s) {
+      mbar_init(&vu_full[s], 1);
+      mbar_init(&vu_empty[s], 1);
+    }
+    for (int s = 0; s < kMasks; ++s) mbar_init(&mask_full[s], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], kSWarps);
+      mbar_init(&p_full[s], kSWarps);
+      mbar_init(&pv_done[s], 1);
+      mbar_init(&drain[s], 1);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(o_free, kSWarps);
+    mbar_init_fence();
+  }
+  if (warp == 1) {  // this warp owns the CTA's tensor memory
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int g0 = sched[2], g1 = sched[3];
+  const int64_t total = static_cast<int64_t>(sched[0]) + static_cast<int64_t>(kPieceCost) * B;
+  const int parts = total < NC ? static_cast<int>(total) : NC;  // chunks with work
+  const BalIter<kTile> it0{sched[4], sched[5], g0, g1, false};
+  const bool has_work = g0 < g1;
+
+  // sequences without tokens: zero output rows (chunk c takes b = c mod NC)
+  for (int b = c; b < B; b += NC) {
+    if (bal_tiles<kTile>(p, b) != 0) continue;
+    for (int i = threadIdx.x; i < HT * (kLat / 8); i += tok::kThreads) {
+      const int h = i / (kLat / 8), e = i % (kLat / 8);
+      reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * p.num_heads + h0 + h) *
+                                           kLat)[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  int issued = 0, nq = 0;  // units and q_lat rows whose loads this warp issued
+  if ((warp == 0 || warp == 3) && has_work) {
+    // ------------------------------------------------------------ TMA loads
+    // Warp 0: the three score units of each tile (chunks 0-2, 3-5, 6-8; unit
+    // n into ring slot n % kSUnits once the score products of unit n -
+    // kSUnits are done), the tile's row mask with its first unit, and each
+    // piece's q_lat (buffer piece & 1, once the score products of the piece
+    // two before are done).  Warp 3: the four value units of each tile
+    // (chunks 2j, 2j + 1: the 128 latent elements of output block j), read
+    // again from L2 for the output products, unit n into slot n % kVUnits
+    // once the output products of unit n - kVUnits are done.  The block id
+    // of the next tile is read before the waits.
+    const bool is_s = warp == 0;
+    const uint64_t pol = is_s ? l2_policy_evict_normal()
+                              : (p.kv_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal());
+    const uint64_t qpol = l2_policy_evict_normal();
+    if (lane == 0) {
+      prefetch_tensormap(is_s ? &tm_s3 : &tm_v2);
+      prefetch_tensormap(&tm_kv);
+      if (is_s) prefetch_tensormap(&tm_q);
+    }
+    TileWalk w;
+    w.start(p, it0, lane);
+    const int nunits = is_s ? 3 : 4;
+    const int ring = is_s ? kSUnits : kVUnits;
+    uint64_t* full = is_s ? su_full : vu_full;
+    uint64_t* empty = is_s ? su_empty : vu_empty;
+    bool ok = true;
+    int u = 0;
+    while (ok && w.have) {
+      const int b_cur = w.pc.b, tok0 = w.tl * kTile, L_cur = w.L, bid_cur = w.bid;
+      const bool first = w.first;
+      ++w.tl;
+      w.have = w.advance(p);
+      w.bid = w.have ? mla_tile_bid(p, w.bt, w.tl * kTile, w.L, kTile, lane) : -1;
+      if (is_s && first) {
+        if (nq >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&q_empty[nq & 1], ((nq - 2) >> 1) & 1,
+                                                         abort_flag));
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&q_full[nq & 1], HT * kRowBytes);
+          // one box: 9 chunks x 16 rows x 128 bytes
+          tma_load_3d(smem + kQOff + (nq & 1) * kQBytes, &tm_q, 0, b_cur * p.num_heads + h0, 0,
+                      &q_full[nq & 1], qpol);
+        }
+        ++nq;
+      }
+      for (int i = 0; i < nunits && ok; ++i) {
+        const int slot = issued % ring;
+        if (issued >= ring) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[slot], ((issued / ring) - 1) & 1,
+                                                         abort_flag));
+          if (!ok) break;
+        }
+        uint8_t* dst = smem + (is_s ? kSUOff + slot * kSUnitBytes : kVUOff + slot * kVUnitBytes);
+        uint64_t* msk = (is_s && i == 0) ? &tile_mask[u % kMasks] : nullptr;
+        issue_chunks(p, is_s ? &tm_s3 : &tm_v2, &tm_kv, dst, is_s ? kSChunks * i : 2 * i,
+                     is_s ? kSChunks : 2, &full[slot], bid_cur, tok0, L_cur, pol, lane, msk);
+        if (msk != nullptr && lane == 0) mbar_arrive(&mask_full[u % kMasks]);  // after the mask store
+        ++issued;
+      }
+      ++u;
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------ MMA issuers
+    // One thread of warp 1 issues the score products, one of warp 2 the
+    // output products; each commits its own (a commit tracks the issuing
+    // thread's products).
+    if (lane == 0 && has_work) {
+      const bool is_s = warp == 1;
+      const uint32_t su0 = smem_u32(smem + kSUOff);
+      const uint32_t vu0 = smem_u32(smem + kVUOff);
+      const uint32_t q0 = smem_u32(smem + kQOff);
+      const uint32_t p0 = smem_u32(smem + kPOff);
+      BalIter<kTile> it = it0;
+      BalPiece pc;
+      bool ok = true;
+      int u = 0, kp = 0, n = 0;  // tile, piece, unit
+      while (ok && it.next(p, pc)) {
+        if (is_s) {
+          // S^T(u) over the 576 elements, unit by unit: 4 k-steps of 16 per
+          // 64-element chunk (a k-step advances the start by 32 bytes inside
+          // the 128-byte swizzled rows), into score buffer u & 1 once the
+          // softmax has read S^T(u - 2) from it; each unit's slot is released
+          // when its products are done
+          const uint32_t qb = q0 + (kp & 1) * kQBytes;
+          ok = mbar_wait_bounded_long(&q_full[kp & 1], (kp >> 1) & 1, abort_flag);
+          for (int tl = pc.tb; tl < pc.te && ok; ++tl, ++u) {
+            ok = u < 2 || mbar_wait_bounded_long(&s_free[u & 1], ((u - 2) >> 1) & 1, abort_flag);
+            const uint32_t d = tmem + kSCol + HT * (u & 1);
+            for (int i = 0; i < 3 && ok; ++i, ++n) {
+              const int slot = n % kSUnits;
+              ok = mbar_wait_bounded_long(&su_full[slot], (n / kSUnits) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t kb = su0 + slot * kSUnitBytes;
+#pragma unroll
+              for (int j = 0; j < kSChunks * 4; ++j) {
+                const int ch = kSChunks * i + (j >> 2);
+                tc_mma_ss(d, smem_desc(kb + (j >> 2) * kChunkBytes + 32 * (j & 3), 16, 1024),
+                          smem_desc(qb + ch * (HT * 128) + 32 * (j & 3), 16, 1024), kIdescS,
+                          (i > 0 || j > 0) ? 1u : 0u);
+              }
+              tc_commit(&su_empty[slot]);
+            }
+            if (ok) tc_commit(&s_full[u & 1]);
+          }
+          if (ok) tc_commit(&q_empty[kp & 1]);  // this piece's q_lat is no longer read
+        } else {
+          // O^T += V(u)^T . P^T(u): block j (latent elements 128 j ..) reads
+          // value unit 4u + j MN-major (leading offset: the next 64 elements
+          // = the next chunk; stride offset: the next 8 tokens = 1 KB; a
+          // k-step of 16 tokens advances 2 KB).  A piece's first tile starts
+          // the output afresh once the previous piece's epilogue has read it.
+          for (int tl = pc.tb; tl < pc.te && ok; ++tl, ++u) {
+            const bool fresh = tl == pc.tb;
+            ok = mbar_wait_bounded_long(&p_full[u & 1], (u >> 1) & 1, abort_flag) &&
+                 (!fresh || kp == 0 || mbar_wait_bounded_long(o_free, (kp - 1) & 1, abort_flag));
+            const uint32_t pb = p0 + (u & 1) * kPBytes;
+            for (int j = 0; j < kLat / 128 && ok; ++j, ++n) {
+              const int slot = n % kVUnits;
+              ok = mbar_wait_bounded_long(&vu_full[slot], (n / kVUnits) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t vb = vu0 + slot * kVUnitBytes;
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                tc_mma_ss(tmem + kOCol + HT * j, smem_desc(vb + kk * 2048, kChunkBytes, 1024),
+                          smem_desc(pb + 32 * kk, 16, 1024), kIdescPV,
+                          (!fresh || kk > 0) ? 1u : 0u);
+              tc_commit(&vu_empty[slot]);
+            }
+            if (!ok) break;
+            tc_commit(&pv_done[u & 1]);
+            if (tl + 1 == pc.te) tc_commit(o_full);
+          }
+        }
+        ++kp;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+      }
+      // every product issued completes before tensor memory is freed
+      tc_commit(&drain[is_s ? 0 : 1]);
+      mbar_wait_bounded(&drain[is_s ? 0 : 1], 0, nullptr);
+    }
+    __syncwarp();
+  } else if (warp >= kSW0 && has_work) {
+    // ------------------------------------------------------------ softmax
+    // Eight warps: warp w reads TMEM lane quadrant q = w % 4 and takes heads
+    // hs .. hs + 7, hs = 8 ((w - 3) / 4).  For the scores lanes 0-15 of a
+    // quadrant hold tokens 16 q .. 16 q + 15 of the tile; for the output
+    // every lane holds latent element 128 j + 32 q + lane of block j.  Per
+    // tile: the per-head maximum over the tile's tokens (16-lane shuffles,
+    // then the four quadrants' maxima through shared memory and one named
+    // barrier), the lazy rescale of the running maximum (it moves only when
+    // a score beats it by more than 2^8; O^T is then scaled in TMEM once the
+    // previous tile's products are done), the bf16 weights into weight
+    // buffer u & 1, and per-lane partial row sums.  Every named barrier
+    // carries the waits' results, so the eight warps leave together.
+    constexpr int kHW = 8;  // heads per softmax warp
+    const int q = warp & 3;
+    const int hs = kHW * ((warp - kSW0) / 4);
+    const int tok = 16 * q + lane;  // the token whose scores this lane reads (lanes 0-15)
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+    bool ok = true, fail = false;
+    BalIter<kTile> it = it0;
+    BalPiece pc;
+    int u = 0, kp = 0;
+    while (ok && it.next(p, pc)) {
+      const int b = pc.b;
+      const bool whole = pc.tb == 0 && pc.te == pc.n;
+      float m_run[kHW], l_part[kHW];
+#pragma unroll
+      for (int h = 0; h < kHW; ++h) {
+        m_run[h] = -INFINITY;
+        l_part[h] = 0.f;
+      }
+      for (int tl = pc.tb; tl < pc.te; ++tl, ++u) {
+        const int k = u & 1;
+        const bool w_ok = __all_sync(
+            0xffffffffu,
+            mbar_wait_bounded_long(&s_full[k], (u >> 1) & 1, abort_flag) &&
+                mbar_wait_bounded(&mask_full[u % kMasks], (u / kMasks) & 1, abort_flag));
+        float x[kHW];
+        uint64_t mask = 0;
+        if (w_ok) {
+          tc_fence_after();
+          tc_ld8_nowait(tmem + lane_base + kSCol + HT * k + hs, x);
+          tc_wait_ld();
+          mask = tile_mask[u % kMasks];  // read before s_free: the slot is reused 4 tiles on
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[k]);  // the score products of tile u + 2 may go
+        }
+        const bool valid = w_ok && lane < 16 && ((mask >> tok) & 1ull);
+        float mx[kHW];
+#pragma unroll
+        for (int h = 0; h < kHW; ++h) {
+          x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+          mx[h] = x[h];
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1)
+#pragma unroll
+          for (int h = 0; h < kHW; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+        if (lane == 0) {
+          float4* wm = reinterpret_cast<float4*>(wmax + (k * 4 + q) * HT + hs);
+          wm[0] = make_float4(mx[0], mx[1], mx[2], mx[3]);
+          wm[1] = make_float4(mx[4], mx[5], mx[6], mx[7]);
+        }
+        if (!named_barrier_and(1, kSWarps * 32, w_ok && !fail)) {
+          ok = false;
+          break;
+        }
+        float tmax[kHW];
+#pragma unroll
+        for (int h = 0; h < kHW; ++h) tmax[h] = -INFINITY;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const float4* wa = reinterpret_cast<const float4*>(wmax + (k * 4 + qq) * HT + hs);
+          const float4 v0 = wa[0], v1 = wa[1];
+          tmax[0] = fmaxf(tmax[0], v0.x);
+          tmax[1] = fmaxf(tmax[1], v0.y);
+          tmax[2] = fmaxf(tmax[2], v0.z);
+          tmax[3] = fmaxf(tmax[3], v0.w);
+          tmax[4] = fmaxf(tmax[4], v1.x);
+          tmax[5] = fmaxf(tmax[5], v1.y);
+          tmax[6] = fmaxf(tmax[6], v1.z);
+          tmax[7] = fmaxf(tmax[7], v1.w);
+        }
+        bool resc = false;
+        float corr[kHW];
+#pragma unroll
+        for (int h = 0; h < kHW; ++h) {
+          corr[h] = 1.f;
+          if (tmax[h] > m_run[h] + kRescaleLog2) {  // always on a piece's first tile
+            corr[h] = exp2f(m_run[h] - tmax[h]);     // 0 while m_run is -inf
+            m_run[h] = tmax[h];
+            resc = true;
+          }
+        }
+        bool t_ok = true;
+        if (resc) {  // the same on every thread of the warp: the maxima are shared
+#pragma unroll
+          for (int h = 0; h < kHW; ++h) l_part[h] *= corr[h];
+          if (tl != pc.tb) {
+            t_ok = __all_sync(0xffffffffu,
+                              mbar_wait_bounded_long(&pv_done[(u - 1) & 1], ((u - 1) >> 1) & 1,
+                                                     abort_flag));
+            if (t_ok) {
+              tc_fence_after();
+#pragma unroll
+              for (int j = 0; j < kLat / 128; ++j) {
+                float o[kHW];
+                tc_ld8_nowait(tmem + lane_base + kOCol + HT * j + hs, o);
+                tc_wait_ld();
+#pragma unroll
+                for (int h = 0; h < kHW; ++h) o[h] *= corr[h];
+                tc_st8_nowait(tmem + lane_base + kOCol + HT * j + hs, o);
+              }
+              tc_wait_st();
+            }
+          }
+        }
+        float pw[kHW];
+#pragma unroll
+        for (int h = 0; h < kHW; ++h) {
+          // a masked score is -inf and m_run is finite once a token was seen
+          pw[h] = x[h] == -INFINITY ? 0.f : exp2f(x[h] - m_run[h]);
+          l_part[h] += pw[h];
+        }
+        // weight buffer k is free once P.V(u - 2) has read it.  A tile with
+        // rows that hold no token waits for this warp's two value units:
+        // first for P.V(u - 1), which releases the ring's slots to this
+        // tile (until then a unit's barrier may still be a phase behind,
+        // and its parity would read as this tile's), then for the units.
+        const bool partial = mask != ~0ull;  // the same on every lane
+        const int n0 = 4 * u + 2 * (hs / kHW);  // value units of this warp's chunks
+        t_ok = __all_sync(
+            0xffffffffu,
+            t_ok &&
+                (u < 2 ||
+                 mbar_wait_bounded_long(&pv_done[k], ((u - 2) >> 1) & 1, abort_flag)) &&
+                (!partial ||
+                 ((u < 1 || mbar_wait_bounded_long(&pv_done[(u - 1) & 1], ((u - 1) >> 1) & 1,
+                                                   abort_flag)) &&
+                  mbar_wait_bounded_long(&vu_full[n0 % kVUnits], (n0 / kVUnits) & 1, abort_flag) &&
+                  mbar_wait_bounded_long(&vu_full[(n0 + 1) % kVUnits], ((n0 + 1) / kVUnits) & 1,
+                                         abort_flag))));
+        if (t_ok) {
+          if (lane < 16) {
+            // element (head h, token tok) of the K-major 128-byte swizzled
+            // [16 x 128 B] weight tile
+            uint8_t* pb = smem + kPOff + k * kPBytes;
+            const uint32_t unit = static_cast<uint32_t>(tok >> 3);
+            const uint32_t sub = static_cast<uint32_t>(tok & 7) << 1;
+#pragma unroll
+            for (int h = 0; h < kHW; ++h)
+              *reinterpret_cast<__nv_bfloat16*>(pb + (hs + h) * 128 +
+                                                (((unit ^ ((hs + h) & 7)) << 4) | sub)) =
+                  __float2bfloat16_rn(pw[h]);
+            if (!valid) {
+              // a row that holds no token: zero its value part (0 x NaN
+              // would poison the output products); the two warps of a
+              // quadrant take two value units (four chunks) each
+#pragma unroll 1
+              for (int i = 0; i < 2; ++i) {
+                uint8_t* row = smem + kVUOff + ((n0 + i) % kVUnits) * kVUnitBytes + tok * 128;
+                for (int e = 0; e < 16; ++e)
+                  *reinterpret_cast<uint4*>(row + (e >> 3) * kChunkBytes + ((e & 7) << 4)) =
+                      make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+          }
+          fence_proxy_async_smem();  // generic writes before the tensor cores read them
+          tc_fence_before();         // and the rescale's TMEM stores
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_full[k]);
+        } else {
+          fail = true;  // the next named barrier takes all eight warps out
+          if (lane == 0) *abort_flag = 1;
+        }
+      }
+      if (!ok) break;
+
+      // ---- epilogue of the piece: 1 / l per head, then O^T from TMEM
+      const bool e_ok = !fail && __all_sync(0xffffffffu,
+                                            mbar_wait_bounded_long(o_full, kp & 1, abort_flag));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1)
+#pragma unroll
+        for (int h = 0; h < kHW; ++h) l_part[h] += __shfl_xor_sync(0xffffffffu, l_part[h], off);
+      if (lane == 0) {
+        float4* ls = reinterpret_cast<float4*>(lsum + q * HT + hs);
+        ls[0] = make_float4(l_part[0], l_part[1], l_part[2], l_part[3]);
+        ls[1] = make_float4(l_part[4], l_part[5], l_part[6], l_part[7]);
+      }
+      if (!named_barrier_and(1, kSWarps * 32, e_ok)) {
+        ok = false;
+        break;
+      }
+      float lrow[kHW], inv[kHW];
+#pragma unroll
+      for (int h = 0; h < kHW; ++h) {
+        lrow[h] = lsum[hs + h] + lsum[HT + hs + h] + lsum[2 * HT + hs + h] + lsum[3 * HT + hs + h];
+        inv[h] = lrow[h] > 0.f ? 1.f / lrow[h] : 0.f;
+      }
+      tc_fence_after();
+      const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + h0 + hs;
+      const int slot = 2 * c + (pc.tb > 0 ? 0 : 1);
+      const int64_t srow0 = (static_cast<int64_t>(ht) * p.num_slots + slot) * HT + hs;
+#pragma unroll
+      for (int j = 0; j < kLat / 128; ++j) {
+        float o[kHW];
+        tc_ld8_nowait(tmem + lane_base + kOCol + HT * j + hs, o);
+        tc_wait_ld();
+        const int col = 128 * j + 32 * q + lane;
+        if (whole) {
+#pragma unroll
+          for (int h = 0; h < kHW; ++h)
+            p.out[(bh0 + h) * kLat + col] = __float2bfloat16_rn(o[h] * inv[h]);
+        } else {
+#pragma unroll
+          for (int h = 0; h < kHW; ++h) p.ws_o[(srow0 + h) * kLat + col] = o[h] * inv[h];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);  // the next piece's products may overwrite O^T
+      if (!whole) {
+        if (q == 0) {
+#pragma unroll
+          for (int h = 0; h < kHW; ++h)
+            if (lane == h)
+              p.ws_lse[srow0 + h] = lrow[h] > 0.f ? m_run[h] + log2f(lrow[h]) : -INFINITY;
+        }
+        // count the piece; the CTA that completes the sequence's count merges
+        // it after its own work and returns the counter to zero
+        named_barrier_and(1, kSWarps * 32, true);  // every partial of this piece is written
+        if (threadIdx.x == kSW0 * 32) {
+          __threadfence();
+          const int c_first = bal_chunk(pc.pre, b, total, parts);
+          const int c_last = bal_chunk(pc.pre + pc.n - 1, b, total, parts);
+          unsigned* ctr = p.counters + static_cast<int64_t>(b) * (p.num_heads / HT) + ht;
+          const unsigned prev = atomicAdd(ctr, 1u);
+          if (prev + 1u == static_cast<unsigned>(c_last - c_first + 1)) {
+            atomicExch(ctr, 0u);
+            __threadfence();
+            const int m = sched[6]++;
+            sched[7 + 3 * m] = b;
+            sched[8 + 3 * m] = pc.pre;
+            sched[9 + 3 * m] = pc.n;
+          }
+        }
+      }
+      ++kp;
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      atomicOr(p.err, PA_DEVERR_WAIT_TIMEOUT);
+    }
+  }
+
+  // ---- teardown: every role is done and the issuing threads drained their
+  // products; after a timeout the loads in flight land first
+  __syncthreads();
+  if (*abort_flag) {
+    if ((warp == 0 || warp == 3) && lane == 0) {
+      const int ring = warp == 0 ? kSUnits : kVUnits;
+      uint64_t* full = warp == 0 ? su_full : vu_full;
+      for (int t = issued > ring ? issued - ring : 0; t < issued; ++t)
+        mbar_wait_bounded(&full[t % ring], (t / ring) & 1, nullptr);
+      for (int k2 = nq > 2 ? nq - 2 : 0; k2 < nq; ++k2)
+        mbar_wait_bounded(&q_full[k2 & 1], (k2 >> 1) & 1, nullptr);
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  // ---- merges this CTA completed; the rings' shared memory holds the weights
+  const int nmerge = sched[6];
+  for (int k = 0; k < nmerge; ++k)
+    merge_pieces_cta<HT>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k], total, parts,
+                         reinterpret_cast<float*>(smem + kSUOff));
+}
+
+pa_status launch_mla_tok(const CUtensorMap& mq, const CUtensorMap& ms3, const CUtensorMap& mv2,
+                         const CUtensorMap& mkv, const MlaParams& p, dim3 grid,
+                         cudaStream_t stream) {
+  static std::atomic<uint64_t> smem_raised{0};
+  auto kern = mla_decode_tok_kernel;
+  if (!ensure_smem_limit(kern, tok::kAlloc, smem_raised)) return PA_ERR_CUDA;
+  kern<<<grid, tok::kThreads, tok::kAlloc, stream>>>(mq, ms3, mv2, mkv, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 template <int HT>
 pa_status launch_mla_split(const CUtensorMap& mq, const CUtensorMap& mkv, const MlaParams& p,
                            dim3 grid, cudaStream_t stream) {
@@ -728,17 +1414,17 @@ bool make_row576_map(CUtensorMap* map, const void* base, int64_t rows, int32_t b
 }
 
 // 3-D bf16 map over the same [rows, 576] rows as {64 elements, rows, 9
-// chunks} (strides 1152 and 128 bytes): a box {64, box_rows, 9} lands as
-// nine [box_rows x 128 B] chunk regions one after another, 128-byte
-// swizzled, the layout the 2-D boxes build one chunk at a time.
+// chunks} (strides 1152 and 128 bytes): a box {64, box_rows, box_chunks}
+// lands as box_chunks [box_rows x 128 B] chunk regions one after another,
+// 128-byte swizzled, the layout the 2-D boxes build one chunk at a time.
 bool make_row576_chunked_map(CUtensorMap* map, const void* base, int64_t rows,
-                             int32_t box_rows) {
+                             int32_t box_rows, int32_t box_chunks = kChunks) {
   auto enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(kChunks)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBytes), 128u};
   const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows),
-                             static_cast<cuuint32_t>(kChunks)};
+                             static_cast<cuuint32_t>(box_chunks)};
   const cuuint32_t es[3] = {1u, 1u, 1u};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -778,8 +1464,7 @@ DecodePlan make_mla_plan(int32_t num_seqs, int32_t num_heads, int32_t max_contex
   // token tiles (the kernels derive their chunk from context_lens);
   // num_splits = chunks (clusters) per head tile
   const int64_t per_tile = ht == 128 ? (num_sms / 2) / (num_heads / 128)
-                                     : static_cast<int64_t>(ht == 16 ? MlaCfg<16>::kCtasPerSm : 1) *
-                                           num_sms / (num_heads / ht);
+                                     : static_cast<int64_t>(num_sms) / (num_heads / ht);
   return {static_cast<int32_t>(per_tile < 1 ? 1 : per_tile), 0};
 }
 
@@ -799,12 +1484,12 @@ size_t mla_workspace_bytes(int32_t num_seqs, int32_t num_heads, const DecodePlan
 pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0) return PA_OK;
   const int ht = mla_head_tile(a.num_heads);
-  const int tile = ht == 128 ? mla_tc_tile() : ht == 64 ? MlaCfg<64>::kTile : MlaCfg<16>::kTile;
+  const int tile = ht == 128 ? mla_tc_tile() : ht == 64 ? MlaCfg<64>::kTile : tok::kTile;
   const int32_t box_rows = a.block_size < tile ? a.block_size : tile;
   CUtensorMap mq, mkv;
   // mma.sync kernel: q_lat rows and, when a block covers a whole tile, the
   // latent tiles come as one 3-D box each (all nine 64-element chunks)
-  const bool chunked_kv = ht != 128 && box_rows == tile;
+  const bool chunked_kv = ht == 64 && box_rows == tile;
   const int64_t cache_rows = a.num_blocks * a.block_size;
   if (!(ht == 128 ? make_row576_map(&mq, a.q_latent, static_cast<int64_t>(a.num_seqs) * a.num_heads, ht)
                   : make_row576_chunked_map(&mq, a.q_latent,
@@ -848,8 +1533,15 @@ pa_status launch_mla_decode(const MlaDecodeArgs& a, cudaStream_t stream) {
   }
   const dim3 grid(static_cast<unsigned>(a.num_heads / ht), static_cast<unsigned>(a.plan.num_splits),
                   1u);
-  return ht == 64 ? launch_mla_split<64>(mq, mkv, p, grid, stream)
-                  : launch_mla_split<16>(mq, mkv, p, grid, stream);
+  if (ht == 64) return launch_mla_split<64>(mq, mkv, p, grid, stream);
+  // 16-head tiles: score units of three chunks and value units of two, as
+  // 3-D boxes when a block covers a tile (else mkv's 2-D boxes)
+  CUtensorMap ms3 = mkv, mv2 = mkv;
+  if (box_rows == tok::kTile &&
+      (!make_row576_chunked_map(&ms3, a.latent_cache, cache_rows, box_rows, tok::kSChunks) ||
+       !make_row576_chunked_map(&mv2, a.latent_cache, cache_rows, box_rows, 2)))
+    return PA_ERR_CUDA;
+  return launch_mla_tok(mq, ms3, mv2, mkv, p, grid, stream);
 }
 
 }  // namespace pa_detail

@@ -556,8 +556,9 @@ def run_extras(args, dev, peak):
                                         "same_bytes_device_copy_us": round(cmed * 1e3, 2),
                                         "frac_of_same_bytes_copy_rate": round(cmed / med, 4)}
     # MLA decode over the latent cache (DeepSeek-V3-shaped: B=64, context
-    # 512..4096, bs=64): 128 heads (tcgen05 kernel) and 16 heads (one TP8
-    # shard, mma.sync kernel); for 128 heads also the absorbed chain
+    # 512..4096, bs=64): 128 heads (tcgen05 kernel, heads on M) and 16 heads
+    # (one TP8 shard, tcgen05 kernel with tokens on M); for 128 heads also
+    # the absorbed chain
     for H in (128, 16):
         mw = wl.mla_decode(num_heads=H, with_weights=(H == 128))
         mq, mc = up(mw.q_lat, torch.bfloat16, dev), up(mw.latent_cache, torch.bfloat16, dev)
@@ -569,7 +570,8 @@ def run_extras(args, dev, peak):
                                                   mw.max_context_len, mws)
         med, _ = timed_loop(attn, iters, 3, dev)
         nbytes, flops = wl.mla_bytes_read(mw), wl.mla_flops(mw)
-        rec = {"kernel": "tcgen05 2-CTA cluster" if H % 128 == 0 else "mma.sync",
+        rec = {"kernel": "tcgen05 2-CTA cluster" if H % 128 == 0 else
+               ("tcgen05 tokens on M" if H % 64 else "mma.sync"),
                "tokens_attended_per_s": round(int(mw.context_lens.sum()) / (med * 1e-3), 1),
                "GB_per_s": round(nbytes / (med * 1e-3) / 1e9, 2),
                "frac_of_hbm_peak": round(nbytes / (med * 1e-3) / 1e9 / peak, 4),

@@ -11,42 +11,35 @@
 // over the first context_lens[b] logical tokens, read through the block
 // table (nano-vLLM walkthrough, section 2.6).  All heads read the same rows.
 //
-// How (sm_103a):
-//  * grid = (head tile, chunk); a head tile is 64 heads (16 when the head
-//    count is not a multiple of 64), one wave of resident CTAs per head
-//    tile.  Balanced schedule: the sequences' 32-token tiles laid end to
-//    end are cut into one chunk of equal cost per CTA (each sequence start
-//    charged 2 tiles), derived by every CTA from context_lens; a chunk that
-//    crosses sequences runs as pieces (q_lat reloaded per piece, the
-//    pipeline's stage and phase counters running on across pieces).  Head tiles of one chunk are adjacent in the launch
-//    order, so the second reads the latent rows from L2.
-//  * the split's tokens stream in tiles of 32 through a TMA ring (3 stages
-//    for 64 heads; for 16 heads 2 stages and two CTAs per SM), 128-byte
-//    swizzled, completion on an mbarrier; a per-tile mask marks the rows
-//    that exist.  When a block covers the tile it is one 3-D box (all nine
-//    64-element chunks), else one [rows x 128 B] box per (block piece,
-//    chunk).  A ninth warp issues the loads: it refills a stage once all
-//    eight compute warps have arrived on the stage's `empty` barrier after
-//    their P . V of the tile there (warp 0 issued them before, between the
-//    CTA barrier and its own softmax, which every warp then waited for).
-//    Compute warp 0 loads each piece's q_lat (one 3-D box).
-//  * eight warps per tile: (1) S = Q . K^T on the tensor cores
-//    (mma.sync m16n8k16, bf16 in, fp32 accumulate; heads on M, each warp a
-//    16-head x 16-token block over all 576 elements, or for 16 heads a
-//    16 x 8 block over half of them) written to a double-buffered fp32
-//    score tile in shared memory; (2) one barrier;
-//    (3) each warp takes 16 heads x (512 / warps per head block) output
-//    elements: reads its heads' scores straight into the A-fragment
-//    positions, runs an fp32 online softmax in base 2 with a lazy rescale
-//    (the running max moves only when a score beats it by more than 2^8),
-//    rounds the weights to bf16 and accumulates O += P . V from the same
-//    shared-memory tile (V = the first 512 elements of each row).
+// Two kernels here (128-head tiles run on mla_decode_tc.cu): an mma.sync
+// kernel for 64-head tiles and a tcgen05 kernel for 16-head tiles.  Both:
+//  * grid = (head tile, chunk), one wave of resident CTAs per head tile.
+//    Balanced schedule: the sequences' tiles laid end to end are cut into
+//    one chunk of equal cost per CTA (each sequence start charged 2 tiles),
+//    derived by every CTA from context_lens; a chunk that crosses sequences
+//    runs as pieces (q_lat reloaded per piece, the pipeline's counters
+//    running on across pieces).  Head tiles of one chunk are adjacent in the
+//    launch order, so the second reads the latent rows from L2.
+//  * rows come by TMA, 128-byte swizzled, in [rows x 128 B] chunk regions
+//    (a 3-D box of several chunks when a block covers the tile, else one
+//    box per block piece and chunk); a per-tile mask marks the rows that
+//    exist, and rows that hold no token are zeroed before P . V reads them.
 //  * epilogue per piece: a piece holding a whole sequence writes bf16 o_lat;
 //    the others write fp32 partials + log2-sum-exp to the chunk's two slots
 //    (a piece whose sequence began in an earlier chunk, one whose sequence
-//    begins in this chunk) and count themselves per (sequence,
-//    head tile); the CTA that completes a count merges that sequence after
-//    its own pieces and zeroes the count.
+//    begins in this chunk) and count themselves per (sequence, head tile);
+//    the CTA that completes a count merges that sequence after its own
+//    pieces and zeroes the count.
+// The mma.sync kernel (64 heads, 32-token tiles, three 72 KB stages, a
+// ninth warp issuing the loads): eight warps compute S = Q . K^T
+// (m16n8k16, heads on M, 16 heads x 16 tokens per warp) into a
+// double-buffered fp32 score tile in shared memory, meet at one barrier,
+// then each takes 16 heads x 256 output elements: an fp32 online softmax in
+// base 2 with a lazy rescale (the running max moves only when a score beats
+// it by more than 2^8) and O += P . V from the same stage.
+// The tcgen05 kernel (16 heads, 64-token tiles) is described at its
+// definition: tokens on M for both products, score units and value units
+// in separate TMA rings.
 //
 // Every wait is bounded (2 s).  A timeout sets an error bit in the
 // workspace's error word, drains the copies in flight and leaves.
@@ -71,35 +64,33 @@ constexpr int kWarps = 8;                 // compute warps; warp kWarps issues t
 constexpr int kComputeThreads = kWarps * 32;
 constexpr int kThreads = kComputeThreads + 32;
 
+// 64-head tiles (16-head tiles run on the tcgen05 kernel further down)
 template <int HT>
 struct MlaCfg {
+  static_assert(HT == 64, "the mma.sync kernel serves 64-head tiles");
   static constexpr int kMB = HT / 16;                   // 16-head blocks
   static constexpr int kTile = 32;                      // tokens per stage
-  static constexpr int kStages = HT == 64 ? 3 : 2;
-  static constexpr int kCtasPerSm = HT == 64 ? 1 : 2;  // 16 heads: two CTAs hide each other's barriers
-  // registers per thread of the nine-warp block (measured on GB300: 16 heads
-  // at 96 keep two CTAs per SM, by ncu's occupancy section, without the
-  // spills of 80; 64 heads launch at 168 and not at 200)
-  static constexpr int kMaxRegs = HT == 64 ? 168 : 96;
-  static constexpr int kWarpsPerMB = kWarps / kMB;      // 2 or 8
-  // S: a 16-head block's warps split the tile's tokens into kTokGroups
-  // groups and, for 16 heads, the 576-element reduction into two halves
-  static constexpr int kKSplit = HT == 64 ? 1 : 2;
-  static constexpr int kTokGroups = kWarpsPerMB / kKSplit;  // 2 or 4
-  static constexpr int kSTok = kTile / kTokGroups;      // tokens per warp in S: 16 or 8
-  static constexpr int kDW = kLat / kWarpsPerMB;        // output elements per warp: 256 or 64
+  static constexpr int kStages = 3;
+  // registers per thread of the nine-warp block (measured on GB300: launches
+  // at 168 and not at 200)
+  static constexpr int kMaxRegs = 168;
+  static constexpr int kWarpsPerMB = kWarps / kMB;      // 2
+  // S: a 16-head block's warps split the tile's tokens into kTokGroups groups
+  static constexpr int kTokGroups = kWarpsPerMB;
+  static constexpr int kSTok = kTile / kTokGroups;      // tokens per warp in S: 16
+  static constexpr int kDW = kLat / kWarpsPerMB;        // output elements per warp: 256
   static constexpr int kQBytes = kChunks * HT * 128;
   static constexpr int kChunkBytes = kTile * 128;
   static constexpr int kStageBytes = kChunks * kChunkBytes;
   static constexpr int kSStride = kTile + 8;            // floats per score row
-  static constexpr int kSBytes = kKSplit * HT * kSStride * 4;  // one partial per k-half
+  static constexpr int kSBytes = HT * kSStride * 4;
   static constexpr int kStageOff = kQBytes;
   static constexpr int kSOff = kStageOff + kStages * kStageBytes;
   static constexpr int kBarOff = kSOff + 2 * kSBytes;
   static constexpr int kBytes = kBarOff + (3 * kStages + 1) * 8 + 64;  // full, mask, q, empty, schedule
   static constexpr int kAlloc = kBytes + 1024;
-  static_assert(kAlloc * kCtasPerSm <= 227 * 1024, "shared memory");
-  static_assert(kSTok == 16 || kSTok == 8, "S split");
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
+  static_assert(kSTok == 16, "S split");
 };
 
 template <int HT>
@@ -182,7 +173,13 @@ struct BalIter {
 // gets weight 2^(lse_i - M) / sum_j 2^(lse_j - M); wsm holds HT * np
 // weights.  The partials were written by other CTAs in this launch: read
 // through L2 (__ldcg).
-template <int HT>
+//
+// kU 16-byte columns per thread and two pieces per round are in flight (the
+// loads are L2 round trips; one column at a time left the merge latency-
+// bound).  With kEarly, the first round's loads of the first two pieces go
+// out before the weights are computed, so their latency overlaps the lse
+// round (a block of 384 threads and kU = 6 covers 16 heads in one round).
+template <int HT, int kU = 4, bool kEarly = false>
 __device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int ht, int pre, int n,
                                                  int64_t total, int parts, float* wsm) {
   const int c_first = bal_chunk(pre, b, total, parts);
@@ -191,6 +188,26 @@ __device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int 
   const int s0 = 2 * c_first + 1;
   auto slot = [&](int i) { return i == 0 ? s0 : 2 * (c_first + i); };
   const int64_t base = static_cast<int64_t>(ht) * p.num_slots;
+  constexpr int kCols = HT * (kLat / 4);
+  const int nthr = blockDim.x;
+  auto part = [&](int i, int idx) {
+    const int h = idx / (kLat / 4), e4 = idx % (kLat / 4);
+    return __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + slot(i)) * HT + h) * kLat) + e4);
+  };
+  // one or two pieces in one round: the loads go out first
+  const bool early = kEarly && np <= 2 && kCols <= kU * nthr;
+  float4 e0[kEarly ? kU : 1], e1[kEarly ? kU : 1];
+  if (early) {
+#pragma unroll
+    for (int u = 0; u < (kEarly ? kU : 1); ++u) {
+      const int idx = static_cast<int>(threadIdx.x) + u * nthr;
+      e0[u] = e1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (idx < kCols) {
+        e0[u] = part(0, idx);
+        if (np > 1) e1[u] = part(1, idx);
+      }
+    }
+  }
   // every (head, piece) lse in one round of loads, then the weights per head
   for (int idx = threadIdx.x; idx < HT * np; idx += blockDim.x) {
     const int h = idx / np, i = idx - (idx / np) * np;
@@ -212,15 +229,21 @@ __device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int 
   }
   __syncthreads();
   const int64_t bh0 = static_cast<int64_t>(b) * p.num_heads + static_cast<int64_t>(ht) * HT;
-  // kU 16-byte columns per thread and two pieces per round in flight (the
-  // loads are L2 round trips; one column at a time left the merge latency-bound)
-  constexpr int kCols = HT * (kLat / 4);
-  constexpr int kU = 4;
-  const int nthr = blockDim.x;
-  auto part = [&](int i, int idx) {
-    const int h = idx / (kLat / 4), e4 = idx % (kLat / 4);
-    return __ldcg(reinterpret_cast<const float4*>(p.ws_o + ((base + slot(i)) * HT + h) * kLat) + e4);
-  };
+  if (early) {
+#pragma unroll
+    for (int u = 0; u < (kEarly ? kU : 1); ++u) {
+      const int idx = static_cast<int>(threadIdx.x) + u * nthr;
+      if (idx < kCols) {
+        const int h = idx / (kLat / 4), e4 = idx % (kLat / 4);
+        const float w0 = wsm[h * np], w1 = np > 1 ? wsm[h * np + 1] : 0.f;
+        *reinterpret_cast<uint2*>(p.out + (bh0 + h) * kLat + 4 * e4) =
+            make_uint2(pack_bf16x2(w0 * e0[u].x + w1 * e1[u].x, w0 * e0[u].y + w1 * e1[u].y),
+                       pack_bf16x2(w0 * e0[u].z + w1 * e1[u].z, w0 * e0[u].w + w1 * e1[u].w));
+      }
+    }
+    __syncthreads();  // wsm is free again
+    return;
+  }
   for (int i0 = threadIdx.x; i0 < kCols; i0 += kU * nthr) {
     float4 acc[kU];
 #pragma unroll
@@ -270,16 +293,36 @@ template <int kTile>
 __device__ __forceinline__ void bal_schedule(const MlaParams& p, int c, int NC, bool report_clip,
                                              int* sched, int lane) {
   const int B = p.num_seqs;
+  // tiles per sequence: up to 32 * kR sequences in registers (their loads
+  // go out together, and the cuts below read no memory), more read again
+  constexpr int kR = 4;
+  const bool in_regs = B <= 32 * kR;
+  int nreg[kR];
   int T = 0;
   bool any_clip = false;
-  for (int b0 = 0; b0 < B; b0 += 32) {
-    int n = 0;
-    if (b0 + lane < B) {
-      bool cl;
-      n = (bal_len(p, b0 + lane, &cl) + kTile - 1) / kTile;
-      any_clip |= cl;
+  if (in_regs) {
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+      nreg[r] = 0;
+      if (32 * r + lane < B) {
+        bool cl;
+        nreg[r] = (bal_len(p, 32 * r + lane, &cl) + kTile - 1) / kTile;
+        any_clip |= cl;
+      }
     }
-    T += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n)));
+#pragma unroll
+    for (int r = 0; r < kR; ++r)
+      T += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(nreg[r])));
+  } else {
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      int n = 0;
+      if (b0 + lane < B) {
+        bool cl;
+        n = (bal_len(p, b0 + lane, &cl) + kTile - 1) / kTile;
+        any_clip |= cl;
+      }
+      T += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(n)));
+    }
   }
   if (__any_sync(0xffffffffu, any_clip) && report_clip && lane == 0)
     atomicOr(p.err, PA_DEVERR_CONTEXT_CLIPPED);
@@ -294,7 +337,13 @@ __device__ __forceinline__ void bal_schedule(const MlaParams& p, int c, int NC, 
     int pre = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int bb = b0 + lane;
-      const int n = bb < B ? bal_tiles<kTile>(p, bb) : 0;
+      int n = 0;
+      if (in_regs) {
+#pragma unroll
+        for (int r = 0; r < kR; ++r) n = 32 * r == b0 ? nreg[r] : n;  // selects, no local array
+      } else {
+        n = bb < B ? bal_tiles<kTile>(p, bb) : 0;
+      }
       int incl = n;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -446,11 +495,9 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
   // lane-constant parts of the ldmatrix addresses
   const int qrow = 16 * mb + (lane & 15);  // Q: A operand rows
   const int qhalf = lane >> 4;             //    second 8 columns of a k-step
-  const int tg = wi % C::kTokGroups;  // S: token group
-  const int kh = wi / C::kTokGroups;  // S: half of the 576-element reduction
-  const int krow = C::kSTok == 16 ? tg * 16 + (lane & 7) + ((lane >> 4) << 3)
-                                  : tg * 8 + (lane & 7);
-  const int khalf = C::kSTok == 16 ? ((lane >> 3) & 1) : (lane >> 3);
+  const int tg = wi;  // S: token group
+  const int krow = tg * 16 + (lane & 7) + ((lane >> 4) << 3);
+  const int khalf = (lane >> 3) & 1;
   const int vrow_l = (lane & 7) + (((lane >> 3) & 1) << 3);  // V: token within the k-step
   const int vhalf = lane >> 4;                               //    second 8 elements
   float* s_tile = reinterpret_cast<float*>(smem + C::kSOff);
@@ -491,53 +538,38 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
       const int stage = u % kStages;
       const bool w_ok = mbar_wait_bounded(&full[stage], (u / kStages) & 1, abort_flag);
       const uint32_t st_base = smem_base + C::kStageOff + stage * C::kStageBytes;
-      float* S = s_tile + (u & 1) * (C::kKSplit * HT * C::kSStride);
+      float* S = s_tile + (u & 1) * (HT * C::kSStride);
       uint64_t mask = 0;
       if (__all_sync(0xffffffffu, w_ok)) {
         mask = tile_mask[stage];
-        // ---- S = Q . K^T for 16 heads x kSTok tokens over the 576 elements
+        // ---- S = Q . K^T for 16 heads x 16 tokens over the 576 elements
         constexpr int NTS = C::kSTok / 8;
-        float sacc[NTS][4], sacc2[1][4];  // sacc2: a second chain for 8-token blocks
+        float sacc[NTS][4];
 #pragma unroll
         for (int nt = 0; nt < NTS; ++nt)
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) sacc[nt][cc] = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) sacc2[0][cc] = 0.f;
-        constexpr int kSteps = kChunks * 4 / C::kKSplit;  // 16-wide k-steps per warp
+        constexpr int kSteps = kChunks * 4;  // 16-wide k-steps
 #pragma unroll 3
-        for (int kc = kh * kSteps; kc < (kh + 1) * kSteps; kc += 2) {
+        for (int kc = 0; kc < kSteps; kc += 2) {
           const int ch = kc >> 2;
           const int j = kc & 3;  // k-steps j and j + 1 of chunk ch
           const uint32_t qreg = smem_base + ch * HT * 128;
           const uint32_t kreg = st_base + ch * C::kChunkBytes;
-          if constexpr (C::kSTok == 16) {
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              uint32_t a[4], bb[4];
-              ldsm_x4(swz(qreg, qrow, 2 * (j + h2) + qhalf), a);
-              ldsm_x4(swz(kreg, krow, 2 * (j + h2) + khalf), bb);
-              mma_bf16_16816(sacc[0], a, bb[0], bb[1]);
-              mma_bf16_16816(sacc[NTS - 1], a, bb[2], bb[3]);
-            }
-          } else {
-            uint32_t a0[4], a1[4], bb[4];
-            ldsm_x4(swz(qreg, qrow, 2 * j + qhalf), a0);
-            ldsm_x4(swz(qreg, qrow, 2 * j + 2 + qhalf), a1);
-            ldsm_x4(swz(kreg, krow, 2 * j + khalf), bb);
-            mma_bf16_16816(sacc[0], a0, bb[0], bb[1]);
-            mma_bf16_16816(sacc2[0], a1, bb[2], bb[3]);
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t a[4], bb[4];
+            ldsm_x4(swz(qreg, qrow, 2 * (j + h2) + qhalf), a);
+            ldsm_x4(swz(kreg, krow, 2 * (j + h2) + khalf), bb);
+            mma_bf16_16816(sacc[0], a, bb[0], bb[1]);
+            mma_bf16_16816(sacc[NTS - 1], a, bb[2], bb[3]);
           }
         }
 #pragma unroll
         for (int nt = 0; nt < NTS; ++nt) {
           const int col = tg * C::kSTok + nt * 8 + 2 * tq;
-          float* r0 = S + (kh * HT + 16 * mb + gq) * C::kSStride + col;
+          float* r0 = S + (16 * mb + gq) * C::kSStride + col;
           float* r1 = r0 + 8 * C::kSStride;
-          if constexpr (NTS == 1) {
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) sacc[nt][cc] += sacc2[0][cc];
-          }
           *reinterpret_cast<float2*>(r0) = make_float2(sacc[nt][0], sacc[nt][1]);
           *reinterpret_cast<float2*>(r1) = make_float2(sacc[nt][2], sacc[nt][3]);
         }
@@ -570,14 +602,8 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
       // rows gq (r = 0) and gq + 8 (r = 1), columns 2tq, 2tq+1, 2tq+8, 2tq+9
       auto load_scores = [&](int kk, int r, float (&x)[4]) {
         const float* row = S + (16 * mb + gq + 8 * r) * C::kSStride + 16 * kk + 2 * tq;
-        float2 x0 = *reinterpret_cast<const float2*>(row);
-        float2 x1 = *reinterpret_cast<const float2*>(row + 8);
-        if constexpr (C::kKSplit == 2) {  // the other half of the reduction
-          const float2 y0 = *reinterpret_cast<const float2*>(row + HT * C::kSStride);
-          const float2 y1 = *reinterpret_cast<const float2*>(row + HT * C::kSStride + 8);
-          x0 = make_float2(x0.x + y0.x, x0.y + y0.y);
-          x1 = make_float2(x1.x + y1.x, x1.y + y1.y);
-        }
+        const float2 x0 = *reinterpret_cast<const float2*>(row);
+        const float2 x1 = *reinterpret_cast<const float2*>(row + 8);
         const uint32_t bits = static_cast<uint32_t>(mask >> (16 * kk + 2 * tq));
         x[0] = (bits & 1u) ? x0.x * p.scale_log2 : -INFINITY;
         x[1] = (bits & 2u) ? x0.y * p.scale_log2 : -INFINITY;
@@ -722,22 +748,34 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
 //                             B = the piece's q_lat rows; into TMEM, where row r
 //                             sits in lane 32 (r / 16) + r % 16
 //   O^T    += V(t)^T . P^T    M = 128 latent elements (four blocks), N = 16,
-//                             K = 64 tokens: 16 tcgen05.mma, A = the same tile
-//                             read MN-major (its 64 elements of a chunk are
-//                             contiguous), B = the bf16 weights written by
-//                             the softmax warps (K-major, [16 heads][64 tokens])
+//                             K = 64 tokens: 16 tcgen05.mma, A = the value
+//                             part of the tile's rows read MN-major (its 64
+//                             elements of a chunk are contiguous), B = the
+//                             bf16 weights written by the softmax warps
+//                             (K-major, [16 heads][64 tokens])
 // A narrow tcgen05.mma costs ~58-60 issue cycles on this part however small
 // it is (measured for M = 64 and 128, N = 16 to 64), so a tile is ~3.1 K
 // cycles of products, about what one SM's share of HBM needs to bring the
-// tile's 72 KB.  The schedule, the partial slots and the merge are those of
-// the mma.sync kernel above, in 64-token tiles and one CTA per SM.
+// tile's 72 KB.  Holding a tile from its load to its P . V left two 72 KB
+// stages in shared memory and one chain (load, scores, softmax, P . V) per
+// stage.  Instead the rows come twice: score units of three chunks stream
+// through a five-slot ring and are released as soon as their score
+// products are done; the value part (chunks 0-7) is read again, from L2,
+// into a four-slot ring of two-chunk units, one per output block, for the
+// output products.  HBM reads stay at the rows' bytes (measured 1.02x); L2
+// to SM traffic doubles.  Eight softmax warps, two per TMEM lane quadrant,
+// eight heads each.  One CTA per SM.
 namespace tok {
 constexpr int HT = 16;
 constexpr int kTile = 64;                           // tokens per tile
 constexpr int kChunkBytes = kTile * 128;            // one 64-element chunk of the tile's rows
-constexpr int kSChunks = 3;                         // chunks per score unit
+// chunks per score unit: one TMA box each, whose issue costs the loading
+// warp ~180 cycles, so units of one chunk (nine boxes a tile) made that warp
+// the bottleneck (88.8 against 53.0 us)
+constexpr int kSChunks = 3;
 constexpr int kSUnitBytes = kSChunks * kChunkBytes; // 24 KB
 constexpr int kSUnits = 5;                          // score-unit ring
+constexpr int kSPerTile = kChunks / kSChunks;       // score units per tile
 constexpr int kVUnitBytes = 2 * kChunkBytes;        // 16 KB: the 128 latent elements of one output block
 constexpr int kVUnits = 4;                          // value-unit ring
 constexpr int kMasks = 4;                           // row-mask ring (tiles)
@@ -760,7 +798,10 @@ static_assert(kQOff % 1024 == 0 && kPOff % 1024 == 0 && kSUOff % 1024 == 0 &&
                   kVUnitBytes % 1024 == 0,
               "128-byte swizzled operands start on 1 KB boundaries");
 static_assert(kAlloc <= 227 * 1024, "shared memory");
-static_assert(kSChunks * 3 == kChunks, "three score units per tile");
+static_assert(kChunks % kSChunks == 0, "whole score units per tile");
+// a tile whose rows are not all tokens waits, in the softmax, for its own
+// value units before P.V(u) can free any slot: the ring must hold one tile
+static_assert(kVUnits >= 4, "value ring of at least one tile");
 // warps: 0 score-unit loads, 1 score products (+ TMEM), 2 output products,
 // 3 value-unit loads, 4-11 softmax
 constexpr int kWarps = 12;
@@ -811,7 +852,7 @@ __device__ __forceinline__ void issue_chunks(const MlaParams& p, const CUtensorM
   if (valid) {
     const int32_t row = lane_bid * bs + row0;
     uint8_t* st = dst + lane * rpb * 128;
-    if (nbox == 1) {
+    if (nbox == 1 && nc > 1) {
       tma_load_3d(st, tm3, 0, row, c0, full, pol);
     } else {
 #pragma unroll 1
@@ -964,7 +1005,7 @@ __global__ void __launch_bounds__(tok::kThreads, 1)
     }
     TileWalk w;
     w.start(p, it0, lane);
-    const int nunits = is_s ? 3 : 4;
+    const int nunits = is_s ? kSPerTile : 4;
     const int ring = is_s ? kSUnits : kVUnits;
     uint64_t* full = is_s ? su_full : vu_full;
     uint64_t* empty = is_s ? su_empty : vu_empty;
@@ -1037,7 +1078,7 @@ __global__ void __launch_bounds__(tok::kThreads, 1)
           for (int tl = pc.tb; tl < pc.te && ok; ++tl, ++u) {
             ok = u < 2 || mbar_wait_bounded_long(&s_free[u & 1], ((u - 2) >> 1) & 1, abort_flag);
             const uint32_t d = tmem + kSCol + HT * (u & 1);
-            for (int i = 0; i < 3 && ok; ++i, ++n) {
+            for (int i = 0; i < kSPerTile && ok; ++i, ++n) {
               const int slot = n % kSUnits;
               ok = mbar_wait_bounded_long(&su_full[slot], (n / kSUnits) & 1, abort_flag);
               if (!ok) break;
@@ -1374,8 +1415,8 @@ __global__ void __launch_bounds__(tok::kThreads, 1)
   // ---- merges this CTA completed; the rings' shared memory holds the weights
   const int nmerge = sched[6];
   for (int k = 0; k < nmerge; ++k)
-    merge_pieces_cta<HT>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k], total, parts,
-                         reinterpret_cast<float*>(smem + kSUOff));
+    merge_pieces_cta<HT, 6, true>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k],
+                                  total, parts, reinterpret_cast<float*>(smem + kSUOff));
 }
 
 pa_status launch_mla_tok(const CUtensorMap& mq, const CUtensorMap& ms3, const CUtensorMap& mv2,

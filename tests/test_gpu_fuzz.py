@@ -135,9 +135,10 @@ def test_fuzz_latent_write(case):
 
 @pytest.mark.parametrize("case", range(8))
 def test_fuzz_mla_decode(case):
-    """MLA decode over the latent cache on a random shape (the mma.sync
-    kernel for 16/32/48/64 heads, tcgen05 for 128 and 256), a sample of rows
-    of every sequence against the oracle."""
+    """MLA decode over the latent cache on a random shape (the tcgen05
+    tokens-on-M kernel for 16/32/48 heads, mma.sync for 64, tcgen05 with
+    heads on M for 128 and 256), a sample of rows of every sequence against
+    the oracle."""
     rng = np.random.default_rng(6000 + case)
     H = int(rng.choice([16, 32, 48, 64, 128, 256]))
     bs = int(rng.choice([8, 16, 32, 64, 128]))

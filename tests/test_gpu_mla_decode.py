@@ -71,9 +71,9 @@ def all_rows(w):
 
 @pytest.mark.parametrize("H", [16, 32, 48, 64, 128, 256])
 def test_mla_head_counts_every_row(H):
-    """mma.sync head tiles of 16 (H = 16, 32, 48) and 64 (H = 64), tcgen05
-    tiles of 128 (H = 128, 256); ragged contexts including 1 and a partial
-    last tile."""
+    """Head tiles of 16 (H = 16, 32, 48: tcgen05, tokens on M), 64 (H = 64:
+    mma.sync) and 128 (H = 128, 256: tcgen05, heads on M); ragged contexts
+    including 1 and a partial last tile."""
     w = wl.make_mla_decode(f"h{H}", 200 + H, 3, 1, 1, H, block_size=64,
                            context_lens=[1, 97, 300], with_weights=False)
     got, err = gpu_mla(w)

@@ -119,9 +119,12 @@ __device__ __forceinline__ void mla_issue_tile(const MlaParams& p, const CUtenso
 // for one whose sequence begins in chunk c (at most one of each), and the
 // CTA that completes a sequence's count merges it once its own work is
 // done.  Every CTA derives the schedule from context_lens itself.
-constexpr int kPieceCost = 2;  // tiles
+// kPC is the charge per sequence start in tiles: 2 (32-token tiles) for the
+// mma.sync kernel, tok::kPieceCost (64-token tiles) for the tcgen05 kernel.
+constexpr int kPieceCost = 2;  // tiles, the mma.sync kernel
+template <int kPC>
 __device__ __forceinline__ int bal_chunk(int64_t t, int b, int64_t total, int parts) {
-  return static_cast<int>((t + static_cast<int64_t>(kPieceCost) * (b + 1)) * parts / total);
+  return static_cast<int>((t + static_cast<int64_t>(kPC) * (b + 1)) * parts / total);
 }
 __device__ __forceinline__ int bal_len(const MlaParams& p, int b, bool* clipped) {
   int L = __ldg(p.context_lens + b);
@@ -179,11 +182,11 @@ struct BalIter {
 // bound).  With kEarly, the first round's loads of the first two pieces go
 // out before the weights are computed, so their latency overlaps the lse
 // round (a block of 384 threads and kU = 6 covers 16 heads in one round).
-template <int HT, int kU = 4, bool kEarly = false>
+template <int HT, int kPC, int kU = 4, bool kEarly = false>
 __device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int ht, int pre, int n,
                                                  int64_t total, int parts, float* wsm) {
-  const int c_first = bal_chunk(pre, b, total, parts);
-  const int c_last = bal_chunk(pre + n - 1, b, total, parts);
+  const int c_first = bal_chunk<kPC>(pre, b, total, parts);
+  const int c_last = bal_chunk<kPC>(pre + n - 1, b, total, parts);
   const int np = c_last - c_first + 1;
   const int s0 = 2 * c_first + 1;
   auto slot = [&](int i) { return i == 0 ? s0 : 2 * (c_first + i); };
@@ -289,7 +292,7 @@ __device__ __forceinline__ void merge_pieces_cta(const MlaParams& p, int b, int 
 // sched[0] = T (the head tile's tiles), sched[2..3] = the chunk's tile range
 // [g0, g1), sched[4..5] = the sequence of its first tile and the tiles before
 // that sequence, sched[6] = 0 (merges recorded), sched[13] = 0 (abort flag).
-template <int kTile>
+template <int kTile, int kPC>
 __device__ __forceinline__ void bal_schedule(const MlaParams& p, int c, int NC, bool report_clip,
                                              int* sched, int lane) {
   const int B = p.num_seqs;
@@ -329,7 +332,7 @@ __device__ __forceinline__ void bal_schedule(const MlaParams& p, int c, int NC, 
   // first tile of chunk k: the smallest t with cost(t) * parts >= k * total,
   // in the first non-empty sequence whose last tile reaches that cost (T
   // when none does); also that sequence and its first tile
-  const int64_t total = static_cast<int64_t>(T) + static_cast<int64_t>(kPieceCost) * B;
+  const int64_t total = static_cast<int64_t>(T) + static_cast<int64_t>(kPC) * B;
   const int parts = total < NC ? static_cast<int>(total) : NC;
   auto cut = [&](int k, int& bk, int& prek) -> int {
     if (k >= parts) return T;
@@ -352,13 +355,13 @@ __device__ __forceinline__ void bal_schedule(const MlaParams& p, int c, int NC, 
       }
       const int excl = incl - n;
       const int64_t last = static_cast<int64_t>(pre) + incl - 1 +
-                           static_cast<int64_t>(kPieceCost) * (bb + 1);
+                           static_cast<int64_t>(kPC) * (bb + 1);
       const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && last >= x);
       if (hit) {
         const int l = __ffs(hit) - 1;
         bk = b0 + l;
         prek = pre + __shfl_sync(0xffffffffu, excl, l);
-        const int64_t t = x - static_cast<int64_t>(kPieceCost) * (bk + 1);
+        const int64_t t = x - static_cast<int64_t>(kPC) * (bk + 1);
         return t > prek ? static_cast<int>(t) : prek;
       }
       pre += __shfl_sync(0xffffffffu, incl, 31);
@@ -405,7 +408,7 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
   const int B = p.num_seqs;
 
   // ---- schedule (warp 0): total tiles, this CTA's chunk, its first sequence
-  if (warp == 0) bal_schedule<kTile>(p, c, NC, c == 0 && ht == 0, sched, lane);
+  if (warp == 0) bal_schedule<kTile, kPieceCost>(p, c, NC, c == 0 && ht == 0, sched, lane);
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) {
@@ -699,8 +702,8 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
       named_barrier_and(1, kComputeThreads, true);  // every partial of this piece is written
       if (threadIdx.x == 0) {
         __threadfence();
-        const int c_first = bal_chunk(pc.pre, b, total, parts);
-        const int c_last = bal_chunk(pc.pre + pc.n - 1, b, total, parts);
+        const int c_first = bal_chunk<kPieceCost>(pc.pre, b, total, parts);
+        const int c_last = bal_chunk<kPieceCost>(pc.pre + pc.n - 1, b, total, parts);
         unsigned* ctr = p.counters + static_cast<int64_t>(b) * (p.num_heads / HT) + ht;
         const unsigned prev = atomicAdd(ctr, 1u);
         if (prev + 1u == static_cast<unsigned>(c_last - c_first + 1)) {
@@ -734,7 +737,7 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
   // pipeline's shared memory is free now and holds the merge weights
   const int nmerge = sched[6];
   for (int k = 0; k < nmerge; ++k)
-    merge_pieces_cta<HT>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k], total, parts,
+    merge_pieces_cta<HT, kPieceCost>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k], total, parts,
                          reinterpret_cast<float*>(smem + C::kStageOff));
 }
 
@@ -768,6 +771,9 @@ __global__ void __maxnreg__(MlaCfg<HT>::kMaxRegs)
 namespace tok {
 constexpr int HT = 16;
 constexpr int kTile = 64;                           // tokens per tile
+// charge per sequence start, in tiles, of the balanced cut (launch, back to
+// back: 53.9 / 53.1 / 52.0 / 53.8 / 54.1 us with 1 / 2 / 3 / 4 / 5)
+constexpr int kPieceCost = 3;
 constexpr int kChunkBytes = kTile * 128;            // one 64-element chunk of the tile's rows
 // chunks per score unit: one TMA box each, whose issue costs the loading
 // warp ~180 cycles, so units of one chunk (nine boxes a tile) made that warp
@@ -931,7 +937,7 @@ __global__ void __launch_bounds__(tok::kThreads, 1)
   const int h0 = ht * HT;
   const int B = p.num_seqs;
 
-  if (warp == 0) bal_schedule<kTile>(p, c, NC, c == 0 && ht == 0, sched, lane);
+  if (warp == 0) bal_schedule<kTile, tok::kPieceCost>(p, c, NC, c == 0 && ht == 0, sched, lane);
   if (threadIdx.x == 64) {  // not warp 1, which allocates the tensor memory meanwhile
     for (int s = 0; s < kSUnits; ++s) {
       mbar_init(&su_full[s], 1);
@@ -967,7 +973,7 @@ __global__ void __launch_bounds__(tok::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int g0 = sched[2], g1 = sched[3];
-  const int64_t total = static_cast<int64_t>(sched[0]) + static_cast<int64_t>(kPieceCost) * B;
+  const int64_t total = static_cast<int64_t>(sched[0]) + static_cast<int64_t>(tok::kPieceCost) * B;
   const int parts = total < NC ? static_cast<int>(total) : NC;  // chunks with work
   const BalIter<kTile> it0{sched[4], sched[5], g0, g1, false};
   const bool has_work = g0 < g1;
@@ -1371,8 +1377,8 @@ __global__ void __launch_bounds__(tok::kThreads, 1)
         named_barrier_and(1, kSWarps * 32, true);  // every partial of this piece is written
         if (threadIdx.x == kSW0 * 32) {
           __threadfence();
-          const int c_first = bal_chunk(pc.pre, b, total, parts);
-          const int c_last = bal_chunk(pc.pre + pc.n - 1, b, total, parts);
+          const int c_first = bal_chunk<tok::kPieceCost>(pc.pre, b, total, parts);
+          const int c_last = bal_chunk<tok::kPieceCost>(pc.pre + pc.n - 1, b, total, parts);
           unsigned* ctr = p.counters + static_cast<int64_t>(b) * (p.num_heads / HT) + ht;
           const unsigned prev = atomicAdd(ctr, 1u);
           if (prev + 1u == static_cast<unsigned>(c_last - c_first + 1)) {
@@ -1415,7 +1421,7 @@ __global__ void __launch_bounds__(tok::kThreads, 1)
   // ---- merges this CTA completed; the rings' shared memory holds the weights
   const int nmerge = sched[6];
   for (int k = 0; k < nmerge; ++k)
-    merge_pieces_cta<HT, 6, true>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k],
+    merge_pieces_cta<HT, tok::kPieceCost, 6, true>(p, sched[7 + 3 * k], ht, sched[8 + 3 * k], sched[9 + 3 * k],
                                   total, parts, reinterpret_cast<float*>(smem + kSUOff));
 }
 

@@ -117,15 +117,18 @@ def test_mla_many_short_sequences(H):
         check_attn(got[key], r, ab, key)
 
 
-@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("H", [16, 48, 64, 128])
 @pytest.mark.parametrize("bs", [8, 16, 32, 64, 128, 256])
 def test_mla_block_sizes_ragged(bs, H):
+    """Every block size on each kernel: many boxes per tile (bs < 64), one
+    box at a row offset inside the block (bs > 64), an empty sequence, one
+    token, a tile edge and a partial last tile."""
     w = wl.make_mla_decode(f"bs{bs}", 210 + bs, 5, 1, 1, H, block_size=bs,
                            context_lens=[0, 1, 64, 65, 531], with_weights=False)
     got, err = gpu_mla(w, max_context_len=600)
     assert err == 0
     assert (got[0] == 0).all()
-    rows = [(b, h) for b in range(1, 5) for h in (0, 17, H - 1)]
+    rows = [(b, h) for b in range(1, 5) for h in sorted({0, min(17, H - 1), H - 1})]
     for key, (r, ab) in oracle_rows(w, rows).items():
         check_attn(got[key], r, ab, key)
 

@@ -11,6 +11,11 @@
 // activations), read once per 64 sequences, so the kernels are built to keep
 // the most weight bytes in flight.
 //
+// mla_head_gemm_tc_kernel (the benchmark shapes: d_h = d_v = 128, d_c =
+// 512, up to 64 sequences): both products on tcgen05, described at its
+// definition.  With L2 flushed, B = 64, 128 heads: absorb 13.8 -> 12.4 us,
+// project 12.4 -> 10.7 us against the two kernels below.
+//
 // mla_head_gemm_tma_kernel (K = 128, N a multiple of 128: the absorb
 // product at d_h = 128): a CTA owns 64 rows (sequences) of one head and 128
 // output columns over the whole reduction.  One thread issues every load of
@@ -39,6 +44,7 @@
 #include <atomic>
 
 #include "pa_internal.cuh"
+#include "tc_ops.cuh"
 
 namespace pa_detail {
 
@@ -364,13 +370,222 @@ __global__ void __launch_bounds__(kThreads) mla_head_gemm_tma_kernel(
   }
 }
 
-// 2-D map over w [rows, cols] bf16, 64 x 64 boxes, 128-byte swizzle.
-bool make_weight_map(CUtensorMap* map, const void* w, int64_t rows, int64_t cols) {
+// ------------------------------------------------------------ tcgen05 path --
+// The two products of the benchmark shapes (d_h = d_v = 128, d_c = 512, up to
+// 64 sequences) on the 5th-generation tensor cores, with the head's outputs
+// on M and the sequences on N (N = 64, rows past M read as zero):
+//   absorb:  D[c, b] = sum_i W_UK[c, h*128 + i] X[b, h, i]  A = the weight
+//            rows (K-major: i is contiguous), B = q_nope rows; a CTA owns one
+//            head and half of the 512 outputs (two M blocks of 128): 64 KB of
+//            weights + 16 KB of q_nope, two CTAs per SM, 256 CTAs;
+//   project: D[i, b] = sum_c W_UV[c, h*128 + i] X[b, h, c]  A = the weight
+//            read MN-major (i is contiguous within a row c), B = o_lat rows;
+//            a CTA owns one head: 128 KB of weights + 64 KB of o_lat, 128 CTAs.
+// Every load of the CTA is issued up front by one thread (128-byte swizzled
+// TMA boxes on a few mbarriers), one thread issues the products as their
+// operands land, and the four warps read D from TMEM (lane = output, column
+// = sequence), stage it as bf16 rows in shared memory and store whole rows.
+namespace tcp {
+constexpr int kB = 64;                 // sequences per CTA: N of the products
+constexpr int kWBox = 128 * 128;       // a weight box: 128 rows x 64 elements (16 KB)
+constexpr int kXBox = kB * 128;        // an activation box: 64 rows x 64 elements (8 KB)
+// absorb: weight boxes [M block j][K half kh], then the two q_nope halves
+constexpr int kAbsW = 4 * kWBox, kAbsX = 2 * kXBox;
+constexpr int kAbsSmem = kAbsW + kAbsX + 1024 + 128;
+// project: weight boxes [c quarter q][i half ih], then eight o_lat chunks
+constexpr int kPrjW = 8 * kWBox, kPrjX = 8 * kXBox;
+constexpr int kPrjSmem = kPrjW + kPrjX + 1024 + 128;
+static_assert(kPrjSmem <= 227 * 1024, "shared memory");
+constexpr int kThreads = 128;
+constexpr uint32_t kIdescAbs = tc::instr_desc(128, kB, false);
+constexpr uint32_t kIdescPrj = tc::instr_desc(128, kB, false, true);
+}  // namespace tcp
+
+struct TcProjParams {
+  __nv_bfloat16* y;            // absorb: q_lat [M, H, ldy]; project: out [M, H, 128]
+  const __nv_bfloat16* extra;  // absorb: q_pe [M, H, extra_dim], copied to columns 512..
+  int32_t M, H, ldy, extra_dim;
+};
+
+// mx: the activations [M, H, K] as 3-D {K, H, M}, box {64, 1, 64};
+// mw: the weights [d_c, H * 128] as 2-D, box {64, 128}.
+template <bool kProject>
+__global__ void __launch_bounds__(tcp::kThreads, 1)
+    mla_head_gemm_tc_kernel(const __grid_constant__ CUtensorMap mx,
+                            const __grid_constant__ CUtensorMap mw, const TcProjParams p) {
+  using namespace tcp;
+  using namespace tc;
+  constexpr int kWBytes = kProject ? kPrjW : kAbsW;
+  constexpr int kXBytes = kProject ? kPrjX : kAbsX;
+  constexpr int kNBar = kProject ? 4 : 2;  // load groups: c quarters / K halves
+  constexpr int kMBlocks = kProject ? 1 : 2;
+  constexpr uint32_t kCols = kProject ? 64 : 128;  // TMEM columns: one N = 64 block per M block
+  extern __shared__ uint8_t dyn_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* wsm = base;
+  uint8_t* xsm = base + kWBytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + kWBytes + kXBytes);  // [kNBar] loads, [kNBar] done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + kNBar + 1);
+  const int h = kProject ? blockIdx.x : blockIdx.x >> 1;
+  const int v = kProject ? 0 : blockIdx.x & 1;  // absorb: outputs 256 v ..
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    prefetch_tensormap(&mx);
+    prefetch_tensormap(&mw);
+    for (int i = 0; i <= kNBar; ++i) mbar_init(&bar[i], 1);
+    mbar_init_fence();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tslot)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  uint64_t* done = &bar[kNBar];
+
+  if (tid == 0) {
+    // every load of the CTA at once
+    const uint64_t pol_w = l2_policy_evict_first();   // weights: read once
+    const uint64_t pol_x = l2_policy_evict_normal();  // activations: shared by the CTAs of a head
+    if constexpr (kProject) {
+      // group q: weight rows c 128 q .. (both i halves) and o_lat chunks 2q, 2q + 1
+      for (int q = 0; q < 4; ++q) {
+        mbar_arrive_expect_tx(&bar[q], 2 * kWBox + 2 * kXBox);
+        for (int ih = 0; ih < 2; ++ih)
+          tma_load_2d(wsm + (2 * q + ih) * kWBox, &mw, h * 128 + 64 * ih, 128 * q, &bar[q], pol_w);
+        for (int k2 = 0; k2 < 2; ++k2)
+          tma_load_3d(xsm + (2 * q + k2) * kXBox, &mx, 64 * (2 * q + k2), h, 0, &bar[q], pol_x);
+      }
+    } else {
+      // group kh: the two weight blocks' K half kh and q_nope half kh
+      for (int kh = 0; kh < 2; ++kh) {
+        mbar_arrive_expect_tx(&bar[kh], 2 * kWBox + kXBox);
+        for (int j = 0; j < 2; ++j)
+          tma_load_2d(wsm + (2 * j + kh) * kWBox, &mw, h * 128 + 64 * kh, 256 * v + 128 * j,
+                      &bar[kh], pol_w);
+        tma_load_3d(xsm + kh * kXBox, &mx, 64 * kh, h, 0, &bar[kh], pol_x);
+      }
+    }
+  }
+
+  // absorb: the rope part of the query rides behind the latent part (the
+  // first CTA of each head copies it); its rows are read now
+  const bool copy_pe = !kProject && p.extra != nullptr && v == 0;
+  const int pe_units = p.extra_dim / 8;
+  uint4 pe[4];
+  if (copy_pe) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + tcp::kThreads * j;
+      const int r = pe_units > 0 ? i / pe_units : 0, u = i - r * pe_units;
+      pe[j] = (pe_units > 0 && i < kB * pe_units && r < p.M)
+                  ? __ldg(reinterpret_cast<const uint4*>(
+                              p.extra + (static_cast<int64_t>(r) * p.H + h) * p.extra_dim) + u)
+                  : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint32_t w0 = smem_u32(wsm), x0 = smem_u32(xsm);
+      for (int g = 0; g < kNBar && ok; ++g) {
+        ok = mbar_wait_bounded(&bar[g], 0, nullptr);
+        if (!ok) break;
+        tc_fence_after();
+        if constexpr (kProject) {
+          // 128 rows c of group g: A = both i halves (leading offset 16 KB),
+          // 16 rows c per k-step (2 KB); B = o_lat chunk 2g + c / 64
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_ss(tmem, smem_desc(w0 + (2 * g) * kWBox + kk * 2048, kWBox, 1024),
+                      smem_desc(x0 + (2 * g + (kk >> 2)) * kXBox + 32 * (kk & 3), 16, 1024),
+                      kIdescPrj, (g > 0 || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kMBlocks; ++j)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_ss(tmem + kB * j, smem_desc(w0 + (2 * j + g) * kWBox + 32 * kk, 16, 1024),
+                        smem_desc(x0 + g * kXBox + 32 * kk, 16, 1024), kIdescAbs,
+                        (g > 0 || kk > 0) ? 1u : 0u);
+        }
+      }
+      tc_commit(done);  // also after a timeout: every product issued completes first
+    }
+    __syncwarp();
+  }
+  // the products are done (their operands are no longer read)
+  ok = __syncthreads_and(ok && mbar_wait_bounded(done, 0, nullptr));
+  if (!ok) {
+    // a load never landed (never expected): wait once more, bounded, for the
+    // copies still in flight into the shared memory staged below; the CTA's
+    // outputs become NaN
+    if (tid == 0)
+      for (int g = 0; g < kNBar; ++g) mbar_wait_bounded(&bar[g], 0, nullptr);
+    __syncthreads();
+  }
+  tc_fence_after();
+
+  // D: lane = output (32 per warp and M block), 64 columns = sequences; staged
+  // as bf16 rows Y[b][outputs of the CTA] in the weight region, then stored
+  // as whole rows
+  constexpr int kOut = 128 * kMBlocks;  // outputs per CTA
+  uint8_t* Y = wsm;
+  const float bad = __int_as_float(0x7fc00000);
+#pragma unroll
+  for (int j = 0; j < kMBlocks; ++j) {
+    float d[kB];
+    tc_ld32_nowait(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kB * j, &d[0]);
+    tc_ld32_nowait(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kB * j + 32, &d[32]);
+    tc_wait_ld();
+    const int o = 128 * j + 32 * warp + lane;
+#pragma unroll
+    for (int b = 0; b < kB; ++b)
+      *reinterpret_cast<__nv_bfloat16*>(Y + (b * kOut + o) * 2) =
+          __float2bfloat16_rn(ok ? d[b] : bad);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
+                 : "memory");
+  constexpr int kRowUnits = kOut / 8;  // 16-byte units per staged row
+  const int col0 = kProject ? 0 : 256 * v;
+  for (int idx = tid; idx < kB * kRowUnits; idx += tcp::kThreads) {
+    const int b = idx / kRowUnits, u = idx % kRowUnits;
+    if (b < p.M)
+      *reinterpret_cast<uint4*>(p.y + (static_cast<int64_t>(b) * p.H + h) * p.ldy + col0 + 8 * u) =
+          *reinterpret_cast<const uint4*>(Y + (b * kOut + 8 * u) * 2);
+  }
+  if (copy_pe) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + tcp::kThreads * j;
+      const int r = pe_units > 0 ? i / pe_units : 0, u = i - r * pe_units;
+      if (pe_units > 0 && i < kB * pe_units && r < p.M)
+        *reinterpret_cast<uint4*>(p.y + (static_cast<int64_t>(r) * p.H + h) * p.ldy + 512 +
+                                  8 * u) = pe[j];
+    }
+  }
+}
+
+// 2-D map over w [rows, cols] bf16, boxes of 64 elements x box_rows rows,
+// 128-byte swizzle.
+bool make_weight_map(CUtensorMap* map, const void* w, int64_t rows, int64_t cols,
+                     uint32_t box_rows = 64) {
   auto enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  const cuuint32_t box[2] = {64u, 64u};
+  const cuuint32_t box[2] = {64u, box_rows};
   const cuuint32_t es[2] = {1u, 1u};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -423,8 +638,42 @@ pa_status launch_gemm_tma(const ProjParams& q, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// The tcgen05 path: absorb with d_h = 128, d_c = 512, a rope part of at most
+// 64 elements; project with d_c = 512, d_v = 128; up to 64 sequences.
+bool tc_path_fits(const ProjParams& p, bool project) {
+  return p.M <= tcp::kB &&
+         (project ? (p.K == 512 && p.N == 128)
+                  : (p.K == 128 && p.N == 512 && p.extra_dim <= 64 && p.extra_dim % 8 == 0));
+}
+
+template <bool kProject>
+pa_status launch_gemm_tc(const ProjParams& q, cudaStream_t stream) {
+  CUtensorMap mx, mw;
+  // weights [d_c, H * 128] in both products (rows = outputs for absorb, the
+  // reduction index for project), boxes of 128 rows
+  const int64_t wrows = kProject ? q.K : q.N;
+  const int64_t wcols = static_cast<int64_t>(q.H) * (kProject ? q.N : q.K);
+  if (!make_rows_map(&mx, q.x, q.M, q.H, q.K) || !make_weight_map(&mw, q.w, wrows, wcols, 128))
+    return PA_ERR_CUDA;
+  TcProjParams p;
+  p.y = q.y;
+  p.extra = q.extra;
+  p.M = q.M;
+  p.H = q.H;
+  p.ldy = q.ldy;
+  p.extra_dim = q.extra_dim;
+  static std::atomic<uint64_t> smem_raised{0};
+  auto kern = mla_head_gemm_tc_kernel<kProject>;
+  constexpr int kSmemTc = kProject ? tcp::kPrjSmem : tcp::kAbsSmem;
+  if (!ensure_smem_limit(kern, kSmemTc, smem_raised)) return PA_ERR_CUDA;
+  const dim3 grid(static_cast<unsigned>(kProject ? q.H : 2 * q.H), 1u, 1u);
+  kern<<<grid, tcp::kThreads, kSmemTc, stream>>>(mx, mw, p);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 template <bool kTransB>
 pa_status launch_gemm(ProjParams p, cudaStream_t stream) {
+  if (tc_path_fits(p, kTransB)) return launch_gemm_tc<kTransB>(p, stream);
   if (tma_path_fits(p)) return launch_gemm_tma<kTransB>(p, stream);
   const int chunks = p.N / kTN;
   const int groups = chunks < kGroups ? chunks : kGroups;
